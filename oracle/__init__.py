@@ -1,0 +1,206 @@
+"""CPU oracle for the reproducible-operator hot path -- TEST INFRASTRUCTURE ONLY.
+
+Only `tests/`, `__graft_entry__.smoke()` and `bench.py`'s CPU-baseline leg may
+import this package.  The product path (the CUDA library and its Python
+binding) never does, and fails loudly when its own extension is missing.
+
+The arithmetic lives in `repops_oracle.c` (plain single-threaded C, built with
+-ffp-contract=off).  This module only marshals numpy arrays through ctypes.
+
+What each function follows (page title, section):
+  gemm       -- "Verde与RepOps" §3.2, the matmul example: any order over i, j;
+                k strictly increasing from sum = 0; sum = sum + a*b with the
+                product and the sum each rounded to binary32 (no FMA, as
+                "Zoo Per-LLM Chain Soundness" §5 "Determinism of left-fold" pins).
+  sort_ids   -- "Zoo Per-LLM Chain Soundness" §2 Lemma "Order independence
+                within a batch" and §5 "Ordering subroutine": contributors in
+                lexicographic DID byte order.
+  mean_sgd   -- same page, §2 Definition "Aggregation rule" (mean over the
+                contributor set), §5 "Ordering subroutine" (left fold in sorted
+                order, scaled by 1/k) and "Update step" (theta -= eta * gbar).
+  sha256     -- FIPS 180-4 (the pages name no hash; SHA-256 is the reading taken).
+  merkle_*   -- "Zoo Per-LLM Chain Soundness" §1 (batch hash = Merkle root),
+                §6 (bytes32 roots); "Verde与RepOps" §2.3.2 (checkpoint hash is a
+                Merkle tree) and §2.4 (membership proofs).
+Pins against things other than the oracle itself live in tests/test_oracle_*.py.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+
+def lib():
+    """Loads (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+        L.oracle_fp_env_ok.restype = i32
+        L.oracle_fp_env_ok.argtypes = []
+        L.oracle_gemm_f32.restype = None
+        L.oracle_gemm_f32.argtypes = [i64, i64, i64, vp, i64, i32, vp, i64, i32, vp, i64]
+        L.oracle_sort_ids.restype = i32
+        L.oracle_sort_ids.argtypes = [i32, vp, vp, vp, vp]
+        L.oracle_mean_sgd.restype = i32
+        L.oracle_mean_sgd.argtypes = [i32, i64, vp, vp, ctypes.c_float, vp]
+        L.oracle_sha256.restype = None
+        L.oracle_sha256.argtypes = [vp, ctypes.c_uint64, vp]
+        L.oracle_sha256_constants.restype = None
+        L.oracle_sha256_constants.argtypes = [vp, vp]
+        L.oracle_merkle_leaf_count.restype = ctypes.c_uint64
+        L.oracle_merkle_leaf_count.argtypes = [ctypes.c_uint64, ctypes.c_uint64]
+        L.oracle_merkle_leaves.restype = i32
+        L.oracle_merkle_leaves.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, vp]
+        L.oracle_merkle_reduce.restype = i32
+        L.oracle_merkle_reduce.argtypes = [vp, ctypes.c_uint64, vp]
+        L.oracle_merkle_root.restype = i32
+        L.oracle_merkle_root.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, vp]
+        if L.oracle_fp_env_ok() != 1:
+            raise RuntimeError("host floating-point environment flushes subnormals "
+                               "or does not round to nearest even; the oracle "
+                               "would not be the IEEE-754 binary32 reference")
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _operand(X: np.ndarray):
+    """(base array, leading dim, transposed flag) for a 2-D float32 view."""
+    if X.dtype != np.float32 or X.ndim != 2:
+        raise TypeError("expected a 2-D float32 array")
+    r, c = X.shape
+    s0, s1 = (s // 4 for s in X.strides)
+    if X.strides[0] % 4 or X.strides[1] % 4:
+        X = np.ascontiguousarray(X)
+        s0, s1 = c, 1
+    if s1 == 1 and s0 >= max(c, 1):
+        return X, s0, 0
+    if s0 == 1 and s1 >= max(r, 1):
+        return X, s1, 1
+    X = np.ascontiguousarray(X)
+    return X, max(c, 1), 0
+
+
+def gemm(A: np.ndarray, B: np.ndarray, out: np.ndarray = None) -> np.ndarray:
+    """C = A @ B with the order-fixed, separately rounded k-chain.
+
+    A (M x K) and B (K x N) may be row-major or transposed (column-major)
+    views; the element values are what count, not the storage."""
+    L = lib()
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    A_, lda, ta = _operand(A)
+    B_, ldb, tb = _operand(B)
+    C = out if out is not None else np.empty((M, N), dtype=np.float32)
+    if C.dtype != np.float32 or C.strides[1] != 4:
+        raise TypeError("out must be float32 with unit column stride")
+    if M and N:
+        L.oracle_gemm_f32(M, N, K, _ptr(A_), lda, ta, _ptr(B_), ldb, tb,
+                          _ptr(C), C.strides[0] // 4)
+    return C
+
+
+def sort_ids(ids) -> list:
+    """Indices of `ids` (a sequence of bytes) in lexicographic unsigned byte order."""
+    L = lib()
+    n = len(ids)
+    blob = b"".join(ids)
+    buf = np.frombuffer(blob, dtype=np.uint8).copy() if blob else np.zeros(1, np.uint8)
+    lens = np.array([len(x) for x in ids], dtype=np.int64)
+    offs = np.zeros(n, dtype=np.int64)
+    if n > 1:
+        offs[1:] = np.cumsum(lens)[:-1]
+    order = np.zeros(max(n, 1), dtype=np.int32)
+    rc = L.oracle_sort_ids(n, _ptr(buf), _ptr(offs), _ptr(lens), _ptr(order))
+    if rc != 0:
+        raise ValueError("duplicate contributor identifiers")
+    return [int(x) for x in order[:n]]
+
+
+def mean_sgd(grads, order, eta: float, theta: np.ndarray) -> np.ndarray:
+    """Returns a new theta: theta - eta * (left fold of grads in `order`) / |C|."""
+    L = lib()
+    nC = len(grads)
+    th = np.array(theta, dtype=np.float32, copy=True)
+    gs = [np.ascontiguousarray(g, dtype=np.float32) for g in grads]
+    for g in gs:
+        if g.shape != th.shape:
+            raise ValueError("gradient and theta shapes differ")
+    ptrs = (ctypes.c_void_p * max(nC, 1))(*[_ptr(g) for g in gs])
+    o = np.array(list(order), dtype=np.int32)
+    if o.size != nC:
+        raise ValueError("order must have one entry per contributor")
+    rc = L.oracle_mean_sgd(nC, th.size, ctypes.cast(ptrs, ctypes.c_void_p),
+                           _ptr(o) if nC else None, ctypes.c_float(eta), _ptr(th))
+    if rc != 0:
+        raise ValueError("order is not a permutation of the contributors")
+    return th
+
+
+def _as_bytes(data) -> np.ndarray:
+    if isinstance(data, (bytes, bytearray, memoryview)):
+        return np.frombuffer(bytes(data), dtype=np.uint8)
+    a = np.ascontiguousarray(data)
+    return a.reshape(-1).view(np.uint8)
+
+
+def sha256(data) -> bytes:
+    L = lib()
+    b = _as_bytes(data)
+    out = np.zeros(32, dtype=np.uint8)
+    L.oracle_sha256(_ptr(b) if b.size else None, b.size, _ptr(out))
+    return out.tobytes()
+
+
+def sha256_constants():
+    """(K[64], H0[8]) derived from the primes, FIPS 180-4 §4.2.2 and §5.3.3."""
+    L = lib()
+    K = np.zeros(64, dtype=np.uint32)
+    H = np.zeros(8, dtype=np.uint32)
+    L.oracle_sha256_constants(_ptr(K), _ptr(H))
+    return [int(x) for x in K], [int(x) for x in H]
+
+
+def merkle_leaves(data, leaf: int = 4096) -> np.ndarray:
+    """(leaf_count, 32) uint8 array of leaf digests SHA256(0x00 || leaf bytes)."""
+    L = lib()
+    b = _as_bytes(data)
+    n = L.oracle_merkle_leaf_count(b.size, leaf)
+    if n == 0:
+        raise ValueError("empty input or zero leaf size")
+    out = np.zeros((n, 32), dtype=np.uint8)
+    L.oracle_merkle_leaves(_ptr(b), b.size, leaf, _ptr(out))
+    return out
+
+
+def merkle_reduce(digests: np.ndarray) -> bytes:
+    """Root over a level of 32-byte digests (pairs hashed with 0x01, odd promoted)."""
+    L = lib()
+    lv = np.array(digests, dtype=np.uint8, copy=True).reshape(-1, 32)
+    if lv.shape[0] == 0:
+        raise ValueError("empty level")
+    root = np.zeros(32, dtype=np.uint8)
+    L.oracle_merkle_reduce(_ptr(lv), lv.shape[0], _ptr(root))
+    return root.tobytes()
+
+
+def merkle_root(data, leaf: int = 4096) -> bytes:
+    """32-byte Merkle root over the bytes of `data` with `leaf`-byte leaves."""
+    L = lib()
+    b = _as_bytes(data)
+    root = np.zeros(32, dtype=np.uint8)
+    rc = L.oracle_merkle_root(_ptr(b) if b.size else None, b.size, leaf, _ptr(root))
+    if rc != 0:
+        raise ValueError("empty input or zero leaf size")
+    return root.tobytes()

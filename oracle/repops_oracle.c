@@ -1,0 +1,421 @@
+/*
+ * repops_oracle.c -- the CPU oracle for the reproducible-operator hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, single-threaded
+ * statement of what the GPU library computes.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load it.  It shares no source,
+ * header, table or constant with the CUDA library, and never calls it.
+ *
+ * Build flags (oracle/build.py): -std=c11 -O2 -ffp-contract=off -fno-fast-math.
+ * -ffp-contract=off matters: GCC's default in GNU mode would fuse a*b+c into a
+ * fused multiply-add on aarch64, which is exactly what the method forbids.
+ *
+ * Sources (page title, section):
+ *  [RepOps]  "Verde与RepOps：机器学习可验证委托与硬件无关确定性",
+ *            §3.1 (sources of non-determinism), §3.2 (design principle and the
+ *            matmul example: any order over i and j, fixed order over k,
+ *            sum starts at 0, sum = sum + a*b), §3.3 (IEEE-754 requirement),
+ *            §2.3.2 (checkpoint hash is a Merkle tree over node hashes),
+ *            §2.4 (Merkle membership proof of an input tensor hash).
+ *  [Zoo]     "Zoo Per-LLM Chain Soundness", §2 Definition "Aggregation rule",
+ *            Lemma "Order independence within a batch"; §5 "Detailed proof:
+ *            deterministic ordering", paragraphs "Ordering subroutine",
+ *            "Determinism of left-fold" (round-to-nearest-even, FMA off) and
+ *            "Update step"; §1 "Background" (batch hash = Merkle root);
+ *            §6 table "Per-LLM chain block field layout" (bytes32 roots);
+ *            §7 "Reproducibility test plan" (verify H(theta) = m).
+ *  [FIPS]    FIPS PUB 180-4, Secure Hash Standard: SHA-256 (§4.1.2 functions,
+ *            §4.2.2 constants, §5.1.1 padding, §5.3.3 initial value,
+ *            §6.2 computation).
+ *
+ * Readings taken where the pages are silent (all stated again in the design
+ * notes):
+ *  - no FMA: the product is rounded to binary32, then added with its own
+ *    rounding; rounding is to nearest even; subnormals are kept (no FTZ/DAZ);
+ *  - the GEMM sum starts at +0.0f;
+ *  - the contributor mean starts the left fold at the first sorted gradient,
+ *    then divides by |C| with one correctly rounded division;
+ *  - SGD: theta = theta - (eta * gbar), each op rounded;
+ *  - the hash is SHA-256; leaf = SHA256(0x00 || leaf bytes), node =
+ *    SHA256(0x01 || left || right); leaves cut from the tensor bytes in
+ *    increasing offset, the last one possibly short; level by level, pairs
+ *    (0,1),(2,3),...; an unpaired last node is promoted unchanged.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Floating-point environment                                                */
+/* ------------------------------------------------------------------------ */
+
+/* Returns 1 when the host keeps subnormal results and subnormal inputs
+ * (no flush-to-zero, no denormals-are-zero) and rounds to nearest even.
+ * [RepOps §3.3] needs IEEE-754 behaviour; [Zoo §5] pins round-to-nearest-even. */
+int oracle_fp_env_ok(void)
+{
+    volatile float tiny = 1.17549435e-38f;      /* FLT_MIN, smallest normal */
+    volatile float half = 0.5f;
+    volatile float sub = tiny * half;           /* 2^-127: subnormal */
+    if (sub == 0.0f) return 0;                  /* FTZ on outputs */
+    volatile float sub2 = sub + 0.0f;
+    if (sub2 == 0.0f) return 0;                 /* DAZ on inputs */
+    /* ties-to-even: 1 + 2^-24 is exactly half-way between 1 and 1 + 2^-23 */
+    volatile float one = 1.0f;
+    volatile float h = 5.9604644775390625e-08f; /* 2^-24 */
+    volatile float t = one + h;
+    if (t != 1.0f) return 0;
+    volatile float odd = 1.00000011920928955078125f; /* 1 + 2^-23 */
+    volatile float t2 = odd + h;                     /* tie: goes to 1 + 2^-22 */
+    if (t2 != 1.0000002384185791015625f) return 0;
+    return 1;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Order-fixed GEMM  [RepOps §3.2, matmul example]                           */
+/* ------------------------------------------------------------------------ */
+
+/* C[i][j] = ((0 + A[i][0]*B[0][j]) + A[i][1]*B[1][j]) + ... + A[i][K-1]*B[K-1][j]
+ * with every product and every sum rounded to binary32.
+ *
+ * Storage: row-major with leading dimensions in elements.
+ *   transA == 0: A(i,k) = A[i*lda + k]      transA != 0: A(i,k) = A[k*lda + i]
+ *   transB == 0: B(k,j) = B[k*ldb + j]      transB != 0: B(k,j) = B[j*ldb + k]
+ *   C(i,j) = C[i*ldc + j]
+ * The loops follow the page: i and j in any order (here increasing), k in
+ * strictly increasing order. */
+void oracle_gemm_f32(int64_t M, int64_t N, int64_t K,
+                     const float *A, int64_t lda, int transA,
+                     const float *B, int64_t ldb, int transB,
+                     float *C, int64_t ldc)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            float sum = 0.0f;
+            for (int64_t k = 0; k < K; ++k) {
+                float a = transA ? A[k * lda + i] : A[i * lda + k];
+                float b = transB ? B[j * ldb + k] : B[k * ldb + j];
+                float p = a * b;        /* product, rounded to binary32 */
+                sum = sum + p;          /* sum, rounded to binary32     */
+            }
+            C[i * ldc + j] = sum;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Contributor order  [Zoo §2 Lemma "Order independence"; §5 "Ordering       */
+/* subroutine"; §6 "contributors (sorted DID list)"]                         */
+/* ------------------------------------------------------------------------ */
+
+/* Lexicographic comparison on unsigned bytes; a proper prefix sorts first. */
+static int id_less(const uint8_t *a, int64_t la, const uint8_t *b, int64_t lb)
+{
+    int64_t n = la < lb ? la : lb;
+    for (int64_t i = 0; i < n; ++i) {
+        if (a[i] != b[i]) return a[i] < b[i];
+    }
+    return la < lb;
+}
+
+/* ids: concatenated identifier bytes; offs[r], lens[r]: where contributor r's
+ * identifier starts and how long it is.  Writes order[0..n-1] such that
+ * order[0] is the contributor with the smallest identifier.  Returns 0, or -1
+ * if two identifiers are equal (the contributor set would not be a set). */
+int oracle_sort_ids(int n, const uint8_t *ids, const int64_t *offs,
+                    const int64_t *lens, int *order)
+{
+    for (int r = 0; r < n; ++r) order[r] = r;
+    /* insertion sort: plain and stable */
+    for (int r = 1; r < n; ++r) {
+        int cur = order[r];
+        int s = r - 1;
+        while (s >= 0 && id_less(ids + offs[cur], lens[cur],
+                                 ids + offs[order[s]], lens[order[s]])) {
+            order[s + 1] = order[s];
+            --s;
+        }
+        order[s + 1] = cur;
+    }
+    for (int r = 1; r < n; ++r) {
+        const int p = order[r - 1], q = order[r];
+        if (!id_less(ids + offs[p], lens[p], ids + offs[q], lens[q])) return -1;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fixed-order contributor mean fused with SGD                               */
+/* [Zoo §2 Def. "Aggregation rule"; §5 "Ordering subroutine" (left fold),    */
+/*  "Update step" (theta_t = theta_{t-1} - eta * gbar_t)]                    */
+/* ------------------------------------------------------------------------ */
+
+/* For each element e:
+ *   S = g[order[0]][e];  S = S + g[order[r]][e] for r = 1..nC-1  (left fold)
+ *   gbar = S / nC                       (one correctly rounded division)
+ *   theta[e] = theta[e] - (eta * gbar)  (product rounded, then difference)
+ * Returns 0, or -1 if order is not a permutation of 0..nC-1 or nC < 1. */
+int oracle_mean_sgd(int nC, int64_t len, const float *const *grads,
+                    const int *order, float eta, float *theta)
+{
+    if (nC < 1) return -1;
+    char *seen = (char *)calloc((size_t)nC, 1);
+    if (!seen) return -1;
+    for (int r = 0; r < nC; ++r) {
+        if (order[r] < 0 || order[r] >= nC || seen[order[r]]) { free(seen); return -1; }
+        seen[order[r]] = 1;
+    }
+    free(seen);
+    const float count = (float)nC;   /* exact for nC < 2^24 */
+    for (int64_t e = 0; e < len; ++e) {
+        float S = grads[order[0]][e];
+        for (int r = 1; r < nC; ++r) {
+            S = S + grads[order[r]][e];
+        }
+        float gbar = S / count;
+        float step = eta * gbar;
+        theta[e] = theta[e] - step;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* SHA-256  [FIPS 180-4]                                                     */
+/* ------------------------------------------------------------------------ */
+
+static uint32_t sha_K[64];
+static uint32_t sha_H0[8];
+static int sha_ready = 0;
+
+/* floor(cbrt(v)) for v < 2^120, by bisection on exact integers. */
+static uint64_t icbrt128(unsigned __int128 v)
+{
+    uint64_t lo = 0, hi = (uint64_t)1 << 41;   /* hi^3 = 2^123 > v */
+    while (hi - lo > 1) {
+        uint64_t mid = lo + (hi - lo) / 2;
+        unsigned __int128 m = mid;
+        if (m * m * m <= v) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+/* floor(sqrt(v)) for v < 2^120. */
+static uint64_t isqrt128(unsigned __int128 v)
+{
+    uint64_t lo = 0, hi = (uint64_t)1 << 61;   /* hi^2 = 2^122 > v */
+    while (hi - lo > 1) {
+        uint64_t mid = lo + (hi - lo) / 2;
+        unsigned __int128 m = mid;
+        if (m * m <= v) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+/* FIPS 180-4 §4.2.2: K[t] is the first 32 bits of the fractional part of the
+ * cube root of the t-th prime; §5.3.3: H0[i] the first 32 bits of the
+ * fractional part of the square root of the i-th prime.  Derived here in exact
+ * integer arithmetic: floor(cbrt(p) * 2^32) = floor(cbrt(p * 2^96)), and its
+ * low 32 bits drop the integer part. */
+static void sha_init_constants(void)
+{
+    if (sha_ready) return;
+    int primes[64];
+    int count = 0;
+    for (int c = 2; count < 64; ++c) {
+        int is_prime = 1;
+        for (int d = 2; d * d <= c; ++d) {
+            if (c % d == 0) { is_prime = 0; break; }
+        }
+        if (is_prime) primes[count++] = c;
+    }
+    for (int t = 0; t < 64; ++t) {
+        unsigned __int128 v = (unsigned __int128)primes[t] << 96;
+        sha_K[t] = (uint32_t)(icbrt128(v) & 0xffffffffu);
+    }
+    for (int i = 0; i < 8; ++i) {
+        unsigned __int128 v = (unsigned __int128)primes[i] << 64;
+        sha_H0[i] = (uint32_t)(isqrt128(v) & 0xffffffffu);
+    }
+    sha_ready = 1;
+}
+
+void oracle_sha256_constants(uint32_t K_out[64], uint32_t H0_out[8])
+{
+    sha_init_constants();
+    memcpy(K_out, sha_K, sizeof(sha_K));
+    memcpy(H0_out, sha_H0, sizeof(sha_H0));
+}
+
+static uint32_t rotr32(uint32_t x, int n) { return (x >> n) | (x << (32 - n)); }
+
+/* FIPS 180-4 §6.2.2: process one 512-bit block. */
+static void sha_block(uint32_t H[8], const uint8_t blk[64])
+{
+    uint32_t W[64];
+    for (int t = 0; t < 16; ++t) {
+        W[t] = ((uint32_t)blk[4 * t] << 24) | ((uint32_t)blk[4 * t + 1] << 16) |
+               ((uint32_t)blk[4 * t + 2] << 8) | (uint32_t)blk[4 * t + 3];
+    }
+    for (int t = 16; t < 64; ++t) {
+        uint32_t s0 = rotr32(W[t - 15], 7) ^ rotr32(W[t - 15], 18) ^ (W[t - 15] >> 3);
+        uint32_t s1 = rotr32(W[t - 2], 17) ^ rotr32(W[t - 2], 19) ^ (W[t - 2] >> 10);
+        W[t] = s1 + W[t - 7] + s0 + W[t - 16];
+    }
+    uint32_t a = H[0], b = H[1], c = H[2], d = H[3];
+    uint32_t e = H[4], f = H[5], g = H[6], h = H[7];
+    for (int t = 0; t < 64; ++t) {
+        uint32_t S1 = rotr32(e, 6) ^ rotr32(e, 11) ^ rotr32(e, 25);
+        uint32_t ch = (e & f) ^ (~e & g);
+        uint32_t T1 = h + S1 + ch + sha_K[t] + W[t];
+        uint32_t S0 = rotr32(a, 2) ^ rotr32(a, 13) ^ rotr32(a, 22);
+        uint32_t maj = (a & b) ^ (a & c) ^ (b & c);
+        uint32_t T2 = S0 + maj;
+        h = g; g = f; f = e; e = d + T1;
+        d = c; c = b; b = a; a = T1 + T2;
+    }
+    H[0] += a; H[1] += b; H[2] += c; H[3] += d;
+    H[4] += e; H[5] += f; H[6] += g; H[7] += h;
+}
+
+typedef struct {
+    uint32_t H[8];
+    uint64_t total;     /* message bytes consumed so far */
+    uint8_t buf[64];
+    unsigned fill;
+} osha_ctx;
+
+static void osha_init(osha_ctx *c)
+{
+    sha_init_constants();
+    memcpy(c->H, sha_H0, sizeof(sha_H0));
+    c->total = 0;
+    c->fill = 0;
+}
+
+static void osha_update(osha_ctx *c, const uint8_t *p, uint64_t n)
+{
+    c->total += n;
+    while (n > 0) {
+        unsigned take = 64 - c->fill;
+        if ((uint64_t)take > n) take = (unsigned)n;
+        memcpy(c->buf + c->fill, p, take);
+        c->fill += take;
+        p += take;
+        n -= take;
+        if (c->fill == 64) {
+            sha_block(c->H, c->buf);
+            c->fill = 0;
+        }
+    }
+}
+
+/* FIPS 180-4 §5.1.1: append 0x80, zeros, and the 64-bit big-endian bit length. */
+static void osha_final(osha_ctx *c, uint8_t out[32])
+{
+    uint64_t bits = c->total * 8u;
+    uint8_t one = 0x80, zero = 0;
+    uint64_t keep_total = c->total;
+    osha_update(c, &one, 1);
+    while (c->fill != 56) osha_update(c, &zero, 1);
+    uint8_t len[8];
+    for (int i = 0; i < 8; ++i) len[i] = (uint8_t)(bits >> (56 - 8 * i));
+    osha_update(c, len, 8);
+    c->total = keep_total;
+    for (int i = 0; i < 8; ++i) {
+        out[4 * i] = (uint8_t)(c->H[i] >> 24);
+        out[4 * i + 1] = (uint8_t)(c->H[i] >> 16);
+        out[4 * i + 2] = (uint8_t)(c->H[i] >> 8);
+        out[4 * i + 3] = (uint8_t)(c->H[i]);
+    }
+}
+
+void oracle_sha256(const uint8_t *msg, uint64_t len, uint8_t out[32])
+{
+    osha_ctx c;
+    osha_init(&c);
+    osha_update(&c, msg, len);
+    osha_final(&c, out);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Merkle commitment over tensor bytes                                       */
+/* [Zoo §1 "batch hash (Merkle root over input batch)", §6 bytes32 roots,    */
+/*  §7 "verify H(theta) = m"; RepOps §2.3.2 Merkle tree over node hashes]    */
+/* ------------------------------------------------------------------------ */
+
+/* Leaf i covers bytes [i*leaf, min((i+1)*leaf, n)):  SHA256(0x00 || bytes). */
+static void merkle_leaf(const uint8_t *data, uint64_t n, uint64_t leaf,
+                        uint64_t i, uint8_t out[32])
+{
+    uint64_t start = i * leaf;
+    uint64_t end = start + leaf;
+    if (end > n) end = n;
+    uint8_t prefix = 0x00;
+    osha_ctx c;
+    osha_init(&c);
+    osha_update(&c, &prefix, 1);
+    osha_update(&c, data + start, end - start);
+    osha_final(&c, out);
+}
+
+/* Interior node: SHA256(0x01 || left || right). */
+static void merkle_node(const uint8_t left[32], const uint8_t right[32], uint8_t out[32])
+{
+    uint8_t msg[65];
+    msg[0] = 0x01;
+    memcpy(msg + 1, left, 32);
+    memcpy(msg + 33, right, 32);
+    oracle_sha256(msg, 65, out);
+}
+
+uint64_t oracle_merkle_leaf_count(uint64_t n, uint64_t leaf)
+{
+    if (n == 0 || leaf == 0) return 0;
+    return (n + leaf - 1) / leaf;
+}
+
+/* Writes every leaf digest (leaf_count * 32 bytes). Returns 0 or -1. */
+int oracle_merkle_leaves(const uint8_t *data, uint64_t n, uint64_t leaf, uint8_t *out)
+{
+    uint64_t nl = oracle_merkle_leaf_count(n, leaf);
+    if (nl == 0) return -1;
+    for (uint64_t i = 0; i < nl; ++i) merkle_leaf(data, n, leaf, i, out + 32 * i);
+    return 0;
+}
+
+/* Root of a level of `count` digests, reduced level by level; an unpaired last
+ * node is carried up unchanged.  `level` is overwritten.  Returns 0 or -1. */
+int oracle_merkle_reduce(uint8_t *level, uint64_t count, uint8_t root[32])
+{
+    if (count == 0) return -1;
+    while (count > 1) {
+        uint64_t next = 0;
+        for (uint64_t j = 0; j + 1 < count; j += 2) {
+            uint8_t parent[32];
+            merkle_node(level + 32 * j, level + 32 * (j + 1), parent);
+            memcpy(level + 32 * next, parent, 32);
+            ++next;
+        }
+        if (count % 2 == 1) {   /* promotion of the unpaired last node */
+            memmove(level + 32 * next, level + 32 * (count - 1), 32);
+            ++next;
+        }
+        count = next;
+    }
+    memcpy(root, level, 32);
+    return 0;
+}
+
+/* Root over the n bytes at data with leaves of `leaf` bytes.  Returns 0, or
+ * -1 for n == 0, leaf == 0, or an allocation failure. */
+int oracle_merkle_root(const uint8_t *data, uint64_t n, uint64_t leaf, uint8_t root[32])
+{
+    uint64_t nl = oracle_merkle_leaf_count(n, leaf);
+    if (nl == 0) return -1;
+    uint8_t *level = (uint8_t *)malloc((size_t)(nl * 32));
+    if (!level) return -1;
+    oracle_merkle_leaves(data, n, leaf, level);
+    int rc = oracle_merkle_reduce(level, nl, root);
+    free(level);
+    return rc;
+}
