@@ -1,0 +1,465 @@
+"""Benchmark of the reproducible-operator hot path on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+  1. order-fixed FP32 GEMM, M = N = K = 8192, A, B ~ N(0, 1)        (headline)
+  2. fixed-order mean of 16 contributor gradients of 2^28 fp32 + SGD in place
+  3. SHA-256 Merkle commitment of a 2^30-element fp32 tensor (4 GiB), and of
+     the GEMM output C (256 MiB), 4096-byte leaves
+Every input is larger than the 129 MB L2, so no flush is needed between steps.
+
+`value` is the GEMM's TFLOP/s (2*M*N*K per launch / its device time, CUDA
+events on the launching stream); `parts` gives each stage's own throughput.
+`--impl reference` times the CPU oracle instead (on a bounded sample of the
+same workload), printing the same JSON line with "impl": "reference".
+
+Multi-GPU (torchrun): every rank runs the same workload on its own GPU
+(replicas, weak scaling); ranks share only a barrier and a max-reduction of
+the elapsed time -- the path has no exchange step.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import verifiable_repops_gemm_gb300 as rp  # noqa: E402
+from verifiable_repops_gemm_gb300 import inputs  # noqa: E402
+
+METRIC = "Bit-exact fixed-order FP32 GEMM TFLOP/s vs FP32 peak; mean/commit HBM GB/s"
+GEMM_N = 8192
+SM_MAX_MHZ_NOMINAL = 2070.0          # GB300 maximum SM clock
+FP32_LANES_PER_SM = 128              # FP32 CUDA cores per SM
+L2_BYTES = 129 * 10 ** 6
+
+# DRAM traffic per GEMM launch at 8192^3 from one ncu capture, valid only for
+# the kernel source it was taken on (sha256 of gemm_kernels.cuh).
+GEMM_TRAFFIC = {"src_sha256": None, "bytes_per_launch": None}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return {"hbm_gbs": 6800.0, "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
+
+
+def kernel_source_sha():
+    p = os.path.join(ROOT, "verifiable_repops_gemm_gb300", "csrc", "gemm_kernels.cuh")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+# ----------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during timing."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            props = torch.cuda.get_device_properties(self.dev)
+            sel = "GPU-%s" % props.uuid if getattr(props, "uuid", None) else str(self.dev)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", sel, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- workload ----
+
+def merkle_launches(nbytes, leaf=4096):
+    """Kernel launches of one Merkle commitment (leaf kernel + reduce passes)."""
+    leaves = -(-nbytes // leaf)
+    n = -(-leaves // 128)
+    launches = 1
+    while n > 1:
+        n = -(-n // 512)
+        launches += 1
+    return launches
+
+
+def sha_compressions(nbytes, leaf=4096):
+    """SHA-256 compressions of one commitment: 1 + leaf/64 per full leaf (the
+    0x00 prefix and padding add one block), 2 per interior node."""
+    leaves = -(-nbytes // leaf)
+    assert nbytes % leaf == 0
+    return leaves * (leaf // 64 + 1) + 2 * (leaves - 1)
+
+
+class Workload:
+    def __init__(self, dev):
+        n = GEMM_N
+        idx = inputs.SQUARE_SWEEP.index(n)
+        self.A = inputs.normal((n, n), 1.0, 10 + idx, dev)
+        self.B = inputs.normal((n, n), 1.0, 20 + idx, dev)
+        self.C = torch.empty((n, n), dtype=torch.float32, device=dev)
+        nC, ln = inputs.MEAN_CONTRIBUTORS, inputs.MEAN_LEN
+        self.grads = [inputs.normal((ln,), 1e-2, 200 + r, dev) for r in range(nC)]
+        self.theta = inputs.normal((ln,), 0.02, 199, dev)
+        self.order = rp.sort_ids(inputs.contributor_ids(nC, 200))
+        self.eta = 1e-3
+        self.T = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300, dev)
+        self.tbytes = self.T.numel() * 4
+        self.cbytes = self.C.numel() * 4
+        ws = max(rp.merkle_workspace_bytes(self.tbytes), rp.merkle_workspace_bytes(self.cbytes), 16)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.root_T = torch.empty(32, dtype=torch.uint8, device=dev)
+        self.root_C = torch.empty(32, dtype=torch.uint8, device=dev)
+        self.gemm_flops = 2.0 * n * n * n
+        self.mean_bytes = float((nC + 2) * ln * 4)
+        self.launches = 1 + 1 + merkle_launches(self.tbytes) + merkle_launches(self.cbytes)
+
+    def step(self, s, ev=None):
+        if ev: ev[0].record(s)
+        rp.gemm(self.A, self.B, out=self.C, stream=s)
+        if ev: ev[1].record(s)
+        rp.fixed_order_mean_sgd(self.grads, self.order, self.eta, self.theta, stream=s)
+        if ev: ev[2].record(s)
+        rp.merkle_sha256(self.T, 4096, out=self.root_T, workspace=self.ws, stream=s)
+        rp.merkle_sha256(self.C, 4096, out=self.root_C, workspace=self.ws, stream=s)
+        if ev: ev[3].record(s)
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(x, world, dev):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle ----
+
+def cpu_oracle_sample(budget_s=12.0):
+    """The oracle (as it stands, one thread) on a bounded sample of the step.
+
+    GEMM: whole rows of the 8192^3 product (k-chains of length 8192), rows
+    added until about half the budget is used.  Mean+SGD: 2^22 elements of
+    the 16-contributor update.  Merkle: 256 MiB of the committed tensor."""
+    import oracle
+    oracle.lib()
+    n = GEMM_N
+    idx = inputs.SQUARE_SWEEP.index(n)
+    A = inputs.normal((n, n), 1.0, 10 + idx, "cpu").numpy()
+    B = inputs.normal((n, n), 1.0, 20 + idx, "cpu").numpy()
+    rows, t_gemm = 0, 0.0
+    while t_gemm < budget_s * 0.5 and rows < n:
+        t0 = time.perf_counter()
+        oracle.gemm(A[rows:rows + 1], B)
+        t_gemm += time.perf_counter() - t0
+        rows += 1
+    gemm_tflops = 2.0 * rows * n * n / t_gemm / 1e12
+    m = 1 << 22
+    grads = [inputs.normal((m,), 1e-2, 200 + r, "cpu").numpy() for r in range(16)]
+    th = inputs.normal((m,), 0.02, 199, "cpu").numpy()
+    order = oracle.sort_ids(inputs.contributor_ids(16, 200))
+    t0 = time.perf_counter()
+    oracle.mean_sgd(grads, order, 1e-3, th)
+    t_mean = time.perf_counter() - t0
+    mb = 256 << 20
+    T = inputs.normal((mb // 4,), 0.02, 300, "cpu").numpy()
+    t0 = time.perf_counter()
+    oracle.merkle_root(T, 4096)
+    t_merk = time.perf_counter() - t0
+    return {
+        "gemm_tflops": gemm_tflops, "gemm_rows": rows, "gemm_s": t_gemm,
+        "mean_gbs": 18 * m * 4 / t_mean / 1e9, "merkle_gbs": mb / t_merk / 1e9,
+        "sample": ("GEMM: %d row(s) of the 8192^3 product (%.1f s); mean+SGD: 2^22 elements x 16 "
+                   "contributors; Merkle: 256 MiB" % (rows, t_gemm)),
+    }
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    oracle.lib()
+    n = GEMM_N
+    idx = inputs.SQUARE_SWEEP.index(n)
+    A = inputs.normal((n, n), 1.0, 10 + idx, "cpu").numpy()
+    B = inputs.normal((n, n), 1.0, 20 + idx, "cpu").numpy()
+    m = 1 << 20
+    grads = [inputs.normal((m,), 1e-2, 200 + r, "cpu").numpy() for r in range(16)]
+    th = inputs.normal((m,), 0.02, 199, "cpu").numpy()
+    order = oracle.sort_ids(inputs.contributor_ids(16, 200))
+    T = inputs.normal(((32 << 20) // 4,), 0.02, 300, "cpu").numpy()
+
+    def step(i):
+        t0 = time.perf_counter()
+        oracle.gemm(A[i % n:i % n + 1], B)      # one row: 8192 k-chains of 8192
+        t1 = time.perf_counter()
+        oracle.mean_sgd(grads, order, 1e-3, th)
+        t2 = time.perf_counter()
+        oracle.merkle_root(T, 4096)
+        t3 = time.perf_counter()
+        return t1 - t0, t2 - t1, t3 - t2
+
+    for i in range(args.warmup):
+        step(i)
+    tg = tm = tk = 0.0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        a, b, c = step(args.warmup + i)
+        tg += a; tm += b; tk += c
+    total = time.perf_counter() - t0
+    val = 2.0 * n * n * args.steps / tg / 1e12
+    sample = ("per step: 1 row of the 8192^3 GEMM, mean+SGD over 2^20 elements x 16 "
+              "contributors, Merkle root of 32 MiB; one thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "order-fixed fp32 GEMM 8192^3 + mean/SGD 16x2^28 + Merkle 4 GiB "
+                               "(bounded CPU sample)", "parallelism": "replicas",
+                   "l2": "inputs larger than L2"},
+        "parts": {"mean_sgd": {"value": 18 * m * 4 * args.steps / tm / 1e9, "unit": "GB/s"},
+                  "merkle": {"value": (32 << 20) * args.steps / tk / 1e9, "unit": "GB/s"}},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- ours ----
+
+def run_e2e(w, dev, steps):
+    """Same metric through the public API from pinned host buffers: each step
+    copies its inputs host->device, runs the path, reads results back."""
+    s = torch.cuda.Stream(device=dev)
+    def pinned_copy(t):
+        h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        h.copy_(t)
+        return h
+    hA, hB = pinned_copy(w.A), pinned_copy(w.B)
+    hC = torch.empty(w.C.shape, dtype=torch.float32, pin_memory=True)
+    hg = [pinned_copy(g) for g in w.grads]
+    hth = pinned_copy(w.theta)
+    hT = pinned_copy(w.T)
+    hroot = torch.empty((2, 32), dtype=torch.uint8, pin_memory=True)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps + 1)]
+    torch.cuda.synchronize(dev)
+    for i in range(steps + 1):          # the first pass is an untimed warm-up
+        e = ev[i]
+        with torch.cuda.stream(s):
+            e[0].record(s)
+            w.A.copy_(hA, non_blocking=True)
+            w.B.copy_(hB, non_blocking=True)
+            rp.gemm(w.A, w.B, out=w.C, stream=s)
+            hC.copy_(w.C, non_blocking=True)
+            e[1].record(s)
+            for g, h in zip(w.grads, hg):
+                g.copy_(h, non_blocking=True)
+            w.theta.copy_(hth, non_blocking=True)
+            rp.fixed_order_mean_sgd(w.grads, w.order, w.eta, w.theta, stream=s)
+            hth.copy_(w.theta, non_blocking=True)
+            e[2].record(s)
+            w.T.copy_(hT, non_blocking=True)
+            rp.merkle_sha256(w.T, 4096, out=w.root_T, workspace=w.ws, stream=s)
+            rp.merkle_sha256(w.C, 4096, out=w.root_C, workspace=w.ws, stream=s)
+            hroot[0].copy_(w.root_T, non_blocking=True)
+            hroot[1].copy_(w.root_C, non_blocking=True)
+            e[3].record(s)
+    torch.cuda.synchronize(dev)
+    ev = ev[1:]
+    tg = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
+    tm = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
+    tk = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    h2d = 2 * w.A.numel() * 4 + len(w.grads) * w.theta.numel() * 4 + w.theta.numel() * 4 + w.tbytes
+    d2h = w.C.numel() * 4 + w.theta.numel() * 4 + 64
+    return {"value": w.gemm_flops * steps / tg / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "parts": {"mean_sgd_gbs": w.mean_bytes * steps / tm / 1e9,
+                      "merkle_gbs": (w.tbytes + w.cbytes) * steps / tk / 1e9},
+            "steps": steps}
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    rp.load()
+    peaks, peaks_kind = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    w = Workload(dev)
+    s = torch.cuda.Stream(device=dev)
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            w.step(s)
+    torch.cuda.synchronize(dev)
+    if rp.device_status(s) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(s):
+            start.record(s)
+            for i in range(args.steps):
+                w.step(s, evs[i])
+            stop.record(s)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    clocks = clk.summary()
+    if rp.device_status(s) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait in the timed region")
+    total_ms = start.elapsed_time(stop)
+    gemm_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    mean_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    merk_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    total_max = max_over_ranks(total_ms, world, dev)
+    gemm_max = max_over_ranks(sum(gemm_ms), world, dev)
+    mean_max = max_over_ranks(sum(mean_ms), world, dev)
+    merk_max = max_over_ranks(sum(merk_ms), world, dev)
+
+    e2e = run_e2e(w, dev, args.e2e_steps) if args.e2e_steps > 0 else None
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample()
+
+    if rank != 0:
+        return
+    gemm_avg_s = statistics.mean(gemm_ms) / 1e3
+    achieved = w.gemm_flops / gemm_avg_s / 1e12
+    peak = sms * FP32_LANES_PER_SM * peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL) * 1e6 / 1e12
+    traffic = None
+    if GEMM_TRAFFIC["src_sha256"] and GEMM_TRAFFIC["src_sha256"] == kernel_source_sha():
+        traffic = GEMM_TRAFFIC["bytes_per_launch"]
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    mean_gbs = w.mean_bytes * args.steps * world / (mean_max / 1e3) / 1e9
+    merk_gbs = (w.tbytes + w.cbytes) * args.steps * world / (merk_max / 1e3) / 1e9
+    value = w.gemm_flops * args.steps * world / (gemm_max / 1e3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded torch generators)",
+        "config": {"workload": "order-fixed fp32 GEMM 8192^3 (A,B ~ N(0,1)) + fixed-order mean/SGD "
+                               "16 x 2^28 + SHA-256 Merkle of 4 GiB and of C, 4096-B leaves",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (129 MB); no flush"},
+        "parts": {
+            "gemm": {"value": value, "unit": "TFLOP/s", "ms": statistics.mean(gemm_ms)},
+            "mean_sgd": {"value": mean_gbs, "unit": "GB/s", "ms": statistics.mean(mean_ms),
+                         "frac_of_hbm": mean_gbs / world / hbm},
+            "merkle": {"value": merk_gbs, "unit": "GB/s", "ms": statistics.mean(merk_ms),
+                       "sha256_compressions_per_step": sha_compressions(w.tbytes) + sha_compressions(w.cbytes)},
+        },
+        "roofline": {"kernel": "gemm_tma_kernel (128x128, 8x8/thread)", "bound": "alu",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_basis": "%d SMs x 128 FP32 lanes x %.0f MHz (%s sm_max_mhz); one FP32 "
+                                   "op per lane per clock: products and sums issue separately"
+                                   % (sms, peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL), peaks_kind)},
+        "clocks": clocks,
+        "gpu_launches": w.launches * args.steps,
+    }
+    if clocks.get("sm_mhz"):
+        line["roofline"]["frac_at_sampled_clock"] = achieved / (
+            sms * FP32_LANES_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12)
+    if e2e is not None:
+        line["e2e"] = e2e
+    if cpu is not None:
+        line["cpu_baseline"] = {"value": cpu["gemm_tflops"], "unit": "TFLOP/s", "cores": 1,
+                                "kind": "oracle", "sample": cpu["sample"],
+                                "parts": {"mean_sgd_gbs": cpu["mean_gbs"],
+                                          "merkle_gbs": cpu["merkle_gbs"]}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,237 @@
+/*
+ * repops.h -- C ABI of librepops: reproducible ("RepOps-style") operators for
+ * verifiable training on one NVIDIA GB300 (sm_103a).
+ *
+ * Every operator returns the same bits on every call, whatever the tile size,
+ * launch shape, operand storage (row- or column-major) or alignment: the order
+ * of every floating-point operation is fixed by the definitions below, not by
+ * the kernel's parallel schedule.
+ *
+ * Sources (page title, section):
+ *   "Verde与RepOps：机器学习可验证委托与硬件无关确定性" (Verde and RepOps)
+ *       §3.1 sources of hardware non-determinism (operation order, core count,
+ *       memory layout/strides); §3.2 design principle (parallelise freely over
+ *       order-independent dimensions, keep order-critical dimensions serial)
+ *       and the matmul example; §3.3 IEEE-754 requirement; §2.3.2 checkpoint
+ *       hashes as Merkle trees; §2.4 Merkle membership proofs.
+ *   "Zoo Per-LLM Chain Soundness"
+ *       §2 Definition "Aggregation rule", Lemma "Order independence within a
+ *       batch"; §5 "Ordering subroutine", "Determinism of left-fold",
+ *       "Update step"; §1 Background (batch hash = Merkle root); §6 table
+ *       "Per-LLM chain block field layout" (bytes32 roots, sorted DIDs);
+ *       §7 "Reproducibility test plan" (verify H(theta) = m).
+ *
+ * Conventions for every call
+ *   - Pointers named "device" must be device memory of the current CUDA device
+ *     (or managed memory); pointers named "host" must be host memory.
+ *   - Calls are asynchronous on `stream` (0 = legacy default stream) unless a
+ *     call says otherwise.  Argument checks run on the host before any launch;
+ *     a call that returns an error launched nothing.
+ *   - The library never takes ownership of a buffer.  It keeps no per-call
+ *     state between calls, except the sticky device status word read by
+ *     repops_device_status().
+ *   - Floating point is IEEE-754 binary32, round-to-nearest-even, subnormals
+ *     kept (no flush-to-zero), no fused multiply-add, no tensor cores.
+ *   - NaN results compare equal as a class (payload bits are not pinned);
+ *     every other value, including signed zeros and infinities, is bit-exact.
+ */
+#ifndef REPOPS_H
+#define REPOPS_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>   /* cudaStream_t */
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every int-valued entry point. */
+typedef enum {
+    REPOPS_OK = 0,
+    REPOPS_ERR_INVALID_ARG = -1,  /* null pointer, negative/overflowing size, bad leading dim */
+    REPOPS_ERR_ALIAS = -2,        /* an output overlaps an input */
+    REPOPS_ERR_ORDER = -3,        /* contributor order is not a permutation / duplicate IDs */
+    REPOPS_ERR_CUDA = -4,         /* a CUDA runtime call failed (see repops_last_cuda_error) */
+    REPOPS_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (sticky, see below) */
+    REPOPS_ERR_ALLOC = -6,        /* stream-ordered scratch allocation failed */
+    REPOPS_ERR_UNSUPPORTED = -7   /* request outside the documented limits */
+} repops_status;
+
+/* Build manifest: library version, target architecture, compile flags that
+ * fix the arithmetic (-fmad=false, -ftz=false, -prec-div=true, ...), and the
+ * GEMM tile configurations.  The role of a "KernelManifest" ("Zoo Per-LLM
+ * Chain Soundness" §5 Setup): it names what produced the bits.  Static string. */
+const char *repops_version(void);
+
+/* Human-readable text for a status code.  Static string. */
+const char *repops_status_string(int status);
+
+/* The cudaError_t value of the most recent REPOPS_ERR_CUDA on this host
+ * thread (0 if none). */
+int repops_last_cuda_error(void);
+
+/* Synchronises `stream`, then reads and clears the library's sticky device
+ * status word.  *status_out = REPOPS_OK, or REPOPS_ERR_TIMEOUT if a kernel's
+ * bounded wait on its own asynchronous copies gave up since the last read (the
+ * output of that kernel is then undefined).  Returns REPOPS_OK or
+ * REPOPS_ERR_CUDA / REPOPS_ERR_INVALID_ARG (null status_out). */
+int repops_device_status(cudaStream_t stream, int *status_out);
+
+/* ------------------------------------------------------------------------ */
+/* Order-fixed FP32 GEMM                                                     */
+/* "Verde与RepOps" §3.2, matmul example; §3.1; §3.3                          */
+/* ------------------------------------------------------------------------ */
+
+/* C = A * B, overwriting C (no alpha/beta), with
+ *
+ *   C[i][j] = fl( ... fl( fl(+0 + fl(A[i][0]*B[0][j])) + fl(A[i][1]*B[1][j]) ) ...
+ *                 + fl(A[i][K-1]*B[K-1][j]) )
+ *
+ * k strictly increasing from +0.0f; every product rounded to binary32 before a
+ * separately rounded add.  Parallel over (i, j) only: no split-K, no
+ * reassociation.  A consequence: C never holds -0.0.
+ *
+ * Row-major storage, leading dimensions in elements:
+ *   A (device): M x K, A[i][k] at A[i*lda + k], lda >= max(1, K)
+ *   B (device): K x N, B[k][j] at B[k*ldb + j], ldb >= max(1, N)
+ *   C (device): M x N, C[i][j] at C[i*ldc + j], ldc >= max(1, N)
+ * M == 0 or N == 0: no-op.  K == 0: C is filled with +0.0f.
+ * Errors: INVALID_ARG (negative size, bad leading dim, null pointer with a
+ * non-empty operand, element offsets that overflow int64); ALIAS (C's span
+ * overlaps A's or B's span); CUDA (launch failure).
+ * Pointers need no alignment: unaligned operands take a 4-byte copy path that
+ * computes the same bits. */
+int repops_gemm_f32(int64_t M, int64_t N, int64_t K,
+                    const float *A, int64_t lda,
+                    const float *B, int64_t ldb,
+                    float *C, int64_t ldc,
+                    cudaStream_t stream);
+
+/* As repops_gemm_f32 with transposed storage options (the backward GEMMs):
+ *   transA == 0: A[i][k] at A[i*lda + k], lda >= max(1, K)
+ *   transA != 0: A[i][k] at A[k*lda + i], lda >= max(1, M)   (dW = X^T dY)
+ *   transB == 0: B[k][j] at B[k*ldb + j], ldb >= max(1, N)
+ *   transB != 0: B[k][j] at B[j*ldb + k], ldb >= max(1, K)   (dX = dY W^T)
+ * The result bits do not depend on transA/transB, only on the element values. */
+int repops_gemm_f32_ex(int transA, int transB,
+                       int64_t M, int64_t N, int64_t K,
+                       const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float *C, int64_t ldc,
+                       cudaStream_t stream);
+
+/* Loader paths for repops_gemm_f32_config. */
+#define REPOPS_LOADER_AUTO 0      /* TMA when operands allow it, else CPASYNC */
+#define REPOPS_LOADER_TMA 1       /* tensor-memory-accelerator tiles; needs 16-byte
+                                     aligned A/B and lda, ldb multiples of 4 */
+#define REPOPS_LOADER_CPASYNC 2   /* 4-byte cp.async with zero fill; any alignment */
+
+/* As repops_gemm_f32_ex with an explicit tile configuration (0 <=
+ * config < repops_gemm_config_count(), or -1 for the automatic choice) and
+ * loader path.  Exists so that callers and tests can show that the bits do not
+ * depend on tiling or launch shape.  UNSUPPORTED if `loader` is TMA and the
+ * operands do not meet its alignment rule. */
+int repops_gemm_f32_config(int config, int loader, int transA, int transB,
+                           int64_t M, int64_t N, int64_t K,
+                           const float *A, int64_t lda,
+                           const float *B, int64_t ldb,
+                           float *C, int64_t ldc,
+                           cudaStream_t stream);
+
+/* Number of GEMM tile configurations compiled into the library. */
+int repops_gemm_config_count(void);
+
+/* CTA tile (bm x bn), threads per CTA and per-thread tile (tm x tn) of a
+ * configuration.  Any output pointer may be null.  INVALID_ARG for a bad id. */
+int repops_gemm_config_info(int config, int *bm, int *bn, int *threads,
+                            int *tm, int *tn);
+
+/* The configuration repops_gemm_f32 would choose for an M x N output on the
+ * current device (-1 when M or N is 0). */
+int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
+
+/* ------------------------------------------------------------------------ */
+/* Contributor order                                                         */
+/* "Zoo Per-LLM Chain Soundness" §2 Lemma "Order independence within a       */
+/* batch", §5 "Ordering subroutine", §6 "contributors (sorted DID list)"     */
+/* ------------------------------------------------------------------------ */
+
+/* Host-only.  Sorts n contributor identifiers (DIDs) by unsigned
+ * lexicographic byte order, a proper prefix first.  Identifier r is the
+ * lengths[r] bytes at ids + offsets[r] (host).  Writes order_out[0..n-1]
+ * (host), order_out[0] being the smallest.  ORDER if two identifiers are
+ * equal (the contributor set must be a set); INVALID_ARG for n < 0 or null
+ * pointers with n > 0. */
+int repops_sort_ids(int n, const uint8_t *ids, const int64_t *offsets,
+                    const int64_t *lengths, int *order_out);
+
+/* ------------------------------------------------------------------------ */
+/* Fixed-order contributor mean fused with SGD                               */
+/* "Zoo Per-LLM Chain Soundness" §2 Def. "Aggregation rule"; §5 "Ordering   */
+/* subroutine", "Determinism of left-fold", "Update step"                    */
+/* ------------------------------------------------------------------------ */
+
+/* Maximum number of contributors per call. */
+#define REPOPS_MEAN_MAX_CONTRIBUTORS 1024
+
+/* For every element e in [0, len), in place:
+ *   S     = g[order[0]][e]
+ *   S     = fl(S + g[order[r]][e])         r = 1 .. nC-1  (left fold)
+ *   gbar  = fl(S / nC)                     one correctly rounded division
+ *   theta[e] = fl(theta[e] - fl(eta * gbar))
+ * ptrs (host array of nC device pointers): contributor r's gradient, len
+ * binary32 values each.  order (host array of nC ints): the fold order, a
+ * permutation of 0..nC-1, normally from repops_sort_ids.  theta (device):
+ * len binary32 values, updated in place.  eta: the step size, binary32.
+ * len == 0: no-op.  Errors: INVALID_ARG (nC < 1, nC >
+ * REPOPS_MEAN_MAX_CONTRIBUTORS, len < 0, null pointers); ORDER (order is not
+ * a permutation); ALIAS (theta's range overlaps a gradient's range); CUDA.
+ * Pointers need no alignment (unaligned inputs take a scalar path with the
+ * same bits). */
+int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs,
+                                const int *order, float eta, float *theta,
+                                cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* SHA-256 Merkle commitment over tensor bytes                               */
+/* "Zoo Per-LLM Chain Soundness" §1, §6 (bytes32 roots), §7 (H(theta) = m);  */
+/* "Verde与RepOps" §2.3.2, §2.4.  Hash: SHA-256, FIPS 180-4.                 */
+/* ------------------------------------------------------------------------ */
+
+/* The bytes at ptr are cut into leaves of `leaf` bytes in increasing offset
+ * (the last leaf may be shorter) and
+ *   leaf digest = SHA256(0x00 || leaf bytes)
+ *   node digest = SHA256(0x01 || left digest || right digest)
+ * Levels are reduced pairwise, (0,1), (2,3), ...; an unpaired last node is
+ * promoted unchanged to the next level; the root is the last node left.  One
+ * leaf: root = its leaf digest.  Tensor bytes are hashed as stored
+ * (little-endian binary32 for float tensors).
+ *
+ * ptr (device): `bytes` bytes, bytes >= 1.  leaf: a multiple of 64, 64 <=
+ * leaf <= 2^30.  root_out (device): receives the 32-byte root, written
+ * asynchronously on `stream`.
+ * Scratch of repops_merkle_workspace_bytes(bytes, leaf) bytes is taken with
+ * cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
+ * stream.  Errors: INVALID_ARG (null pointer, bytes == 0, bad leaf); ALIAS
+ * (root_out inside the input); ALLOC; CUDA. */
+int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t leaf,
+                         uint8_t *root_out, cudaStream_t stream);
+
+/* Scratch bytes repops_merkle_sha256_ws needs for this input (0 if the input
+ * is invalid). */
+uint64_t repops_merkle_workspace_bytes(uint64_t bytes, uint32_t leaf);
+
+/* As repops_merkle_sha256, with caller-provided device scratch `workspace`
+ * of `workspace_bytes` >= repops_merkle_workspace_bytes(bytes, leaf) bytes,
+ * 16-byte aligned.  The workspace must not be touched by anything else until
+ * the call's work on `stream` is done.  INVALID_ARG if it is too small or
+ * misaligned; ALIAS if it overlaps the input or root_out. */
+int repops_merkle_sha256_ws(const void *ptr, uint64_t bytes, uint32_t leaf,
+                            uint8_t *root_out, void *workspace,
+                            uint64_t workspace_bytes, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* REPOPS_H */

@@ -1,0 +1,168 @@
+"""Host-only checks of the C ABI: the library loads without a GPU, exports
+every entry point include/repops.h declares, and rejects bad arguments before
+launching anything (those paths touch no CUDA call, so fake pointers are safe:
+they are never dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "repops.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from verifiable_repops_gemm_gb300 import build, _capi
+    build.build()
+    return _capi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(repops_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for need in ("repops_gemm_f32", "repops_fixed_order_mean_sgd", "repops_merkle_sha256"):
+        assert need in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    from verifiable_repops_gemm_gb300 import _capi
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in _capi.SIGNATURES, "binding lacks " + name
+
+
+def test_manifest_names_arithmetic_flags(L):
+    v = L.repops_version().decode()
+    for s in ("sm_103a", "-fmad=false", "-ftz=false", "-prec-div=true", "no tensor cores"):
+        assert s in v, s
+
+
+def test_status_strings(L):
+    for code in range(-7, 1):
+        assert L.repops_status_string(code).decode() != "unknown status"
+
+
+FAKE_A, FAKE_B, FAKE_C = 0x10000000, 0x20000000, 0x30000000
+
+
+def test_gemm_rejects_bad_arguments(L):
+    g = L.repops_gemm_f32_ex
+    assert g(0, 0, -1, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert g(0, 0, 4, 4, 4, FAKE_A, 3, FAKE_B, 4, FAKE_C, 4, None) == -1     # lda < K
+    assert g(0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 3, FAKE_C, 4, None) == -1     # ldb < N
+    assert g(0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 3, None) == -1     # ldc < N
+    assert g(1, 0, 8, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1     # transA: lda < M
+    assert g(0, 1, 4, 8, 4, FAKE_A, 4, FAKE_B, 3, FAKE_C, 8, None) == -1     # transB: ldb < K
+    assert g(0, 0, 4, 4, 4, None, 4, FAKE_B, 4, FAKE_C, 4, None) == -1       # null A
+    assert g(0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, None, 4, None) == -1       # null C
+    # C overlapping A or B
+    assert g(0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 32, 4, None) == -2
+    assert g(0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_B + 60, 4, None) == -2
+    # empty output: nothing to do, no launch
+    assert g(0, 0, 0, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == 0
+    assert g(0, 0, 4, 0, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == 0
+    # overflowing spans
+    assert g(0, 0, 1 << 62, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    # bad config / loader ids
+    assert L.repops_gemm_f32_config(99, 0, 0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert L.repops_gemm_f32_config(0, 7, 0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+
+
+def test_gemm_config_table(L):
+    n = L.repops_gemm_config_count()
+    assert n >= 3
+    seen = set()
+    for c in range(n):
+        v = [ctypes.c_int() for _ in range(5)]
+        assert L.repops_gemm_config_info(c, *[ctypes.byref(x) for x in v]) == 0
+        bm, bn, th, tm, tn = (x.value for x in v)
+        assert bm % 8 == 0 and bn % 8 == 0 and th % 32 == 0
+        assert (bm // (4 * tm)) * (bn // (8 * tn)) * 32 == th
+        seen.add((bm, bn, th))
+    assert len(seen) == n
+    assert L.repops_gemm_config_info(n, None, None, None, None, None) == -1
+
+
+def _mean(L, nC, ln, ptrs, order, theta):
+    P = (ctypes.c_void_p * max(nC, 1))(*ptrs)
+    O = (ctypes.c_int * max(len(order), 1))(*order)
+    return L.repops_fixed_order_mean_sgd(nC, ln, ctypes.cast(P, ctypes.c_void_p),
+                                         ctypes.cast(O, ctypes.c_void_p), ctypes.c_float(1e-3),
+                                         theta, None)
+
+
+def test_mean_rejects_bad_arguments(L):
+    p = [FAKE_A, FAKE_A + 4096, FAKE_A + 8192]
+    assert _mean(L, 0, 16, [], [], FAKE_C) == -1
+    assert _mean(L, 1025, 16, [FAKE_A] * 1025, list(range(1025)), FAKE_C) == -1
+    assert _mean(L, 3, -1, p, [0, 1, 2], FAKE_C) == -1
+    assert _mean(L, 3, 16, p, [0, 1, 1], FAKE_C) == -3      # duplicate
+    assert _mean(L, 3, 16, p, [0, 1, 3], FAKE_C) == -3      # out of range
+    assert _mean(L, 3, 16, p, [2, 0, 1], FAKE_A + 4096 + 8) == -2   # theta inside a gradient
+    assert _mean(L, 3, 0, p, [2, 0, 1], FAKE_C) == 0        # empty: no launch
+    assert _mean(L, 3, 16, p, [2, 0, 1], None) == -1
+
+
+def test_merkle_rejects_bad_arguments(L):
+    m = L.repops_merkle_sha256
+    assert m(FAKE_A, 0, 4096, FAKE_C, None) == -1
+    assert m(FAKE_A, 100, 100, FAKE_C, None) == -1          # leaf not a multiple of 64
+    assert m(FAKE_A, 100, 0, FAKE_C, None) == -1
+    assert m(None, 100, 4096, FAKE_C, None) == -1
+    assert m(FAKE_A, 100, 4096, None, None) == -1
+    assert m(FAKE_A, 100, 4096, FAKE_A + 50, None) == -2    # root inside the input
+    ws = L.repops_merkle_workspace_bytes
+    assert ws(1 << 32, 4096) == (8192 + 16) * 32            # 2^20 leaves, 128 per CTA
+    assert ws(4096 * 128, 4096) == 0                        # one CTA writes the root
+    assert ws(0, 4096) == 0
+    mw = L.repops_merkle_sha256_ws
+    n = 4096 * 1000
+    need = ws(n, 4096)
+    assert need > 0
+    assert mw(FAKE_A, n, 4096, FAKE_C, FAKE_B, need - 1, None) == -1     # too small
+    assert mw(FAKE_A, n, 4096, FAKE_C, FAKE_B + 4, need, None) == -1     # misaligned
+    assert mw(FAKE_A, n, 4096, FAKE_C, FAKE_A + 16, need, None) == -2    # overlaps input
+
+
+def test_sort_ids_matches_oracle(L, orc):
+    import numpy as np
+    import verifiable_repops_gemm_gb300 as rp
+    rng = np.random.default_rng(11)
+    for n in (1, 2, 16, 100):
+        ids = [rng.bytes(int(rng.integers(1, 40))) for _ in range(n)]
+        ids = list(dict.fromkeys(ids))
+        assert rp.sort_ids(ids) == orc.sort_ids(ids)
+    ids = [b"did:a", b"did:", b"did:ab", b"\x80", b"\x7f\xff"]
+    assert rp.sort_ids(ids) == orc.sort_ids(ids)
+    with pytest.raises(rp.RepopsError):
+        rp.sort_ids([b"x", b"y", b"x"])
+
+
+def test_sha256_constant_table_matches_derivation(orc):
+    # the CUDA source's FIPS 180-4 table, read as text, against the oracle's
+    # derivation from the primes
+    src = open(os.path.join(ROOT, "verifiable_repops_gemm_gb300", "csrc", "merkle.cu")).read()
+    k_block = src[src.index("c_K[64]"):src.index("};", src.index("c_K[64]"))]
+    h_block = src[src.index("c_H0[8]"):src.index("};", src.index("c_H0[8]"))]
+    K = [int(x, 16) for x in re.findall(r"0x([0-9a-f]{8})u", k_block)]
+    H = [int(x, 16) for x in re.findall(r"0x([0-9a-f]{8})u", h_block)]
+    K0, H0 = orc.sha256_constants()
+    assert K == K0
+    assert H == H0
+
+
+def test_product_path_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "verifiable_repops_gemm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
+                assert "repops_oracle" not in text and "liboracle" not in text, f

@@ -1,0 +1,218 @@
+"""GPU parity of the order-fixed GEMM against the oracle, through the C ABI.
+
+Bar: bit-exact (0 ULP, identical bytes) for every tile configuration, loader
+path, operand layout and alignment ("Verde与RepOps" §3.1: operation order,
+core count and strides must not change the result; §3.2: k in a fixed order).
+"""
+import numpy as np
+import pytest
+import torch
+
+from verifiable_repops_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def bits(t):
+    return t.contiguous().view(torch.int32).cpu()
+
+
+def np_bits(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).view(torch.int32)
+
+
+def all_configs(rp):
+    return list(range(rp.gemm_config_count()))
+
+
+def run(rp, A, B, config=-1, loader=0, out=None):
+    C = rp.gemm(A, B, out=out, config=config, loader=loader)
+    torch.cuda.synchronize()
+    assert rp.device_status() == 0
+    return C
+
+
+def oracle_full(orc, A, B):
+    return orc.gemm(A.cpu().numpy(), B.cpu().numpy())
+
+
+def test_gemm_256_uniform_bit_exact(rp, orc):
+    # 256^3, U[-1,1), seeds 0 (A) and 1 (B)
+    A = inputs.uniform_pm1((256, 256), 0, DEV)
+    B = inputs.uniform_pm1((256, 256), 1, DEV)
+    want = np_bits(oracle_full(orc, A, B))
+    for cfg in all_configs(rp):
+        for loader in (rp.LOADER_TMA, rp.LOADER_CPASYNC):
+            C = run(rp, A, B, cfg, loader)
+            assert torch.equal(bits(C), want), (cfg, loader)
+    assert torch.equal(bits(run(rp, A, B)), want)
+
+
+LAYOUTS = [(False, False), (True, False), (False, True), (True, True)]
+
+
+def make_operand(X, transposed):
+    """Same logical matrix, stored row-major or as a transposed view."""
+    return X.t().contiguous().t() if transposed else X.contiguous()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 5, 3), (129, 257, 33), (300, 200, 100),
+                                   (64, 64, 32), (65, 129, 97), (256, 130, 1000)])
+def test_gemm_ragged_all_configs_layouts_loaders(rp, orc, M, N, K):
+    A = inputs.normal((M, K), 1.0, 10 + M, DEV)
+    B = inputs.normal((K, N), 1.0, 20 + N, DEV)
+    want = np_bits(oracle_full(orc, A, B))
+    for ta, tb in LAYOUTS:
+        Aop, Bop = make_operand(A, ta), make_operand(B, tb)
+        for cfg in all_configs(rp):
+            loaders = [rp.LOADER_CPASYNC]
+            # TMA needs 16-byte aligned bases and leading dims that are multiples of 4
+            lda = Aop.stride(1) if ta else Aop.stride(0)
+            ldb = Bop.stride(1) if tb else Bop.stride(0)
+            if lda % 4 == 0 and ldb % 4 == 0:
+                loaders.append(rp.LOADER_TMA)
+            for loader in loaders:
+                C = run(rp, Aop, Bop, cfg, loader)
+                assert torch.equal(bits(C), want), (ta, tb, cfg, loader)
+
+
+def test_gemm_crafted_detectors_all_configs(rp, golden):
+    od, fd = golden["gemm_order_detector"], golden["gemm_fma_detector"]
+    M, N, K = 70, 68, 40      # ldb = 68 keeps the TMA loader eligible; both edges ragged
+    A = inputs.integer_matrix((M, K), -3, 3, 5, DEV)
+    B = torch.ones((K, N), device=DEV)
+    a_od = torch.tensor(od["a_row"], dtype=torch.float32, device=DEV)
+    a_fd = torch.tensor([int(x, 16) for x in fd["a_row_bits"]], dtype=torch.int64).to(torch.int32).view(torch.float32).to(DEV)
+    b_fd = torch.tensor([int(x, 16) for x in fd["b_col_bits"]], dtype=torch.int64).to(torch.int32).view(torch.float32).to(DEV)
+    # order detector in row 33, columns of B all ones over k = 10..13, zeros elsewhere
+    A[33].zero_(); A[33, 10:14] = a_od
+    # FMA detector in row 69 (a ragged tile edge) against column 67
+    A[69].zero_(); A[69, 38:40] = a_fd
+    B[:, 67].zero_(); B[38:40, 67] = b_fd
+    for cfg in all_configs(rp):
+        for loader in (rp.LOADER_TMA, rp.LOADER_CPASYNC):
+            C = run(rp, A, B, cfg, loader).cpu()
+            assert int(C[33, 0].view(torch.int32)) == int(od["expected_bits"], 16)
+            assert int(C[69, 67].view(torch.int32)) == int(fd["expected_bits"], 16), (cfg, loader)
+
+
+def test_gemm_integer_exact_large(rp):
+    # entries in [-8, 8], K = 4096: every partial sum < 2^24, so C is the exact
+    # integer product
+    M, N, K = 512, 384, 4096
+    A = inputs.integer_matrix((M, K), -8, 8, 1, DEV)
+    B = inputs.integer_matrix((K, N), -8, 8, 2, DEV)
+    want = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
+    for cfg in all_configs(rp):
+        assert torch.equal(run(rp, A, B, cfg).cpu(), want), cfg
+
+
+def test_gemm_unaligned_and_padded_operands(rp, orc):
+    M, N, K = 131, 97, 75
+    base_a = inputs.normal((M * 80 + 1,), 1.0, 3, DEV)
+    base_b = inputs.normal((K * 101 + 3,), 1.0, 4, DEV)
+    A = base_a[1:1 + M * 80].view(M, 80)[:, :K]          # 4-byte aligned only, lda = 80
+    B = base_b[3:3 + K * 101].view(K, 101)[:, :N]        # ldb = 101
+    want = np_bits(oracle_full(orc, A, B))
+    Cbuf = torch.full((M, 104), float("nan"), device=DEV)
+    C = Cbuf[:, 1:1 + N]                                  # ldc = 104, unaligned
+    for cfg in all_configs(rp):
+        run(rp, A, B, cfg, 0, out=C)
+        assert torch.equal(bits(C), want), cfg
+    # padding columns untouched
+    assert torch.isnan(Cbuf[:, 0]).all() and torch.isnan(Cbuf[:, 1 + N:]).all()
+    with pytest.raises(rp.RepopsError):
+        rp.gemm(A, B, config=0, loader=rp.LOADER_TMA)
+
+
+def test_gemm_zero_k_and_empty(rp):
+    A = torch.empty((5, 0), device=DEV)
+    B = torch.empty((0, 7), device=DEV)
+    C = torch.full((5, 7), float("nan"), device=DEV)
+    run(rp, A, B, out=C)
+    assert torch.equal(bits(C), torch.zeros((5, 7), dtype=torch.int32))
+    E = torch.full((0, 7), 1.0, device=DEV)
+    rp.gemm(torch.empty((0, 3), device=DEV), torch.empty((3, 7), device=DEV), out=E)
+
+
+def test_gemm_output_guard_band(rp):
+    # canaries around C stay untouched
+    M, N, K = 67, 45, 33
+    A = inputs.normal((M, K), 1.0, 8, DEV)
+    B = inputs.normal((K, N), 1.0, 9, DEV)
+    buf = torch.full((M * N + 2048,), 12345.0, device=DEV)
+    C = buf[1024:1024 + M * N].view(M, N)
+    for cfg in all_configs(rp):
+        run(rp, A, B, cfg, out=C)
+        assert (buf[:1024] == 12345.0).all() and (buf[1024 + M * N:] == 12345.0).all()
+
+
+def sampled_check(orc, A, B, C, rows, cols):
+    """Oracle on the selected rows x cols only (any order over i, j)."""
+    Ar = A[rows].cpu().numpy()
+    Bc = B[:, cols].cpu().numpy()
+    want = orc.gemm(Ar, Bc)
+    got = C[rows][:, cols].cpu().numpy()
+    assert np.array_equal(np_bits(got), np_bits(want))
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("n", inputs.SQUARE_SWEEP)
+def test_gemm_square_sweep_sampled_and_layout_invariant(rp, orc, n):
+    idx = inputs.SQUARE_SWEEP.index(n)
+    A = inputs.normal((n, n), 1.0, 10 + idx, DEV)
+    B = inputs.normal((n, n), 1.0, 20 + idx, DEV)
+    C = run(rp, A, B)
+    g = torch.Generator().manual_seed(n)
+    rows = torch.cat([torch.tensor([0, n - 1]), torch.randint(0, n, (6,), generator=g)])
+    cols = torch.cat([torch.tensor([0, n - 1]), torch.randint(0, n, (30,), generator=g)])
+    sampled_check(orc, A, B, C, rows, cols)
+    # B column-major (same logical B, transposed storage): identical bytes
+    Bcm = B.t().contiguous().t()
+    C2 = run(rp, A, Bcm)
+    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
+    # another tile configuration: identical bytes
+    C3 = run(rp, A, B, config=3 if n <= 2048 else 1)
+    assert torch.equal(C.view(torch.int32), C3.view(torch.int32))
+    # Merkle root of the output matches the oracle's root of the same bytes
+    root = rp.merkle_sha256(C).cpu().numpy().tobytes()
+    assert root == orc.merkle_root(C.cpu().numpy(), 4096)
+
+
+@pytest.mark.slow
+def test_gemm_ragged_4097_1023_3001(rp, orc):
+    M, N, K = inputs.RAGGED
+    A = inputs.normal((M, K), 1.0, 30, DEV)
+    B = inputs.normal((K, N), 1.0, 31, DEV)
+    C = run(rp, A, B)
+    rows = torch.tensor([0, 1, 2047, 4095, 4096])
+    cols = torch.tensor(list(range(0, N, 61)) + [N - 2, N - 1])
+    sampled_check(orc, A, B, C, rows, cols)
+    C2 = run(rp, A.t().contiguous().t(), B.t().contiguous().t())
+    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
+    root = rp.merkle_sha256(C).cpu().numpy().tobytes()
+    assert root == orc.merkle_root(C.cpu().numpy(), 4096)
+
+
+@pytest.mark.slow
+def test_gemm_decoder_layer_set(rp, orc):
+    T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
+    X = inputs.normal((T, D), 1.0, 100, DEV)
+    g = torch.Generator().manual_seed(7)
+    for li, (name, kin, nout) in enumerate(inputs.DECODER_LAYERS):
+        Xin = X if kin == D else inputs.normal((T, kin), 1.0, 150 + li, DEV)
+        W = inputs.normal((kin, nout), 0.02, 110 + li, DEV)
+        dY = inputs.normal((T, nout), 1e-3, 120 + li, DEV)
+        Y = run(rp, Xin, W)                       # forward
+        dX = run(rp, dY, W.t())                   # dX = dY W^T (B as a transposed view)
+        dW = run(rp, Xin.t(), dY)                 # dW = X^T dY (A as a transposed view)
+        for out, a, b in ((Y, Xin, W), (dX, dY, W.t()), (dW, Xin.t(), dY)):
+            m, n = out.shape
+            rows = torch.cat([torch.tensor([m - 1]), torch.randint(0, m, (3,), generator=g)])
+            cols = torch.cat([torch.tensor([n - 1]), torch.randint(0, n, (16,), generator=g)])
+            sampled_check(orc, a, b, out, rows, cols)
+        # transposed views give the bytes of materialised transposes
+        assert torch.equal(dX.view(torch.int32), run(rp, dY, W.t().contiguous()).view(torch.int32))
+        assert torch.equal(dW.view(torch.int32), run(rp, Xin.t().contiguous(), dY).view(torch.int32))

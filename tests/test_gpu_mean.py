@@ -1,0 +1,111 @@
+"""GPU parity of the fixed-order contributor mean + SGD against the oracle.
+
+"Zoo Per-LLM Chain Soundness" §2 Def. "Aggregation rule", §5 "Ordering
+subroutine" / "Update step".  Bar: bit-exact theta.
+"""
+import numpy as np
+import pytest
+import torch
+
+from verifiable_repops_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def _hex(lst):
+    return np.array([int(x, 16) for x in lst], dtype=np.uint32)
+
+
+def run_both(rp, orc, grads, order, eta, theta):
+    want = orc.mean_sgd([g.cpu().numpy() for g in grads], order, eta, theta.cpu().numpy())
+    th = theta.clone()
+    rp.fixed_order_mean_sgd(grads, order, eta, th)
+    torch.cuda.synchronize()
+    return th.cpu().numpy(), want
+
+
+@pytest.mark.parametrize("nC,n", [(1, 1), (1, 1000), (2, 4099), (3, 1000003), (7, 513),
+                                  (16, 1 << 20), (16, (1 << 20) + 3), (33, 10007), (100, 4096)])
+def test_mean_sgd_bit_exact(rp, orc, nC, n):
+    grads = [inputs.normal((n,), 1e-2, 1000 + r, DEV) for r in range(nC)]
+    theta = inputs.normal((n,), 0.02, 999, DEV)
+    ids = inputs.contributor_ids(nC, 7 + nC)
+    order = rp.sort_ids(ids)
+    got, want = run_both(rp, orc, grads, order, 1e-3, theta)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_mean_sgd_crafted_cases(rp, golden):
+    c = golden["mean_order_detector"]
+    gs = [torch.tensor(g, dtype=torch.float32, device=DEV) for g in c["grads"]]
+    for case in c["cases"]:
+        th = torch.tensor(c["theta"], dtype=torch.float32, device=DEV)
+        rp.fixed_order_mean_sgd(gs, case["order"], c["eta"], th)
+        assert np.array_equal(th.cpu().numpy().view(np.uint32), _hex(case["expected_bits"]))
+    z = golden["mean_fold_starts_at_first_gradient"]
+    gs = [torch.from_numpy(_hex(g).view(np.float32)).to(DEV) for g in z["grads_bits"]]
+    th = torch.from_numpy(_hex(z["theta_bits"]).view(np.float32)).to(DEV)
+    eta = float(_hex([z["eta_bits"]]).view(np.float32)[0])
+    rp.fixed_order_mean_sgd(gs, z["order"], eta, th)
+    assert np.array_equal(th.cpu().numpy().view(np.uint32), _hex(z["expected_bits"]))
+    d = golden["mean_divides_by_count"]
+    gs = [torch.tensor(g, dtype=torch.float32, device=DEV) for g in d["grads"]]
+    th = torch.tensor(d["theta"], dtype=torch.float32, device=DEV)
+    rp.fixed_order_mean_sgd(gs, d["order"], d["eta"], th)
+    assert np.array_equal(th.cpu().numpy().view(np.uint32), _hex(d["expected_bits"]))
+
+
+def test_mean_sgd_order_changes_bits(rp):
+    n = 4096
+    big = torch.full((n,), 1e8, device=DEV)
+    one = torch.ones(n, device=DEV)
+    gs = [big, one, -big, one]
+    a = torch.zeros(n, device=DEV)
+    b = torch.zeros(n, device=DEV)
+    rp.fixed_order_mean_sgd(gs, [0, 1, 2, 3], 1.0, a)
+    rp.fixed_order_mean_sgd(gs, [0, 2, 1, 3], 1.0, b)
+    assert (a == -0.25).all() and (b == -0.5).all()
+
+
+def test_mean_sgd_unaligned_and_guard_band(rp, orc):
+    n, nC = 100003, 5
+    bases = [inputs.normal((n + 8,), 1e-2, 50 + r, DEV) for r in range(nC)]
+    grads = [b[r % 4 + 1:r % 4 + 1 + n] for r, b in enumerate(bases)]   # misaligned views
+    tbuf = torch.full((n + 2048,), 777.0, device=DEV)
+    theta = tbuf[1025:1025 + n]
+    theta.copy_(inputs.normal((n,), 0.02, 49, DEV))
+    order = [3, 1, 4, 0, 2]
+    want = orc.mean_sgd([g.cpu().numpy() for g in grads], order, 1e-3, theta.cpu().numpy())
+    rp.fixed_order_mean_sgd(grads, order, 1e-3, theta)
+    assert np.array_equal(theta.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert (tbuf[:1025] == 777.0).all() and (tbuf[1025 + n:] == 777.0).all()
+
+
+def test_mean_sgd_rejects_alias_and_order(rp):
+    g = torch.zeros(1000, device=DEV)
+    with pytest.raises(rp.RepopsError):
+        rp.fixed_order_mean_sgd([g, g.clone()], [0, 0], 1e-3, torch.zeros(1000, device=DEV))
+    with pytest.raises(rp.RepopsError):
+        rp.fixed_order_mean_sgd([g, g.clone()], [0, 1], 1e-3, g)
+
+
+@pytest.mark.slow
+def test_mean_sgd_full_size_sampled(rp, orc):
+    # 16 contributors x 2^28 fp32, N(0, 1e-2); theta 2^28, N(0, 0.02); eta = 1e-3
+    nC, n = inputs.MEAN_CONTRIBUTORS, inputs.MEAN_LEN
+    grads = [inputs.normal((n,), 1e-2, 200 + r, DEV) for r in range(nC)]
+    theta = inputs.normal((n,), 0.02, 199, DEV)
+    order = rp.sort_ids(inputs.contributor_ids(nC, 200))
+    before = {}
+    g = torch.Generator().manual_seed(1)
+    starts = [0, n - 4096] + [int(x) for x in torch.randint(0, n - 4096, (14,), generator=g)]
+    for s in starts:
+        before[s] = theta[s:s + 4096].cpu().numpy()
+    rp.fixed_order_mean_sgd(grads, order, 1e-3, theta)
+    torch.cuda.synchronize()
+    for s in starts:   # elements are independent: the oracle on a slice is exact
+        want = orc.mean_sgd([gr[s:s + 4096].cpu().numpy() for gr in grads], order, 1e-3, before[s])
+        got = theta[s:s + 4096].cpu().numpy()
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), s

@@ -1,0 +1,73 @@
+"""GPU parity of the SHA-256 Merkle commitment against the oracle.
+
+"Zoo Per-LLM Chain Soundness" §1, §6, §7; "Verde与RepOps" §2.3.2.  Bar:
+byte-identical roots.
+"""
+import numpy as np
+import pytest
+import torch
+
+from verifiable_repops_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def dev_bytes(n, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    return torch.randint(0, 256, (n,), generator=g, device=DEV, dtype=torch.uint8)
+
+
+def root(rp, t, leaf=4096, **kw):
+    r = rp.merkle_sha256(t, leaf, **kw)
+    torch.cuda.synchronize()
+    return r.cpu().numpy().tobytes()
+
+
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 4095, 4096, 4097, 8192, 3 * 4096 + 5,
+                               128 * 4096, 128 * 4096 + 1, 129 * 4096 + 100, 1000 * 4096,
+                               300 * 128 * 4096 + 17])
+def test_merkle_roots_match_oracle(rp, orc, n):
+    t = dev_bytes(n, n % 1000)
+    assert root(rp, t) == orc.merkle_root(t.cpu().numpy(), 4096)
+
+
+@pytest.mark.parametrize("leaf", [64, 128, 1024, 65536])
+def test_merkle_other_leaf_sizes(rp, orc, leaf):
+    for n in (leaf, 5 * leaf + 3, 300 * leaf):
+        t = dev_bytes(n, leaf + n)
+        assert root(rp, t, leaf) == orc.merkle_root(t.cpu().numpy(), leaf), (leaf, n)
+
+
+def test_merkle_unaligned_input_and_workspace(rp, orc):
+    n = 777 * 4096 + 123
+    buf = dev_bytes(n + 16, 5)
+    t = buf[3:3 + n]          # not 16-byte aligned: generic leaf path
+    want = orc.merkle_root(t.cpu().numpy(), 4096)
+    assert root(rp, t) == want
+    ws = torch.empty(rp.merkle_workspace_bytes(n, 4096), dtype=torch.uint8, device=DEV)
+    assert root(rp, t, workspace=ws) == want
+    aligned = t.clone()
+    assert root(rp, aligned) == want
+
+
+def test_merkle_float_tensor_bytes_little_endian(rp, orc):
+    x = inputs.normal((1 << 20,), 0.02, 300, DEV)
+    assert root(rp, x) == orc.merkle_root(x.cpu().numpy(), 4096)
+
+
+def test_merkle_detects_one_bit_flip(rp):
+    x = inputs.normal((1 << 20,), 0.02, 301, DEV)
+    r0 = root(rp, x)
+    y = x.clone()
+    y.view(torch.int32)[123457] ^= 1
+    assert root(rp, y) != r0
+
+
+@pytest.mark.slow
+def test_merkle_4gib_tensor(rp, orc):
+    # 2^30 fp32 (4 GiB), N(0, 0.02), 4096-byte leaves: 2^20 leaves
+    x = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300, DEV)
+    got = root(rp, x)
+    assert got == orc.merkle_root(x.cpu().numpy(), 4096)

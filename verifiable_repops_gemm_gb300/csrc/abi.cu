@@ -1,0 +1,113 @@
+// abi.cu -- library-wide C-ABI entry points: build manifest, status strings,
+// CUDA error bookkeeping, device properties, the contributor sort and the
+// sticky device status word.
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <vector>
+
+#include "internal.cuh"
+
+#ifndef REPOPS_BUILD_FLAGS
+#define REPOPS_BUILD_FLAGS "unknown"
+#endif
+
+namespace repops {
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+
+constexpr int kMaxDevices = 64;
+struct CachedInfo {
+    std::atomic<int> ready{0};
+    DeviceInfo info;
+};
+CachedInfo g_info[kMaxDevices];
+}  // namespace
+
+int set_cuda_error(cudaError_t e) {
+    t_last_cuda_error = int(e);
+    return REPOPS_ERR_CUDA;
+}
+
+int current_device_info(DeviceInfo *out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev < 0 || dev >= kMaxDevices) return REPOPS_ERR_UNSUPPORTED;
+    CachedInfo &c = g_info[dev];
+    if (!c.ready.load(std::memory_order_acquire)) {
+        DeviceInfo d;
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+                cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return set_cuda_error(e);
+        c.info = d;   // identical values if two threads race here
+        c.ready.store(1, std::memory_order_release);
+    }
+    *out = c.info;
+    return REPOPS_OK;
+}
+
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" const char *repops_version(void) {
+    return "librepops 0.1.0; arch sm_103a; fp32 IEEE-754 round-to-nearest-even, no FMA, no FTZ, "
+           "no tensor cores; gemm tiles 128x128/256t 8x8, 64x128/128t 8x8, 128x64/128t 8x8, "
+           "64x64/128t 8x4, 32x64/128t 4x4, BK 32, loaders TMA(128B swizzle)+cp.async; "
+           "mean+sgd left fold, divide by count; merkle sha256 leaf 0x00 node 0x01 promote-odd; "
+           "flags: " REPOPS_BUILD_FLAGS;
+}
+
+extern "C" const char *repops_status_string(int status) {
+    switch (status) {
+        case REPOPS_OK: return "ok";
+        case REPOPS_ERR_INVALID_ARG: return "invalid argument";
+        case REPOPS_ERR_ALIAS: return "output overlaps an input";
+        case REPOPS_ERR_ORDER: return "contributor order is not a permutation or identifiers repeat";
+        case REPOPS_ERR_CUDA: return "CUDA runtime error";
+        case REPOPS_ERR_TIMEOUT: return "a bounded device-side wait gave up";
+        case REPOPS_ERR_ALLOC: return "scratch allocation failed";
+        case REPOPS_ERR_UNSUPPORTED: return "outside the supported limits";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int repops_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int repops_device_status(cudaStream_t stream, int *status_out) {
+    if (!status_out) return REPOPS_ERR_INVALID_ARG;
+    unsigned v = 0;
+    int rc = gemm_read_and_clear_device_status(stream, &v);
+    if (rc != REPOPS_OK) return rc;
+    *status_out = v ? REPOPS_ERR_TIMEOUT : REPOPS_OK;
+    return REPOPS_OK;
+}
+
+// "Zoo Per-LLM Chain Soundness" §5 "Ordering subroutine": contributors sorted
+// lexicographically by DID bytes (unsigned; a proper prefix first).
+extern "C" int repops_sort_ids(int n, const uint8_t *ids, const int64_t *offsets, const int64_t *lengths,
+                               int *order_out) {
+    if (n < 0) return REPOPS_ERR_INVALID_ARG;
+    if (n == 0) return REPOPS_OK;
+    if (!ids || !offsets || !lengths || !order_out) return REPOPS_ERR_INVALID_ARG;
+    for (int r = 0; r < n; ++r)
+        if (offsets[r] < 0 || lengths[r] < 0) return REPOPS_ERR_INVALID_ARG;
+    auto less = [&](int a, int b) {
+        const int64_t la = lengths[a], lb = lengths[b];
+        const int c = std::memcmp(ids + offsets[a], ids + offsets[b], size_t(std::min(la, lb)));
+        return c != 0 ? c < 0 : la < lb;
+    };
+    std::vector<int> idx(static_cast<size_t>(n));
+    for (int r = 0; r < n; ++r) idx[size_t(r)] = r;
+    std::stable_sort(idx.begin(), idx.end(), less);
+    for (int r = 1; r < n; ++r)
+        if (!less(idx[size_t(r - 1)], idx[size_t(r)])) return REPOPS_ERR_ORDER;
+    std::copy(idx.begin(), idx.end(), order_out);
+    return REPOPS_OK;
+}

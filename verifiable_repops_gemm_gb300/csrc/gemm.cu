@@ -1,0 +1,245 @@
+// gemm.cu -- C-ABI entry points of the order-fixed FP32 GEMM: argument checks,
+// choice of tile configuration and loader, the sticky device status word.
+//
+// The arithmetic itself is in gemm_kernels.cuh ("Verde与RepOps" §3.2 matmul
+// example; §3.1: the bits must not depend on core count, tiling or strides).
+#include <algorithm>
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <mutex>
+
+#include "gemm_common.h"
+#include "gemm_kernels.cuh"
+#include "internal.cuh"
+
+namespace repops {
+
+namespace {
+
+// Sticky status word: bit 0 = a TMA wait gave up.  One per device (a
+// __device__ variable exists once per device that loads the library).
+__device__ unsigned g_gemm_status;
+
+constexpr int kMaxDevices = 64;
+std::atomic<unsigned *> g_status_addr[kMaxDevices];
+
+int status_address(unsigned **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev < 0 || dev >= kMaxDevices) return REPOPS_ERR_UNSUPPORTED;
+    unsigned *p = g_status_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_gemm_status);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        g_status_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return REPOPS_OK;
+}
+
+const GemmLauncher kLaunch[kGemmConfigCount] = {gemm_launch_cfg0, gemm_launch_cfg1, gemm_launch_cfg2,
+                                                gemm_launch_cfg3, gemm_launch_cfg4};
+const GemmOccupancy kOccupancy[kGemmConfigCount] = {gemm_occupancy_cfg0, gemm_occupancy_cfg1,
+                                                    gemm_occupancy_cfg2, gemm_occupancy_cfg3,
+                                                    gemm_occupancy_cfg4};
+GemmConfigInfo config_info(int c) {
+    switch (c) {
+        case 0: return gemm_info_cfg0();
+        case 1: return gemm_info_cfg1();
+        case 2: return gemm_info_cfg2();
+        case 3: return gemm_info_cfg3();
+        default: return gemm_info_cfg4();
+    }
+}
+
+// Resident CTAs per SM for each configuration, cached per device.
+std::atomic<int> g_occ[kMaxDevices][kGemmConfigCount];
+
+int occupancy_of(int dev, int c) {
+    int v = g_occ[dev][c].load(std::memory_order_relaxed);
+    if (v == 0) {
+        v = std::max(1, kOccupancy[c]());
+        g_occ[dev][c].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+// Picks the configuration with the smallest modelled time: each SM runs
+// ceil(tiles / SMs) tiles, `conc` of them at once; an SM with fewer than 8
+// resident warps is modelled as proportionally slower; per-thread efficiency
+// falls with the thread tile (shared-memory loads per FP32 instruction).
+int choose_config(int64_t M, int64_t N) {
+    DeviceInfo di;
+    if (current_device_info(&di) != REPOPS_OK || di.device < 0 || di.device >= kMaxDevices) return 0;
+    double best_t = 0;
+    int best = 0;
+    for (int c = 0; c < kGemmConfigCount; ++c) {
+        const GemmConfigInfo ci = config_info(c);
+        const double tiles = double((M + ci.bm - 1) / ci.bm) * double((N + ci.bn - 1) / ci.bn);
+        const double per_sm = std::ceil(tiles / di.sms);
+        const double conc = std::min<double>(occupancy_of(di.device, c), per_sm);
+        const double rounds = std::ceil(per_sm / conc);
+        const double warps = conc * ci.threads / 32.0;
+        const double eff = double(ci.tm * ci.tn) / double(ci.tm * ci.tn + ci.tm + ci.tn) *
+                           std::min(1.0, warps / 8.0);
+        const double t = rounds * conc * double(ci.bm) * double(ci.bn) / eff;
+        if (c == 0 || t < best_t * 0.999) { best_t = t; best = c; }
+    }
+    return best;
+}
+
+// Span in elements of a rows x cols operand with leading dimension ld.
+bool operand_span(int64_t rows, int64_t cols, int64_t ld, uint64_t *bytes) {
+    if (rows == 0 || cols == 0) { *bytes = 0; return true; }
+    // (rows - 1) * ld + cols must fit in int64 (element index)
+    if (rows - 1 > (INT64_MAX - cols) / std::max<int64_t>(ld, 1)) return false;
+    const int64_t elems = (rows - 1) * ld + cols;
+    if (elems > INT64_MAX / 4) return false;
+    *bytes = uint64_t(elems) * 4u;
+    return true;
+}
+
+__global__ void fill_positive_zero(float *C, int64_t M, int64_t N, int64_t ldc) {
+    const int64_t total = M * N;
+    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total;
+         e += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t i = e / N, j = e - i * N;
+        C[i * ldc + j] = 0.0f;
+    }
+}
+
+int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int64_t N, int64_t K,
+                  const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                  cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
+    if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
+    if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC)
+        return REPOPS_ERR_INVALID_ARG;
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < std::max<int64_t>(1, a_cols) || ldb < std::max<int64_t>(1, b_cols) ||
+        ldc < std::max<int64_t>(1, N))
+        return REPOPS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return REPOPS_OK;
+    if (!C) return REPOPS_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return REPOPS_ERR_INVALID_ARG;
+    uint64_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
+    if (!operand_span(a_rows, a_cols, lda, &a_bytes) || !operand_span(b_rows, b_cols, ldb, &b_bytes) ||
+        !operand_span(M, N, ldc, &c_bytes))
+        return REPOPS_ERR_INVALID_ARG;
+    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
+        return REPOPS_ERR_ALIAS;
+
+    if (K == 0) {
+        const int64_t total = M * N;
+        const int threads = 256;
+        const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 65536);
+        fill_positive_zero<<<int(blocks), threads, 0, stream>>>(C, M, N, ldc);
+        return check_launch();
+    }
+
+    GemmProblem p;
+    p.transA = transA ? 1 : 0;
+    p.transB = transB ? 1 : 0;
+    p.M = M; p.N = N; p.K = K;
+    p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
+    p.stream = stream;
+    int rc = status_address(&p.status);
+    if (rc != REPOPS_OK) return rc;
+
+    const int cfg = config >= 0 ? config : choose_config(M, N);
+    const bool tma_ok = gemm_tma_eligible(p);
+    if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
+    const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
+    rc = kLaunch[cfg](p, use);
+    if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO)
+        rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);   // encoder refused the map
+    return rc;
+}
+
+}  // namespace
+
+namespace gemm {
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+}  // namespace gemm
+
+bool gemm_tma_eligible(const GemmProblem &p) {
+    if (!gemm::tensor_map_encoder()) return false;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p.A), b = reinterpret_cast<uintptr_t>(p.B);
+    if (a % 16 || b % 16) return false;          // tensor-map base alignment
+    if (p.lda % 4 || p.ldb % 4) return false;    // row pitch: multiple of 16 bytes
+    if (p.lda >= (int64_t(1) << 37) || p.ldb >= (int64_t(1) << 37)) return false;   // pitch < 2^40 B
+    const int64_t lim = int64_t(1) << 31;        // int32 box coordinates
+    if (p.M >= lim || p.N >= lim || p.K >= lim) return false;
+    return true;
+}
+
+int gemm_read_and_clear_device_status(cudaStream_t stream, unsigned *value) {
+    unsigned *addr = nullptr;
+    int rc = status_address(&addr);
+    if (rc != REPOPS_OK) return rc;
+    unsigned v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, addr, sizeof(v), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(addr, &zero, sizeof(zero), cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    *value = v;
+    return REPOPS_OK;
+}
+
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" int repops_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                               const float *B, int64_t ldb, float *C, int64_t ldc,
+                               cudaStream_t stream) {
+    return gemm_dispatch(-1, REPOPS_LOADER_AUTO, 0, 0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+extern "C" int repops_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                  const float *A, int64_t lda, const float *B, int64_t ldb, float *C,
+                                  int64_t ldc, cudaStream_t stream) {
+    return gemm_dispatch(-1, REPOPS_LOADER_AUTO, transA, transB, M, N, K, A, lda, B, ldb, C, ldc,
+                         stream);
+}
+
+extern "C" int repops_gemm_f32_config(int config, int loader, int transA, int transB, int64_t M,
+                                      int64_t N, int64_t K, const float *A, int64_t lda,
+                                      const float *B, int64_t ldb, float *C, int64_t ldc,
+                                      cudaStream_t stream) {
+    return gemm_dispatch(config, loader, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+extern "C" int repops_gemm_config_count(void) { return kGemmConfigCount; }
+
+extern "C" int repops_gemm_config_info(int config, int *bm, int *bn, int *threads, int *tm, int *tn) {
+    if (config < 0 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
+    const GemmConfigInfo ci = config_info(config);
+    if (bm) *bm = ci.bm;
+    if (bn) *bn = ci.bn;
+    if (threads) *threads = ci.threads;
+    if (tm) *tm = ci.tm;
+    if (tn) *tn = ci.tn;
+    return REPOPS_OK;
+}
+
+extern "C" int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K) {
+    (void)K;
+    if (M <= 0 || N <= 0) return -1;
+    return choose_config(M, N);
+}

@@ -1,0 +1,180 @@
+// mean_sgd.cu -- fixed-order contributor mean fused with the SGD update.
+//
+// "Zoo Per-LLM Chain Soundness" §2 Definition "Aggregation rule" (the average
+// over the contributor set), §5 "Ordering subroutine" (contributors sorted by
+// DID bytes, left fold g(c1) + g(c2) + ... + g(ck), scaled by 1/k),
+// "Determinism of left-fold" (round-to-nearest-even, no FMA) and "Update step"
+// (theta_t = theta_{t-1} - eta * gbar_t).  Per element e:
+//     S = g[o0][e]; S = fl(S + g[o_r][e]) for r = 1..k-1
+//     gbar = fl(S / k)
+//     theta[e] = fl(theta[e] - fl(eta * gbar))
+// The fold order is per element and fixed; elements are independent, so the
+// kernel is a coalesced stream: each thread takes float4 chunks, issues all
+// gradient loads of a chunk before folding them in order, and writes theta
+// back in place.  HBM-bound: (k + 2) * 4 bytes of traffic per element.
+//
+// Division: when k is a power of two, S / k and S * (1/k) are the same real
+// number and 1/k is exact in binary32, so both round to the same binary32
+// value; the kernel then multiplies.  Otherwise it calls __fdiv_rn, the
+// correctly rounded IEEE division.
+#include <algorithm>
+#include <vector>
+
+#include "internal.cuh"
+
+namespace repops {
+namespace {
+
+struct GradPtrs {
+    const float *g[REPOPS_MEAN_MAX_CONTRIBUTORS];   // already in fold order
+};
+
+struct MeanScalars {
+    int nC;
+    int pow2;        // k is a power of two: multiply by inv
+    float count;     // (float)k, exact for k < 2^24
+    float inv;       // 1/k when pow2
+    float eta;
+};
+
+__device__ __forceinline__ float mean_of(float S, const MeanScalars &s) {
+    return s.pow2 ? __fmul_rn(S, s.inv) : __fdiv_rn(S, s.count);
+}
+
+__device__ __forceinline__ float sgd(float th, float gbar, float eta) {
+    return __fsub_rn(th, __fmul_rn(eta, gbar));
+}
+
+__device__ __forceinline__ void fold4(float4 &S, const float4 v) {
+    S.x = __fadd_rn(S.x, v.x);
+    S.y = __fadd_rn(S.y, v.y);
+    S.z = __fadd_rn(S.z, v.z);
+    S.w = __fadd_rn(S.w, v.w);
+}
+
+__device__ __forceinline__ float4 ld4(const float *p, int64_t i) {
+    return __ldcs(reinterpret_cast<const float4 *>(p) + i);
+}
+
+// NC > 0: exactly NC contributors, fully unrolled (all loads of a chunk in
+// flight together).  NC == 0: any count, loads issued in batches of 8.
+template <int NC>
+__global__ void __launch_bounds__(256)
+mean_sgd_vec4(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t n4,
+              float *__restrict__ theta) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+        float4 th = __ldcs(reinterpret_cast<const float4 *>(theta) + i);
+        float4 S;
+        if constexpr (NC > 0) {
+            float4 v[NC];
+#pragma unroll
+            for (int r = 0; r < NC; ++r) v[r] = ld4(gp.g[r], i);
+            S = v[0];
+#pragma unroll
+            for (int r = 1; r < NC; ++r) fold4(S, v[r]);
+        } else {
+            constexpr int BATCH = 8;
+            S = ld4(gp.g[0], i);
+            int r = 1;
+            for (; r + BATCH <= sc.nC; r += BATCH) {
+                float4 v[BATCH];
+#pragma unroll
+                for (int j = 0; j < BATCH; ++j) v[j] = ld4(gp.g[r + j], i);
+#pragma unroll
+                for (int j = 0; j < BATCH; ++j) fold4(S, v[j]);
+            }
+            for (; r < sc.nC; ++r) fold4(S, ld4(gp.g[r], i));
+        }
+        th.x = sgd(th.x, mean_of(S.x, sc), sc.eta);
+        th.y = sgd(th.y, mean_of(S.y, sc), sc.eta);
+        th.z = sgd(th.z, mean_of(S.z, sc), sc.eta);
+        th.w = sgd(th.w, mean_of(S.w, sc), sc.eta);
+        __stcs(reinterpret_cast<float4 *>(theta) + i, th);
+    }
+}
+
+// Elements [first, len) one at a time: unaligned buffers, and the len % 4 tail.
+__global__ void __launch_bounds__(256)
+mean_sgd_scalar(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t first, int64_t len,
+                float *__restrict__ theta) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t e = first + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < len; e += stride) {
+        float S = gp.g[0][e];
+        for (int r = 1; r < sc.nC; ++r) S = __fadd_rn(S, gp.g[r][e]);
+        theta[e] = sgd(theta[e], mean_of(S, sc), sc.eta);
+    }
+}
+
+template <int NC>
+int launch_vec(const GradPtrs &gp, const MeanScalars &sc, int64_t n4, float *theta, int blocks,
+               cudaStream_t s) {
+    mean_sgd_vec4<NC><<<blocks, 256, 0, s>>>(gp, sc, n4, theta);
+    return check_launch();
+}
+
+}  // namespace
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs, const int *order,
+                                           float eta, float *theta, cudaStream_t stream) {
+    if (nC < 1 || nC > REPOPS_MEAN_MAX_CONTRIBUTORS || len < 0) return REPOPS_ERR_INVALID_ARG;
+    if (!ptrs || !order) return REPOPS_ERR_INVALID_ARG;
+    std::vector<char> seen(size_t(nC), 0);
+    for (int r = 0; r < nC; ++r) {
+        if (order[r] < 0 || order[r] >= nC || seen[size_t(order[r])]) return REPOPS_ERR_ORDER;
+        seen[size_t(order[r])] = 1;
+    }
+    if (len == 0) return REPOPS_OK;
+    if (!theta || len > INT64_MAX / 4) return REPOPS_ERR_INVALID_ARG;
+    const uint64_t bytes = uint64_t(len) * 4u;
+    GradPtrs gp;
+    bool aligned = reinterpret_cast<uintptr_t>(theta) % 16 == 0;
+    for (int r = 0; r < nC; ++r) {
+        const float *g = ptrs[order[r]];
+        if (!g) return REPOPS_ERR_INVALID_ARG;
+        if (ranges_overlap(theta, bytes, g, bytes)) return REPOPS_ERR_ALIAS;
+        aligned = aligned && reinterpret_cast<uintptr_t>(g) % 16 == 0;
+        gp.g[r] = g;
+    }
+    for (int r = nC; r < REPOPS_MEAN_MAX_CONTRIBUTORS; ++r) gp.g[r] = nullptr;
+
+    MeanScalars sc;
+    sc.nC = nC;
+    sc.pow2 = (nC & (nC - 1)) == 0;
+    sc.count = float(nC);
+    sc.inv = sc.pow2 ? 1.0f / float(nC) : 0.0f;   // exact: a power of two
+    sc.eta = eta;
+
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != REPOPS_OK) return rc;
+    const int max_blocks = di.sms * 8;   // 8 CTAs of 256 threads per SM
+
+    int64_t first_scalar = 0;
+    if (aligned) {
+        const int64_t n4 = len / 4;
+        first_scalar = n4 * 4;
+        if (n4 > 0) {
+            const int blocks = int(std::min<int64_t>((n4 + 255) / 256, max_blocks));
+            switch (nC) {
+                case 1: rc = launch_vec<1>(gp, sc, n4, theta, blocks, stream); break;
+                case 2: rc = launch_vec<2>(gp, sc, n4, theta, blocks, stream); break;
+                case 4: rc = launch_vec<4>(gp, sc, n4, theta, blocks, stream); break;
+                case 8: rc = launch_vec<8>(gp, sc, n4, theta, blocks, stream); break;
+                case 16: rc = launch_vec<16>(gp, sc, n4, theta, blocks, stream); break;
+                default: rc = launch_vec<0>(gp, sc, n4, theta, blocks, stream); break;
+            }
+            if (rc != REPOPS_OK) return rc;
+        }
+    }
+    if (first_scalar < len) {
+        const int64_t n = len - first_scalar;
+        const int blocks = int(std::min<int64_t>((n + 255) / 256, max_blocks));
+        mean_sgd_scalar<<<blocks, 256, 0, stream>>>(gp, sc, first_scalar, len, theta);
+        rc = check_launch();
+    }
+    return rc;
+}

@@ -1,0 +1,360 @@
+// merkle.cu -- SHA-256 Merkle commitment over tensor bytes.
+//
+// "Zoo Per-LLM Chain Soundness" §1 (a block carries the Merkle root of its
+// input batch and the model state root), §6 (roots are bytes32), §7 (a
+// replaying party checks H(theta) = m); "Verde与RepOps" §2.3.2 (checkpoint
+// hashes are Merkle trees over node hashes) and §2.4 (Merkle membership
+// proofs).  The pages name no hash function or encoding; the library takes
+//   leaf = SHA256(0x00 || leaf bytes), node = SHA256(0x01 || left || right),
+// leaves of `leaf` bytes in increasing offset (the last may be short), levels
+// reduced pairwise with an unpaired last node promoted unchanged.  SHA-256 is
+// FIPS 180-4.
+//
+// Kernels:
+//   merkle_leaf_subtree: one leaf per thread (65 compressions for a 4 KiB
+//     leaf), then the CTA folds its LEAF_CTA leaves into the level-log2(LEAF_CTA)
+//     node in shared memory.  Node j of level l covers leaves [j*2^l,
+//     (j+1)*2^l), so a CTA-aligned block of leaves reduces to exactly that
+//     node, promotion included.
+//   merkle_reduce: each CTA folds up to 2*RED_CTA consecutive nodes of a level
+//     into one; repeated until one node, the root, remains.
+// SHA-256 is bound by the integer ALU (about 22 integer instructions per
+// message byte), far below HBM bandwidth.
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace repops {
+namespace {
+
+constexpr int LEAF_CTA = 128;   // leaves per CTA in the leaf kernel (power of two)
+constexpr int RED_CTA = 256;    // threads per CTA in the reduce kernel
+
+// FIPS 180-4 §4.2.2: first 32 bits of the fractional parts of the cube roots
+// of the first 64 primes.
+__constant__ uint32_t c_K[64] = {
+    0x428a2f98u, 0x71374491u, 0xb5c0fbcfu, 0xe9b5dba5u, 0x3956c25bu, 0x59f111f1u, 0x923f82a4u, 0xab1c5ed5u,
+    0xd807aa98u, 0x12835b01u, 0x243185beu, 0x550c7dc3u, 0x72be5d74u, 0x80deb1feu, 0x9bdc06a7u, 0xc19bf174u,
+    0xe49b69c1u, 0xefbe4786u, 0x0fc19dc6u, 0x240ca1ccu, 0x2de92c6fu, 0x4a7484aau, 0x5cb0a9dcu, 0x76f988dau,
+    0x983e5152u, 0xa831c66du, 0xb00327c8u, 0xbf597fc7u, 0xc6e00bf3u, 0xd5a79147u, 0x06ca6351u, 0x14292967u,
+    0x27b70a85u, 0x2e1b2138u, 0x4d2c6dfcu, 0x53380d13u, 0x650a7354u, 0x766a0abbu, 0x81c2c92eu, 0x92722c85u,
+    0xa2bfe8a1u, 0xa81a664bu, 0xc24b8b70u, 0xc76c51a3u, 0xd192e819u, 0xd6990624u, 0xf40e3585u, 0x106aa070u,
+    0x19a4c116u, 0x1e376c08u, 0x2748774cu, 0x34b0bcb5u, 0x391c0cb3u, 0x4ed8aa4au, 0x5b9cca4fu, 0x682e6ff3u,
+    0x748f82eeu, 0x78a5636fu, 0x84c87814u, 0x8cc70208u, 0x90befffau, 0xa4506cebu, 0xbef9a3f7u, 0xc67178f2u};
+
+// FIPS 180-4 §5.3.3: first 32 bits of the fractional parts of the square roots
+// of the first 8 primes.
+__constant__ uint32_t c_H0[8] = {0x6a09e667u, 0xbb67ae85u, 0x3c6ef372u, 0xa54ff53au,
+                                 0x510e527fu, 0x9b05688cu, 0x1f83d9abu, 0x5be0cd19u};
+
+__device__ __forceinline__ uint32_t rotr(uint32_t x, int n) { return __funnelshift_r(x, x, n); }
+
+// FIPS 180-4 §6.2.2 for one 512-bit block held as 16 big-endian words in W
+// (W is used as the rolling message schedule and is clobbered).
+__device__ __forceinline__ void sha256_compress(uint32_t (&st)[8], uint32_t (&W)[16]) {
+    uint32_t a = st[0], b = st[1], c = st[2], d = st[3];
+    uint32_t e = st[4], f = st[5], g = st[6], h = st[7];
+#pragma unroll
+    for (int t = 0; t < 64; ++t) {
+        uint32_t w;
+        if (t < 16) {
+            w = W[t];
+        } else {
+            const uint32_t x = W[(t - 15) & 15], y = W[(t - 2) & 15];
+            const uint32_t s0 = rotr(x, 7) ^ rotr(x, 18) ^ (x >> 3);
+            const uint32_t s1 = rotr(y, 17) ^ rotr(y, 19) ^ (y >> 10);
+            w = s1 + W[(t - 7) & 15] + s0 + W[t & 15];
+            W[t & 15] = w;
+        }
+        const uint32_t S1 = rotr(e, 6) ^ rotr(e, 11) ^ rotr(e, 25);
+        const uint32_t ch = (e & f) ^ (~e & g);
+        const uint32_t T1 = h + S1 + ch + c_K[t] + w;
+        const uint32_t S0 = rotr(a, 2) ^ rotr(a, 13) ^ rotr(a, 22);
+        const uint32_t maj = (a & b) ^ (a & c) ^ (b & c);
+        const uint32_t T2 = S0 + maj;
+        h = g; g = f; f = e; e = d + T1;
+        d = c; c = b; b = a; a = T1 + T2;
+    }
+    st[0] += a; st[1] += b; st[2] += c; st[3] += d;
+    st[4] += e; st[5] += f; st[6] += g; st[7] += h;
+}
+
+__device__ __forceinline__ void sha256_init(uint32_t (&st)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) st[i] = c_H0[i];
+}
+
+// Digest of a full, 16-byte aligned leaf of `leaf` bytes (a multiple of 64):
+// the message 0x00 || data is shifted one byte against the data, so message
+// word t of block b is bytes [64b + 4t - 1, 64b + 4t + 3) of the data, built
+// from two little-endian data words with one byte permute.
+__device__ __forceinline__ void leaf_digest_fast(const uint8_t *__restrict__ p, uint32_t leaf,
+                                                 uint32_t (&st)[8]) {
+    sha256_init(st);
+    const uint4 *q = reinterpret_cast<const uint4 *>(p);
+    uint32_t prev = 0;   // byte 3 of "word -1" is the 0x00 prefix
+    const uint32_t nblk = leaf / 64;
+#pragma unroll 1
+    for (uint32_t blk = 0; blk < nblk; ++blk) {
+        uint32_t d[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint4 x = __ldcs(q + 4 * blk + v);
+            d[4 * v] = x.x; d[4 * v + 1] = x.y; d[4 * v + 2] = x.z; d[4 * v + 3] = x.w;
+        }
+        uint32_t W[16];
+        W[0] = __byte_perm(prev, d[0], 0x3456);
+#pragma unroll
+        for (int t = 1; t < 16; ++t) W[t] = __byte_perm(d[t - 1], d[t], 0x3456);
+        prev = d[15];
+        sha256_compress(st, W);
+    }
+    // final block: last data byte, 0x80, zeros, 64-bit big-endian bit length
+    const uint64_t bits = (uint64_t(leaf) + 1u) * 8u;
+    uint32_t W[16];
+    W[0] = (prev & 0xff000000u) | 0x00800000u;
+#pragma unroll
+    for (int t = 1; t < 14; ++t) W[t] = 0u;
+    W[14] = uint32_t(bits >> 32);
+    W[15] = uint32_t(bits);
+    sha256_compress(st, W);
+}
+
+// Digest of 0x00 || p[0 .. L) for any L and alignment, byte by byte (the
+// short last leaf, or inputs that are not 16-byte aligned).
+__device__ void leaf_digest_generic(const uint8_t *__restrict__ p, uint64_t L, uint32_t (&st)[8]) {
+    sha256_init(st);
+    const uint64_t ml = L + 1;                 // message bytes
+    const uint64_t nblk = (ml + 8) / 64 + 1;   // with 0x80 and the 8-byte length
+    const uint64_t len_at = nblk * 64 - 8;
+    const uint64_t bits = ml * 8u;
+#pragma unroll 1
+    for (uint64_t blk = 0; blk < nblk; ++blk) {
+        uint32_t W[16];
+#pragma unroll 1
+        for (int t = 0; t < 16; ++t) {
+            uint32_t w = 0;
+            for (int j = 0; j < 4; ++j) {
+                const uint64_t pos = blk * 64 + 4 * t + j;
+                uint32_t byte;
+                if (pos == 0) byte = 0x00u;
+                else if (pos <= L) byte = p[pos - 1];
+                else if (pos == L + 1) byte = 0x80u;
+                else if (pos >= len_at) byte = uint32_t(bits >> (56 - 8 * (pos - len_at))) & 0xffu;
+                else byte = 0u;
+                w = (w << 8) | byte;
+            }
+            W[t] = w;
+        }
+        sha256_compress(st, W);
+    }
+}
+
+// SHA256(0x01 || L || R) for two digests held as big-endian state words.
+__device__ __forceinline__ void node_digest(const uint32_t (&L)[8], const uint32_t (&R)[8],
+                                            uint32_t (&out)[8]) {
+    sha256_init(out);
+    uint32_t W[16];
+    W[0] = 0x01000000u | (L[0] >> 8);
+#pragma unroll
+    for (int t = 1; t < 8; ++t) W[t] = (L[t - 1] << 24) | (L[t] >> 8);
+    W[8] = (L[7] << 24) | (R[0] >> 8);
+#pragma unroll
+    for (int t = 9; t < 16; ++t) W[t] = (R[t - 9] << 24) | (R[t - 8] >> 8);
+    sha256_compress(out, W);
+    // second block: last byte of R, 0x80, zeros, bit length 65 * 8 = 520
+    W[0] = (R[7] << 24) | 0x00800000u;
+#pragma unroll
+    for (int t = 1; t < 15; ++t) W[t] = 0u;
+    W[15] = 520u;
+    sha256_compress(out, W);
+}
+
+__device__ __forceinline__ void store_root(uint8_t *root, const uint32_t (&st)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        root[4 * i] = uint8_t(st[i] >> 24);
+        root[4 * i + 1] = uint8_t(st[i] >> 16);
+        root[4 * i + 2] = uint8_t(st[i] >> 8);
+        root[4 * i + 3] = uint8_t(st[i]);
+    }
+}
+
+// Folds `cnt` digests held word-major in buf[0] ([8][N]) down to buf[?][.][0]
+// level by level; returns the buffer index holding the result.  Every thread
+// of the CTA must call it (it synchronises).
+template <int N>
+__device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt) {
+    int cur = 0;
+    while (cnt > 1) {   // uniform across the CTA
+        __syncthreads();
+        const int pairs = cnt / 2;
+        for (int j = threadIdx.x; j < (cnt + 1) / 2; j += blockDim.x) {
+            uint32_t o[8];
+            if (j < pairs) {
+                uint32_t l[8], r[8];
+#pragma unroll
+                for (int w = 0; w < 8; ++w) { l[w] = buf[cur][w][2 * j]; r[w] = buf[cur][w][2 * j + 1]; }
+                node_digest(l, r, o);
+            } else {   // unpaired last node: promoted unchanged
+#pragma unroll
+                for (int w = 0; w < 8; ++w) o[w] = buf[cur][w][cnt - 1];
+            }
+#pragma unroll
+            for (int w = 0; w < 8; ++w) buf[cur ^ 1][w][j] = o[w];
+        }
+        cur ^= 1;
+        cnt = (cnt + 1) / 2;
+    }
+    __syncthreads();
+    return cur;
+}
+
+__global__ void __launch_bounds__(LEAF_CTA)
+merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t leaf, uint64_t nleaves,
+                    int fast_ok, uint32_t *__restrict__ level_out, uint8_t *__restrict__ root_out) {
+    __shared__ uint32_t buf[2][8][LEAF_CTA];
+    const uint64_t base = uint64_t(blockIdx.x) * LEAF_CTA;
+    const uint64_t i = base + threadIdx.x;
+    if (i < nleaves) {
+        const uint64_t start = i * leaf;
+        const uint64_t len = min(uint64_t(leaf), bytes - start);
+        uint32_t st[8];
+        if (fast_ok && len == leaf) leaf_digest_fast(data + start, leaf, st);
+        else leaf_digest_generic(data + start, len, st);
+#pragma unroll
+        for (int w = 0; w < 8; ++w) buf[0][w][threadIdx.x] = st[w];
+    }
+    const int cnt = int(min(uint64_t(LEAF_CTA), nleaves - base));
+    const int cur = cta_fold<LEAF_CTA>(buf, cnt);
+    if (threadIdx.x == 0) {
+        uint32_t st[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) st[w] = buf[cur][w][0];
+        if (root_out) {
+            store_root(root_out, st);
+        } else {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) level_out[8 * blockIdx.x + w] = st[w];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(RED_CTA)
+merkle_reduce(const uint32_t *__restrict__ in, uint64_t n, uint32_t *__restrict__ out,
+              uint8_t *__restrict__ root_out) {
+    __shared__ uint32_t buf[2][8][2 * RED_CTA];
+    const uint64_t base = uint64_t(blockIdx.x) * 2 * RED_CTA;
+    const int cnt = int(min(uint64_t(2 * RED_CTA), n - base));
+    for (int j = threadIdx.x; j < cnt; j += RED_CTA) {
+        const uint4 lo = *reinterpret_cast<const uint4 *>(in + 8 * (base + j));
+        const uint4 hi = *reinterpret_cast<const uint4 *>(in + 8 * (base + j) + 4);
+        buf[0][0][j] = lo.x; buf[0][1][j] = lo.y; buf[0][2][j] = lo.z; buf[0][3][j] = lo.w;
+        buf[0][4][j] = hi.x; buf[0][5][j] = hi.y; buf[0][6][j] = hi.z; buf[0][7][j] = hi.w;
+    }
+    const int cur = cta_fold<2 * RED_CTA>(buf, cnt);
+    if (threadIdx.x == 0) {
+        uint32_t st[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) st[w] = buf[cur][w][0];
+        if (root_out) {
+            store_root(root_out, st);
+        } else {
+#pragma unroll
+            for (int w = 0; w < 8; ++w) out[8 * blockIdx.x + w] = st[w];
+        }
+    }
+}
+
+struct Plan {
+    uint64_t nleaves = 0;
+    uint64_t n1 = 0;          // nodes after the leaf kernel
+    uint64_t n2 = 0;          // nodes after the first reduce pass
+    uint64_t ws_bytes = 0;    // scratch: n1 + n2 nodes of 32 bytes (0 if n1 == 1)
+};
+
+bool plan_for(uint64_t bytes, uint32_t leaf, Plan *p) {
+    if (bytes == 0 || leaf < 64 || leaf % 64 != 0 || leaf > (1u << 30)) return false;
+    p->nleaves = (bytes + leaf - 1) / leaf;
+    p->n1 = (p->nleaves + LEAF_CTA - 1) / LEAF_CTA;
+    if (p->n1 > 0x7fffffffull) return false;
+    p->n2 = p->n1 > 1 ? (p->n1 + 2 * RED_CTA - 1) / (2 * RED_CTA) : 0;
+    p->ws_bytes = p->n1 > 1 ? (p->n1 + p->n2) * 32u : 0;
+    return true;
+}
+
+int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void *ws, const Plan &pl,
+        cudaStream_t stream) {
+    const uint8_t *data = static_cast<const uint8_t *>(ptr);
+    const int fast_ok = reinterpret_cast<uintptr_t>(data) % 16 == 0;
+    uint32_t *bufA = static_cast<uint32_t *>(ws);
+    uint32_t *bufB = bufA ? bufA + 8 * pl.n1 : nullptr;
+    merkle_leaf_subtree<<<unsigned(pl.n1), LEAF_CTA, 0, stream>>>(
+        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr);
+    int rc = check_launch();
+    if (rc != REPOPS_OK) return rc;
+    uint64_t n = pl.n1;
+    uint32_t *src = bufA, *dst = bufB;
+    while (n > 1) {
+        const uint64_t blocks = (n + 2 * RED_CTA - 1) / (2 * RED_CTA);
+        merkle_reduce<<<unsigned(blocks), RED_CTA, 0, stream>>>(src, n, dst, blocks == 1 ? root_out : nullptr);
+        rc = check_launch();
+        if (rc != REPOPS_OK) return rc;
+        n = blocks;
+        std::swap(src, dst);
+    }
+    return REPOPS_OK;
+}
+
+int check_args(const void *ptr, uint64_t bytes, uint32_t leaf, const uint8_t *root_out, Plan *pl) {
+    if (!ptr || !root_out) return REPOPS_ERR_INVALID_ARG;
+    if (!plan_for(bytes, leaf, pl)) return REPOPS_ERR_INVALID_ARG;
+    if (ranges_overlap(ptr, bytes, root_out, 32)) return REPOPS_ERR_ALIAS;
+    return REPOPS_OK;
+}
+
+}  // namespace
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" uint64_t repops_merkle_workspace_bytes(uint64_t bytes, uint32_t leaf) {
+    Plan pl;
+    return plan_for(bytes, leaf, &pl) ? pl.ws_bytes : 0;
+}
+
+extern "C" int repops_merkle_sha256_ws(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out,
+                                       void *workspace, uint64_t workspace_bytes, cudaStream_t stream) {
+    Plan pl;
+    int rc = check_args(ptr, bytes, leaf, root_out, &pl);
+    if (rc != REPOPS_OK) return rc;
+    if (pl.ws_bytes > 0) {
+        if (!workspace || workspace_bytes < pl.ws_bytes || reinterpret_cast<uintptr_t>(workspace) % 16)
+            return REPOPS_ERR_INVALID_ARG;
+        if (ranges_overlap(workspace, pl.ws_bytes, ptr, bytes) ||
+            ranges_overlap(workspace, pl.ws_bytes, root_out, 32))
+            return REPOPS_ERR_ALIAS;
+    }
+    return run(ptr, bytes, leaf, root_out, pl.ws_bytes ? workspace : nullptr, pl, stream);
+}
+
+extern "C" int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out,
+                                    cudaStream_t stream) {
+    Plan pl;
+    int rc = check_args(ptr, bytes, leaf, root_out, &pl);
+    if (rc != REPOPS_OK) return rc;
+    void *ws = nullptr;
+    if (pl.ws_bytes > 0) {
+        cudaError_t e = cudaMallocAsync(&ws, pl.ws_bytes, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return REPOPS_ERR_ALLOC;
+        }
+    }
+    rc = run(ptr, bytes, leaf, root_out, ws, pl, stream);
+    if (ws) {
+        cudaError_t e = cudaFreeAsync(ws, stream);
+        if (e != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
+    }
+    return rc;
+}
