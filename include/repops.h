@@ -230,6 +230,37 @@ int repops_merkle_sha256_ws(const void *ptr, uint64_t bytes, uint32_t leaf,
                             uint8_t *root_out, void *workspace,
                             uint64_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the fixed device scratch behind repops_merkle_sha256_noalloc. */
+#define REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES (1u << 20)
+
+/* The paper has no counterpart to this entry point; it is a deployment aid.
+ *
+ * As repops_merkle_sha256, but it allocates nothing: no cudaMalloc, no
+ * cudaMallocAsync, no caller workspace.  It is meant for callers that cannot
+ * allocate device memory when they hash -- a host framework that has reserved
+ * all device memory for its own pool, a latency-critical path on which an
+ * allocation could block or synchronise, a plug-in whose host forbids
+ * allocations after start-up.  The caller still passes the input (ptr,
+ * device) and the output (root_out, device, 32 bytes).
+ *
+ * Scratch comes from one fixed array of REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES
+ * (1 MiB) in the library's device image; every GPU that loads the library
+ * holds it until the process exits.  Inputs whose
+ * repops_merkle_workspace_bytes(bytes, leaf) exceeds that size are rejected
+ * with REPOPS_ERR_UNSUPPORTED before anything runs: at 4096-byte leaves the
+ * limit is 4,186,112 leaves (about 16 GiB of input); inputs of at most 128
+ * leaves need no scratch at all.
+ *
+ * The first call on each device looks up the array's device address (once
+ * per device, with that device current) and caches it; make that first call
+ * before any stream capture.  All calls share the array and it keeps the last
+ * call's contents (nothing in it needs to start at zero).  Calls whose work
+ * overlaps on the GPU -- e.g. on two streams with no ordering between them --
+ * race on the array: order them on one stream.  Other errors as
+ * repops_merkle_sha256, without ALLOC. */
+int repops_merkle_sha256_noalloc(const void *ptr, uint64_t bytes, uint32_t leaf,
+                                 uint8_t *root_out, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

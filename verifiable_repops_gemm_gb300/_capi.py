@@ -45,7 +45,10 @@ SIGNATURES = {
     "repops_merkle_sha256": (_i32, [_vp, _u64, _u32, _vp, _vp]),
     "repops_merkle_workspace_bytes": (_u64, [_u64, _u32]),
     "repops_merkle_sha256_ws": (_i32, [_vp, _u64, _u32, _vp, _vp, _u64, _vp]),
+    "repops_merkle_sha256_noalloc": (_i32, [_vp, _u64, _u32, _vp, _vp]),
 }
+
+MERKLE_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 _lib = None
 

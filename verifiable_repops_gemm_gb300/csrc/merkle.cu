@@ -21,6 +21,7 @@
 // SHA-256 is bound by the integer ALU (about 22 integer instructions per
 // message byte), far below HBM bandwidth.
 #include <algorithm>
+#include <atomic>
 
 #include "internal.cuh"
 
@@ -357,4 +358,66 @@ extern "C" int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t le
         if (e != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
     }
     return rc;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant.
+//
+// For callers that must not allocate device memory when they hash: a host
+// framework that has reserved all device memory for its own pool, a
+// latency-critical path on which an allocation could block or synchronise, or
+// a plug-in whose host forbids allocations after start-up.  The scratch of the
+// level nodes lives in the fixed array below instead of coming from
+// cudaMallocAsync or from the caller.
+//
+// The array is part of the library's device image: every GPU that loads the
+// library holds these bytes until the process exits.  All calls share it and
+// it keeps whatever the last call left there; nothing in it needs to start at
+// zero, because every node is written before it is read.  Two calls whose work
+// overlaps on the GPU (different streams, no ordering between them) race on
+// the array and may return wrong roots.
+// ---------------------------------------------------------------------------
+
+static_assert(REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES % 256 == 0, "scratch size");
+static __device__ __align__(256) unsigned char g_merkle_noalloc_scratch[REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES];
+
+namespace repops {
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::atomic<void *> g_noalloc_scratch_addr[kNoallocMaxDevices];
+
+// Device address of the scratch array on the current device.  In host code the
+// array's name only stands in for the symbol, so the address is looked up once
+// per device, with that device current, and cached.
+int noalloc_scratch_address(void **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev < 0 || dev >= kNoallocMaxDevices) return REPOPS_ERR_UNSUPPORTED;
+    void *p = g_noalloc_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_merkle_noalloc_scratch);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        g_noalloc_scratch_addr[dev].store(p, std::memory_order_release);
+    }
+    *out = p;
+    return REPOPS_OK;
+}
+
+}  // namespace
+}  // namespace repops
+
+extern "C" int repops_merkle_sha256_noalloc(const void *ptr, uint64_t bytes, uint32_t leaf,
+                                            uint8_t *root_out, cudaStream_t stream) {
+    Plan pl;
+    int rc = check_args(ptr, bytes, leaf, root_out, &pl);
+    if (rc != REPOPS_OK) return rc;
+    if (pl.ws_bytes > REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES) return REPOPS_ERR_UNSUPPORTED;
+    void *ws = nullptr;
+    if (pl.ws_bytes > 0) {
+        rc = noalloc_scratch_address(&ws);
+        if (rc != REPOPS_OK) return rc;
+    }
+    return run(ptr, bytes, leaf, root_out, ws, pl, stream);
 }
