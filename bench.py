@@ -39,11 +39,21 @@ METRIC = "Bit-exact fixed-order FP32 GEMM TFLOP/s vs FP32 peak; mean/commit HBM 
 GEMM_N = 8192
 SM_MAX_MHZ_NOMINAL = 2070.0          # GB300 maximum SM clock
 FP32_LANES_PER_SM = 128              # FP32 CUDA cores per SM
+# integer lanes per SM that SHA-256 can use: the ALU pipe (16 lanes per SM
+# sub-partition) plus the integer multiply-add pipe (16 per sub-partition)
+INT_LANES_PER_SM = 128
+# integer operations of one SHA-256 compression in its standard form with
+# 3-input logic/add instructions and funnel-shift rotates: 64 rounds x 14
+# (6 rotates, Ch, Maj, 2 XOR3, 4 adds) + 48 schedule words x 10 + 24
+# (message words and state update)
+SHA_OPS_PER_COMPRESSION = 64 * 14 + 48 * 10 + 24
 L2_BYTES = 129 * 10 ** 6
 
-# DRAM traffic per GEMM launch at 8192^3 from one ncu capture, valid only for
-# the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": None, "bytes_per_launch": None}
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
+# launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
+# valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
+GEMM_TRAFFIC = {"src_sha256": "472911c05f88fb688f0f0c6f76587296d5af57943c2b4c0f0f3b3f85feb4a8f5",
+                "bytes_per_launch": 4900395264 + 267397376}
 
 
 def measured_peaks():
@@ -52,6 +62,13 @@ def measured_peaks():
         with open(p) as f:
             return json.load(f), "measured"
     return {"hbm_gbs": 6800.0, "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
+
+
+def gemm_kernel_label():
+    cfg = rp.gemm_auto_config(GEMM_N, GEMM_N, GEMM_N)
+    ci = rp.gemm_config_info(cfg)
+    return ("gemm_tma_ws_kernel config %d: %dx%d CTA tile, %d consumer threads + 1 producer warp, "
+            "%dx%d per thread" % (cfg, ci["bm"], ci["bn"], ci["threads"], ci["tm"], ci["tn"]))
 
 
 def kernel_source_sha():
@@ -406,6 +423,10 @@ def run_ours(args):
     mean_gbs = w.mean_bytes * args.steps * world / (mean_max / 1e3) / 1e9
     merk_gbs = (w.tbytes + w.cbytes) * args.steps * world / (merk_max / 1e3) / 1e9
     value = w.gemm_flops * args.steps * world / (gemm_max / 1e3) / 1e12
+    ncomp = sha_compressions(w.tbytes) + sha_compressions(w.cbytes)
+    comp_rate = ncomp * args.steps / (merk_max / 1e3) / 1e9
+    comp_peak = sms * INT_LANES_PER_SM * peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL) * 1e6 \
+        / SHA_OPS_PER_COMPRESSION / 1e9
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_max / args.steps,
@@ -418,11 +439,20 @@ def run_ours(args):
         "parts": {
             "gemm": {"value": value, "unit": "TFLOP/s", "ms": statistics.mean(gemm_ms)},
             "mean_sgd": {"value": mean_gbs, "unit": "GB/s", "ms": statistics.mean(mean_ms),
-                         "frac_of_hbm": mean_gbs / world / hbm},
+                         "roofline": {"bound": "hbm", "achieved": mean_gbs / world, "peak": hbm,
+                                      "unit": "GB/s", "frac": mean_gbs / world / hbm,
+                                      "basis": "(16 + 2) x 2^28 x 4 B per step; peak = %s hbm_gbs"
+                                               % peaks_kind}},
             "merkle": {"value": merk_gbs, "unit": "GB/s", "ms": statistics.mean(merk_ms),
-                       "sha256_compressions_per_step": sha_compressions(w.tbytes) + sha_compressions(w.cbytes)},
+                       "sha256_compressions_per_step": ncomp,
+                       "roofline": {"bound": "alu", "achieved": comp_rate, "peak": comp_peak,
+                                    "unit": "Gcompressions/s", "frac": comp_rate / comp_peak,
+                                    "basis": "(64 ALU + 64 IMAD lanes) x %d SMs x %.0f MHz / %d integer "
+                                             "operations per SHA-256 compression"
+                                             % (sms, peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL),
+                                                SHA_OPS_PER_COMPRESSION)}},
         },
-        "roofline": {"kernel": "gemm_tma_kernel (128x128, 8x8/thread)", "bound": "alu",
+        "roofline": {"kernel": gemm_kernel_label(), "bound": "alu",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_basis": "%d SMs x 128 FP32 lanes x %.0f MHz (%s sm_max_mhz); one FP32 "

@@ -66,6 +66,13 @@ def test_merkle_detects_one_bit_flip(rp):
 
 
 @pytest.mark.slow
+def test_merkle_1gib_tensor(rp, orc):
+    # 2^28 fp32 (1 GiB), N(0, 0.02): 2^18 leaves, 2048 leaf CTAs (a full GPU)
+    x = inputs.normal((1 << 28,), 0.02, 302, DEV)
+    assert root(rp, x) == orc.merkle_root(x.cpu().numpy(), 4096)
+
+
+@pytest.mark.slow
 def test_merkle_4gib_tensor(rp, orc):
     # 2^30 fp32 (4 GiB), N(0, 0.02), 4096-byte leaves: 2^20 leaves
     x = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300, DEV)

@@ -3,10 +3,11 @@
 // What is computed ("Verde与RepOps" §3.2, matmul example): for every output
 // element, sum = +0; for k = 0 .. K-1 in increasing order: sum = fl(sum +
 // fl(A[i][k] * B[k][j])).  The product and the add are separate IEEE
-// round-to-nearest operations (__fmul_rn / __fadd_rn are never contracted into
-// a fused multiply-add; the library is also built with -fmad=false).  Tensor
-// cores are not used: their internal accumulation order and rounding would
-// change the bits.
+// round-to-nearest operations: products are __fmul_rn (never contracted into a
+// fused multiply-add), sums are add.rn.f32x2 -- two independent binary32 adds
+// in one instruction, each rounded on its own -- and the library is built with
+// -fmad=false.  Tensor cores are not used: their internal accumulation order
+// and rounding would change the bits.
 //
 // How it is parallelised (§3.2 design principle: order-independent dimensions
 // run in parallel, the order-critical one runs serially):
@@ -14,10 +15,12 @@
 //     registers; the k loop is the only serial loop and every accumulator sees
 //     k = 0, 1, 2, ... in that order -- no split-K, no reassociation;
 //   - operands are staged through a STAGES-deep shared-memory ring of BK = 32
-//     k-slices, filled either by TMA (cp.async.bulk.tensor, one elected thread,
-//     completion on an mbarrier) or, for operands TMA cannot describe
-//     (unaligned pointers or leading dimensions), by 4-byte cp.async with zero
-//     fill.  Both loaders produce the same shared-memory image;
+//     k-slices.  TMA path: a producer warp issues cp.async.bulk.tensor copies,
+//     completion is counted on a "full" mbarrier per slot, consumer warps
+//     release a slot on its "empty" mbarrier -- no CTA-wide barrier in the main
+//     loop.  cp.async path (operands TMA cannot describe: unaligned pointers or
+//     leading dimensions): every thread copies 4-byte elements with zero fill.
+//     Both loaders produce the same shared-memory image;
 //   - the k tail is zero-filled in BOTH operands.  fl(0*0) = +0, and the
 //     accumulator is never -0 (it starts at +0, and round-to-nearest gives +0
 //     for an exact cancellation), so adding +0 leaves it bit-identical.
@@ -43,18 +46,30 @@ namespace gemm {
 
 constexpr int BK = 32;   // k-extent of one stage: 32 fp32 = one 128-byte row
 
-template <int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_>
+// Unroll of the 4-k chunk loop inside one 32-k slice.  Measured at 8192^3:
+// both operands K-inner run best at 1, every other layout at 4.
+template <bool A_KIN, bool B_KIN>
+struct K4Unroll {
+    static constexpr int value = (A_KIN && B_KIN) ? 1 : 4;
+};
+
+// TM x TN accumulators per thread, WARPS_M x WARPS_N consumer warps, STAGES
+// ring slots.  MINB_: CTAs per SM the register allocation must allow (0 means
+// 2 for CTAs of at most 128 consumer threads, else 1).
+template <int TM_, int TN_, int WARPS_M_, int WARPS_N_, int STAGES_, int MINB_ = 0>
 struct Tile {
     static constexpr int TM = TM_, TN = TN_;
     static constexpr int WARPS_M = WARPS_M_, WARPS_N = WARPS_N_, STAGES = STAGES_;
+    static constexpr int MINB = MINB_ ? MINB_ : (32 * WARPS_M_ * WARPS_N_ <= 128 ? 2 : 1);
     static constexpr int WM = 4 * TM, WN = 8 * TN;   // warp tile: 4 x 8 lanes
     static constexpr int BM = WARPS_M * WM, BN = WARPS_N * WN;
-    static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
+    static constexpr int THREADS = 32 * WARPS_M * WARPS_N;   // consumer threads
     static constexpr int A_FLOATS = BM * BK, B_FLOATS = BN * BK;
     static constexpr int STAGE_FLOATS = A_FLOATS + B_FLOATS;
     static constexpr int STAGE_BYTES = STAGE_FLOATS * 4;
-    // ring + 1 KiB for aligning the base to the 1 KiB swizzle atom + barriers
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 8 * STAGES;
+    // ring + 1 KiB for aligning the base to the 1 KiB swizzle atom + full and
+    // empty barriers
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 16 * STAGES;
     static_assert(TM % 4 == 0 && TN % 4 == 0, "per-thread tile is made of float4 runs");
     static_assert(BM % 8 == 0 && BN % 8 == 0, "the swizzle atom is 8 rows");
     static_assert(BM <= 256 && BN <= 256, "TMA box extent is at most 256");
@@ -67,15 +82,16 @@ __device__ __forceinline__ int kin_off(int r, int k) {
 }
 
 // Grouped rasterisation: consecutive CTAs walk down GROUP tile-rows before
-// moving right, so CTAs resident together share A row-panels and B column-panels
-// in L2.
+// moving right, so the CTAs resident together share A row-panels and B
+// column-panels in L2 (GROUP * BM = 2048 rows).
+template <int BM>
 __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int &tm, int &tn) {
-    constexpr int GROUP = 8;
-    const int per_group = GROUP * tiles_n;
-    const int g = bid / per_group;
+    constexpr int GROUP = BM >= 2048 ? 1 : 2048 / BM;
+    const long long per_group = (long long)GROUP * tiles_n;
+    const int g = int(bid / per_group);
     const int first_m = g * GROUP;
     const int gm = min(tiles_m - first_m, GROUP);
-    const int in_group = bid - g * per_group;
+    const int in_group = int(bid - g * per_group);
     tm = first_m + in_group % gm;
     tn = in_group / gm;
 }
@@ -95,13 +111,73 @@ __device__ __forceinline__ int b_col(int bbase, int c) {
     return B_KIN ? bbase + 8 * c : bbase + 32 * (c / 4) + (c % 4);
 }
 
-// One stage (32 k-steps) of the serial k-chain for this thread's TM x TN
-// accumulators.  k advances in increasing order: k4 (chunks of 4), then kk.
+// ------------------------------------------------------ packed FP32 adds ----
+// The products stay scalar (__fmul_rn, one rounding each) and one packed add
+// folds two of them into two accumulators: 3 FP32 instructions per pair of
+// multiply-adds instead of 4, the same per-lane operations and bits.  Packed
+// multiplies are not used: ptxas has been measured fusing a packed multiply
+// with a packed add into a fused multiply-add even with explicit
+// round-to-nearest modifiers and -fmad=false.
+
+using u64 = unsigned long long;
+
+__device__ __forceinline__ u64 pack2(float lo, float hi) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ void unpack2(u64 v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+__device__ __forceinline__ u64 add2_rn(u64 a, u64 b) {
+    u64 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// acc (two lanes) = (fl(acc.lo + fl(x0*y0)), fl(acc.hi + fl(x1*y1)))
+__device__ __forceinline__ u64 fold2(u64 acc, float x0, float y0, float x1, float y1) {
+    return add2_rn(acc, pack2(__fmul_rn(x0, y0), __fmul_rn(x1, y1)));
+}
+
+// A thread's accumulators, held in pairs: along n when A is K-inner, along m
+// when A is MN-inner (the two products of a pair are independent scalars).
+template <class T, bool A_KIN>
+struct PackedAcc {
+    static constexpr bool PAIR_N = A_KIN;
+    static constexpr int R = PAIR_N ? T::TM : T::TM / 2;
+    static constexpr int C = PAIR_N ? T::TN / 2 : T::TN;
+    u64 v[R][C];
+
+    __device__ __forceinline__ void zero() {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int j = 0; j < C; ++j) v[i][j] = 0ull;   // two +0.0f
+    }
+
+    __device__ __forceinline__ void to_float(float (&f)[T::TM][T::TN]) const {
+#pragma unroll
+        for (int i = 0; i < R; ++i)
+#pragma unroll
+            for (int j = 0; j < C; ++j) {
+                float lo, hi;
+                unpack2(v[i][j], lo, hi);
+                if (PAIR_N) { f[i][2 * j] = lo; f[i][2 * j + 1] = hi; }
+                else        { f[2 * i][j] = lo; f[2 * i + 1][j] = hi; }
+            }
+    }
+};
+
+// One stage (32 k-steps) of the serial k-chain for this thread's accumulators.
+// k advances in increasing order: k4 (chunks of 4), then kk.
 template <class T, bool A_KIN, bool B_KIN>
 __device__ __forceinline__ void mma_stage(const float *__restrict__ As, const float *__restrict__ Bs,
                                           int abase, int bbase, int lm, int ln,
-                                          float (&acc)[T::TM][T::TN]) {
-#pragma unroll 2
+                                          PackedAcc<T, A_KIN> &acc) {
+#pragma unroll(K4Unroll<A_KIN, B_KIN>::value)
     for (int k4 = 0; k4 < BK / 4; ++k4) {
         float a[T::TM][4];
         float b[T::TN][4];
@@ -149,12 +225,18 @@ __device__ __forceinline__ void mma_stage(const float *__restrict__ As, const fl
         }
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
+            if constexpr (PackedAcc<T, A_KIN>::PAIR_N) {
 #pragma unroll
-            for (int r = 0; r < T::TM; ++r) {
+                for (int r = 0; r < T::TM; ++r)
 #pragma unroll
-                for (int c = 0; c < T::TN; ++c) {
-                    acc[r][c] = __fadd_rn(acc[r][c], __fmul_rn(a[r][kk], b[c][kk]));
-                }
+                    for (int j = 0; j < T::TN / 2; ++j)
+                        acc.v[r][j] = fold2(acc.v[r][j], a[r][kk], b[2 * j][kk], a[r][kk], b[2 * j + 1][kk]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < T::TM / 2; ++i)
+#pragma unroll
+                    for (int c = 0; c < T::TN; ++c)
+                        acc.v[i][c] = fold2(acc.v[i][c], a[2 * i][kk], b[c][kk], a[2 * i + 1][kk], b[c][kk]);
             }
         }
     }
@@ -164,7 +246,9 @@ __device__ __forceinline__ void mma_stage(const float *__restrict__ As, const fl
 template <class T, bool A_KIN, bool B_KIN>
 __device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
                                            int64_t m0, int64_t n0, int abase, int bbase,
-                                           const float (&acc)[T::TM][T::TN], bool c_vec) {
+                                           const PackedAcc<T, A_KIN> &pacc, bool c_vec) {
+    float acc[T::TM][T::TN];
+    pacc.to_float(acc);
 #pragma unroll
     for (int r = 0; r < T::TM; ++r) {
         const int64_t gm = m0 + a_row<A_KIN>(abase, r);
@@ -193,54 +277,77 @@ __device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, i
     }
 }
 
-template <class T>
 __device__ __forceinline__ float *aligned_smem_base(unsigned char *raw) {
     return reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
 
 // ------------------------------------------------------------------ TMA ----
 
+// THREADS consumer threads plus one producer warp.  The producer's lane 0
+// refills ring slot s with TMA once every consumer warp has arrived on
+// empty[s]; consumers wait on full[s] (TMA transaction bytes) and never
+// synchronise the whole CTA, so warps drift within the ring instead of meeting
+// at a barrier every k-slice.  Every wait is bounded; on a timeout the status
+// bit is set, the producer lets its in-flight copies land, and the tile is not
+// stored.
 template <class T, bool A_KIN, bool B_KIN>
-__global__ void __launch_bounds__(T::THREADS, 1)
-gemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                float *__restrict__ C, int64_t M, int64_t N, int64_t K, int64_t ldc,
-                int tiles_m, int tiles_n, int c_vec, unsigned *status) {
+__global__ void __launch_bounds__(T::THREADS + 32, T::MINB)
+gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   float *__restrict__ C, int64_t M, int64_t N, int64_t K, int64_t ldc,
+                   int tiles_m, int tiles_n, int c_vec, unsigned *status) {
+    constexpr int CONSUMER_WARPS = T::THREADS / 32;
     extern __shared__ unsigned char smem_raw[];
-    float *smem = aligned_smem_base<T>(smem_raw);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + T::STAGES * T::STAGE_FLOATS);
+    float *smem = aligned_smem_base(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::STAGES * T::STAGE_FLOATS);
+    uint64_t *empty = full + T::STAGES;
 
     const int tid = threadIdx.x;
     int tm, tn;
-    tile_coords(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
     const int KT = int((K + BK - 1) / BK);
 
-    if (tid == 0) {
+    if (tid == T::THREADS) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
 #pragma unroll 1
-        for (int s = 0; s < T::STAGES; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CONSUMER_WARPS);
+        }
         fence_barrier_init();
     }
     __syncthreads();
 
-    // thread 0 only: put k-slice `kt` in flight into its ring slot
-    auto issue = [&](int kt) {
-        const int s = kt % T::STAGES;
-        float *As = smem + s * T::STAGE_FLOATS;
-        float *Bs = As + T::A_FLOATS;
-        mbar_arrive_expect_tx(&bars[s], T::STAGE_BYTES);
-        const int k0 = kt * BK;
-        if constexpr (A_KIN) tma_load_2d(As, &tmA, &bars[s], k0, int(m0));
-        else                 tma_load_2d(As, &tmA, &bars[s], int(m0), k0);
-        if constexpr (B_KIN) tma_load_2d(Bs, &tmB, &bars[s], k0, int(n0));
-        else                 tma_load_2d(Bs, &tmB, &bars[s], int(n0), k0);
-    };
-
-    int issued = 0;
-    if (tid == 0) {
+    if (tid >= T::THREADS) {   // producer warp
+        if (tid == T::THREADS) {
+            int issued = 0;
+            bool ok = true;
 #pragma unroll 1
-        for (; issued < T::STAGES - 1 && issued < KT; ++issued) issue(issued);
+            for (int kt = 0; kt < KT; ++kt) {
+                const int s = kt % T::STAGES;
+                if (kt >= T::STAGES &&
+                    !mbar_wait_bounded(&empty[s], uint32_t(kt / T::STAGES - 1) & 1u)) {
+                    ok = false;
+                    break;
+                }
+                float *As = smem + s * T::STAGE_FLOATS;
+                float *Bs = As + T::A_FLOATS;
+                mbar_arrive_expect_tx(&full[s], T::STAGE_BYTES);
+                const int k0 = kt * BK;
+                if constexpr (A_KIN) tma_load_2d(As, &tmA, &full[s], k0, int(m0));
+                else                 tma_load_2d(As, &tmA, &full[s], int(m0), k0);
+                if constexpr (B_KIN) tma_load_2d(Bs, &tmB, &full[s], k0, int(n0));
+                else                 tma_load_2d(Bs, &tmB, &full[s], int(n0), k0);
+                issued = kt + 1;
+            }
+            if (!ok) atomicOr(status, 1u);
+            // every copy in flight must land before the CTA's shared memory is released
+#pragma unroll 1
+            for (int kt = max(0, issued - T::STAGES); kt < issued; ++kt)
+                mbar_wait_bounded(&full[kt % T::STAGES], uint32_t(kt / T::STAGES) & 1u);
+        }
+        return;
     }
 
     const int warp = tid >> 5, lane = tid & 31;
@@ -249,32 +356,19 @@ gemm_tma_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     const int abase = warp_m * T::WM + (A_KIN ? lm : lm * T::TM);
     const int bbase = warp_n * T::WN + (B_KIN ? ln : ln * 4);
 
-    float acc[T::TM][T::TN];
-#pragma unroll
-    for (int r = 0; r < T::TM; ++r)
-#pragma unroll
-        for (int c = 0; c < T::TN; ++c) acc[r][c] = 0.0f;
-
-    int bail = 0;
+    PackedAcc<T, A_KIN> acc;
+    acc.zero();
 #pragma unroll 1
     for (int kt = 0; kt < KT; ++kt) {
-        // every thread is done with the slot consumed in iteration kt-1
-        if (__syncthreads_or(bail)) { bail = 1; break; }
-        if (tid == 0 && issued < KT) { issue(issued); ++issued; }
         const int s = kt % T::STAGES;
-        if (!mbar_wait_bounded(&bars[s], uint32_t(kt / T::STAGES) & 1u)) { bail = 1; continue; }
+        if (!mbar_wait_bounded(&full[s], uint32_t(kt / T::STAGES) & 1u)) {
+            atomicOr(status, 1u);
+            return;
+        }
         const float *As = smem + s * T::STAGE_FLOATS;
         mma_stage<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, abase, bbase, lm, ln, acc);
-    }
-    if (__syncthreads_or(bail)) {
-        if (tid == 0) {
-            atomicOr(status, 1u);
-            // let this CTA's copies still in flight land before it exits
-#pragma unroll 1
-            for (int kt = max(0, issued - T::STAGES); kt < issued; ++kt)
-                mbar_wait_bounded(&bars[kt % T::STAGES], uint32_t(kt / T::STAGES) & 1u);
-        }
-        return;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
     }
     store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
 }
@@ -329,16 +423,16 @@ __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const f
 }
 
 template <class T, bool A_KIN, bool B_KIN>
-__global__ void __launch_bounds__(T::THREADS, 1)
+__global__ void __launch_bounds__(T::THREADS, T::MINB)
 gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__restrict__ B, int64_t ldb,
                     float *__restrict__ C, int64_t M, int64_t N, int64_t K, int64_t ldc,
                     int tiles_m, int tiles_n, int c_vec) {
     extern __shared__ unsigned char smem_raw[];
-    float *smem = aligned_smem_base<T>(smem_raw);
+    float *smem = aligned_smem_base(smem_raw);
 
     const int tid = threadIdx.x;
     int tm, tn;
-    tile_coords(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
     const int KT = int((K + BK - 1) / BK);
 
@@ -358,12 +452,8 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
     const int abase = warp_m * T::WM + (A_KIN ? lm : lm * T::TM);
     const int bbase = warp_n * T::WN + (B_KIN ? ln : ln * 4);
 
-    float acc[T::TM][T::TN];
-#pragma unroll
-    for (int r = 0; r < T::TM; ++r)
-#pragma unroll
-        for (int c = 0; c < T::TN; ++c) acc[r][c] = 0.0f;
-
+    PackedAcc<T, A_KIN> acc;
+    acc.zero();
 #pragma unroll 1
     for (int kt = 0; kt < KT; ++kt) {
         cp_async_wait<T::STAGES - 2>();   // slice kt has landed (this thread's copies)
@@ -419,10 +509,10 @@ int launch_tma(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     const bool okB = B_KIN ? make_map(&mb, p.B, p.K, p.N, p.ldb, BK, T::BN, true)
                            : make_map(&mb, p.B, p.N, p.K, p.ldb, T::BN, BK, false);
     if (!okA || !okB) return REPOPS_ERR_UNSUPPORTED;
-    auto kern = gemm_tma_kernel<T, A_KIN, B_KIN>;
+    auto kern = gemm_tma_ws_kernel<T, A_KIN, B_KIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
-    kern<<<tiles_m * tiles_n, T::THREADS, T::SMEM_BYTES, p.stream>>>(
+    kern<<<tiles_m * tiles_n, T::THREADS + 32, T::SMEM_BYTES, p.stream>>>(
         ma, mb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n, c_vec, p.status);
     return check_launch();
 }
@@ -458,13 +548,14 @@ int launch_config(const GemmProblem &p, int loader) {
     return launch_cpasync<T, false, true>(p, tmi, tni, c_vec);
 }
 
+// Resident CTAs per SM of the TMA kernel (row-major operands) on the current device.
 template <class T>
 int occupancy() {
-    auto kern = gemm_tma_kernel<T, true, false>;
+    auto kern = gemm_tma_ws_kernel<T, true, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::THREADS, T::SMEM_BYTES) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, T::THREADS + 32, T::SMEM_BYTES) != cudaSuccess)
         return 0;
     return n;
 }
