@@ -194,12 +194,16 @@ class Workload:
         if ev: ev[3].record(s)
 
 
-def dist_setup():
+def dist_setup(backend=None):
+    """Rank layout from the torchrun environment; joins the process group
+    (NCCL on GPUs unless `backend` says otherwise) when there is more than one
+    rank.  The group carries only a barrier and a max-reduction of times."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
-        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        torch.distributed.init_process_group(
+            backend or ("nccl" if torch.cuda.is_available() else "gloo"))
     return world, rank, local
 
 
@@ -258,7 +262,7 @@ def cpu_oracle_sample(budget_s=12.0):
 
 
 def run_reference(args):
-    world, rank, _ = dist_setup()
+    world, rank, _ = dist_setup("gloo")   # the oracle runs on host cores only
     if rank != 0:
         return
     import oracle
@@ -474,6 +478,79 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def run_sweep(args):
+    """One JSON line per GEMM workload: the 256^3 case, the square sweep with B
+    row- and column-major, the ragged 4097x1023x3001 case, and the 15 GEMMs of
+    the decoder-layer set.  Each timed launch is bracketed by its own CUDA
+    events and preceded by an L2 flush (a 256 MiB write)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rp.load()
+    peaks, _ = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * FP32_LANES_PER_SM * peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL) * 1e6 / 1e12
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def timed(A, B, C):
+        M, K = A.shape
+        N = B.shape[1]
+        flops = 2.0 * M * N * K
+        reps = max(3, min(50, int(2e11 / max(flops, 1.0))))
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                rp.gemm(A, B, out=C, stream=s)
+            evs = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                rp.gemm(A, B, out=C, stream=s)
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+        return flops, ms
+
+    def emit(name, A, B, extra=None):
+        C = torch.empty((A.shape[0], B.shape[1]), dtype=torch.float32, device=dev)
+        flops, ms = timed(A, B, C)
+        cfg = rp.gemm_auto_config(A.shape[0], B.shape[1], A.shape[1])
+        tf = flops / ms / 1e9
+        rec = {"sweep": name, "M": A.shape[0], "N": B.shape[1], "K": A.shape[1], "ms": ms,
+               "tflops": tf, "frac_of_fp32_peak": tf / peak, "tile_config": cfg}
+        rec.update(extra or {})
+        print(json.dumps(rec), flush=True)
+        return flops, ms
+
+    A = inputs.uniform_pm1((256, 256), 0, dev)
+    B = inputs.uniform_pm1((256, 256), 1, dev)
+    emit("gemm 256^3 U[-1,1)", A, B)
+    for i, n in enumerate(inputs.SQUARE_SWEEP):
+        A = inputs.normal((n, n), 1.0, 10 + i, dev)
+        B = inputs.normal((n, n), 1.0, 20 + i, dev)
+        emit("gemm %d^3 B row-major" % n, A, B)
+        emit("gemm %d^3 B column-major" % n, A, B.t().contiguous().t())
+        del A, B
+    M, N, K = inputs.RAGGED
+    A = inputs.normal((M, K), 1.0, 30, dev)
+    B = inputs.normal((K, N), 1.0, 31, dev)
+    emit("gemm ragged 4097x1023x3001 (cp.async loader)", A, B)
+    T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
+    X = inputs.normal((T, D), 1.0, 100, dev)
+    tot_f = tot_ms = 0.0
+    for li, (name, kin, nout) in enumerate(inputs.DECODER_LAYERS):
+        Xin = X if kin == D else inputs.normal((T, kin), 1.0, 150 + li, dev)
+        W = inputs.normal((kin, nout), 0.02, 110 + li, dev)
+        dY = inputs.normal((T, nout), 1e-3, 120 + li, dev)
+        for kind, a, b in (("forward Y=XW", Xin, W), ("dX=dY W^T", dY, W.t()), ("dW=X^T dY", Xin.t(), dY)):
+            f, ms = emit("decoder %s %s" % (name, kind), a, b)
+            tot_f += f
+            tot_ms += ms
+    print(json.dumps({"sweep": "decoder layer set, 15 GEMMs", "ms": tot_ms, "tflops": tot_f / tot_ms / 1e9,
+                      "frac_of_fp32_peak": tot_f / tot_ms / 1e9 / peak}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,8 +559,12 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every GEMM workload (one JSON line each) instead of the step")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
