@@ -22,6 +22,8 @@ What each function follows (page title, section):
   merkle_*   -- "Zoo Per-LLM Chain Soundness" §1 (batch hash = Merkle root),
                 §6 (bytes32 roots); "Verde与RepOps" §2.3.2 (checkpoint hash is a
                 Merkle tree) and §2.4 (membership proofs).
+  replay     -- "Zoo Per-LLM Chain Soundness" §7 "Reproducibility test plan":
+                replay each block's batch in order, then check H(theta) = m.
 Pins against things other than the oracle itself live in tests/test_oracle_*.py.
 """
 import ctypes
@@ -61,6 +63,15 @@ def lib():
         L.oracle_merkle_reduce.argtypes = [vp, ctypes.c_uint64, vp]
         L.oracle_merkle_root.restype = i32
         L.oracle_merkle_root.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, vp]
+        L.oracle_merkle_total_nodes.restype = ctypes.c_uint64
+        L.oracle_merkle_total_nodes.argtypes = [ctypes.c_uint64]
+        L.oracle_merkle_tree.restype = i32
+        L.oracle_merkle_tree.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, vp]
+        L.oracle_merkle_proof.restype = i32
+        L.oracle_merkle_proof.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, vp]
+        L.oracle_merkle_verify.restype = i32
+        L.oracle_merkle_verify.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, vp,
+                                           i32, vp]
         if L.oracle_fp_env_ok() != 1:
             raise RuntimeError("host floating-point environment flushes subnormals "
                                "or does not round to nearest even; the oracle "
@@ -204,3 +215,51 @@ def merkle_root(data, leaf: int = 4096) -> bytes:
     if rc != 0:
         raise ValueError("empty input or zero leaf size")
     return root.tobytes()
+
+
+def merkle_tree(data, leaf: int = 4096) -> np.ndarray:
+    """(total_nodes, 32) uint8: every level, leaf digests first; last row = root."""
+    L = lib()
+    b = _as_bytes(data)
+    nl = L.oracle_merkle_leaf_count(b.size, leaf)
+    if nl == 0:
+        raise ValueError("empty input or zero leaf size")
+    out = np.zeros((L.oracle_merkle_total_nodes(nl), 32), dtype=np.uint8)
+    L.oracle_merkle_tree(_ptr(b), b.size, leaf, _ptr(out))
+    return out
+
+
+def merkle_proof(tree: np.ndarray, nleaves: int, index: int) -> np.ndarray:
+    """(steps, 32) uint8 siblings of leaf `index`, bottom-up."""
+    L = lib()
+    t = np.ascontiguousarray(tree, dtype=np.uint8)
+    buf = np.zeros((64, 32), dtype=np.uint8)
+    n = L.oracle_merkle_proof(_ptr(t), nleaves, index, _ptr(buf))
+    if n < 0:
+        raise ValueError("leaf index out of range")
+    return buf[:n].copy()
+
+
+def merkle_verify(leaf_bytes, nleaves: int, index: int, proof, root: bytes) -> bool:
+    """Membership of a leaf's bytes at `index` in the tree with this root."""
+    L = lib()
+    lb = _as_bytes(leaf_bytes)
+    pf = np.ascontiguousarray(np.asarray(proof, dtype=np.uint8).reshape(-1, 32))
+    r = np.frombuffer(bytes(root), dtype=np.uint8).copy()
+    rc = L.oracle_merkle_verify(_ptr(lb) if lb.size else None, lb.size, nleaves, index,
+                                _ptr(pf) if pf.size else None, pf.shape[0], _ptr(r))
+    if rc < 0:
+        raise ValueError("leaf index out of range")
+    return rc == 1
+
+
+def replay(grads_per_step, orders, etas, theta, leaf: int = 4096):
+    """theta_t = mean_sgd(theta_{t-1}, G_t) and m_t = root(theta_t) per step.
+
+    Returns (final theta, [m_1, ..., m_T])."""
+    th = np.array(theta, dtype=np.float32, copy=True)
+    roots = []
+    for gs, order, eta in zip(grads_per_step, orders, etas):
+        th = mean_sgd(gs, order, eta, th)
+        roots.append(merkle_root(th, leaf))
+    return th, roots

@@ -419,3 +419,95 @@ int oracle_merkle_root(const uint8_t *data, uint64_t n, uint64_t leaf, uint8_t r
     free(level);
     return rc;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Whole tree, inclusion proofs, verification                                */
+/* [RepOps §2.4: the referee asks for a Merkle membership proof of an input  */
+/*  tensor hash against the checkpoint; §2.3.2 checkpoint hash = Merkle tree] */
+/* ------------------------------------------------------------------------ */
+
+/* Number of nodes of level l for a tree of nl leaves; levels until one node. */
+uint64_t oracle_merkle_total_nodes(uint64_t nl)
+{
+    if (nl == 0) return 0;
+    uint64_t total = 0, count = nl;
+    for (;;) {
+        total += count;
+        if (count == 1) break;
+        count = (count + 1) / 2;
+    }
+    return total;
+}
+
+/* Every level, leaf digests first, each level's nodes in index order, 32
+ * bytes each; the last node written is the root.  Returns 0 or -1. */
+int oracle_merkle_tree(const uint8_t *data, uint64_t n, uint64_t leaf, uint8_t *tree)
+{
+    uint64_t nl = oracle_merkle_leaf_count(n, leaf);
+    if (nl == 0) return -1;
+    oracle_merkle_leaves(data, n, leaf, tree);
+    uint64_t off = 0, count = nl;
+    while (count > 1) {
+        uint8_t *cur = tree + 32 * off;
+        uint8_t *nxt = cur + 32 * count;
+        uint64_t k = 0;
+        for (uint64_t j = 0; j + 1 < count; j += 2) merkle_node(cur + 32 * j, cur + 32 * (j + 1), nxt + 32 * k++);
+        if (count % 2 == 1) memcpy(nxt + 32 * k++, cur + 32 * (count - 1), 32);
+        off += count;
+        count = k;
+    }
+    return 0;
+}
+
+/* Siblings of leaf `index`, bottom-up, one per level where the node on the
+ * path has a sibling (an unpaired node rises without one).  Writes them to
+ * `proof` (32 bytes each) and returns their number, or -1 for a bad index. */
+int oracle_merkle_proof(const uint8_t *tree, uint64_t nl, uint64_t index, uint8_t *proof)
+{
+    if (nl == 0 || index >= nl) return -1;
+    uint64_t off = 0, count = nl, j = index;
+    int steps = 0;
+    while (count > 1) {
+        uint64_t sib;
+        int has = 1;
+        if (j % 2 == 1) sib = j - 1;
+        else if (j + 1 < count) sib = j + 1;
+        else { has = 0; sib = 0; }
+        if (has) memcpy(proof + 32 * steps++, tree + 32 * (off + sib), 32);
+        off += count;
+        count = (count + 1) / 2;
+        j /= 2;
+    }
+    return steps;
+}
+
+/* Recomputes the root from the leaf's bytes, its position and the siblings,
+ * and compares it with `root`.  Returns 1 (member), 0 (not), -1 (bad args). */
+int oracle_merkle_verify(const uint8_t *leaf_bytes, uint64_t leaf_len, uint64_t nl, uint64_t index,
+                         const uint8_t *proof, int steps, const uint8_t root[32])
+{
+    if (nl == 0 || index >= nl) return -1;
+    uint8_t h[32], t[32];
+    uint8_t prefix = 0x00;
+    osha_ctx c;
+    osha_init(&c);
+    osha_update(&c, &prefix, 1);
+    osha_update(&c, leaf_bytes, leaf_len);
+    osha_final(&c, h);
+    uint64_t count = nl, j = index;
+    int used = 0;
+    while (count > 1) {
+        if (j % 2 == 1) {
+            if (used >= steps) return 0;
+            merkle_node(proof + 32 * used++, h, t);
+            memcpy(h, t, 32);
+        } else if (j + 1 < count) {
+            if (used >= steps) return 0;
+            merkle_node(h, proof + 32 * used++, t);
+            memcpy(h, t, 32);
+        }
+        count = (count + 1) / 2;
+        j /= 2;
+    }
+    return used == steps && memcmp(h, root, 32) == 0;
+}
