@@ -549,6 +549,63 @@ def run_sweep(args):
             tot_ms += ms
     print(json.dumps({"sweep": "decoder layer set, 15 GEMMs", "ms": tot_ms, "tflops": tot_f / tot_ms / 1e9,
                       "frac_of_fp32_peak": tot_f / tot_ms / 1e9 / peak}), flush=True)
+    del X, Xin, W, dY
+    run_sweep_commitments(dev, s, flush)
+
+
+def run_sweep_commitments(dev, s, flush):
+    """Merkle root versus whole stored tree of the 4 GiB tensor, one inclusion
+    proof and one membership check, and replayed blocks of the 16 x 2^28
+    workload (mean + SGD, then the root of theta)."""
+    def ev_time(fn, reps):
+        with torch.cuda.stream(s):
+            fn()
+            evs = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                fn()
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+    T = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300, dev)
+    nb = T.numel() * 4
+    ws = torch.empty(rp.merkle_workspace_bytes(nb), dtype=torch.uint8, device=dev)
+    root = torch.empty(32, dtype=torch.uint8, device=dev)
+    tree = torch.empty((rp.load().repops_merkle_tree_bytes(nb, 4096) // 32, 32), dtype=torch.uint8, device=dev)
+    ms = ev_time(lambda: rp.merkle_sha256(T, 4096, out=root, workspace=ws, stream=s), 5)
+    print(json.dumps({"sweep": "merkle root 4 GiB", "ms": ms, "gbs": nb / ms / 1e6}), flush=True)
+    ms = ev_time(lambda: rp.merkle_tree(T, 4096, tree=tree, root=root, stream=s), 5)
+    print(json.dumps({"sweep": "merkle whole tree 4 GiB (2^21 - 1 nodes stored)", "ms": ms,
+                      "gbs": nb / ms / 1e6}), flush=True)
+    nleaves = nb // 4096
+    idx = nleaves - 12345
+    with torch.cuda.stream(s):
+        proof = rp.merkle_proof(tree, nleaves, idx, stream=s)
+    ms = ev_time(lambda: rp.merkle_proof(tree, nleaves, idx, stream=s), 20)
+    leaf = T.view(torch.uint8)[idx * 4096:(idx + 1) * 4096]
+    ms_v = ev_time(lambda: rp.merkle_verify(leaf, nleaves, idx, proof, root, stream=s), 20)
+    with torch.cuda.stream(s):
+        okt = rp.merkle_verify(leaf, nleaves, idx, proof, root, stream=s)
+    torch.cuda.synchronize(dev)
+    ok = int(okt.item())
+    print(json.dumps({"sweep": "inclusion proof (20 siblings) and membership check", "proof_us": ms * 1e3,
+                      "verify_us": ms_v * 1e3, "verified": ok}), flush=True)
+    del T, tree, ws
+    nC, ln = inputs.MEAN_CONTRIBUTORS, inputs.MEAN_LEN
+    grads = [inputs.normal((ln,), 1e-2, 200 + r, dev) for r in range(nC)]
+    theta = inputs.normal((ln,), 0.02, 199, dev)
+    order = rp.sort_ids(inputs.contributor_ids(nC, 200))
+    blocks = 3
+    roots = torch.empty((blocks, 32), dtype=torch.uint8, device=dev)
+    ms = ev_time(lambda: rp.replay([grads] * blocks, [order] * blocks, [1e-3] * blocks, theta, 4096,
+                                   roots=roots, stream=s), 3) / blocks
+    per_block = (nC + 2) * ln * 4 + ln * 4
+    print(json.dumps({"sweep": "replay, per block: mean+SGD of 16 x 2^28 then root of theta (1 GiB)",
+                      "ms_per_block": ms, "gbs": per_block / ms / 1e6}), flush=True)
 
 
 def main():

@@ -230,6 +230,71 @@ int repops_merkle_sha256_ws(const void *ptr, uint64_t bytes, uint32_t leaf,
                             uint8_t *root_out, void *workspace,
                             uint64_t workspace_bytes, cudaStream_t stream);
 
+/* ------------------------------------------------------------------------ */
+/* Whole tree and inclusion proofs                                           */
+/* "Verde与RepOps" §2.4 (the referee asks for a Merkle membership proof of an */
+/* input tensor hash against the checkpoint); §2.3.2 (checkpoint hashes are  */
+/* Merkle trees)                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of the stored tree of repops_merkle_tree_sha256: 32 per node over all
+ * levels (0 if the input is invalid). */
+uint64_t repops_merkle_tree_bytes(uint64_t bytes, uint32_t leaf);
+
+/* As repops_merkle_sha256, and also stores every node of the tree in `tree`
+ * (device, tree_bytes >= repops_merkle_tree_bytes(bytes, leaf), 16-byte
+ * aligned): level 0 (the leaf digests) first, then level 1, ..., the root
+ * last; within a level, nodes in index order; each node as its 32-byte digest.
+ * A level's unpaired last node appears again as the last node of the next
+ * level.  Errors as repops_merkle_sha256, plus INVALID_ARG for a short or
+ * misaligned tree buffer and ALIAS if it overlaps the input or root_out. */
+int repops_merkle_tree_sha256(const void *ptr, uint64_t bytes, uint32_t leaf,
+                              uint8_t *tree, uint64_t tree_bytes,
+                              uint8_t *root_out, cudaStream_t stream);
+
+/* Host-only.  Number of sibling digests in the inclusion proof of leaf
+ * `index` in a tree of `nleaves` leaves (levels where the path's node is
+ * unpaired contribute none), or INVALID_ARG for index >= nleaves. */
+int repops_merkle_proof_steps(uint64_t nleaves, uint64_t index);
+
+/* Inclusion proof of leaf `index`: the sibling digests on its path to the
+ * root, bottom-up, 32 bytes each, gathered from a tree stored by
+ * repops_merkle_tree_sha256 (device) into proof_out (device,
+ * 32 * repops_merkle_proof_steps(nleaves, index) bytes).  Asynchronous.
+ * INVALID_ARG for null pointers or index >= nleaves; ALIAS if proof_out
+ * overlaps the tree. */
+int repops_merkle_proof(const uint8_t *tree, uint64_t nleaves, uint64_t index,
+                        uint8_t *proof_out, cudaStream_t stream);
+
+/* Membership check: hashes the leaf's bytes (leaf_bytes, device, leaf_len
+ * bytes) as SHA256(0x00 || bytes), climbs with the proof's siblings (device)
+ * -- on the left when the path's node index is odd, on the right when it is
+ * even and has a right neighbour, none when it is unpaired -- and writes 1 to
+ * *ok_out (device int) if the result equals root (device, 32 bytes), else 0.
+ * Asynchronous.  INVALID_ARG for null pointers or index >= nleaves. */
+int repops_merkle_verify(const void *leaf_bytes, uint64_t leaf_len, uint64_t nleaves,
+                         uint64_t index, const uint8_t *proof, const uint8_t *root,
+                         int *ok_out, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Step replay                                                               */
+/* "Zoo Per-LLM Chain Soundness" §7 "Reproducibility test plan": replay the  */
+/* blocks in order from the genesis state, then verify H(theta) = m          */
+/* ------------------------------------------------------------------------ */
+
+/* For t = 0 .. steps-1, on `stream`:
+ *   repops_fixed_order_mean_sgd(nC, len, ptrs + t*nC, orders + t*nC, etas[t], theta)
+ *   roots_out[32*t .. 32*t+31] = Merkle root of theta's len*4 bytes (leaf bytes)
+ * ptrs (host, steps*nC device pointers, step-major), orders (host, steps*nC
+ * ints, each step's row a permutation), etas (host, steps floats), theta
+ * (device, updated in place), roots_out (device, 32*steps bytes).  Every step
+ * is validated before the first launch (ORDER, ALIAS, INVALID_ARG as the two
+ * calls it makes).  Merkle scratch comes from cudaMallocAsync on `stream`. */
+int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len,
+                                  const float *const *ptrs, const int *orders,
+                                  const float *etas, float *theta, uint32_t leaf,
+                                  uint8_t *roots_out, cudaStream_t stream);
+
 /* Size of the fixed device scratch behind repops_merkle_sha256_noalloc. */
 #define REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

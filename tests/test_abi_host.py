@@ -166,3 +166,31 @@ def test_product_path_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, re.M), f
                 assert "repops_oracle" not in text and "liboracle" not in text, f
+
+
+def test_proof_shape_and_tree_size_match_oracle(L, orc):
+    import numpy as np
+    for nl in (1, 2, 3, 5, 8, 13, 128, 129, 1000):
+        data = np.zeros(nl * 64, np.uint8)
+        tree = orc.merkle_tree(data, 64)
+        assert L.repops_merkle_tree_bytes(nl * 64, 64) == 32 * tree.shape[0]
+        for i in sorted({0, nl // 2, nl - 1}):
+            assert L.repops_merkle_proof_steps(nl, i) == orc.merkle_proof(tree, nl, i).shape[0]
+    assert L.repops_merkle_proof_steps(5, 5) == -1
+    assert L.repops_merkle_proof_steps(0, 0) == -1
+
+
+def test_replay_validates_every_block_before_launching(L):
+    steps, nC, n = 3, 2, 1024
+    P = (ctypes.c_void_p * (steps * nC))(*[FAKE_A + 0x100000 * i for i in range(steps * nC)])
+    E = (ctypes.c_float * steps)(1e-3, 1e-3, 1e-3)
+
+    def call(orders, theta=FAKE_C, roots=FAKE_B):
+        O = (ctypes.c_int * (steps * nC))(*orders)
+        return L.repops_replay_mean_sgd_commit(steps, nC, n, ctypes.cast(P, ctypes.c_void_p),
+                                               ctypes.cast(O, ctypes.c_void_p),
+                                               ctypes.cast(E, ctypes.c_void_p), theta, 4096, roots, None)
+    assert call([0, 1, 1, 0, 0, 0]) == -3            # the last block repeats a contributor
+    assert call([0, 1, 1, 0, 0, 1], theta=FAKE_A + 0x100000 * 5 + 64) == -2
+    assert call([0, 1, 1, 0, 0, 1], roots=FAKE_C + 16) == -2
+    assert L.repops_replay_mean_sgd_commit(0, nC, n, P, None, E, FAKE_C, 4096, FAKE_B, None) == -1

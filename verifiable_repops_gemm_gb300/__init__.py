@@ -13,6 +13,10 @@ memory and streams.
   merkle_sha256(t, leaf)            SHA-256 Merkle root of a tensor's bytes
                                     ("Zoo Per-LLM Chain Soundness" §1, §6, §7;
                                      "Verde与RepOps" §2.3.2)
+  merkle_tree / merkle_proof /      whole tree, inclusion proofs, membership check
+  merkle_verify                     ("Verde与RepOps" §2.4)
+  replay(...)                       mean + SGD + commit per block, in order
+                                    ("Zoo Per-LLM Chain Soundness" §7)
 """
 import ctypes
 
@@ -22,10 +26,14 @@ from ._capi import (LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA, MEAN_MAX_CONTRIBUTO
 
 __all__ = ["load", "version", "gemm", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
-           "merkle_workspace_bytes", "device_status", "RepopsError",
+           "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
+           "device_status", "RepopsError",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
 
 
+# Outputs the functions below allocate come from torch's caching allocator on
+# the current stream; a caller passing another `stream` must keep them alive
+# (or record them on that stream) until that stream has finished with them.
 def _stream_handle(stream):
     import torch
     if stream is None:
@@ -175,3 +183,77 @@ def device_status(stream=None) -> int:
     rc = load().repops_device_status(_stream_handle(stream), ctypes.byref(v))
     _capi.check(rc, "repops_device_status")
     return v.value
+
+
+def merkle_tree(t, leaf: int = 4096, *, nbytes: int = None, tree=None, root=None, stream=None):
+    """(tree, root): every node of the Merkle tree of t's bytes (uint8 CUDA
+    tensor of shape (nodes, 32), leaf digests first, root last) and the root."""
+    import torch
+    L = load()
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("t must be a contiguous CUDA tensor")
+    n = t.numel() * t.element_size() if nbytes is None else int(nbytes)
+    need = L.repops_merkle_tree_bytes(n, leaf)
+    if need == 0:
+        raise ValueError("empty input or bad leaf size")
+    if tree is None:
+        tree = torch.empty((need // 32, 32), dtype=torch.uint8, device=t.device)
+    if root is None:
+        root = torch.empty(32, dtype=torch.uint8, device=t.device)
+    rc = L.repops_merkle_tree_sha256(t.data_ptr(), n, leaf, tree.data_ptr(),
+                                     tree.numel() * tree.element_size(), root.data_ptr(),
+                                     _stream_handle(stream))
+    _capi.check(rc, "repops_merkle_tree_sha256")
+    return tree, root
+
+
+def merkle_proof(tree, nleaves: int, index: int, *, stream=None):
+    """(steps, 32) uint8 CUDA tensor: siblings of leaf `index`, bottom-up."""
+    import torch
+    L = load()
+    steps = L.repops_merkle_proof_steps(nleaves, index)
+    if steps < 0:
+        raise RepopsError(steps, "repops_merkle_proof_steps")
+    out = torch.empty((max(steps, 1), 32), dtype=torch.uint8, device=tree.device)
+    rc = L.repops_merkle_proof(tree.data_ptr(), nleaves, index, out.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_merkle_proof")
+    return out[:steps]
+
+
+def merkle_verify(leaf_bytes, nleaves: int, index: int, proof, root, *, stream=None):
+    """int32 CUDA tensor: 1 if leaf_bytes (a CUDA tensor's bytes) is leaf
+    `index` of the tree with this root, else 0."""
+    import torch
+    L = load()
+    ok = torch.empty(1, dtype=torch.int32, device=root.device)   # the kernel always writes it
+    nb = leaf_bytes.numel() * leaf_bytes.element_size()
+    rc = L.repops_merkle_verify(leaf_bytes.data_ptr() if nb else None, nb, nleaves, index,
+                                proof.data_ptr() if proof.numel() else None, root.data_ptr(),
+                                ok.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_merkle_verify")
+    return ok
+
+
+def replay(grads_per_step, orders, etas, theta, leaf: int = 4096, *, roots=None, stream=None):
+    """Replays blocks in order: theta -= eta_t * mean_t (fixed order), then
+    commits theta; returns the (steps, 32) uint8 CUDA tensor of roots."""
+    import torch
+    L = load()
+    steps = len(grads_per_step)
+    nC = len(grads_per_step[0]) if steps else 0
+    flat_p, flat_o = [], []
+    for gs, order in zip(grads_per_step, orders):
+        if len(gs) != nC or len(order) != nC:
+            raise ValueError("every block needs the same number of contributors")
+        flat_p += [g if isinstance(g, int) else g.data_ptr() for g in gs]
+        flat_o += [int(x) for x in order]
+    parr = (ctypes.c_void_p * max(len(flat_p), 1))(*flat_p)
+    oarr = (ctypes.c_int * max(len(flat_o), 1))(*flat_o)
+    earr = (ctypes.c_float * max(steps, 1))(*[float(e) for e in etas])
+    if roots is None:
+        roots = torch.empty((steps, 32), dtype=torch.uint8, device=theta.device)
+    rc = L.repops_replay_mean_sgd_commit(steps, nC, theta.numel(), ctypes.cast(parr, ctypes.c_void_p),
+                                         ctypes.cast(oarr, ctypes.c_void_p), ctypes.cast(earr, ctypes.c_void_p),
+                                         theta.data_ptr(), leaf, roots.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_replay_mean_sgd_commit")
+    return roots

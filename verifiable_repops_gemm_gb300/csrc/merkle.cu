@@ -29,7 +29,10 @@ namespace repops {
 namespace {
 
 constexpr int LEAF_CTA = 128;   // leaves per CTA in the leaf kernel (power of two)
+constexpr int LOG_LEAF_CTA = 7;
 constexpr int RED_CTA = 256;    // threads per CTA in the reduce kernel
+constexpr int LOG_RED_NODES = 9;   // a reduce CTA folds 2 * RED_CTA = 2^9 nodes
+static_assert((1 << LOG_LEAF_CTA) == LEAF_CTA && (1 << LOG_RED_NODES) == 2 * RED_CTA, "fold depths");
 
 // FIPS 180-4 §4.2.2: first 32 bits of the fractional parts of the cube roots
 // of the first 64 primes.
@@ -216,12 +219,44 @@ __device__ __forceinline__ void store_root(uint8_t *root, const uint32_t (&st)[8
     }
 }
 
+// Optional sink for every node of the tree: level l's nodes are stored in
+// index order after all nodes of the levels below it, each as its 32-byte
+// digest (big-endian words).  tree == nullptr: nothing is stored.
+struct TreeOut {
+    uint8_t *tree;
+    uint64_t nleaves;
+};
+
+// Highest level of a tree of n leaves (the root's level).
+__host__ __device__ __forceinline__ int top_level(uint64_t n) {
+    int l = 0;
+    while (n > 1) { n = (n + 1) / 2; ++l; }
+    return l;
+}
+
+// Node offset of `level` in the stored tree.
+__device__ __forceinline__ uint64_t level_offset(uint64_t n, int level) {
+    uint64_t off = 0;
+    for (int l = 0; l < level; ++l) { off += n; n = (n + 1) / 2; }
+    return off;
+}
+
+__device__ __forceinline__ void store_node(const TreeOut &to, int level, uint64_t idx, const uint32_t (&st)[8]) {
+    uint4 *dst = reinterpret_cast<uint4 *>(to.tree + 32 * (level_offset(to.nleaves, level) + idx));
+    dst[0] = make_uint4(__byte_perm(st[0], 0, 0x0123), __byte_perm(st[1], 0, 0x0123),
+                        __byte_perm(st[2], 0, 0x0123), __byte_perm(st[3], 0, 0x0123));
+    dst[1] = make_uint4(__byte_perm(st[4], 0, 0x0123), __byte_perm(st[5], 0, 0x0123),
+                        __byte_perm(st[6], 0, 0x0123), __byte_perm(st[7], 0, 0x0123));
+}
+
 // Folds `cnt` digests held word-major in buf[0] ([8][N]) down to buf[?][.][0]
 // level by level; returns the buffer index holding the result.  Every thread
 // of the CTA must call it (it synchronises).
 template <int N>
-__device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const PipeConst &pc) {
+__device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const PipeConst &pc,
+                                        const TreeOut &to, int level_in, uint64_t base, int fold_levels) {
     int cur = 0;
+    int k = 0;   // levels folded so far
     while (cnt > 1) {   // uniform across the CTA
         __syncthreads();
         const int pairs = cnt / 2;
@@ -238,18 +273,31 @@ __device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const Pi
             }
 #pragma unroll
             for (int w = 0; w < 8; ++w) buf[cur ^ 1][w][j] = o[w];
+            if (to.tree) store_node(to, level_in + k + 1, (base >> (k + 1)) + j, o);
         }
         cur ^= 1;
         cnt = (cnt + 1) / 2;
+        ++k;
     }
     __syncthreads();
+    // a short block reached one node early: it is promoted through the levels
+    // this CTA would still have folded, up to the tree's top
+    if (to.tree && threadIdx.x == 0) {
+        const int last = min(fold_levels, top_level(to.nleaves) - level_in);
+        if (k < last) {
+            uint32_t o[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) o[w] = buf[cur][w][0];
+            for (int kk = k + 1; kk <= last; ++kk) store_node(to, level_in + kk, base >> kk, o);
+        }
+    }
     return cur;
 }
 
 __global__ void __launch_bounds__(LEAF_CTA)
 merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t leaf, uint64_t nleaves,
                     int fast_ok, uint32_t *__restrict__ level_out, uint8_t *__restrict__ root_out,
-                    const PipeConst pc) {
+                    const PipeConst pc, const TreeOut to) {
     __shared__ uint32_t buf[2][8][LEAF_CTA];
     const uint64_t base = uint64_t(blockIdx.x) * LEAF_CTA;
     const uint64_t i = base + threadIdx.x;
@@ -261,9 +309,10 @@ merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t l
         else leaf_digest_generic(data + start, len, st, pc);
 #pragma unroll
         for (int w = 0; w < 8; ++w) buf[0][w][threadIdx.x] = st[w];
+        if (to.tree) store_node(to, 0, i, st);
     }
     const int cnt = int(min(uint64_t(LEAF_CTA), nleaves - base));
-    const int cur = cta_fold<LEAF_CTA>(buf, cnt, pc);
+    const int cur = cta_fold<LEAF_CTA>(buf, cnt, pc, to, 0, base, LOG_LEAF_CTA);
     if (threadIdx.x == 0) {
         uint32_t st[8];
 #pragma unroll
@@ -279,7 +328,7 @@ merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t l
 
 __global__ void __launch_bounds__(RED_CTA)
 merkle_reduce(const uint32_t *__restrict__ in, uint64_t n, uint32_t *__restrict__ out,
-              uint8_t *__restrict__ root_out, const PipeConst pc) {
+              uint8_t *__restrict__ root_out, const PipeConst pc, const TreeOut to, int level_in) {
     __shared__ uint32_t buf[2][8][2 * RED_CTA];
     const uint64_t base = uint64_t(blockIdx.x) * 2 * RED_CTA;
     const int cnt = int(min(uint64_t(2 * RED_CTA), n - base));
@@ -289,7 +338,7 @@ merkle_reduce(const uint32_t *__restrict__ in, uint64_t n, uint32_t *__restrict_
         buf[0][0][j] = lo.x; buf[0][1][j] = lo.y; buf[0][2][j] = lo.z; buf[0][3][j] = lo.w;
         buf[0][4][j] = hi.x; buf[0][5][j] = hi.y; buf[0][6][j] = hi.z; buf[0][7][j] = hi.w;
     }
-    const int cur = cta_fold<2 * RED_CTA>(buf, cnt, pc);
+    const int cur = cta_fold<2 * RED_CTA>(buf, cnt, pc, to, level_in, base, LOG_RED_NODES);
     if (threadIdx.x == 0) {
         uint32_t st[8];
 #pragma unroll
@@ -321,25 +370,27 @@ bool plan_for(uint64_t bytes, uint32_t leaf, Plan *p) {
 }
 
 int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void *ws, const Plan &pl,
-        cudaStream_t stream) {
+        cudaStream_t stream, const TreeOut to = TreeOut{nullptr, 0}) {
     const uint8_t *data = static_cast<const uint8_t *>(ptr);
     const int fast_ok = reinterpret_cast<uintptr_t>(data) % 16 == 0;
     const PipeConst pc{1u, 1u << 29, 1u << 22};
     uint32_t *bufA = static_cast<uint32_t *>(ws);
     uint32_t *bufB = bufA ? bufA + 8 * pl.n1 : nullptr;
     merkle_leaf_subtree<<<unsigned(pl.n1), LEAF_CTA, 0, stream>>>(
-        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr, pc);
+        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr, pc, to);
     int rc = check_launch();
     if (rc != REPOPS_OK) return rc;
     uint64_t n = pl.n1;
+    int level = LOG_LEAF_CTA;
     uint32_t *src = bufA, *dst = bufB;
     while (n > 1) {
         const uint64_t blocks = (n + 2 * RED_CTA - 1) / (2 * RED_CTA);
         merkle_reduce<<<unsigned(blocks), RED_CTA, 0, stream>>>(src, n, dst, blocks == 1 ? root_out : nullptr,
-                                                                pc);
+                                                                pc, to, level);
         rc = check_launch();
         if (rc != REPOPS_OK) return rc;
         n = blocks;
+        level += LOG_RED_NODES;
         std::swap(src, dst);
     }
     return REPOPS_OK;
@@ -396,6 +447,160 @@ extern "C" int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t le
         if (e != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
     }
     return rc;
+}
+
+// ---------------------------------------------------------------------------
+// Whole tree, inclusion proofs, verification ("Verde与RepOps" §2.4: the
+// referee asks for a Merkle membership proof of an input tensor hash against
+// the checkpoint).  A proof is the list of sibling digests on the path from a
+// leaf to the root, bottom-up, one per level where the path's node has a
+// sibling; its shape follows from (leaf count, leaf index) alone.
+// ---------------------------------------------------------------------------
+
+namespace repops {
+namespace {
+
+__host__ __device__ __forceinline__ int path_steps(uint64_t nleaves, uint64_t index) {
+    int steps = 0;
+    uint64_t count = nleaves, j = index;
+    while (count > 1) {
+        if ((j & 1) || j + 1 < count) ++steps;
+        count = (count + 1) / 2;
+        j >>= 1;
+    }
+    return steps;
+}
+
+__device__ __forceinline__ void load_digest(const uint8_t *p, uint32_t (&w)[8]) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = (uint32_t(p[4 * i]) << 24) | (uint32_t(p[4 * i + 1]) << 16) | (uint32_t(p[4 * i + 2]) << 8) |
+               uint32_t(p[4 * i + 3]);
+}
+
+// One thread gathers the siblings of leaf `index` from the stored tree.
+__global__ void merkle_proof_kernel(const uint8_t *__restrict__ tree, uint64_t nleaves, uint64_t index,
+                                    uint8_t *__restrict__ proof) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    uint64_t off = 0, count = nleaves, j = index;
+    int s = 0;
+    while (count > 1) {
+        uint64_t sib = 0;
+        bool has = true;
+        if (j & 1) sib = j - 1;
+        else if (j + 1 < count) sib = j + 1;
+        else has = false;
+        if (has) {
+            const uint8_t *src = tree + 32 * (off + sib);
+            for (int b = 0; b < 32; ++b) proof[32 * s + b] = src[b];
+            ++s;
+        }
+        off += count;
+        count = (count + 1) / 2;
+        j >>= 1;
+    }
+}
+
+// One thread hashes the leaf bytes, climbs with the siblings and compares the
+// result with the root: *ok = 1 (member) or 0.
+__global__ void merkle_verify_kernel(const uint8_t *__restrict__ leaf_bytes, uint64_t leaf_len,
+                                     uint64_t nleaves, uint64_t index, const uint8_t *__restrict__ proof,
+                                     const uint8_t *__restrict__ root, int *__restrict__ ok,
+                                     const PipeConst pc) {
+    if (blockIdx.x != 0 || threadIdx.x != 0) return;
+    uint32_t h[8];
+    leaf_digest_generic(leaf_bytes, leaf_len, h, pc);
+    uint64_t count = nleaves, j = index;
+    int s = 0;
+    while (count > 1) {
+        const bool left_sib = (j & 1) != 0, right_sib = !(j & 1) && j + 1 < count;
+        if (left_sib || right_sib) {
+            uint32_t sib[8], o[8];
+            load_digest(proof + 32 * s, sib);
+            ++s;
+            if (left_sib) node_digest(sib, h, o, pc);
+            else node_digest(h, sib, o, pc);
+#pragma unroll
+            for (int w = 0; w < 8; ++w) h[w] = o[w];
+        }
+        count = (count + 1) / 2;
+        j >>= 1;
+    }
+    uint32_t r[8];
+    load_digest(root, r);
+    bool same = true;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) same = same && (r[w] == h[w]);
+    *ok = same ? 1 : 0;
+}
+
+uint64_t total_nodes(uint64_t nleaves) {
+    uint64_t t = 0, c = nleaves;
+    for (;;) {
+        t += c;
+        if (c == 1) break;
+        c = (c + 1) / 2;
+    }
+    return t;
+}
+
+}  // namespace
+}  // namespace repops
+
+extern "C" uint64_t repops_merkle_tree_bytes(uint64_t bytes, uint32_t leaf) {
+    Plan pl;
+    if (!plan_for(bytes, leaf, &pl)) return 0;
+    return 32 * total_nodes(pl.nleaves);
+}
+
+extern "C" int repops_merkle_tree_sha256(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *tree,
+                                         uint64_t tree_bytes, uint8_t *root_out, cudaStream_t stream) {
+    Plan pl;
+    int rc = check_args(ptr, bytes, leaf, root_out, &pl);
+    if (rc != REPOPS_OK) return rc;
+    const uint64_t need = 32 * total_nodes(pl.nleaves);
+    if (!tree || tree_bytes < need || reinterpret_cast<uintptr_t>(tree) % 16) return REPOPS_ERR_INVALID_ARG;
+    if (ranges_overlap(tree, need, ptr, bytes) || ranges_overlap(tree, need, root_out, 32)) return REPOPS_ERR_ALIAS;
+    void *ws = nullptr;
+    if (pl.ws_bytes > 0) {
+        cudaError_t e = cudaMallocAsync(&ws, pl.ws_bytes, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return REPOPS_ERR_ALLOC;
+        }
+    }
+    rc = run(ptr, bytes, leaf, root_out, ws, pl, stream, TreeOut{tree, pl.nleaves});
+    if (ws) {
+        cudaError_t e = cudaFreeAsync(ws, stream);
+        if (e != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
+    }
+    return rc;
+}
+
+extern "C" int repops_merkle_proof_steps(uint64_t nleaves, uint64_t index) {
+    if (nleaves == 0 || index >= nleaves) return REPOPS_ERR_INVALID_ARG;
+    return path_steps(nleaves, index);
+}
+
+extern "C" int repops_merkle_proof(const uint8_t *tree, uint64_t nleaves, uint64_t index, uint8_t *proof_out,
+                                   cudaStream_t stream) {
+    if (!tree || !proof_out || nleaves == 0 || index >= nleaves) return REPOPS_ERR_INVALID_ARG;
+    const uint64_t tree_bytes = 32 * total_nodes(nleaves);
+    if (ranges_overlap(tree, tree_bytes, proof_out, 32u * uint64_t(path_steps(nleaves, index))))
+        return REPOPS_ERR_ALIAS;
+    merkle_proof_kernel<<<1, 32, 0, stream>>>(tree, nleaves, index, proof_out);
+    return check_launch();
+}
+
+extern "C" int repops_merkle_verify(const void *leaf_bytes, uint64_t leaf_len, uint64_t nleaves, uint64_t index,
+                                    const uint8_t *proof, const uint8_t *root, int *ok_out, cudaStream_t stream) {
+    if ((!leaf_bytes && leaf_len) || !root || !ok_out || nleaves == 0 || index >= nleaves)
+        return REPOPS_ERR_INVALID_ARG;
+    if (!proof && path_steps(nleaves, index) > 0) return REPOPS_ERR_INVALID_ARG;
+    const PipeConst pc{1u, 1u << 29, 1u << 22};
+    merkle_verify_kernel<<<1, 32, 0, stream>>>(static_cast<const uint8_t *>(leaf_bytes), leaf_len, nleaves, index,
+                                               proof, root, ok_out, pc);
+    return check_launch();
 }
 
 // ---------------------------------------------------------------------------
