@@ -535,7 +535,7 @@ def run_sweep(args):
     M, N, K = inputs.RAGGED
     A = inputs.normal((M, K), 1.0, 30, dev)
     B = inputs.normal((K, N), 1.0, 31, dev)
-    emit("gemm ragged 4097x1023x3001 (cp.async loader)", A, B)
+    emit("gemm ragged 4097x1023x3001 (lda = 3001: operands repacked to a 16-byte pitch)", A, B)
     T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
     X = inputs.normal((T, D), 1.0, 100, dev)
     tot_f = tot_ms = 0.0

@@ -99,8 +99,12 @@ int repops_device_status(cudaStream_t stream, int *status_out);
  * Errors: INVALID_ARG (negative size, bad leading dim, null pointer with a
  * non-empty operand, element offsets that overflow int64); ALIAS (C's span
  * overlaps A's or B's span); CUDA (launch failure).
- * Pointers need no alignment: unaligned operands take a 4-byte copy path that
- * computes the same bits. */
+ * Pointers need no alignment.  An operand TMA cannot describe (base not
+ * 16-byte aligned, or leading dimension not a multiple of 4) is, for problems
+ * of at least 4 GFLOP (2*M*N*K), first copied with a 16-byte pitch into
+ * scratch taken with cudaMallocAsync on `stream` (and released the same way);
+ * smaller problems, or a refused allocation, read it with 4-byte copies.  The
+ * bits are the same on every path. */
 int repops_gemm_f32(int64_t M, int64_t N, int64_t K,
                     const float *A, int64_t lda,
                     const float *B, int64_t ldb,

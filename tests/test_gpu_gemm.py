@@ -216,3 +216,20 @@ def test_gemm_decoder_layer_set(rp, orc):
         # transposed views give the bytes of materialised transposes
         assert torch.equal(dX.view(torch.int32), run(rp, dY, W.t().contiguous()).view(torch.int32))
         assert torch.equal(dW.view(torch.int32), run(rp, Xin.t().contiguous(), dY).view(torch.int32))
+
+
+def test_gemm_repacked_operands_match_every_loader(rp, orc):
+    # 2*1601^3 = 8.2 GFLOP with lda = ldb = 1601: the automatic path copies both
+    # operands to a 16-byte pitch and runs the TMA kernels
+    n = 1601
+    A = inputs.normal((n, n), 1.0, 41, DEV)
+    B = inputs.normal((n, n), 1.0, 42, DEV)
+    C_auto = run(rp, A, B)
+    C_cp = run(rp, A, B, config=rp.gemm_auto_config(n, n, n), loader=rp.LOADER_CPASYNC)
+    assert torch.equal(C_auto.view(torch.int32), C_cp.view(torch.int32))
+    rows = torch.tensor([0, 777, n - 1])
+    cols = torch.tensor([0, 5, 1000, n - 2, n - 1])
+    sampled_check(orc, A, B, C_auto, rows, cols)
+    # transposed storage of both operands (ld = 1601 again)
+    C_t = run(rp, A.t().contiguous().t(), B.t().contiguous().t())
+    assert torch.equal(C_auto.view(torch.int32), C_t.view(torch.int32))

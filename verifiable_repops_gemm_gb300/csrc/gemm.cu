@@ -113,6 +113,37 @@ __global__ void fill_positive_zero(float *C, int64_t M, int64_t N, int64_t ldc) 
     }
 }
 
+// Copies a rows x cols row-major block from pitch ld_src to pitch ld_dst
+// (elements).  A pure copy: the GEMM reads the same values in the same order.
+__global__ void repack_rows(const float *__restrict__ src, int64_t ld_src, float *__restrict__ dst,
+                            int64_t ld_dst, int64_t rows, int64_t cols) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+        const float *s = src + r * ld_src;
+        float *d = dst + r * ld_dst;
+        for (int64_t c = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; c < cols;
+             c += int64_t(gridDim.x) * blockDim.x)
+            d[c] = s[c];
+    }
+}
+
+// Work (2*M*N*K) from which repacking TMA-incompatible operands pays off: the
+// copy streams each operand once (~10-20 us for the ragged 4097x1023x3001
+// workload) and lets the TMA kernels run instead of the 4-byte loader.
+constexpr double kRepackMinFlops = 4.0e9;
+
+bool operand_tma_ready(const float *ptr, int64_t ld) {
+    return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && ld % 4 == 0;
+}
+
+int launch_repack(const float *src, int64_t ld_src, float *dst, int64_t ld_dst, int64_t rows, int64_t cols,
+                  cudaStream_t stream) {
+    const int threads = 256;
+    const int64_t gx = std::min<int64_t>((cols + threads - 1) / threads, 64);
+    const int64_t gy = std::min<int64_t>(rows, 65535);
+    repack_rows<<<dim3(unsigned(gx), unsigned(gy)), threads, 0, stream>>>(src, ld_src, dst, ld_dst, rows, cols);
+    return check_launch();
+}
+
 int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
                   cudaStream_t stream) {
@@ -153,12 +184,60 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     if (rc != REPOPS_OK) return rc;
 
     const int cfg = config >= 0 ? config : choose_config(M, N);
-    const bool tma_ok = gemm_tma_eligible(p);
+    bool tma_ok = gemm_tma_eligible(p);
     if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
+
+    // Large problems whose operands TMA cannot describe (a base not 16-byte
+    // aligned, a leading dimension not a multiple of 4): copy the offending
+    // operand(s) into stream-ordered scratch with a 16-byte pitch and run the
+    // TMA kernels on the copy.  Falls back to the 4-byte loader when the
+    // scratch cannot be had.
+    void *scratch = nullptr;
+    if (loader == REPOPS_LOADER_AUTO && !tma_ok && 2.0 * double(M) * double(N) * double(K) >= kRepackMinFlops) {
+        GemmProblem q = p;
+        const bool packA = !operand_tma_ready(A, lda), packB = !operand_tma_ready(B, ldb);
+        const int64_t lda2 = packA ? (a_cols + 3) / 4 * 4 : lda, ldb2 = packB ? (b_cols + 3) / 4 * 4 : ldb;
+        q.lda = lda2;
+        q.ldb = ldb2;
+        q.A = reinterpret_cast<const float *>(uintptr_t(16));   // any aligned address: eligibility only
+        q.B = q.A;
+        if (!packA) q.A = A;
+        if (!packB) q.B = B;
+        const uint64_t bytesA = packA ? uint64_t(a_rows) * uint64_t(lda2) * 4u : 0;
+        const uint64_t bytesB = packB ? uint64_t(b_rows) * uint64_t(ldb2) * 4u : 0;
+        if ((packA || packB) && gemm_tma_eligible(q) &&
+            cudaMallocAsync(&scratch, bytesA + bytesB, stream) == cudaSuccess) {
+            float *dA = static_cast<float *>(scratch);
+            float *dB = dA + bytesA / 4;
+            if (packA) rc = launch_repack(A, lda, dA, lda2, a_rows, a_cols, stream);
+            if (rc == REPOPS_OK && packB) rc = launch_repack(B, ldb, dB, ldb2, b_rows, b_cols, stream);
+            if (rc == REPOPS_OK) {
+                p.A = packA ? dA : A;
+                p.lda = lda2;
+                p.B = packB ? dB : B;
+                p.ldb = ldb2;
+                tma_ok = true;
+            }
+        } else {
+            cudaGetLastError();   // a refused allocation is not an error here
+            scratch = nullptr;
+        }
+        if (rc != REPOPS_OK) {
+            if (scratch) cudaFreeAsync(scratch, stream);
+            return rc;
+        }
+    }
     const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
     rc = kLaunch[cfg](p, use);
-    if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO)
-        rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);   // encoder refused the map
+    if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO) {
+        // the encoder refused a map: run on the caller's operands with the 4-byte loader
+        p.A = A; p.lda = lda; p.B = B; p.ldb = ldb;
+        rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);
+    }
+    if (scratch) {
+        cudaError_t e = cudaFreeAsync(scratch, stream);
+        if (e != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
+    }
     return rc;
 }
 
