@@ -37,10 +37,13 @@ _lib = None
 
 
 def lib():
-    """Loads (building first if needed) the oracle shared library."""
+    """Loads (building first if needed) the oracle shared library.
+
+    REPOPS_ORACLE_LIB names another build of repops_oracle.c to load instead;
+    the mutation tests use it to show that the pins catch planted mistakes."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = os.environ.get("REPOPS_ORACLE_LIB") or _build.build()
         L = ctypes.CDLL(path)
         i64, i32, vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
         L.oracle_fp_env_ok.restype = i32

@@ -1,0 +1,80 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case plants one mistake in a copy of oracle/repops_oracle.c, builds it
+with the oracle's own flags, and runs the pin suite (tests/test_oracle_*.py)
+against it in a subprocess: the suite must fail.  The unmodified source must
+pass.  Nothing here touches the CUDA library.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "repops_oracle.c")
+PINS = [os.path.join(ROOT, "tests", f) for f in
+        ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py")]
+
+MUTATIONS = {
+    "gemm: fused multiply-add": (
+        "float p = a * b;        /* product, rounded to binary32 */\n                sum = sum + p; ",
+        "sum = __builtin_fmaf(a, b, sum); "),
+    "gemm: k in decreasing order": (
+        "for (int64_t k = 0; k < K; ++k) {", "for (int64_t k = K - 1; k >= 0; --k) {"),
+    "gemm: sum starts at -0": ("float sum = 0.0f;", "float sum = -0.0f;"),
+    "gemm: B indexed as if transposed": (
+        "float b = transB ? B[j * ldb + k] : B[k * ldb + j];",
+        "float b = transB ? B[k * ldb + j] : B[j * ldb + k];"),
+    "gemm: product in double": ("float p = a * b; ", "float p = (float)((double)a * (double)b + 1e-30); "),
+    "mean: fold starts at zero": (
+        "float S = grads[order[0]][e];\n        for (int r = 1; r < nC; ++r) {",
+        "float S = 0.0f;\n        for (int r = 0; r < nC; ++r) {"),
+    "mean: multiply by the reciprocal": ("float gbar = S / count;", "float gbar = S * (1.0f / count);"),
+    "mean: SGD adds the step": ("theta[e] = theta[e] - step;", "theta[e] = theta[e] + step;"),
+    "mean: contributor order ignored": ("S = S + grads[order[r]][e];", "S = S + grads[r][e];"),
+    "sort: signed byte comparison": ("if (a[i] != b[i]) return a[i] < b[i];",
+                                     "if (a[i] != b[i]) return (signed char)a[i] < (signed char)b[i];"),
+    "sort: longer prefix first": ("    return la < lb;\n}", "    return la > lb;\n}"),
+    "sha256: rotate by 7 in Sigma1": ("uint32_t S1 = rotr32(e, 6)", "uint32_t S1 = rotr32(e, 7)"),
+    "sha256: length in bytes, not bits": ("uint64_t bits = c->total * 8u;", "uint64_t bits = c->total;"),
+    "merkle: node prefix 0x02": ("msg[0] = 0x01;", "msg[0] = 0x02;"),
+    "merkle: no leaf prefix": ("osha_update(&c, &prefix, 1);\n    osha_update(&c, data + start, end - start);",
+                               "osha_update(&c, data + start, end - start);"),
+    "merkle: unpaired node hashed with itself": (
+        "memmove(level + 32 * next, level + 32 * (count - 1), 32);",
+        "merkle_node(level + 32 * (count - 1), level + 32 * (count - 1), level + 32 * next);"),
+    "merkle: leaves one byte short": ("uint64_t end = start + leaf;", "uint64_t end = start + leaf - 1;"),
+    "proof: sibling side swapped": ("merkle_node(proof + 32 * used++, h, t);", "merkle_node(h, proof + 32 * used++, t);"),
+}
+
+
+def build_variant(tmp_path, name, source):
+    sys.path.insert(0, ROOT)
+    from oracle import build as ob
+    src = tmp_path / (name + ".c")
+    src.write_text(source)
+    lib = tmp_path / (name + ".so")
+    subprocess.run([os.environ.get("CC", "gcc")] + ob.CFLAGS + ["-o", str(lib), str(src)], check=True)
+    return str(lib)
+
+
+def run_pins(lib):
+    env = dict(os.environ, REPOPS_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"] + PINS,
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=600)
+    return r.returncode, r.stdout[-2000:]
+
+
+def test_unmodified_source_passes_the_pins(tmp_path):
+    rc, out = run_pins(build_variant(tmp_path, "original", open(SRC).read()))
+    assert rc == 0, out
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistake_fails_a_pin(tmp_path, name):
+    old, new = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, "mutation anchor not found exactly once: " + name
+    rc, out = run_pins(build_variant(tmp_path, "m", src.replace(old, new)))
+    assert rc != 0, "the pins did not catch: " + name
