@@ -22,6 +22,11 @@ What each function follows (page title, section):
   merkle_*   -- "Zoo Per-LLM Chain Soundness" §1 (batch hash = Merkle root),
                 §6 (bytes32 roots); "Verde与RepOps" §2.3.2 (checkpoint hash is a
                 Merkle tree) and §2.4 (membership proofs).
+  exp, erfc_pos, gelu, row_sum, softmax_rows, layernorm_rows, rmsnorm_rows
+             -- "Verde与RepOps" §3.2 (order-critical dimensions serial or with
+                synchronised threads), §4.3 (LayerNorm, GeLU, ERF): reductions in
+                a fixed 32-ary tree, exp by Cody-Waite reduction + Horner, erfc
+                by the Numerical Recipes §6.2 Chebyshev fit (see the C source).
   replay     -- "Zoo Per-LLM Chain Soundness" §7 "Reproducibility test plan":
                 replay each block's batch in order, then check H(theta) = m.
 Pins against things other than the oracle itself live in tests/test_oracle_*.py.
@@ -75,6 +80,23 @@ def lib():
         L.oracle_merkle_verify.restype = i32
         L.oracle_merkle_verify.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, vp,
                                            i32, vp]
+        f32 = ctypes.c_float
+        L.oracle_exp.restype = f32
+        L.oracle_exp.argtypes = [f32]
+        L.oracle_erfc_pos.restype = f32
+        L.oracle_erfc_pos.argtypes = [f32]
+        L.oracle_gelu.restype = f32
+        L.oracle_gelu.argtypes = [f32]
+        L.oracle_gelu_vec.restype = None
+        L.oracle_gelu_vec.argtypes = [i64, vp, vp]
+        L.oracle_row_sum.restype = f32
+        L.oracle_row_sum.argtypes = [vp, i64]
+        L.oracle_softmax_rows.restype = None
+        L.oracle_softmax_rows.argtypes = [i64, i64, vp, i64, vp, i64]
+        L.oracle_layernorm_rows.restype = None
+        L.oracle_layernorm_rows.argtypes = [i64, i64, vp, i64, vp, vp, f32, vp, i64]
+        L.oracle_rmsnorm_rows.restype = None
+        L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64]
         if L.oracle_fp_env_ok() != 1:
             raise RuntimeError("host floating-point environment flushes subnormals "
                                "or does not round to nearest even; the oracle "
@@ -266,3 +288,57 @@ def replay(grads_per_step, orders, etas, theta, leaf: int = 4096):
         th = mean_sgd(gs, order, eta, th)
         roots.append(merkle_root(th, leaf))
     return th, roots
+
+
+def exp(x: float) -> float:
+    return float(lib().oracle_exp(ctypes.c_float(x)))
+
+
+def erfc_pos(z: float) -> float:
+    return float(lib().oracle_erfc_pos(ctypes.c_float(z)))
+
+
+def gelu(x) -> np.ndarray:
+    L = lib()
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty_like(a)
+    L.oracle_gelu_vec(a.size, _ptr(a), _ptr(out))
+    return out
+
+
+def row_sum(x) -> float:
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    return float(lib().oracle_row_sum(_ptr(a), a.size))
+
+
+def _rows(x):
+    a = np.asarray(x, dtype=np.float32)
+    if a.ndim != 2 or a.strides[1] != 4:
+        a = np.ascontiguousarray(a)
+    return a, a.strides[0] // 4
+
+
+def softmax_rows(x) -> np.ndarray:
+    a, lda = _rows(x)
+    y = np.empty(a.shape, dtype=np.float32)
+    lib().oracle_softmax_rows(a.shape[0], a.shape[1], _ptr(a), lda, _ptr(y), a.shape[1])
+    return y
+
+
+def layernorm_rows(x, gamma, beta, eps: float) -> np.ndarray:
+    a, lda = _rows(x)
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    b = np.ascontiguousarray(beta, dtype=np.float32)
+    y = np.empty(a.shape, dtype=np.float32)
+    lib().oracle_layernorm_rows(a.shape[0], a.shape[1], _ptr(a), lda, _ptr(g), _ptr(b),
+                                ctypes.c_float(eps), _ptr(y), a.shape[1])
+    return y
+
+
+def rmsnorm_rows(x, gamma, eps: float) -> np.ndarray:
+    a, lda = _rows(x)
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    y = np.empty(a.shape, dtype=np.float32)
+    lib().oracle_rmsnorm_rows(a.shape[0], a.shape[1], _ptr(a), lda, _ptr(g), ctypes.c_float(eps),
+                              _ptr(y), a.shape[1])
+    return y

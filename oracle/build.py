@@ -15,6 +15,7 @@ LIB = os.path.join(OUT_DIR, "liboracle.so")
 
 CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
           "-fno-strict-aliasing", "-fPIC", "-shared", "-Wall"]
+LDLIBS = ["-lm"]
 
 
 def build(force: bool = False) -> str:
@@ -24,7 +25,7 @@ def build(force: bool = False) -> str:
         return LIB
     os.makedirs(OUT_DIR, exist_ok=True)
     tmp = LIB + ".tmp.%d" % os.getpid()
-    cmd = [os.environ.get("CC", "gcc")] + CFLAGS + ["-o", tmp, SRC]
+    cmd = [os.environ.get("CC", "gcc")] + CFLAGS + ["-o", tmp, SRC] + LDLIBS
     subprocess.run(cmd, check=True)
     os.replace(tmp, LIB)
     return LIB

@@ -44,6 +44,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#include <math.h>   /* rintf, sqrtf: IEEE round-to-integral and correctly rounded square root */
 
 /* ------------------------------------------------------------------------ */
 /* Floating-point environment                                                */
@@ -510,4 +511,174 @@ int oracle_merkle_verify(const uint8_t *leaf_bytes, uint64_t leaf_len, uint64_t 
         j /= 2;
     }
     return used == steps && memcmp(h, root, 32) == 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Order-fixed row operators: softmax, LayerNorm, RMSNorm, GeLU              */
+/* [RepOps §3.2 (order-critical dimensions run serially or with synchronised */
+/*  threads), §3.3 and §4.3 (LayerNorm, GeLU and ERF are the operators that  */
+/*  dominate DistilBERT's overhead); §3.1 (the order must not depend on the  */
+/*  hardware)]                                                               */
+/*                                                                           */
+/* The pages fix no algorithm for these operators; the library defines:      */
+/*  - reductions over a row in a fixed 32-ary tree: each run of 32           */
+/*    consecutive values is folded left to right from its first value; the   */
+/*    run results are folded the same way, level by level, until one value   */
+/*    is left;                                                               */
+/*  - exp by Cody-Waite range reduction x = k*ln2 + r (ln2 split in two      */
+/*    parts), a degree-7 Taylor polynomial in r by Horner's rule, and exact  */
+/*    scaling by 2^k; every step one rounded IEEE operation, no FMA;         */
+/*  - erfc(z), z >= 0, by the Chebyshev fit of Press, Teukolsky, Vetterling  */
+/*    and Flannery, Numerical Recipes, section 6.2 (fractional error below   */
+/*    1.2e-7), with the exp above;                                           */
+/*  - GeLU(x) = 0.5*x*(1 + erf(x/sqrt 2)), with 1 + erf(z) = 2 - erfc(z)     */
+/*    for z >= 0 and erfc(-z) for z < 0 (no cancellation).                  */
+/* ------------------------------------------------------------------------ */
+
+#define ROW_RUN 32
+
+/* Fixed 32-ary tree reduction, in place over v[0..n-1]; op 0 = sum, 1 = max.
+ * max keeps the earlier value unless the later one is strictly greater. */
+static float tree_reduce(float *v, int64_t n, int op)
+{
+    while (n > 1) {
+        int64_t m = 0;
+        for (int64_t s = 0; s < n; s += ROW_RUN) {
+            int64_t e = s + ROW_RUN < n ? s + ROW_RUN : n;
+            float acc = v[s];
+            for (int64_t i = s + 1; i < e; ++i) {
+                if (op == 0) acc = acc + v[i];
+                else if (v[i] > acc) acc = v[i];
+            }
+            v[m++] = acc;
+        }
+        n = m;
+    }
+    return v[0];
+}
+
+float oracle_row_sum(const float *x, int64_t n)
+{
+    float *v = (float *)malloc((size_t)n * sizeof(float));
+    memcpy(v, x, (size_t)n * sizeof(float));
+    float r = tree_reduce(v, n, 0);
+    free(v);
+    return r;
+}
+
+static float f_from_bits(uint32_t b) { float f; memcpy(&f, &b, 4); return f; }
+
+/* 2^k as a float, for -126 <= k <= 127. */
+static float pow2i(int k) { return f_from_bits((uint32_t)(k + 127) << 23); }
+
+float oracle_exp(float x)
+{
+    if (x != x) return x;
+    if (x > 88.72283935546875f) return f_from_bits(0x7f800000u);   /* overflow */
+    if (x < -103.972084045410156f) return 0.0f;                    /* below half the least subnormal */
+    const float log2e = 1.44269502162933349609375f;   /* float nearest log2(e) */
+    const float ln2_hi = 0.693145751953125f;          /* 16 significant bits: k*ln2_hi is exact */
+    const float ln2_lo = 1.428606765330187045037746e-06f;
+    float t = x * log2e;
+    float kf = rintf(t);
+    int k = (int)kf;
+    float r = x - kf * ln2_hi;
+    r = r - kf * ln2_lo;
+    /* e^r ~ sum_{i<=7} r^i / i!, Horner from the highest term */
+    float p = 1.98412701e-04f;          /* 1/5040 */
+    p = p * r + 1.38888892e-03f;        /* 1/720 */
+    p = p * r + 8.33333377e-03f;        /* 1/120 */
+    p = p * r + 4.16666679e-02f;        /* 1/24 */
+    p = p * r + 1.66666672e-01f;        /* 1/6 */
+    p = p * r + 0.5f;
+    p = p * r + 1.0f;
+    p = p * r + 1.0f;
+    if (k > 127) return (p * pow2i(127)) * pow2i(k - 127);
+    if (k < -126) return (p * pow2i(k + 64)) * pow2i(-64);
+    return p * pow2i(k);
+}
+
+/* erfc(z) for z >= 0 (Numerical Recipes §6.2 Chebyshev fit). */
+float oracle_erfc_pos(float z)
+{
+    float t = 1.0f / (1.0f + 0.5f * z);
+    float q = 0.17087277f;
+    q = q * t + -0.82215223f;
+    q = q * t + 1.48851587f;
+    q = q * t + -1.13520398f;
+    q = q * t + 0.27886807f;
+    q = q * t + -0.18628806f;
+    q = q * t + 0.09678418f;
+    q = q * t + 0.37409196f;
+    q = q * t + 1.00002368f;
+    q = q * t;
+    float zz = z * z;
+    float arg = (-zz + -1.26551223f) + q;
+    return t * oracle_exp(arg);
+}
+
+float oracle_gelu(float x)
+{
+    float z = x * 0.707106769084930419921875f;   /* float nearest 1/sqrt(2) */
+    float phi2 = z >= 0.0f ? 2.0f - oracle_erfc_pos(z) : oracle_erfc_pos(-z);
+    return (0.5f * x) * phi2;
+}
+
+void oracle_gelu_vec(int64_t n, const float *x, float *y)
+{
+    for (int64_t i = 0; i < n; ++i) y[i] = oracle_gelu(x[i]);
+}
+
+/* y_i = e_i / s, e_i = exp(x_i - m), m = tree max of the row, s = tree sum of e. */
+void oracle_softmax_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y, int64_t ldy)
+{
+    float *v = (float *)malloc((size_t)cols * sizeof(float));
+    float *e = (float *)malloc((size_t)cols * sizeof(float));
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *xr = x + i * ldx;
+        memcpy(v, xr, (size_t)cols * sizeof(float));
+        float m = tree_reduce(v, cols, 1);
+        for (int64_t j = 0; j < cols; ++j) e[j] = oracle_exp(xr[j] - m);
+        memcpy(v, e, (size_t)cols * sizeof(float));
+        float s = tree_reduce(v, cols, 0);
+        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = e[j] / s;
+    }
+    free(v);
+    free(e);
+}
+
+/* mean = sum/n; d = x - mean; var = sum(d*d)/n; y = (d / sqrt(var + eps)) * gamma + beta. */
+void oracle_layernorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *gamma,
+                           const float *beta, float eps, float *y, int64_t ldy)
+{
+    float *v = (float *)malloc((size_t)cols * sizeof(float));
+    float *d = (float *)malloc((size_t)cols * sizeof(float));
+    const float n = (float)cols;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *xr = x + i * ldx;
+        memcpy(v, xr, (size_t)cols * sizeof(float));
+        float mean = tree_reduce(v, cols, 0) / n;
+        for (int64_t j = 0; j < cols; ++j) { d[j] = xr[j] - mean; v[j] = d[j] * d[j]; }
+        float var = tree_reduce(v, cols, 0) / n;
+        float denom = sqrtf(var + eps);
+        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (d[j] / denom) * gamma[j] + beta[j];
+    }
+    free(v);
+    free(d);
+}
+
+/* ms = sum(x*x)/n; y = (x / sqrt(ms + eps)) * gamma. */
+void oracle_rmsnorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *gamma,
+                         float eps, float *y, int64_t ldy)
+{
+    float *v = (float *)malloc((size_t)cols * sizeof(float));
+    const float n = (float)cols;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *xr = x + i * ldx;
+        for (int64_t j = 0; j < cols; ++j) v[j] = xr[j] * xr[j];
+        float ms = tree_reduce(v, cols, 0) / n;
+        float denom = sqrtf(ms + eps);
+        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (xr[j] / denom) * gamma[j];
+    }
+    free(v);
 }

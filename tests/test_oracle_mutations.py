@@ -14,7 +14,7 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "repops_oracle.c")
 PINS = [os.path.join(ROOT, "tests", f) for f in
-        ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py")]
+        ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py", "test_oracle_rowops.py")]
 
 MUTATIONS = {
     "gemm: fused multiply-add": (
@@ -46,6 +46,18 @@ MUTATIONS = {
         "merkle_node(level + 32 * (count - 1), level + 32 * (count - 1), level + 32 * next);"),
     "merkle: leaves one byte short": ("uint64_t end = start + leaf;", "uint64_t end = start + leaf - 1;"),
     "proof: sibling side swapped": ("merkle_node(proof + 32 * used++, h, t);", "merkle_node(h, proof + 32 * used++, t);"),
+    "rows: runs of 16": ("#define ROW_RUN 32", "#define ROW_RUN 16"),
+    "exp: degree-6 polynomial": ("float p = 1.98412701e-04f;          /* 1/5040 */\n    p = p * r + 1.38888892e-03f;",
+                                 "float p = 1.38888892e-03f;"),
+    "exp: one-part ln 2": ("    r = r - kf * ln2_lo;\n", ""),
+    "erfc: final factor t dropped": ("return t * oracle_exp(arg);", "return oracle_exp(arg);"),
+    "gelu: branches swapped": ("z >= 0.0f ? 2.0f - oracle_erfc_pos(z) : oracle_erfc_pos(-z)",
+                               "z >= 0.0f ? oracle_erfc_pos(z) : 2.0f - oracle_erfc_pos(-z)"),
+    "softmax: no max subtraction": ("e[j] = oracle_exp(xr[j] - m);", "e[j] = oracle_exp(xr[j]);"),
+    "layernorm: variance over n - 1": ("float var = tree_reduce(v, cols, 0) / n;",
+                                       "float var = tree_reduce(v, cols, 0) / (n - 1.0f);"),
+    "rmsnorm: multiply by a reciprocal": ("y[i * ldy + j] = (xr[j] / denom) * gamma[j];",
+                                          "y[i * ldy + j] = (xr[j] * (1.0f / denom)) * gamma[j];"),
 }
 
 
@@ -55,7 +67,8 @@ def build_variant(tmp_path, name, source):
     src = tmp_path / (name + ".c")
     src.write_text(source)
     lib = tmp_path / (name + ".so")
-    subprocess.run([os.environ.get("CC", "gcc")] + ob.CFLAGS + ["-o", str(lib), str(src)], check=True)
+    subprocess.run([os.environ.get("CC", "gcc")] + ob.CFLAGS + ["-o", str(lib), str(src)] + ob.LDLIBS,
+                   check=True)
     return str(lib)
 
 
