@@ -532,7 +532,10 @@ int oracle_merkle_verify(const uint8_t *leaf_bytes, uint64_t leaf_len, uint64_t 
 /*    and Flannery, Numerical Recipes, section 6.2 (fractional error below   */
 /*    1.2e-7), with the exp above;                                           */
 /*  - GeLU(x) = 0.5*x*(1 + erf(x/sqrt 2)), with 1 + erf(z) = 2 - erfc(z)     */
-/*    for z >= 0 and erfc(-z) for z < 0 (no cancellation).                  */
+/*    for z >= 0 and erfc(-z) for z < 0 (no cancellation);                  */
+/*  - a row's normaliser is one correctly rounded reciprocal per row         */
+/*    (1/s for softmax, 1/sqrt(var + eps) for the norms), applied to each    */
+/*    element by one multiplication.                                         */
 /* ------------------------------------------------------------------------ */
 
 #define ROW_RUN 32
@@ -629,7 +632,8 @@ void oracle_gelu_vec(int64_t n, const float *x, float *y)
     for (int64_t i = 0; i < n; ++i) y[i] = oracle_gelu(x[i]);
 }
 
-/* y_i = e_i / s, e_i = exp(x_i - m), m = tree max of the row, s = tree sum of e. */
+/* y_i = e_i * (1/s), e_i = exp(x_i - m), m = tree max of the row, s = tree sum
+ * of e, 1/s one correctly rounded division per row. */
 void oracle_softmax_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y, int64_t ldy)
 {
     float *v = (float *)malloc((size_t)cols * sizeof(float));
@@ -641,13 +645,15 @@ void oracle_softmax_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx
         for (int64_t j = 0; j < cols; ++j) e[j] = oracle_exp(xr[j] - m);
         memcpy(v, e, (size_t)cols * sizeof(float));
         float s = tree_reduce(v, cols, 0);
-        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = e[j] / s;
+        float inv = 1.0f / s;
+        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = e[j] * inv;
     }
     free(v);
     free(e);
 }
 
-/* mean = sum/n; d = x - mean; var = sum(d*d)/n; y = (d / sqrt(var + eps)) * gamma + beta. */
+/* mean = sum/n; d = x - mean; var = sum(d*d)/n; inv = 1/sqrt(var + eps);
+ * y = (d * inv) * gamma + beta. */
 void oracle_layernorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *gamma,
                            const float *beta, float eps, float *y, int64_t ldy)
 {
@@ -660,14 +666,14 @@ void oracle_layernorm_rows(int64_t rows, int64_t cols, const float *x, int64_t l
         float mean = tree_reduce(v, cols, 0) / n;
         for (int64_t j = 0; j < cols; ++j) { d[j] = xr[j] - mean; v[j] = d[j] * d[j]; }
         float var = tree_reduce(v, cols, 0) / n;
-        float denom = sqrtf(var + eps);
-        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (d[j] / denom) * gamma[j] + beta[j];
+        float inv = 1.0f / sqrtf(var + eps);
+        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (d[j] * inv) * gamma[j] + beta[j];
     }
     free(v);
     free(d);
 }
 
-/* ms = sum(x*x)/n; y = (x / sqrt(ms + eps)) * gamma. */
+/* ms = sum(x*x)/n; inv = 1/sqrt(ms + eps); y = (x * inv) * gamma. */
 void oracle_rmsnorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *gamma,
                          float eps, float *y, int64_t ldy)
 {
@@ -677,8 +683,8 @@ void oracle_rmsnorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx
         const float *xr = x + i * ldx;
         for (int64_t j = 0; j < cols; ++j) v[j] = xr[j] * xr[j];
         float ms = tree_reduce(v, cols, 0) / n;
-        float denom = sqrtf(ms + eps);
-        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (xr[j] / denom) * gamma[j];
+        float inv = 1.0f / sqrtf(ms + eps);
+        for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (xr[j] * inv) * gamma[j];
     }
     free(v);
 }

@@ -56,8 +56,9 @@ MUTATIONS = {
     "softmax: no max subtraction": ("e[j] = oracle_exp(xr[j] - m);", "e[j] = oracle_exp(xr[j]);"),
     "layernorm: variance over n - 1": ("float var = tree_reduce(v, cols, 0) / n;",
                                        "float var = tree_reduce(v, cols, 0) / (n - 1.0f);"),
-    "rmsnorm: multiply by a reciprocal": ("y[i * ldy + j] = (xr[j] / denom) * gamma[j];",
-                                          "y[i * ldy + j] = (xr[j] * (1.0f / denom)) * gamma[j];"),
+    "rmsnorm: divide each element": ("y[i * ldy + j] = (xr[j] * inv) * gamma[j];",
+                                     "y[i * ldy + j] = (xr[j] / sqrtf(ms + eps)) * gamma[j];"),
+    "softmax: divide each element": ("y[i * ldy + j] = e[j] * inv;", "y[i * ldy + j] = e[j] / s;"),
 }
 
 

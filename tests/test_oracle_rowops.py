@@ -115,7 +115,8 @@ def ref_softmax_row(row, orc):
     m = ref_tree(row, "max")
     e = [orc.exp(fx.sub(float(x), m)) for x in row]
     s = ref_tree(e, "sum")
-    return [fx.div(v, s) for v in e]
+    inv = fx.div(1.0, s)
+    return [fx.mul(v, inv) for v in e]
 
 
 @pytest.mark.parametrize("cols", [1, 7, 32, 33, 100, 257])
@@ -131,7 +132,7 @@ def test_softmax_exact_composition(orc, cols):
 def test_softmax_closed_forms(orc):
     for n in (1, 5, 32, 1000):
         y = orc.softmax_rows(np.full((2, n), 3.25, np.float32))
-        assert np.all(y == np.float32(1) / np.float32(n))     # exp(0) = 1, sum = n, 1/n rounded
+        assert np.all(y == np.float32(1) / np.float32(n))     # exp(0) = 1, sum = n, 1 * fl(1/n)
     # shifting an integer-valued row by an integer keeps x - max exact: same bits
     rng = np.random.default_rng(3)
     x = rng.integers(-20, 20, (4, 300)).astype(np.float32)
@@ -150,7 +151,8 @@ def ref_layernorm_row(row, gamma, beta, eps):
     d = [fx.sub(float(x), mean) for x in row]
     var = fx.div(ref_tree([fx.mul(v, v) for v in d], "sum"), n)
     denom = f32(math.sqrt(fx.add(var, eps)))   # double then float: innocuous double rounding
-    return [fx.add(fx.mul(fx.div(v, denom), float(g)), float(b)) for v, g, b in zip(d, gamma, beta)]
+    inv = fx.div(1.0, denom)
+    return [fx.add(fx.mul(fx.mul(v, inv), float(g)), float(b)) for v, g, b in zip(d, gamma, beta)]
 
 
 @pytest.mark.parametrize("cols", [1, 2, 31, 64, 129])
@@ -185,7 +187,8 @@ def ref_rmsnorm_row(row, gamma, eps):
     n = float(np.float32(len(row)))
     ms = fx.div(ref_tree([fx.mul(float(x), float(x)) for x in row], "sum"), n)
     denom = f32(math.sqrt(fx.add(ms, eps)))
-    return [fx.mul(fx.div(float(x), denom), float(g)) for x, g in zip(row, gamma)]
+    inv = fx.div(1.0, denom)
+    return [fx.mul(fx.mul(float(x), inv), float(g)) for x, g in zip(row, gamma)]
 
 
 @pytest.mark.parametrize("cols", [1, 3, 32, 65, 200])
