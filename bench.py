@@ -550,7 +550,51 @@ def run_sweep(args):
     print(json.dumps({"sweep": "decoder layer set, 15 GEMMs", "ms": tot_ms, "tflops": tot_f / tot_ms / 1e9,
                       "frac_of_fp32_peak": tot_f / tot_ms / 1e9 / peak}), flush=True)
     del X, Xin, W, dY
+    run_sweep_rowops(dev, s, flush, measured_peaks()[0].get("hbm_gbs", 6800.0))
     run_sweep_commitments(dev, s, flush)
+
+
+def run_sweep_rowops(dev, s, flush, hbm):
+    """The order-fixed row operators on decoder-sized tensors: LayerNorm and
+    RMSNorm over 16 x 4096 tokens x 2048, GeLU over 4096 x 8192 activations,
+    softmax over 8 heads of 4096 x 4096 scores.  Bytes = one read of x and one
+    write of y (HBM roofline); the L2 is flushed before each launch."""
+    def ev_time(fn, reps=5):
+        with torch.cuda.stream(s):
+            fn()
+            evs = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                fn()
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+    def emit(name, nbytes, ms):
+        gbs = nbytes / ms / 1e6
+        print(json.dumps({"sweep": name, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm}), flush=True)
+
+    T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
+    X = inputs.normal((16 * T, D), 1.0, 100, dev)
+    Y = torch.empty_like(X)
+    g = inputs.normal((D,), 1.0, 101, dev)
+    b = inputs.normal((D,), 0.1, 102, dev)
+    emit("layernorm rows 65536 x 2048", 2 * X.numel() * 4,
+         ev_time(lambda: rp.layernorm_rows(X, g, b, 1e-5, out=Y, stream=s)))
+    emit("rmsnorm rows 65536 x 2048", 2 * X.numel() * 4,
+         ev_time(lambda: rp.rmsnorm_rows(X, g, 1e-6, out=Y, stream=s)))
+    del X, Y
+    H = inputs.normal((T, 4 * D), 1.0, 103, dev)
+    G = torch.empty_like(H)
+    emit("gelu 4096 x 8192", 2 * H.numel() * 4, ev_time(lambda: rp.gelu(H, out=G, stream=s)))
+    del H, G
+    S = inputs.normal((8 * T, T), 3.0, 104, dev)
+    P = torch.empty_like(S)
+    emit("softmax rows 8 x 4096 x 4096", 2 * S.numel() * 4, ev_time(lambda: rp.softmax_rows(S, out=P, stream=s)))
+    del S, P
 
 
 def run_sweep_commitments(dev, s, flush):

@@ -281,6 +281,57 @@ int repops_merkle_verify(const void *leaf_bytes, uint64_t leaf_len, uint64_t nle
                          int *ok_out, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Order-fixed row operators: softmax, LayerNorm, RMSNorm, GeLU              */
+/* "Verde与RepOps" §3.2 (order-critical dimensions run serially or with      */
+/* synchronised threads), §3.3 and §4.3 (LayerNorm, GeLU and ERF are the     */
+/* operators behind DistilBERT's overhead).  The pages fix no algorithm; the */
+/* library's are:                                                            */
+/*  - row reductions in a fixed 32-ary tree: each run of 32 consecutive      */
+/*    values is folded left to right from its first value, the run results   */
+/*    are folded the same way, level by level, until one value is left (max  */
+/*    keeps the earlier value unless a later one is strictly greater);       */
+/*  - exp(x): k = rint(x*log2 e) (ties to even), r = (x - k*ln2_hi) -        */
+/*    k*ln2_lo (Cody-Waite two-part ln 2), e^r by the degree-7 Taylor        */
+/*    polynomial in Horner form, times 2^k by exact power-of-two scaling;    */
+/*    within 1.1 ulp of e^x; +inf above 88.7228394, 0 below -103.972084;     */
+/*  - erfc(z), z >= 0: the Chebyshev fit of Numerical Recipes §6.2 with the  */
+/*    exp above;                                                             */
+/*  - a row's normaliser is one correctly rounded reciprocal per row,        */
+/*    applied to each element by one multiplication;                         */
+/*  - every other step one correctly rounded binary32 operation (division    */
+/*    and square root included), no fused multiply-add.                      */
+/* Matrices are row-major with leading dimensions in elements (ld >= cols).  */
+/* y may be x itself (same pointer and leading dimension); any other overlap */
+/* is ALIAS.  rows == 0 or cols == 0: no-op.  cols up to 393216              */
+/* (UNSUPPORTED beyond).  Rows of at most 32768 values are read once and     */
+/* written once.                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* y[i][j] = e[i][j] * fl(1/s_i) with e[i][j] = exp(x[i][j] - m_i), m_i the
+ * tree max of row i and s_i the tree sum of its e. */
+int repops_softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                            float *y, int64_t ldy, cudaStream_t stream);
+
+/* mean = S/n, d = x - mean, var = tree sum of d*d / n,
+ * inv = fl(1 / fl(sqrt(var + eps))), y = (d * inv) * gamma[j] + beta[j];
+ * S = tree sum of the row, n = cols as binary32.  gamma, beta (device): cols
+ * values each. */
+int repops_layernorm_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                              const float *gamma, const float *beta, float eps,
+                              float *y, int64_t ldy, cudaStream_t stream);
+
+/* ms = tree sum of x*x / n, inv = fl(1 / fl(sqrt(ms + eps))),
+ * y = (x * inv) * gamma[j]. */
+int repops_rmsnorm_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                            const float *gamma, float eps, float *y, int64_t ldy,
+                            cudaStream_t stream);
+
+/* y = 0.5*x * (1 + erf(x/sqrt 2)), with z = x * fl(1/sqrt 2) and 1 + erf(z)
+ * evaluated as 2 - erfc(z) for z >= 0 and erfc(-z) for z < 0.  Elementwise
+ * over n values (device); y may be x. */
+int repops_gelu_f32(int64_t n, const float *x, float *y, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Step replay                                                               */
 /* "Zoo Per-LLM Chain Soundness" §7 "Reproducibility test plan": replay the  */
 /* blocks in order from the genesis state, then verify H(theta) = m          */

@@ -194,3 +194,20 @@ def test_replay_validates_every_block_before_launching(L):
     assert call([0, 1, 1, 0, 0, 1], theta=FAKE_A + 0x100000 * 5 + 64) == -2
     assert call([0, 1, 1, 0, 0, 1], roots=FAKE_C + 16) == -2
     assert L.repops_replay_mean_sgd_commit(0, nC, n, P, None, E, FAKE_C, 4096, FAKE_B, None) == -1
+
+
+def test_row_operators_reject_bad_arguments(L):
+    sm = L.repops_softmax_rows_f32
+    assert sm(-1, 4, FAKE_A, 4, FAKE_B, 4, None) == -1
+    assert sm(4, 4, FAKE_A, 3, FAKE_B, 4, None) == -1            # ldx < cols
+    assert sm(4, 4, FAKE_A, 4, FAKE_A + 8, 4, None) == -2        # partial overlap
+    assert sm(0, 4, FAKE_A, 4, FAKE_B, 4, None) == 0
+    assert sm(4, 400000, FAKE_A, 400000, FAKE_B, 400000, None) == -7
+    ln = L.repops_layernorm_rows_f32
+    assert ln(4, 4, FAKE_A, 4, None, FAKE_C, ctypes.c_float(1e-5), FAKE_B, 4, None) == -1
+    assert ln(4, 4, FAKE_A, 4, FAKE_B + 16, FAKE_C, ctypes.c_float(1e-5), FAKE_B, 4, None) == -2
+    rn = L.repops_rmsnorm_rows_f32
+    assert rn(4, 4, FAKE_A, 4, FAKE_B, ctypes.c_float(1e-5), FAKE_B, 4, None) == -2
+    assert L.repops_gelu_f32(-1, FAKE_A, FAKE_B, None) == -1
+    assert L.repops_gelu_f32(8, FAKE_A, FAKE_A + 4, None) == -2
+    assert L.repops_gelu_f32(0, None, None, None) == 0

@@ -1,0 +1,117 @@
+"""GPU parity of the order-fixed row operators (softmax, LayerNorm, RMSNorm,
+GeLU) against the oracle, through the C ABI.
+
+"Verde与RepOps" §3.2 (order-critical dimensions serial or with synchronised
+threads), §4.3 (LayerNorm, GeLU, ERF).  Bar: bit-exact, for every kernel
+variant (threads per row, runs per thread, the long-row kernel), aligned and
+unaligned rows, and in place.
+"""
+import numpy as np
+import pytest
+import torch
+
+from verifiable_repops_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+# columns chosen to hit each kernel shape: 32, 64, 128, 256 threads x 1 run,
+# 256 x 2, 256 x 4 runs per thread, and the long-row kernel
+COLS = [1, 5, 32, 33, 1000, 2048, 4096, 8192, 8193, 16384, 16385, 32768, 40000]
+
+
+def u32(a):
+    return np.ascontiguousarray(a).view(np.uint32)
+
+
+def rows_input(rows, cols, seed, scale=3.0, pad=0):
+    x = inputs.normal((rows, cols + pad), scale, seed, DEV)
+    return x[:, :cols] if pad else x
+
+
+@pytest.mark.parametrize("cols", COLS)
+def test_softmax_matches_oracle(rp, orc, cols):
+    rows = 5 if cols <= 8192 else 3
+    x = rows_input(rows, cols, 1000 + cols)
+    y = rp.softmax_rows(x)
+    assert np.array_equal(u32(y.cpu().numpy()), u32(orc.softmax_rows(x.cpu().numpy())))
+
+
+@pytest.mark.parametrize("cols", COLS)
+def test_layernorm_matches_oracle(rp, orc, cols):
+    rows = 5 if cols <= 8192 else 3
+    x = rows_input(rows, cols, 2000 + cols, 2.0)
+    g = inputs.normal((cols,), 1.0, 3, DEV)
+    b = inputs.normal((cols,), 1.0, 4, DEV)
+    y = rp.layernorm_rows(x, g, b, 1e-5)
+    want = orc.layernorm_rows(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(), 1e-5)
+    assert np.array_equal(u32(y.cpu().numpy()), u32(want))
+
+
+@pytest.mark.parametrize("cols", COLS)
+def test_rmsnorm_matches_oracle(rp, orc, cols):
+    rows = 5 if cols <= 8192 else 3
+    x = rows_input(rows, cols, 3000 + cols, 1.0)
+    g = inputs.normal((cols,), 1.0, 5, DEV)
+    y = rp.rmsnorm_rows(x, g, 1e-6)
+    want = orc.rmsnorm_rows(x.cpu().numpy(), g.cpu().numpy(), 1e-6)
+    assert np.array_equal(u32(y.cpu().numpy()), u32(want))
+
+
+@pytest.mark.parametrize("cols", [7, 1000, 8195])
+def test_unaligned_rows_and_in_place(rp, orc, cols):
+    # ld = cols + 1: rows are not 16-byte aligned -> scalar loads, same bits
+    x = rows_input(4, cols, 4000 + cols, 3.0, pad=1)
+    want = orc.softmax_rows(x.cpu().numpy())
+    assert np.array_equal(u32(rp.softmax_rows(x).cpu().numpy()), u32(want))
+    g = inputs.normal((cols,), 1.0, 6, DEV)
+    b = inputs.normal((cols,), 1.0, 7, DEV)
+    want_ln = orc.layernorm_rows(x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy(), 1e-5)
+    z = x.clone()
+    rp.layernorm_rows(z, g, b, 1e-5, out=z)            # in place
+    assert np.array_equal(u32(z.cpu().numpy()), u32(want_ln))
+
+
+@pytest.mark.parametrize("n", [1, 7, 4096, (1 << 20) + 3])
+def test_gelu_matches_oracle(rp, orc, n):
+    x = inputs.normal((n,), 3.0, 5000 + n, DEV)
+    y = rp.gelu(x)
+    assert np.array_equal(u32(y.cpu().numpy()), u32(orc.gelu(x.cpu().numpy())))
+    base = inputs.normal((n + 1,), 3.0, 6000 + n, DEV)
+    xs = base[1:]                                        # 4-byte aligned only
+    assert np.array_equal(u32(rp.gelu(xs).cpu().numpy()), u32(orc.gelu(xs.cpu().numpy())))
+    xi = x.clone()
+    rp.gelu(xi, out=xi)
+    assert torch.equal(xi, y)
+
+
+def test_closed_forms_on_gpu(rp):
+    y = rp.softmax_rows(torch.full((3, 1000), 2.5, device=DEV))
+    assert torch.all(y == torch.tensor(1.0, dtype=torch.float32) / 1000.0)
+    b = torch.linspace(-1, 1, 300, device=DEV)
+    g = torch.full((300,), 2.0, device=DEV)
+    y = rp.layernorm_rows(torch.full((2, 300), 7.5, device=DEV), g, b, 1e-5)
+    assert torch.equal(y, torch.stack([b, b]))
+
+
+@pytest.mark.slow
+def test_decoder_sized_workloads_sampled(rp, orc):
+    T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
+    X = inputs.normal((T, D), 1.0, 100, DEV)
+    g = inputs.normal((D,), 1.0, 101, DEV)
+    b = inputs.normal((D,), 0.1, 102, DEV)
+    Y = rp.layernorm_rows(X, g, b, 1e-5)
+    R = rp.rmsnorm_rows(X, g, 1e-6)
+    rows = [0, 1, 2047, T - 1]
+    Xh = X[rows].cpu().numpy()
+    assert np.array_equal(u32(Y[rows].cpu().numpy()),
+                          u32(orc.layernorm_rows(Xh, g.cpu().numpy(), b.cpu().numpy(), 1e-5)))
+    assert np.array_equal(u32(R[rows].cpu().numpy()), u32(orc.rmsnorm_rows(Xh, g.cpu().numpy(), 1e-6)))
+    H = inputs.normal((T, 4 * D), 1.0, 103, DEV)          # MLP activations 4096 x 8192
+    G = rp.gelu(H)
+    assert np.array_equal(u32(G[rows].cpu().numpy()), u32(orc.gelu(H[rows].cpu().numpy())))
+    S = inputs.normal((8 * T, T), 3.0, 104, DEV)          # 8 heads of 4096 x 4096 scores
+    P = rp.softmax_rows(S)
+    srows = [0, 4095, 4096, 8 * T - 1]
+    assert np.array_equal(u32(P[srows].cpu().numpy()), u32(orc.softmax_rows(S[srows].cpu().numpy())))

@@ -17,6 +17,8 @@ memory and streams.
   merkle_verify                     ("Verde与RepOps" §2.4)
   replay(...)                       mean + SGD + commit per block, in order
                                     ("Zoo Per-LLM Chain Soundness" §7)
+  softmax_rows / layernorm_rows /   order-fixed row operators and GeLU
+  rmsnorm_rows / gelu               ("Verde与RepOps" §3.2, §4.3)
 """
 import ctypes
 
@@ -27,6 +29,7 @@ from ._capi import (LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA, MEAN_MAX_CONTRIBUTO
 __all__ = ["load", "version", "gemm", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
+           "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu",
            "device_status", "RepopsError",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
 
@@ -257,3 +260,69 @@ def replay(grads_per_step, orders, etas, theta, leaf: int = 4096, *, roots=None,
                                          theta.data_ptr(), leaf, roots.data_ptr(), _stream_handle(stream))
     _capi.check(rc, "repops_replay_mean_sgd_commit")
     return roots
+
+
+def _row_operand(x, name):
+    import torch
+    if x.dtype != torch.float32 or x.dim() != 2 or not x.is_cuda or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError("%s must be a 2-D float32 CUDA tensor with unit column stride" % name)
+    return x.data_ptr(), max(x.stride(0), x.shape[1], 1)
+
+
+def _row_out(x, out):
+    import torch
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
+    if tuple(out.shape) != tuple(x.shape):
+        raise ValueError("out must have the shape of x")
+    return out
+
+
+def softmax_rows(x, out=None, *, stream=None):
+    """Row softmax with the order-fixed max/sum trees and the library's exp."""
+    L = load()
+    px, ldx = _row_operand(x, "x")
+    out = _row_out(x, out)
+    py, ldy = _row_operand(out, "out")
+    rc = L.repops_softmax_rows_f32(x.shape[0], x.shape[1], px, ldx, py, ldy, _stream_handle(stream))
+    _capi.check(rc, "repops_softmax_rows_f32")
+    return out
+
+
+def layernorm_rows(x, gamma, beta, eps: float = 1e-5, out=None, *, stream=None):
+    L = load()
+    px, ldx = _row_operand(x, "x")
+    out = _row_out(x, out)
+    py, ldy = _row_operand(out, "out")
+    if gamma.numel() != x.shape[1] or beta.numel() != x.shape[1]:
+        raise ValueError("gamma and beta need one value per column")
+    rc = L.repops_layernorm_rows_f32(x.shape[0], x.shape[1], px, ldx, gamma.data_ptr(), beta.data_ptr(),
+                                     ctypes.c_float(eps), py, ldy, _stream_handle(stream))
+    _capi.check(rc, "repops_layernorm_rows_f32")
+    return out
+
+
+def rmsnorm_rows(x, gamma, eps: float = 1e-6, out=None, *, stream=None):
+    L = load()
+    px, ldx = _row_operand(x, "x")
+    out = _row_out(x, out)
+    py, ldy = _row_operand(out, "out")
+    if gamma.numel() != x.shape[1]:
+        raise ValueError("gamma needs one value per column")
+    rc = L.repops_rmsnorm_rows_f32(x.shape[0], x.shape[1], px, ldx, gamma.data_ptr(), ctypes.c_float(eps),
+                                   py, ldy, _stream_handle(stream))
+    _capi.check(rc, "repops_rmsnorm_rows_f32")
+    return out
+
+
+def gelu(x, out=None, *, stream=None):
+    """Elementwise GeLU (erf form) of a contiguous float32 CUDA tensor."""
+    import torch
+    L = load()
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty_like(x)
+    rc = L.repops_gelu_f32(x.numel(), x.data_ptr(), out.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_gelu_f32")
+    return out

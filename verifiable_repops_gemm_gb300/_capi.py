@@ -52,6 +52,10 @@ SIGNATURES = {
     "repops_merkle_proof": (_i32, [_vp, _u64, _u64, _vp, _vp]),
     "repops_merkle_verify": (_i32, [_vp, _u64, _u64, _u64, _vp, _vp, _vp, _vp]),
     "repops_replay_mean_sgd_commit": (_i32, [_i32, _i32, _i64, _vp, _vp, _vp, _vp, _u32, _vp, _vp]),
+    "repops_softmax_rows_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "repops_layernorm_rows_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _vp, _f32, _vp, _i64, _vp]),
+    "repops_rmsnorm_rows_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _f32, _vp, _i64, _vp]),
+    "repops_gelu_f32": (_i32, [_i64, _vp, _vp, _vp]),
 }
 
 MERKLE_NOALLOC_SCRATCH_BYTES = 1 << 20

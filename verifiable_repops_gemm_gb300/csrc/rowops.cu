@@ -1,0 +1,492 @@
+// rowops.cu -- order-fixed row operators: softmax, LayerNorm, RMSNorm, GeLU.
+//
+// "Verde与RepOps" §3.2: dimensions whose order matters run serially or with
+// synchronised threads; §3.3 and §4.3: LayerNorm, GeLU and ERF are the
+// operators behind DistilBERT's overhead.  The pages fix no algorithm for
+// them, so the library defines one whose every operation is a single IEEE
+// binary32 rounding in a fixed order -- the same bits on any hardware:
+//   - a reduction over a row is a fixed 32-ary tree: each run of 32
+//     consecutive values is folded left to right from its first value, the run
+//     results are folded the same way, level by level, until one value is left
+//     (max keeps the earlier value unless a later one is strictly greater);
+//   - exp(x): k = rint(x * log2 e); r = (x - k*ln2_hi) - k*ln2_lo (Cody and
+//     Waite's two-part ln 2, k*ln2_hi exact); e^r by the degree-7 Taylor
+//     polynomial in Horner form; times 2^k by exact power-of-two scaling;
+//   - erfc(z), z >= 0: the Chebyshev fit of Numerical Recipes §6.2 (Press,
+//     Teukolsky, Vetterling, Flannery), with the exp above;
+//   - GeLU(x) = 0.5*x*(1 + erf(x/sqrt 2)) with 1 + erf(z) = 2 - erfc(z) for
+//     z >= 0 and erfc(-z) for z < 0;
+//   - a row's normaliser is one correctly rounded reciprocal per row (1/s for
+//     softmax, 1/sqrt(var + eps) for the norms: __frcp_rn of __fsqrt_rn),
+//     applied to each element by one multiplication; products and sums never
+//     fuse.
+//
+// Kernels: one CTA per row.  Each thread owns whole runs (R runs of 32 values,
+// in registers), folds them, and the run results go through shared memory for
+// the upper tree levels; the row is read once and written once.  Rows longer
+// than 32 * 256 * 4 values use a kernel that re-reads the row for each phase.
+#include <algorithm>
+
+#include "internal.cuh"
+
+namespace repops {
+namespace {
+
+constexpr int RUN = 32;
+
+__device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ? a : b; }
+constexpr int MAX_FAST_RUNS = 256 * 4;          // register-resident rows: up to 32768 values
+constexpr int MAX_GENERIC_RUNS = 12288;         // run results in 48 KB of shared memory
+
+// ------------------------------------------------------------ arithmetic ----
+
+__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
+
+__device__ float exp_fixed(float x) {
+    if (x != x) return x;
+    if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
+    if (x < -103.972084045410156f) return 0.0f;
+    const float t = __fmul_rn(x, 1.44269502162933349609375f);
+    const float kf = rintf(t);
+    const int k = int(kf);
+    float r = __fsub_rn(x, __fmul_rn(kf, 0.693145751953125f));
+    r = __fsub_rn(r, __fmul_rn(kf, 1.428606765330187045037746e-06f));
+    float p = 1.98412701e-04f;
+    p = __fadd_rn(__fmul_rn(p, r), 1.38888892e-03f);
+    p = __fadd_rn(__fmul_rn(p, r), 8.33333377e-03f);
+    p = __fadd_rn(__fmul_rn(p, r), 4.16666679e-02f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.66666672e-01f);
+    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
+    if (k > 127) return __fmul_rn(__fmul_rn(p, pow2i(127)), pow2i(k - 127));
+    if (k < -126) return __fmul_rn(__fmul_rn(p, pow2i(k + 64)), pow2i(-64));
+    return __fmul_rn(p, pow2i(k));
+}
+
+__device__ float erfc_pos(float z) {
+    // correctly rounded reciprocal: the same value as a correctly rounded 1/x
+    const float t = __frcp_rn(__fadd_rn(1.0f, __fmul_rn(0.5f, z)));
+    float q = 0.17087277f;
+    q = __fadd_rn(__fmul_rn(q, t), -0.82215223f);
+    q = __fadd_rn(__fmul_rn(q, t), 1.48851587f);
+    q = __fadd_rn(__fmul_rn(q, t), -1.13520398f);
+    q = __fadd_rn(__fmul_rn(q, t), 0.27886807f);
+    q = __fadd_rn(__fmul_rn(q, t), -0.18628806f);
+    q = __fadd_rn(__fmul_rn(q, t), 0.09678418f);
+    q = __fadd_rn(__fmul_rn(q, t), 0.37409196f);
+    q = __fadd_rn(__fmul_rn(q, t), 1.00002368f);
+    q = __fmul_rn(q, t);
+    const float zz = __fmul_rn(z, z);
+    const float arg = __fadd_rn(__fadd_rn(-zz, -1.26551223f), q);
+    return __fmul_rn(t, exp_fixed(arg));
+}
+
+__device__ __forceinline__ float gelu_fixed(float x) {
+    const float z = __fmul_rn(x, 0.707106769084930419921875f);
+    // one erfc for either sign: no divergent branch
+    const float e = erfc_pos(fabsf(z));
+    const float phi2 = z >= 0.0f ? __fsub_rn(2.0f, e) : e;
+    return __fmul_rn(__fmul_rn(0.5f, x), phi2);
+}
+
+enum class Op { Sum, Max };
+
+template <Op OP>
+__device__ __forceinline__ float combine(float acc, float v) {
+    if constexpr (OP == Op::Sum) return __fadd_rn(acc, v);
+    else return v > acc ? v : acc;
+}
+
+// Upper levels of the tree over the m run results in a[] (shared memory),
+// ping-ponging with b[]; every thread of the CTA calls it and receives the
+// root.  Both buffers are clobbered.
+template <Op OP>
+__device__ float tree_upper(float *a, float *b, int m, float *bcast) {
+    __syncthreads();
+    while (m > 1) {
+        const int groups = (m + RUN - 1) / RUN;
+        for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+            const int s = g * RUN, e = min(s + RUN, m);
+            float acc = a[s];
+            for (int i = s + 1; i < e; ++i) acc = combine<OP>(acc, a[i]);
+            b[g] = acc;
+        }
+        __syncthreads();
+        float *t = a; a = b; b = t;
+        m = groups;
+    }
+    if (threadIdx.x == 0) *bcast = a[0];
+    __syncthreads();
+    const float r = *bcast;
+    __syncthreads();
+    return r;
+}
+
+// ------------------------------------------------------ register rows ----
+
+// A thread's R runs of one row: run j of the thread is run (threadIdx.x + j*T)
+// of the row.  Elements past the row end are never read or written.
+template <int T, int R>
+struct RowRuns {
+    float v[R][RUN];
+    int len[R];   // values in each run (0 when the run is past the end)
+
+    __device__ __forceinline__ void load(const float *__restrict__ row, int64_t n, bool vec) {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
+            len[j] = s < n ? int(imin64(RUN, n - s)) : 0;
+            if (vec && len[j] == RUN) {
+                const float4 *p = reinterpret_cast<const float4 *>(row + s);
+#pragma unroll
+                for (int q = 0; q < RUN / 4; ++q) {
+                    const float4 w = __ldcs(p + q);
+                    v[j][4 * q] = w.x; v[j][4 * q + 1] = w.y; v[j][4 * q + 2] = w.z; v[j][4 * q + 3] = w.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < RUN; ++i) v[j][i] = i < len[j] ? row[s + i] : 0.0f;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void store(float *__restrict__ row, bool vec) const {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
+            if (vec && len[j] == RUN) {
+                float4 *p = reinterpret_cast<float4 *>(row + s);
+#pragma unroll
+                for (int q = 0; q < RUN / 4; ++q)
+                    __stcs(p + q, make_float4(v[j][4 * q], v[j][4 * q + 1], v[j][4 * q + 2], v[j][4 * q + 3]));
+            } else {
+#pragma unroll
+                for (int i = 0; i < RUN; ++i)
+                    if (i < len[j]) row[s + i] = v[j][i];
+            }
+        }
+    }
+
+    // Folds each run (of f(value)) left to right into buf[run index]; returns
+    // the tree's root over the whole row.
+    template <Op OP, class F>
+    __device__ __forceinline__ float reduce(F f, float *buf, float *buf2, int runs, float *bcast) const {
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            if (len[j] > 0) {
+                float acc = f(v[j][0]);
+#pragma unroll
+                for (int i = 1; i < RUN; ++i)
+                    if (i < len[j]) acc = combine<OP>(acc, f(v[j][i]));
+                buf[threadIdx.x + j * T] = acc;
+            }
+        }
+        return tree_upper<OP>(buf, buf2, runs, bcast);
+    }
+};
+
+// The 32 values of run `s` of a per-column vector (gamma, beta): all loads in
+// flight together instead of one per element.
+__device__ __forceinline__ void load_run(const float *__restrict__ p, int64_t s, int len, bool vec,
+                                         float (&out)[RUN]) {
+    if (vec && len == RUN) {
+        const float4 *q = reinterpret_cast<const float4 *>(p + s);
+#pragma unroll
+        for (int k = 0; k < RUN / 4; ++k) {
+            const float4 w = __ldg(q + k);
+            out[4 * k] = w.x; out[4 * k + 1] = w.y; out[4 * k + 2] = w.z; out[4 * k + 3] = w.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) out[i] = i < len ? __ldg(p + s + i) : 0.0f;
+    }
+}
+
+struct Ident {
+    __device__ __forceinline__ float operator()(float x) const { return x; }
+};
+struct Square {
+    __device__ __forceinline__ float operator()(float x) const { return __fmul_rn(x, x); }
+};
+
+template <int T, int R>
+__global__ void __launch_bounds__(T)
+softmax_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx, float *__restrict__ y,
+                    int64_t ldy, int vec) {
+    __shared__ float buf[T * R];
+    __shared__ float buf2[(T * R + RUN - 1) / RUN];
+    __shared__ float bcast;
+    const int runs = int((n + RUN - 1) / RUN);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        RowRuns<T, R> rr;
+        rr.load(x + row * ldx, n, vec);
+        const float m = rr.template reduce<Op::Max>(Ident(), buf, buf2, runs, &bcast);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < rr.len[j]) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+        const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), buf, buf2, runs, &bcast));
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < rr.len[j]) rr.v[j][i] = __fmul_rn(rr.v[j][i], inv);
+        rr.store(y + row * ldy, vec);
+    }
+}
+
+template <int T, int R>
+__global__ void __launch_bounds__(T)
+layernorm_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
+                      const float *__restrict__ gamma, const float *__restrict__ beta, float eps,
+                      float *__restrict__ y, int64_t ldy, int vec, int pvec) {
+    __shared__ float buf[T * R];
+    __shared__ float buf2[(T * R + RUN - 1) / RUN];
+    __shared__ float bcast;
+    const int runs = int((n + RUN - 1) / RUN);
+    const float nf = float(n);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        RowRuns<T, R> rr;
+        rr.load(x + row * ldx, n, vec);
+        const float mean = __fdiv_rn(rr.template reduce<Op::Sum>(Ident(), buf, buf2, runs, &bcast), nf);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < rr.len[j]) rr.v[j][i] = __fsub_rn(rr.v[j][i], mean);
+        const float var = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), buf, buf2, runs, &bcast), nf);
+        const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            if (rr.len[j] == 0) continue;
+            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
+            float g[RUN], b[RUN];
+            load_run(gamma, s, rr.len[j], pvec, g);
+            load_run(beta, s, rr.len[j], pvec, b);
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < rr.len[j]) rr.v[j][i] = __fadd_rn(__fmul_rn(__fmul_rn(rr.v[j][i], inv), g[i]), b[i]);
+        }
+        rr.store(y + row * ldy, vec);
+    }
+}
+
+template <int T, int R>
+__global__ void __launch_bounds__(T)
+rmsnorm_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
+                    const float *__restrict__ gamma, float eps, float *__restrict__ y, int64_t ldy, int vec,
+                    int pvec) {
+    __shared__ float buf[T * R];
+    __shared__ float buf2[(T * R + RUN - 1) / RUN];
+    __shared__ float bcast;
+    const int runs = int((n + RUN - 1) / RUN);
+    const float nf = float(n);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        RowRuns<T, R> rr;
+        rr.load(x + row * ldx, n, vec);
+        const float ms = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), buf, buf2, runs, &bcast), nf);
+        const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            if (rr.len[j] == 0) continue;
+            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
+            float g[RUN];
+            load_run(gamma, s, rr.len[j], pvec, g);
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < rr.len[j]) rr.v[j][i] = __fmul_rn(__fmul_rn(rr.v[j][i], inv), g[i]);
+        }
+        rr.store(y + row * ldy, vec);
+    }
+}
+
+// ------------------------------------------------------ long rows ----
+
+// Run results of f over the row, each run folded from global memory.
+template <Op OP, class F>
+__device__ float generic_reduce(const float *__restrict__ row, int64_t n, F f, float *buf, float *buf2,
+                                float *bcast) {
+    const int runs = int((n + RUN - 1) / RUN);
+    for (int j = threadIdx.x; j < runs; j += blockDim.x) {
+        const int64_t s = int64_t(j) * RUN, e = imin64(s + RUN, n);
+        float acc = f(row[s]);
+        for (int64_t i = s + 1; i < e; ++i) acc = combine<OP>(acc, f(row[i]));
+        buf[j] = acc;
+    }
+    return tree_upper<OP>(buf, buf2, runs, bcast);
+}
+
+struct ExpShift {
+    float m;
+    __device__ __forceinline__ float operator()(float x) const { return exp_fixed(__fsub_rn(x, m)); }
+};
+struct SquareShift {
+    float m;
+    __device__ __forceinline__ float operator()(float x) const {
+        const float d = __fsub_rn(x, m);
+        return __fmul_rn(d, d);
+    }
+};
+
+// kind 0 = softmax, 1 = LayerNorm, 2 = RMSNorm.  Each thread writes only the
+// runs it read in the same pass, so y may be x.
+__global__ void __launch_bounds__(256)
+rows_generic_kernel(int kind, int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
+                    const float *__restrict__ gamma, const float *__restrict__ beta, float eps,
+                    float *__restrict__ y, int64_t ldy) {
+    extern __shared__ float buf[];   // runs + ceil(runs / 32) floats
+    __shared__ float bcast;
+    const int runs = int((n + RUN - 1) / RUN);
+    float *buf2 = buf + runs;
+    const float nf = float(n);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *row = x + r * ldx;
+        float *out = y + r * ldy;
+        if (kind == 0) {
+            const float m = generic_reduce<Op::Max>(row, n, Ident(), buf, buf2, &bcast);
+            const float inv = __frcp_rn(generic_reduce<Op::Sum>(row, n, ExpShift{m}, buf, buf2, &bcast));
+            for (int j = threadIdx.x; j < runs; j += blockDim.x)
+                for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i)
+                    out[i] = __fmul_rn(exp_fixed(__fsub_rn(row[i], m)), inv);
+        } else if (kind == 1) {
+            const float mean = __fdiv_rn(generic_reduce<Op::Sum>(row, n, Ident(), buf, buf2, &bcast), nf);
+            const float var = __fdiv_rn(generic_reduce<Op::Sum>(row, n, SquareShift{mean}, buf, buf2, &bcast), nf);
+            const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
+            for (int j = threadIdx.x; j < runs; j += blockDim.x)
+                for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i)
+                    out[i] = __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(row[i], mean), inv), gamma[i]), beta[i]);
+        } else {
+            const float ms = __fdiv_rn(generic_reduce<Op::Sum>(row, n, Square(), buf, buf2, &bcast), nf);
+            const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+            for (int j = threadIdx.x; j < runs; j += blockDim.x)
+                for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i)
+                    out[i] = __fmul_rn(__fmul_rn(row[i], inv), gamma[i]);
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(256)
+gelu_kernel(int64_t n, const float *__restrict__ x, float *__restrict__ y, int vec) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const int64_t first = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    if (vec) {
+        const int64_t n4 = n / 4;
+        for (int64_t i = first; i < n4; i += stride) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(x) + i);
+            __stcs(reinterpret_cast<float4 *>(y) + i,
+                   make_float4(gelu_fixed(v.x), gelu_fixed(v.y), gelu_fixed(v.z), gelu_fixed(v.w)));
+        }
+        for (int64_t i = n4 * 4 + first; i < n; i += stride) y[i] = gelu_fixed(x[i]);
+    } else {
+        for (int64_t i = first; i < n; i += stride) y[i] = gelu_fixed(x[i]);
+    }
+}
+
+// ------------------------------------------------------------ host ----
+
+int check_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *y, int64_t ldy) {
+    if (rows < 0 || cols < 0) return REPOPS_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return REPOPS_OK;
+    if (!x || !y || ldx < cols || ldy < cols) return REPOPS_ERR_INVALID_ARG;
+    if ((rows - 1) > (INT64_MAX / 4 - cols) / std::max<int64_t>(ldx, ldy)) return REPOPS_ERR_INVALID_ARG;
+    if ((cols + RUN - 1) / RUN > MAX_GENERIC_RUNS) return REPOPS_ERR_UNSUPPORTED;
+    const uint64_t xb = uint64_t((rows - 1) * ldx + cols) * 4u, yb = uint64_t((rows - 1) * ldy + cols) * 4u;
+    // in place (the same rows) is allowed; any other overlap is not
+    if (x == y && ldx == ldy) return REPOPS_OK;
+    if (ranges_overlap(x, xb, y, yb)) return REPOPS_ERR_ALIAS;
+    return REPOPS_OK;
+}
+
+bool rows_vec_ok(const float *x, int64_t ldx, const float *y, int64_t ldy) {
+    return reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0 &&
+           ldx % 4 == 0 && ldy % 4 == 0;
+}
+
+int grid_for_rows(int64_t rows) {
+    DeviceInfo di;
+    const int sms = current_device_info(&di) == REPOPS_OK ? di.sms : 152;
+    return int(std::min<int64_t>(rows, int64_t(sms) * 32));
+}
+
+// kind 0 = softmax, 1 = LayerNorm, 2 = RMSNorm
+template <int T, int R>
+int launch_fast(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma,
+                const float *beta, float eps, float *y, int64_t ldy, cudaStream_t s) {
+    const int grid = grid_for_rows(rows);
+    const int vec = rows_vec_ok(x, ldx, y, ldy);
+    const int pvec = reinterpret_cast<uintptr_t>(gamma) % 16 == 0 && reinterpret_cast<uintptr_t>(beta) % 16 == 0;
+    if (kind == 0) softmax_rows_kernel<T, R><<<grid, T, 0, s>>>(rows, n, x, ldx, y, ldy, vec);
+    else if (kind == 1)
+        layernorm_rows_kernel<T, R><<<grid, T, 0, s>>>(rows, n, x, ldx, gamma, beta, eps, y, ldy, vec, pvec);
+    else rmsnorm_rows_kernel<T, R><<<grid, T, 0, s>>>(rows, n, x, ldx, gamma, eps, y, ldy, vec, pvec);
+    return check_launch();
+}
+
+int run_rows(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma, const float *beta,
+             float eps, float *y, int64_t ldy, cudaStream_t s) {
+    const int64_t runs = (n + RUN - 1) / RUN;
+    // threads per row: enough for one run each up to 256, then up to 4 runs per thread
+    if (runs <= 32) return launch_fast<32, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    if (runs <= 64) return launch_fast<64, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    if (runs <= 128) return launch_fast<128, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    if (runs <= 256) return launch_fast<256, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    if (runs <= 512) return launch_fast<256, 2>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    if (runs <= MAX_FAST_RUNS) return launch_fast<256, 4>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(rows_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    rows_generic_kernel<<<grid_for_rows(rows), 256, smem, s>>>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy);
+    return check_launch();
+}
+
+}  // namespace
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" int repops_softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
+                                       int64_t ldy, cudaStream_t stream) {
+    int rc = check_rows(rows, cols, x, ldx, y, ldy);
+    if (rc != REPOPS_OK || rows == 0 || cols == 0) return rc;
+    return run_rows(0, rows, cols, x, ldx, nullptr, nullptr, 0.0f, y, ldy, stream);
+}
+
+extern "C" int repops_layernorm_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                                         const float *gamma, const float *beta, float eps, float *y, int64_t ldy,
+                                         cudaStream_t stream) {
+    int rc = check_rows(rows, cols, x, ldx, y, ldy);
+    if (rc != REPOPS_OK || rows == 0 || cols == 0) return rc;
+    if (!gamma || !beta) return REPOPS_ERR_INVALID_ARG;
+    const uint64_t yb = uint64_t((rows - 1) * ldy + cols) * 4u;
+    if (ranges_overlap(gamma, uint64_t(cols) * 4u, y, yb) || ranges_overlap(beta, uint64_t(cols) * 4u, y, yb))
+        return REPOPS_ERR_ALIAS;
+    return run_rows(1, rows, cols, x, ldx, gamma, beta, eps, y, ldy, stream);
+}
+
+extern "C" int repops_rmsnorm_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                                       const float *gamma, float eps, float *y, int64_t ldy, cudaStream_t stream) {
+    int rc = check_rows(rows, cols, x, ldx, y, ldy);
+    if (rc != REPOPS_OK || rows == 0 || cols == 0) return rc;
+    if (!gamma) return REPOPS_ERR_INVALID_ARG;
+    const uint64_t yb = uint64_t((rows - 1) * ldy + cols) * 4u;
+    if (ranges_overlap(gamma, uint64_t(cols) * 4u, y, yb)) return REPOPS_ERR_ALIAS;
+    return run_rows(2, rows, cols, x, ldx, gamma, nullptr, eps, y, ldy, stream);
+}
+
+extern "C" int repops_gelu_f32(int64_t n, const float *x, float *y, cudaStream_t stream) {
+    if (n < 0) return REPOPS_ERR_INVALID_ARG;
+    if (n == 0) return REPOPS_OK;
+    if (!x || !y || n > INT64_MAX / 4) return REPOPS_ERR_INVALID_ARG;
+    if (x != y && ranges_overlap(x, uint64_t(n) * 4u, y, uint64_t(n) * 4u)) return REPOPS_ERR_ALIAS;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != REPOPS_OK) return rc;
+    const int vec = reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(y) % 16 == 0;
+    const int64_t per = vec ? (n + 3) / 4 : n;
+    const int grid = int(std::min<int64_t>((per + 255) / 256, int64_t(di.sms) * 8));
+    gelu_kernel<<<std::max(grid, 1), 256, 0, stream>>>(n, x, y, vec);
+    return check_launch();
+}
