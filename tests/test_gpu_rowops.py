@@ -115,3 +115,40 @@ def test_decoder_sized_workloads_sampled(rp, orc):
     P = rp.softmax_rows(S)
     srows = [0, 4095, 4096, 8 * T - 1]
     assert np.array_equal(u32(P[srows].cpu().numpy()), u32(orc.softmax_rows(S[srows].cpu().numpy())))
+
+
+# ragged column counts on 16-byte aligned rows (ld a multiple of 4): the staged
+# kernels with a partial last chunk and a partial last run, at every shape
+@pytest.mark.parametrize("cols,pad", [(33, 3), (1001, 3), (8193, 3), (16385, 3), (32767, 1)])
+def test_staged_rows_with_ragged_columns(rp, orc, cols, pad):
+    x = rows_input(3, cols, 7000 + cols, 2.0, pad=pad)
+    xh = x.cpu().numpy()
+    assert np.array_equal(u32(rp.softmax_rows(x).cpu().numpy()), u32(orc.softmax_rows(xh)))
+    g = inputs.normal((cols,), 1.0, 8, DEV)
+    b = inputs.normal((cols,), 1.0, 9, DEV)
+    assert np.array_equal(u32(rp.layernorm_rows(x, g, b, 1e-5).cpu().numpy()),
+                          u32(orc.layernorm_rows(xh, g.cpu().numpy(), b.cpu().numpy(), 1e-5)))
+    assert np.array_equal(u32(rp.rmsnorm_rows(x, g, 1e-6).cpu().numpy()),
+                          u32(orc.rmsnorm_rows(xh, g.cpu().numpy(), 1e-6)))
+
+
+# gamma and beta that are not 16-byte aligned are read per element instead of
+# being staged in shared memory: same bits
+@pytest.mark.parametrize("cols", [64, 2048, 12000])
+def test_norms_with_unaligned_parameters(rp, orc, cols):
+    x = rows_input(4, cols, 8000 + cols, 2.0)
+    gb = inputs.normal((2, cols + 1), 1.0, 10, DEV)
+    g, b = gb[0, 1:], gb[1, 1:]
+    xh, gh, bh = x.cpu().numpy(), g.cpu().numpy(), b.cpu().numpy()
+    assert np.array_equal(u32(rp.layernorm_rows(x, g, b, 1e-5).cpu().numpy()),
+                          u32(orc.layernorm_rows(xh, gh, bh, 1e-5)))
+    assert np.array_equal(u32(rp.rmsnorm_rows(x, g, 1e-6).cpu().numpy()), u32(orc.rmsnorm_rows(xh, gh, 1e-6)))
+
+
+# many more rows than resident CTAs: every CTA strides over rows with the
+# next row's copy in flight
+def test_persistent_row_loop(rp, orc):
+    x = rows_input(5000, 256, 9000, 3.0)
+    y = rp.softmax_rows(x)
+    pick = [0, 1, 1215, 1216, 2431, 4999]
+    assert np.array_equal(u32(y[pick].cpu().numpy()), u32(orc.softmax_rows(x[pick].cpu().numpy())))

@@ -126,6 +126,14 @@ __device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t 
                  : "memory");
 }
 
+// 16-byte asynchronous global->shared copy bypassing L1; bytes past
+// src_bytes (0..16) are written as zeros.  Both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }

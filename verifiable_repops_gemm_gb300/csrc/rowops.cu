@@ -21,10 +21,15 @@
 //     applied to each element by one multiplication; products and sums never
 //     fuse.
 //
-// Kernels: one CTA per row.  Each thread owns whole runs (R runs of 32 values,
-// in registers), folds them, and the run results go through shared memory for
-// the upper tree levels; the row is read once and written once.  Rows longer
-// than 32 * 256 * 4 values use a kernel that re-reads the row for each phase.
+// Kernels: one CTA per row, persistent over rows.  Each thread owns whole runs
+// (R runs of 32 values, in registers) and folds them; a warp folds its 32 run
+// results by shuffles, and the group results meet in shared memory after one
+// barrier per reduction; the row is read once and written once.  Aligned rows move between HBM and registers through a
+// shared-memory stage: each warp copies its 32 consecutive runs (4 KB) with
+// coalesced 16-byte cp.async, each lane then reads its own run; the next row's
+// copy is in flight while the current row is reduced.  Outputs leave the same
+// way.  Rows longer than 32 * 256 * 4 values, and rows that are not 16-byte
+// aligned, use a kernel that re-reads the row for each phase.
 #include <algorithm>
 
 #include "internal.cuh"
@@ -59,9 +64,11 @@ __device__ float exp_fixed(float x) {
     p = __fadd_rn(__fmul_rn(p, r), 0.5f);
     p = __fadd_rn(__fmul_rn(p, r), 1.0f);
     p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    if (k > 127) return __fmul_rn(__fmul_rn(p, pow2i(127)), pow2i(k - 127));
-    if (k < -126) return __fmul_rn(__fmul_rn(p, pow2i(k + 64)), pow2i(-64));
-    return __fmul_rn(p, pow2i(k));
+    // p * 2^k as (p * 2^k1) * 2^k2: k1 = 127, k2 = k - 127 above the normal
+    // range; k1 = k + 64, k2 = -64 below it (one rounding, at the end); else
+    // k1 = k and the second factor is 1 (exact).  Selects, not branches.
+    const int k2 = k > 127 ? k - 127 : (k < -126 ? -64 : 0);
+    return __fmul_rn(__fmul_rn(p, pow2i(k - k2)), pow2i(k2));
 }
 
 __device__ float erfc_pos(float z) {
@@ -132,57 +139,54 @@ struct RowRuns {
     float v[R][RUN];
     int len[R];   // values in each run (0 when the run is past the end)
 
-    __device__ __forceinline__ void load(const float *__restrict__ row, int64_t n, bool vec) {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
-            len[j] = s < n ? int(imin64(RUN, n - s)) : 0;
-            if (vec && len[j] == RUN) {
-                const float4 *p = reinterpret_cast<const float4 *>(row + s);
-#pragma unroll
-                for (int q = 0; q < RUN / 4; ++q) {
-                    const float4 w = __ldcs(p + q);
-                    v[j][4 * q] = w.x; v[j][4 * q + 1] = w.y; v[j][4 * q + 2] = w.z; v[j][4 * q + 3] = w.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < RUN; ++i) v[j][i] = i < len[j] ? row[s + i] : 0.0f;
-            }
-        }
-    }
-
-    __device__ __forceinline__ void store(float *__restrict__ row, bool vec) const {
-#pragma unroll
-        for (int j = 0; j < R; ++j) {
-            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
-            if (vec && len[j] == RUN) {
-                float4 *p = reinterpret_cast<float4 *>(row + s);
-#pragma unroll
-                for (int q = 0; q < RUN / 4; ++q)
-                    __stcs(p + q, make_float4(v[j][4 * q], v[j][4 * q + 1], v[j][4 * q + 2], v[j][4 * q + 3]));
-            } else {
-#pragma unroll
-                for (int i = 0; i < RUN; ++i)
-                    if (i < len[j]) row[s + i] = v[j][i];
-            }
-        }
-    }
-
-    // Folds each run (of f(value)) left to right into buf[run index]; returns
-    // the tree's root over the whole row.
+    // The tree's root over the row, to every thread.  Each thread folds its
+    // runs (of f(value)) left to right; a group of 32 consecutive runs is one
+    // warp's lanes for one j, and every lane folds the group's run results left
+    // to right by shuffles; lane 0 posts the group result and, after one
+    // barrier, every thread folds the (at most 32) group results left to right.
+    // gbuf: two halves of 32 floats, alternated through `phase`, so that a
+    // thread still reading one reduction's half never races the next one's
+    // writes.
     template <Op OP, class F>
-    __device__ __forceinline__ float reduce(F f, float *buf, float *buf2, int runs, float *bcast) const {
+    __device__ __forceinline__ float reduce(F f, float (*gbuf)[RUN], int &phase, int runs) const {
+        constexpr int GROUPS = T * R / RUN;
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        float *gb = gbuf[phase];
+        phase ^= 1;
+        float root = 0.0f;
 #pragma unroll
         for (int j = 0; j < R; ++j) {
-            if (len[j] > 0) {
-                float acc = f(v[j][0]);
+            const int u0 = j * T + warp * RUN;   // the group's first run
+            if (u0 >= runs) continue;           // warp-uniform
+            // a lane past the row end folds garbage that the group fold skips
+            float acc = f(v[j][0]);
+            if (len[j] == RUN) {
+#pragma unroll
+                for (int i = 1; i < RUN; ++i) acc = combine<OP>(acc, f(v[j][i]));
+            } else {
 #pragma unroll
                 for (int i = 1; i < RUN; ++i)
                     if (i < len[j]) acc = combine<OP>(acc, f(v[j][i]));
-                buf[threadIdx.x + j * T] = acc;
             }
+            const int have = runs - u0;         // runs present in the group, >= 1
+            float g = __shfl_sync(0xffffffffu, acc, 0);
+#pragma unroll
+            for (int i = 1; i < RUN; ++i) {
+                const float o = __shfl_sync(0xffffffffu, acc, i);
+                if (i < have) g = combine<OP>(g, o);
+            }
+            if constexpr (GROUPS == 1) root = g;
+            else if (lane == 0) gb[j * (T / RUN) + warp] = g;
         }
-        return tree_upper<OP>(buf, buf2, runs, bcast);
+        if constexpr (GROUPS == 1) {
+            return root;
+        } else {
+            __syncthreads();
+            const int G = (runs + RUN - 1) / RUN;
+            float r = gb[0];
+            for (int k = 1; k < G; ++k) r = combine<OP>(r, gb[k]);
+            return r;
+        }
     }
 };
 
@@ -203,6 +207,145 @@ __device__ __forceinline__ void load_run(const float *__restrict__ p, int64_t s,
     }
 }
 
+// ------------------------------------------------ shared-memory stage ----
+
+// Run u of a row occupies 128 bytes of the stage at u*128; its 16-byte chunk c
+// sits in slot c ^ (u & 7).  Eight consecutive lanes then hit eight different
+// bank groups both when they copy eight consecutive chunks of one run and when
+// each reads the same chunk of its own run.
+__device__ __forceinline__ int stage_slot(int u, int c) { return u * 8 + (c ^ (u & 7)); }
+
+// Starts the copy of the row's runs [0, T*R) into the stage; each warp copies
+// the runs its own lanes own (so only __syncwarp is needed before reading).
+template <int T, int R>
+__device__ __forceinline__ void stage_in(float4 *stage, const float *__restrict__ row, int64_t n) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int u0 = j * T + warp * 32;
+        if (int64_t(u0) * RUN >= n) continue;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int g = k * 32 + lane, u = u0 + (g >> 3), c = g & 7;
+            const int64_t f = int64_t(u) * RUN + 4 * c;
+            if (f < n) cp_async_16(stage + stage_slot(u, c), row + f, uint32_t(imin64(4, n - f)) * 4u);
+        }
+    }
+}
+
+// Stores the row's first n values from the stage with coalesced 16-byte stores.
+template <int T, int R>
+__device__ __forceinline__ void stage_out(const float4 *stage, float *__restrict__ row, int64_t n) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int u0 = j * T + warp * 32;
+        if (int64_t(u0) * RUN >= n) continue;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int g = k * 32 + lane, u = u0 + (g >> 3), c = g & 7;
+            const int64_t f = int64_t(u) * RUN + 4 * c;
+            if (f >= n) continue;
+            const float4 w = stage[stage_slot(u, c)];
+            if (f + 4 <= n) {
+                __stcs(reinterpret_cast<float4 *>(row + f), w);
+            } else {
+                row[f] = w.x;
+                if (f + 1 < n) row[f + 1] = w.y;
+                if (f + 2 < n) row[f + 2] = w.z;
+            }
+        }
+    }
+}
+
+template <int T, int R>
+__device__ __forceinline__ void read_stage(RowRuns<T, R> &rr, const float4 *stage, int64_t n) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        const int u = threadIdx.x + j * T;
+        const int64_t s = int64_t(u) * RUN;
+        rr.len[j] = s < n ? int(imin64(RUN, n - s)) : 0;
+        if (rr.len[j] == 0) continue;
+#pragma unroll
+        for (int c = 0; c < RUN / 4; ++c) {
+            const float4 w = stage[stage_slot(u, c)];
+            rr.v[j][4 * c] = w.x; rr.v[j][4 * c + 1] = w.y; rr.v[j][4 * c + 2] = w.z; rr.v[j][4 * c + 3] = w.w;
+        }
+    }
+}
+
+template <int T, int R>
+__device__ __forceinline__ void write_stage(const RowRuns<T, R> &rr, float4 *stage) {
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+        if (rr.len[j] == 0) continue;
+        const int u = threadIdx.x + j * T;
+#pragma unroll
+        for (int c = 0; c < RUN / 4; ++c)
+            stage[stage_slot(u, c)] =
+                make_float4(rr.v[j][4 * c], rr.v[j][4 * c + 1], rr.v[j][4 * c + 2], rr.v[j][4 * c + 3]);
+    }
+}
+
+// A per-column vector (gamma, beta) staged once per CTA in the same layout,
+// read back one run at a time.
+template <int T, int R>
+__device__ __forceinline__ void read_param_run(const float4 *pstage, int u, float (&out)[RUN]) {
+#pragma unroll
+    for (int c = 0; c < RUN / 4; ++c) {
+        const float4 w = pstage[stage_slot(u, c)];
+        out[4 * c] = w.x; out[4 * c + 1] = w.y; out[4 * c + 2] = w.z; out[4 * c + 3] = w.w;
+    }
+}
+
+// Two stages (the next row's copy overlaps this row's work) while they fit in
+// 128 KB; one beyond.
+template <int T, int R>
+constexpr bool kPrefetch = T * R <= 512;
+template <int T, int R>
+constexpr size_t kStageBytes = size_t(T) * R * RUN * sizeof(float) * (kPrefetch<T, R> ? 2 : 1);
+// NP per-column vectors staged after the row stages when all fit in 200 KB.
+template <int T, int R, int NP>
+constexpr size_t kParamBytes =
+    kStageBytes<T, R> + size_t(NP) * T * R * RUN * sizeof(float) <= 200 * 1024 ? size_t(NP) * T * R * RUN * 4 : 0;
+
+// The row loop shared by the three row kernels: body(rr) turns the row's
+// values in rr into its outputs.  x, y and their leading dimensions are
+// 16-byte aligned (other rows take the long-row kernel).
+template <int T, int R, class Body>
+__device__ __forceinline__ void for_each_row(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
+                                             float *__restrict__ y, int64_t ldy, Body body) {
+    extern __shared__ float4 stage_mem[];
+    constexpr bool PF = kPrefetch<T, R>;
+    float4 *in = stage_mem;
+    float4 *out = PF ? stage_mem + T * R * RUN / 4 : stage_mem;
+    int64_t row = blockIdx.x;
+    if (row < rows) stage_in<T, R>(in, x + row * ldx, n);
+    cp_async_commit();
+    for (; row < rows; row += gridDim.x) {
+        const int64_t next = row + gridDim.x;
+        cp_async_wait<0>();
+        __syncwarp();
+        RowRuns<T, R> rr;
+        read_stage(rr, in, n);
+        if constexpr (PF) {
+            __syncwarp();                       // every lane has its run before `in` is refilled
+            if (next < rows) stage_in<T, R>(in, x + next * ldx, n);
+            cp_async_commit();
+        }
+        body(rr);
+        write_stage(rr, out);
+        __syncwarp();
+        stage_out<T, R>(out, y + row * ldy, n);
+        __syncwarp();                           // `out` read back before it is written again
+        if constexpr (!PF) {
+            if (next < rows) stage_in<T, R>(in, x + next * ldx, n);
+            cp_async_commit();
+        }
+    }
+    cp_async_wait<0>();
+}
+
 struct Ident {
     __device__ __forceinline__ float operator()(float x) const { return x; }
 };
@@ -213,93 +356,94 @@ struct Square {
 template <int T, int R>
 __global__ void __launch_bounds__(T)
 softmax_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx, float *__restrict__ y,
-                    int64_t ldy, int vec) {
-    __shared__ float buf[T * R];
-    __shared__ float buf2[(T * R + RUN - 1) / RUN];
-    __shared__ float bcast;
+                    int64_t ldy) {
+    __shared__ float gbuf[2][RUN];
+    int phase = 0;
     const int runs = int((n + RUN - 1) / RUN);
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        RowRuns<T, R> rr;
-        rr.load(x + row * ldx, n, vec);
-        const float m = rr.template reduce<Op::Max>(Ident(), buf, buf2, runs, &bcast);
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr) {
+        const float m = rr.template reduce<Op::Max>(Ident(), gbuf, phase, runs);
+        // element-wise steps need no guard: values past the row end are never
+        // folded or stored
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < rr.len[j]) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
-        const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), buf, buf2, runs, &bcast));
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+        const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs));
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < rr.len[j]) rr.v[j][i] = __fmul_rn(rr.v[j][i], inv);
-        rr.store(y + row * ldy, vec);
-    }
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = __fmul_rn(rr.v[j][i], inv);
+    });
 }
 
+// psm: gamma and beta are staged in shared memory (aligned, and they fit).
 template <int T, int R>
 __global__ void __launch_bounds__(T)
 layernorm_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
                       const float *__restrict__ gamma, const float *__restrict__ beta, float eps,
-                      float *__restrict__ y, int64_t ldy, int vec, int pvec) {
-    __shared__ float buf[T * R];
-    __shared__ float buf2[(T * R + RUN - 1) / RUN];
-    __shared__ float bcast;
+                      float *__restrict__ y, int64_t ldy, int pvec, int psm) {
+    extern __shared__ float4 stage_mem[];
+    __shared__ float gbuf[2][RUN];
+    int phase = 0;
     const int runs = int((n + RUN - 1) / RUN);
     const float nf = float(n);
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        RowRuns<T, R> rr;
-        rr.load(x + row * ldx, n, vec);
-        const float mean = __fdiv_rn(rr.template reduce<Op::Sum>(Ident(), buf, buf2, runs, &bcast), nf);
+    float4 *pg = stage_mem + kStageBytes<T, R> / 16, *pb = pg + T * R * RUN / 4;
+    if (kParamBytes<T, R, 2> != 0 && psm && blockIdx.x < rows) {
+        stage_in<T, R>(pg, gamma, n);   // waited for with the first row
+        stage_in<T, R>(pb, beta, n);
+    }
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr) {
+        const float mean = __fdiv_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs), nf);
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < rr.len[j]) rr.v[j][i] = __fsub_rn(rr.v[j][i], mean);
-        const float var = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), buf, buf2, runs, &bcast), nf);
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = __fsub_rn(rr.v[j][i], mean);
+        const float var = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), gbuf, phase, runs), nf);
         const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(var, eps)));
 #pragma unroll
         for (int j = 0; j < R; ++j) {
             if (rr.len[j] == 0) continue;
-            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
+            const int u = threadIdx.x + j * T;
             float g[RUN], b[RUN];
-            load_run(gamma, s, rr.len[j], pvec, g);
-            load_run(beta, s, rr.len[j], pvec, b);
+            if (kParamBytes<T, R, 2> != 0 && psm) {
+                read_param_run<T, R>(pg, u, g);
+                read_param_run<T, R>(pb, u, b);
+            } else {
+                load_run(gamma, int64_t(u) * RUN, rr.len[j], pvec, g);
+                load_run(beta, int64_t(u) * RUN, rr.len[j], pvec, b);
+            }
 #pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < rr.len[j]) rr.v[j][i] = __fadd_rn(__fmul_rn(__fmul_rn(rr.v[j][i], inv), g[i]), b[i]);
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = __fadd_rn(__fmul_rn(__fmul_rn(rr.v[j][i], inv), g[i]), b[i]);
         }
-        rr.store(y + row * ldy, vec);
-    }
+    });
 }
 
 template <int T, int R>
 __global__ void __launch_bounds__(T)
 rmsnorm_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
-                    const float *__restrict__ gamma, float eps, float *__restrict__ y, int64_t ldy, int vec,
-                    int pvec) {
-    __shared__ float buf[T * R];
-    __shared__ float buf2[(T * R + RUN - 1) / RUN];
-    __shared__ float bcast;
+                    const float *__restrict__ gamma, float eps, float *__restrict__ y, int64_t ldy, int pvec,
+                    int psm) {
+    extern __shared__ float4 stage_mem[];
+    __shared__ float gbuf[2][RUN];
+    int phase = 0;
     const int runs = int((n + RUN - 1) / RUN);
     const float nf = float(n);
-    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        RowRuns<T, R> rr;
-        rr.load(x + row * ldx, n, vec);
-        const float ms = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), buf, buf2, runs, &bcast), nf);
+    float4 *pg = stage_mem + kStageBytes<T, R> / 16;
+    if (kParamBytes<T, R, 1> != 0 && psm && blockIdx.x < rows) stage_in<T, R>(pg, gamma, n);
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr) {
+        const float ms = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), gbuf, phase, runs), nf);
         const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
 #pragma unroll
         for (int j = 0; j < R; ++j) {
             if (rr.len[j] == 0) continue;
-            const int64_t s = int64_t(threadIdx.x + j * T) * RUN;
+            const int u = threadIdx.x + j * T;
             float g[RUN];
-            load_run(gamma, s, rr.len[j], pvec, g);
+            if (kParamBytes<T, R, 1> != 0 && psm) read_param_run<T, R>(pg, u, g);
+            else load_run(gamma, int64_t(u) * RUN, rr.len[j], pvec, g);
 #pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < rr.len[j]) rr.v[j][i] = __fmul_rn(__fmul_rn(rr.v[j][i], inv), g[i]);
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = __fmul_rn(__fmul_rn(rr.v[j][i], inv), g[i]);
         }
-        rr.store(y + row * ldy, vec);
-    }
+    });
 }
 
 // ------------------------------------------------------ long rows ----
@@ -411,24 +555,45 @@ int grid_for_rows(int64_t rows) {
     return int(std::min<int64_t>(rows, int64_t(sms) * 32));
 }
 
+// Launches `kern` with as many CTAs as fit on the device at once (at most one
+// per row); each CTA then strides over the rows.
+template <class Kern, class... Args>
+int launch_persistent(Kern kern, int threads, size_t smem, int64_t rows, cudaStream_t s, Args... args) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    DeviceInfo di;
+    const int sms = current_device_info(&di) == REPOPS_OK ? di.sms : 152;
+    const int grid = int(std::min<int64_t>(rows, int64_t(std::max(per_sm, 1)) * sms));
+    kern<<<grid, threads, smem, s>>>(args...);
+    return check_launch();
+}
+
 // kind 0 = softmax, 1 = LayerNorm, 2 = RMSNorm
 template <int T, int R>
 int launch_fast(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma,
                 const float *beta, float eps, float *y, int64_t ldy, cudaStream_t s) {
-    const int grid = grid_for_rows(rows);
-    const int vec = rows_vec_ok(x, ldx, y, ldy);
     const int pvec = reinterpret_cast<uintptr_t>(gamma) % 16 == 0 && reinterpret_cast<uintptr_t>(beta) % 16 == 0;
-    if (kind == 0) softmax_rows_kernel<T, R><<<grid, T, 0, s>>>(rows, n, x, ldx, y, ldy, vec);
-    else if (kind == 1)
-        layernorm_rows_kernel<T, R><<<grid, T, 0, s>>>(rows, n, x, ldx, gamma, beta, eps, y, ldy, vec, pvec);
-    else rmsnorm_rows_kernel<T, R><<<grid, T, 0, s>>>(rows, n, x, ldx, gamma, eps, y, ldy, vec, pvec);
-    return check_launch();
+    const size_t smem = kStageBytes<T, R>;
+    if (kind == 0) return launch_persistent(softmax_rows_kernel<T, R>, T, smem, rows, s, rows, n, x, ldx, y, ldy);
+    if (kind == 1) {
+        const size_t p = pvec ? kParamBytes<T, R, 2> : 0;
+        return launch_persistent(layernorm_rows_kernel<T, R>, T, smem + p, rows, s, rows, n, x, ldx, gamma, beta,
+                                 eps, y, ldy, pvec, int(p != 0));
+    }
+    const size_t p = pvec ? kParamBytes<T, R, 1> : 0;
+    return launch_persistent(rmsnorm_rows_kernel<T, R>, T, smem + p, rows, s, rows, n, x, ldx, gamma, eps, y, ldy,
+                             pvec, int(p != 0));
 }
 
 int run_rows(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma, const float *beta,
              float eps, float *y, int64_t ldy, cudaStream_t s) {
-    const int64_t runs = (n + RUN - 1) / RUN;
+    int64_t runs = (n + RUN - 1) / RUN;
     // threads per row: enough for one run each up to 256, then up to 4 runs per thread
+    // rows that are not 16-byte aligned take the long-row kernel (same bits)
+    if (!rows_vec_ok(x, ldx, y, ldy)) runs = MAX_FAST_RUNS + 1;
     if (runs <= 32) return launch_fast<32, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
     if (runs <= 64) return launch_fast<64, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
     if (runs <= 128) return launch_fast<128, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
