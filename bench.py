@@ -479,10 +479,11 @@ def run_ours(args):
 
 
 def run_sweep(args):
-    """One JSON line per GEMM workload: the 256^3 case, the square sweep with B
-    row- and column-major, the ragged 4097x1023x3001 case, and the 15 GEMMs of
-    the decoder-layer set.  Each timed launch is bracketed by its own CUDA
-    events and preceded by an L2 flush (a 256 MiB write)."""
+    """One JSON line per workload.  GEMM: the 256^3 case, the square sweep with
+    B row- and column-major, the ragged 4097x1023x3001 case, and the 15 GEMMs
+    of the decoder-layer set; then the row operators and the commitments.
+    Each timed launch is bracketed by its own CUDA events and preceded by an L2
+    flush (a 256 MiB write).  `args.sweep` picks one part or all of them."""
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     rp.load()
@@ -491,6 +492,15 @@ def run_sweep(args):
     peak = sms * FP32_LANES_PER_SM * peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL) * 1e6 / 1e12
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream(device=dev)
+    if args.sweep in ("all", "gemm"):
+        run_sweep_gemm(dev, s, flush, peak)
+    if args.sweep in ("all", "rowops"):
+        run_sweep_rowops(dev, s, flush, peaks.get("hbm_gbs", 6800.0))
+    if args.sweep in ("all", "commitments"):
+        run_sweep_commitments(dev, s, flush)
+
+
+def run_sweep_gemm(dev, s, flush, peak):
 
     def timed(A, B, C):
         M, K = A.shape
@@ -550,8 +560,6 @@ def run_sweep(args):
     print(json.dumps({"sweep": "decoder layer set, 15 GEMMs", "ms": tot_ms, "tflops": tot_f / tot_ms / 1e9,
                       "frac_of_fp32_peak": tot_f / tot_ms / 1e9 / peak}), flush=True)
     del X, Xin, W, dY
-    run_sweep_rowops(dev, s, flush, measured_peaks()[0].get("hbm_gbs", 6800.0))
-    run_sweep_commitments(dev, s, flush)
 
 
 def run_sweep_rowops(dev, s, flush, hbm):
@@ -660,8 +668,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--sweep", action="store_true",
-                    help="time every GEMM workload (one JSON line each) instead of the step")
+    ap.add_argument("--sweep", nargs="?", const="all", default=None,
+                    choices=("all", "gemm", "rowops", "commitments"),
+                    help="time every workload of a part (one JSON line each) instead of the step")
     args = ap.parse_args()
     if args.sweep:
         run_sweep(args)

@@ -52,8 +52,12 @@ __device__ float exp_fixed(float x) {
     if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
     if (x < -103.972084045410156f) return 0.0f;
     const float t = __fmul_rn(x, 1.44269502162933349609375f);
-    const float kf = rintf(t);
-    const int k = int(kf);
+    // k = rint(t), ties to even: adding 1.5 * 2^23 leaves rint(t) in the low
+    // mantissa bits (exact for |t| < 2^22; past the checks above |t| < 151),
+    // and subtracting it back is exact
+    const float big = __fadd_rn(t, 12582912.0f);
+    const float kf = __fsub_rn(big, 12582912.0f);
+    const int k = __float_as_int(big) - 0x4B400000;
     float r = __fsub_rn(x, __fmul_rn(kf, 0.693145751953125f));
     r = __fsub_rn(r, __fmul_rn(kf, 1.428606765330187045037746e-06f));
     float p = 1.98412701e-04f;
