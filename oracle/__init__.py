@@ -97,6 +97,9 @@ def lib():
         L.oracle_layernorm_rows.argtypes = [i64, i64, vp, i64, vp, vp, f32, vp, i64]
         L.oracle_rmsnorm_rows.restype = None
         L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64]
+        L.oracle_gemm_batched.restype = None
+        L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
+                                          vp, i64, i64, f32, vp, i32, vp, i64, i64]
         if L.oracle_fp_env_ok() != 1:
             raise RuntimeError("host floating-point environment flushes subnormals "
                                "or does not round to nearest even; the oracle "
@@ -342,3 +345,22 @@ def rmsnorm_rows(x, gamma, eps: float) -> np.ndarray:
     lib().oracle_rmsnorm_rows(a.shape[0], a.shape[1], _ptr(a), lda, _ptr(g), ctypes.c_float(eps),
                               _ptr(y), a.shape[1])
     return y
+
+
+ACT_NONE, ACT_GELU = 0, 1
+
+
+def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, strideB,
+                 C, ldc, strideC, alpha=1.0, bias=None, act=ACT_NONE, R=None, ldr=0, strideR=0):
+    """Batched GEMM with the fused epilogue, on flat float32 buffers (element
+    offsets and strides exactly as the library's batched entry point takes
+    them).  C is written in place; R may be C itself."""
+    L = lib()
+    for X in (A, B, C) + tuple(x for x in (bias, R) if x is not None):
+        if X.dtype != np.float32 or not X.flags.c_contiguous:
+            raise TypeError("flat contiguous float32 buffers expected")
+    L.oracle_gemm_batched(int(bool(transA)), int(bool(transB)), batch, M, N, K,
+                          _ptr(A), lda, strideA, _ptr(B), ldb, strideB, _ptr(C), ldc, strideC,
+                          float(alpha), _ptr(bias) if bias is not None else None, int(act),
+                          _ptr(R) if R is not None else None, ldr, strideR)
+    return C

@@ -39,7 +39,9 @@
  *  - the hash is SHA-256; leaf = SHA256(0x00 || leaf bytes), node =
  *    SHA256(0x01 || left || right); leaves cut from the tensor bytes in
  *    increasing offset, the last one possibly short; level by level, pairs
- *    (0,1),(2,3),...; an unpaired last node is promoted unchanged.
+ *    (0,1),(2,3),...; an unpaired last node is promoted unchanged;
+ *  - a GEMM epilogue runs after the whole k-chain of its element:
+ *    y = alpha*acc, then + bias[j], then GeLU, then + residual, each rounded.
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -687,4 +689,50 @@ void oracle_rmsnorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx
         for (int64_t j = 0; j < cols; ++j) y[i * ldy + j] = (xr[j] * inv) * gamma[j];
     }
     free(v);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Batched GEMM with a fused epilogue  [RepOps §3.2 matmul example for the   */
+/* k-chain; §4.3 (GeLU behind DistilBERT's overhead).  The pages fix no      */
+/* epilogue; this is the library's definition.]                             */
+/* ------------------------------------------------------------------------ */
+
+/* For b = 0 .. batch-1, with X_b = X + b*strideX for every operand:
+ *   acc  = the k-chain of oracle_gemm_f32 for element (i, j) of A_b * B_b;
+ *   y    = alpha * acc;
+ *   y    = y + bias[j]                  (when bias is not NULL);
+ *   y    = GeLU(y)                      (when act == 1);
+ *   y    = y + R_b[i*ldr + j]           (when R is not NULL);
+ *   C_b[i*ldc + j] = y.
+ * Every step is one binary32 rounding.  R may be C itself (same ld and
+ * stride): each element reads its residual before it is overwritten. */
+void oracle_gemm_batched(int transA, int transB, int64_t batch, int64_t M, int64_t N, int64_t K,
+                         const float *A, int64_t lda, int64_t strideA,
+                         const float *B, int64_t ldb, int64_t strideB,
+                         float *C, int64_t ldc, int64_t strideC,
+                         float alpha, const float *bias, int act,
+                         const float *R, int64_t ldr, int64_t strideR)
+{
+    for (int64_t b = 0; b < batch; ++b) {
+        const float *Ab = A + b * strideA;
+        const float *Bb = B + b * strideB;
+        float *Cb = C + b * strideC;
+        const float *Rb = R ? R + b * strideR : NULL;
+        for (int64_t i = 0; i < M; ++i) {
+            for (int64_t j = 0; j < N; ++j) {
+                float acc = 0.0f;
+                for (int64_t kk = 0; kk < K; ++kk) {
+                    float a = transA ? Ab[kk * lda + i] : Ab[i * lda + kk];
+                    float bv = transB ? Bb[j * ldb + kk] : Bb[kk * ldb + j];
+                    float p = a * bv;
+                    acc = acc + p;
+                }
+                float y = alpha * acc;
+                if (bias) y = y + bias[j];
+                if (act == 1) y = oracle_gelu(y);
+                if (Rb) y = y + Rb[i * ldr + j];
+                Cb[i * ldc + j] = y;
+            }
+        }
+    }
 }

@@ -14,7 +14,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "repops_oracle.c")
 PINS = [os.path.join(ROOT, "tests", f) for f in
-        ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py", "test_oracle_rowops.py")]
+        ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py", "test_oracle_rowops.py",
+         "test_oracle_epilogue.py")]
 
 MUTATIONS = {
     "gemm: fused multiply-add": (
@@ -59,6 +60,17 @@ MUTATIONS = {
     "rmsnorm: divide each element": ("y[i * ldy + j] = (xr[j] * inv) * gamma[j];",
                                      "y[i * ldy + j] = (xr[j] / sqrtf(ms + eps)) * gamma[j];"),
     "softmax: divide each element": ("y[i * ldy + j] = e[j] * inv;", "y[i * ldy + j] = e[j] / s;"),
+    "epilogue: bias before alpha": ("float y = alpha * acc;\n                if (bias) y = y + bias[j];",
+                                    "float y = acc;\n                if (bias) y = y + bias[j];\n"
+                                    "                y = alpha * y;"),
+    "batched: k in decreasing order": ("for (int64_t kk = 0; kk < K; ++kk) {",
+                                       "for (int64_t kk = K - 1; kk >= 0; --kk) {"),
+    "batched: acc starts at -0": ("float acc = 0.0f;", "float acc = -0.0f;"),
+    "batched: fused multiply-add": ("float p = a * bv;\n                    acc = acc + p;",
+                                    "acc = __builtin_fmaf(a, bv, acc);"),
+    "epilogue: residual before GeLU": ("if (act == 1) y = oracle_gelu(y);\n                if (Rb) y = y + Rb[i * ldr + j];",
+                                       "if (Rb) y = y + Rb[i * ldr + j];\n                if (act == 1) y = oracle_gelu(y);"),
+    "batched: A advanced by B's stride": ("const float *Ab = A + b * strideA;", "const float *Ab = A + b * strideB;"),
 }
 
 
