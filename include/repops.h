@@ -155,6 +155,53 @@ int repops_gemm_config_info(int config, int *bm, int *bn, int *threads,
 int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
 
 /* ------------------------------------------------------------------------ */
+/* Batched GEMM with a fused epilogue                                        */
+/* "Verde与RepOps" §3.2 matmul example (the k-chain); §4.3 (GeLU among the   */
+/* operators behind DistilBERT's overhead).  The pages fix no epilogue; this */
+/* is the library's definition.                                              */
+/* ------------------------------------------------------------------------ */
+
+#define REPOPS_ACT_NONE 0
+#define REPOPS_ACT_GELU 1   /* the order-fixed GeLU of repops_gelu_f32 */
+
+/* For b = 0 .. batch-1, with X_b = X + b*strideX (elements) for A, B, C, R:
+ *
+ *   acc = the k-chain of repops_gemm_f32 for element (i, j) of A_b * B_b
+ *   y   = fl(alpha * acc)
+ *   y   = fl(y + bias[j])          if bias != NULL   (device, N values, shared)
+ *   y   = GeLU(y)                  if act == REPOPS_ACT_GELU
+ *   y   = fl(y + R_b[i*ldr + j])   if R != NULL      (device)
+ *   C_b[i*ldc + j] = y
+ *
+ * The epilogue runs after the element's whole k-chain, so the bits equal
+ * those of repops_gemm_f32 followed by the separate element-wise steps.
+ * Storage of A_b and B_b as in repops_gemm_f32_ex (transA, transB).  A stride
+ * of 0 shares one operand between all batches (e.g. one weight matrix); a
+ * stride smaller than a matrix interleaves the batches (attention heads as
+ * column blocks of one row-major matrix: head h at column h*d, stride d).
+ * The outputs C_b must not overlap one another: stacked (strideC at least one
+ * C span) or interleaved within one row pitch ((batch-1)*strideC + N <= ldc,
+ * strideC >= N); otherwise ALIAS.  R may be C itself (same ld and stride):
+ * every element reads its residual before writing it; any other overlap of C
+ * with A, B, bias or R is ALIAS.  K == 0 gives the epilogue of +0.
+ * config / loader: as repops_gemm_f32_config (-1 / REPOPS_LOADER_AUTO for the
+ * automatic choice); the bits do not depend on them.  TMA needs, besides its
+ * repops_gemm_f32_config rule, batch strides of A and B that are multiples
+ * of 4 elements.  No scratch memory is taken.
+ * Errors: INVALID_ARG (negative size or stride, bad leading dim, null
+ * pointer with a non-empty operand, act not NONE/GELU, spans that overflow);
+ * ALIAS; UNSUPPORTED (batch > 65535, or loader TMA when TMA cannot serve the
+ * operands); CUDA. */
+int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
+                            int64_t batch, int64_t M, int64_t N, int64_t K,
+                            const float *A, int64_t lda, int64_t strideA,
+                            const float *B, int64_t ldb, int64_t strideB,
+                            float *C, int64_t ldc, int64_t strideC,
+                            float alpha, const float *bias, int act,
+                            const float *R, int64_t ldr, int64_t strideR,
+                            cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Contributor order                                                         */
 /* "Zoo Per-LLM Chain Soundness" §2 Lemma "Order independence within a       */
 /* batch", §5 "Ordering subroutine", §6 "contributors (sorted DID list)"     */

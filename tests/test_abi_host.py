@@ -211,3 +211,30 @@ def test_row_operators_reject_bad_arguments(L):
     assert L.repops_gelu_f32(-1, FAKE_A, FAKE_B, None) == -1
     assert L.repops_gelu_f32(8, FAKE_A, FAKE_A + 4, None) == -2
     assert L.repops_gelu_f32(0, None, None, None) == 0
+
+
+def _bat(L, batch=2, M=4, N=4, K=4, A=FAKE_A, lda=4, sA=16, B=FAKE_B, ldb=4, sB=16, C=FAKE_C, ldc=4,
+         sC=16, alpha=1.0, bias=None, act=0, R=None, ldr=4, sR=16, config=-1, loader=0, tA=0, tB=0):
+    return L.repops_gemm_f32_batched(config, loader, tA, tB, batch, M, N, K, A, lda, sA, B, ldb, sB,
+                                     C, ldc, sC, ctypes.c_float(alpha), bias, act, R, ldr, sR, None)
+
+
+def test_batched_gemm_rejects_bad_arguments(L):
+    assert _bat(L, batch=-1) == -1
+    assert _bat(L, sA=-4) == -1                                    # negative stride
+    assert _bat(L, act=2) == -1                                    # unknown activation
+    assert _bat(L, ldc=3) == -1
+    assert _bat(L, R=FAKE_B + 4096, ldr=3) == -1                   # residual ld < N
+    assert _bat(L, config=99) == -1
+    assert _bat(L, loader=7) == -1
+    assert _bat(L, A=None) == -1
+    assert _bat(L, batch=0) == 0                                   # empty: no launch
+    assert _bat(L, M=0) == 0
+    assert _bat(L, batch=70000) == -7                              # one grid row per batch
+    # outputs of two batches overlap: neither stacked nor interleaved
+    assert _bat(L, sC=8) == -2
+    assert _bat(L, sC=2, ldc=6) == -2                              # interleaved, but 2 < N
+    assert _bat(L, C=FAKE_A + 32, sA=0) == -2                      # C over A
+    assert _bat(L, bias=FAKE_C + 8) == -2                          # bias inside C
+    assert _bat(L, R=FAKE_C + 4) == -2                             # residual overlapping C, not in place
+    assert _bat(L, R=FAKE_C, sR=20, sC=16) == -2                   # same base, other stride

@@ -19,18 +19,20 @@ memory and streams.
                                     ("Zoo Per-LLM Chain Soundness" §7)
   softmax_rows / layernorm_rows /   order-fixed row operators and GeLU
   rmsnorm_rows / gelu               ("Verde与RepOps" §3.2, §4.3)
+  gemm_batched(A, B, ...)           batched GEMM with a fused epilogue
+                                    (alpha, bias, GeLU, residual)
 """
 import ctypes
 
 from . import _capi
-from ._capi import (LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA, MEAN_MAX_CONTRIBUTORS,
-                    RepopsError, load)
+from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA,
+                    MEAN_MAX_CONTRIBUTORS, RepopsError, load)
 
 __all__ = ["load", "version", "gemm", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
-           "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu",
-           "device_status", "RepopsError",
+           "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
+           "device_status", "RepopsError", "ACT_NONE", "ACT_GELU",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
 
 
@@ -86,6 +88,79 @@ def gemm(A, B, out=None, *, config: int = -1, loader: int = LOADER_AUTO, stream=
     rc = L.repops_gemm_f32_config(config, loader, ta, tb, M, N, K, pa, lda, pb, ldb,
                                   out.data_ptr(), ldc, _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32")
+    return out
+
+
+def _batched_operand(X, name):
+    """(pointer, leading dim, batch stride, transposed, batch) of a float32 CUDA
+    tensor of shape (batch, rows, cols), or (rows, cols) shared by all batches.
+    Each matrix must be row-major or a transposed view; the batch stride is
+    whatever the tensor's first stride is (0 for an expanded tensor)."""
+    import torch
+    if X.dtype != torch.float32 or X.dim() not in (2, 3) or not X.is_cuda:
+        raise TypeError("%s must be a 2-D or 3-D float32 CUDA tensor" % name)
+    if X.dim() == 2:
+        p, ld, t = _operand(X, name)
+        return p, ld, 0, t, None
+    b, r, c = X.shape
+    sb, s0, s1 = X.stride()
+    if s1 == 1 and s0 >= max(c, 1):
+        return X.data_ptr(), s0, sb, 0, b
+    if s0 == 1 and s1 >= max(r, 1):
+        return X.data_ptr(), s1, sb, 1, b
+    raise ValueError("%s: each matrix must be row-major or a transposed view" % name)
+
+
+def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = ACT_NONE,
+                 residual=None, config: int = -1, loader: int = LOADER_AUTO, stream=None):
+    """out[b] = epilogue(A[b] @ B[b]) with the order-fixed k-chain, then
+    y = alpha*acc, + bias[j], GeLU (act=ACT_GELU), + residual[b][i][j], each one
+    binary32 rounding (repops_gemm_f32_batched).
+
+    A: (batch, M, K) or (M, K) shared; B: (batch, K, N) or (K, N) shared; every
+    matrix row-major or a transposed view, batches at any stride (attention
+    heads as column blocks: X.view(T, H, d).transpose(0, 1)).  out: (batch, M,
+    N) or (M, N), unit column stride, batches stacked or interleaved.
+    residual: shaped like out; may be out itself.  bias: (N,) contiguous."""
+    import torch
+    L = load()
+    pa, lda, sa, ta, ba = _batched_operand(A, "A")
+    pb, ldb, sb, tb, bb = _batched_operand(B, "B")
+    M, K = A.shape[-2:]
+    K2, N = B.shape[-2:]
+    if K != K2:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    sizes = {x for x in (ba, bb) if x is not None}
+    if len(sizes) > 1:
+        raise ValueError("A and B have different batch sizes")
+    batch = sizes.pop() if sizes else None
+    if out is None:
+        shape = (M, N) if batch is None else (batch, M, N)
+        out = torch.empty(shape, dtype=torch.float32, device=A.device)
+    nb = 1 if batch is None else batch
+    if out.dtype != torch.float32 or tuple(out.shape[-2:]) != (M, N) or \
+            out.dim() != (2 if batch is None else 3) or (batch is not None and out.shape[0] != batch) or \
+            (N > 0 and out.stride(-1) != 1):
+        raise ValueError("out must be a float32 tensor of shape %s with unit column stride"
+                         % (((M, N) if batch is None else (batch, M, N)),))
+    ldc = max(out.stride(-2), N, 1)
+    sc = out.stride(0) if batch is not None else 0
+    pr, ldr, sr = None, 0, 0
+    if residual is not None:
+        if residual.dtype != torch.float32 or residual.shape != out.shape or \
+                (N > 0 and residual.stride(-1) != 1):
+            raise ValueError("residual must be shaped like out, float32, unit column stride")
+        pr, ldr = residual.data_ptr(), max(residual.stride(-2), N, 1)
+        sr = residual.stride(0) if batch is not None else 0
+    pbias = None
+    if bias is not None:
+        if bias.dtype != torch.float32 or bias.dim() != 1 or bias.numel() != N or not bias.is_contiguous():
+            raise ValueError("bias must be a contiguous float32 vector of N values")
+        pbias = bias.data_ptr()
+    rc = L.repops_gemm_f32_batched(config, loader, ta, tb, nb, M, N, K, pa, lda, sa, pb, ldb, sb,
+                                   out.data_ptr(), ldc, sc, ctypes.c_float(alpha), pbias, int(act),
+                                   pr, ldr, sr, _stream_handle(stream))
+    _capi.check(rc, "repops_gemm_f32_batched")
     return out
 
 

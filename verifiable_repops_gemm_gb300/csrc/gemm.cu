@@ -71,14 +71,15 @@ int occupancy_of(int dev, int c) {
 // resident consumer warps is modelled as proportionally slower; per-thread
 // efficiency falls with the thread tile (shared-memory loads per FP32
 // instruction).
-int choose_config(int64_t M, int64_t N) {
+int choose_config(int64_t M, int64_t N, int64_t batch = 1) {
     DeviceInfo di;
     if (current_device_info(&di) != REPOPS_OK || di.device < 0 || di.device >= kMaxDevices) return 0;
     double best_t = 0;
     int best = 0;
     for (int c = 0; c < kGemmConfigCount; ++c) {
         const GemmConfigInfo ci = config_info(c);
-        const double tiles = double((M + ci.bm - 1) / ci.bm) * double((N + ci.bn - 1) / ci.bn);
+        const double tiles =
+            double((M + ci.bm - 1) / ci.bm) * double((N + ci.bn - 1) / ci.bn) * double(std::max<int64_t>(batch, 1));
         const double per_sm = std::ceil(tiles / di.sms);
         const double conc = std::min<double>(occupancy_of(di.device, c), per_sm);
         const double rounds = std::ceil(per_sm / conc);
@@ -241,6 +242,90 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     return rc;
 }
 
+// Span in bytes of `batch` operands `stride` elements apart, each spanning
+// `one` bytes.
+bool batched_span(int64_t batch, int64_t stride, uint64_t one, uint64_t *bytes) {
+    if (one == 0 || batch <= 1 || stride == 0) { *bytes = one; return true; }
+    const uint64_t s = uint64_t(stride) * 4u;
+    if (uint64_t(batch - 1) > (uint64_t(INT64_MAX) - one) / s) return false;
+    *bytes = uint64_t(batch - 1) * s + one;
+    return true;
+}
+
+int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_t batch, int64_t M, int64_t N,
+                          int64_t K, const float *A, int64_t lda, int64_t strideA, const float *B, int64_t ldb,
+                          int64_t strideB, float *C, int64_t ldc, int64_t strideC, float alpha,
+                          const float *bias, int act, const float *R, int64_t ldr, int64_t strideR,
+                          cudaStream_t stream) {
+    if (batch < 0 || M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
+    if (strideA < 0 || strideB < 0 || strideC < 0 || strideR < 0) return REPOPS_ERR_INVALID_ARG;
+    if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
+    if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC)
+        return REPOPS_ERR_INVALID_ARG;
+    if (act != REPOPS_ACT_NONE && act != REPOPS_ACT_GELU) return REPOPS_ERR_INVALID_ARG;
+    const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
+    const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
+    if (lda < std::max<int64_t>(1, a_cols) || ldb < std::max<int64_t>(1, b_cols) ||
+        ldc < std::max<int64_t>(1, N) || (R && ldr < std::max<int64_t>(1, N)))
+        return REPOPS_ERR_INVALID_ARG;
+    if (batch == 0 || M == 0 || N == 0) return REPOPS_OK;
+    if (batch > 65535) return REPOPS_ERR_UNSUPPORTED;   // one grid row per batch
+    if (!C) return REPOPS_ERR_INVALID_ARG;
+    if (K > 0 && (!A || !B)) return REPOPS_ERR_INVALID_ARG;
+    uint64_t a1 = 0, b1 = 0, c1 = 0, r1 = 0, a_bytes = 0, b_bytes = 0, c_bytes = 0, r_bytes = 0;
+    if (!operand_span(a_rows, a_cols, lda, &a1) || !operand_span(b_rows, b_cols, ldb, &b1) ||
+        !operand_span(M, N, ldc, &c1) || (R && !operand_span(M, N, ldr, &r1)))
+        return REPOPS_ERR_INVALID_ARG;
+    if (!batched_span(batch, strideA, a1, &a_bytes) || !batched_span(batch, strideB, b1, &b_bytes) ||
+        !batched_span(batch, strideC, c1, &c_bytes) || (R && !batched_span(batch, strideR, r1, &r_bytes)))
+        return REPOPS_ERR_INVALID_ARG;
+    // The batches' outputs must not overlap one another: either stacked (each
+    // C_b past the end of the previous one) or interleaved within one row
+    // pitch (C_b = columns [b*strideC, b*strideC + N) of shared rows).
+    if (batch > 1) {
+        const bool stacked = uint64_t(strideC) * 4u >= c1;
+        const bool interleaved = strideC >= N && (batch - 1) * strideC + N <= ldc;
+        if (!stacked && !interleaved) return REPOPS_ERR_ALIAS;
+    }
+    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
+        return REPOPS_ERR_ALIAS;
+    if (bias && ranges_overlap(C, c_bytes, bias, uint64_t(N) * 4u)) return REPOPS_ERR_ALIAS;
+    // a residual is either C itself (each element reads its own old value
+    // before writing it) or disjoint from C
+    const bool r_in_place = R == C && ldr == ldc && (batch == 1 || strideR == strideC);
+    if (R && !r_in_place && ranges_overlap(C, c_bytes, R, r_bytes)) return REPOPS_ERR_ALIAS;
+
+    GemmProblem p;
+    p.transA = transA ? 1 : 0;
+    p.transB = transB ? 1 : 0;
+    p.M = M; p.N = N; p.K = K;
+    p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
+    p.stream = stream;
+    p.ex = true;
+    p.batch = batch;
+    p.strideA = batch > 1 ? strideA : 0;
+    p.strideB = batch > 1 ? strideB : 0;
+    p.strideC = batch > 1 ? strideC : 0;
+    p.alpha = alpha;
+    p.bias = bias;
+    p.act = act;
+    p.R = R;
+    p.ldr = ldr;
+    p.strideR = batch > 1 ? strideR : 0;
+    int rc = status_address(&p.status);
+    if (rc != REPOPS_OK) return rc;
+
+    const int cfg = config >= 0 ? config : choose_config(M, N, batch);
+    // K == 0 has no k-slices to copy: the cp.async kernel runs the epilogue on +0
+    const bool tma_ok = K > 0 && gemm_tma_eligible(p);
+    if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
+    const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
+    rc = kLaunch[cfg](p, use);
+    if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO)
+        rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);   // the encoder refused a map
+    return rc;
+}
+
 }  // namespace
 
 namespace gemm {
@@ -267,6 +352,12 @@ bool gemm_tma_eligible(const GemmProblem &p) {
     if (p.lda >= (int64_t(1) << 37) || p.ldb >= (int64_t(1) << 37)) return false;   // pitch < 2^40 B
     const int64_t lim = int64_t(1) << 31;        // int32 box coordinates
     if (p.M >= lim || p.N >= lim || p.K >= lim) return false;
+    if (p.ex && p.batch > 1) {
+        // a batch stride is the pitch of a third map dimension: a multiple of
+        // 16 bytes below 2^40 bytes (0 = shared operand, no third dimension)
+        for (int64_t st : {p.strideA, p.strideB})
+            if (st % 4 || st >= (int64_t(1) << 37)) return false;
+    }
     return true;
 }
 
@@ -305,6 +396,16 @@ extern "C" int repops_gemm_f32_config(int config, int loader, int transA, int tr
                                       const float *B, int64_t ldb, float *C, int64_t ldc,
                                       cudaStream_t stream) {
     return gemm_dispatch(config, loader, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+extern "C" int repops_gemm_f32_batched(int config, int loader, int transA, int transB, int64_t batch,
+                                       int64_t M, int64_t N, int64_t K, const float *A, int64_t lda,
+                                       int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
+                                       float *C, int64_t ldc, int64_t strideC, float alpha,
+                                       const float *bias, int act, const float *R, int64_t ldr,
+                                       int64_t strideR, cudaStream_t stream) {
+    return gemm_dispatch_batched(config, loader, transA, transB, batch, M, N, K, A, lda, strideA, B, ldb,
+                                 strideB, C, ldc, strideC, alpha, bias, act, R, ldr, strideR, stream);
 }
 
 extern "C" int repops_gemm_config_count(void) { return kGemmConfigCount; }

@@ -18,6 +18,16 @@ struct GemmProblem {
     int64_t ldc = 0;
     cudaStream_t stream = nullptr;
     unsigned *status = nullptr;   // device address of the sticky status word
+    // Batched / fused-epilogue form (repops_gemm_f32_batched).  ex == false is
+    // the plain GEMM and ignores the fields below.
+    bool ex = false;
+    int64_t batch = 1;
+    int64_t strideA = 0, strideB = 0, strideC = 0;   // elements; 0 = shared by every batch
+    float alpha = 1.0f;
+    const float *bias = nullptr;                      // N values, or null
+    int act = 0;                                      // 0 none, 1 GeLU
+    const float *R = nullptr;                         // residual, or null
+    int64_t ldr = 0, strideR = 0;
 };
 
 struct GemmConfigInfo {

@@ -31,6 +31,12 @@
 //     row r sits at chunk c ^ (r mod 8).  A thread reads a float4 along k.
 //   MN-inner operand (A stored transposed, or B row-major): [32][rows] plain.
 //     A thread reads float4 runs along m or n.
+// Batched / fused-epilogue variant (EX = true): blockIdx.y is the batch; every
+// operand advances by its own stride (TMA: a 3-D tensor map whose third
+// dimension is the batch, so out-of-bounds zero fill stays per batch).  After
+// an element's whole k-chain the epilogue applies y = fl(alpha*acc), then
+// fl(y + bias[j]), then GeLU, then fl(y + R[i][j]), each part optional.
+//
 // Within a warp the 32 lanes form a 4 (m) x 8 (n) grid.  Lanes that share m
 // read the same A address (broadcast); the n mapping is chosen per B layout so
 // that each quarter-warp's B reads hit 8 distinct 16-byte bank groups:
@@ -38,6 +44,7 @@
 //   B K-inner : lane ln owns columns ln + 8*c              (distinct swizzle rows)
 #pragma once
 
+#include "fixed_math.cuh"
 #include "gemm_common.h"
 #include "internal.cuh"
 
@@ -242,13 +249,11 @@ __device__ __forceinline__ void mma_stage(const float *__restrict__ As, const fl
     }
 }
 
-// Writes the thread's accumulators; rows/columns past M/N are skipped.
+// Writes the thread's results; rows/columns past M/N are skipped.
 template <class T, bool A_KIN, bool B_KIN>
-__device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
-                                           int64_t m0, int64_t n0, int abase, int bbase,
-                                           const PackedAcc<T, A_KIN> &pacc, bool c_vec) {
-    float acc[T::TM][T::TN];
-    pacc.to_float(acc);
+__device__ __forceinline__ void store_acc(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
+                                          int64_t m0, int64_t n0, int abase, int bbase,
+                                          const float (&acc)[T::TM][T::TN], bool c_vec) {
 #pragma unroll
     for (int r = 0; r < T::TM; ++r) {
         const int64_t gm = m0 + a_row<A_KIN>(abase, r);
@@ -277,6 +282,50 @@ __device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, i
     }
 }
 
+template <class T, bool A_KIN, bool B_KIN>
+__device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
+                                           int64_t m0, int64_t n0, int abase, int bbase,
+                                           const PackedAcc<T, A_KIN> &pacc, bool c_vec) {
+    float acc[T::TM][T::TN];
+    pacc.to_float(acc);
+    store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec);
+}
+
+// Batch strides and epilogue of the EX kernels (kernel parameter).
+struct ExArgs {
+    int64_t sA, sB, sC;    // batch strides of the operands, elements (cp.async path)
+    int zA, zB;            // TMA: 1 when the operand's map has a batch dimension
+    float alpha;
+    const float *bias;     // N values or null
+    int act;               // 0 none, 1 GeLU
+    const float *R;        // residual of batch 0 or null; batch b at R + b*sR
+    int64_t ldr, sR;
+};
+
+// The epilogue, element by element after the whole k-chain, then the store.
+// The element loop is not unrolled: one copy of the GeLU code per kernel.
+template <class T, bool A_KIN, bool B_KIN>
+__device__ __forceinline__ void store_tile_ex(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
+                                              int64_t m0, int64_t n0, int abase, int bbase,
+                                              const PackedAcc<T, A_KIN> &pacc, bool c_vec, const ExArgs &ep,
+                                              const float *__restrict__ Rb) {
+    float acc[T::TM][T::TN];
+    pacc.to_float(acc);
+#pragma unroll 1
+    for (int e = 0; e < T::TM * T::TN; ++e) {
+        const int r = e / T::TN, c = e % T::TN;
+        const int64_t gm = m0 + a_row<A_KIN>(abase, r), gn = n0 + b_col<B_KIN>(bbase, c);
+        float y = __fmul_rn(acc[r][c], ep.alpha);
+        if (gm < M && gn < N) {
+            if (ep.bias) y = __fadd_rn(y, ep.bias[gn]);
+            if (ep.act == 1) y = gelu_fixed(y);
+            if (Rb) y = __fadd_rn(y, Rb[gm * ep.ldr + gn]);
+        }
+        acc[r][c] = y;
+    }
+    store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec);
+}
+
 __device__ __forceinline__ float *aligned_smem_base(unsigned char *raw) {
     return reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
 }
@@ -290,11 +339,11 @@ __device__ __forceinline__ float *aligned_smem_base(unsigned char *raw) {
 // at a barrier every k-slice.  Every wait is bounded; on a timeout the status
 // bit is set, the producer lets its in-flight copies land, and the tile is not
 // stored.
-template <class T, bool A_KIN, bool B_KIN>
+template <class T, bool A_KIN, bool B_KIN, bool EX>
 __global__ void __launch_bounds__(T::THREADS + 32, T::MINB)
 gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    float *__restrict__ C, int64_t M, int64_t N, int64_t K, int64_t ldc,
-                   int tiles_m, int tiles_n, int c_vec, unsigned *status) {
+                   int tiles_m, int tiles_n, int c_vec, unsigned *status, const ExArgs ep) {
     constexpr int CONSUMER_WARPS = T::THREADS / 32;
     extern __shared__ unsigned char smem_raw[];
     float *smem = aligned_smem_base(smem_raw);
@@ -335,10 +384,12 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 float *Bs = As + T::A_FLOATS;
                 mbar_arrive_expect_tx(&full[s], T::STAGE_BYTES);
                 const int k0 = kt * BK;
-                if constexpr (A_KIN) tma_load_2d(As, &tmA, &full[s], k0, int(m0));
-                else                 tma_load_2d(As, &tmA, &full[s], int(m0), k0);
-                if constexpr (B_KIN) tma_load_2d(Bs, &tmB, &full[s], k0, int(n0));
-                else                 tma_load_2d(Bs, &tmB, &full[s], int(n0), k0);
+                const int ax = A_KIN ? k0 : int(m0), ay = A_KIN ? int(m0) : k0;
+                const int bx = B_KIN ? k0 : int(n0), by = B_KIN ? int(n0) : k0;
+                if (EX && ep.zA) tma_load_3d(As, &tmA, &full[s], ax, ay, int(blockIdx.y));
+                else             tma_load_2d(As, &tmA, &full[s], ax, ay);
+                if (EX && ep.zB) tma_load_3d(Bs, &tmB, &full[s], bx, by, int(blockIdx.y));
+                else             tma_load_2d(Bs, &tmB, &full[s], bx, by);
                 issued = kt + 1;
             }
             if (!ok) atomicOr(status, 1u);
@@ -370,7 +421,13 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[s]);
     }
-    store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+    if constexpr (EX) {
+        const int64_t b = blockIdx.y;
+        store_tile_ex<T, A_KIN, B_KIN>(C + b * ep.sC, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep,
+                                       ep.R ? ep.R + b * ep.sR : nullptr);
+    } else {
+        store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+    }
 }
 
 // ------------------------------------------------------------- cp.async ----
@@ -422,13 +479,19 @@ __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const f
     }
 }
 
-template <class T, bool A_KIN, bool B_KIN>
+template <class T, bool A_KIN, bool B_KIN, bool EX>
 __global__ void __launch_bounds__(T::THREADS, T::MINB)
 gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__restrict__ B, int64_t ldb,
                     float *__restrict__ C, int64_t M, int64_t N, int64_t K, int64_t ldc,
-                    int tiles_m, int tiles_n, int c_vec) {
+                    int tiles_m, int tiles_n, int c_vec, const ExArgs ep) {
     extern __shared__ unsigned char smem_raw[];
     float *smem = aligned_smem_base(smem_raw);
+    if constexpr (EX) {
+        const int64_t b = blockIdx.y;
+        A += b * ep.sA;
+        B += b * ep.sB;
+        C += b * ep.sC;
+    }
 
     const int tid = threadIdx.x;
     int tm, tn;
@@ -469,7 +532,11 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
         mma_stage<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, abase, bbase, lm, ln, acc);
     }
     cp_async_wait<0>();
-    store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+    if constexpr (EX)
+        store_tile_ex<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep,
+                                       ep.R ? ep.R + int64_t(blockIdx.y) * ep.sR : nullptr);
+    else
+        store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
 }
 
 // --------------------------------------------------------------- host ----
@@ -499,32 +566,90 @@ inline bool make_map(CUtensorMap *map, const float *base, int64_t inner, int64_t
     return r == CUDA_SUCCESS;
 }
 
-template <class T, bool A_KIN, bool B_KIN>
+// 3-D fp32 tensor map: as make_map plus a batch dimension of `batch`
+// matrices `stride` elements apart (box extent 1 in it).
+inline bool make_map_3d(CUtensorMap *map, const float *base, int64_t inner, int64_t outer, int64_t batch,
+                        int64_t ld, int64_t stride, int box_inner, int box_outer, bool swizzle128) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {cuuint64_t(inner), cuuint64_t(outer), cuuint64_t(batch)};
+    cuuint64_t strides[2] = {cuuint64_t(ld) * 4u, cuuint64_t(stride) * 4u};
+    cuuint32_t box[3] = {cuuint32_t(box_inner), cuuint32_t(box_outer), 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// An operand's map: 3-D when it advances with the batch (z = 1), else 2-D.
+inline bool make_operand_map(CUtensorMap *map, const float *base, int64_t inner, int64_t outer, int64_t ld,
+                             int64_t batch, int64_t stride, int z, int box_inner, int box_outer, bool swz) {
+    return z ? make_map_3d(map, base, inner, outer, batch, ld, stride, box_inner, box_outer, swz)
+             : make_map(map, base, inner, outer, ld, box_inner, box_outer, swz);
+}
+
+inline ExArgs ex_args(const GemmProblem &p) {
+    ExArgs ep{};
+    ep.alpha = 1.0f;
+    if (!p.ex) return ep;
+    ep.sA = p.strideA; ep.sB = p.strideB; ep.sC = p.strideC;
+    ep.zA = p.batch > 1 && p.strideA != 0;
+    ep.zB = p.batch > 1 && p.strideB != 0;
+    ep.alpha = p.alpha;
+    ep.bias = p.bias;
+    ep.act = p.act;
+    ep.R = p.R;
+    ep.ldr = p.ldr;
+    ep.sR = p.strideR;
+    return ep;
+}
+
+template <class T, bool A_KIN, bool B_KIN, bool EX>
 int launch_tma(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     CUtensorMap ma, mb;
+    const ExArgs ep = ex_args(p);
     // A: row-major (K-inner) -> dims {K, M}; transposed (M-inner) -> {M, K}
-    const bool okA = A_KIN ? make_map(&ma, p.A, p.K, p.M, p.lda, BK, T::BM, true)
-                           : make_map(&ma, p.A, p.M, p.K, p.lda, T::BM, BK, false);
+    const bool okA = A_KIN ? make_operand_map(&ma, p.A, p.K, p.M, p.lda, p.batch, p.strideA, ep.zA, BK, T::BM, true)
+                           : make_operand_map(&ma, p.A, p.M, p.K, p.lda, p.batch, p.strideA, ep.zA, T::BM, BK, false);
     // B: transposed (K-inner) -> dims {K, N}; row-major (N-inner) -> {N, K}
-    const bool okB = B_KIN ? make_map(&mb, p.B, p.K, p.N, p.ldb, BK, T::BN, true)
-                           : make_map(&mb, p.B, p.N, p.K, p.ldb, T::BN, BK, false);
+    const bool okB = B_KIN ? make_operand_map(&mb, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, ep.zB, BK, T::BN, true)
+                           : make_operand_map(&mb, p.B, p.N, p.K, p.ldb, p.batch, p.strideB, ep.zB, T::BN, BK, false);
     if (!okA || !okB) return REPOPS_ERR_UNSUPPORTED;
-    auto kern = gemm_tma_ws_kernel<T, A_KIN, B_KIN>;
+    auto kern = gemm_tma_ws_kernel<T, A_KIN, B_KIN, EX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
-    kern<<<tiles_m * tiles_n, T::THREADS + 32, T::SMEM_BYTES, p.stream>>>(
-        ma, mb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n, c_vec, p.status);
+    const dim3 grid(unsigned(tiles_m * tiles_n), EX ? unsigned(p.batch) : 1u);
+    kern<<<grid, T::THREADS + 32, T::SMEM_BYTES, p.stream>>>(ma, mb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n,
+                                                             c_vec, p.status, ep);
     return check_launch();
 }
 
-template <class T, bool A_KIN, bool B_KIN>
+template <class T, bool A_KIN, bool B_KIN, bool EX>
 int launch_cpasync(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
-    auto kern = gemm_cpasync_kernel<T, A_KIN, B_KIN>;
+    auto kern = gemm_cpasync_kernel<T, A_KIN, B_KIN, EX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (e != cudaSuccess) return set_cuda_error(e);
-    kern<<<tiles_m * tiles_n, T::THREADS, T::SMEM_BYTES, p.stream>>>(
-        p.A, p.lda, p.B, p.ldb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n, c_vec);
+    const dim3 grid(unsigned(tiles_m * tiles_n), EX ? unsigned(p.batch) : 1u);
+    kern<<<grid, T::THREADS, T::SMEM_BYTES, p.stream>>>(p.A, p.lda, p.B, p.ldb, p.C, p.M, p.N, p.K, p.ldc,
+                                                        tiles_m, tiles_n, c_vec, ex_args(p));
     return check_launch();
+}
+
+template <class T, bool EX>
+int launch_layout(const GemmProblem &p, int loader, int tmi, int tni, int c_vec) {
+    const bool a_kin = p.transA == 0, b_kin = p.transB != 0;
+    if (loader == REPOPS_LOADER_TMA) {
+        if (a_kin && !b_kin) return launch_tma<T, true, false, EX>(p, tmi, tni, c_vec);
+        if (a_kin && b_kin) return launch_tma<T, true, true, EX>(p, tmi, tni, c_vec);
+        if (!a_kin && !b_kin) return launch_tma<T, false, false, EX>(p, tmi, tni, c_vec);
+        return launch_tma<T, false, true, EX>(p, tmi, tni, c_vec);
+    }
+    if (a_kin && !b_kin) return launch_cpasync<T, true, false, EX>(p, tmi, tni, c_vec);
+    if (a_kin && b_kin) return launch_cpasync<T, true, true, EX>(p, tmi, tni, c_vec);
+    if (!a_kin && !b_kin) return launch_cpasync<T, false, false, EX>(p, tmi, tni, c_vec);
+    return launch_cpasync<T, false, true, EX>(p, tmi, tni, c_vec);
 }
 
 // loader: REPOPS_LOADER_TMA or REPOPS_LOADER_CPASYNC (already resolved).
@@ -533,25 +658,18 @@ int launch_config(const GemmProblem &p, int loader) {
     const int64_t tiles_m = (p.M + T::BM - 1) / T::BM;
     const int64_t tiles_n = (p.N + T::BN - 1) / T::BN;
     if (tiles_m * tiles_n > 0x7fffffffLL) return REPOPS_ERR_UNSUPPORTED;
-    const int c_vec = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0);
-    const bool a_kin = p.transA == 0, b_kin = p.transB != 0;
+    // C of every batch is 16-byte aligned with a 16-byte pitch
+    const int c_vec = (reinterpret_cast<uintptr_t>(p.C) % 16 == 0) && (p.ldc % 4 == 0) &&
+                      (!p.ex || p.strideC % 4 == 0);
     const int tmi = int(tiles_m), tni = int(tiles_n);
-    if (loader == REPOPS_LOADER_TMA) {
-        if (a_kin && !b_kin) return launch_tma<T, true, false>(p, tmi, tni, c_vec);
-        if (a_kin && b_kin) return launch_tma<T, true, true>(p, tmi, tni, c_vec);
-        if (!a_kin && !b_kin) return launch_tma<T, false, false>(p, tmi, tni, c_vec);
-        return launch_tma<T, false, true>(p, tmi, tni, c_vec);
-    }
-    if (a_kin && !b_kin) return launch_cpasync<T, true, false>(p, tmi, tni, c_vec);
-    if (a_kin && b_kin) return launch_cpasync<T, true, true>(p, tmi, tni, c_vec);
-    if (!a_kin && !b_kin) return launch_cpasync<T, false, false>(p, tmi, tni, c_vec);
-    return launch_cpasync<T, false, true>(p, tmi, tni, c_vec);
+    return p.ex ? launch_layout<T, true>(p, loader, tmi, tni, c_vec)
+                : launch_layout<T, false>(p, loader, tmi, tni, c_vec);
 }
 
 // Resident CTAs per SM of the TMA kernel (row-major operands) on the current device.
 template <class T>
 int occupancy() {
-    auto kern = gemm_tma_ws_kernel<T, true, false>;
+    auto kern = gemm_tma_ws_kernel<T, true, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES) != cudaSuccess)
         return 0;
     int n = 0;

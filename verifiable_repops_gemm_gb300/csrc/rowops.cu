@@ -32,6 +32,7 @@
 // aligned, use a kernel that re-reads the row for each phase.
 #include <algorithm>
 
+#include "fixed_math.cuh"
 #include "internal.cuh"
 
 namespace repops {
@@ -44,62 +45,6 @@ constexpr int MAX_FAST_RUNS = 256 * 4;          // register-resident rows: up to
 constexpr int MAX_GENERIC_RUNS = 12288;         // run results in 48 KB of shared memory
 
 // ------------------------------------------------------------ arithmetic ----
-
-__device__ __forceinline__ float pow2i(int k) { return __int_as_float((k + 127) << 23); }
-
-__device__ float exp_fixed(float x) {
-    if (x != x) return x;
-    if (x > 88.72283935546875f) return __int_as_float(0x7f800000);
-    if (x < -103.972084045410156f) return 0.0f;
-    const float t = __fmul_rn(x, 1.44269502162933349609375f);
-    // k = rint(t), ties to even: adding 1.5 * 2^23 leaves rint(t) in the low
-    // mantissa bits (exact for |t| < 2^22; past the checks above |t| < 151),
-    // and subtracting it back is exact
-    const float big = __fadd_rn(t, 12582912.0f);
-    const float kf = __fsub_rn(big, 12582912.0f);
-    const int k = __float_as_int(big) - 0x4B400000;
-    float r = __fsub_rn(x, __fmul_rn(kf, 0.693145751953125f));
-    r = __fsub_rn(r, __fmul_rn(kf, 1.428606765330187045037746e-06f));
-    float p = 1.98412701e-04f;
-    p = __fadd_rn(__fmul_rn(p, r), 1.38888892e-03f);
-    p = __fadd_rn(__fmul_rn(p, r), 8.33333377e-03f);
-    p = __fadd_rn(__fmul_rn(p, r), 4.16666679e-02f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.66666672e-01f);
-    p = __fadd_rn(__fmul_rn(p, r), 0.5f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    p = __fadd_rn(__fmul_rn(p, r), 1.0f);
-    // p * 2^k as (p * 2^k1) * 2^k2: k1 = 127, k2 = k - 127 above the normal
-    // range; k1 = k + 64, k2 = -64 below it (one rounding, at the end); else
-    // k1 = k and the second factor is 1 (exact).  Selects, not branches.
-    const int k2 = k > 127 ? k - 127 : (k < -126 ? -64 : 0);
-    return __fmul_rn(__fmul_rn(p, pow2i(k - k2)), pow2i(k2));
-}
-
-__device__ float erfc_pos(float z) {
-    // correctly rounded reciprocal: the same value as a correctly rounded 1/x
-    const float t = __frcp_rn(__fadd_rn(1.0f, __fmul_rn(0.5f, z)));
-    float q = 0.17087277f;
-    q = __fadd_rn(__fmul_rn(q, t), -0.82215223f);
-    q = __fadd_rn(__fmul_rn(q, t), 1.48851587f);
-    q = __fadd_rn(__fmul_rn(q, t), -1.13520398f);
-    q = __fadd_rn(__fmul_rn(q, t), 0.27886807f);
-    q = __fadd_rn(__fmul_rn(q, t), -0.18628806f);
-    q = __fadd_rn(__fmul_rn(q, t), 0.09678418f);
-    q = __fadd_rn(__fmul_rn(q, t), 0.37409196f);
-    q = __fadd_rn(__fmul_rn(q, t), 1.00002368f);
-    q = __fmul_rn(q, t);
-    const float zz = __fmul_rn(z, z);
-    const float arg = __fadd_rn(__fadd_rn(-zz, -1.26551223f), q);
-    return __fmul_rn(t, exp_fixed(arg));
-}
-
-__device__ __forceinline__ float gelu_fixed(float x) {
-    const float z = __fmul_rn(x, 0.707106769084930419921875f);
-    // one erfc for either sign: no divergent branch
-    const float e = erfc_pos(fabsf(z));
-    const float phi2 = z >= 0.0f ? __fsub_rn(2.0f, e) : e;
-    return __fmul_rn(__fmul_rn(0.5f, x), phi2);
-}
 
 enum class Op { Sum, Max };
 
