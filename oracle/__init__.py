@@ -97,6 +97,8 @@ def lib():
         L.oracle_layernorm_rows.argtypes = [i64, i64, vp, i64, vp, vp, f32, vp, i64]
         L.oracle_rmsnorm_rows.restype = None
         L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64]
+        L.oracle_softmax_rows_causal.restype = None
+        L.oracle_softmax_rows_causal.argtypes = [i64, i64, vp, i64, vp, i64, i64]
         L.oracle_gemm_batched.restype = None
         L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
                                           vp, i64, i64, f32, vp, i32, vp, i64, i64]
@@ -364,3 +366,14 @@ def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, stride
                           float(alpha), _ptr(bias) if bias is not None else None, int(act),
                           _ptr(R) if R is not None else None, ldr, strideR)
     return C
+
+
+def softmax_rows_causal(X: np.ndarray, first: int) -> np.ndarray:
+    """Row i: softmax over its first min(cols, first + i + 1) values, +0 after."""
+    L = lib()
+    X = np.ascontiguousarray(X, dtype=np.float32)
+    rows, cols = X.shape
+    Y = np.empty_like(X)
+    if rows and cols:
+        L.oracle_softmax_rows_causal(rows, cols, _ptr(X), cols, _ptr(Y), cols, first)
+    return Y

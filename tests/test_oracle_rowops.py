@@ -236,3 +236,26 @@ def test_exp_steps_exact_rational(orc):
                          [0.0, -0.0, 88.72, -87.3, -100.0, -103.9, 0.34657359, -0.34657359]]).astype(np.float32)
     for x in xs:
         assert fx.bits(orc.exp(float(x))) == fx.bits(ref_exp(float(x))), float(x)
+
+
+@pytest.mark.parametrize("first", [0, 3, 40])
+def test_causal_softmax_is_the_prefix_softmax(orc, first):
+    # row i sees keys 0 .. first + i: the softmax of that prefix, restated in
+    # exact rational arithmetic, then +0
+    rng = np.random.default_rng(100 + first)
+    x = (rng.standard_normal((6, 37)) * 3).astype(np.float32)
+    y = orc.softmax_rows_causal(x, first)
+    for i in range(6):
+        L = min(37, first + i + 1)
+        want = ref_softmax_row(x[i, :L], orc) + [0.0] * (37 - L)
+        assert [fx.bits(float(v)) for v in y[i]] == [fx.bits(v) for v in want]
+
+
+def test_causal_softmax_closed_forms(orc):
+    x = np.full((4, 9), 5.0, np.float32)
+    y = orc.softmax_rows_causal(x, 0)
+    for i in range(4):                      # a constant prefix of length i + 1: 1 * fl(1/(i+1))
+        assert np.all(y[i, :i + 1] == np.float32(1) / np.float32(i + 1))
+        assert np.all(y[i, i + 1:].view(np.uint32) == 0)
+    x = np.random.default_rng(1).standard_normal((5, 33)).astype(np.float32)
+    assert np.array_equal(orc.softmax_rows_causal(x, 1000).view(np.uint32), orc.softmax_rows(x).view(np.uint32))
