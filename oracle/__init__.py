@@ -98,7 +98,7 @@ def lib():
         L.oracle_rmsnorm_rows.restype = None
         L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64]
         L.oracle_softmax_rows_causal.restype = None
-        L.oracle_softmax_rows_causal.argtypes = [i64, i64, vp, i64, vp, i64, i64]
+        L.oracle_softmax_rows_causal.argtypes = [i64, i64, vp, i64, vp, i64, i64, i64]
         L.oracle_gemm_batched.restype = None
         L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
                                           vp, i64, i64, f32, vp, i32, vp, i64, i64]
@@ -368,12 +368,13 @@ def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, stride
     return C
 
 
-def softmax_rows_causal(X: np.ndarray, first: int) -> np.ndarray:
-    """Row i: softmax over its first min(cols, first + i + 1) values, +0 after."""
+def softmax_rows_causal(X: np.ndarray, first: int, period: int = None) -> np.ndarray:
+    """Row i: softmax over its first min(cols, first + (i mod period) + 1)
+    values, +0 after (period defaults to the row count: no repetition)."""
     L = lib()
     X = np.ascontiguousarray(X, dtype=np.float32)
     rows, cols = X.shape
     Y = np.empty_like(X)
     if rows and cols:
-        L.oracle_softmax_rows_causal(rows, cols, _ptr(X), cols, _ptr(Y), cols, first)
+        L.oracle_softmax_rows_causal(rows, cols, _ptr(X), cols, _ptr(Y), cols, first, period or rows)
     return Y

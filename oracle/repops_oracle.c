@@ -655,14 +655,15 @@ void oracle_softmax_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx
 }
 
 /* Causal softmax: row i is the softmax above over its first
- * L_i = min(cols, first + i + 1) values; y[i][j] = +0 for j >= L_i.  (Row i
- * of an attention block whose queries sit at positions first + i sees the keys
- * at positions 0 .. first + i.)  first >= 0. */
+ * L_i = min(cols, first + (i mod period) + 1) values; y[i][j] = +0 for
+ * j >= L_i.  (Row i of an attention block whose queries sit at positions
+ * first + i sees the keys at positions 0 .. first + i; `period` stacks several
+ * heads' blocks of `period` rows.)  first >= 0, period >= 1. */
 void oracle_softmax_rows_causal(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
-                                int64_t ldy, int64_t first)
+                                int64_t ldy, int64_t first, int64_t period)
 {
     for (int64_t i = 0; i < rows; ++i) {
-        int64_t L = first + i + 1;
+        int64_t L = first + i % period + 1;
         if (L > cols) L = cols;
         oracle_softmax_rows(1, L, x + i * ldx, ldx, y + i * ldy, ldy);
         for (int64_t j = L; j < cols; ++j) y[i * ldy + j] = 0.0f;

@@ -70,7 +70,9 @@ MUTATIONS = {
                                     "acc = __builtin_fmaf(a, bv, acc);"),
     "epilogue: residual before GeLU": ("if (act == 1) y = oracle_gelu(y);\n                if (Rb) y = y + Rb[i * ldr + j];",
                                        "if (Rb) y = y + Rb[i * ldr + j];\n                if (act == 1) y = oracle_gelu(y);"),
-    "causal softmax: one key too many": ("int64_t L = first + i + 1;", "int64_t L = first + i + 2;"),
+    "causal softmax: one key too many": ("int64_t L = first + i % period + 1;",
+                                         "int64_t L = first + i % period + 2;"),
+    "causal softmax: period ignored": ("int64_t L = first + i % period + 1;", "int64_t L = first + i + 1;"),
     "batched: A advanced by B's stride": ("const float *Ab = A + b * strideA;", "const float *Ab = A + b * strideB;"),
 }
 

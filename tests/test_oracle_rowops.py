@@ -259,3 +259,15 @@ def test_causal_softmax_closed_forms(orc):
         assert np.all(y[i, i + 1:].view(np.uint32) == 0)
     x = np.random.default_rng(1).standard_normal((5, 33)).astype(np.float32)
     assert np.array_equal(orc.softmax_rows_causal(x, 1000).view(np.uint32), orc.softmax_rows(x).view(np.uint32))
+
+
+def test_causal_softmax_period_repeats_the_block(orc):
+    # period p: rows are blocks of p queries (one per head), each block masked
+    # like the first
+    x = (np.random.default_rng(2).standard_normal((12, 20)) * 2).astype(np.float32)
+    y = orc.softmax_rows_causal(x, 2, period=4)
+    for b in range(3):
+        blk = slice(4 * b, 4 * b + 4)
+        assert np.array_equal(y[blk].view(np.uint32), orc.softmax_rows_causal(x[blk], 2).view(np.uint32))
+    assert np.array_equal(orc.softmax_rows_causal(x, 2, period=12).view(np.uint32),
+                          orc.softmax_rows_causal(x, 2).view(np.uint32))
