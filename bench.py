@@ -498,6 +498,8 @@ def run_sweep(args):
         run_sweep_rowops(dev, s, flush, peaks.get("hbm_gbs", 6800.0))
     if args.sweep in ("all", "commitments"):
         run_sweep_commitments(dev, s, flush)
+    if args.sweep in ("all", "decoder"):
+        run_sweep_decoder(dev, s, flush, peak)
 
 
 def run_sweep_gemm(dev, s, flush, peak):
@@ -605,6 +607,52 @@ def run_sweep_rowops(dev, s, flush, hbm):
     del S, P
 
 
+def run_sweep_decoder(dev, s, flush, peak):
+    """One decoder layer forward (Llama-3.2-1B sizes: d 2048, 32 query and 8
+    key/value heads of 64, MLP 8192; GeLU MLP, no rotary embedding) over two
+    causal sequences of 2048 tokens, every step a library call: the fused
+    layer, the same layer with its epilogues as separate steps, and the
+    attention alone.  Synthetic N(0, 0.02) weights; L2 flushed before each
+    timed layer."""
+    from verifiable_repops_gemm_gb300 import decoder
+    cfg = decoder.DecoderConfig()
+    T = 2 * cfg.seq_len
+    w = decoder.init_weights(cfg, 300, dev)
+    x0 = inputs.normal((T, cfg.d), 1.0, 301, dev)
+    x = torch.empty_like(x0)
+    ws = decoder.workspace(cfg, T, dev)
+
+    def timed(fn, reps=5):
+        with torch.cuda.stream(s):
+            for _ in range(2):
+                x.copy_(x0)
+                fn()
+            evs = []
+            for _ in range(reps):
+                x.copy_(x0)
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                fn()
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+    flops = cfg.flops(T)
+    for name, fused, ge in (("decoder layer forward, fused bias/residual epilogues, GeLU kernel", True, False),
+                            ("decoder layer forward, GeLU in the GEMM epilogue too", True, True),
+                            ("decoder layer forward, epilogues as separate steps", False, False)):
+        ms = timed(lambda: decoder.forward(x, w, cfg, fused=fused, gelu_epilogue=ge, work=ws))
+        print(json.dumps({"sweep": name, "tokens": T, "ms": ms, "tokens_per_s": T / ms * 1e3,
+                          "tflops": flops / ms / 1e9, "frac_of_fp32_peak": flops / ms / 1e9 / peak}),
+              flush=True)
+    attn_flops = 2 * 2.0 * (T // cfg.seq_len) * cfg.heads * cfg.seq_len ** 2 * cfg.d_head
+    ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"]))
+    print(json.dumps({"sweep": "causal grouped-query attention (batched QK^T, softmax, PV)", "tokens": T,
+                      "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
+
+
 def run_sweep_commitments(dev, s, flush):
     """Merkle root versus whole stored tree of the 4 GiB tensor, one inclusion
     proof and one membership check, and replayed blocks of the 16 x 2^28
@@ -669,7 +717,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
-                    choices=("all", "gemm", "rowops", "commitments"),
+                    choices=("all", "gemm", "rowops", "commitments", "decoder"),
                     help="time every workload of a part (one JSON line each) instead of the step")
     args = ap.parse_args()
     if args.sweep:

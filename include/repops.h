@@ -188,10 +188,16 @@ int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
  * automatic choice); the bits do not depend on them.  TMA needs, besides its
  * repops_gemm_f32_config rule, batch strides of A and B that are multiples
  * of 4 elements.  No scratch memory is taken.
+ * causal_first (attention scores Q K^T of queries at positions causal_first +
+ * i): -1 computes every element; >= 0 leaves the elements with
+ * j > causal_first + i unspecified -- whole output tiles above that boundary
+ * are neither computed nor written, tiles crossing it are computed in full --
+ * and every element on or below it exact.  Pair with
+ * repops_softmax_rows_causal_f32, which never reads them.
  * Errors: INVALID_ARG (negative size or stride, bad leading dim, null
- * pointer with a non-empty operand, act not NONE/GELU, spans that overflow);
- * ALIAS; UNSUPPORTED (batch > 65535, or loader TMA when TMA cannot serve the
- * operands); CUDA. */
+ * pointer with a non-empty operand, act not NONE/GELU, causal_first < -1,
+ * spans that overflow); ALIAS; UNSUPPORTED (batch > 65535, or loader TMA when
+ * TMA cannot serve the operands); CUDA. */
 int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
                             int64_t batch, int64_t M, int64_t N, int64_t K,
                             const float *A, int64_t lda, int64_t strideA,
@@ -199,7 +205,7 @@ int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
                             float *C, int64_t ldc, int64_t strideC,
                             float alpha, const float *bias, int act,
                             const float *R, int64_t ldr, int64_t strideR,
-                            cudaStream_t stream);
+                            int64_t causal_first, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Contributor order                                                         */
@@ -358,6 +364,17 @@ int repops_merkle_verify(const void *leaf_bytes, uint64_t leaf_len, uint64_t nle
  * tree max of row i and s_i the tree sum of its e. */
 int repops_softmax_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
                             float *y, int64_t ldy, cudaStream_t stream);
+
+/* Causal softmax of attention blocks whose query rows sit at positions
+ * first, first + 1, ...: row i is the softmax above over its first
+ * L_i = min(cols, first + (i mod period) + 1) values and y[i][j] = +0 for
+ * j >= L_i.  `period` rows form one block (one head); several heads' blocks
+ * stacked row after row share one call.  first >= 0 and period >= 1, else
+ * INVALID_ARG.  The masked scores are never read as values (they may hold
+ * anything, NaN included). */
+int repops_softmax_rows_causal_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                                   float *y, int64_t ldy, int64_t first, int64_t period,
+                                   cudaStream_t stream);
 
 /* mean = S/n, d = x - mean, var = tree sum of d*d / n,
  * inv = fl(1 / fl(sqrt(var + eps))), y = (d * inv) * gamma[j] + beta[j];

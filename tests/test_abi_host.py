@@ -214,15 +214,17 @@ def test_row_operators_reject_bad_arguments(L):
 
 
 def _bat(L, batch=2, M=4, N=4, K=4, A=FAKE_A, lda=4, sA=16, B=FAKE_B, ldb=4, sB=16, C=FAKE_C, ldc=4,
-         sC=16, alpha=1.0, bias=None, act=0, R=None, ldr=4, sR=16, config=-1, loader=0, tA=0, tB=0):
+         sC=16, alpha=1.0, bias=None, act=0, R=None, ldr=4, sR=16, config=-1, loader=0, tA=0, tB=0,
+         causal=-1):
     return L.repops_gemm_f32_batched(config, loader, tA, tB, batch, M, N, K, A, lda, sA, B, ldb, sB,
-                                     C, ldc, sC, ctypes.c_float(alpha), bias, act, R, ldr, sR, None)
+                                     C, ldc, sC, ctypes.c_float(alpha), bias, act, R, ldr, sR, causal, None)
 
 
 def test_batched_gemm_rejects_bad_arguments(L):
     assert _bat(L, batch=-1) == -1
     assert _bat(L, sA=-4) == -1                                    # negative stride
     assert _bat(L, act=2) == -1                                    # unknown activation
+    assert _bat(L, causal=-2) == -1
     assert _bat(L, ldc=3) == -1
     assert _bat(L, R=FAKE_B + 4096, ldr=3) == -1                   # residual ld < N
     assert _bat(L, config=99) == -1
@@ -238,3 +240,11 @@ def test_batched_gemm_rejects_bad_arguments(L):
     assert _bat(L, bias=FAKE_C + 8) == -2                          # bias inside C
     assert _bat(L, R=FAKE_C + 4) == -2                             # residual overlapping C, not in place
     assert _bat(L, R=FAKE_C, sR=20, sC=16) == -2                   # same base, other stride
+
+
+def test_causal_softmax_rejects_bad_arguments(L):
+    c = L.repops_softmax_rows_causal_f32
+    assert c(4, 4, FAKE_A, 4, FAKE_B, 4, -1, 4, None) == -1                # first < 0
+    assert c(4, 4, FAKE_A, 4, FAKE_B, 4, 0, 0, None) == -1                 # period < 1
+    assert c(4, 4, FAKE_A, 4, FAKE_A + 8, 4, 0, 4, None) == -2
+    assert c(0, 4, FAKE_A, 4, FAKE_B, 4, 0, 4, None) == 0

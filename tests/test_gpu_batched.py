@@ -168,3 +168,27 @@ def test_decoder_sized_fused_gemms_sampled(rp, orc):
     orc.gemm_batched(0, 0, 1, len(rows), D, 4 * D, Hh, 4 * D, 0, Wdh.reshape(-1), D, 0, Yh, D, 0,
                      1.0, None, 0, Yh, D, 0)
     assert np.array_equal(u32(Y[rows].cpu().numpy().reshape(-1)), u32(Yh))
+
+
+@pytest.mark.parametrize("config", [-1, 0, 3])
+@pytest.mark.parametrize("first", [0, 70])
+def test_causal_tile_skip_keeps_the_lower_part_exact(rp, orc, config, first):
+    # scores of 3 heads, 300 queries x 300 keys: every element on or below
+    # j = first + i equals the oracle's; tiles wholly above are not written
+    H, T, d = 3, 300, 64
+    Q = inputs.normal((H, T, d), 1.0, 400 + first, DEV)
+    K = inputs.normal((H, T, d), 1.0, 401 + first, DEV)
+    S = torch.full((H, T, T), 12345.0, device=DEV)
+    rp.gemm_batched(Q, K.transpose(1, 2), out=S, alpha=0.125, causal_first=first, config=config)
+    Sh = np.empty(H * T * T, np.float32)
+    orc.gemm_batched(0, 1, H, T, T, d, Q.cpu().numpy().reshape(-1), d, T * d, K.cpu().numpy().reshape(-1), d,
+                     T * d, Sh, T, T * T, 0.125)
+    lower = np.tril(np.ones((T, T), bool), k=first)
+    got = S.cpu().numpy()
+    want = Sh.reshape(H, T, T)
+    for h in range(H):
+        assert np.array_equal(u32(got[h][lower]), u32(want[h][lower]))
+    assert (got == 12345.0).any()                     # some tiles were skipped
+    P = rp.softmax_rows(S.view(H * T, T), causal_first=first, causal_period=T)
+    Ph = orc.softmax_rows_causal(want.reshape(H * T, T), first, T)
+    assert np.array_equal(u32(P.cpu().numpy()), u32(Ph))

@@ -152,3 +152,38 @@ def test_persistent_row_loop(rp, orc):
     y = rp.softmax_rows(x)
     pick = [0, 1, 1215, 1216, 2431, 4999]
     assert np.array_equal(u32(y[pick].cpu().numpy()), u32(orc.softmax_rows(x[pick].cpu().numpy())))
+
+
+# causal: every kernel shape, aligned and unaligned rows, in place, first = 0
+# and first > 0 (a later query block), and first past the row (no mask)
+@pytest.mark.parametrize("cols,pad", [(5, 0), (37, 3), (1000, 0), (2048, 0), (4096, 1), (8193, 3),
+                                      (16385, 3), (40000, 0)])
+@pytest.mark.parametrize("first", [0, 700])
+def test_causal_softmax_matches_oracle(rp, orc, cols, pad, first):
+    rows = 6 if cols <= 8192 else 3
+    x = rows_input(rows, cols, 11000 + cols + first, 3.0, pad=pad)
+    want = orc.softmax_rows_causal(x.cpu().numpy(), first)
+    assert np.array_equal(u32(rp.softmax_rows(x, causal_first=first).cpu().numpy()), u32(want))
+    z = x.clone()
+    rp.softmax_rows(z, out=z, causal_first=first)
+    assert np.array_equal(u32(z.cpu().numpy()), u32(want))
+
+
+def test_causal_softmax_ignores_masked_values(rp):
+    x = rows_input(64, 64, 12000, 3.0)
+    y = rp.softmax_rows(x, causal_first=0)
+    x2 = x.clone()
+    mask = torch.triu(torch.ones(64, 64, dtype=torch.bool, device=DEV), diagonal=1)
+    x2[mask] = float("nan")
+    assert torch.equal(rp.softmax_rows(x2, causal_first=0), y)
+    assert torch.equal(rp.softmax_rows(x, causal_first=64), rp.softmax_rows(x))
+    assert torch.equal(rp.softmax_rows(x, causal_first=1 << 62), rp.softmax_rows(x))
+
+
+@pytest.mark.parametrize("cols,period", [(64, 16), (2048, 100), (40000, 3)])
+def test_causal_softmax_with_period(rp, orc, cols, period):
+    rows = 3 * period if cols <= 2048 else 6
+    x = rows_input(rows, cols, 13000 + cols, 3.0)
+    want = orc.softmax_rows_causal(x.cpu().numpy(), 5, period)
+    got = rp.softmax_rows(x, causal_first=5, causal_period=period)
+    assert np.array_equal(u32(got.cpu().numpy()), u32(want))

@@ -112,7 +112,8 @@ def _batched_operand(X, name):
 
 
 def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = ACT_NONE,
-                 residual=None, config: int = -1, loader: int = LOADER_AUTO, stream=None):
+                 residual=None, causal_first: int = -1, config: int = -1, loader: int = LOADER_AUTO,
+                 stream=None):
     """out[b] = epilogue(A[b] @ B[b]) with the order-fixed k-chain, then
     y = alpha*acc, + bias[j], GeLU (act=ACT_GELU), + residual[b][i][j], each one
     binary32 rounding (repops_gemm_f32_batched).
@@ -121,7 +122,9 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
     matrix row-major or a transposed view, batches at any stride (attention
     heads as column blocks: X.view(T, H, d).transpose(0, 1)).  out: (batch, M,
     N) or (M, N), unit column stride, batches stacked or interleaved.
-    residual: shaped like out; may be out itself.  bias: (N,) contiguous."""
+    residual: shaped like out; may be out itself.  bias: (N,) contiguous.
+    causal_first >= 0: elements with j > causal_first + i are left unspecified
+    (whole tiles above that boundary are skipped)."""
     import torch
     L = load()
     pa, lda, sa, ta, ba = _batched_operand(A, "A")
@@ -159,7 +162,7 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
         pbias = bias.data_ptr()
     rc = L.repops_gemm_f32_batched(config, loader, ta, tb, nb, M, N, K, pa, lda, sa, pb, ldb, sb,
                                    out.data_ptr(), ldc, sc, ctypes.c_float(alpha), pbias, int(act),
-                                   pr, ldr, sr, _stream_handle(stream))
+                                   pr, ldr, sr, int(causal_first), _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32_batched")
     return out
 
@@ -353,14 +356,23 @@ def _row_out(x, out):
     return out
 
 
-def softmax_rows(x, out=None, *, stream=None):
-    """Row softmax with the order-fixed max/sum trees and the library's exp."""
+def softmax_rows(x, out=None, *, causal_first=None, causal_period=None, stream=None):
+    """Row softmax with the order-fixed max/sum trees and the library's exp.
+    causal_first=p: row i sees only its first p + (i mod causal_period) + 1
+    values (queries at positions p, p + 1, ...; the period defaults to the row
+    count), +0 after (repops_softmax_rows_causal_f32)."""
     L = load()
     px, ldx = _row_operand(x, "x")
     out = _row_out(x, out)
     py, ldy = _row_operand(out, "out")
-    rc = L.repops_softmax_rows_f32(x.shape[0], x.shape[1], px, ldx, py, ldy, _stream_handle(stream))
-    _capi.check(rc, "repops_softmax_rows_f32")
+    if causal_first is None:
+        rc = L.repops_softmax_rows_f32(x.shape[0], x.shape[1], px, ldx, py, ldy, _stream_handle(stream))
+        _capi.check(rc, "repops_softmax_rows_f32")
+    else:
+        period = int(causal_period) if causal_period is not None else max(x.shape[0], 1)
+        rc = L.repops_softmax_rows_causal_f32(x.shape[0], x.shape[1], px, ldx, py, ldy, int(causal_first),
+                                              period, _stream_handle(stream))
+        _capi.check(rc, "repops_softmax_rows_causal_f32")
     return out
 
 

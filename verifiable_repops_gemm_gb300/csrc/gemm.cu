@@ -67,11 +67,14 @@ int occupancy_of(int dev, int c) {
 }
 
 // Picks the configuration with the smallest modelled time: each SM runs
-// ceil(tiles / SMs) tiles, `conc` of them at once; an SM with fewer than 8
-// resident consumer warps is modelled as proportionally slower; per-thread
-// efficiency falls with the thread tile (shared-memory loads per FP32
-// instruction).
-int choose_config(int64_t M, int64_t N, int64_t batch = 1) {
+// ceil(tiles / SMs) tiles, `conc` of them at once; an SM with fewer resident
+// consumer warps than it needs to hide the ring's fill and the epilogue is
+// modelled as proportionally slower -- 8 warps for long k-chains, more as K
+// shrinks below 256 (each tile then has few k-slices to overlap them with);
+// per-thread efficiency falls with the thread tile (shared-memory loads per
+// FP32 instruction).  Measured on short-K batched attention (K = 64): 64x64
+// tiles 1.6x faster than 64x128.
+int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) {
     DeviceInfo di;
     if (current_device_info(&di) != REPOPS_OK || di.device < 0 || di.device >= kMaxDevices) return 0;
     double best_t = 0;
@@ -84,10 +87,11 @@ int choose_config(int64_t M, int64_t N, int64_t batch = 1) {
         const double conc = std::min<double>(occupancy_of(di.device, c), per_sm);
         const double rounds = std::ceil(per_sm / conc);
         const double warps = conc * ci.threads / 32.0;
+        const double need = std::min(32.0, 8.0 * std::max(1.0, 256.0 / double(std::max<int64_t>(K, 1))));
         // two or more CTAs per SM hide each other's ring refills and epilogues:
         // 64x128 tiles measured 2-5% faster than 128x128 at 8192^3
         const double eff = double(ci.tm * ci.tn) / double(ci.tm * ci.tn + ci.tm + ci.tn) *
-                           std::min(1.0, warps / 8.0) * (conc >= 2 ? 1.03 : 1.0);
+                           std::min(1.0, warps / need) * (conc >= 2 ? 1.03 : 1.0);
         const double t = rounds * conc * double(ci.bm) * double(ci.bn) / eff;
         if (c == 0 || t < best_t * 0.999) { best_t = t; best = c; }
     }
@@ -184,7 +188,7 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
 
-    const int cfg = config >= 0 ? config : choose_config(M, N);
+    const int cfg = config >= 0 ? config : choose_config(M, N, K);
     bool tma_ok = gemm_tma_eligible(p);
     if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
 
@@ -256,8 +260,9 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
                           int64_t K, const float *A, int64_t lda, int64_t strideA, const float *B, int64_t ldb,
                           int64_t strideB, float *C, int64_t ldc, int64_t strideC, float alpha,
                           const float *bias, int act, const float *R, int64_t ldr, int64_t strideR,
-                          cudaStream_t stream) {
+                          int64_t causal_first, cudaStream_t stream) {
     if (batch < 0 || M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
+    if (causal_first < -1) return REPOPS_ERR_INVALID_ARG;
     if (strideA < 0 || strideB < 0 || strideC < 0 || strideR < 0) return REPOPS_ERR_INVALID_ARG;
     if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
     if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC)
@@ -312,10 +317,11 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     p.R = R;
     p.ldr = ldr;
     p.strideR = batch > 1 ? strideR : 0;
+    p.causal = causal_first < N ? causal_first : -1;   // from N on, no tile lies above the boundary
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
 
-    const int cfg = config >= 0 ? config : choose_config(M, N, batch);
+    const int cfg = config >= 0 ? config : choose_config(M, N, K, batch);
     // K == 0 has no k-slices to copy: the cp.async kernel runs the epilogue on +0
     const bool tma_ok = K > 0 && gemm_tma_eligible(p);
     if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
@@ -403,9 +409,10 @@ extern "C" int repops_gemm_f32_batched(int config, int loader, int transA, int t
                                        int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
                                        float *C, int64_t ldc, int64_t strideC, float alpha,
                                        const float *bias, int act, const float *R, int64_t ldr,
-                                       int64_t strideR, cudaStream_t stream) {
+                                       int64_t strideR, int64_t causal_first, cudaStream_t stream) {
     return gemm_dispatch_batched(config, loader, transA, transB, batch, M, N, K, A, lda, strideA, B, ldb,
-                                 strideB, C, ldc, strideC, alpha, bias, act, R, ldr, strideR, stream);
+                                 strideB, C, ldc, strideC, alpha, bias, act, R, ldr, strideR, causal_first,
+                                 stream);
 }
 
 extern "C" int repops_gemm_config_count(void) { return kGemmConfigCount; }
@@ -422,7 +429,6 @@ extern "C" int repops_gemm_config_info(int config, int *bm, int *bn, int *thread
 }
 
 extern "C" int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K) {
-    (void)K;
     if (M <= 0 || N <= 0) return -1;
-    return choose_config(M, N);
+    return choose_config(M, N, std::max<int64_t>(K, 1));
 }

@@ -28,6 +28,7 @@ struct GemmProblem {
     int act = 0;                                      // 0 none, 1 GeLU
     const float *R = nullptr;                         // residual, or null
     int64_t ldr = 0, strideR = 0;
+    int64_t causal = -1;   // >= 0: tiles wholly above j = causal + i are skipped
 };
 
 struct GemmConfigInfo {

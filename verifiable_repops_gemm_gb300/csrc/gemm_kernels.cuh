@@ -300,10 +300,19 @@ struct ExArgs {
     int act;               // 0 none, 1 GeLU
     const float *R;        // residual of batch 0 or null; batch b at R + b*sR
     int64_t ldr, sR;
+    int64_t causal;        // >= 0: a tile wholly above j = causal + i is skipped
 };
 
-// The epilogue, element by element after the whole k-chain, then the store.
-// The element loop is not unrolled: one copy of the GeLU code per kernel.
+// True when every element (i, j) of the tile has j > causal + i: the tile is
+// neither computed nor written.
+template <int BM>
+__device__ __forceinline__ bool tile_above_causal(const ExArgs &ep, int64_t m0, int64_t n0) {
+    return ep.causal >= 0 && n0 > m0 + (BM - 1) + ep.causal;
+}
+
+// The epilogue after the whole k-chain of every element, then the store.
+// Unrolled over the thread's TM x TN results (registers, independent chains);
+// fl(1 * acc) = acc, so alpha = 1 skips the multiply.
 template <class T, bool A_KIN, bool B_KIN>
 __device__ __forceinline__ void store_tile_ex(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
                                               int64_t m0, int64_t n0, int abase, int bbase,
@@ -311,17 +320,52 @@ __device__ __forceinline__ void store_tile_ex(float *__restrict__ C, int64_t ldc
                                               const float *__restrict__ Rb) {
     float acc[T::TM][T::TN];
     pacc.to_float(acc);
-#pragma unroll 1
-    for (int e = 0; e < T::TM * T::TN; ++e) {
-        const int r = e / T::TN, c = e % T::TN;
-        const int64_t gm = m0 + a_row<A_KIN>(abase, r), gn = n0 + b_col<B_KIN>(bbase, c);
-        float y = __fmul_rn(acc[r][c], ep.alpha);
-        if (gm < M && gn < N) {
-            if (ep.bias) y = __fadd_rn(y, ep.bias[gn]);
-            if (ep.act == 1) y = gelu_fixed(y);
-            if (Rb) y = __fadd_rn(y, Rb[gm * ep.ldr + gn]);
+    if (ep.alpha != 1.0f) {
+#pragma unroll
+        for (int r = 0; r < T::TM; ++r)
+#pragma unroll
+            for (int c = 0; c < T::TN; ++c) acc[r][c] = __fmul_rn(acc[r][c], ep.alpha);
+    }
+    if (ep.bias) {
+#pragma unroll
+        for (int c = 0; c < T::TN; ++c) {
+            const int64_t gn = n0 + b_col<B_KIN>(bbase, c);
+            const float bv = gn < N ? ep.bias[gn] : 0.0f;   // columns past N are not stored
+#pragma unroll
+            for (int r = 0; r < T::TM; ++r) acc[r][c] = __fadd_rn(acc[r][c], bv);
         }
-        acc[r][c] = y;
+    }
+    if (ep.act == 1) {
+        // four independent GeLUs per trip of a loop that is not unrolled:
+        // the fully unrolled form (TM*TN inlined copies) measured slower, its
+        // code crowding out the main loop of the CTA sharing the SM
+        float v[T::TM * T::TN];
+#pragma unroll
+        for (int r = 0; r < T::TM; ++r)
+#pragma unroll
+            for (int c = 0; c < T::TN; ++c) v[r * T::TN + c] = acc[r][c];
+#pragma unroll 1
+        for (int e = 0; e < T::TM * T::TN; e += 4) {
+            const float y0 = gelu_fixed(v[e]), y1 = gelu_fixed(v[e + 1]);
+            const float y2 = gelu_fixed(v[e + 2]), y3 = gelu_fixed(v[e + 3]);
+            v[e] = y0; v[e + 1] = y1; v[e + 2] = y2; v[e + 3] = y3;
+        }
+#pragma unroll
+        for (int r = 0; r < T::TM; ++r)
+#pragma unroll
+            for (int c = 0; c < T::TN; ++c) acc[r][c] = v[r * T::TN + c];
+    }
+    if (Rb) {
+#pragma unroll
+        for (int r = 0; r < T::TM; ++r) {
+            const int64_t gm = m0 + a_row<A_KIN>(abase, r);
+            if (gm >= M) break;   // rows increase with r; later rows are not stored
+#pragma unroll
+            for (int c = 0; c < T::TN; ++c) {
+                const int64_t gn = n0 + b_col<B_KIN>(bbase, c);
+                if (gn < N) acc[r][c] = __fadd_rn(acc[r][c], Rb[gm * ep.ldr + gn]);
+            }
+        }
     }
     store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec);
 }
@@ -355,6 +399,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
     const int KT = int((K + BK - 1) / BK);
+    if (EX && tile_above_causal<T::BM>(ep, m0, n0)) return;   // the whole CTA, before any barrier
 
     if (tid == T::THREADS) {
         prefetch_tensormap(&tmA);
@@ -498,6 +543,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
     tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
     const int KT = int((K + BK - 1) / BK);
+    if (EX && tile_above_causal<T::BM>(ep, m0, n0)) return;   // the whole CTA, before any barrier
 
 #pragma unroll 1
     for (int s = 0; s < T::STAGES - 1; ++s) {
@@ -593,6 +639,7 @@ inline bool make_operand_map(CUtensorMap *map, const float *base, int64_t inner,
 inline ExArgs ex_args(const GemmProblem &p) {
     ExArgs ep{};
     ep.alpha = 1.0f;
+    ep.causal = -1;
     if (!p.ex) return ep;
     ep.sA = p.strideA; ep.sB = p.strideB; ep.sC = p.strideC;
     ep.zA = p.batch > 1 && p.strideA != 0;
@@ -603,6 +650,7 @@ inline ExArgs ex_args(const GemmProblem &p) {
     ep.R = p.R;
     ep.ldr = p.ldr;
     ep.sR = p.strideR;
+    ep.causal = p.causal;
     return ep;
 }
 

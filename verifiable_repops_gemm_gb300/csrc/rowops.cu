@@ -258,7 +258,7 @@ template <int T, int R, int NP>
 constexpr size_t kParamBytes =
     kStageBytes<T, R> + size_t(NP) * T * R * RUN * sizeof(float) <= 200 * 1024 ? size_t(NP) * T * R * RUN * 4 : 0;
 
-// The row loop shared by the three row kernels: body(rr) turns the row's
+// The row loop shared by the three row kernels: body(rr, row) turns the row's
 // values in rr into its outputs.  x, y and their leading dimensions are
 // 16-byte aligned (other rows take the long-row kernel).
 template <int T, int R, class Body>
@@ -282,7 +282,7 @@ __device__ __forceinline__ void for_each_row(int64_t rows, int64_t n, const floa
             if (next < rows) stage_in<T, R>(in, x + next * ldx, n);
             cp_async_commit();
         }
-        body(rr);
+        body(rr, row);
         write_stage(rr, out);
         __syncwarp();
         stage_out<T, R>(out, y + row * ldy, n);
@@ -305,11 +305,22 @@ struct Square {
 template <int T, int R>
 __global__ void __launch_bounds__(T)
 softmax_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx, float *__restrict__ y,
-                    int64_t ldy) {
+                    int64_t ldy, int64_t first, int64_t period) {
     __shared__ float gbuf[2][RUN];
     int phase = 0;
     const int runs = int((n + RUN - 1) / RUN);
-    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr) {
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr, int64_t row) {
+        if (first >= 0) {
+            // causal: scores past position first + row become -inf, so their
+            // exp is +0; adding +0 to a sum of non-negative terms changes no
+            // bit, and the result is the softmax of the prefix, then +0
+            const int64_t L = first + row % period + 1;
+#pragma unroll
+            for (int j = 0; j < R; ++j)
+#pragma unroll
+                for (int i = 0; i < RUN; ++i)
+                    if (int64_t(threadIdx.x + j * T) * RUN + i >= L) rr.v[j][i] = -__int_as_float(0x7f800000);
+        }
         const float m = rr.template reduce<Op::Max>(Ident(), gbuf, phase, runs);
         // element-wise steps need no guard: values past the row end are never
         // folded or stored
@@ -341,7 +352,7 @@ layernorm_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int6
         stage_in<T, R>(pg, gamma, n);   // waited for with the first row
         stage_in<T, R>(pb, beta, n);
     }
-    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr) {
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr, int64_t) {
         const float mean = __fdiv_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs), nf);
 #pragma unroll
         for (int j = 0; j < R; ++j)
@@ -379,7 +390,7 @@ rmsnorm_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_
     const float nf = float(n);
     float4 *pg = stage_mem + kStageBytes<T, R> / 16;
     if (kParamBytes<T, R, 1> != 0 && psm && blockIdx.x < rows) stage_in<T, R>(pg, gamma, n);
-    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr) {
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr, int64_t) {
         const float ms = __fdiv_rn(rr.template reduce<Op::Sum>(Square(), gbuf, phase, runs), nf);
         const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
 #pragma unroll
@@ -424,11 +435,12 @@ struct SquareShift {
 };
 
 // kind 0 = softmax, 1 = LayerNorm, 2 = RMSNorm.  Each thread writes only the
-// runs it read in the same pass, so y may be x.
+// runs it read in the same pass, so y may be x.  first >= 0: causal softmax,
+// row r over its first min(n, first + (r mod period) + 1) values, +0 after.
 __global__ void __launch_bounds__(256)
 rows_generic_kernel(int kind, int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
                     const float *__restrict__ gamma, const float *__restrict__ beta, float eps,
-                    float *__restrict__ y, int64_t ldy) {
+                    float *__restrict__ y, int64_t ldy, int64_t first, int64_t period) {
     extern __shared__ float buf[];   // runs + ceil(runs / 32) floats
     __shared__ float bcast;
     const int runs = int((n + RUN - 1) / RUN);
@@ -438,11 +450,12 @@ rows_generic_kernel(int kind, int64_t rows, int64_t n, const float *__restrict__
         const float *row = x + r * ldx;
         float *out = y + r * ldy;
         if (kind == 0) {
-            const float m = generic_reduce<Op::Max>(row, n, Ident(), buf, buf2, &bcast);
-            const float inv = __frcp_rn(generic_reduce<Op::Sum>(row, n, ExpShift{m}, buf, buf2, &bcast));
+            const int64_t L = first >= 0 ? imin64(n, first + r % period + 1) : n;
+            const float m = generic_reduce<Op::Max>(row, L, Ident(), buf, buf2, &bcast);
+            const float inv = __frcp_rn(generic_reduce<Op::Sum>(row, L, ExpShift{m}, buf, buf2, &bcast));
             for (int j = threadIdx.x; j < runs; j += blockDim.x)
                 for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i)
-                    out[i] = __fmul_rn(exp_fixed(__fsub_rn(row[i], m)), inv);
+                    out[i] = i < L ? __fmul_rn(exp_fixed(__fsub_rn(row[i], m)), inv) : 0.0f;
         } else if (kind == 1) {
             const float mean = __fdiv_rn(generic_reduce<Op::Sum>(row, n, Ident(), buf, buf2, &bcast), nf);
             const float var = __fdiv_rn(generic_reduce<Op::Sum>(row, n, SquareShift{mean}, buf, buf2, &bcast), nf);
@@ -523,10 +536,13 @@ int launch_persistent(Kern kern, int threads, size_t smem, int64_t rows, cudaStr
 // kind 0 = softmax, 1 = LayerNorm, 2 = RMSNorm
 template <int T, int R>
 int launch_fast(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma,
-                const float *beta, float eps, float *y, int64_t ldy, cudaStream_t s) {
+                const float *beta, float eps, float *y, int64_t ldy, int64_t first, int64_t period,
+                cudaStream_t s) {
     const int pvec = reinterpret_cast<uintptr_t>(gamma) % 16 == 0 && reinterpret_cast<uintptr_t>(beta) % 16 == 0;
     const size_t smem = kStageBytes<T, R>;
-    if (kind == 0) return launch_persistent(softmax_rows_kernel<T, R>, T, smem, rows, s, rows, n, x, ldx, y, ldy);
+    if (kind == 0)
+        return launch_persistent(softmax_rows_kernel<T, R>, T, smem, rows, s, rows, n, x, ldx, y, ldy, first,
+                                 period);
     if (kind == 1) {
         const size_t p = pvec ? kParamBytes<T, R, 2> : 0;
         return launch_persistent(layernorm_rows_kernel<T, R>, T, smem + p, rows, s, rows, n, x, ldx, gamma, beta,
@@ -538,21 +554,22 @@ int launch_fast(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, 
 }
 
 int run_rows(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma, const float *beta,
-             float eps, float *y, int64_t ldy, cudaStream_t s) {
+             float eps, float *y, int64_t ldy, cudaStream_t s, int64_t first = -1, int64_t period = 1) {
     int64_t runs = (n + RUN - 1) / RUN;
     // threads per row: enough for one run each up to 256, then up to 4 runs per thread
     // rows that are not 16-byte aligned take the long-row kernel (same bits)
     if (!rows_vec_ok(x, ldx, y, ldy)) runs = MAX_FAST_RUNS + 1;
-    if (runs <= 32) return launch_fast<32, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
-    if (runs <= 64) return launch_fast<64, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
-    if (runs <= 128) return launch_fast<128, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
-    if (runs <= 256) return launch_fast<256, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
-    if (runs <= 512) return launch_fast<256, 2>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
-    if (runs <= MAX_FAST_RUNS) return launch_fast<256, 4>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, s);
+    if (runs <= 32) return launch_fast<32, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    if (runs <= 64) return launch_fast<64, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    if (runs <= 128) return launch_fast<128, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    if (runs <= 256) return launch_fast<256, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    if (runs <= 512) return launch_fast<256, 2>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    if (runs <= MAX_FAST_RUNS) return launch_fast<256, 4>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(rows_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
-    rows_generic_kernel<<<grid_for_rows(rows), 256, smem, s>>>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy);
+    rows_generic_kernel<<<grid_for_rows(rows), 256, smem, s>>>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy,
+                                                               first, period);
     return check_launch();
 }
 
@@ -566,6 +583,16 @@ extern "C" int repops_softmax_rows_f32(int64_t rows, int64_t cols, const float *
     int rc = check_rows(rows, cols, x, ldx, y, ldy);
     if (rc != REPOPS_OK || rows == 0 || cols == 0) return rc;
     return run_rows(0, rows, cols, x, ldx, nullptr, nullptr, 0.0f, y, ldy, stream);
+}
+
+extern "C" int repops_softmax_rows_causal_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
+                                              int64_t ldy, int64_t first, int64_t period, cudaStream_t stream) {
+    if (first < 0 || period < 1) return REPOPS_ERR_INVALID_ARG;
+    int rc = check_rows(rows, cols, x, ldx, y, ldy);
+    if (rc != REPOPS_OK || rows == 0 || cols == 0) return rc;
+    // from first >= cols on, every row sees all its columns
+    return run_rows(0, rows, cols, x, ldx, nullptr, nullptr, 0.0f, y, ldy, stream, first < cols ? first : -1,
+                    period);
 }
 
 extern "C" int repops_layernorm_rows_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
