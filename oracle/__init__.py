@@ -99,6 +99,14 @@ def lib():
         L.oracle_rmsnorm_rows.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64]
         L.oracle_softmax_rows_causal.restype = None
         L.oracle_softmax_rows_causal.argtypes = [i64, i64, vp, i64, vp, i64, i64, i64]
+        L.oracle_convert.restype = None
+        L.oracle_convert.argtypes = [i64, vp, i32, vp, i32]
+        L.oracle_gemm_typed.restype = None
+        L.oracle_gemm_typed.argtypes = [i64, i64, i64, vp, i32, i64, i32, vp, i32, i64, i32, vp, i32, i64]
+        L.oracle_mean_sgd_typed.restype = i32
+        L.oracle_mean_sgd_typed.argtypes = [i32, i64, vp, i32, vp, f32, vp]
+        L.oracle_rolling_hash.restype = None
+        L.oracle_rolling_hash.argtypes = [i64, i64, vp, i64, i64, vp, i64]
         L.oracle_gemm_batched.restype = None
         L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
                                           vp, i64, i64, f32, vp, i32, vp, i64, i64]
@@ -378,3 +386,61 @@ def softmax_rows_causal(X: np.ndarray, first: int, period: int = None) -> np.nda
     if rows and cols:
         L.oracle_softmax_rows_causal(rows, cols, _ptr(X), cols, _ptr(Y), cols, first, period or rows)
     return Y
+
+
+F32, F16, BF16 = 0, 1, 2
+
+
+def _storage(a, t):
+    """Flat contiguous buffer of storage type t (F32: float32; F16/BF16: uint16 bits)."""
+    return np.ascontiguousarray(a, dtype=np.float32 if t == F32 else np.uint16)
+
+
+def convert(x, src_type: int, dst_type: int) -> np.ndarray:
+    """Element-wise conversion between stored types (exact widening, round to
+    nearest even narrowing); half types travel as their uint16 bit patterns."""
+    a = _storage(x, src_type)
+    out = np.empty(a.shape, dtype=np.float32 if dst_type == F32 else np.uint16)
+    if a.size:
+        lib().oracle_convert(a.size, _ptr(a), src_type, _ptr(out), dst_type)
+    return out
+
+
+def gemm_typed(A, typeA: int, B, typeB: int, typeC: int) -> np.ndarray:
+    """C = A @ B on stored operands (row-major 2-D arrays of their storage
+    type), computed on the exactly widened values, narrowed once to typeC."""
+    L = lib()
+    A_ = _storage(A, typeA)
+    B_ = _storage(B, typeB)
+    M, K = A_.shape
+    N = B_.shape[1]
+    C = np.empty((M, N), dtype=np.float32 if typeC == F32 else np.uint16)
+    if M and N:
+        L.oracle_gemm_typed(M, N, K, _ptr(A_), typeA, max(K, 1), 0, _ptr(B_), typeB, max(N, 1), 0,
+                            _ptr(C), typeC, max(N, 1))
+    return C
+
+
+def mean_sgd_typed(grads, gtype: int, order, eta: float, theta: np.ndarray) -> np.ndarray:
+    """As mean_sgd with gradients stored as gtype; returns a new float32 theta."""
+    L = lib()
+    th = np.array(theta, dtype=np.float32, copy=True)
+    gs = [_storage(g, gtype) for g in grads]
+    ptrs = (ctypes.c_void_p * max(len(gs), 1))(*[_ptr(g) for g in gs])
+    o = np.ascontiguousarray(order, dtype=np.int32)
+    rc = L.oracle_mean_sgd_typed(len(gs), th.size, ctypes.cast(ptrs, ctypes.c_void_p), gtype, _ptr(o),
+                                 ctypes.c_float(eta), _ptr(th))
+    if rc != 0:
+        raise ValueError("bad contributor set")
+    return th
+
+
+def rolling_hash(words: np.ndarray, window: int) -> np.ndarray:
+    """(rows, width - window + 1) uint64 window hashes of a (rows, width) uint32 batch."""
+    w = np.ascontiguousarray(words, dtype=np.uint32)
+    rows, width = w.shape
+    n = width - window + 1
+    out = np.empty((rows, max(n, 0)), dtype=np.uint64)
+    if rows and n > 0:
+        lib().oracle_rolling_hash(rows, width, _ptr(w), width, window, _ptr(out), n)
+    return out

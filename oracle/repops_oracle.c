@@ -752,3 +752,164 @@ void oracle_gemm_batched(int transA, int transB, int64_t batch, int64_t M, int64
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Half-precision storage  [RepOps §3.3 limitations (IEEE-754 hardware; FP16 */
+/* support limited) and §5.3 future work (lower precision such as FP16).     */
+/* The pages fix no format rules; the library's: operands stored as IEEE    */
+/* binary16 or bfloat16 are widened exactly to binary32, the binary32        */
+/* order-fixed path computes, a half output is one round-to-nearest-even.]  */
+/* ------------------------------------------------------------------------ */
+
+enum { ORACLE_F32 = 0, ORACLE_F16 = 1, ORACLE_BF16 = 2 };
+
+static uint32_t f32_bits(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float f32_from(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* binary16 -> binary32, exact: subnormals m * 2^-24, normals (1.m) 2^(e-15). */
+float oracle_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) << 31;
+    uint32_t e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+    if (e == 0) {
+        float v = (float)m * 5.9604644775390625e-08f;      /* m * 2^-24: exact */
+        return f32_from(f32_bits(v) | sign);
+    }
+    if (e == 31) return f32_from(sign | 0x7f800000u | (m << 13));   /* inf, NaN */
+    return f32_from(sign | ((e - 15 + 127) << 23) | (m << 13));
+}
+
+/* bfloat16 -> binary32, exact: the 16 bits are the high half. */
+float oracle_bf16_to_f32(uint16_t b) { return f32_from((uint32_t)b << 16); }
+
+/* binary32 -> binary16, round to nearest, ties to even.  The value M * 2^E
+ * (M the 24-bit significand) is rounded to a multiple of the binary16 quantum
+ * 2^Q, Q = max(e - 10, -24) for e = floor(log2 |x|); the count r of quanta
+ * gives the encoding ((Q + 24) << 10) + r, which carries into the exponent when
+ * r reaches the next power of two.  Past the largest finite value: infinity.
+ * NaN: a quiet NaN keeping the top payload bits. */
+uint16_t oracle_f32_to_f16(float f)
+{
+    uint32_t x = f32_bits(f);
+    uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+    uint32_t ax = x & 0x7fffffffu;
+    if (ax > 0x7f800000u) return (uint16_t)(sign | 0x7e00u | ((ax >> 13) & 0x3ffu));
+    if (ax == 0x7f800000u) return (uint16_t)(sign | 0x7c00u);
+    if (ax == 0) return sign;
+    int32_t E;
+    uint64_t M;
+    if ((ax >> 23) == 0) { M = ax; E = -149; }                       /* binary32 subnormal */
+    else { M = (ax & 0x7fffffu) | 0x800000u; E = (int32_t)(ax >> 23) - 127 - 23; }
+    int32_t e = E + 23;
+    while ((M >> (e - E)) == 0) --e;                                 /* subnormal input: true exponent */
+    int32_t Q = e - 10 > -24 ? e - 10 : -24;
+    int32_t s = Q - E;                                               /* >= 13 */
+    uint64_t r, rem, half;
+    if (s > 40) { r = 0; rem = M; half = (uint64_t)1 << 40; }
+    else {
+        r = M >> s;
+        rem = M - (r << s);
+        half = (uint64_t)1 << (s - 1);
+    }
+    if (rem > half || (rem == half && (r & 1))) ++r;
+    uint32_t bits = ((uint32_t)(Q + 24) << 10) + (uint32_t)r;
+    if (bits >= 0x7c00u) bits = 0x7c00u;
+    return (uint16_t)(sign | bits);
+}
+
+/* binary32 -> bfloat16, round to nearest, ties to even: bfloat16 keeps the
+ * exponent range, so rounding is on the low 16 bits alone -- adding
+ * 0x7fff + (bit 16) carries into the kept half exactly when the discarded half
+ * is above one half, or equal to it with the kept half odd (a carry out of the
+ * largest finite value gives infinity).  NaN: quiet, top payload bits kept. */
+uint16_t oracle_f32_to_bf16(float f)
+{
+    uint32_t x = f32_bits(f);
+    if ((x & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((x >> 16) | 0x40u);
+    uint32_t rounded = x + 0x7fffu + ((x >> 16) & 1u);
+    return (uint16_t)(rounded >> 16);
+}
+
+static float load_as_f32(const void *p, int64_t i, int type)
+{
+    if (type == ORACLE_F16) return oracle_f16_to_f32(((const uint16_t *)p)[i]);
+    if (type == ORACLE_BF16) return oracle_bf16_to_f32(((const uint16_t *)p)[i]);
+    return ((const float *)p)[i];
+}
+
+static void store_from_f32(void *p, int64_t i, int type, float v)
+{
+    if (type == ORACLE_F16) ((uint16_t *)p)[i] = oracle_f32_to_f16(v);
+    else if (type == ORACLE_BF16) ((uint16_t *)p)[i] = oracle_f32_to_bf16(v);
+    else ((float *)p)[i] = v;
+}
+
+/* dst[i] = src[i] converted: widening exact, narrowing round-to-nearest-even. */
+void oracle_convert(int64_t n, const void *src, int src_type, void *dst, int dst_type)
+{
+    for (int64_t i = 0; i < n; ++i) store_from_f32(dst, i, dst_type, load_as_f32(src, i, src_type));
+}
+
+/* GEMM on stored operands of any of the three types: every element widened to
+ * binary32 (exact), the k-chain of oracle_gemm_f32, the result narrowed once
+ * to C's type. */
+void oracle_gemm_typed(int64_t M, int64_t N, int64_t K,
+                       const void *A, int typeA, int64_t lda, int transA,
+                       const void *B, int typeB, int64_t ldb, int transB,
+                       void *C, int typeC, int64_t ldc)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            float s = 0.0f;
+            for (int64_t q = 0; q < K; ++q) {
+                float a = load_as_f32(A, transA ? q * lda + i : i * lda + q, typeA);
+                float b = load_as_f32(B, transB ? j * ldb + q : q * ldb + j, typeB);
+                float prod = a * b;
+                s = s + prod;
+            }
+            store_from_f32(C, i * ldc + j, typeC, s);
+        }
+    }
+}
+
+/* oracle_mean_sgd with gradients stored as `gtype` (widened exactly); theta
+ * stays binary32 (the master weights). */
+int oracle_mean_sgd_typed(int nC, int64_t len, const void *const *grads, int gtype,
+                          const int *order, float eta, float *theta)
+{
+    if (nC <= 0) return -1;
+    for (int64_t e = 0; e < len; ++e) {
+        float S = load_as_f32(grads[order[0]], e, gtype);
+        for (int r = 1; r < nC; ++r) S = S + load_as_f32(grads[order[r]], e, gtype);
+        float gbar = S / (float)nC;
+        float step = eta * gbar;
+        float updated = theta[e] - step;
+        theta[e] = updated;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rolling hashes of batch rows  [ZKDV page, proof.start: rolling_window     */
+/* hashes within each committed batch row, window at most the row's packed   */
+/* width; the protocol commits a rectangular uint32 batch.  The page names   */
+/* no hash; the library's: the Rabin-Karp polynomial of the window's words   */
+/* modulo the Mersenne prime 2^61 - 1.]                                      */
+/* ------------------------------------------------------------------------ */
+
+#define ROLL_P ((((uint64_t)1) << 61) - 1)
+#define ROLL_B 4294967311ull     /* the smallest prime above 2^32 */
+
+/* out[r*ldo + i] = (sum_{t<W} words[r*ldw + i + t] * B^(W-1-t)) mod P for every
+ * window start i = 0 .. width - W, evaluated directly by Horner's rule. */
+void oracle_rolling_hash(int64_t rows, int64_t width, const uint32_t *words, int64_t ldw,
+                         int64_t W, uint64_t *out, int64_t ldo)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t i = 0; i + W <= width; ++i) {
+            unsigned __int128 h = 0;
+            for (int64_t t = 0; t < W; ++t) h = (h * ROLL_B + words[r * ldw + i + t]) % ROLL_P;
+            out[r * ldo + i] = (uint64_t)h;
+        }
+    }
+}

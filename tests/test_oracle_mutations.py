@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "repops_oracle.c")
 PINS = [os.path.join(ROOT, "tests", f) for f in
         ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py", "test_oracle_rowops.py",
-         "test_oracle_epilogue.py")]
+         "test_oracle_epilogue.py", "test_oracle_halfstore.py")]
 
 MUTATIONS = {
     "gemm: fused multiply-add": (
@@ -73,6 +73,15 @@ MUTATIONS = {
     "causal softmax: one key too many": ("int64_t L = first + i % period + 1;",
                                          "int64_t L = first + i % period + 2;"),
     "causal softmax: period ignored": ("int64_t L = first + i % period + 1;", "int64_t L = first + i + 1;"),
+    "f16: ties rounded up": ("if (rem > half || (rem == half && (r & 1))) ++r;", "if (rem >= half) ++r;"),
+    "f16: subnormals scaled by 2^-23": ("float v = (float)m * 5.9604644775390625e-08f;",
+                                        "float v = (float)m * 1.1920928955078125e-07f;"),
+    "bf16: truncation": ("uint32_t rounded = x + 0x7fffu + ((x >> 16) & 1u);", "uint32_t rounded = x;"),
+    "rolling hash: wrong base": ("#define ROLL_B 4294967311ull", "#define ROLL_B 4294967291ull"),
+    "typed gemm: q in decreasing order": ("for (int64_t q = 0; q < K; ++q) {", "for (int64_t q = K - 1; q >= 0; --q) {"),
+    "typed mean: SGD adds the step": ("float updated = theta[e] - step;", "float updated = theta[e] + step;"),
+    "typed mean: last gradient dropped": ("for (int r = 1; r < nC; ++r) S = S + load_as_f32(grads[order[r]], e, gtype);",
+                                          "for (int r = 1; r < nC - 1; ++r) S = S + load_as_f32(grads[order[r]], e, gtype);"),
     "batched: A advanced by B's stride": ("const float *Ab = A + b * strideA;", "const float *Ab = A + b * strideB;"),
 }
 
