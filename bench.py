@@ -500,6 +500,8 @@ def run_sweep(args):
         run_sweep_commitments(dev, s, flush)
     if args.sweep in ("all", "decoder"):
         run_sweep_decoder(dev, s, flush, peak)
+    if args.sweep in ("all", "halfstore"):
+        run_sweep_halfstore(dev, s, flush, peak, peaks.get("hbm_gbs", 6800.0))
 
 
 def run_sweep_gemm(dev, s, flush, peak):
@@ -653,6 +655,64 @@ def run_sweep_decoder(dev, s, flush, peak):
                       "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
 
 
+def run_sweep_halfstore(dev, s, flush, peak, hbm):
+    """Half-precision storage around the binary32 path: the mean + SGD step of
+    the hot path (16 contributors x 2^28) with bfloat16 gradients next to
+    float32 ones, a float32 -> bfloat16 conversion, the 8192^3 GEMM on
+    bfloat16 operands; and the rolling hash of a 8192 x 4096-word uint32
+    batch, window 32.  L2 flushed before each timed launch."""
+    def ev_time(fn, reps=5):
+        with torch.cuda.stream(s):
+            fn()
+            evs = []
+            for _ in range(reps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                fn()
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
+
+    nC, n = inputs.MEAN_CONTRIBUTORS, inputs.MEAN_LEN
+    theta = inputs.normal((n,), 0.02, 500, dev)
+    order = list(range(nC))
+    for name, dt, size in (("float32", torch.float32, 4), ("bfloat16", torch.bfloat16, 2)):
+        grads = [inputs.normal((n,), 1e-2, 510 + r, dev).to(dt) for r in range(nC)]
+        ms = ev_time(lambda: rp.fixed_order_mean_sgd(grads, order, 1e-3, theta, stream=s))
+        nb = n * (nC * size + 8)
+        print(json.dumps({"sweep": "mean + SGD 16 x 2^28, %s gradients" % name, "ms": ms, "gbs": nb / ms / 1e6,
+                          "frac_of_hbm": nb / ms / 1e6 / hbm}), flush=True)
+        del grads
+    x = inputs.normal((n,), 1.0, 520, dev)
+    y = torch.empty(n, dtype=torch.bfloat16, device=dev)
+    ms = ev_time(lambda: rp.convert(x, torch.bfloat16, out=y, stream=s))
+    print(json.dumps({"sweep": "convert 2^28 float32 -> bfloat16", "ms": ms, "gbs": n * 6 / ms / 1e6,
+                      "frac_of_hbm": n * 6 / ms / 1e6 / hbm}), flush=True)
+    del x, y, theta
+    N = GEMM_N
+    A = inputs.normal((N, N), 1.0, 530, dev).to(torch.bfloat16)
+    B = inputs.normal((N, N), 1.0, 531, dev).to(torch.bfloat16)
+    C = torch.empty(N, N, device=dev)
+    ms = ev_time(lambda: rp.gemm_typed(A, B, out=C, stream=s), reps=3)
+    tf = 2.0 * N ** 3 / ms / 1e9
+    print(json.dumps({"sweep": "gemm 8192^3 on bfloat16 operands (widened, binary32 k-chain)", "ms": ms,
+                      "tflops": tf, "frac_of_fp32_peak": tf / peak}), flush=True)
+    del A, B, C
+    rows, width, win = 8192, 4096, 32
+    g = torch.Generator(device=dev)
+    g.manual_seed(540)
+    words = torch.randint(-(1 << 31), 1 << 31, (rows, width), generator=g, dtype=torch.int64,
+                          device=dev).to(torch.int32)
+    out = torch.empty(rows, width - win + 1, dtype=torch.int64, device=dev)
+    ms = ev_time(lambda: rp.rolling_hash(words, win, out=out, stream=s))
+    nb = words.numel() * 4 + out.numel() * 8
+    print(json.dumps({"sweep": "rolling hash 8192 x 4096 uint32 words, window 32", "ms": ms,
+                      "hashes_per_s": out.numel() / ms * 1e3, "gbs": nb / ms / 1e6,
+                      "frac_of_hbm": nb / ms / 1e6 / hbm}), flush=True)
+
+
 def run_sweep_commitments(dev, s, flush):
     """Merkle root versus whole stored tree of the 4 GiB tensor, one inclusion
     proof and one membership check, and replayed blocks of the 16 x 2^28
@@ -717,7 +777,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
-                    choices=("all", "gemm", "rowops", "commitments", "decoder"),
+                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore"),
                     help="time every workload of a part (one JSON line each) instead of the step")
     args = ap.parse_args()
     if args.sweep:

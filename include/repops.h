@@ -57,6 +57,12 @@ typedef enum {
     REPOPS_ERR_UNSUPPORTED = -7   /* request outside the documented limits */
 } repops_status;
 
+/* Storage types of tensors whose elements the order-fixed binary32 path reads
+ * or writes (see "Half-precision storage"). */
+#define REPOPS_TYPE_F32 0    /* IEEE binary32 */
+#define REPOPS_TYPE_F16 1    /* IEEE binary16 */
+#define REPOPS_TYPE_BF16 2   /* bfloat16: the high 16 bits of a binary32 */
+
 /* Build manifest: library version, target architecture, compile flags that
  * fix the arithmetic (-fmad=false, -ftz=false, -prec-div=true, ...), and the
  * GEMM tile configurations.  The role of a "KernelManifest" ("Zoo Per-LLM
@@ -248,6 +254,17 @@ int repops_sort_ids(int n, const uint8_t *ids, const int64_t *offsets,
 int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs,
                                 const int *order, float eta, float *theta,
                                 cudaStream_t stream);
+
+/* As repops_fixed_order_mean_sgd with the gradients stored as grad_type
+ * (REPOPS_TYPE_F32, _F16 or _BF16, see "Half-precision storage" below): each
+ * gradient element is widened exactly to binary32 before the fold; theta stays
+ * binary32.  The bits equal those of repops_fixed_order_mean_sgd on the
+ * widened gradients.  Gradients need no alignment (8-byte aligned half
+ * gradients and a 16-byte aligned theta take the vector path).
+ * INVALID_ARG also for an unknown grad_type. */
+int repops_fixed_order_mean_sgd_typed(int nC, int64_t len, const void *const *ptrs,
+                                      int grad_type, const int *order, float eta,
+                                      float *theta, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* SHA-256 Merkle commitment over tensor bytes                               */
@@ -444,6 +461,60 @@ int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len,
  * repops_merkle_sha256, without ALLOC. */
 int repops_merkle_sha256_noalloc(const void *ptr, uint64_t bytes, uint32_t leaf,
                                  uint8_t *root_out, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Half-precision storage                                                    */
+/* "Verde与RepOps" §3.3 (IEEE-754 hardware needed; FP16 support limited) and */
+/* §5.3 (lower-precision training as future work).  The pages fix no format  */
+/* rules; the library's: a binary16 or bfloat16 element is widened exactly   */
+/* to binary32, the binary32 order-fixed path computes, and a half result is */
+/* narrowed once, round to nearest, ties to even (overflow to infinity,      */
+/* subnormals kept).  NaNs stay NaN (payloads not pinned).                   */
+/* ------------------------------------------------------------------------ */
+
+/* dst[i] = src[i] converted from src_type to dst_type (REPOPS_TYPE_*), i < n.
+ * src, dst (device) hold n elements each; they may be the same buffer only
+ * when both types have the same size; any other overlap is ALIAS.  INVALID_ARG
+ * for n < 0, unknown types or null pointers with n > 0. */
+int repops_convert(int64_t n, const void *src, int src_type, void *dst, int dst_type,
+                   cudaStream_t stream);
+
+/* C = A * B as repops_gemm_f32_config (same storage, transposition, config and
+ * loader arguments) with A, B and C stored as typeA, typeB, typeC: the
+ * operands are widened exactly to binary32, the order-fixed k-chain runs, and
+ * the result is narrowed once to typeC.  The bits equal repops_gemm_f32 on the
+ * widened operands, narrowed.  Half operands are widened into scratch taken
+ * with cudaMallocAsync on `stream` (4 bytes per element of each widened
+ * operand, and of C when typeC is a half type), released the same way; ALLOC
+ * when it cannot be had.  INVALID_ARG for unknown types, and as
+ * repops_gemm_f32_ex otherwise; ALIAS when C's bytes overlap A's or B's. */
+int repops_gemm_typed(int config, int loader, int transA, int transB,
+                      int64_t M, int64_t N, int64_t K,
+                      const void *A, int typeA, int64_t lda,
+                      const void *B, int typeB, int64_t ldb,
+                      void *C, int typeC, int64_t ldc,
+                      cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Rolling hashes of batch rows                                              */
+/* ZKDV page, proof.start(rolling_window=...): rolling hashes within each    */
+/* committed batch row, the window at most the row's packed width; the       */
+/* protocol commits a rectangular uint32 batch.  The page names no hash; the */
+/* library's: Rabin-Karp modulo the Mersenne prime P = 2^61 - 1.             */
+/* ------------------------------------------------------------------------ */
+
+#define REPOPS_ROLLING_HASH_BASE 4294967311ull   /* smallest prime above 2^32 */
+
+/* For every row r < rows and window start i = 0 .. width - window:
+ *   out[r*ldo + i] = (sum_{t < window} words[r*ldw + i + t] * B^(window-1-t)) mod P
+ * with B = REPOPS_ROLLING_HASH_BASE (so a window of two words maps injectively).
+ * words (device): rows x width uint32, row pitch ldw >= width; out (device):
+ * rows x (width - window + 1) uint64, row pitch ldo >= width - window + 1.
+ * 1 <= window <= width (the window must not exceed the packed row width),
+ * else INVALID_ARG; out overlapping words is ALIAS.  Exact integers: the bits
+ * do not depend on how the kernel splits a row. */
+int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32_t *words, int64_t ldw,
+                            int64_t window, uint64_t *out, int64_t ldo, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

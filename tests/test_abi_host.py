@@ -248,3 +248,31 @@ def test_causal_softmax_rejects_bad_arguments(L):
     assert c(4, 4, FAKE_A, 4, FAKE_B, 4, 0, 0, None) == -1                 # period < 1
     assert c(4, 4, FAKE_A, 4, FAKE_A + 8, 4, 0, 4, None) == -2
     assert c(0, 4, FAKE_A, 4, FAKE_B, 4, 0, 4, None) == 0
+
+
+def test_half_storage_and_rolling_hash_reject_bad_arguments(L):
+    cv = L.repops_convert
+    assert cv(-1, FAKE_A, 0, FAKE_B, 1, None) == -1
+    assert cv(8, FAKE_A, 3, FAKE_B, 1, None) == -1                     # unknown type
+    assert cv(8, FAKE_A, 0, FAKE_A + 8, 1, None) == -2                 # overlap, not in place
+    assert cv(8, FAKE_A, 0, FAKE_A, 1, None) == -2                     # in place needs equal sizes
+    assert cv(0, None, 0, None, 1, None) == 0
+    gt = L.repops_gemm_typed
+    assert gt(-1, 0, 0, 0, 4, 4, 4, FAKE_A, 5, 4, FAKE_B, 1, 4, FAKE_C, 0, 4, None) == -1   # type 5
+    assert gt(-1, 0, 0, 0, 4, 4, 4, FAKE_A, 1, 3, FAKE_B, 1, 4, FAKE_C, 0, 4, None) == -1   # lda < K
+    assert gt(-1, 0, 0, 0, 4, 4, 4, FAKE_A, 1, 4, FAKE_B, 1, 4, FAKE_A + 8, 1, 4, None) == -2
+    assert gt(-1, 0, 0, 0, 0, 4, 4, FAKE_A, 1, 4, FAKE_B, 1, 4, FAKE_C, 1, 4, None) == 0
+    ms = L.repops_fixed_order_mean_sgd_typed
+    p = (ctypes.c_void_p * 2)(FAKE_A, FAKE_A + 4096)
+    o = (ctypes.c_int * 2)(1, 0)
+    assert ms(2, 16, ctypes.cast(p, ctypes.c_void_p), 7, ctypes.cast(o, ctypes.c_void_p), ctypes.c_float(1e-3),
+              FAKE_C, None) == -1                                                        # unknown type
+    assert ms(2, 16, ctypes.cast(p, ctypes.c_void_p), 1, ctypes.cast(o, ctypes.c_void_p), ctypes.c_float(1e-3),
+              FAKE_A + 16, None) == -2                                                   # theta over a gradient
+    rh = L.repops_rolling_hash_u32
+    assert rh(4, 10, FAKE_A, 10, 0, FAKE_B, 10, None) == -1          # window 0
+    assert rh(4, 10, FAKE_A, 10, 11, FAKE_B, 10, None) == -1         # window above the row width
+    assert rh(4, 10, FAKE_A, 9, 3, FAKE_B, 8, None) == -1            # ldw < width
+    assert rh(4, 10, FAKE_A, 10, 3, FAKE_B, 7, None) == -1           # ldo < width - window + 1
+    assert rh(4, 10, FAKE_A, 10, 3, FAKE_A + 40, 8, None) == -2
+    assert rh(0, 10, FAKE_A, 10, 3, FAKE_B, 8, None) == 0

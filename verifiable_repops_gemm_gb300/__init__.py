@@ -21,17 +21,21 @@ memory and streams.
   rmsnorm_rows / gelu               ("Verde与RepOps" §3.2, §4.3)
   gemm_batched(A, B, ...)           batched GEMM with a fused epilogue
                                     (alpha, bias, GeLU, residual)
+  convert / gemm_typed              binary16 / bfloat16 storage around the
+                                    binary32 path ("Verde与RepOps" §3.3, §5.3)
+  rolling_hash(words, window)       Rabin-Karp hashes of uint32 batch rows (ZKDV)
 """
 import ctypes
 
 from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA,
-                    MEAN_MAX_CONTRIBUTORS, RepopsError, load)
+                    MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
 __all__ = ["load", "version", "gemm", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
+           "convert", "gemm_typed", "rolling_hash", "TYPE_F32", "TYPE_F16", "TYPE_BF16",
            "device_status", "RepopsError", "ACT_NONE", "ACT_GELU",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
 
@@ -208,13 +212,29 @@ def sort_ids(ids) -> list:
     return [int(order[i]) for i in range(n)]
 
 
-def fixed_order_mean_sgd(grads, order, eta: float, theta, *, stream=None):
+def _storage_type(dtype):
+    import torch
+    t = {torch.float32: TYPE_F32, torch.float16: TYPE_F16, torch.bfloat16: TYPE_BF16}.get(dtype)
+    if t is None:
+        raise TypeError("storage type must be float32, float16 or bfloat16, not %s" % dtype)
+    return t
+
+
+def fixed_order_mean_sgd(grads, order, eta: float, theta, *, grad_dtype=None, stream=None):
     """theta -= eta * (left fold of grads in `order`) / len(grads), in place.
 
-    grads: sequence of float32 CUDA tensors (or raw device pointers) with
-    theta.numel() elements each; order: permutation of range(len(grads))."""
+    grads: sequence of CUDA tensors (or raw device pointers) with theta.numel()
+    elements each, stored as float32, float16 or bfloat16 (widened exactly;
+    theta stays float32); order: permutation of range(len(grads)).
+    grad_dtype: the gradients' dtype when they are raw pointers."""
     L = load()
     nC = len(grads)
+    dts = {g.dtype for g in grads if not isinstance(g, int)}
+    if grad_dtype is not None:
+        dts.add(grad_dtype)
+    if len(dts) > 1:
+        raise TypeError("gradients of different dtypes")
+    gtype = _storage_type(dts.pop()) if dts else TYPE_F32
     ptrs = [g if isinstance(g, int) else g.data_ptr() for g in grads]
     for g in grads:
         if not isinstance(g, int) and g.numel() != theta.numel():
@@ -223,10 +243,16 @@ def fixed_order_mean_sgd(grads, order, eta: float, theta, *, stream=None):
     oarr = (ctypes.c_int * max(nC, 1))(*[int(x) for x in order])
     if len(order) != nC:
         raise ValueError("order must have one entry per contributor")
-    rc = L.repops_fixed_order_mean_sgd(nC, theta.numel(), ctypes.cast(parr, ctypes.c_void_p),
-                                       ctypes.cast(oarr, ctypes.c_void_p), ctypes.c_float(eta),
-                                       theta.data_ptr(), _stream_handle(stream))
-    _capi.check(rc, "repops_fixed_order_mean_sgd")
+    if gtype == TYPE_F32:
+        rc = L.repops_fixed_order_mean_sgd(nC, theta.numel(), ctypes.cast(parr, ctypes.c_void_p),
+                                           ctypes.cast(oarr, ctypes.c_void_p), ctypes.c_float(eta),
+                                           theta.data_ptr(), _stream_handle(stream))
+        _capi.check(rc, "repops_fixed_order_mean_sgd")
+    else:
+        rc = L.repops_fixed_order_mean_sgd_typed(nC, theta.numel(), ctypes.cast(parr, ctypes.c_void_p), gtype,
+                                                 ctypes.cast(oarr, ctypes.c_void_p), ctypes.c_float(eta),
+                                                 theta.data_ptr(), _stream_handle(stream))
+        _capi.check(rc, "repops_fixed_order_mean_sgd_typed")
     return theta
 
 
@@ -412,4 +438,77 @@ def gelu(x, out=None, *, stream=None):
         out = torch.empty_like(x)
     rc = L.repops_gelu_f32(x.numel(), x.data_ptr(), out.data_ptr(), _stream_handle(stream))
     _capi.check(rc, "repops_gelu_f32")
+    return out
+
+
+def convert(x, dtype, out=None, *, stream=None):
+    """x converted to `dtype` (float32, float16, bfloat16): exact widening,
+    round-to-nearest-even narrowing (repops_convert).  x: contiguous CUDA tensor."""
+    import torch
+    st, dt = _storage_type(x.dtype), _storage_type(dtype)
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty(x.shape, dtype=dtype, device=x.device)
+    if out.dtype != dtype or out.numel() != x.numel() or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor of dtype %s with x's size" % dtype)
+    rc = load().repops_convert(x.numel(), x.data_ptr(), st, out.data_ptr(), dt, _stream_handle(stream))
+    _capi.check(rc, "repops_convert")
+    return out
+
+
+def _typed_operand(X, name):
+    """(pointer, leading dim, transposed) of a 2-D CUDA view of any storage type."""
+    if X.dim() != 2 or not X.is_cuda:
+        raise TypeError("%s must be a 2-D CUDA tensor" % name)
+    r, c = X.shape
+    s0, s1 = X.stride()
+    if s1 == 1 and s0 >= max(c, 1):
+        return X.data_ptr(), s0, 0
+    if s0 == 1 and s1 >= max(r, 1):
+        return X.data_ptr(), s1, 1
+    raise ValueError("%s must be row-major or a transposed (column-major) view" % name)
+
+
+def gemm_typed(A, B, out=None, *, out_dtype=None, config: int = -1, loader: int = LOADER_AUTO, stream=None):
+    """C = A @ B on operands stored as float32, float16 or bfloat16: widened
+    exactly, the order-fixed binary32 k-chain, narrowed once to out's dtype
+    (repops_gemm_typed).  out_dtype defaults to float32."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    pa, lda, ta = _typed_operand(A, "A")
+    pb, ldb, tb = _typed_operand(B, "B")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype or torch.float32, device=A.device)
+    if out.dim() != 2 or tuple(out.shape) != (M, N) or (N > 0 and out.stride(1) != 1):
+        raise ValueError("out must be (M, N) with unit column stride")
+    rc = load().repops_gemm_typed(config, loader, ta, tb, M, N, K, pa, _storage_type(A.dtype), lda, pb,
+                                  _storage_type(B.dtype), ldb, out.data_ptr(), _storage_type(out.dtype),
+                                  max(out.stride(0), N, 1), _stream_handle(stream))
+    _capi.check(rc, "repops_gemm_typed")
+    return out
+
+
+def rolling_hash(words, window: int, out=None, *, stream=None):
+    """(rows, width - window + 1) Rabin-Karp window hashes modulo 2^61 - 1 of
+    a (rows, width) batch of uint32 words (an int32 or uint32 CUDA tensor, its
+    bits read as uint32; unit column stride).  Returned as int64 (every hash
+    is below 2^61)."""
+    import torch
+    if words.dim() != 2 or not words.is_cuda or words.element_size() != 4 or words.dtype.is_floating_point:
+        raise TypeError("words must be a 2-D 32-bit integer CUDA tensor")
+    rows, width = words.shape
+    if width > 0 and words.stride(1) != 1:
+        raise ValueError("words must have unit column stride")
+    n = width - window + 1
+    if out is None:
+        out = torch.empty((rows, max(n, 0)), dtype=torch.int64, device=words.device)
+    if out.dtype != torch.int64 or tuple(out.shape) != (rows, max(n, 0)) or (n > 0 and out.stride(1) != 1):
+        raise ValueError("out must be an int64 (rows, width - window + 1) tensor with unit column stride")
+    rc = load().repops_rolling_hash_u32(rows, width, words.data_ptr(), max(words.stride(0), width, 1), window,
+                                        out.data_ptr(), max(out.stride(0), n, 1), _stream_handle(stream))
+    _capi.check(rc, "repops_rolling_hash_u32")
     return out

@@ -56,6 +56,11 @@ SIGNATURES = {
     "repops_layernorm_rows_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _vp, _f32, _vp, _i64, _vp]),
     "repops_rmsnorm_rows_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _f32, _vp, _i64, _vp]),
     "repops_gelu_f32": (_i32, [_i64, _vp, _vp, _vp]),
+    "repops_fixed_order_mean_sgd_typed": (_i32, [_i32, _i64, _vp, _i32, _vp, ctypes.c_float, _vp, _vp]),
+    "repops_convert": (_i32, [_i64, _vp, _i32, _vp, _i32, _vp]),
+    "repops_gemm_typed": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64,
+                                 _vp, _i32, _i64, _vp]),
+    "repops_rolling_hash_u32": (_i32, [_i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]),
     "repops_softmax_rows_causal_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp]),
     "repops_gemm_f32_batched": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _i64,
                                        _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
@@ -63,6 +68,7 @@ SIGNATURES = {
 }
 
 ACT_NONE, ACT_GELU = 0, 1
+TYPE_F32, TYPE_F16, TYPE_BF16 = 0, 1, 2
 
 MERKLE_NOALLOC_SCRATCH_BYTES = 1 << 20
 

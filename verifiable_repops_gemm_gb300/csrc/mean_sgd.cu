@@ -13,6 +13,9 @@
 // gradient loads of a chunk before folding them in order, and writes theta
 // back in place.  HBM-bound: (k + 2) * 4 bytes of traffic per element.
 //
+// Gradients may be stored as binary16 or bfloat16 (widened exactly to binary32
+// before the fold; theta stays binary32): (k/2 + 2) * 4 bytes per element.
+//
 // Division: when k is a power of two, S / k and S * (1/k) are the same real
 // number and 1/k is exact in binary32, so both round to the same binary32
 // value; the kernel then multiplies.  Otherwise it calls __fdiv_rn, the
@@ -20,14 +23,30 @@
 #include <algorithm>
 #include <vector>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "internal.cuh"
 
 namespace repops {
 namespace {
 
 struct GradPtrs {
-    const float *g[REPOPS_MEAN_MAX_CONTRIBUTORS];   // already in fold order
+    const void *g[REPOPS_MEAN_MAX_CONTRIBUTORS];   // already in fold order
 };
+
+// Storage types of the gradients (REPOPS_TYPE_*); widening is exact.
+template <int TY>
+__device__ __forceinline__ float widen(unsigned short b) {
+    if constexpr (TY == REPOPS_TYPE_F16) return __half2float(__ushort_as_half(b));
+    else return __uint_as_float(unsigned(b) << 16);
+}
+
+template <int TY>
+__device__ __forceinline__ float ld1(const void *p, int64_t e) {
+    if constexpr (TY == REPOPS_TYPE_F32) return static_cast<const float *>(p)[e];
+    else return widen<TY>(static_cast<const unsigned short *>(p)[e]);
+}
 
 struct MeanScalars {
     int nC;
@@ -52,13 +71,21 @@ __device__ __forceinline__ void fold4(float4 &S, const float4 v) {
     S.w = __fadd_rn(S.w, v.w);
 }
 
-__device__ __forceinline__ float4 ld4(const float *p, int64_t i) {
-    return __ldcs(reinterpret_cast<const float4 *>(p) + i);
+// Elements 4i .. 4i+3 (16-byte loads for binary32, 8-byte for the half types).
+template <int TY>
+__device__ __forceinline__ float4 ld4(const void *p, int64_t i) {
+    if constexpr (TY == REPOPS_TYPE_F32) {
+        return __ldcs(reinterpret_cast<const float4 *>(p) + i);
+    } else {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(p) + i);
+        return make_float4(widen<TY>(w.x & 0xffffu), widen<TY>(w.x >> 16), widen<TY>(w.y & 0xffffu),
+                           widen<TY>(w.y >> 16));
+    }
 }
 
 // NC > 0: exactly NC contributors, fully unrolled (all loads of a chunk in
 // flight together).  NC == 0: any count, loads issued in batches of 8.
-template <int NC>
+template <int TY, int NC>
 __global__ void __launch_bounds__(256)
 mean_sgd_vec4(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t n4,
               float *__restrict__ theta) {
@@ -69,22 +96,22 @@ mean_sgd_vec4(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t
         if constexpr (NC > 0) {
             float4 v[NC];
 #pragma unroll
-            for (int r = 0; r < NC; ++r) v[r] = ld4(gp.g[r], i);
+            for (int r = 0; r < NC; ++r) v[r] = ld4<TY>(gp.g[r], i);
             S = v[0];
 #pragma unroll
             for (int r = 1; r < NC; ++r) fold4(S, v[r]);
         } else {
             constexpr int BATCH = 8;
-            S = ld4(gp.g[0], i);
+            S = ld4<TY>(gp.g[0], i);
             int r = 1;
             for (; r + BATCH <= sc.nC; r += BATCH) {
                 float4 v[BATCH];
 #pragma unroll
-                for (int j = 0; j < BATCH; ++j) v[j] = ld4(gp.g[r + j], i);
+                for (int j = 0; j < BATCH; ++j) v[j] = ld4<TY>(gp.g[r + j], i);
 #pragma unroll
                 for (int j = 0; j < BATCH; ++j) fold4(S, v[j]);
             }
-            for (; r < sc.nC; ++r) fold4(S, ld4(gp.g[r], i));
+            for (; r < sc.nC; ++r) fold4(S, ld4<TY>(gp.g[r], i));
         }
         th.x = sgd(th.x, mean_of(S.x, sc), sc.eta);
         th.y = sgd(th.y, mean_of(S.y, sc), sc.eta);
@@ -95,31 +122,59 @@ mean_sgd_vec4(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t
 }
 
 // Elements [first, len) one at a time: unaligned buffers, and the len % 4 tail.
+template <int TY>
 __global__ void __launch_bounds__(256)
 mean_sgd_scalar(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t first, int64_t len,
                 float *__restrict__ theta) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t e = first + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < len; e += stride) {
-        float S = gp.g[0][e];
-        for (int r = 1; r < sc.nC; ++r) S = __fadd_rn(S, gp.g[r][e]);
+        float S = ld1<TY>(gp.g[0], e);
+        for (int r = 1; r < sc.nC; ++r) S = __fadd_rn(S, ld1<TY>(gp.g[r], e));
         theta[e] = sgd(theta[e], mean_of(S, sc), sc.eta);
     }
 }
 
-template <int NC>
+template <int TY, int NC>
 int launch_vec(const GradPtrs &gp, const MeanScalars &sc, int64_t n4, float *theta, int blocks,
                cudaStream_t s) {
-    mean_sgd_vec4<NC><<<blocks, 256, 0, s>>>(gp, sc, n4, theta);
+    mean_sgd_vec4<TY, NC><<<blocks, 256, 0, s>>>(gp, sc, n4, theta);
     return check_launch();
 }
 
-}  // namespace
-}  // namespace repops
+template <int TY>
+int launch_all(const GradPtrs &gp, const MeanScalars &sc, int64_t len, float *theta, bool aligned, int max_blocks,
+               cudaStream_t stream) {
+    int rc = REPOPS_OK;
+    int64_t first_scalar = 0;
+    if (aligned) {
+        const int64_t n4 = len / 4;
+        first_scalar = n4 * 4;
+        if (n4 > 0) {
+            const int blocks = int(std::min<int64_t>((n4 + 255) / 256, max_blocks));
+            switch (sc.nC) {
+                case 1: rc = launch_vec<TY, 1>(gp, sc, n4, theta, blocks, stream); break;
+                case 2: rc = launch_vec<TY, 2>(gp, sc, n4, theta, blocks, stream); break;
+                case 4: rc = launch_vec<TY, 4>(gp, sc, n4, theta, blocks, stream); break;
+                case 8: rc = launch_vec<TY, 8>(gp, sc, n4, theta, blocks, stream); break;
+                case 16: rc = launch_vec<TY, 16>(gp, sc, n4, theta, blocks, stream); break;
+                default: rc = launch_vec<TY, 0>(gp, sc, n4, theta, blocks, stream); break;
+            }
+            if (rc != REPOPS_OK) return rc;
+        }
+    }
+    if (first_scalar < len) {
+        const int64_t n = len - first_scalar;
+        const int blocks = int(std::min<int64_t>((n + 255) / 256, max_blocks));
+        mean_sgd_scalar<TY><<<blocks, 256, 0, stream>>>(gp, sc, first_scalar, len, theta);
+        rc = check_launch();
+    }
+    return rc;
+}
 
-using namespace repops;
-
-extern "C" int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs, const int *order,
-                                           float eta, float *theta, cudaStream_t stream) {
+int mean_sgd_typed(int nC, int64_t len, const void *const *ptrs, int gtype, const int *order, float eta,
+                   float *theta, cudaStream_t stream) {
+    if (gtype != REPOPS_TYPE_F32 && gtype != REPOPS_TYPE_F16 && gtype != REPOPS_TYPE_BF16)
+        return REPOPS_ERR_INVALID_ARG;
     if (nC < 1 || nC > REPOPS_MEAN_MAX_CONTRIBUTORS || len < 0) return REPOPS_ERR_INVALID_ARG;
     if (!ptrs || !order) return REPOPS_ERR_INVALID_ARG;
     std::vector<char> seen(size_t(nC), 0);
@@ -130,13 +185,15 @@ extern "C" int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *con
     if (len == 0) return REPOPS_OK;
     if (!theta || len > INT64_MAX / 4) return REPOPS_ERR_INVALID_ARG;
     const uint64_t bytes = uint64_t(len) * 4u;
+    const unsigned gsize = gtype == REPOPS_TYPE_F32 ? 4u : 2u;
+    const uint64_t gbytes = uint64_t(len) * gsize;
     GradPtrs gp;
     bool aligned = reinterpret_cast<uintptr_t>(theta) % 16 == 0;
     for (int r = 0; r < nC; ++r) {
-        const float *g = ptrs[order[r]];
+        const void *g = ptrs[order[r]];
         if (!g) return REPOPS_ERR_INVALID_ARG;
-        if (ranges_overlap(theta, bytes, g, bytes)) return REPOPS_ERR_ALIAS;
-        aligned = aligned && reinterpret_cast<uintptr_t>(g) % 16 == 0;
+        if (ranges_overlap(theta, bytes, g, gbytes)) return REPOPS_ERR_ALIAS;
+        aligned = aligned && reinterpret_cast<uintptr_t>(g) % (4u * gsize) == 0;
         gp.g[r] = g;
     }
     for (int r = nC; r < REPOPS_MEAN_MAX_CONTRIBUTORS; ++r) gp.g[r] = nullptr;
@@ -152,29 +209,24 @@ extern "C" int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *con
     int rc = current_device_info(&di);
     if (rc != REPOPS_OK) return rc;
     const int max_blocks = di.sms * 8;   // 8 CTAs of 256 threads per SM
+    if (gtype == REPOPS_TYPE_F16) return launch_all<REPOPS_TYPE_F16>(gp, sc, len, theta, aligned, max_blocks, stream);
+    if (gtype == REPOPS_TYPE_BF16)
+        return launch_all<REPOPS_TYPE_BF16>(gp, sc, len, theta, aligned, max_blocks, stream);
+    return launch_all<REPOPS_TYPE_F32>(gp, sc, len, theta, aligned, max_blocks, stream);
+}
 
-    int64_t first_scalar = 0;
-    if (aligned) {
-        const int64_t n4 = len / 4;
-        first_scalar = n4 * 4;
-        if (n4 > 0) {
-            const int blocks = int(std::min<int64_t>((n4 + 255) / 256, max_blocks));
-            switch (nC) {
-                case 1: rc = launch_vec<1>(gp, sc, n4, theta, blocks, stream); break;
-                case 2: rc = launch_vec<2>(gp, sc, n4, theta, blocks, stream); break;
-                case 4: rc = launch_vec<4>(gp, sc, n4, theta, blocks, stream); break;
-                case 8: rc = launch_vec<8>(gp, sc, n4, theta, blocks, stream); break;
-                case 16: rc = launch_vec<16>(gp, sc, n4, theta, blocks, stream); break;
-                default: rc = launch_vec<0>(gp, sc, n4, theta, blocks, stream); break;
-            }
-            if (rc != REPOPS_OK) return rc;
-        }
-    }
-    if (first_scalar < len) {
-        const int64_t n = len - first_scalar;
-        const int blocks = int(std::min<int64_t>((n + 255) / 256, max_blocks));
-        mean_sgd_scalar<<<blocks, 256, 0, stream>>>(gp, sc, first_scalar, len, theta);
-        rc = check_launch();
-    }
-    return rc;
+}  // namespace
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs, const int *order,
+                                           float eta, float *theta, cudaStream_t stream) {
+    return mean_sgd_typed(nC, len, reinterpret_cast<const void *const *>(ptrs), REPOPS_TYPE_F32, order, eta,
+                          theta, stream);
+}
+
+extern "C" int repops_fixed_order_mean_sgd_typed(int nC, int64_t len, const void *const *ptrs, int grad_type,
+                                                 const int *order, float eta, float *theta, cudaStream_t stream) {
+    return mean_sgd_typed(nC, len, ptrs, grad_type, order, eta, theta, stream);
 }
