@@ -15,6 +15,8 @@
 // takes 16 consecutive window starts of one row: Horner's rule for the first,
 // then h' = (h - w_out * B^(W-1)) * B + w_in for the rest -- exact modular
 // integers, so the split of a row across threads does not change a bit.
+// Windows up to 1024 words stage a warp's words and hashes in shared memory
+// (coalesced global accesses); longer ones read global memory directly.
 #include <algorithm>
 
 #include <cuda_bf16.h>
@@ -26,7 +28,7 @@ namespace repops {
 namespace {
 
 bool known_type(int t) { return t == REPOPS_TYPE_F32 || t == REPOPS_TYPE_F16 || t == REPOPS_TYPE_BF16; }
-unsigned type_size(int t) { return t == REPOPS_TYPE_F32 ? 4u : 2u; }
+constexpr unsigned type_size(int t) { return t == REPOPS_TYPE_F32 ? 4u : 2u; }
 
 // ------------------------------------------------------------ conversions ----
 
@@ -44,35 +46,86 @@ __device__ __forceinline__ void store_from_f32(void *p, int64_t i, float v) {
     else static_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(v);
 }
 
-// rows x cols elements: source element (r, c) at src[r*lds + c], destination at
-// dst[r*ldd + c] (a 1-D conversion is one row).  Each thread handles the same
-// element of source and destination, so an in-place conversion between types
-// of one size is safe.
+// Elements 4i .. 4i+3 (16-byte accesses for binary32, 8-byte for the halves).
+template <int TY>
+__device__ __forceinline__ float4 load4(const void *p, int64_t i) {
+    if constexpr (TY == REPOPS_TYPE_F32) {
+        return __ldcs(reinterpret_cast<const float4 *>(p) + i);
+    } else {
+        const uint2 w = __ldcs(reinterpret_cast<const uint2 *>(p) + i);
+        const unsigned short h[4] = {(unsigned short)(w.x & 0xffffu), (unsigned short)(w.x >> 16),
+                                     (unsigned short)(w.y & 0xffffu), (unsigned short)(w.y >> 16)};
+        return make_float4(load_f32<TY>(h, 0), load_f32<TY>(h, 1), load_f32<TY>(h, 2), load_f32<TY>(h, 3));
+    }
+}
+
+template <int TY>
+__device__ __forceinline__ void store4(void *p, int64_t i, float4 v) {
+    if constexpr (TY == REPOPS_TYPE_F32) {
+        __stcs(reinterpret_cast<float4 *>(p) + i, v);
+    } else {
+        unsigned short h[4];
+        store_from_f32<TY>(h, 0, v.x);
+        store_from_f32<TY>(h, 1, v.y);
+        store_from_f32<TY>(h, 2, v.z);
+        store_from_f32<TY>(h, 3, v.w);
+        __stcs(reinterpret_cast<uint2 *>(p) + i, make_uint2(h[0] | (unsigned(h[1]) << 16), h[2] | (unsigned(h[3]) << 16)));
+    }
+}
+
+// n contiguous elements; vec: both buffers aligned to 4 elements, so whole
+// groups of four move with one vector access each.  Each thread converts the
+// same elements it reads, so an in-place conversion between types of one size
+// is safe.
 template <int S, int D>
 __global__ void __launch_bounds__(256)
-convert_kernel(int64_t rows, int64_t cols, const void *src, int64_t lds, void *dst, int64_t ldd) {
-    const int64_t total = rows * cols;
+convert_1d_kernel(int64_t n, const void *src, void *dst, int vec) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t e = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < total; e += stride) {
-        const int64_t r = e / cols, c = e - r * cols;
-        store_from_f32<D>(dst, r * ldd + c, load_f32<S>(src, r * lds + c));
+    const int64_t first = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t n4 = n / 4;
+        for (int64_t i = first; i < n4; i += stride) store4<D>(dst, i, load4<S>(src, i));
+        done = n4 * 4;
     }
+    for (int64_t e = done + first; e < n; e += stride) store_from_f32<D>(dst, e, load_f32<S>(src, e));
+}
+
+// rows x cols elements: source element (r, c) at src[r*lds + c], destination at
+// dst[r*ldd + c]; rows over blockIdx.y, columns over the x dimension.
+template <int S, int D>
+__global__ void __launch_bounds__(256)
+convert_2d_kernel(int64_t rows, int64_t cols, const void *src, int64_t lds, void *dst, int64_t ldd) {
+    for (int64_t r = blockIdx.y; r < rows; r += gridDim.y)
+        for (int64_t c = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; c < cols; c += int64_t(gridDim.x) * blockDim.x)
+            store_from_f32<D>(dst, r * ldd + c, load_f32<S>(src, r * lds + c));
+}
+
+template <int S, int D>
+int launch_convert_pair(int64_t rows, int64_t cols, const void *src, int64_t lds, void *dst, int64_t ldd,
+                        cudaStream_t s) {
+    DeviceInfo di;
+    const int sms = current_device_info(&di) == REPOPS_OK ? di.sms : 152;
+    if (rows == 1 || (lds == cols && ldd == cols)) {
+        const int64_t n = rows * cols;
+        const int vec = reinterpret_cast<uintptr_t>(src) % (4u * type_size(S)) == 0 &&
+                        reinterpret_cast<uintptr_t>(dst) % (4u * type_size(D)) == 0;
+        const int blocks = int(std::min<int64_t>((n / 4 + 255) / 256 + 1, int64_t(sms) * 16));
+        convert_1d_kernel<S, D><<<blocks, 256, 0, s>>>(n, src, dst, vec);
+    } else {
+        const int gx = int(std::min<int64_t>((cols + 255) / 256, 32));
+        const int gy = int(std::min<int64_t>(rows, 65535));
+        convert_2d_kernel<S, D><<<dim3(gx, gy), 256, 0, s>>>(rows, cols, src, lds, dst, ldd);
+    }
+    return check_launch();
 }
 
 template <int S>
 int launch_convert_to(int dtype, int64_t rows, int64_t cols, const void *src, int64_t lds, void *dst,
                       int64_t ldd, cudaStream_t s) {
-    DeviceInfo di;
-    const int sms = current_device_info(&di) == REPOPS_OK ? di.sms : 152;
-    const int64_t total = rows * cols;
-    const int blocks = int(std::min<int64_t>((total + 255) / 256, int64_t(sms) * 16));
-    if (dtype == REPOPS_TYPE_F32)
-        convert_kernel<S, REPOPS_TYPE_F32><<<blocks, 256, 0, s>>>(rows, cols, src, lds, dst, ldd);
-    else if (dtype == REPOPS_TYPE_F16)
-        convert_kernel<S, REPOPS_TYPE_F16><<<blocks, 256, 0, s>>>(rows, cols, src, lds, dst, ldd);
-    else
-        convert_kernel<S, REPOPS_TYPE_BF16><<<blocks, 256, 0, s>>>(rows, cols, src, lds, dst, ldd);
-    return check_launch();
+    if (dtype == REPOPS_TYPE_F32) return launch_convert_pair<S, REPOPS_TYPE_F32>(rows, cols, src, lds, dst, ldd, s);
+    if (dtype == REPOPS_TYPE_F16) return launch_convert_pair<S, REPOPS_TYPE_F16>(rows, cols, src, lds, dst, ldd, s);
+    return launch_convert_pair<S, REPOPS_TYPE_BF16>(rows, cols, src, lds, dst, ldd, s);
 }
 
 int launch_convert(int stype, int dtype, int64_t rows, int64_t cols, const void *src, int64_t lds, void *dst,
@@ -133,6 +186,57 @@ rolling_hash_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ wo
         }
     }
 }
+
+// Shared-memory staging: a warp takes SEG = 32 * ROLL_CHUNK consecutive window
+// starts of one row and copies the SEG + W - 1 words they read with coalesced
+// loads; lane L then rolls over starts 16L .. 16L + 15 reading the stage, and
+// the hashes leave through a second stage with coalesced 8-byte stores.  Both
+// stages put one pad slot after every 16 (index j at j + j/16): lane L's
+// element k sits at 17L + k + k/16, so the 32 lanes hit 32 different banks.
+constexpr int ROLL_SEG = 32 * ROLL_CHUNK;
+constexpr int ROLL_WARPS = 8;
+constexpr int64_t ROLL_MAX_STAGED_WINDOW = 1024;
+
+__device__ __forceinline__ int padded(int j) { return j + (j >> 4); }
+
+__global__ void __launch_bounds__(32 * ROLL_WARPS)
+rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ words, int64_t ldw, int W,
+                           uint64_t base, uint64_t base_w1, uint64_t *__restrict__ out, int64_t ldo, int64_t segs) {
+    extern __shared__ uint64_t roll_smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int wcap = padded(ROLL_SEG + W - 1) + 1;                       // words per warp stage
+    uint64_t *ostage = roll_smem + warp * (padded(ROLL_SEG) + 1);
+    uint32_t *wstage = reinterpret_cast<uint32_t *>(roll_smem + ROLL_WARPS * (padded(ROLL_SEG) + 1)) + warp * wcap;
+    const int64_t n = width - W + 1;
+    const int64_t total = rows * segs;
+    for (int64_t t = int64_t(blockIdx.x) * ROLL_WARPS + warp; t < total; t += int64_t(gridDim.x) * ROLL_WARPS) {
+        const int64_t r = t / segs, s0 = (t - r * segs) * ROLL_SEG;
+        const uint32_t *w = words + r * ldw + s0;
+        const int nw = int(min(int64_t(ROLL_SEG + W - 1), width - s0));   // words of this segment
+        for (int j = lane; j < nw; j += 32) wstage[padded(j)] = __ldcs(w + j);
+        __syncwarp();
+        const int i0 = lane * ROLL_CHUNK;                                // local start of this lane
+        const int cnt = int(max(int64_t(0), min(int64_t(ROLL_CHUNK), n - s0 - i0)));
+        if (cnt > 0) {
+            uint64_t h = 0;
+            for (int k = 0; k < W; ++k) h = addmod61(mulmod61(h, base), wstage[padded(i0 + k)]);
+            ostage[padded(i0)] = h;
+            for (int i = 1; i < cnt; ++i) {
+                const uint64_t drop = mulmod61(wstage[padded(i0 + i - 1)], base_w1);
+                h = h >= drop ? h - drop : h + (P61 - drop);
+                h = addmod61(mulmod61(h, base), wstage[padded(i0 + i + W - 1)]);
+                ostage[padded(i0 + i)] = h;
+            }
+        }
+        __syncwarp();
+        const int nout = int(min(int64_t(ROLL_SEG), n - s0));
+        uint64_t *o = out + r * ldo + s0;
+        for (int j = lane; j < nout; j += 32) __stcs(o + j, ostage[padded(j)]);
+        __syncwarp();                                                     // stages free for the next segment
+    }
+}
+
+constexpr size_t padded_host(int j) { return size_t(j) + size_t(j >> 4); }
 
 uint64_t powmod61_host(uint64_t b, int64_t e) {
     unsigned __int128 r = 1, x = b % P61;
@@ -226,12 +330,28 @@ extern "C" int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32
         return REPOPS_ERR_INVALID_ARG;
     const uint64_t wb = uint64_t((rows - 1) * ldw + width) * 4u, ob = uint64_t((rows - 1) * ldo + n) * 8u;
     if (ranges_overlap(words, wb, out, ob)) return REPOPS_ERR_ALIAS;
-    const int64_t chunks = (n + ROLL_CHUNK - 1) / ROLL_CHUNK;
     DeviceInfo di;
     const int sms = current_device_info(&di) == REPOPS_OK ? di.sms : 152;
+    const uint64_t bw1 = powmod61_host(REPOPS_ROLLING_HASH_BASE, window - 1);
+    if (window <= ROLL_MAX_STAGED_WINDOW) {
+        const int64_t segs = (n + ROLL_SEG - 1) / ROLL_SEG;
+        const int wcap = int(ROLL_SEG + window - 1) + int((ROLL_SEG + window - 1) >> 4) + 1;
+        const size_t smem = size_t(ROLL_WARPS) * ((padded_host(ROLL_SEG) + 1) * 8u + size_t(wcap) * 4u);
+        cudaError_t e = cudaFuncSetAttribute(rolling_hash_staged_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+        if (e != cudaSuccess) return set_cuda_error(e);
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, rolling_hash_staged_kernel, 32 * ROLL_WARPS, smem);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        const int blocks = int(std::min<int64_t>((rows * segs + ROLL_WARPS - 1) / ROLL_WARPS,
+                                                 int64_t(std::max(per_sm, 1)) * sms));
+        rolling_hash_staged_kernel<<<blocks, 32 * ROLL_WARPS, smem, stream>>>(
+            rows, width, words, ldw, int(window), REPOPS_ROLLING_HASH_BASE, bw1, out, ldo, segs);
+        return check_launch();
+    }
+    const int64_t chunks = (n + ROLL_CHUNK - 1) / ROLL_CHUNK;
     const int blocks = int(std::min<int64_t>((rows * chunks + 255) / 256, int64_t(sms) * 16));
-    rolling_hash_kernel<<<blocks, 256, 0, stream>>>(rows, width, words, ldw, window, REPOPS_ROLLING_HASH_BASE,
-                                                    powmod61_host(REPOPS_ROLLING_HASH_BASE, window - 1), out, ldo,
-                                                    chunks);
+    rolling_hash_kernel<<<blocks, 256, 0, stream>>>(rows, width, words, ldw, window, REPOPS_ROLLING_HASH_BASE, bw1,
+                                                    out, ldo, chunks);
     return check_launch();
 }
