@@ -52,8 +52,8 @@ L2_BYTES = 129 * 10 ** 6
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
 # valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "472911c05f88fb688f0f0c6f76587296d5af57943c2b4c0f0f3b3f85feb4a8f5",
-                "bytes_per_launch": 4900395264 + 267397376}
+GEMM_TRAFFIC = {"src_sha256": "752278687937feca11f702b4e0bb5c41d29e4c9bab7ada3d61790b976c449bde",
+                "bytes_per_launch": 4893530880 + 266178048}
 
 
 def measured_peaks():
