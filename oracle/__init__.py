@@ -107,6 +107,16 @@ def lib():
         L.oracle_mean_sgd_typed.argtypes = [i32, i64, vp, i32, vp, f32, vp]
         L.oracle_rolling_hash.restype = None
         L.oracle_rolling_hash.argtypes = [i64, i64, vp, i64, i64, vp, i64]
+        L.oracle_colsum.restype = None
+        L.oracle_colsum.argtypes = [i64, i64, vp, i64, vp]
+        L.oracle_gelu_grad.restype = f32
+        L.oracle_gelu_grad.argtypes = [f32]
+        L.oracle_gelu_backward.restype = None
+        L.oracle_gelu_backward.argtypes = [i64, vp, vp, vp]
+        L.oracle_rmsnorm_backward.restype = None
+        L.oracle_rmsnorm_backward.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64, vp, i64, vp, i64]
+        L.oracle_softmax_backward.restype = None
+        L.oracle_softmax_backward.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64]
         L.oracle_gemm_batched.restype = None
         L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
                                           vp, i64, i64, f32, vp, i32, vp, i64, i64]
@@ -443,4 +453,47 @@ def rolling_hash(words: np.ndarray, window: int) -> np.ndarray:
     out = np.empty((rows, max(n, 0)), dtype=np.uint64)
     if rows and n > 0:
         lib().oracle_rolling_hash(rows, width, _ptr(w), width, window, _ptr(out), n)
+    return out
+
+
+def colsum(x) -> np.ndarray:
+    """Column sums of a 2-D float32 array, each over the 32-ary tree in row order."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(a.shape[1], dtype=np.float32)
+    if a.shape[1]:
+        lib().oracle_colsum(a.shape[0], a.shape[1], _ptr(a), a.shape[1], _ptr(y))
+    return y
+
+
+def gelu_grad(x: float) -> float:
+    return lib().oracle_gelu_grad(float(x))
+
+
+def gelu_backward(x, dy) -> np.ndarray:
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    d = np.ascontiguousarray(dy, dtype=np.float32)
+    out = np.empty_like(a)
+    lib().oracle_gelu_backward(a.size, _ptr(a), _ptr(d), _ptr(out))
+    return out
+
+
+def rmsnorm_backward(x, gamma, eps: float, dy):
+    """(dx, dy * xhat) of RMSNorm rows; dgamma = colsum(dy * xhat)."""
+    a = np.ascontiguousarray(x, dtype=np.float32)
+    g = np.ascontiguousarray(gamma, dtype=np.float32)
+    d = np.ascontiguousarray(dy, dtype=np.float32)
+    dx = np.empty_like(a)
+    pr = np.empty_like(a)
+    r, c = a.shape
+    lib().oracle_rmsnorm_backward(r, c, _ptr(a), c, _ptr(g), ctypes.c_float(eps), _ptr(d), c, _ptr(dx), c,
+                                  _ptr(pr), c)
+    return dx, pr
+
+
+def softmax_backward(p, dp) -> np.ndarray:
+    a = np.ascontiguousarray(p, dtype=np.float32)
+    d = np.ascontiguousarray(dp, dtype=np.float32)
+    out = np.empty_like(a)
+    r, c = a.shape
+    lib().oracle_softmax_backward(r, c, _ptr(a), c, _ptr(d), c, _ptr(out), c)
     return out

@@ -913,3 +913,90 @@ void oracle_rolling_hash(int64_t rows, int64_t width, const uint32_t *words, int
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward operators of a training step  [RepOps §3.2 (order-critical     */
+/* reductions in a fixed order), §4.3 (training: LayerNorm, GeLU, ERF among  */
+/* the operators that need reproducible forms).  The pages fix none of      */
+/* these; the library's definitions follow, every step one binary32         */
+/* rounding, every reduction the 32-ary tree above.]                        */
+/* ------------------------------------------------------------------------ */
+
+/* y[j] = tree sum over rows i of x[i*ldx + j]: the column's values in row
+ * order, folded by the same 32-ary tree as a row reduction. */
+void oracle_colsum(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y)
+{
+    float *v = (float *)malloc((size_t)(rows > 0 ? rows : 1) * sizeof(float));
+    for (int64_t j = 0; j < cols; ++j) {
+        for (int64_t i = 0; i < rows; ++i) v[i] = x[i * ldx + j];
+        y[j] = rows > 0 ? tree_reduce(v, rows, 0) : 0.0f;
+    }
+    free(v);
+}
+
+/* dx = dy * GeLU'(x), GeLU'(x) = Phi(x) + x * phi(x):
+ *   Phi(x) = 0.5 * (1 + erf(x/sqrt 2)), 1 + erf taken as in oracle_gelu;
+ *   phi(x) = exp(-(0.5 * x*x)) * (1/sqrt(2 pi)). */
+float oracle_gelu_grad(float x)
+{
+    float z = x * 0.707106769084930419921875f;
+    float az = z < 0.0f ? -z : z;
+    float e = oracle_erfc_pos(az);
+    float phi2 = z >= 0.0f ? 2.0f - e : e;
+    float cdf = 0.5f * phi2;
+    float xx = x * x;
+    float a = -(0.5f * xx);
+    float pdf = oracle_exp(a) * 0.3989422917366028f;
+    return cdf + x * pdf;
+}
+
+void oracle_gelu_backward(int64_t n, const float *x, const float *dy, float *dx)
+{
+    for (int64_t i = 0; i < n; ++i) dx[i] = dy[i] * oracle_gelu_grad(x[i]);
+}
+
+/* RMSNorm backward, per row (forward: inv = 1/sqrt(tree sum(x*x)/n + eps),
+ * y = (x * inv) * gamma):
+ *   xh = x * inv;  gy = dy * gamma;  c = tree sum(gy * xh) / n;
+ *   dx = inv * (gy - xh * c);  dyxh = dy * xh  (its column sums are dgamma). */
+void oracle_rmsnorm_backward(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *gamma,
+                             float eps, const float *dy, int64_t lddy, float *dx, int64_t lddx,
+                             float *dyxh, int64_t ldp)
+{
+    float *v = (float *)malloc((size_t)cols * sizeof(float));
+    const float n = (float)cols;
+    for (int64_t i = 0; i < rows; ++i) {
+        const float *xr = x + i * ldx;
+        const float *dr = dy + i * lddy;
+        for (int64_t j = 0; j < cols; ++j) v[j] = xr[j] * xr[j];
+        float ms = tree_reduce(v, cols, 0) / n;
+        float inv = 1.0f / sqrtf(ms + eps);
+        for (int64_t j = 0; j < cols; ++j) {
+            float xh = xr[j] * inv;
+            float gy = dr[j] * gamma[j];
+            v[j] = gy * xh;
+        }
+        float c = tree_reduce(v, cols, 0) / n;
+        for (int64_t j = 0; j < cols; ++j) {
+            float xh = xr[j] * inv;
+            float gy = dr[j] * gamma[j];
+            dx[i * lddx + j] = inv * (gy - xh * c);
+            dyxh[i * ldp + j] = dr[j] * xh;
+        }
+    }
+    free(v);
+}
+
+/* Softmax backward, per row: s = tree sum(dp * p); ds = p * (dp - s).  A
+ * causal block's masked entries have p = +0, so their ds is a signed zero. */
+void oracle_softmax_backward(int64_t rows, int64_t cols, const float *p, int64_t ldp, const float *dp,
+                             int64_t lddp, float *ds, int64_t ldds)
+{
+    float *v = (float *)malloc((size_t)cols * sizeof(float));
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < cols; ++j) v[j] = dp[i * lddp + j] * p[i * ldp + j];
+        float s = tree_reduce(v, cols, 0);
+        for (int64_t j = 0; j < cols; ++j) ds[i * ldds + j] = p[i * ldp + j] * (dp[i * lddp + j] - s);
+    }
+    free(v);
+}

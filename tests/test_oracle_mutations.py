@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "repops_oracle.c")
 PINS = [os.path.join(ROOT, "tests", f) for f in
         ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py", "test_oracle_rowops.py",
-         "test_oracle_epilogue.py", "test_oracle_halfstore.py")]
+         "test_oracle_epilogue.py", "test_oracle_halfstore.py", "test_oracle_backward.py")]
 
 MUTATIONS = {
     "gemm: fused multiply-add": (
@@ -82,6 +82,15 @@ MUTATIONS = {
     "typed mean: SGD adds the step": ("float updated = theta[e] - step;", "float updated = theta[e] + step;"),
     "typed mean: last gradient dropped": ("for (int r = 1; r < nC; ++r) S = S + load_as_f32(grads[order[r]], e, gtype);",
                                           "for (int r = 1; r < nC - 1; ++r) S = S + load_as_f32(grads[order[r]], e, gtype);"),
+    "colsum: rows in reverse order": ("for (int64_t i = 0; i < rows; ++i) v[i] = x[i * ldx + j];",
+                                      "for (int64_t i = 0; i < rows; ++i) v[i] = x[(rows - 1 - i) * ldx + j];"),
+    "gelu grad: pdf without 1/sqrt(2 pi)": ("float pdf = oracle_exp(a) * 0.3989422917366028f;",
+                                            "float pdf = oracle_exp(a);"),
+    "gelu grad: cdf not halved": ("float cdf = 0.5f * phi2;", "float cdf = phi2;"),
+    "rmsnorm backward: inv dropped": ("dx[i * lddx + j] = inv * (gy - xh * c);", "dx[i * lddx + j] = gy - xh * c;"),
+    "rmsnorm backward: dgamma from gy": ("dyxh[i * ldp + j] = dr[j] * xh;", "dyxh[i * ldp + j] = gy * xh;"),
+    "softmax backward: s not subtracted": ("ds[i * ldds + j] = p[i * ldp + j] * (dp[i * lddp + j] - s);",
+                                           "ds[i * ldds + j] = p[i * ldp + j] * dp[i * lddp + j];"),
     "batched: A advanced by B's stride": ("const float *Ab = A + b * strideA;", "const float *Ab = A + b * strideB;"),
 }
 
