@@ -114,7 +114,7 @@ def lib():
         L.oracle_gelu_backward.restype = None
         L.oracle_gelu_backward.argtypes = [i64, vp, vp, vp]
         L.oracle_rmsnorm_backward.restype = None
-        L.oracle_rmsnorm_backward.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64, vp, i64, vp, i64]
+        L.oracle_rmsnorm_backward.argtypes = [i64, i64, vp, i64, vp, f32, vp, i64, vp, i64, vp, i64, vp, i64]
         L.oracle_softmax_backward.restype = None
         L.oracle_softmax_backward.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64]
         L.oracle_gemm_batched.restype = None
@@ -477,16 +477,18 @@ def gelu_backward(x, dy) -> np.ndarray:
     return out
 
 
-def rmsnorm_backward(x, gamma, eps: float, dy):
-    """(dx, dy * xhat) of RMSNorm rows; dgamma = colsum(dy * xhat)."""
+def rmsnorm_backward(x, gamma, eps: float, dy, res=None):
+    """(dx, dy * xhat) of RMSNorm rows, dx + res when res is given;
+    dgamma = colsum(dy * xhat)."""
     a = np.ascontiguousarray(x, dtype=np.float32)
     g = np.ascontiguousarray(gamma, dtype=np.float32)
     d = np.ascontiguousarray(dy, dtype=np.float32)
+    rr = np.ascontiguousarray(res, dtype=np.float32) if res is not None else None
     dx = np.empty_like(a)
     pr = np.empty_like(a)
     r, c = a.shape
-    lib().oracle_rmsnorm_backward(r, c, _ptr(a), c, _ptr(g), ctypes.c_float(eps), _ptr(d), c, _ptr(dx), c,
-                                  _ptr(pr), c)
+    lib().oracle_rmsnorm_backward(r, c, _ptr(a), c, _ptr(g), ctypes.c_float(eps), _ptr(d), c,
+                                  _ptr(rr) if rr is not None else None, c, _ptr(dx), c, _ptr(pr), c)
     return dx, pr
 
 

@@ -958,10 +958,12 @@ void oracle_gelu_backward(int64_t n, const float *x, const float *dy, float *dx)
 /* RMSNorm backward, per row (forward: inv = 1/sqrt(tree sum(x*x)/n + eps),
  * y = (x * inv) * gamma):
  *   xh = x * inv;  gy = dy * gamma;  c = tree sum(gy * xh) / n;
- *   dx = inv * (gy - xh * c);  dyxh = dy * xh  (its column sums are dgamma). */
+ *   dx = inv * (gy - xh * c), then + res when res is given (the gradient of a
+ *   residual branch around the norm);  dyxh = dy * xh (its column sums are
+ *   dgamma).  res may be dx itself. */
 void oracle_rmsnorm_backward(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *gamma,
-                             float eps, const float *dy, int64_t lddy, float *dx, int64_t lddx,
-                             float *dyxh, int64_t ldp)
+                             float eps, const float *dy, int64_t lddy, const float *res, int64_t ldres,
+                             float *dx, int64_t lddx, float *dyxh, int64_t ldp)
 {
     float *v = (float *)malloc((size_t)cols * sizeof(float));
     const float n = (float)cols;
@@ -980,7 +982,9 @@ void oracle_rmsnorm_backward(int64_t rows, int64_t cols, const float *x, int64_t
         for (int64_t j = 0; j < cols; ++j) {
             float xh = xr[j] * inv;
             float gy = dr[j] * gamma[j];
-            dx[i * lddx + j] = inv * (gy - xh * c);
+            float d = inv * (gy - xh * c);
+            if (res) d = d + res[i * ldres + j];
+            dx[i * lddx + j] = d;
             dyxh[i * ldp + j] = dr[j] * xh;
         }
     }

@@ -99,12 +99,16 @@ def test_rmsnorm_backward_exact_composition(orc, cols):
     x = rng.standard_normal((3, cols)).astype(np.float32)
     g = rng.standard_normal(cols).astype(np.float32)
     dy = rng.standard_normal((3, cols)).astype(np.float32)
+    res = rng.standard_normal((3, cols)).astype(np.float32)
     eps = float(np.float32(1e-5))
     dx, p = orc.rmsnorm_backward(x, g, eps, dy)
+    dxr, pr = orc.rmsnorm_backward(x, g, eps, dy, res)
     for i in range(3):
         wdx, wp = ref_rms_bwd_row(x[i], g, eps, dy[i])
         assert [fx.bits(float(v)) for v in dx[i]] == [fx.bits(v) for v in wdx]
         assert [fx.bits(float(v)) for v in p[i]] == [fx.bits(v) for v in wp]
+        assert [fx.bits(float(v)) for v in dxr[i]] == [fx.bits(fx.add(a, float(b))) for a, b in zip(wdx, res[i])]
+        assert np.array_equal(pr[i].view(np.uint32), p[i].view(np.uint32))
 
 
 def test_rmsnorm_backward_against_float64(orc):

@@ -87,7 +87,8 @@ MUTATIONS = {
     "gelu grad: pdf without 1/sqrt(2 pi)": ("float pdf = oracle_exp(a) * 0.3989422917366028f;",
                                             "float pdf = oracle_exp(a);"),
     "gelu grad: cdf not halved": ("float cdf = 0.5f * phi2;", "float cdf = phi2;"),
-    "rmsnorm backward: inv dropped": ("dx[i * lddx + j] = inv * (gy - xh * c);", "dx[i * lddx + j] = gy - xh * c;"),
+    "rmsnorm backward: inv dropped": ("float d = inv * (gy - xh * c);", "float d = gy - xh * c;"),
+    "rmsnorm backward: residual ignored": ("if (res) d = d + res[i * ldres + j];", ""),
     "rmsnorm backward: dgamma from gy": ("dyxh[i * ldp + j] = dr[j] * xh;", "dyxh[i * ldp + j] = gy * xh;"),
     "softmax backward: s not subtracted": ("ds[i * ldds + j] = p[i * ldp + j] * (dp[i * lddp + j] - s);",
                                            "ds[i * ldds + j] = p[i * ldp + j] * dp[i * lddp + j];"),
