@@ -463,6 +463,52 @@ int repops_merkle_sha256_noalloc(const void *ptr, uint64_t bytes, uint32_t leaf,
                                  uint8_t *root_out, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Backward operators of a training step                                     */
+/* "Verde与RepOps" §3.2 (order-critical reductions in a fixed order), §4.3   */
+/* (training; LayerNorm, GeLU, ERF need reproducible forms).  The pages fix  */
+/* none of these; the library's definitions, every step one binary32         */
+/* rounding, every reduction the 32-ary tree of the row operators.           */
+/* ------------------------------------------------------------------------ */
+
+/* y[j] = tree sum over i = 0 .. rows-1 of x[i*ldx + j] (the column's values in
+ * row order, folded by the 32-ary tree): bias and gain gradients.  rows == 0
+ * gives +0.  Scratch for the tree's middle levels (about rows/31 * cols
+ * floats) is taken with cudaMallocAsync on `stream` (ALLOC when refused).
+ * y (device, cols floats) must not overlap x (ALIAS). */
+int repops_colsum_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
+                      cudaStream_t stream);
+
+/* dx[i] = fl(dy[i] * GeLU'(x[i])), GeLU'(x) = Phi(x) + x*phi(x):
+ *   z = x * (1/sqrt 2); 1 + erf(z) as in repops_gelu_f32; Phi = 0.5 * (1 + erf(z));
+ *   phi = exp(-(0.5 * (x*x))) * 0.3989422917366028 (1/sqrt(2 pi) in binary32);
+ *   GeLU' = Phi + x * phi.
+ * dx may be x or dy (the same pointer); other overlaps are ALIAS. */
+int repops_gelu_backward_f32(int64_t n, const float *x, const float *dy, float *dx,
+                             cudaStream_t stream);
+
+/* RMSNorm backward per row (the forward's inv = 1/sqrt(tree sum(x*x)/n + eps)
+ * recomputed with the same operations):
+ *   xh = x * inv, gy = dy * gamma[j], c = tree sum(gy * xh) / n,
+ *   dx = inv * (gy - xh * c), then fl(dx + res) when res is not NULL (the
+ *   gradient arriving through a pre-norm layer's residual path),
+ *   dyxh = dy * xh   (repops_colsum_f32 of dyxh is dgamma).
+ * x, dy, res, dx, dyxh: rows x cols with their own pitches; gamma: cols.
+ * res may be dx itself (same pitch); otherwise outputs must not overlap any
+ * input or each other (ALIAS); cols up to 393216 (UNSUPPORTED beyond). */
+int repops_rmsnorm_backward_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                                const float *gamma, float eps, const float *dy, int64_t lddy,
+                                const float *res, int64_t ldres, float *dx, int64_t lddx,
+                                float *dyxh, int64_t ldp, cudaStream_t stream);
+
+/* Softmax backward per row: s = tree sum(dp * p), ds = p * (dp - s).  p is the
+ * forward's output (a causal block's masked entries are +0, so theirs is a
+ * signed zero).  ds may be p or dp (same pointer and pitch); other overlaps
+ * are ALIAS; cols up to 393216. */
+int repops_softmax_backward_f32(int64_t rows, int64_t cols, const float *p, int64_t ldp,
+                                const float *dp, int64_t lddp, float *ds, int64_t ldds,
+                                cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Half-precision storage                                                    */
 /* "Verde与RepOps" §3.3 (IEEE-754 hardware needed; FP16 support limited) and */
 /* §5.3 (lower-precision training as future work).  The pages fix no format  */

@@ -276,3 +276,24 @@ def test_half_storage_and_rolling_hash_reject_bad_arguments(L):
     assert rh(4, 10, FAKE_A, 10, 3, FAKE_B, 7, None) == -1           # ldo < width - window + 1
     assert rh(4, 10, FAKE_A, 10, 3, FAKE_A + 40, 8, None) == -2
     assert rh(0, 10, FAKE_A, 10, 3, FAKE_B, 8, None) == 0
+
+
+def test_backward_operators_reject_bad_arguments(L):
+    assert L.repops_colsum_f32(-1, 4, FAKE_A, 4, FAKE_B, None) == -1
+    assert L.repops_colsum_f32(4, 4, FAKE_A, 3, FAKE_B, None) == -1          # ldx < cols
+    assert L.repops_colsum_f32(4, 4, FAKE_A, 4, FAKE_A + 8, None) == -2
+    assert L.repops_colsum_f32(4, 0, FAKE_A, 4, FAKE_B, None) == 0
+    assert L.repops_gelu_backward_f32(-1, FAKE_A, FAKE_B, FAKE_C, None) == -1
+    assert L.repops_gelu_backward_f32(8, FAKE_A, FAKE_B, FAKE_A + 4, None) == -2
+    assert L.repops_gelu_backward_f32(0, None, None, None, None) == 0
+    rb = L.repops_rmsnorm_backward_f32
+    eps = ctypes.c_float(1e-5)
+    assert rb(4, 4, FAKE_A, 4, None, eps, FAKE_B, 4, None, 0, FAKE_C, 4, FAKE_C + 4096, 4, None) == -1   # null gamma
+    assert rb(4, 4, FAKE_A, 4, FAKE_A + 4096, eps, FAKE_B, 4, None, 0, FAKE_A, 4, FAKE_C, 4, None) == -2  # dx over x
+    assert rb(4, 4, FAKE_A, 4, FAKE_A + 4096, eps, FAKE_B, 4, None, 0, FAKE_C, 4, FAKE_C + 8, 4, None) == -2
+    assert rb(4, 4, FAKE_A, 4, FAKE_A + 4096, eps, FAKE_B, 4, FAKE_C + 8, 4, FAKE_C, 4, FAKE_C + 4096, 4,
+              None) == -2                                                                    # res partly over dx
+    sb = L.repops_softmax_backward_f32
+    assert sb(4, 4, FAKE_A, 3, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert sb(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 8, 4, None) == -2
+    assert sb(4, 400000, FAKE_A, 400000, FAKE_B, 400000, FAKE_C, 400000, None) == -7

@@ -24,6 +24,8 @@ memory and streams.
   convert / gemm_typed              binary16 / bfloat16 storage around the
                                     binary32 path ("Verde与RepOps" §3.3, §5.3)
   rolling_hash(words, window)       Rabin-Karp hashes of uint32 batch rows (ZKDV)
+  colsum / gelu_backward /          backward operators of a training step
+  rmsnorm_backward / softmax_backward
 """
 import ctypes
 
@@ -36,6 +38,7 @@ __all__ = ["load", "version", "gemm", "gemm_config_count", "gemm_config_info",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
            "convert", "gemm_typed", "rolling_hash", "TYPE_F32", "TYPE_F16", "TYPE_BF16",
+           "colsum", "gelu_backward", "rmsnorm_backward", "softmax_backward",
            "device_status", "RepopsError", "ACT_NONE", "ACT_GELU",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
 
@@ -511,4 +514,66 @@ def rolling_hash(words, window: int, out=None, *, stream=None):
     rc = load().repops_rolling_hash_u32(rows, width, words.data_ptr(), max(words.stride(0), width, 1), window,
                                         out.data_ptr(), max(out.stride(0), n, 1), _stream_handle(stream))
     _capi.check(rc, "repops_rolling_hash_u32")
+    return out
+
+
+def colsum(x, out=None, *, stream=None):
+    """Column sums of a 2-D float32 CUDA tensor (unit column stride), each over
+    the 32-ary tree in row order (repops_colsum_f32)."""
+    import torch
+    rows, cols = x.shape
+    px, ldx = _row_operand(x, "x") if rows else (x.data_ptr(), max(cols, 1))
+    if out is None:
+        out = torch.empty(cols, dtype=torch.float32, device=x.device)
+    rc = load().repops_colsum_f32(rows, cols, px, ldx, out.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_colsum_f32")
+    return out
+
+
+def gelu_backward(x, dy, out=None, *, stream=None):
+    """dy * GeLU'(x) for contiguous float32 CUDA tensors of one size."""
+    import torch
+    for t, n in ((x, "x"), (dy, "dy")):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous float32 CUDA tensor" % n)
+    if x.numel() != dy.numel():
+        raise ValueError("x and dy differ in size")
+    if out is None:
+        out = torch.empty_like(x)
+    rc = load().repops_gelu_backward_f32(x.numel(), x.data_ptr(), dy.data_ptr(), out.data_ptr(),
+                                         _stream_handle(stream))
+    _capi.check(rc, "repops_gelu_backward_f32")
+    return out
+
+
+def rmsnorm_backward(x, gamma, eps, dy, dx=None, dyxh=None, *, res=None, stream=None):
+    """(dx, dy * xhat) of RMSNorm rows (repops_rmsnorm_backward_f32), dx + res
+    when res is given (res may be dx); colsum(dy * xhat) is dgamma."""
+    px, ldx = _row_operand(x, "x")
+    pd, ldd = _row_operand(dy, "dy")
+    dx = _row_out(x, dx)
+    dyxh = _row_out(x, dyxh)
+    pdx, lddx = _row_operand(dx, "dx")
+    pp, ldp = _row_operand(dyxh, "dyxh")
+    pr, ldr = _row_operand(res, "res") if res is not None else (None, 0)
+    if gamma.numel() != x.shape[1] or tuple(dy.shape) != tuple(x.shape) or \
+            (res is not None and tuple(res.shape) != tuple(x.shape)):
+        raise ValueError("gamma needs one value per column; dy and res x's shape")
+    rc = load().repops_rmsnorm_backward_f32(x.shape[0], x.shape[1], px, ldx, gamma.data_ptr(), ctypes.c_float(eps),
+                                            pd, ldd, pr, ldr, pdx, lddx, pp, ldp, _stream_handle(stream))
+    _capi.check(rc, "repops_rmsnorm_backward_f32")
+    return dx, dyxh
+
+
+def softmax_backward(p, dp, out=None, *, stream=None):
+    """p * (dp - rowsum(dp * p)) (repops_softmax_backward_f32); out may be dp."""
+    pp, ldp = _row_operand(p, "p")
+    pg, ldg = _row_operand(dp, "dp")
+    out = _row_out(p, out)
+    po, ldo = _row_operand(out, "out")
+    if tuple(dp.shape) != tuple(p.shape):
+        raise ValueError("p and dp differ in shape")
+    rc = load().repops_softmax_backward_f32(p.shape[0], p.shape[1], pp, ldp, pg, ldg, po, ldo,
+                                            _stream_handle(stream))
+    _capi.check(rc, "repops_softmax_backward_f32")
     return out

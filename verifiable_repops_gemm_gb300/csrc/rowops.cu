@@ -491,6 +491,128 @@ gelu_kernel(int64_t n, const float *__restrict__ x, float *__restrict__ y, int v
     }
 }
 
+// ---------------------------------------------------------- backward ----
+// Backward operators of a training step, with the forward's tree and
+// arithmetic: GeLU backward (element-wise), RMSNorm and softmax backward (one
+// CTA per row, each phase re-reading the row from global memory, where the
+// row stays cached between phases), column sums (repeated passes folding runs
+// of 32 rows: the level-by-level tree).
+
+// Tree reduction over i in [0, n) of f(i) (an index functor), as generic_reduce.
+template <Op OP, class F>
+__device__ float generic_reduce_idx(int64_t n, F f, float *buf, float *buf2, float *bcast) {
+    const int runs = int((n + RUN - 1) / RUN);
+    for (int j = threadIdx.x; j < runs; j += blockDim.x) {
+        const int64_t s = int64_t(j) * RUN, e = imin64(s + RUN, n);
+        float acc = f(s);
+        for (int64_t i = s + 1; i < e; ++i) acc = combine<OP>(acc, f(i));
+        buf[j] = acc;
+    }
+    return tree_upper<OP>(buf, buf2, runs, bcast);
+}
+
+__device__ __forceinline__ float gelu_grad_fixed(float x) {
+    const float z = __fmul_rn(x, 0.707106769084930419921875f);
+    const float e = erfc_pos(fabsf(z));
+    const float phi2 = z >= 0.0f ? __fsub_rn(2.0f, e) : e;
+    const float cdf = __fmul_rn(0.5f, phi2);
+    const float a = -__fmul_rn(0.5f, __fmul_rn(x, x));
+    const float pdf = __fmul_rn(exp_fixed(a), 0.3989422917366028f);   // 1/sqrt(2 pi)
+    return __fadd_rn(cdf, __fmul_rn(x, pdf));
+}
+
+__global__ void __launch_bounds__(256)
+gelu_backward_kernel(int64_t n, const float *__restrict__ x, const float *__restrict__ dy, float *__restrict__ dx,
+                     int vec) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const int64_t first = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t n4 = n / 4;
+        for (int64_t i = first; i < n4; i += stride) {
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(x) + i);
+            const float4 d = __ldcs(reinterpret_cast<const float4 *>(dy) + i);
+            __stcs(reinterpret_cast<float4 *>(dx) + i,
+                   make_float4(__fmul_rn(d.x, gelu_grad_fixed(v.x)), __fmul_rn(d.y, gelu_grad_fixed(v.y)),
+                               __fmul_rn(d.z, gelu_grad_fixed(v.z)), __fmul_rn(d.w, gelu_grad_fixed(v.w))));
+        }
+        done = n4 * 4;
+    }
+    for (int64_t i = done + first; i < n; i += stride) dx[i] = __fmul_rn(dy[i], gelu_grad_fixed(x[i]));
+}
+
+// RMSNorm backward: xh = x*inv, gy = dy*gamma, c = tree sum(gy*xh)/n,
+// dx = inv*(gy - xh*c) (+ res), p = dy*xh (column sums of p give dgamma).
+// res may be dx: each element is read just before it is written.
+__global__ void __launch_bounds__(256)
+rmsnorm_backward_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
+                        const float *__restrict__ gamma, float eps, const float *__restrict__ dy, int64_t lddy,
+                        const float *res, int64_t ldres, float *dx, int64_t lddx, float *__restrict__ p,
+                        int64_t ldp) {
+    extern __shared__ float buf[];
+    __shared__ float bcast;
+    const int runs = int((n + RUN - 1) / RUN);
+    float *buf2 = buf + runs;
+    const float nf = float(n);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *xr = x + r * ldx, *dr = dy + r * lddy;
+        const float ms = __fdiv_rn(
+            generic_reduce_idx<Op::Sum>(n, [&](int64_t i) { return __fmul_rn(xr[i], xr[i]); }, buf, buf2, &bcast),
+            nf);
+        const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+        const float c = __fdiv_rn(generic_reduce_idx<Op::Sum>(n, [&](int64_t i) {
+            return __fmul_rn(__fmul_rn(dr[i], gamma[i]), __fmul_rn(xr[i], inv));
+        }, buf, buf2, &bcast), nf);
+        for (int j = threadIdx.x; j < runs; j += blockDim.x)
+            for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i) {
+                const float xh = __fmul_rn(xr[i], inv), gy = __fmul_rn(dr[i], gamma[i]);
+                float d = __fmul_rn(inv, __fsub_rn(gy, __fmul_rn(xh, c)));
+                if (res) d = __fadd_rn(d, res[r * ldres + i]);
+                dx[r * lddx + i] = d;
+                p[r * ldp + i] = __fmul_rn(dr[i], xh);
+            }
+        __syncthreads();
+    }
+}
+
+// Softmax backward: s = tree sum(dp*p), ds = p*(dp - s).  Each thread writes
+// only the elements it read in the same pass, so ds may be dp or p.
+__global__ void __launch_bounds__(256)
+softmax_backward_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, const float *dp, int64_t lddp,
+                        float *ds, int64_t ldds) {
+    extern __shared__ float buf[];
+    __shared__ float bcast;
+    const int runs = int((n + RUN - 1) / RUN);
+    float *buf2 = buf + runs;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const float *pr = p + r * ldp, *gr = dp + r * lddp;
+        const float sum = generic_reduce_idx<Op::Sum>(n, [&](int64_t i) { return __fmul_rn(gr[i], pr[i]); }, buf,
+                                                      buf2, &bcast);
+        for (int j = threadIdx.x; j < runs; j += blockDim.x)
+            for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i)
+                ds[r * ldds + i] = __fmul_rn(pr[i], __fsub_rn(gr[i], sum));
+        __syncthreads();
+    }
+}
+
+// One tree level of a column sum: out[q][j] = fold of rows [32q, 32q + 32) of
+// column j (left to right from the first).  Threads run along columns
+// (coalesced), the grid's y dimension along q.
+__global__ void __launch_bounds__(256)
+colsum_pass_kernel(int64_t rows, int64_t cols, const float *__restrict__ x, int64_t ldx, float *__restrict__ out,
+                   int64_t ldo) {
+    const int64_t groups = (rows + RUN - 1) / RUN;
+    for (int64_t q = blockIdx.y; q < groups; q += gridDim.y) {
+        const int64_t r0 = q * RUN, r1 = imin64(r0 + RUN, rows);
+        for (int64_t j = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; j < cols;
+             j += int64_t(gridDim.x) * blockDim.x) {
+            float acc = x[r0 * ldx + j];
+            for (int64_t i = r0 + 1; i < r1; ++i) acc = __fadd_rn(acc, x[i * ldx + j]);
+            out[q * ldo + j] = acc;
+        }
+    }
+}
+
 // ------------------------------------------------------------ host ----
 
 int check_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx, const float *y, int64_t ldy) {
@@ -630,4 +752,134 @@ extern "C" int repops_gelu_f32(int64_t n, const float *x, float *y, cudaStream_t
     const int grid = int(std::min<int64_t>((per + 255) / 256, int64_t(di.sms) * 8));
     gelu_kernel<<<std::max(grid, 1), 256, 0, stream>>>(n, x, y, vec);
     return check_launch();
+}
+
+
+extern "C" int repops_gelu_backward_f32(int64_t n, const float *x, const float *dy, float *dx, cudaStream_t stream) {
+    if (n < 0) return REPOPS_ERR_INVALID_ARG;
+    if (n == 0) return REPOPS_OK;
+    if (!x || !dy || !dx || n > INT64_MAX / 4) return REPOPS_ERR_INVALID_ARG;
+    const uint64_t b = uint64_t(n) * 4u;
+    if ((dx != x && ranges_overlap(x, b, dx, b)) || (dx != dy && ranges_overlap(dy, b, dx, b)))
+        return REPOPS_ERR_ALIAS;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != REPOPS_OK) return rc;
+    const int vec = reinterpret_cast<uintptr_t>(x) % 16 == 0 && reinterpret_cast<uintptr_t>(dy) % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(dx) % 16 == 0;
+    const int64_t per = vec ? (n + 3) / 4 : n;
+    const int grid = int(std::min<int64_t>((per + 255) / 256, int64_t(di.sms) * 8));
+    gelu_backward_kernel<<<std::max(grid, 1), 256, 0, stream>>>(n, x, dy, dx, vec);
+    return check_launch();
+}
+
+namespace {
+// Span check for a rows x cols operand with pitch ld; false on overflow.
+bool rows_span(int64_t rows, int64_t cols, int64_t ld, uint64_t *bytes) {
+    if (rows == 0 || cols == 0) { *bytes = 0; return true; }
+    if (ld < cols || rows - 1 > (INT64_MAX / 4 - cols) / ld) return false;
+    *bytes = uint64_t((rows - 1) * ld + cols) * 4u;
+    return true;
+}
+}  // namespace
+
+extern "C" int repops_rmsnorm_backward_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx,
+                                           const float *gamma, float eps, const float *dy, int64_t lddy,
+                                           const float *res, int64_t ldres, float *dx, int64_t lddx, float *dyxh,
+                                           int64_t ldp, cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return REPOPS_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return REPOPS_OK;
+    if (!x || !gamma || !dy || !dx || !dyxh) return REPOPS_ERR_INVALID_ARG;
+    if ((cols + RUN - 1) / RUN > MAX_GENERIC_RUNS) return REPOPS_ERR_UNSUPPORTED;
+    uint64_t xb, yb, dxb, pb;
+    if (!rows_span(rows, cols, ldx, &xb) || !rows_span(rows, cols, lddy, &yb) || !rows_span(rows, cols, lddx, &dxb) ||
+        !rows_span(rows, cols, ldp, &pb))
+        return REPOPS_ERR_INVALID_ARG;
+    const uint64_t gb = uint64_t(cols) * 4u;
+    // outputs are written while every input row is still being re-read: no overlap at all
+    for (const void *o : {static_cast<const void *>(dx), static_cast<const void *>(dyxh)})
+        for (auto in : {std::make_pair(static_cast<const void *>(x), xb), std::make_pair(static_cast<const void *>(dy), yb),
+                        std::make_pair(static_cast<const void *>(gamma), gb)})
+            if (ranges_overlap(o, o == dx ? dxb : pb, in.first, in.second)) return REPOPS_ERR_ALIAS;
+    if (ranges_overlap(dx, dxb, dyxh, pb)) return REPOPS_ERR_ALIAS;
+    if (res) {
+        uint64_t rb;
+        if (!rows_span(rows, cols, ldres, &rb)) return REPOPS_ERR_INVALID_ARG;
+        const bool in_place = res == dx && ldres == lddx;
+        if ((!in_place && ranges_overlap(res, rb, dx, dxb)) || ranges_overlap(res, rb, dyxh, pb))
+            return REPOPS_ERR_ALIAS;
+    }
+    const int64_t runs = (cols + RUN - 1) / RUN;
+    const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(rmsnorm_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    rmsnorm_backward_kernel<<<grid_for_rows(rows), 256, smem, stream>>>(rows, cols, x, ldx, gamma, eps, dy, lddy, res,
+                                                                         ldres, dx, lddx, dyxh, ldp);
+    return check_launch();
+}
+
+extern "C" int repops_softmax_backward_f32(int64_t rows, int64_t cols, const float *p, int64_t ldp, const float *dp,
+                                           int64_t lddp, float *ds, int64_t ldds, cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return REPOPS_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return REPOPS_OK;
+    if (!p || !dp || !ds) return REPOPS_ERR_INVALID_ARG;
+    if ((cols + RUN - 1) / RUN > MAX_GENERIC_RUNS) return REPOPS_ERR_UNSUPPORTED;
+    uint64_t pb, gb, sb;
+    if (!rows_span(rows, cols, ldp, &pb) || !rows_span(rows, cols, lddp, &gb) || !rows_span(rows, cols, ldds, &sb))
+        return REPOPS_ERR_INVALID_ARG;
+    // in place over p or dp (same pitch) is allowed: each element is written after its last read
+    const bool on_p = ds == p && ldds == ldp, on_dp = ds == dp && ldds == lddp;
+    if ((!on_p && ranges_overlap(ds, sb, p, pb)) || (!on_dp && ranges_overlap(ds, sb, dp, gb))) return REPOPS_ERR_ALIAS;
+    const int64_t runs = (cols + RUN - 1) / RUN;
+    const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(softmax_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    softmax_backward_kernel<<<grid_for_rows(rows), 256, smem, stream>>>(rows, cols, p, ldp, dp, lddp, ds, ldds);
+    return check_launch();
+}
+
+extern "C" int repops_colsum_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
+                                 cudaStream_t stream) {
+    if (rows < 0 || cols < 0) return REPOPS_ERR_INVALID_ARG;
+    if (cols == 0) return REPOPS_OK;
+    if (!y) return REPOPS_ERR_INVALID_ARG;
+    if (rows == 0) {   // an empty column sums to +0
+        cudaError_t e = cudaMemsetAsync(y, 0, size_t(cols) * 4u, stream);
+        return e == cudaSuccess ? REPOPS_OK : set_cuda_error(e);
+    }
+    uint64_t xb;
+    if (!x || !rows_span(rows, cols, ldx, &xb)) return REPOPS_ERR_INVALID_ARG;
+    if (ranges_overlap(x, xb, y, uint64_t(cols) * 4u)) return REPOPS_ERR_ALIAS;
+    // scratch for the levels between the input and y: ceil(rows/32) rows, then ceil(rows/1024), ...
+    int64_t need = 0;
+    for (int64_t r = (rows + RUN - 1) / RUN; r > 1; r = (r + RUN - 1) / RUN) need += r;
+    float *scratch = nullptr;
+    if (need > 0) {
+        if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), size_t(need) * size_t(cols) * 4u, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return REPOPS_ERR_ALLOC;
+        }
+    }
+    int rc = REPOPS_OK;
+    const float *in = x;
+    int64_t in_rows = rows, in_ld = ldx;
+    float *level = scratch;
+    while (rc == REPOPS_OK) {
+        const int64_t out_rows = (in_rows + RUN - 1) / RUN;
+        float *out = out_rows == 1 ? y : level;   // every level is packed: pitch cols
+        const int gx = int(std::min<int64_t>((cols + 255) / 256, 64));
+        const int gy = int(std::min<int64_t>(out_rows, 65535));
+        colsum_pass_kernel<<<dim3(gx, gy), 256, 0, stream>>>(in_rows, cols, in, in_ld, out, cols);
+        rc = check_launch();
+        if (out_rows == 1) break;
+        in = out;
+        in_rows = out_rows;
+        in_ld = cols;
+        level += out_rows * cols;
+    }
+    if (scratch) {
+        cudaError_t e = cudaFreeAsync(scratch, stream);
+        if (rc == REPOPS_OK && e != cudaSuccess) rc = set_cuda_error(e);
+    }
+    return rc;
 }

@@ -18,6 +18,12 @@ Layer (pre-norm, causal, grouped-query attention):
     u    = GeLU(h W_up + b_up)                      GEMM, bias epilogue; GeLU kernel
     x    = x + u W_down + b_down                    GEMM, bias + residual epilogue
 
+`backward` runs the layer's backward pass from saved activations: weight,
+bias and gain gradients and the input gradient, every step again a library
+call (transposed GEMMs, the backward row operators, column sums); the key and
+value gradients of a key/value head accumulate its query heads in head order
+through the GEMM's residual epilogue.
+
 Every step is a library call (this module only slices tensors); the bits of
 the result depend on nothing but the inputs.  GeLU runs as its own kernel by
 default: inside the GEMM's epilogue it measured 2.5x its stand-alone cost (the
@@ -31,7 +37,8 @@ from dataclasses import dataclass
 
 import torch
 
-from . import gemm, gemm_batched, gelu, rmsnorm_rows, softmax_rows, ACT_GELU
+from . import (gemm, gemm_batched, gelu, rmsnorm_rows, softmax_rows, ACT_GELU, colsum, gelu_backward,
+               rmsnorm_backward, softmax_backward)
 
 
 @dataclass(frozen=True)
@@ -78,8 +85,15 @@ def init_weights(cfg: DecoderConfig, seed: int, device) -> dict:
     }
 
 
-def attention(qkv, cfg: DecoderConfig, out, scores):
-    """Causal grouped-query attention of every sequence into `out` (T x d)."""
+def _heads(t, rows, col0, group, dh):
+    """(group, S, dh) view of `group` heads' column blocks starting at col0."""
+    return t[rows, col0:col0 + group * dh].unflatten(1, (group, dh)).transpose(0, 1)
+
+
+def attention(qkv, cfg: DecoderConfig, out, scores, probs=None):
+    """Causal grouped-query attention of every sequence into `out` (T x d).
+    probs: optional (sequences * kv_heads, group, S, S) buffer that keeps
+    every head's softmax output for the backward pass."""
     S, dh, group = cfg.seq_len, cfg.d_head, cfg.heads // cfg.kv_heads
     k0, v0 = cfg.d, cfg.d + cfg.kv_heads * dh
     scale = 1.0 / float(dh) ** 0.5
@@ -92,32 +106,46 @@ def attention(qkv, cfg: DecoderConfig, out, scores):
             V = qkv[rows, v0 + k * dh:v0 + (k + 1) * dh]                        # (S, dh), shared
             # tiles wholly above the diagonal are skipped: the causal softmax
             # never reads them
-            gemm_batched(Q, Kt, out=scores, alpha=scale, causal_first=0)
-            P = scores.view(group * S, S)
+            sc = scores if probs is None else probs[s * cfg.kv_heads + k]
+            gemm_batched(Q, Kt, out=sc, alpha=scale, causal_first=0)
+            P = sc.view(group * S, S)
             softmax_rows(P, out=P, causal_first=0, causal_period=S)
             O = out[rows, q_cols].unflatten(1, (group, dh)).transpose(0, 1)     # heads' column blocks
-            gemm_batched(scores, V, out=O)
+            gemm_batched(sc, V, out=O)
 
 
 def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue: bool = False,
-            work: dict = None):
+            work: dict = None, save: dict = None):
     """Runs the layer on x (T x d, T a multiple of seq_len) in place and
     returns it.  `work`: reusable buffers from `workspace` (allocated when
-    absent)."""
+    absent).  `save`: a dict (from `activations`) that receives what
+    `backward` needs; the layer then keeps its GeLU input and runs GeLU as its
+    own kernel."""
     T = x.shape[0]
     if T % cfg.seq_len:
         raise ValueError("tokens must be a whole number of sequences")
     ws = work if work is not None else workspace(cfg, T, x.device)
-    h, qkv, attn, u = ws["h"], ws["qkv"], ws["attn"], ws["u"]
+    if save is not None:
+        save["x0"].copy_(x)
+        h, qkv, attn, u = save["h1"], save["qkv"], save["attn"], save["u"]
+    else:
+        h, qkv, attn, u = ws["h"], ws["qkv"], ws["attn"], ws["u"]
     rmsnorm_rows(x, w["g1"], cfg.eps, out=h)
     gemm(h, w["w_qkv"], out=qkv)
-    attention(qkv, cfg, attn, ws["scores"])
+    attention(qkv, cfg, attn, ws["scores"], save["probs"] if save is not None else None)
     if fused:
         gemm_batched(attn, w["w_o"], out=x, residual=x)
     else:
         x += gemm(attn, w["w_o"], out=ws["tmp_d"])
+    if save is not None:
+        save["x1"].copy_(x)
+        h = save["h2"]
     rmsnorm_rows(x, w["g2"], cfg.eps, out=h)
-    if fused:
+    if save is not None:
+        gemm_batched(h, w["w_up"], out=save["a"], bias=w["b_up"])
+        gelu(save["a"], out=u)
+        gemm_batched(u, w["w_down"], out=x, bias=w["b_down"], residual=x)
+    elif fused:
         if gelu_epilogue:
             gemm_batched(h, w["w_up"], out=u, bias=w["b_up"], act=ACT_GELU)
         else:
@@ -132,6 +160,87 @@ def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue
         y += w["b_down"]
         x += y
     return x
+
+
+def activations(cfg: DecoderConfig, tokens: int, device) -> dict:
+    """Buffers for the activations `forward(save=...)` keeps for `backward`
+    (every head's attention probabilities included: seqs * heads * S^2)."""
+    e = dict(dtype=torch.float32, device=device)
+    group, S = cfg.heads // cfg.kv_heads, cfg.seq_len
+    return {"x0": torch.empty(tokens, cfg.d, **e), "h1": torch.empty(tokens, cfg.d, **e),
+            "qkv": torch.empty(tokens, cfg.qkv_width, **e), "attn": torch.empty(tokens, cfg.d, **e),
+            "probs": torch.empty(tokens // S * cfg.kv_heads, group, S, S, **e),
+            "x1": torch.empty(tokens, cfg.d, **e), "h2": torch.empty(tokens, cfg.d, **e),
+            "a": torch.empty(tokens, cfg.ffn, **e), "u": torch.empty(tokens, cfg.ffn, **e)}
+
+
+def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None):
+    """Gradients of the layer given dy = dL/d(output): returns (dx, grads) with
+    grads holding one tensor per weight of `init_weights`.  dy is consumed
+    (used as scratch).  Every step is a library call:
+
+        dW_down = u^T dy, db_down = colsum(dy), du = dy W_down^T
+        da = GeLU'(a) du, dW_up = h2^T da, db_up = colsum(da), dh2 = da W_up^T
+        dx1 = RMSNorm'(x1; dh2) + dy, dg2 = colsum(dh2 * xhat2)
+        dW_o = attn^T dx1, dattn = dx1 W_o^T
+        attention, per sequence and key/value head k (its query heads h):
+            dP_h = dO_h V_k^T;  dV_k = sum_h P_h^T dO_h (head order)
+            dS_h = softmax'(P_h; dP_h)
+            dQ_h = s dS_h K_k;  dK_k = sum_h s dS_h^T Q_h (head order), s = 1/sqrt(d_head)
+        dW_qkv = h1^T dqkv, dh1 = dqkv W_qkv^T
+        dx0 = RMSNorm'(x0; dh1) + dx1, dg1 = colsum(dh1 * xhat1)
+    """
+    T = dy.shape[0]
+    S, dh, group = cfg.seq_len, cfg.d_head, cfg.heads // cfg.kv_heads
+    scale = 1.0 / float(dh) ** 0.5
+    k0, v0 = cfg.d, cfg.d + cfg.kv_heads * dh
+    ws = work if work is not None else backward_workspace(cfg, T, dy.device)
+    g = {}
+    g["w_down"] = gemm(saved["u"].t(), dy)
+    g["b_down"] = colsum(dy)
+    du = gemm(dy, w["w_down"].t(), out=ws["t_ffn"])
+    da = gelu_backward(saved["a"], du, out=du)
+    g["w_up"] = gemm(saved["h2"].t(), da)
+    g["b_up"] = colsum(da)
+    dh2 = gemm(da, w["w_up"].t(), out=ws["t_d"])
+    dx1, p2 = rmsnorm_backward(saved["x1"], w["g2"], cfg.eps, dh2, dx=dy, dyxh=ws["t_d2"], res=dy)
+    g["g2"] = colsum(p2)
+    g["w_o"] = gemm(saved["attn"].t(), dx1)
+    dattn = gemm(dx1, w["w_o"].t(), out=ws["t_d"])
+    dqkv = ws["dqkv"]
+    qkv = saved["qkv"]
+    dP = ws["dp"]
+    for s in range(T // S):
+        rows = slice(s * S, (s + 1) * S)
+        for k in range(cfg.kv_heads):
+            P = saved["probs"][s * cfg.kv_heads + k]                               # (group, S, S)
+            dO = _heads(dattn, rows, k * group * dh, group, dh)
+            V = qkv[rows, v0 + k * dh:v0 + (k + 1) * dh]
+            K = qkv[rows, k0 + k * dh:k0 + (k + 1) * dh]
+            Q = _heads(qkv, rows, k * group * dh, group, dh)
+            gemm_batched(dO, V.t(), out=dP)                                      # dP_h = dO_h V^T
+            dV = dqkv[rows, v0 + k * dh:v0 + (k + 1) * dh]
+            dK = dqkv[rows, k0 + k * dh:k0 + (k + 1) * dh]
+            for h in range(group):                                               # dV = sum_h P_h^T dO_h
+                gemm_batched(P[h].t(), dO[h], out=dV, residual=dV if h else None)
+            dS = dP.view(group * S, S)
+            softmax_backward(P.view(group * S, S), dS, out=dS)
+            gemm_batched(dP, K, out=_heads(dqkv, rows, k * group * dh, group, dh), alpha=scale)
+            for h in range(group):                                               # dK = sum_h s dS_h^T Q_h
+                gemm_batched(dP[h].t(), Q[h], out=dK, alpha=scale, residual=dK if h else None)
+    g["w_qkv"] = gemm(saved["h1"].t(), dqkv)
+    dh1 = gemm(dqkv, w["w_qkv"].t(), out=ws["t_d"])
+    dx0, p1 = rmsnorm_backward(saved["x0"], w["g1"], cfg.eps, dh1, dx=dx1, dyxh=ws["t_d2"], res=dx1)
+    g["g1"] = colsum(p1)
+    return dx0, g
+
+
+def backward_workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
+    e = dict(dtype=torch.float32, device=device)
+    group, S = cfg.heads // cfg.kv_heads, cfg.seq_len
+    return {"t_ffn": torch.empty(tokens, cfg.ffn, **e), "t_d": torch.empty(tokens, cfg.d, **e),
+            "t_d2": torch.empty(tokens, cfg.d, **e), "dqkv": torch.empty(tokens, cfg.qkv_width, **e),
+            "dp": torch.empty(group, S, S, **e)}
 
 
 def workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
