@@ -653,6 +653,24 @@ def run_sweep_decoder(dev, s, flush, peak):
     ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"]))
     print(json.dumps({"sweep": "causal grouped-query attention (batched QK^T, softmax, PV)", "tokens": T,
                       "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
+    # a training step of the layer: forward keeping its activations, then the
+    # backward pass from an upstream gradient (every weight's gradient and dx);
+    # backward does two GEMMs for each forward one: 3x the forward FLOPs
+    saved = decoder.activations(cfg, T, dev)
+    bws = decoder.backward_workspace(cfg, T, dev)
+    dy0 = inputs.normal((T, cfg.d), 1e-2, 302, dev)
+    dy = torch.empty_like(dy0)
+    ms_f = timed(lambda: decoder.forward(x, w, cfg, work=ws, save=saved))
+
+    def step():
+        decoder.forward(x, w, cfg, work=ws, save=saved)
+        dy.copy_(dy0)
+        decoder.backward(dy, w, cfg, saved, work=bws)
+    ms = timed(step)
+    print(json.dumps({"sweep": "decoder layer training step (forward keeping activations + backward)",
+                      "tokens": T, "ms": ms, "forward_ms": ms_f, "tokens_per_s": T / ms * 1e3,
+                      "tflops": 3 * flops / ms / 1e9, "frac_of_fp32_peak": 3 * flops / ms / 1e9 / peak}),
+          flush=True)
 
 
 def run_sweep_halfstore(dev, s, flush, peak, hbm):

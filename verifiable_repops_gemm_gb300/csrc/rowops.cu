@@ -595,6 +595,43 @@ softmax_backward_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, co
     }
 }
 
+// Softmax backward on aligned rows of up to 8192 values: each warp stages its
+// slices of the p and dp rows (coalesced 16-byte copies, swizzled as in the
+// forward), each lane folds its run of dp*p, the group fold is by shuffles,
+// and ds leaves through the p stage.  dp is read back from its stage after
+// the reduction instead of being held in registers.
+template <int T>
+__global__ void __launch_bounds__(T)
+softmax_backward_staged_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, const float *dp, int64_t lddp,
+                               float *ds, int64_t ldds) {
+    extern __shared__ float4 stage_mem[];
+    __shared__ float gbuf[2][RUN];
+    int phase = 0;
+    float4 *sp = stage_mem, *sd = stage_mem + T * RUN / 4;
+    const int runs = int((n + RUN - 1) / RUN);
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        stage_in<T, 1>(sp, p + row * ldp, n);
+        stage_in<T, 1>(sd, dp + row * lddp, n);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+        RowRuns<T, 1> a, b;
+        read_stage(a, sp, n);
+        read_stage(b, sd, n);
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) b.v[0][i] = __fmul_rn(b.v[0][i], a.v[0][i]);   // dp * p
+        const float sum = b.template reduce<Op::Sum>(Ident(), gbuf, phase, runs);
+        read_stage(b, sd, n);                                                          // dp again
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) a.v[0][i] = __fmul_rn(a.v[0][i], __fsub_rn(b.v[0][i], sum));
+        __syncwarp();                      // every lane has read both stages before the p stage is rewritten
+        write_stage(a, sp);
+        __syncwarp();
+        stage_out<T, 1>(sp, ds + row * ldds, n);
+        __syncwarp();
+    }
+}
+
 // One tree level of a column sum: out[q][j] = fold of rows [32q, 32q + 32) of
 // column j (left to right from the first).  Threads run along columns
 // (coalesced), the grid's y dimension along q.
@@ -831,6 +868,17 @@ extern "C" int repops_softmax_backward_f32(int64_t rows, int64_t cols, const flo
     const bool on_p = ds == p && ldds == ldp, on_dp = ds == dp && ldds == lddp;
     if ((!on_p && ranges_overlap(ds, sb, p, pb)) || (!on_dp && ranges_overlap(ds, sb, dp, gb))) return REPOPS_ERR_ALIAS;
     const int64_t runs = (cols + RUN - 1) / RUN;
+    const bool staged = runs <= 256 && rows_vec_ok(p, ldp, ds, ldds) && rows_vec_ok(dp, lddp, ds, ldds);
+    if (staged) {
+        auto go = [&](auto kern, int T) {
+            return launch_persistent(kern, T, size_t(2) * T * RUN * sizeof(float), rows, stream, rows, cols, p,
+                                     ldp, dp, lddp, ds, ldds);
+        };
+        if (runs <= 32) return go(softmax_backward_staged_kernel<32>, 32);
+        if (runs <= 64) return go(softmax_backward_staged_kernel<64>, 64);
+        if (runs <= 128) return go(softmax_backward_staged_kernel<128>, 128);
+        return go(softmax_backward_staged_kernel<256>, 256);
+    }
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(softmax_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);

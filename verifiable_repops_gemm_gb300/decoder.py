@@ -7,10 +7,11 @@ Layer (pre-norm, causal, grouped-query attention):
 
     h    = RMSNorm(x; g1)
     qkv  = h W_qkv                                  one GEMM
-    for every sequence s and key/value head k (its H/KV query heads batched):
+    for every sequence (each GEMM call batches one query head of every
+    key/value group, whose operands lie one stride apart):
         S = (Q K^T) / sqrt(d_head)                  batched GEMM, alpha epilogue,
                                                     tiles above the diagonal skipped
-        P = causal softmax of the heads' rows       one row-operator call
+        P = causal softmax of every head's rows     one row-operator call
         O = P V                                     batched GEMM, written as the
                                                     heads' column blocks
     x    = x + O W_o                                GEMM, residual epilogue (in place)
@@ -85,33 +86,41 @@ def init_weights(cfg: DecoderConfig, seed: int, device) -> dict:
     }
 
 
-def _heads(t, rows, col0, group, dh):
-    """(group, S, dh) view of `group` heads' column blocks starting at col0."""
-    return t[rows, col0:col0 + group * dh].unflatten(1, (group, dh)).transpose(0, 1)
+def _per_kv(t, rows, col0, kv, group, h, dh):
+    """(kv, S, dh) view of query head h of every key/value group: the column
+    block (k*group + h)*dh of rows, k = 0 .. kv-1 (a batch stride of
+    group*dh)."""
+    return t[rows, col0:col0 + kv * group * dh].unflatten(1, (kv, group, dh))[:, :, h, :].transpose(0, 1)
+
+
+def _kv(t, rows, col0, kv, dh):
+    """(kv, S, dh) view of the key or value heads: column block col0 + k*dh."""
+    return t[rows, col0:col0 + kv * dh].unflatten(1, (kv, dh)).transpose(0, 1)
 
 
 def attention(qkv, cfg: DecoderConfig, out, scores, probs=None):
     """Causal grouped-query attention of every sequence into `out` (T x d).
-    probs: optional (sequences * kv_heads, group, S, S) buffer that keeps
-    every head's softmax output for the backward pass."""
-    S, dh, group = cfg.seq_len, cfg.d_head, cfg.heads // cfg.kv_heads
-    k0, v0 = cfg.d, cfg.d + cfg.kv_heads * dh
+    scores: (kv_heads, group, S, S) scratch; probs: optional
+    (sequences * kv_heads, group, S, S) buffer that keeps every head's softmax
+    output for the backward pass.  Each GEMM call batches query head h of all
+    key/value groups (their operands sit at one stride apart)."""
+    S, dh, kv = cfg.seq_len, cfg.d_head, cfg.kv_heads
+    group = cfg.heads // kv
+    k0, v0 = cfg.d, cfg.d + kv * dh
     scale = 1.0 / float(dh) ** 0.5
     for s in range(qkv.shape[0] // S):
         rows = slice(s * S, (s + 1) * S)
-        for k in range(cfg.kv_heads):
-            q_cols = slice(k * group * dh, (k + 1) * group * dh)
-            Q = qkv[rows, q_cols].unflatten(1, (group, dh)).transpose(0, 1)     # (group, S, dh)
-            Kt = qkv[rows, k0 + k * dh:k0 + (k + 1) * dh].t()                   # (dh, S), shared
-            V = qkv[rows, v0 + k * dh:v0 + (k + 1) * dh]                        # (S, dh), shared
+        sc = scores if probs is None else probs[s * kv:(s + 1) * kv]               # (kv, group, S, S)
+        Kt = _kv(qkv, rows, k0, kv, dh).transpose(1, 2)                          # (kv, dh, S)
+        V = _kv(qkv, rows, v0, kv, dh)
+        for h in range(group):
             # tiles wholly above the diagonal are skipped: the causal softmax
             # never reads them
-            sc = scores if probs is None else probs[s * cfg.kv_heads + k]
-            gemm_batched(Q, Kt, out=sc, alpha=scale, causal_first=0)
-            P = sc.view(group * S, S)
-            softmax_rows(P, out=P, causal_first=0, causal_period=S)
-            O = out[rows, q_cols].unflatten(1, (group, dh)).transpose(0, 1)     # heads' column blocks
-            gemm_batched(sc, V, out=O)
+            gemm_batched(_per_kv(qkv, rows, 0, kv, group, h, dh), Kt, out=sc[:, h], alpha=scale, causal_first=0)
+        P = sc.view(kv * group * S, S)
+        softmax_rows(P, out=P, causal_first=0, causal_period=S)
+        for h in range(group):
+            gemm_batched(sc[:, h], V, out=_per_kv(out, rows, 0, kv, group, h, dh))
 
 
 def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue: bool = False,
@@ -209,25 +218,25 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None)
     dattn = gemm(dx1, w["w_o"].t(), out=ws["t_d"])
     dqkv = ws["dqkv"]
     qkv = saved["qkv"]
-    dP = ws["dp"]
+    kv = cfg.kv_heads
+    dP = ws["dp"]                                                                # (kv, group, S, S)
     for s in range(T // S):
         rows = slice(s * S, (s + 1) * S)
-        for k in range(cfg.kv_heads):
-            P = saved["probs"][s * cfg.kv_heads + k]                               # (group, S, S)
-            dO = _heads(dattn, rows, k * group * dh, group, dh)
-            V = qkv[rows, v0 + k * dh:v0 + (k + 1) * dh]
-            K = qkv[rows, k0 + k * dh:k0 + (k + 1) * dh]
-            Q = _heads(qkv, rows, k * group * dh, group, dh)
-            gemm_batched(dO, V.t(), out=dP)                                      # dP_h = dO_h V^T
-            dV = dqkv[rows, v0 + k * dh:v0 + (k + 1) * dh]
-            dK = dqkv[rows, k0 + k * dh:k0 + (k + 1) * dh]
-            for h in range(group):                                               # dV = sum_h P_h^T dO_h
-                gemm_batched(P[h].t(), dO[h], out=dV, residual=dV if h else None)
-            dS = dP.view(group * S, S)
-            softmax_backward(P.view(group * S, S), dS, out=dS)
-            gemm_batched(dP, K, out=_heads(dqkv, rows, k * group * dh, group, dh), alpha=scale)
-            for h in range(group):                                               # dK = sum_h s dS_h^T Q_h
-                gemm_batched(dP[h].t(), Q[h], out=dK, alpha=scale, residual=dK if h else None)
+        P = saved["probs"][s * kv:(s + 1) * kv]
+        V, K = _kv(qkv, rows, v0, kv, dh), _kv(qkv, rows, k0, kv, dh)
+        dV, dK = _kv(dqkv, rows, v0, kv, dh), _kv(dqkv, rows, k0, kv, dh)
+        for h in range(group):
+            dO = _per_kv(dattn, rows, 0, kv, group, h, dh)
+            gemm_batched(dO, V.transpose(1, 2), out=dP[:, h])                    # dP_h = dO_h V^T
+            # dV = sum over the group's heads, in head order, of P_h^T dO_h
+            gemm_batched(P[:, h].transpose(1, 2), dO, out=dV, residual=dV if h else None)
+        dS = dP.view(kv * group * S, S)
+        softmax_backward(P.view(kv * group * S, S), dS, out=dS)
+        for h in range(group):
+            gemm_batched(dP[:, h], K, out=_per_kv(dqkv, rows, 0, kv, group, h, dh), alpha=scale)
+            # dK = sum over the group's heads, in head order, of s dS_h^T Q_h
+            gemm_batched(dP[:, h].transpose(1, 2), _per_kv(qkv, rows, 0, kv, group, h, dh), out=dK, alpha=scale,
+                         residual=dK if h else None)
     g["w_qkv"] = gemm(saved["h1"].t(), dqkv)
     dh1 = gemm(dqkv, w["w_qkv"].t(), out=ws["t_d"])
     dx0, p1 = rmsnorm_backward(saved["x0"], w["g1"], cfg.eps, dh1, dx=dx1, dyxh=ws["t_d2"], res=dx1)
@@ -240,7 +249,7 @@ def backward_workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
     group, S = cfg.heads // cfg.kv_heads, cfg.seq_len
     return {"t_ffn": torch.empty(tokens, cfg.ffn, **e), "t_d": torch.empty(tokens, cfg.d, **e),
             "t_d2": torch.empty(tokens, cfg.d, **e), "dqkv": torch.empty(tokens, cfg.qkv_width, **e),
-            "dp": torch.empty(group, S, S, **e)}
+            "dp": torch.empty(cfg.kv_heads, group, S, S, **e)}
 
 
 def workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
@@ -248,5 +257,5 @@ def workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
     group = cfg.heads // cfg.kv_heads
     return {"h": torch.empty(tokens, cfg.d, **e), "qkv": torch.empty(tokens, cfg.qkv_width, **e),
             "attn": torch.empty(tokens, cfg.d, **e), "u": torch.empty(tokens, cfg.ffn, **e),
-            "scores": torch.empty(group, cfg.seq_len, cfg.seq_len, **e),
+            "scores": torch.empty(cfg.kv_heads, group, cfg.seq_len, cfg.seq_len, **e),
             "tmp_d": torch.empty(tokens, cfg.d, **e)}
