@@ -502,6 +502,8 @@ def run_sweep(args):
         run_sweep_decoder(dev, s, flush, peak)
     if args.sweep in ("all", "halfstore"):
         run_sweep_halfstore(dev, s, flush, peak, peaks.get("hbm_gbs", 6800.0))
+    if args.sweep in ("all", "train"):
+        run_sweep_train(dev, s, flush, peak)
 
 
 def run_sweep_gemm(dev, s, flush, peak):
@@ -673,6 +675,54 @@ def run_sweep_decoder(dev, s, flush, peak):
           flush=True)
 
 
+def run_sweep_train(dev, s, flush, peak):
+    """The verifiable training step end to end: 4 contributors (DIDs), each
+    with 2 x 2048 tokens through 2 Llama-3.2-1B-sized decoder layers, forward
+    and backward; their gradients folded in DID order into the mean, SGD on the
+    flat theta (88 M parameters) and the Merkle root of theta.  Synthetic
+    inputs and upstream gradients; the step is timed as a whole and by part."""
+    from verifiable_repops_gemm_gb300 import decoder, train
+    cfg = decoder.DecoderConfig()
+    T, layers, C = 2 * cfg.seq_len, 2, 4
+    model = train.Model(cfg, layers, dev, seed=700)
+    ws = train.Workspace(model, T, dev)
+    grads = [model.gradient_buffer() for _ in range(C)]
+    contribs = [(b"did:zoo:contributor-%02d" % c, inputs.normal((T, cfg.d), 1.0, 710 + c, dev),
+                 inputs.normal((T, cfg.d), 1e-2, 720 + c, dev)) for c in range(C)]
+    theta0 = model.theta.clone()
+
+    def step():
+        model.theta.copy_(theta0)
+        return train.train_step(model, contribs, 1e-3, ws, grads)
+
+    with torch.cuda.stream(s):
+        step()
+        torch.cuda.synchronize(dev)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        model.theta.copy_(theta0)
+        ev[0].record(s)
+        for (did, x, dy), g in zip(contribs, grads):
+            train.contributor_gradient(model, x, dy, g, ws)
+        ev[1].record(s)
+        order = rp.sort_ids([did for did, _, _ in contribs])
+        rp.fixed_order_mean_sgd(grads, order, 1e-3, model.theta, stream=s)
+        ev[2].record(s)
+        root = rp.merkle_sha256(model.theta, stream=s)
+        ev[3].record(s)
+    torch.cuda.synchronize(dev)
+    total = ev[0].elapsed_time(ev[3])
+    flops = 3 * layers * C * cfg.flops(T)
+    n = model.theta.numel()
+    print(json.dumps({"sweep": "verifiable training step: 4 contributors x 2 decoder layers x 4096 tokens, "
+                               "fixed-order mean + SGD over %d parameters, Merkle root of theta" % n,
+                      "ms": total, "tokens_per_s": C * T / total * 1e3, "tflops": flops / total / 1e9,
+                      "frac_of_fp32_peak": flops / total / 1e9 / peak,
+                      "gradients_ms": ev[0].elapsed_time(ev[1]), "mean_sgd_ms": ev[1].elapsed_time(ev[2]),
+                      "commit_ms": ev[2].elapsed_time(ev[3]), "root": bytes(root.cpu().numpy()).hex()[:16]}),
+          flush=True)
+
+
 def run_sweep_halfstore(dev, s, flush, peak, hbm):
     """Half-precision storage around the binary32 path: the mean + SGD step of
     the hot path (16 contributors x 2^28) with bfloat16 gradients next to
@@ -795,7 +845,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
-                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore"),
+                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore", "train"),
                     help="time every workload of a part (one JSON line each) instead of the step")
     args = ap.parse_args()
     if args.sweep:

@@ -183,10 +183,12 @@ def activations(cfg: DecoderConfig, tokens: int, device) -> dict:
             "a": torch.empty(tokens, cfg.ffn, **e), "u": torch.empty(tokens, cfg.ffn, **e)}
 
 
-def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None):
+def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None, grads: dict = None):
     """Gradients of the layer given dy = dL/d(output): returns (dx, grads) with
-    grads holding one tensor per weight of `init_weights`.  dy is consumed
-    (used as scratch).  Every step is a library call:
+    grads holding one tensor per weight of `init_weights` (written into the
+    tensors of `grads` when given, e.g. views of one flat gradient buffer).
+    dy is consumed (used as scratch) and dx is returned in its storage.  Every
+    step is a library call:
 
         dW_down = u^T dy, db_down = colsum(dy), du = dy W_down^T
         da = GeLU'(a) du, dW_up = h2^T da, db_up = colsum(da), dh2 = da W_up^T
@@ -205,16 +207,17 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None)
     k0, v0 = cfg.d, cfg.d + cfg.kv_heads * dh
     ws = work if work is not None else backward_workspace(cfg, T, dy.device)
     g = {}
-    g["w_down"] = gemm(saved["u"].t(), dy)
-    g["b_down"] = colsum(dy)
+    o = grads if grads is not None else {}
+    g["w_down"] = gemm(saved["u"].t(), dy, out=o.get("w_down"))
+    g["b_down"] = colsum(dy, out=o.get("b_down"))
     du = gemm(dy, w["w_down"].t(), out=ws["t_ffn"])
     da = gelu_backward(saved["a"], du, out=du)
-    g["w_up"] = gemm(saved["h2"].t(), da)
-    g["b_up"] = colsum(da)
+    g["w_up"] = gemm(saved["h2"].t(), da, out=o.get("w_up"))
+    g["b_up"] = colsum(da, out=o.get("b_up"))
     dh2 = gemm(da, w["w_up"].t(), out=ws["t_d"])
     dx1, p2 = rmsnorm_backward(saved["x1"], w["g2"], cfg.eps, dh2, dx=dy, dyxh=ws["t_d2"], res=dy)
-    g["g2"] = colsum(p2)
-    g["w_o"] = gemm(saved["attn"].t(), dx1)
+    g["g2"] = colsum(p2, out=o.get("g2"))
+    g["w_o"] = gemm(saved["attn"].t(), dx1, out=o.get("w_o"))
     dattn = gemm(dx1, w["w_o"].t(), out=ws["t_d"])
     dqkv = ws["dqkv"]
     qkv = saved["qkv"]
@@ -237,10 +240,10 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None)
             # dK = sum over the group's heads, in head order, of s dS_h^T Q_h
             gemm_batched(dP[:, h].transpose(1, 2), _per_kv(qkv, rows, 0, kv, group, h, dh), out=dK, alpha=scale,
                          residual=dK if h else None)
-    g["w_qkv"] = gemm(saved["h1"].t(), dqkv)
+    g["w_qkv"] = gemm(saved["h1"].t(), dqkv, out=o.get("w_qkv"))
     dh1 = gemm(dqkv, w["w_qkv"].t(), out=ws["t_d"])
     dx0, p1 = rmsnorm_backward(saved["x0"], w["g1"], cfg.eps, dh1, dx=dx1, dyxh=ws["t_d2"], res=dx1)
-    g["g1"] = colsum(p1)
+    g["g1"] = colsum(p1, out=o.get("g1"))
     return dx0, g
 
 
