@@ -130,6 +130,23 @@ int repops_gemm_f32_ex(int transA, int transB,
                        float *C, int64_t ldc,
                        cudaStream_t stream);
 
+/* As repops_gemm_f32 with A, B and C in HOST memory (row-major, pitches as
+ * there; page-locked memory for full speed).  The call takes device memory
+ * for A, B and C (16-byte pitches) with cudaMallocAsync on `stream`, copies B,
+ * then copies A in row blocks on a helper stream while the previous block's
+ * GEMM runs on `stream`, copies each block of C back on a second helper stream
+ * as it completes, and releases the memory; everything is ordered before work
+ * later enqueued on `stream`.  Asynchronous: A, B and C must stay valid, and C
+ * is complete, once `stream` has reached this point.  The bits equal
+ * repops_gemm_f32's (rows of C are independent k-chains).  Errors as
+ * repops_gemm_f32, plus ALLOC (device memory refused) and ALIAS (C's host
+ * bytes overlap A's or B's). */
+int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K,
+                         const float *A, int64_t lda,
+                         const float *B, int64_t ldb,
+                         float *C, int64_t ldc,
+                         cudaStream_t stream);
+
 /* Loader paths for repops_gemm_f32_config. */
 #define REPOPS_LOADER_AUTO 0      /* TMA when operands allow it, else CPASYNC */
 #define REPOPS_LOADER_TMA 1       /* tensor-memory-accelerator tiles; needs 16-byte

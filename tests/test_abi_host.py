@@ -297,3 +297,12 @@ def test_backward_operators_reject_bad_arguments(L):
     assert sb(4, 4, FAKE_A, 3, FAKE_B, 4, FAKE_C, 4, None) == -1
     assert sb(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 8, 4, None) == -2
     assert sb(4, 400000, FAKE_A, 400000, FAKE_B, 400000, FAKE_C, 400000, None) == -7
+
+
+def test_host_buffer_gemm_rejects_bad_arguments(L):
+    g = L.repops_gemm_f32_host
+    assert g(-1, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert g(4, 4, 4, FAKE_A, 3, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert g(4, 4, 4, None, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert g(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 16, 4, None) == -2
+    assert g(0, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == 0

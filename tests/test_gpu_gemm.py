@@ -233,3 +233,19 @@ def test_gemm_repacked_operands_match_every_loader(rp, orc):
     # transposed storage of both operands (ld = 1601 again)
     C_t = run(rp, A.t().contiguous().t(), B.t().contiguous().t())
     assert torch.equal(C_auto.view(torch.int32), C_t.view(torch.int32))
+
+
+@pytest.mark.parametrize("M,N,K,pinned", [(300, 260, 70, True), (1000, 129, 33, False), (4097, 1023, 3001, True),
+                                          (64, 64, 0, True)])
+def test_host_buffer_gemm_same_bits(rp, M, N, K, pinned):
+    # row blocks of C are independent k-chains: the pipelined host-buffer call
+    # gives the device GEMM's bits, for pinned and pageable host memory
+    A = torch.randn(M, K + 1)[:, :K] if K else torch.randn(M, 0)
+    B = torch.randn(K, N)
+    if pinned:
+        A, B = A.pin_memory(), B.pin_memory()
+    s = torch.cuda.Stream()
+    C = rp.gemm_host(A, B, stream=s)
+    s.synchronize()
+    want = rp.gemm(A.cuda(), B.cuda()).cpu()
+    assert torch.equal(C.view(torch.int32), want.view(torch.int32))

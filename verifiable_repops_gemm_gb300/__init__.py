@@ -33,7 +33,7 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "gemm", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "gemm", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
@@ -171,6 +171,30 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
                                    out.data_ptr(), ldc, sc, ctypes.c_float(alpha), pbias, int(act),
                                    pr, ldr, sr, int(causal_first), _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32_batched")
+    return out
+
+
+def gemm_host(A, B, out=None, *, stream=None):
+    """C = A @ B for row-major float32 CPU tensors (pin them for full speed):
+    the copies to and from the device overlap the GEMM's row blocks
+    (repops_gemm_f32_host).  Asynchronous on `stream`: synchronise it before
+    reading `out`; A, B and out must stay alive until then."""
+    import torch
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    for t, n in ((A, "A"), (B, "B")):
+        if t.dtype != torch.float32 or t.is_cuda or t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError("%s must be a row-major float32 CPU tensor" % n)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, pin_memory=A.is_pinned())
+    if out.dtype != torch.float32 or out.is_cuda or tuple(out.shape) != (M, N) or (N > 1 and out.stride(1) != 1):
+        raise ValueError("out must be a row-major (M, N) float32 CPU tensor")
+    rc = load().repops_gemm_f32_host(M, N, K, A.data_ptr(), max(A.stride(0), K, 1), B.data_ptr(),
+                                     max(B.stride(0), N, 1), out.data_ptr(), max(out.stride(0), N, 1),
+                                     _stream_handle(stream))
+    _capi.check(rc, "repops_gemm_f32_host")
     return out
 
 

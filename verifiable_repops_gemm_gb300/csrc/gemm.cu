@@ -415,6 +415,110 @@ extern "C" int repops_gemm_f32_batched(int config, int loader, int transA, int t
                                  stream);
 }
 
+namespace {
+
+// Ordered teardown of the helper streams and events of one host-buffer call:
+// destruction is deferred by the runtime until their pending work completes.
+struct HostCallResources {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t ev[4 + 2 * 64] = {};
+    int nev = 0;
+    ~HostCallResources() {
+        for (int i = 0; i < nev; ++i)
+            if (ev[i]) cudaEventDestroy(ev[i]);
+        if (in) cudaStreamDestroy(in);
+        if (out) cudaStreamDestroy(out);
+    }
+    cudaError_t event(cudaEvent_t *e) {
+        cudaError_t r = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
+        if (r == cudaSuccess) *e = ev[nev++];
+        return r;
+    }
+};
+
+}  // namespace
+
+extern "C" int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float *A, int64_t lda, const float *B,
+                                    int64_t ldb, float *C, int64_t ldc, cudaStream_t stream) {
+    if (M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
+    if (lda < std::max<int64_t>(1, K) || ldb < std::max<int64_t>(1, N) || ldc < std::max<int64_t>(1, N))
+        return REPOPS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return REPOPS_OK;
+    if (!C || (K > 0 && (!A || !B))) return REPOPS_ERR_INVALID_ARG;
+    uint64_t ab = 0, bb = 0, cb = 0;
+    if (!operand_span(M, K, lda, &ab) || !operand_span(K, N, ldb, &bb) || !operand_span(M, N, ldc, &cb))
+        return REPOPS_ERR_INVALID_ARG;
+    if (ranges_overlap(C, cb, A, ab) || ranges_overlap(C, cb, B, bb)) return REPOPS_ERR_ALIAS;
+    // device copies with a 16-byte pitch (the TMA loader's rule)
+    const int64_t pk = std::max<int64_t>(4, (K + 3) / 4 * 4), pn = (N + 3) / 4 * 4;   // pitches >= 1 even for K = 0
+    const size_t bytesA = size_t(M) * size_t(pk) * 4u, bytesB = size_t(K) * size_t(pn) * 4u;
+    const size_t bytesC = size_t(M) * size_t(pn) * 4u;
+    // A's row blocks: about four, each a multiple of 128 rows, at most 64
+    const int64_t rows = std::max<int64_t>(128, (M / 4 + 127) / 128 * 128);
+    const int blocks = int(std::min<int64_t>((M + rows - 1) / rows, 64));
+    const int64_t step = (M + blocks - 1) / blocks;
+    HostCallResources res;
+    cudaError_t e = cudaStreamCreateWithFlags(&res.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&res.out, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    void *mem = nullptr;
+    if (cudaMallocAsync(&mem, bytesA + bytesB + bytesC, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return REPOPS_ERR_ALLOC;
+    }
+    float *dA = static_cast<float *>(mem), *dB = dA + bytesA / 4, *dC = dB + bytesB / 4;
+    cudaEvent_t ready, b_in, done_in, done_out;
+    int rc = REPOPS_OK;
+    if ((e = res.event(&ready)) != cudaSuccess || (e = res.event(&b_in)) != cudaSuccess ||
+        (e = res.event(&done_in)) != cudaSuccess || (e = res.event(&done_out)) != cudaSuccess) {
+        cudaFreeAsync(mem, stream);
+        return set_cuda_error(e);
+    }
+    // the helper streams start once the allocation is ordered on `stream`
+    if (rc == REPOPS_OK && ((e = cudaEventRecord(ready, stream)) != cudaSuccess ||
+                            (e = cudaStreamWaitEvent(res.in, ready, 0)) != cudaSuccess ||
+                            (e = cudaStreamWaitEvent(res.out, ready, 0)) != cudaSuccess))
+        rc = set_cuda_error(e);
+    if (rc == REPOPS_OK && K > 0 &&
+        ((e = cudaMemcpy2DAsync(dB, size_t(pn) * 4u, B, size_t(ldb) * 4u, size_t(N) * 4u, size_t(K),
+                                cudaMemcpyHostToDevice, res.in)) != cudaSuccess ||
+         (e = cudaEventRecord(b_in, res.in)) != cudaSuccess ||
+         (e = cudaStreamWaitEvent(stream, b_in, 0)) != cudaSuccess))
+        rc = set_cuda_error(e);
+    for (int i = 0; rc == REPOPS_OK && i < blocks; ++i) {
+        const int64_t r0 = int64_t(i) * step, r1 = std::min<int64_t>(M, r0 + step);
+        if (r0 >= r1) break;
+        cudaEvent_t a_in, c_done;
+        if ((e = res.event(&a_in)) != cudaSuccess || (e = res.event(&c_done)) != cudaSuccess) {
+            rc = set_cuda_error(e);
+            break;
+        }
+        if (K > 0 && ((e = cudaMemcpy2DAsync(dA + r0 * pk, size_t(pk) * 4u, A + r0 * lda, size_t(lda) * 4u,
+                                             size_t(K) * 4u, size_t(r1 - r0), cudaMemcpyHostToDevice, res.in)) !=
+                          cudaSuccess ||
+                      (e = cudaEventRecord(a_in, res.in)) != cudaSuccess ||
+                      (e = cudaStreamWaitEvent(stream, a_in, 0)) != cudaSuccess)) {
+            rc = set_cuda_error(e);
+            break;
+        }
+        rc = gemm_dispatch(-1, REPOPS_LOADER_AUTO, 0, 0, r1 - r0, N, K, dA + r0 * pk, pk, dB, pn, dC + r0 * pn, pn,
+                           stream);
+        if (rc != REPOPS_OK) break;
+        if ((e = cudaEventRecord(c_done, stream)) != cudaSuccess || (e = cudaStreamWaitEvent(res.out, c_done, 0)) != cudaSuccess ||
+            (e = cudaMemcpy2DAsync(C + r0 * ldc, size_t(ldc) * 4u, dC + r0 * pn, size_t(pn) * 4u, size_t(N) * 4u,
+                                   size_t(r1 - r0), cudaMemcpyDeviceToHost, res.out)) != cudaSuccess)
+            rc = set_cuda_error(e);
+    }
+    // `stream` resumes after every copy in and back; then the memory is released
+    if ((e = cudaEventRecord(done_in, res.in)) != cudaSuccess || (e = cudaStreamWaitEvent(stream, done_in, 0)) != cudaSuccess ||
+        (e = cudaEventRecord(done_out, res.out)) != cudaSuccess || (e = cudaStreamWaitEvent(stream, done_out, 0)) != cudaSuccess) {
+        if (rc == REPOPS_OK) rc = set_cuda_error(e);
+    }
+    e = cudaFreeAsync(mem, stream);
+    if (rc == REPOPS_OK && e != cudaSuccess) rc = set_cuda_error(e);
+    return rc;
+}
+
 extern "C" int repops_gemm_config_count(void) { return kGemmConfigCount; }
 
 extern "C" int repops_gemm_config_info(int config, int *bm, int *bn, int *threads, int *tm, int *tn) {
