@@ -249,3 +249,18 @@ def test_host_buffer_gemm_same_bits(rp, M, N, K, pinned):
     s.synchronize()
     want = rp.gemm(A.cuda(), B.cuda()).cpu()
     assert torch.equal(C.view(torch.int32), want.view(torch.int32))
+
+
+def test_transposed_b_large_problem_same_bits(rp):
+    # >= 4 GFLOP with B stored transposed: B is transposed into padded scratch
+    # and the row-major kernels run; the bits equal row-major B's and the
+    # forced 4-byte loader's (which reads the transposed storage directly)
+    M, N, K = 1024, 1001, 2048
+    A = inputs.normal((M, K), 1.0, 700, DEV)
+    B = inputs.normal((K, N), 1.0, 701, DEV)
+    Bcm = B.t().contiguous().t()
+    C_rm = run(rp, A, B)
+    C_cm = run(rp, A, Bcm)
+    C_forced = run(rp, A, Bcm, config=1, loader=2)
+    assert torch.equal(C_rm.view(torch.int32), C_cm.view(torch.int32))
+    assert torch.equal(C_rm.view(torch.int32), C_forced.view(torch.int32))
