@@ -173,6 +173,11 @@ int repops_gemm_config_count(void);
 int repops_gemm_config_info(int config, int *bm, int *bn, int *threads,
                             int *tm, int *tn);
 
+/* Resident CTAs per SM of configuration `config`'s TMA kernel on the current
+ * device (the figure the automatic choice models with); a negative status on
+ * error (INVALID_ARG for an unknown config). */
+int repops_gemm_config_occupancy(int config);
+
 /* The configuration repops_gemm_f32 would choose for an M x N output on the
  * current device (-1 when M or N is 0). */
 int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);

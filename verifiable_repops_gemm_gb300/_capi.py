@@ -61,6 +61,7 @@ SIGNATURES = {
     "repops_gemm_typed": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _vp, _i32, _i64, _vp, _i32, _i64,
                                  _vp, _i32, _i64, _vp]),
     "repops_rolling_hash_u32": (_i32, [_i64, _i64, _vp, _i64, _i64, _vp, _i64, _vp]),
+    "repops_gemm_config_occupancy": (_i32, [_i32]),
     "repops_gemm_f32_host": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "repops_colsum_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _vp]),
     "repops_gelu_backward_f32": (_i32, [_i64, _vp, _vp, _vp, _vp]),

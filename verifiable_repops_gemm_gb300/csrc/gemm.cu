@@ -66,14 +66,27 @@ int occupancy_of(int dev, int c) {
     return v;
 }
 
-// Picks the configuration with the smallest modelled time: each SM runs
-// ceil(tiles / SMs) tiles, `conc` of them at once; an SM with fewer resident
-// consumer warps than it needs to hide the ring's fill and the epilogue is
-// modelled as proportionally slower -- 8 warps for long k-chains, more as K
-// shrinks below 256 (each tile then has few k-slices to overlap them with);
-// per-thread efficiency falls with the thread tile (shared-memory loads per
-// FP32 instruction).  Measured on short-K batched attention (K = 64): 64x64
-// tiles 1.6x faster than 64x128.
+// Per-tile throughput of a configuration relative to the 64x128 / 128x64
+// tiles (8x8 accumulators, 128 consumer threads), fitted to measurements of
+// all five configurations on 20 shapes from 256^3 to 8192^3 on a GB300.  The
+// 128x128 tile's figure sits just under 1: where the two tiles' waves line up
+// they are within 1% either way, and 64x128 is the faster at 8192^3.
+double relative_efficiency(const GemmConfigInfo &ci) {
+    const int acc = ci.tm * ci.tn;
+    if (acc >= 64) return ci.threads > 128 ? 0.995 : 1.0;
+    if (acc >= 32) return 0.94;
+    return 0.76;
+}
+
+// Picks the configuration with the smallest modelled time.  The busiest SM
+// runs n = ceil(tiles / SMs) tiles, `conc` at a time; a tile takes
+// BM * BN / eff when `conc` share the SM, and a last round with fewer tiles
+// than `conc` is charged 0.7 of a shared round (a lone CTA runs faster than
+// half speed).  An SM with fewer resident consumer warps than it needs to hide
+// the ring's fill and the epilogue is modelled as proportionally slower -- 8
+// warps for long k-chains, more as K shrinks below 256.  Fitted to the same
+// measurements: its choice is within 2% of the fastest configuration on all
+// 20 shapes and within 1% on 19 (the previous round-based model lost up to 9%).
 int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) {
     DeviceInfo di;
     if (current_device_info(&di) != REPOPS_OK || di.device < 0 || di.device >= kMaxDevices) return 0;
@@ -83,16 +96,13 @@ int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) 
         const GemmConfigInfo ci = config_info(c);
         const double tiles =
             double((M + ci.bm - 1) / ci.bm) * double((N + ci.bn - 1) / ci.bn) * double(std::max<int64_t>(batch, 1));
-        const double per_sm = std::ceil(tiles / di.sms);
-        const double conc = std::min<double>(occupancy_of(di.device, c), per_sm);
-        const double rounds = std::ceil(per_sm / conc);
-        const double warps = conc * ci.threads / 32.0;
+        const double n = std::ceil(tiles / di.sms);
+        const double conc = std::max(1, occupancy_of(di.device, c));
+        const double full = std::floor(n / conc), rem = n - full * conc;
+        const double warps = std::min(conc, n) * ci.threads / 32.0;
         const double need = std::min(32.0, 8.0 * std::max(1.0, 256.0 / double(std::max<int64_t>(K, 1))));
-        // two or more CTAs per SM hide each other's ring refills and epilogues:
-        // 64x128 tiles measured 2-5% faster than 128x128 at 8192^3
-        const double eff = double(ci.tm * ci.tn) / double(ci.tm * ci.tn + ci.tm + ci.tn) *
-                           std::min(1.0, warps / need) * (conc >= 2 ? 1.03 : 1.0);
-        const double t = rounds * conc * double(ci.bm) * double(ci.bn) / eff;
+        const double eff = relative_efficiency(ci) * std::min(1.0, warps / need);
+        const double t = (full * conc + (rem > 0 ? 0.7 * conc : 0.0)) * double(ci.bm) * double(ci.bn) / eff;
         if (c == 0 || t < best_t * 0.999) { best_t = t; best = c; }
     }
     return best;
@@ -589,6 +599,15 @@ extern "C" int repops_gemm_config_info(int config, int *bm, int *bn, int *thread
     if (tm) *tm = ci.tm;
     if (tn) *tn = ci.tn;
     return REPOPS_OK;
+}
+
+extern "C" int repops_gemm_config_occupancy(int config) {
+    if (config < 0 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != REPOPS_OK) return rc;
+    if (di.device < 0 || di.device >= kMaxDevices) return REPOPS_ERR_UNSUPPORTED;
+    return occupancy_of(di.device, config);
 }
 
 extern "C" int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K) {
