@@ -27,6 +27,11 @@ What each function follows (page title, section):
                 synchronised threads), §4.3 (LayerNorm, GeLU, ERF): reductions in
                 a fixed 32-ary tree, exp by Cody-Waite reduction + Horner, erfc
                 by the Numerical Recipes §6.2 Chebyshev fit (see the C source).
+  silu, swiglu, swiglu_backward, rope_frequencies, rope_table, rope,
+  softmax_backward_causal, gemm_batched(k_lo, k_hi)
+             -- "Verde与RepOps" §4.3 (Llama-style training as the workload); the
+                pages fix none of these; the library's definitions are in the
+                C source, each step one IEEE rounding.
   replay     -- "Zoo Per-LLM Chain Soundness" §7 "Reproducibility test plan":
                 replay each block's batch in order, then check H(theta) = m.
 Pins against things other than the oracle itself live in tests/test_oracle_*.py.
@@ -119,7 +124,21 @@ def lib():
         L.oracle_softmax_backward.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64]
         L.oracle_gemm_batched.restype = None
         L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
-                                          vp, i64, i64, f32, vp, i32, vp, i64, i64]
+                                          vp, i64, i64, f32, vp, i32, vp, i64, i64, i64, i64]
+        L.oracle_softmax_backward_causal.restype = None
+        L.oracle_softmax_backward_causal.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64, i64, i64]
+        L.oracle_silu.restype = f32
+        L.oracle_silu.argtypes = [f32]
+        L.oracle_swiglu.restype = None
+        L.oracle_swiglu.argtypes = [i64, vp, vp, vp]
+        L.oracle_swiglu_backward.restype = None
+        L.oracle_swiglu_backward.argtypes = [i64, vp, vp, vp, vp, vp]
+        L.oracle_rope_frequencies.restype = None
+        L.oracle_rope_frequencies.argtypes = [i64, f32, vp]
+        L.oracle_rope_table.restype = None
+        L.oracle_rope_table.argtypes = [i64, i64, vp, vp, vp]
+        L.oracle_rope.restype = None
+        L.oracle_rope.argtypes = [i64, i64, i64, vp, i64, vp, vp, i64, i64, i32]
         if L.oracle_fp_env_ok() != 1:
             raise RuntimeError("host floating-point environment flushes subnormals "
                                "or does not round to nearest even; the oracle "
@@ -371,10 +390,12 @@ ACT_NONE, ACT_GELU = 0, 1
 
 
 def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, strideB,
-                 C, ldc, strideC, alpha=1.0, bias=None, act=ACT_NONE, R=None, ldr=0, strideR=0):
+                 C, ldc, strideC, alpha=1.0, bias=None, act=ACT_NONE, R=None, ldr=0, strideR=0,
+                 k_lo=-1, k_hi=-1):
     """Batched GEMM with the fused epilogue, on flat float32 buffers (element
     offsets and strides exactly as the library's batched entry point takes
-    them).  C is written in place; R may be C itself."""
+    them).  C is written in place; R may be C itself.  k_lo / k_hi >= 0
+    restrict row i's k-chain to [i - k_lo, i + k_hi] (see the C source)."""
     L = lib()
     for X in (A, B, C) + tuple(x for x in (bias, R) if x is not None):
         if X.dtype != np.float32 or not X.flags.c_contiguous:
@@ -382,7 +403,7 @@ def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, stride
     L.oracle_gemm_batched(int(bool(transA)), int(bool(transB)), batch, M, N, K,
                           _ptr(A), lda, strideA, _ptr(B), ldb, strideB, _ptr(C), ldc, strideC,
                           float(alpha), _ptr(bias) if bias is not None else None, int(act),
-                          _ptr(R) if R is not None else None, ldr, strideR)
+                          _ptr(R) if R is not None else None, ldr, strideR, int(k_lo), int(k_hi))
     return C
 
 
@@ -499,3 +520,66 @@ def softmax_backward(p, dp) -> np.ndarray:
     r, c = a.shape
     lib().oracle_softmax_backward(r, c, _ptr(a), c, _ptr(d), c, _ptr(out), c)
     return out
+
+
+def softmax_backward_causal(p, dp, first: int, period: int = None) -> np.ndarray:
+    """Row i: the softmax backward over its first min(cols, first + (i mod
+    period) + 1) entries, +0 after (period defaults to the row count)."""
+    a = np.ascontiguousarray(p, dtype=np.float32)
+    d = np.ascontiguousarray(dp, dtype=np.float32)
+    out = np.empty_like(a)
+    r, c = a.shape
+    if r and c:
+        lib().oracle_softmax_backward_causal(r, c, _ptr(a), c, _ptr(d), c, _ptr(out), c, first, period or r)
+    return out
+
+
+def silu(x: float) -> float:
+    return float(lib().oracle_silu(ctypes.c_float(x)))
+
+
+def swiglu(g, u) -> np.ndarray:
+    """SiLU(g) * u element by element."""
+    a = np.ascontiguousarray(g, dtype=np.float32)
+    b = np.ascontiguousarray(u, dtype=np.float32)
+    out = np.empty_like(a)
+    lib().oracle_swiglu(a.size, _ptr(a), _ptr(b), _ptr(out))
+    return out
+
+
+def swiglu_backward(g, u, dh):
+    """(dg, du) of h = SiLU(g) * u given dh."""
+    a = np.ascontiguousarray(g, dtype=np.float32)
+    b = np.ascontiguousarray(u, dtype=np.float32)
+    d = np.ascontiguousarray(dh, dtype=np.float32)
+    dg, du = np.empty_like(a), np.empty_like(a)
+    lib().oracle_swiglu_backward(a.size, _ptr(a), _ptr(b), _ptr(d), _ptr(dg), _ptr(du))
+    return dg, du
+
+
+def rope_frequencies(pairs: int, ln_base: float) -> np.ndarray:
+    out = np.empty(pairs, np.float32)
+    lib().oracle_rope_frequencies(pairs, ctypes.c_float(ln_base), _ptr(out))
+    return out
+
+
+def rope_table(positions: int, freq):
+    """(cos, sin), each positions x pairs, of angle p * freq[i]."""
+    f = np.ascontiguousarray(freq, dtype=np.float32)
+    c = np.empty((positions, f.size), np.float32)
+    s = np.empty((positions, f.size), np.float32)
+    lib().oracle_rope_table(positions, f.size, _ptr(f), _ptr(c), _ptr(s))
+    return c, s
+
+
+def rope(x, heads: int, cos, sin, first: int = 0, period: int = None, inverse: bool = False) -> np.ndarray:
+    """Returns x (rows x heads*d_head, at least) with every head's pairs
+    rotated to row r's position first + (r mod period)."""
+    a = np.array(x, dtype=np.float32, order="C", copy=True)
+    c = np.ascontiguousarray(cos, dtype=np.float32)
+    s = np.ascontiguousarray(sin, dtype=np.float32)
+    rows, cols = a.shape
+    if rows:
+        lib().oracle_rope(rows, heads, c.shape[1], _ptr(a), cols, _ptr(c), _ptr(s), first, period or rows,
+                          int(bool(inverse)))
+    return a

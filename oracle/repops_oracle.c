@@ -46,7 +46,7 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
-#include <math.h>   /* rintf, sqrtf: IEEE round-to-integral and correctly rounded square root */
+#include <math.h>   /* rintf, rint, sqrtf: IEEE round-to-integral and correctly rounded square root */
 
 /* ------------------------------------------------------------------------ */
 /* Floating-point environment                                                */
@@ -721,13 +721,20 @@ void oracle_rmsnorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx
  *   y    = y + R_b[i*ldr + j]           (when R is not NULL);
  *   C_b[i*ldc + j] = y.
  * Every step is one binary32 rounding.  R may be C itself (same ld and
- * stride): each element reads its residual before it is overwritten. */
+ * stride): each element reads its residual before it is overwritten.
+ *
+ * k window (the library's banded reading of a causal product): when
+ * k_lo >= 0 the k-chain of row i starts at k = max(0, i - k_lo); when
+ * k_hi >= 0 it ends at k = min(K - 1, i + k_hi); -1 leaves that side open.
+ * The chain still starts from +0 and runs with k increasing; a row whose
+ * window is empty gets the epilogue of +0. */
 void oracle_gemm_batched(int transA, int transB, int64_t batch, int64_t M, int64_t N, int64_t K,
                          const float *A, int64_t lda, int64_t strideA,
                          const float *B, int64_t ldb, int64_t strideB,
                          float *C, int64_t ldc, int64_t strideC,
                          float alpha, const float *bias, int act,
-                         const float *R, int64_t ldr, int64_t strideR)
+                         const float *R, int64_t ldr, int64_t strideR,
+                         int64_t k_lo, int64_t k_hi)
 {
     for (int64_t b = 0; b < batch; ++b) {
         const float *Ab = A + b * strideA;
@@ -735,9 +742,12 @@ void oracle_gemm_batched(int transA, int transB, int64_t batch, int64_t M, int64
         float *Cb = C + b * strideC;
         const float *Rb = R ? R + b * strideR : NULL;
         for (int64_t i = 0; i < M; ++i) {
+            int64_t k0 = 0, k1 = K;                   /* the chain covers [k0, k1) */
+            if (k_lo >= 0 && i - k_lo > k0) k0 = i - k_lo;
+            if (k_hi >= 0 && i + k_hi + 1 < k1) k1 = i + k_hi + 1;
             for (int64_t j = 0; j < N; ++j) {
                 float acc = 0.0f;
-                for (int64_t kk = 0; kk < K; ++kk) {
+                for (int64_t kk = k0; kk < k1; ++kk) {
                     float a = transA ? Ab[kk * lda + i] : Ab[i * lda + kk];
                     float bv = transB ? Bb[j * ldb + kk] : Bb[kk * ldb + j];
                     float p = a * bv;
@@ -1003,4 +1013,174 @@ void oracle_softmax_backward(int64_t rows, int64_t cols, const float *p, int64_t
         for (int64_t j = 0; j < cols; ++j) ds[i * ldds + j] = p[i * ldp + j] * (dp[i * lddp + j] - s);
     }
     free(v);
+}
+
+/* Causal softmax backward: row i is the backward of the causal softmax's
+ * prefix, L_i = min(cols, first + (i mod period) + 1) as in
+ * oracle_softmax_rows_causal: s = tree sum over j < L_i of dp_j * p_j (the
+ * tree of L_i values), ds_j = p_j * (dp_j - s) for j < L_i and +0 for
+ * j >= L_i; nothing beyond the prefix is read. */
+void oracle_softmax_backward_causal(int64_t rows, int64_t cols, const float *p, int64_t ldp, const float *dp,
+                                    int64_t lddp, float *ds, int64_t ldds, int64_t first, int64_t period)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        int64_t seen = first + (i % period) + 1;
+        if (seen > cols) seen = cols;
+        oracle_softmax_backward(1, seen, p + i * ldp, ldp, dp + i * lddp, lddp, ds + i * ldds, ldds);
+        for (int64_t j = seen; j < cols; ++j) ds[i * ldds + j] = 0.0f;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* SiLU-gated MLP (SwiGLU) and rotary position embeddings  [RepOps §4.3:    */
+/* Llama-style training is the measured workload; the pages fix neither     */
+/* operator.  The library's definitions, every step one IEEE rounding.]    */
+/* ------------------------------------------------------------------------ */
+
+/* sigma(x) = 1 / (1 + exp(-x)): one correctly rounded division of 1 by
+ * (1 + e); exp as oracle_exp (+inf for large -x gives sigma = +0). */
+static float sigmoid_fixed(float x)
+{
+    float e = oracle_exp(-x);
+    float den = 1.0f + e;
+    return 1.0f / den;
+}
+
+/* SiLU(x) = x * sigma(x). */
+float oracle_silu(float x)
+{
+    float sg = sigmoid_fixed(x);
+    return x * sg;
+}
+
+/* h = SiLU(g) * u, element by element (the gated MLP's hidden activation). */
+void oracle_swiglu(int64_t n, const float *g, const float *u, float *h)
+{
+    for (int64_t i = 0; i < n; ++i) h[i] = oracle_silu(g[i]) * u[i];
+}
+
+/* Backward of h = SiLU(g) * u given dh:
+ *   du = dh * SiLU(g);
+ *   dg = (dh * u) * SiLU'(g),  SiLU'(g) = sigma * (1 + g * (1 - sigma)). */
+void oracle_swiglu_backward(int64_t n, const float *g, const float *u, const float *dh, float *dg, float *du)
+{
+    for (int64_t i = 0; i < n; ++i) {
+        float sg = sigmoid_fixed(g[i]);
+        float a = g[i] * sg;
+        float up = u[i];
+        float dhi = dh[i];
+        du[i] = dhi * a;
+        float t = dhi * up;
+        float one_minus = 1.0f - sg;
+        float gq = g[i] * one_minus;
+        float w = 1.0f + gq;
+        float dsilu = sg * w;
+        dg[i] = t * dsilu;
+    }
+}
+
+/* Rotary frequencies: f_i = exp(-((i / pairs) * ln_base)), i = 0 .. pairs-1
+ * (base^(-2i/d_head) with pairs = d_head / 2; ln_base is the binary32 value
+ * of ln(base) the caller passes).  Each operation one binary32 rounding. */
+void oracle_rope_frequencies(int64_t pairs, float ln_base, float *freq)
+{
+    for (int64_t i = 0; i < pairs; ++i) {
+        float frac = (float)i / (float)pairs;
+        float x = frac * ln_base;
+        freq[i] = oracle_exp(-x);
+    }
+}
+
+/* cos and sin of a = pos * f, in binary64 with every operation rounded (no
+ * FMA), then each rounded once to binary32.  pos * f is exact in binary64
+ * (pos < 2^24).  Cody-Waite reduction a = k * (pi/2) + r with pi/2 split in
+ * three binary64 parts, the first two of 29 significant bits so that k * part
+ * is exact for k < 2^24; Taylor series of sin (to r^15) and cos (to r^16) on
+ * |r| <= pi/4 by Horner's rule in z = r^2; the quadrant k mod 4 picks signs
+ * and swaps. */
+static const double RP_PIO2_1 = 0x1.921fb54p+0;            /* pi/2, leading 29 bits */
+static const double RP_PIO2_2 = 0x1.10b4611p-30;           /* next 29 bits */
+static const double RP_PIO2_3 = 0x1.4c4c6628b80dcp-59;     /* pi/2 - the two above, rounded */
+static const double RP_2_OVER_PI = 0x1.45f306dc9c883p-1;  /* 2/pi, rounded */
+
+static void rope_sincos(int64_t pos, float f, float *c_out, float *s_out)
+{
+    double a = (double)pos * (double)f;
+    double k = rint(a * RP_2_OVER_PI);
+    double r = a - k * RP_PIO2_1;
+    r = r - k * RP_PIO2_2;
+    r = r - k * RP_PIO2_3;
+    double z = r * r;
+    /* sin r = r + (r z) * q_s;  q_s = -1/3! + z/5! - z^2/7! + ... - z^6/15! */
+    double qs = -0x1.ae7f3e733b81fp-41;                   /* -1/15! */
+    qs = qs * z + 0x1.6124613a86d09p-33;                 /* 1/13! */
+    qs = qs * z + -0x1.ae64567f544e4p-26;                /* -1/11! */
+    qs = qs * z + 0x1.71de3a556c734p-19;                 /* 1/9! */
+    qs = qs * z + -0x1.a01a01a01a01ap-13;                /* -1/7! */
+    qs = qs * z + 0x1.1111111111111p-7;                  /* 1/5! */
+    qs = qs * z + -0x1.5555555555555p-3;                 /* -1/3! */
+    double rz = r * z;
+    double sr = r + rz * qs;
+    /* cos r = 1 + z * q_c;  q_c = -1/2! + z/4! - z^2/6! + ... + z^7/16! */
+    double qc = 0x1.ae7f3e733b81fp-45;                    /* 1/16! */
+    qc = qc * z + -0x1.93974a8c07c9dp-37;                /* -1/14! */
+    qc = qc * z + 0x1.1eed8eff8d898p-29;                 /* 1/12! */
+    qc = qc * z + -0x1.27e4fb7789f5cp-22;                /* -1/10! */
+    qc = qc * z + 0x1.a01a01a01a01ap-16;                 /* 1/8! */
+    qc = qc * z + -0x1.6c16c16c16c17p-10;                /* -1/6! */
+    qc = qc * z + 0x1.5555555555555p-5;                  /* 1/4! */
+    qc = qc * z + -0.5;                                  /* -1/2! */
+    double cr = 1.0 + z * qc;
+    long long q = (long long)k & 3;
+    double sv, cv;
+    if (q == 0)      { sv = sr;  cv = cr; }
+    else if (q == 1) { sv = cr;  cv = -sr; }
+    else if (q == 2) { sv = -sr; cv = -cr; }
+    else             { sv = -cr; cv = sr; }
+    *c_out = (float)cv;
+    *s_out = (float)sv;
+}
+
+/* The rotation table: cos[p*pairs + i], sin[p*pairs + i] of angle p * f_i
+ * for positions p = 0 .. positions-1. */
+void oracle_rope_table(int64_t positions, int64_t pairs, const float *freq, float *cosv, float *sinv)
+{
+    for (int64_t p = 0; p < positions; ++p)
+        for (int64_t i = 0; i < pairs; ++i)
+            rope_sincos(p, freq[i], cosv + p * pairs + i, sinv + p * pairs + i);
+}
+
+/* Rotates, in place, pair i = (x[2i], x[2i+1]) of every head of every row:
+ * row r sits at position pos = first + (r mod period), c = cos[pos][i],
+ * s = sin[pos][i];
+ *   forward:  (x0 c - x1 s,  x0 s + x1 c)
+ *   inverse:  (x0 c + x1 s,  x1 c - x0 s)   (the transpose: the backward).
+ * Heads are d_head = 2 * pairs values each, head h at column h * d_head. */
+void oracle_rope(int64_t rows, int64_t heads, int64_t pairs, float *x, int64_t ldx, const float *cosv,
+                 const float *sinv, int64_t first, int64_t period, int inverse)
+{
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t pos = first + r % period;
+        for (int64_t h = 0; h < heads; ++h) {
+            float *v = x + r * ldx + h * 2 * pairs;
+            for (int64_t i = 0; i < pairs; ++i) {
+                float c = cosv[pos * pairs + i], sn = sinv[pos * pairs + i];
+                float x0 = v[2 * i], x1 = v[2 * i + 1];
+                float y0, y1;
+                if (!inverse) {
+                    float a = x0 * c, b = x1 * sn;
+                    y0 = a - b;
+                    float e = x0 * sn, f = x1 * c;
+                    y1 = e + f;
+                } else {
+                    float a = x0 * c, b = x1 * sn;
+                    y0 = a + b;
+                    float e = x1 * c, f = x0 * sn;
+                    y1 = e - f;
+                }
+                v[2 * i] = y0;
+                v[2 * i + 1] = y1;
+            }
+        }
+    }
 }

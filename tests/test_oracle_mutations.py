@@ -15,7 +15,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "repops_oracle.c")
 PINS = [os.path.join(ROOT, "tests", f) for f in
         ("test_oracle_gemm.py", "test_oracle_mean.py", "test_oracle_merkle.py", "test_oracle_rowops.py",
-         "test_oracle_epilogue.py", "test_oracle_halfstore.py", "test_oracle_backward.py")]
+         "test_oracle_epilogue.py", "test_oracle_halfstore.py", "test_oracle_backward.py",
+         "test_oracle_llama.py")]
 
 MUTATIONS = {
     "gemm: fused multiply-add": (
@@ -63,8 +64,8 @@ MUTATIONS = {
     "epilogue: bias before alpha": ("float y = alpha * acc;\n                if (bias) y = y + bias[j];",
                                     "float y = acc;\n                if (bias) y = y + bias[j];\n"
                                     "                y = alpha * y;"),
-    "batched: k in decreasing order": ("for (int64_t kk = 0; kk < K; ++kk) {",
-                                       "for (int64_t kk = K - 1; kk >= 0; --kk) {"),
+    "batched: k in decreasing order": ("for (int64_t kk = k0; kk < k1; ++kk) {",
+                                       "for (int64_t kk = k1 - 1; kk >= k0; --kk) {"),
     "batched: acc starts at -0": ("float acc = 0.0f;", "float acc = -0.0f;"),
     "batched: fused multiply-add": ("float p = a * bv;\n                    acc = acc + p;",
                                     "acc = __builtin_fmaf(a, bv, acc);"),
@@ -93,6 +94,26 @@ MUTATIONS = {
     "softmax backward: s not subtracted": ("ds[i * ldds + j] = p[i * ldp + j] * (dp[i * lddp + j] - s);",
                                            "ds[i * ldds + j] = p[i * ldp + j] * dp[i * lddp + j];"),
     "batched: A advanced by B's stride": ("const float *Ab = A + b * strideA;", "const float *Ab = A + b * strideB;"),
+    "window: one k past the upper band": ("if (k_hi >= 0 && i + k_hi + 1 < k1) k1 = i + k_hi + 1;",
+                                          "if (k_hi >= 0 && i + k_hi + 2 < k1) k1 = i + k_hi + 2;"),
+    "window: lower band ignored": ("if (k_lo >= 0 && i - k_lo > k0) k0 = i - k_lo;", ""),
+    "causal softmax backward: one entry too many": ("int64_t seen = first + (i % period) + 1;",
+                                                    "int64_t seen = first + (i % period) + 2;"),
+    "causal softmax backward: masked entries -0": ("ds[i * ldds + j] = 0.0f;", "ds[i * ldds + j] = -0.0f;"),
+    "silu: sigma without the 1 +": ("float den = 1.0f + e;", "float den = e;"),
+    "silu: exp of +x": ("float e = oracle_exp(-x);", "float e = oracle_exp(x);"),
+    "swiglu backward: du from u": ("du[i] = dhi * a;", "du[i] = dhi * up;"),
+    "swiglu backward: 1 - sigma as sigma": ("float one_minus = 1.0f - sg;", "float one_minus = sg;"),
+    "rope frequencies: growing": ("freq[i] = oracle_exp(-x);", "freq[i] = oracle_exp(x);"),
+    "rope table: quadrant 1 swapped": ("else if (q == 1) { sv = cr;  cv = -sr; }",
+                                       "else if (q == 1) { sv = -cr; cv = sr; }"),
+    "rope table: one-part pi/2": ("    r = r - k * RP_PIO2_2;\n    r = r - k * RP_PIO2_3;\n", ""),
+    "rope table: cos series without z^2/4!": (
+        "    qc = qc * z + 0x1.5555555555555p-5;                  /* 1/4! */\n", ""),
+    "rope: sin term added": ("y0 = a - b;", "y0 = a + b;"),
+    "rope: position ignores first": ("int64_t pos = first + r % period;", "int64_t pos = r % period;"),
+    "rope inverse: forward formula": ("float e = x1 * c, f = x0 * sn;\n                    y1 = e - f;",
+                                      "float e = x0 * sn, f = x1 * c;\n                    y1 = e + f;"),
 }
 
 
