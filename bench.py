@@ -619,19 +619,24 @@ def run_sweep_rowops(dev, s, flush, hbm):
 
 
 def run_sweep_decoder(dev, s, flush, peak):
-    """One decoder layer forward (Llama-3.2-1B sizes: d 2048, 32 query and 8
-    key/value heads of 64, MLP 8192; GeLU MLP, no rotary embedding) over two
-    causal sequences of 2048 tokens, every step a library call: the fused
-    layer, the same layer with its epilogues as separate steps, and the
-    attention alone.  Synthetic N(0, 0.02) weights; L2 flushed before each
-    timed layer."""
+    """One decoder layer (Llama-3.2-1B sizes: d 2048, 32 query and 8 key/value
+    heads of 64, MLP 8192) over two causal sequences of 2048 tokens, every
+    step a library call.  The Llama layer (rotary embedding, SwiGLU MLP) and
+    the GeLU layer (no rotary): the fused forward, the forward with its
+    epilogues as separate steps, the training step (forward keeping the
+    activations, then the backward pass); and the attention alone.  FLOPs
+    count the causal band of the attention products.  Synthetic N(0, 0.02)
+    weights; L2 flushed before each timed layer."""
     from verifiable_repops_gemm_gb300 import decoder
-    cfg = decoder.DecoderConfig()
-    T = 2 * cfg.seq_len
-    w = decoder.init_weights(cfg, 300, dev)
-    x0 = inputs.normal((T, cfg.d), 1.0, 301, dev)
+    llama = decoder.DecoderConfig()
+    layers = (("llama layer (rotary, SwiGLU)", llama, ((True, False), (False, False))),
+              ("GeLU layer", decoder.DecoderConfig(mlp="gelu", rope_base=0.0),
+               ((True, False), (True, True), (False, False))))
+    T = 2 * llama.seq_len
+    x0 = inputs.normal((T, llama.d), 1.0, 301, dev)
     x = torch.empty_like(x0)
-    ws = decoder.workspace(cfg, T, dev)
+    dy0 = inputs.normal((T, llama.d), 1e-2, 302, dev)
+    dy = torch.empty_like(dy0)
 
     def timed(fn, reps=5):
         with torch.cuda.stream(s):
@@ -650,44 +655,48 @@ def run_sweep_decoder(dev, s, flush, peak):
         torch.cuda.synchronize(dev)
         return sum(a.elapsed_time(b) for a, b in evs) / reps
 
-    flops = cfg.flops(T)
-    for name, fused, ge in (("decoder layer forward, fused bias/residual epilogues, GeLU kernel", True, False),
-                            ("decoder layer forward, GeLU in the GEMM epilogue too", True, True),
-                            ("decoder layer forward, epilogues as separate steps", False, False)):
-        ms = timed(lambda: decoder.forward(x, w, cfg, fused=fused, gelu_epilogue=ge, work=ws))
-        print(json.dumps({"sweep": name, "tokens": T, "ms": ms, "tokens_per_s": T / ms * 1e3,
-                          "tflops": flops / ms / 1e9, "frac_of_fp32_peak": flops / ms / 1e9 / peak}),
-              flush=True)
-    attn_flops = 2 * 2.0 * (T // cfg.seq_len) * cfg.heads * cfg.seq_len ** 2 * cfg.d_head
-    ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"]))
-    print(json.dumps({"sweep": "causal grouped-query attention (batched QK^T, softmax, PV)", "tokens": T,
-                      "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
-    # a training step of the layer: forward keeping its activations, then the
-    # backward pass from an upstream gradient (every weight's gradient and dx);
-    # backward does two GEMMs for each forward one: 3x the forward FLOPs
-    saved = decoder.activations(cfg, T, dev)
-    bws = decoder.backward_workspace(cfg, T, dev)
-    dy0 = inputs.normal((T, cfg.d), 1e-2, 302, dev)
-    dy = torch.empty_like(dy0)
-    ms_f = timed(lambda: decoder.forward(x, w, cfg, work=ws, save=saved))
+    for label, cfg, variants in layers:
+        w = decoder.init_weights(cfg, 300, dev)
+        ws = decoder.workspace(cfg, T, dev)
+        flops = cfg.flops(T)
+        for fused, ge in variants:
+            what = ("fused residual/bias epilogues" if fused else "epilogues as separate steps") + \
+                   (", GeLU in the GEMM epilogue" if ge else "")
+            ms = timed(lambda: decoder.forward(x, w, cfg, fused=fused, gelu_epilogue=ge, work=ws))
+            print(json.dumps({"sweep": "%s forward, %s" % (label, what), "tokens": T, "ms": ms,
+                              "tokens_per_s": T / ms * 1e3, "tflops": flops / ms / 1e9,
+                              "frac_of_fp32_peak": flops / ms / 1e9 / peak}), flush=True)
+        if cfg is llama:
+            S = cfg.seq_len
+            attn_flops = 2 * 2.0 * (T // S) * cfg.heads * (S * (S + 1) / 2) * cfg.d_head
+            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"]))
+            print(json.dumps({"sweep": "causal grouped-query attention (batched QK^T, softmax, banded PV)",
+                              "tokens": T, "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
+        # the training step: forward keeping its activations, then the backward
+        # pass (every weight's gradient and dx): 3x the forward FLOPs
+        saved = decoder.activations(cfg, T, dev)
+        bws = decoder.backward_workspace(cfg, T, dev)
+        ms_f = timed(lambda: decoder.forward(x, w, cfg, work=ws, save=saved))
 
-    def step():
-        decoder.forward(x, w, cfg, work=ws, save=saved)
-        dy.copy_(dy0)
-        decoder.backward(dy, w, cfg, saved, work=bws)
-    ms = timed(step)
-    print(json.dumps({"sweep": "decoder layer training step (forward keeping activations + backward)",
-                      "tokens": T, "ms": ms, "forward_ms": ms_f, "tokens_per_s": T / ms * 1e3,
-                      "tflops": 3 * flops / ms / 1e9, "frac_of_fp32_peak": 3 * flops / ms / 1e9 / peak}),
-          flush=True)
+        def step():
+            decoder.forward(x, w, cfg, work=ws, save=saved)
+            dy.copy_(dy0)
+            decoder.backward(dy, w, cfg, saved, work=bws)
+        ms = timed(step)
+        print(json.dumps({"sweep": "%s training step (forward keeping activations + backward)" % label,
+                          "tokens": T, "ms": ms, "forward_ms": ms_f, "tokens_per_s": T / ms * 1e3,
+                          "tflops": 3 * flops / ms / 1e9, "frac_of_fp32_peak": 3 * flops / ms / 1e9 / peak}),
+              flush=True)
+        del saved, bws, ws, w
 
 
 def run_sweep_train(dev, s, flush, peak):
     """The verifiable training step end to end: 4 contributors (DIDs), each
-    with 2 x 2048 tokens through 2 Llama-3.2-1B-sized decoder layers, forward
-    and backward; their gradients folded in DID order into the mean, SGD on the
-    flat theta (88 M parameters) and the Merkle root of theta.  Synthetic
-    inputs and upstream gradients; the step is timed as a whole and by part."""
+    with 2 x 2048 tokens through 2 Llama-3.2-1B-sized decoder layers (rotary,
+    SwiGLU), forward and backward; their gradients folded in DID order into
+    the mean, SGD on the flat theta (122 M parameters) and the Merkle root of
+    theta.  Synthetic inputs and upstream gradients; the step is timed as a
+    whole and by part."""
     from verifiable_repops_gemm_gb300 import decoder, train
     cfg = decoder.DecoderConfig()
     T, layers, C = 2 * cfg.seq_len, 2, 4

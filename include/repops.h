@@ -222,10 +222,21 @@ int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
  * are neither computed nor written, tiles crossing it are computed in full --
  * and every element on or below it exact.  Pair with
  * repops_softmax_rows_causal_f32, which never reads them.
+ * k_lo, k_hi (the banded k-chain of causal attention's P V, dS K (k_hi) and
+ * P^T dO, dS^T Q (k_lo)): -1 leaves that side of the chain open; k_lo >= 0
+ * starts row i's chain at k = max(0, i - k_lo), k_hi >= 0 ends it at
+ * k = min(K-1, i + k_hi); the chain still starts from +0 with k increasing,
+ * and a row with an empty window gets the epilogue of +0.  The kernel runs
+ * each tile's rows over the union of their windows (whole 32-k slices); the
+ * extra terms of a row then add fl(+-0 * b) = +-0, which changes no bit
+ * provided A_b[i][k] is +-0 outside row i's window and B_b is finite on the
+ * k rows the tile reads -- as for a causal softmax output (+0 past each
+ * row's prefix) times finite values.  The caller guarantees that; otherwise
+ * the rows concerned are unspecified.
  * Errors: INVALID_ARG (negative size or stride, bad leading dim, null
- * pointer with a non-empty operand, act not NONE/GELU, causal_first < -1,
- * spans that overflow); ALIAS; UNSUPPORTED (batch > 65535, or loader TMA when
- * TMA cannot serve the operands); CUDA. */
+ * pointer with a non-empty operand, act not NONE/GELU, causal_first, k_lo or
+ * k_hi < -1, spans that overflow); ALIAS; UNSUPPORTED (batch > 65535, or
+ * loader TMA when TMA cannot serve the operands); CUDA. */
 int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
                             int64_t batch, int64_t M, int64_t N, int64_t K,
                             const float *A, int64_t lda, int64_t strideA,
@@ -233,7 +244,8 @@ int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
                             float *C, int64_t ldc, int64_t strideC,
                             float alpha, const float *bias, int act,
                             const float *R, int64_t ldr, int64_t strideR,
-                            int64_t causal_first, cudaStream_t stream);
+                            int64_t causal_first, int64_t k_lo, int64_t k_hi,
+                            cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Contributor order                                                         */
@@ -530,6 +542,17 @@ int repops_softmax_backward_f32(int64_t rows, int64_t cols, const float *p, int6
                                 const float *dp, int64_t lddp, float *ds, int64_t ldds,
                                 cudaStream_t stream);
 
+/* Backward of repops_softmax_rows_causal_f32 (first >= 0, period >= 1; else
+ * INVALID_ARG): row r covers its prefix of L = min(cols, first + (r mod
+ * period) + 1) entries -- s = tree sum(dp * p) over the L prefix values (the
+ * tree of L values), ds = p * (dp - s) there -- and ds = +0 past the prefix,
+ * where p and dp are never read (dp may hold anything there, e.g. the
+ * unspecified tiles of a causal repops_gemm_f32_batched).  Aliasing and sizes
+ * as repops_softmax_backward_f32. */
+int repops_softmax_backward_causal_f32(int64_t rows, int64_t cols, const float *p, int64_t ldp,
+                                       const float *dp, int64_t lddp, float *ds, int64_t ldds,
+                                       int64_t first, int64_t period, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Half-precision storage                                                    */
 /* "Verde与RepOps" §3.3 (IEEE-754 hardware needed; FP16 support limited) and */
@@ -583,6 +606,69 @@ int repops_gemm_typed(int config, int loader, int transA, int transB,
  * do not depend on how the kernel splits a row. */
 int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32_t *words, int64_t ldw,
                             int64_t window, uint64_t *out, int64_t ldo, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* SiLU-gated MLP (SwiGLU) and rotary position embeddings                     */
+/* "Verde与RepOps" §4.3 (Llama-style training is the measured workload).     */
+/* The pages fix neither operator; the library's definitions follow, every  */
+/* step one IEEE rounding in a fixed order (exp as in repops_gelu_f32).      */
+/* ------------------------------------------------------------------------ */
+
+/* h[i][j] = fl(SiLU(g[i][j]) * u[i][j]) over rows x cols:
+ *   sigma = fl(1 / fl(1 + exp(-g)))   (one correctly rounded division;
+ *                                      exp overflow gives sigma = +0)
+ *   SiLU  = fl(g * sigma).
+ * g, u, h (device) with their own row pitches (>= cols); h may be g or u
+ * itself (same pointer and pitch), any other overlap is ALIAS. */
+int repops_swiglu_f32(int64_t rows, int64_t cols, const float *g, int64_t ldg,
+                      const float *u, int64_t ldu, float *h, int64_t ldh, cudaStream_t stream);
+
+/* Backward of repops_swiglu_f32 given dh, element by element (sigma recomputed
+ * as in the forward):
+ *   du = fl(dh * SiLU(g))
+ *   dg = fl(fl(dh * u) * fl(sigma * fl(1 + fl(g * fl(1 - sigma)))))
+ * dg may be g or dh, du may be u or dh (same pointer and pitch); dg and du
+ * must not overlap each other, nor any input otherwise (ALIAS). */
+int repops_swiglu_backward_f32(int64_t rows, int64_t cols, const float *g, int64_t ldg,
+                               const float *u, int64_t ldu, const float *dh, int64_t lddh,
+                               float *dg, int64_t lddg, float *du, int64_t lddu,
+                               cudaStream_t stream);
+
+/* Rotary frequencies f_i = exp(-fl(fl(i / pairs) * ln_base)), i < pairs
+ * (base^(-2i/d_head) with pairs = d_head/2; ln_base is the caller's binary32
+ * value of ln(base), which fixes the bits).  freq: device, pairs floats.
+ * INVALID_ARG for pairs < 1 or a null pointer. */
+int repops_rope_frequencies_f32(int64_t pairs, float ln_base, float *freq, cudaStream_t stream);
+
+/* The rotation table for positions p < positions and pairs i < pairs:
+ * cos[p*pairs + i], sin[p*pairs + i] of a = p * freq[i], computed in binary64
+ * (every operation rounded, no FMA) and rounded once to binary32:
+ *   a exact (p < 2^24 and a binary32 freq); k = rint(a * fl64(2/pi));
+ *   r = ((a - k*P1) - k*P2) - k*P3 with pi/2 = P1 + P2 + P3, P1 and P2 of 29
+ *   significant bits (k*P1, k*P2 exact for |k| < 2^24);
+ *   sin r = r + (r*z) * S(z), cos r = 1 + z * C(z), z = r*r, S and C the
+ *   Taylor series to r^15 and r^16 by Horner's rule; quadrant k mod 4.
+ * For |a| < 2^24 the binary64 value is accurate to about 2^-50 relative, so
+ * each result is the correctly rounded binary32 value unless the exact one
+ * lies that close to a rounding boundary.  positions in [1, 2^24],
+ * pairs >= 1; freq, cos, sin
+ * device buffers that must not overlap (ALIAS); else INVALID_ARG. */
+int repops_rope_table_f32(int64_t positions, int64_t pairs, const float *freq, float *cos_out,
+                          float *sin_out, cudaStream_t stream);
+
+/* Rotates in place pair i = (x0, x1) = (x[r][h*2*pairs + 2i], ... + 1) of head
+ * h < heads of row r < rows, at position pos = first + (r mod period) with
+ * c = cos[pos*pairs + i], s = sin[pos*pairs + i] (a repops_rope_table_f32
+ * table of `positions` rows):
+ *   inverse == 0:  (fl(fl(x0*c) - fl(x1*s)),  fl(fl(x0*s) + fl(x1*c)))
+ *   inverse != 0:  (fl(fl(x0*c) + fl(x1*s)),  fl(fl(x1*c) - fl(x0*s)))
+ * The inverse is the transpose: the backward of the rotation.  Columns past
+ * heads*2*pairs are not touched.  x: device, row pitch ldx >= heads*2*pairs;
+ * every position reached must be < positions; first >= 0, period >= 1
+ * (INVALID_ARG otherwise); x must not overlap the table (ALIAS). */
+int repops_rope_f32(int64_t rows, int64_t heads, int64_t pairs, float *x, int64_t ldx,
+                    const float *cos_tab, const float *sin_tab, int64_t positions, int64_t first,
+                    int64_t period, int inverse, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -215,9 +215,10 @@ def test_row_operators_reject_bad_arguments(L):
 
 def _bat(L, batch=2, M=4, N=4, K=4, A=FAKE_A, lda=4, sA=16, B=FAKE_B, ldb=4, sB=16, C=FAKE_C, ldc=4,
          sC=16, alpha=1.0, bias=None, act=0, R=None, ldr=4, sR=16, config=-1, loader=0, tA=0, tB=0,
-         causal=-1):
+         causal=-1, k_lo=-1, k_hi=-1):
     return L.repops_gemm_f32_batched(config, loader, tA, tB, batch, M, N, K, A, lda, sA, B, ldb, sB,
-                                     C, ldc, sC, ctypes.c_float(alpha), bias, act, R, ldr, sR, causal, None)
+                                     C, ldc, sC, ctypes.c_float(alpha), bias, act, R, ldr, sR, causal, k_lo, k_hi,
+                                     None)
 
 
 def test_batched_gemm_rejects_bad_arguments(L):
@@ -225,6 +226,7 @@ def test_batched_gemm_rejects_bad_arguments(L):
     assert _bat(L, sA=-4) == -1                                    # negative stride
     assert _bat(L, act=2) == -1                                    # unknown activation
     assert _bat(L, causal=-2) == -1
+    assert _bat(L, k_lo=-2) == -1 and _bat(L, k_hi=-5) == -1                 # k window bounds
     assert _bat(L, ldc=3) == -1
     assert _bat(L, R=FAKE_B + 4096, ldr=3) == -1                   # residual ld < N
     assert _bat(L, config=99) == -1
@@ -306,3 +308,37 @@ def test_host_buffer_gemm_rejects_bad_arguments(L):
     assert g(4, 4, 4, None, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
     assert g(4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 16, 4, None) == -2
     assert g(0, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == 0
+
+
+def test_llama_operators_reject_bad_arguments(L):
+    f = ctypes.c_float
+    sbc = L.repops_softmax_backward_causal_f32
+    assert sbc(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, -1, 4, None) == -1        # first < 0
+    assert sbc(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, 0, 0, None) == -1         # period < 1
+    assert sbc(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 4, 4, 0, 4, None) == -2     # ds overlaps p
+    sw = L.repops_swiglu_f32
+    assert sw(-1, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert sw(4, 4, FAKE_A, 3, FAKE_B, 4, FAKE_C, 4, None) == -1                # ldg < cols
+    assert sw(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 4, 4, None) == -2            # h overlaps g, not in place
+    assert sw(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A, 8, None) == -2                # same start, other pitch
+    assert sw(0, 4, None, 4, None, 4, None, 4, None) == 0
+    sb = L.repops_swiglu_backward_f32
+    assert sb(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, FAKE_A, 4, FAKE_A + 8, 4, None) == -2   # dg, du overlap
+    assert sb(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, FAKE_B, 4, FAKE_C + 4096, 4, None) == -2  # dg on u
+    assert sb(4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, FAKE_C + 4096, 4, FAKE_A, 4, None) == -2  # du on g
+    assert sb(4, 4, FAKE_A, 4, FAKE_B, 4, None, 4, FAKE_C, 4, FAKE_C + 4096, 4, None) == -1
+    assert L.repops_rope_frequencies_f32(0, f(13.0), FAKE_A, None) == -1
+    assert L.repops_rope_frequencies_f32(4, f(13.0), None, None) == -1
+    rt = L.repops_rope_table_f32
+    assert rt(0, 4, FAKE_A, FAKE_B, FAKE_C, None) == -1
+    assert rt((1 << 24) + 1, 4, FAKE_A, FAKE_B, FAKE_C, None) == -1
+    assert rt(16, 4, FAKE_A, FAKE_B, FAKE_B + 16, None) == -2                   # cos and sin overlap
+    assert rt(16, 4, FAKE_A, FAKE_A + 4, FAKE_C, None) == -2                    # cos over freq
+    rp = L.repops_rope_f32
+    assert rp(4, 2, 0, FAKE_A, 8, FAKE_B, FAKE_C, 16, 0, 4, 0, None) == -1      # pairs < 1
+    assert rp(4, 2, 2, FAKE_A, 7, FAKE_B, FAKE_C, 16, 0, 4, 0, None) == -1      # ldx < heads * 2 * pairs
+    assert rp(4, 2, 2, FAKE_A, 8, FAKE_B, FAKE_C, 16, 13, 4, 0, None) == -1     # position 16 past the table
+    assert rp(40, 2, 2, FAKE_B - 64, 8, FAKE_B, FAKE_C, 16, 12, 4, 0, None) == -2  # positions 12..15 fit; x runs into cos
+    assert rp(4, 2, 2, FAKE_A, 8, FAKE_B, FAKE_C, 16, 0, 0, 0, None) == -1      # period < 1
+    assert rp(4, 2, 2, FAKE_B + 8, 8, FAKE_B, FAKE_C, 16, 0, 4, 0, None) == -2  # x overlaps cos
+    assert rp(0, 2, 2, None, 8, None, None, 16, 0, 4, 0, None) == 0

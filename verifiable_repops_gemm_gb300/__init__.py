@@ -26,6 +26,9 @@ memory and streams.
   rolling_hash(words, window)       Rabin-Karp hashes of uint32 batch rows (ZKDV)
   colsum / gelu_backward /          backward operators of a training step
   rmsnorm_backward / softmax_backward
+  swiglu / swiglu_backward /        SiLU-gated MLP activation and rotary
+  rope_frequencies / rope_table /   position embeddings of a Llama-style layer
+  rope                              ("Verde与RepOps" §4.3)
 """
 import ctypes
 
@@ -39,6 +42,7 @@ __all__ = ["load", "version", "gemm", "gemm_host", "gemm_config_count", "gemm_co
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
            "convert", "gemm_typed", "rolling_hash", "TYPE_F32", "TYPE_F16", "TYPE_BF16",
            "colsum", "gelu_backward", "rmsnorm_backward", "softmax_backward",
+           "swiglu", "swiglu_backward", "rope_frequencies", "rope_table", "rope",
            "device_status", "RepopsError", "ACT_NONE", "ACT_GELU",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
 
@@ -119,8 +123,8 @@ def _batched_operand(X, name):
 
 
 def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = ACT_NONE,
-                 residual=None, causal_first: int = -1, config: int = -1, loader: int = LOADER_AUTO,
-                 stream=None):
+                 residual=None, causal_first: int = -1, k_lo: int = -1, k_hi: int = -1, config: int = -1,
+                 loader: int = LOADER_AUTO, stream=None):
     """out[b] = epilogue(A[b] @ B[b]) with the order-fixed k-chain, then
     y = alpha*acc, + bias[j], GeLU (act=ACT_GELU), + residual[b][i][j], each one
     binary32 rounding (repops_gemm_f32_batched).
@@ -131,7 +135,9 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
     N) or (M, N), unit column stride, batches stacked or interleaved.
     residual: shaped like out; may be out itself.  bias: (N,) contiguous.
     causal_first >= 0: elements with j > causal_first + i are left unspecified
-    (whole tiles above that boundary are skipped)."""
+    (whole tiles above that boundary are skipped).  k_lo / k_hi >= 0: row i's
+    k-chain covers [i - k_lo, i + k_hi] only (A must be +-0 outside that band
+    and B finite: see repops_gemm_f32_batched)."""
     import torch
     L = load()
     pa, lda, sa, ta, ba = _batched_operand(A, "A")
@@ -169,7 +175,7 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
         pbias = bias.data_ptr()
     rc = L.repops_gemm_f32_batched(config, loader, ta, tb, nb, M, N, K, pa, lda, sa, pb, ldb, sb,
                                    out.data_ptr(), ldc, sc, ctypes.c_float(alpha), pbias, int(act),
-                                   pr, ldr, sr, int(causal_first), _stream_handle(stream))
+                                   pr, ldr, sr, int(causal_first), int(k_lo), int(k_hi), _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32_batched")
     return out
 
@@ -589,15 +595,98 @@ def rmsnorm_backward(x, gamma, eps, dy, dx=None, dyxh=None, *, res=None, stream=
     return dx, dyxh
 
 
-def softmax_backward(p, dp, out=None, *, stream=None):
-    """p * (dp - rowsum(dp * p)) (repops_softmax_backward_f32); out may be dp."""
+def softmax_backward(p, dp, out=None, *, causal_first=None, causal_period=None, stream=None):
+    """p * (dp - rowsum(dp * p)) (repops_softmax_backward_f32); out may be dp.
+    causal_first / causal_period: the backward of softmax_rows with the same
+    arguments -- row i covers its prefix only, +0 after, and never reads dp
+    past it (repops_softmax_backward_causal_f32)."""
     pp, ldp = _row_operand(p, "p")
     pg, ldg = _row_operand(dp, "dp")
     out = _row_out(p, out)
     po, ldo = _row_operand(out, "out")
     if tuple(dp.shape) != tuple(p.shape):
         raise ValueError("p and dp differ in shape")
-    rc = load().repops_softmax_backward_f32(p.shape[0], p.shape[1], pp, ldp, pg, ldg, po, ldo,
-                                            _stream_handle(stream))
-    _capi.check(rc, "repops_softmax_backward_f32")
+    if causal_first is None:
+        rc = load().repops_softmax_backward_f32(p.shape[0], p.shape[1], pp, ldp, pg, ldg, po, ldo,
+                                                _stream_handle(stream))
+        _capi.check(rc, "repops_softmax_backward_f32")
+    else:
+        period = int(causal_period) if causal_period is not None else max(p.shape[0], 1)
+        rc = load().repops_softmax_backward_causal_f32(p.shape[0], p.shape[1], pp, ldp, pg, ldg, po, ldo,
+                                                       int(causal_first), period, _stream_handle(stream))
+        _capi.check(rc, "repops_softmax_backward_causal_f32")
     return out
+
+
+def swiglu(g, u, out=None, *, stream=None):
+    """SiLU(g) * u element by element (repops_swiglu_f32); g, u and out are
+    2-D float32 CUDA tensors of one shape with unit column stride (column
+    blocks of a wider matrix are fine); out may be g or u."""
+    pg, ldg = _row_operand(g, "g")
+    pu, ldu = _row_operand(u, "u")
+    out = _row_out(g, out)
+    ph, ldh = _row_operand(out, "out")
+    if tuple(u.shape) != tuple(g.shape):
+        raise ValueError("g and u differ in shape")
+    rc = load().repops_swiglu_f32(g.shape[0], g.shape[1], pg, ldg, pu, ldu, ph, ldh, _stream_handle(stream))
+    _capi.check(rc, "repops_swiglu_f32")
+    return out
+
+
+def swiglu_backward(g, u, dh, dg=None, du=None, *, stream=None):
+    """(dg, du) of h = SiLU(g) * u given dh (repops_swiglu_backward_f32); dg
+    may be g or dh, du may be u or dh."""
+    pg, ldg = _row_operand(g, "g")
+    pu, ldu = _row_operand(u, "u")
+    pd, ldd = _row_operand(dh, "dh")
+    dg = _row_out(g, dg)
+    du = _row_out(g, du)
+    pdg, lddg = _row_operand(dg, "dg")
+    pdu, lddu = _row_operand(du, "du")
+    if tuple(u.shape) != tuple(g.shape) or tuple(dh.shape) != tuple(g.shape):
+        raise ValueError("g, u and dh differ in shape")
+    rc = load().repops_swiglu_backward_f32(g.shape[0], g.shape[1], pg, ldg, pu, ldu, pd, ldd, pdg, lddg, pdu, lddu,
+                                           _stream_handle(stream))
+    _capi.check(rc, "repops_swiglu_backward_f32")
+    return dg, du
+
+
+def rope_frequencies(pairs: int, ln_base: float, device="cuda", *, stream=None):
+    """f_i = exp(-((i / pairs) * ln_base)), i < pairs, with ln_base rounded to
+    binary32 (repops_rope_frequencies_f32)."""
+    import torch
+    out = torch.empty(pairs, dtype=torch.float32, device=device)
+    rc = load().repops_rope_frequencies_f32(pairs, ctypes.c_float(ln_base), out.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_rope_frequencies_f32")
+    return out
+
+
+def rope_table(positions: int, freq, *, stream=None):
+    """(cos, sin), each positions x pairs, of the angles p * freq[i]
+    (repops_rope_table_f32)."""
+    import torch
+    if freq.dtype != torch.float32 or not freq.is_cuda or not freq.is_contiguous() or freq.dim() != 1:
+        raise ValueError("freq must be a contiguous float32 CUDA vector")
+    c = torch.empty(positions, freq.numel(), dtype=torch.float32, device=freq.device)
+    s = torch.empty_like(c)
+    rc = load().repops_rope_table_f32(positions, freq.numel(), freq.data_ptr(), c.data_ptr(), s.data_ptr(),
+                                      _stream_handle(stream))
+    _capi.check(rc, "repops_rope_table_f32")
+    return c, s
+
+
+def rope(x, heads: int, cos, sin, *, first: int = 0, period: int = None, inverse: bool = False, stream=None):
+    """Rotates, in place, the adjacent pairs of the first `heads` heads of
+    every row of x (2-D float32 CUDA, unit column stride; head width 2 *
+    cos.shape[1]) to position first + (row mod period) (repops_rope_f32);
+    inverse=True applies the transpose (the backward).  Returns x."""
+    px, ldx = _row_operand(x, "x")
+    for t, n in ((cos, "cos"), (sin, "sin")):
+        if not t.is_contiguous() or t.dim() != 2 or t.shape != cos.shape:
+            raise ValueError("%s must be a contiguous positions x pairs table" % n)
+    positions, pairs = cos.shape
+    per = int(period) if period is not None else max(x.shape[0], 1)
+    rc = load().repops_rope_f32(x.shape[0], heads, pairs, px, ldx, cos.data_ptr(), sin.data_ptr(), positions,
+                                int(first), per, int(bool(inverse)), _stream_handle(stream))
+    _capi.check(rc, "repops_rope_f32")
+    return x

@@ -329,9 +329,9 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
                           int64_t K, const float *A, int64_t lda, int64_t strideA, const float *B, int64_t ldb,
                           int64_t strideB, float *C, int64_t ldc, int64_t strideC, float alpha,
                           const float *bias, int act, const float *R, int64_t ldr, int64_t strideR,
-                          int64_t causal_first, cudaStream_t stream) {
+                          int64_t causal_first, int64_t k_lo, int64_t k_hi, cudaStream_t stream) {
     if (batch < 0 || M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
-    if (causal_first < -1) return REPOPS_ERR_INVALID_ARG;
+    if (causal_first < -1 || k_lo < -1 || k_hi < -1) return REPOPS_ERR_INVALID_ARG;
     if (strideA < 0 || strideB < 0 || strideC < 0 || strideR < 0) return REPOPS_ERR_INVALID_ARG;
     if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
     if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC)
@@ -387,6 +387,9 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     p.ldr = ldr;
     p.strideR = batch > 1 ? strideR : 0;
     p.causal = causal_first < N ? causal_first : -1;   // from N on, no tile lies above the boundary
+    // a bound that no row reaches leaves that side open
+    p.k_lo = k_lo >= 0 && k_lo < M - 1 ? k_lo : -1;
+    p.k_hi = k_hi >= 0 && k_hi < K - 1 ? k_hi : -1;
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
 
@@ -478,10 +481,11 @@ extern "C" int repops_gemm_f32_batched(int config, int loader, int transA, int t
                                        int64_t strideA, const float *B, int64_t ldb, int64_t strideB,
                                        float *C, int64_t ldc, int64_t strideC, float alpha,
                                        const float *bias, int act, const float *R, int64_t ldr,
-                                       int64_t strideR, int64_t causal_first, cudaStream_t stream) {
+                                       int64_t strideR, int64_t causal_first, int64_t k_lo, int64_t k_hi,
+                                       cudaStream_t stream) {
     return gemm_dispatch_batched(config, loader, transA, transB, batch, M, N, K, A, lda, strideA, B, ldb,
                                  strideB, C, ldc, strideC, alpha, bias, act, R, ldr, strideR, causal_first,
-                                 stream);
+                                 k_lo, k_hi, stream);
 }
 
 namespace {

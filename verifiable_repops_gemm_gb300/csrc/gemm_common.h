@@ -29,6 +29,8 @@ struct GemmProblem {
     const float *R = nullptr;                         // residual, or null
     int64_t ldr = 0, strideR = 0;
     int64_t causal = -1;   // >= 0: tiles wholly above j = causal + i are skipped
+    int64_t k_lo = -1;     // >= 0: row i's k-chain starts at max(0, i - k_lo)
+    int64_t k_hi = -1;     // >= 0: row i's k-chain ends at min(K - 1, i + k_hi)
 };
 
 struct GemmConfigInfo {

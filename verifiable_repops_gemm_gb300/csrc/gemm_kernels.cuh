@@ -301,6 +301,7 @@ struct ExArgs {
     const float *R;        // residual of batch 0 or null; batch b at R + b*sR
     int64_t ldr, sR;
     int64_t causal;        // >= 0: a tile wholly above j = causal + i is skipped
+    int64_t k_lo, k_hi;    // >= 0: row i's k-chain covers [i - k_lo, i + k_hi] only
 };
 
 // True when every element (i, j) of the tile has j > causal + i: the tile is
@@ -308,6 +309,19 @@ struct ExArgs {
 template <int BM>
 __device__ __forceinline__ bool tile_above_causal(const ExArgs &ep, int64_t m0, int64_t n0) {
     return ep.causal >= 0 && n0 > m0 + (BM - 1) + ep.causal;
+}
+
+// The k-slices [kb, ke) a tile of rows m0 .. m0+BM-1 runs: the union of its
+// rows' k windows, widened to whole slices (all KT slices without a band).
+// Terms outside a row's own window multiply A entries that the caller keeps
+// at +-0 by finite B values: they add +-0 and change no bit.
+template <int BM>
+__device__ __forceinline__ void tile_k_range(const ExArgs &ep, int64_t m0, int64_t K, int &kb, int &ke) {
+    int64_t lo = 0, hi = K;                                   // k in [lo, hi)
+    if (ep.k_lo >= 0 && m0 - ep.k_lo > 0) lo = m0 - ep.k_lo;
+    if (ep.k_hi >= 0 && m0 + (BM - 1) + ep.k_hi + 1 < hi) hi = m0 + (BM - 1) + ep.k_hi + 1;
+    kb = int(lo / BK);
+    ke = lo < hi ? int((hi + BK - 1) / BK) : kb;
 }
 
 // The epilogue after the whole k-chain of every element, then the store.
@@ -398,7 +412,9 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     int tm, tn;
     tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
-    const int KT = int((K + BK - 1) / BK);
+    int kb = 0, ke = int((K + BK - 1) / BK);
+    if constexpr (EX) tile_k_range<T::BM>(ep, m0, K, kb, ke);
+    const int NKT = ke - kb;                                   // slices this tile runs
     if (EX && tile_above_causal<T::BM>(ep, m0, n0)) return;   // the whole CTA, before any barrier
 
     if (tid == T::THREADS) {
@@ -418,7 +434,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             int issued = 0;
             bool ok = true;
 #pragma unroll 1
-            for (int kt = 0; kt < KT; ++kt) {
+            for (int kt = 0; kt < NKT; ++kt) {
                 const int s = kt % T::STAGES;
                 if (kt >= T::STAGES &&
                     !mbar_wait_bounded(&empty[s], uint32_t(kt / T::STAGES - 1) & 1u)) {
@@ -428,7 +444,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 float *As = smem + s * T::STAGE_FLOATS;
                 float *Bs = As + T::A_FLOATS;
                 mbar_arrive_expect_tx(&full[s], T::STAGE_BYTES);
-                const int k0 = kt * BK;
+                const int k0 = (kb + kt) * BK;
                 const int ax = A_KIN ? k0 : int(m0), ay = A_KIN ? int(m0) : k0;
                 const int bx = B_KIN ? k0 : int(n0), by = B_KIN ? int(n0) : k0;
                 if (EX && ep.zA) tma_load_3d(As, &tmA, &full[s], ax, ay, int(blockIdx.y));
@@ -455,7 +471,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     PackedAcc<T, A_KIN> acc;
     acc.zero();
 #pragma unroll 1
-    for (int kt = 0; kt < KT; ++kt) {
+    for (int kt = 0; kt < NKT; ++kt) {
         const int s = kt % T::STAGES;
         if (!mbar_wait_bounded(&full[s], uint32_t(kt / T::STAGES) & 1u)) {
             atomicOr(status, 1u);
@@ -542,7 +558,9 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
     int tm, tn;
     tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
-    const int KT = int((K + BK - 1) / BK);
+    int kb = 0, ke = int((K + BK - 1) / BK);
+    if constexpr (EX) tile_k_range<T::BM>(ep, m0, K, kb, ke);
+    const int KT = ke - kb;                                    // slices this tile runs
     if (EX && tile_above_causal<T::BM>(ep, m0, n0)) return;   // the whole CTA, before any barrier
 
 #pragma unroll 1
@@ -550,7 +568,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
         if (s < KT) {
             float *As = smem + s * T::STAGE_FLOATS;
             load_slice_cpasync<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, A, lda, B, ldb, M, N, K,
-                                                m0, n0, int64_t(s) * BK, tid);
+                                                m0, n0, int64_t(kb + s) * BK, tid);
         }
         cp_async_commit();
     }
@@ -571,7 +589,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
         if (nk < KT) {
             float *As = smem + (nk % T::STAGES) * T::STAGE_FLOATS;
             load_slice_cpasync<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, A, lda, B, ldb, M, N, K,
-                                                m0, n0, int64_t(nk) * BK, tid);
+                                                m0, n0, int64_t(kb + nk) * BK, tid);
         }
         cp_async_commit();
         const float *As = smem + (kt % T::STAGES) * T::STAGE_FLOATS;
@@ -640,6 +658,7 @@ inline ExArgs ex_args(const GemmProblem &p) {
     ExArgs ep{};
     ep.alpha = 1.0f;
     ep.causal = -1;
+    ep.k_lo = ep.k_hi = -1;
     if (!p.ex) return ep;
     ep.sA = p.strideA; ep.sB = p.strideB; ep.sC = p.strideC;
     ep.zA = p.batch > 1 && p.strideA != 0;
@@ -651,6 +670,8 @@ inline ExArgs ex_args(const GemmProblem &p) {
     ep.ldr = p.ldr;
     ep.sR = p.strideR;
     ep.causal = p.causal;
+    ep.k_lo = p.k_lo;
+    ep.k_hi = p.k_hi;
     return ep;
 }
 

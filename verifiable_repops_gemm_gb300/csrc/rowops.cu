@@ -575,22 +575,30 @@ rmsnorm_backward_kernel(int64_t rows, int64_t n, const float *__restrict__ x, in
     }
 }
 
-// Softmax backward: s = tree sum(dp*p), ds = p*(dp - s).  Each thread writes
-// only the elements it read in the same pass, so ds may be dp or p.
+// Values of row r a causal softmax (first, period) saw: all n when first < 0.
+__device__ __forceinline__ int64_t causal_prefix(int64_t r, int64_t n, int64_t first, int64_t period) {
+    return first < 0 ? n : imin64(n, first + r % period + 1);
+}
+
+// Softmax backward over each row's prefix of L values (L = n unless causal):
+// s = tree sum(dp*p) over the prefix, ds = p*(dp - s) there and +0 after; the
+// entries past the prefix are never read.  Each thread writes only the
+// elements it read in the same pass, so ds may be dp or p.
 __global__ void __launch_bounds__(256)
 softmax_backward_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, const float *dp, int64_t lddp,
-                        float *ds, int64_t ldds) {
+                        float *ds, int64_t ldds, int64_t first, int64_t period) {
     extern __shared__ float buf[];
     __shared__ float bcast;
     const int runs = int((n + RUN - 1) / RUN);
     float *buf2 = buf + runs;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const float *pr = p + r * ldp, *gr = dp + r * lddp;
-        const float sum = generic_reduce_idx<Op::Sum>(n, [&](int64_t i) { return __fmul_rn(gr[i], pr[i]); }, buf,
+        const int64_t L = causal_prefix(r, n, first, period);
+        const float sum = generic_reduce_idx<Op::Sum>(L, [&](int64_t i) { return __fmul_rn(gr[i], pr[i]); }, buf,
                                                       buf2, &bcast);
         for (int j = threadIdx.x; j < runs; j += blockDim.x)
             for (int64_t i = int64_t(j) * RUN; i < imin64(int64_t(j + 1) * RUN, n); ++i)
-                ds[r * ldds + i] = __fmul_rn(pr[i], __fsub_rn(gr[i], sum));
+                ds[r * ldds + i] = i < L ? __fmul_rn(pr[i], __fsub_rn(gr[i], sum)) : 0.0f;
         __syncthreads();
     }
 }
@@ -603,27 +611,31 @@ softmax_backward_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, co
 template <int T>
 __global__ void __launch_bounds__(T)
 softmax_backward_staged_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, const float *dp, int64_t lddp,
-                               float *ds, int64_t ldds) {
+                               float *ds, int64_t ldds, int64_t first, int64_t period) {
     extern __shared__ float4 stage_mem[];
     __shared__ float gbuf[2][RUN];
     int phase = 0;
     float4 *sp = stage_mem, *sd = stage_mem + T * RUN / 4;
-    const int runs = int((n + RUN - 1) / RUN);
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
-        stage_in<T, 1>(sp, p + row * ldp, n);
-        stage_in<T, 1>(sd, dp + row * lddp, n);
+        // only the prefix is copied and reduced; the rest of ds is +0
+        const int64_t L = causal_prefix(row, n, first, period);
+        stage_in<T, 1>(sp, p + row * ldp, L);
+        stage_in<T, 1>(sd, dp + row * lddp, L);
         cp_async_commit();
         cp_async_wait<0>();
         __syncwarp();
         RowRuns<T, 1> a, b;
-        read_stage(a, sp, n);
-        read_stage(b, sd, n);
+        read_stage(a, sp, L);
+        read_stage(b, sd, L);
 #pragma unroll
         for (int i = 0; i < RUN; ++i) b.v[0][i] = __fmul_rn(b.v[0][i], a.v[0][i]);   // dp * p
-        const float sum = b.template reduce<Op::Sum>(Ident(), gbuf, phase, runs);
-        read_stage(b, sd, n);                                                          // dp again
+        const float sum = b.template reduce<Op::Sum>(Ident(), gbuf, phase, int((L + RUN - 1) / RUN));
+        read_stage(b, sd, L);                                                          // dp again
+        const int64_t s0 = int64_t(threadIdx.x) * RUN;
+        a.len[0] = s0 < n ? int(imin64(RUN, n - s0)) : 0;
 #pragma unroll
-        for (int i = 0; i < RUN; ++i) a.v[0][i] = __fmul_rn(a.v[0][i], __fsub_rn(b.v[0][i], sum));
+        for (int i = 0; i < RUN; ++i)
+            a.v[0][i] = s0 + i < L ? __fmul_rn(a.v[0][i], __fsub_rn(b.v[0][i], sum)) : 0.0f;
         __syncwarp();                      // every lane has read both stages before the p stage is rewritten
         write_stage(a, sp);
         __syncwarp();
@@ -855,8 +867,9 @@ extern "C" int repops_rmsnorm_backward_f32(int64_t rows, int64_t cols, const flo
     return check_launch();
 }
 
-extern "C" int repops_softmax_backward_f32(int64_t rows, int64_t cols, const float *p, int64_t ldp, const float *dp,
-                                           int64_t lddp, float *ds, int64_t ldds, cudaStream_t stream) {
+namespace {
+int softmax_backward(int64_t rows, int64_t cols, const float *p, int64_t ldp, const float *dp, int64_t lddp,
+                     float *ds, int64_t ldds, int64_t first, int64_t period, cudaStream_t stream) {
     if (rows < 0 || cols < 0) return REPOPS_ERR_INVALID_ARG;
     if (rows == 0 || cols == 0) return REPOPS_OK;
     if (!p || !dp || !ds) return REPOPS_ERR_INVALID_ARG;
@@ -872,7 +885,7 @@ extern "C" int repops_softmax_backward_f32(int64_t rows, int64_t cols, const flo
     if (staged) {
         auto go = [&](auto kern, int T) {
             return launch_persistent(kern, T, size_t(2) * T * RUN * sizeof(float), rows, stream, rows, cols, p,
-                                     ldp, dp, lddp, ds, ldds);
+                                     ldp, dp, lddp, ds, ldds, first, period);
         };
         if (runs <= 32) return go(softmax_backward_staged_kernel<32>, 32);
         if (runs <= 64) return go(softmax_backward_staged_kernel<64>, 64);
@@ -882,8 +895,23 @@ extern "C" int repops_softmax_backward_f32(int64_t rows, int64_t cols, const flo
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(softmax_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
-    softmax_backward_kernel<<<grid_for_rows(rows), 256, smem, stream>>>(rows, cols, p, ldp, dp, lddp, ds, ldds);
+    softmax_backward_kernel<<<grid_for_rows(rows), 256, smem, stream>>>(rows, cols, p, ldp, dp, lddp, ds, ldds,
+                                                                        first, period);
     return check_launch();
+}
+}  // namespace
+
+extern "C" int repops_softmax_backward_f32(int64_t rows, int64_t cols, const float *p, int64_t ldp, const float *dp,
+                                           int64_t lddp, float *ds, int64_t ldds, cudaStream_t stream) {
+    return softmax_backward(rows, cols, p, ldp, dp, lddp, ds, ldds, -1, 1, stream);
+}
+
+extern "C" int repops_softmax_backward_causal_f32(int64_t rows, int64_t cols, const float *p, int64_t ldp,
+                                                  const float *dp, int64_t lddp, float *ds, int64_t ldds,
+                                                  int64_t first, int64_t period, cudaStream_t stream) {
+    if (first < 0 || period < 1) return REPOPS_ERR_INVALID_ARG;
+    // from first >= cols - 1 on, every row's prefix is the whole row
+    return softmax_backward(rows, cols, p, ldp, dp, lddp, ds, ldds, first < cols - 1 ? first : -1, period, stream);
 }
 
 extern "C" int repops_colsum_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,

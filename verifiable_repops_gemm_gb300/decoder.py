@@ -1,55 +1,70 @@
-"""One transformer decoder layer, forward, built only from the library's
-order-fixed operators: the workload of a verifiable training step on a
-Llama-style model ("Verde与RepOps" §4.3, the Llama-1B training measurement),
+"""One transformer decoder layer, forward and backward, built only from the
+library's order-fixed operators: the workload of a verifiable training step on
+a Llama-style model ("Verde与RepOps" §4.3, the Llama-1B training measurement),
 driven with synthetic weights.
 
 Layer (pre-norm, causal, grouped-query attention):
 
     h    = RMSNorm(x; g1)
     qkv  = h W_qkv                                  one GEMM
+    q, k = rotary(q, k)                             in place, the heads' pairs
+                                                    rotated to each token's position
     for every sequence (each GEMM call batches one query head of every
     key/value group, whose operands lie one stride apart):
         S = (Q K^T) / sqrt(d_head)                  batched GEMM, alpha epilogue,
                                                     tiles above the diagonal skipped
         P = causal softmax of every head's rows     one row-operator call
-        O = P V                                     batched GEMM, written as the
-                                                    heads' column blocks
+        O = P V                                     batched GEMM over k <= i only,
+                                                    written as the heads' column blocks
     x    = x + O W_o                                GEMM, residual epilogue (in place)
     h    = RMSNorm(x; g2)
-    u    = GeLU(h W_up + b_up)                      GEMM, bias epilogue; GeLU kernel
-    x    = x + u W_down + b_down                    GEMM, bias + residual epilogue
+    SwiGLU MLP (mlp="swiglu", Llama):
+        [g | u] = h W_gu                            one GEMM, gate and up side by side
+        a    = SiLU(g) * u                          element-wise kernel
+        x    = x + a W_down                         GEMM, residual epilogue
+    GeLU MLP (mlp="gelu"):
+        a    = GeLU(h W_up + b_up)                  GEMM, bias epilogue; GeLU kernel
+        x    = x + a W_down + b_down                GEMM, bias + residual epilogue
+
+The causal attention GEMMs run over the band where the probabilities are not
++0 (P V over k <= i; the gradients P^T dO and dS^T Q over k >= i, dS K over
+k <= i): the skipped terms would add fl(+0 * v) = +-0 to each chain, so the
+bits equal those of the full chains while the work halves.
 
 `backward` runs the layer's backward pass from saved activations: weight,
 bias and gain gradients and the input gradient, every step again a library
-call (transposed GEMMs, the backward row operators, column sums); the key and
-value gradients of a key/value head accumulate its query heads in head order
-through the GEMM's residual epilogue.
+call (transposed GEMMs, the backward row operators, column sums, the inverse
+rotation); the key and value gradients of a key/value head accumulate its
+query heads in head order through the GEMM's residual epilogue.
 
 Every step is a library call (this module only slices tensors); the bits of
-the result depend on nothing but the inputs.  GeLU runs as its own kernel by
-default: inside the GEMM's epilogue it measured 2.5x its stand-alone cost (the
-GEMM is bound by the FP32 pipe, and its epilogue runs on few warps), more than
-the memory pass it saves; `gelu_epilogue=True` fuses it anyway.  `fused=False`
-runs every epilogue as a separate step (GEMM, then element-wise adds in
-PyTorch, then the library's GeLU): the same bits, more memory traffic; it
-exists to measure what the fusion saves.
+the result depend on nothing but the inputs.  In the GeLU layer, GeLU runs as
+its own kernel by default: inside the GEMM's epilogue it measured 2.5x its
+stand-alone cost (the GEMM is bound by the FP32 pipe, and its epilogue runs on
+few warps), more than the memory pass it saves; `gelu_epilogue=True` fuses it
+anyway.  `fused=False` runs every epilogue as a separate step (GEMM, then
+element-wise adds in PyTorch): the same bits, more memory traffic; it exists
+to measure what the fusion saves.
 """
+import math
 from dataclasses import dataclass
 
 import torch
 
 from . import (gemm, gemm_batched, gelu, rmsnorm_rows, softmax_rows, ACT_GELU, colsum, gelu_backward,
-               rmsnorm_backward, softmax_backward)
+               rmsnorm_backward, softmax_backward, swiglu, swiglu_backward, rope_frequencies, rope_table, rope)
 
 
 @dataclass(frozen=True)
 class DecoderConfig:
-    d: int = 2048            # model width
-    heads: int = 32          # query heads
-    kv_heads: int = 8        # key/value heads (grouped-query attention)
-    ffn: int = 8192          # MLP width
-    seq_len: int = 2048      # tokens per sequence
+    d: int = 2048              # model width
+    heads: int = 32            # query heads
+    kv_heads: int = 8          # key/value heads (grouped-query attention)
+    ffn: int = 8192            # MLP width
+    seq_len: int = 2048        # tokens per sequence
     eps: float = 1e-5
+    mlp: str = "swiglu"        # "swiglu" (Llama: gate and up, no biases) or "gelu" (up + bias)
+    rope_base: float = 500000.0  # rotary base; 0 turns the rotary embedding off
 
     @property
     def d_head(self) -> int:
@@ -60,30 +75,56 @@ class DecoderConfig:
         return self.d + 2 * self.kv_heads * self.d_head
 
     def flops(self, tokens: int) -> float:
-        """Multiply-adds x 2 of the layer's GEMMs (attention computed over the
-        full score matrix, masked entries included)."""
+        """Multiply-adds x 2 of the layer's GEMMs, attention counted over the
+        causal band only (S (S + 1) / 2 scores per head): the work the layer
+        needs, not the full score matrix."""
         d, f, w = self.d, self.ffn, self.qkv_width
         seqs = tokens // self.seq_len
-        attn = 2 * 2.0 * seqs * self.heads * self.seq_len * self.seq_len * self.d_head
-        return 2.0 * tokens * (d * w + d * d + 2 * d * f) + attn
+        S = self.seq_len
+        attn = 2 * 2.0 * seqs * self.heads * (S * (S + 1) / 2) * self.d_head
+        mlp = 3 * d * f if self.mlp == "swiglu" else 2 * d * f
+        return 2.0 * tokens * (d * w + d * d + mlp) + attn
+
+
+def weight_shapes(cfg: DecoderConfig) -> dict:
+    """Every weight of a layer and its shape, in a fixed order."""
+    d, w, f = cfg.d, cfg.qkv_width, cfg.ffn
+    if cfg.mlp == "swiglu":
+        return {"g1": (d,), "w_qkv": (d, w), "w_o": (d, d), "g2": (d,), "w_gu": (d, 2 * f), "w_down": (f, d)}
+    if cfg.mlp == "gelu":
+        return {"g1": (d,), "w_qkv": (d, w), "w_o": (d, d), "g2": (d,), "w_up": (d, f), "b_up": (f,),
+                "w_down": (f, d), "b_down": (d,)}
+    raise ValueError("mlp must be 'swiglu' or 'gelu'")
 
 
 def init_weights(cfg: DecoderConfig, seed: int, device) -> dict:
-    """Synthetic weights: N(0, 0.02) matrices, N(0, 0.02) biases, norm gains
+    """Synthetic weights: N(0, 0.02) matrices and biases, norm gains
     N(1, 0.1); seeded, generated on `device`."""
     g = torch.Generator(device=device)
     g.manual_seed(seed)
+    out = {}
+    for name, shape in weight_shapes(cfg).items():
+        t = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        out[name] = t * 0.1 + 1.0 if name in ("g1", "g2") else t * 0.02
+    return out
 
-    def n(shape, std, mean=0.0):
-        return torch.randn(shape, generator=g, device=device, dtype=torch.float32) * std + mean
 
-    return {
-        "g1": n((cfg.d,), 0.1, 1.0), "g2": n((cfg.d,), 0.1, 1.0),
-        "w_qkv": n((cfg.d, cfg.qkv_width), 0.02),
-        "w_o": n((cfg.d, cfg.d), 0.02),
-        "w_up": n((cfg.d, cfg.ffn), 0.02), "b_up": n((cfg.ffn,), 0.02),
-        "w_down": n((cfg.ffn, cfg.d), 0.02), "b_down": n((cfg.d,), 0.02),
-    }
+def rope_tables(cfg: DecoderConfig, device):
+    """(cos, sin), seq_len x d_head/2, of the layer's rotary embedding, or
+    None when it is off: frequencies base^(-2i/d_head) from the binary32
+    value of ln(base), angles p * f_i for positions p < seq_len."""
+    if not cfg.rope_base:
+        return None
+    freq = rope_frequencies(cfg.d_head // 2, math.log(cfg.rope_base), device)
+    return rope_table(cfg.seq_len, freq)
+
+
+def _rotate(qkv, cfg: DecoderConfig, tables, inverse: bool):
+    """The rotary embedding (or its transpose) of the query and key heads:
+    columns [0, (heads + kv_heads) * d_head) of every row, position = the row's
+    index within its sequence."""
+    if tables is not None:
+        rope(qkv, cfg.heads + cfg.kv_heads, tables[0], tables[1], first=0, period=cfg.seq_len, inverse=inverse)
 
 
 def _per_kv(t, rows, col0, kv, group, h, dh):
@@ -120,7 +161,8 @@ def attention(qkv, cfg: DecoderConfig, out, scores, probs=None):
         P = sc.view(kv * group * S, S)
         softmax_rows(P, out=P, causal_first=0, causal_period=S)
         for h in range(group):
-            gemm_batched(sc[:, h], V, out=_per_kv(out, rows, 0, kv, group, h, dh))
+            # P is +0 past the diagonal: row i's chain stops at k = i
+            gemm_batched(sc[:, h], V, out=_per_kv(out, rows, 0, kv, group, h, dh), k_hi=0)
 
 
 def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue: bool = False,
@@ -128,19 +170,21 @@ def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue
     """Runs the layer on x (T x d, T a multiple of seq_len) in place and
     returns it.  `work`: reusable buffers from `workspace` (allocated when
     absent).  `save`: a dict (from `activations`) that receives what
-    `backward` needs; the layer then keeps its GeLU input and runs GeLU as its
-    own kernel."""
+    `backward` needs; a GeLU layer then keeps its GeLU input and runs GeLU as
+    its own kernel."""
     T = x.shape[0]
     if T % cfg.seq_len:
         raise ValueError("tokens must be a whole number of sequences")
     ws = work if work is not None else workspace(cfg, T, x.device)
+    f = cfg.ffn
     if save is not None:
         save["x0"].copy_(x)
-        h, qkv, attn, u = save["h1"], save["qkv"], save["attn"], save["u"]
+        h, qkv, attn, a = save["h1"], save["qkv"], save["attn"], save["a"]
     else:
-        h, qkv, attn, u = ws["h"], ws["qkv"], ws["attn"], ws["u"]
+        h, qkv, attn, a = ws["h"], ws["qkv"], ws["attn"], ws["a"]
     rmsnorm_rows(x, w["g1"], cfg.eps, out=h)
     gemm(h, w["w_qkv"], out=qkv)
+    _rotate(qkv, cfg, ws["rope"], inverse=False)
     attention(qkv, cfg, attn, ws["scores"], save["probs"] if save is not None else None)
     if fused:
         gemm_batched(attn, w["w_o"], out=x, residual=x)
@@ -150,22 +194,31 @@ def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue
         save["x1"].copy_(x)
         h = save["h2"]
     rmsnorm_rows(x, w["g2"], cfg.eps, out=h)
+    if cfg.mlp == "swiglu":
+        gu = save["gu"] if save is not None else ws["gu"]
+        gemm(h, w["w_gu"], out=gu)
+        swiglu(gu[:, :f], gu[:, f:], out=a)
+        if fused:
+            gemm_batched(a, w["w_down"], out=x, residual=x)
+        else:
+            x += gemm(a, w["w_down"], out=ws["tmp_d"])
+        return x
     if save is not None:
-        gemm_batched(h, w["w_up"], out=save["a"], bias=w["b_up"])
-        gelu(save["a"], out=u)
-        gemm_batched(u, w["w_down"], out=x, bias=w["b_down"], residual=x)
+        gemm_batched(h, w["w_up"], out=save["pre"], bias=w["b_up"])
+        gelu(save["pre"], out=a)
+        gemm_batched(a, w["w_down"], out=x, bias=w["b_down"], residual=x)
     elif fused:
         if gelu_epilogue:
-            gemm_batched(h, w["w_up"], out=u, bias=w["b_up"], act=ACT_GELU)
+            gemm_batched(h, w["w_up"], out=a, bias=w["b_up"], act=ACT_GELU)
         else:
-            gemm_batched(h, w["w_up"], out=u, bias=w["b_up"])
-            gelu(u, out=u)
-        gemm_batched(u, w["w_down"], out=x, bias=w["b_down"], residual=x)
+            gemm_batched(h, w["w_up"], out=a, bias=w["b_up"])
+            gelu(a, out=a)
+        gemm_batched(a, w["w_down"], out=x, bias=w["b_down"], residual=x)
     else:
-        gemm(h, w["w_up"], out=u)
-        u += w["b_up"]
-        gelu(u, out=u)
-        y = gemm(u, w["w_down"], out=ws["tmp_d"])
+        gemm(h, w["w_up"], out=a)
+        a += w["b_up"]
+        gelu(a, out=a)
+        y = gemm(a, w["w_down"], out=ws["tmp_d"])
         y += w["b_down"]
         x += y
     return x
@@ -176,45 +229,65 @@ def activations(cfg: DecoderConfig, tokens: int, device) -> dict:
     (every head's attention probabilities included: seqs * heads * S^2)."""
     e = dict(dtype=torch.float32, device=device)
     group, S = cfg.heads // cfg.kv_heads, cfg.seq_len
-    return {"x0": torch.empty(tokens, cfg.d, **e), "h1": torch.empty(tokens, cfg.d, **e),
-            "qkv": torch.empty(tokens, cfg.qkv_width, **e), "attn": torch.empty(tokens, cfg.d, **e),
-            "probs": torch.empty(tokens // S * cfg.kv_heads, group, S, S, **e),
-            "x1": torch.empty(tokens, cfg.d, **e), "h2": torch.empty(tokens, cfg.d, **e),
-            "a": torch.empty(tokens, cfg.ffn, **e), "u": torch.empty(tokens, cfg.ffn, **e)}
+    out = {"x0": torch.empty(tokens, cfg.d, **e), "h1": torch.empty(tokens, cfg.d, **e),
+           "qkv": torch.empty(tokens, cfg.qkv_width, **e), "attn": torch.empty(tokens, cfg.d, **e),
+           "probs": torch.empty(tokens // S * cfg.kv_heads, group, S, S, **e),
+           "x1": torch.empty(tokens, cfg.d, **e), "h2": torch.empty(tokens, cfg.d, **e),
+           "a": torch.empty(tokens, cfg.ffn, **e)}
+    if cfg.mlp == "swiglu":
+        out["gu"] = torch.empty(tokens, 2 * cfg.ffn, **e)
+    else:
+        out["pre"] = torch.empty(tokens, cfg.ffn, **e)
+    return out
 
 
 def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None, grads: dict = None):
     """Gradients of the layer given dy = dL/d(output): returns (dx, grads) with
     grads holding one tensor per weight of `init_weights` (written into the
     tensors of `grads` when given, e.g. views of one flat gradient buffer).
-    dy is consumed (used as scratch) and dx is returned in its storage.  Every
-    step is a library call:
+    dy is consumed (used as scratch) and dx is returned in its storage; a
+    SwiGLU layer's saved["gu"] is overwritten with its gradient.  Every step
+    is a library call:
 
-        dW_down = u^T dy, db_down = colsum(dy), du = dy W_down^T
-        da = GeLU'(a) du, dW_up = h2^T da, db_up = colsum(da), dh2 = da W_up^T
+        SwiGLU MLP:
+          dW_down = a^T dy, da = dy W_down^T
+          [dg | du] = SwiGLU'(g, u; da), dW_gu = h2^T [dg | du], dh2 = [dg | du] W_gu^T
+        GeLU MLP:
+          dW_down = a^T dy, db_down = colsum(dy), da = dy W_down^T
+          dpre = GeLU'(pre) da, dW_up = h2^T dpre, db_up = colsum(dpre), dh2 = dpre W_up^T
         dx1 = RMSNorm'(x1; dh2) + dy, dg2 = colsum(dh2 * xhat2)
         dW_o = attn^T dx1, dattn = dx1 W_o^T
         attention, per sequence and key/value head k (its query heads h):
-            dP_h = dO_h V_k^T;  dV_k = sum_h P_h^T dO_h (head order)
-            dS_h = softmax'(P_h; dP_h)
-            dQ_h = s dS_h K_k;  dK_k = sum_h s dS_h^T Q_h (head order), s = 1/sqrt(d_head)
+            dP_h = dO_h V_k^T (on and below the diagonal);
+            dV_k = sum_h P_h^T dO_h (head order, k >= i)
+            dS_h = causal softmax'(P_h; dP_h)
+            dQ_h = s dS_h K_k (k <= i);  dK_k = sum_h s dS_h^T Q_h (head order,
+            k >= i), s = 1/sqrt(d_head)
+        dq, dk rotated back (the rotary embedding's transpose)
         dW_qkv = h1^T dqkv, dh1 = dqkv W_qkv^T
         dx0 = RMSNorm'(x0; dh1) + dx1, dg1 = colsum(dh1 * xhat1)
     """
     T = dy.shape[0]
     S, dh, group = cfg.seq_len, cfg.d_head, cfg.heads // cfg.kv_heads
+    f = cfg.ffn
     scale = 1.0 / float(dh) ** 0.5
     k0, v0 = cfg.d, cfg.d + cfg.kv_heads * dh
     ws = work if work is not None else backward_workspace(cfg, T, dy.device)
     g = {}
     o = grads if grads is not None else {}
-    g["w_down"] = gemm(saved["u"].t(), dy, out=o.get("w_down"))
-    g["b_down"] = colsum(dy, out=o.get("b_down"))
-    du = gemm(dy, w["w_down"].t(), out=ws["t_ffn"])
-    da = gelu_backward(saved["a"], du, out=du)
-    g["w_up"] = gemm(saved["h2"].t(), da, out=o.get("w_up"))
-    g["b_up"] = colsum(da, out=o.get("b_up"))
-    dh2 = gemm(da, w["w_up"].t(), out=ws["t_d"])
+    g["w_down"] = gemm(saved["a"].t(), dy, out=o.get("w_down"))
+    da = gemm(dy, w["w_down"].t(), out=ws["t_ffn"])
+    if cfg.mlp == "swiglu":
+        gu = saved["gu"]
+        swiglu_backward(gu[:, :f], gu[:, f:], da, dg=gu[:, :f], du=gu[:, f:])     # gu <- [dg | du]
+        g["w_gu"] = gemm(saved["h2"].t(), gu, out=o.get("w_gu"))
+        dh2 = gemm(gu, w["w_gu"].t(), out=ws["t_d"])
+    else:
+        g["b_down"] = colsum(dy, out=o.get("b_down"))
+        dpre = gelu_backward(saved["pre"], da, out=da)
+        g["w_up"] = gemm(saved["h2"].t(), dpre, out=o.get("w_up"))
+        g["b_up"] = colsum(dpre, out=o.get("b_up"))
+        dh2 = gemm(dpre, w["w_up"].t(), out=ws["t_d"])
     dx1, p2 = rmsnorm_backward(saved["x1"], w["g2"], cfg.eps, dh2, dx=dy, dyxh=ws["t_d2"], res=dy)
     g["g2"] = colsum(p2, out=o.get("g2"))
     g["w_o"] = gemm(saved["attn"].t(), dx1, out=o.get("w_o"))
@@ -230,16 +303,19 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None,
         dV, dK = _kv(dqkv, rows, v0, kv, dh), _kv(dqkv, rows, k0, kv, dh)
         for h in range(group):
             dO = _per_kv(dattn, rows, 0, kv, group, h, dh)
-            gemm_batched(dO, V.transpose(1, 2), out=dP[:, h])                    # dP_h = dO_h V^T
-            # dV = sum over the group's heads, in head order, of P_h^T dO_h
-            gemm_batched(P[:, h].transpose(1, 2), dO, out=dV, residual=dV if h else None)
+            # dP_h = dO_h V^T on and below the diagonal (the causal backward reads no more)
+            gemm_batched(dO, V.transpose(1, 2), out=dP[:, h], causal_first=0)
+            # dV = sum over the group's heads, in head order, of P_h^T dO_h;
+            # row i of P^T is +0 before k = i
+            gemm_batched(P[:, h].transpose(1, 2), dO, out=dV, residual=dV if h else None, k_lo=0)
         dS = dP.view(kv * group * S, S)
-        softmax_backward(P.view(kv * group * S, S), dS, out=dS)
+        softmax_backward(P.view(kv * group * S, S), dS, out=dS, causal_first=0, causal_period=S)
         for h in range(group):
-            gemm_batched(dP[:, h], K, out=_per_kv(dqkv, rows, 0, kv, group, h, dh), alpha=scale)
+            gemm_batched(dP[:, h], K, out=_per_kv(dqkv, rows, 0, kv, group, h, dh), alpha=scale, k_hi=0)
             # dK = sum over the group's heads, in head order, of s dS_h^T Q_h
             gemm_batched(dP[:, h].transpose(1, 2), _per_kv(qkv, rows, 0, kv, group, h, dh), out=dK, alpha=scale,
-                         residual=dK if h else None)
+                         residual=dK if h else None, k_lo=0)
+    _rotate(dqkv, cfg, ws["rope"], inverse=True)
     g["w_qkv"] = gemm(saved["h1"].t(), dqkv, out=o.get("w_qkv"))
     dh1 = gemm(dqkv, w["w_qkv"].t(), out=ws["t_d"])
     dx0, p1 = rmsnorm_backward(saved["x0"], w["g1"], cfg.eps, dh1, dx=dx1, dyxh=ws["t_d2"], res=dx1)
@@ -252,13 +328,16 @@ def backward_workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
     group, S = cfg.heads // cfg.kv_heads, cfg.seq_len
     return {"t_ffn": torch.empty(tokens, cfg.ffn, **e), "t_d": torch.empty(tokens, cfg.d, **e),
             "t_d2": torch.empty(tokens, cfg.d, **e), "dqkv": torch.empty(tokens, cfg.qkv_width, **e),
-            "dp": torch.empty(cfg.kv_heads, group, S, S, **e)}
+            "dp": torch.empty(cfg.kv_heads, group, S, S, **e), "rope": rope_tables(cfg, device)}
 
 
 def workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
     e = dict(dtype=torch.float32, device=device)
     group = cfg.heads // cfg.kv_heads
-    return {"h": torch.empty(tokens, cfg.d, **e), "qkv": torch.empty(tokens, cfg.qkv_width, **e),
-            "attn": torch.empty(tokens, cfg.d, **e), "u": torch.empty(tokens, cfg.ffn, **e),
-            "scores": torch.empty(cfg.kv_heads, group, cfg.seq_len, cfg.seq_len, **e),
-            "tmp_d": torch.empty(tokens, cfg.d, **e)}
+    out = {"h": torch.empty(tokens, cfg.d, **e), "qkv": torch.empty(tokens, cfg.qkv_width, **e),
+           "attn": torch.empty(tokens, cfg.d, **e), "a": torch.empty(tokens, cfg.ffn, **e),
+           "scores": torch.empty(cfg.kv_heads, group, cfg.seq_len, cfg.seq_len, **e),
+           "tmp_d": torch.empty(tokens, cfg.d, **e), "rope": rope_tables(cfg, device)}
+    if cfg.mlp == "swiglu":
+        out["gu"] = torch.empty(tokens, 2 * cfg.ffn, **e)
+    return out

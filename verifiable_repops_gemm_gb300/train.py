@@ -22,23 +22,14 @@ import torch
 
 from . import decoder, fixed_order_mean_sgd, merkle_sha256, sort_ids
 
-LAYER_KEYS = ("g1", "w_qkv", "w_o", "g2", "w_up", "b_up", "w_down", "b_down")   # order inside theta
-
-
-def layer_shapes(cfg: decoder.DecoderConfig) -> dict:
-    d, w, f = cfg.d, cfg.qkv_width, cfg.ffn
-    return {"g1": (d,), "w_qkv": (d, w), "w_o": (d, d), "g2": (d,), "w_up": (d, f), "b_up": (f,),
-            "w_down": (f, d), "b_down": (d,)}
-
-
 def layout(cfg: decoder.DecoderConfig, layers: int):
-    """[(layer, key, offset, shape)] and the total length of theta: every
-    tensor starts at a multiple of 4 elements (16 bytes: TMA-describable)."""
+    """[(layer, key, offset, shape)] and the total length of theta: layer by
+    layer, each layer's weights in `decoder.weight_shapes` order, every tensor
+    starting at a multiple of 4 elements (16 bytes: TMA-describable)."""
     out, off = [], 0
-    shapes = layer_shapes(cfg)
+    shapes = decoder.weight_shapes(cfg)
     for layer in range(layers):
-        for key in LAYER_KEYS:
-            shape = shapes[key]
+        for key, shape in shapes.items():
             n = 1
             for s in shape:
                 n *= s
@@ -57,8 +48,8 @@ class Model:
         self.weights = self.views(self.theta)
         for layer in range(layers):
             init = decoder.init_weights(cfg, seed + layer, device)
-            for key in LAYER_KEYS:
-                self.weights[layer][key].copy_(init[key])
+            for key, v in init.items():
+                self.weights[layer][key].copy_(v)
 
     def views(self, flat):
         """Per layer, {key: view} of a flat buffer with theta's layout."""
