@@ -669,7 +669,7 @@ def run_sweep_decoder(dev, s, flush, peak):
         if cfg is llama:
             S = cfg.seq_len
             attn_flops = 2 * 2.0 * (T // S) * cfg.heads * (S * (S + 1) / 2) * cfg.d_head
-            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"]))
+            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"], streams=ws["streams"]))
             print(json.dumps({"sweep": "causal grouped-query attention (batched QK^T, softmax, banded PV)",
                               "tokens": T, "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
         # the training step: forward keeping its activations, then the backward

@@ -67,3 +67,28 @@ def test_decoder_layer_backward_matches_oracle(rp, orc, name):
     assert set(grads) == set(w)
     for key, gv in grads.items():
         assert np.array_equal(gv.cpu().numpy().view(np.uint32), g_want[key].view(np.uint32)), key
+
+
+def test_side_streams_do_not_change_the_bits(rp):
+    # the attention's sequences and heads on side streams, on the caller's
+    # stream alone, and with one score scratch shared by the sequences
+    cfg = SMALL
+    T = 3 * cfg.seq_len
+    w = decoder.init_weights(cfg, 13, DEV)
+    x = torch.randn(T, cfg.d, device=DEV)
+    dy = torch.randn(T, cfg.d, device=DEV)
+    ws = decoder.workspace(cfg, T, DEV)
+    serial = dict(ws, streams=None)
+    shared = dict(ws, scores=ws["scores"][:cfg.kv_heads])
+    ys = [decoder.forward(x.clone(), w, cfg, work=k) for k in (ws, serial, shared)]
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+    outs = []
+    for streams in (True, False):
+        saved = decoder.activations(cfg, T, DEV)
+        bws = decoder.backward_workspace(cfg, T, DEV)
+        if not streams:
+            bws["streams"] = None
+        decoder.forward(x.clone(), w, cfg, work=ws, save=saved)
+        outs.append(decoder.backward(dy.clone(), w, cfg, saved, work=bws))
+    (dx0, g0), (dx1, g1) = outs
+    assert torch.equal(dx0, dx1) and all(torch.equal(g0[k], g1[k]) for k in g0)

@@ -411,6 +411,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     const int tid = threadIdx.x;
     int tm, tn;
     tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    if (EX && ep.k_hi >= 0) tm = tiles_m - 1 - tm;             // longest k-ranges first
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
     int kb = 0, ke = int((K + BK - 1) / BK);
     if constexpr (EX) tile_k_range<T::BM>(ep, m0, K, kb, ke);
@@ -557,6 +558,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
     const int tid = threadIdx.x;
     int tm, tn;
     tile_coords<T::BM>(blockIdx.x, tiles_m, tiles_n, tm, tn);
+    if (EX && ep.k_hi >= 0) tm = tiles_m - 1 - tm;             // longest k-ranges first
     const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
     int kb = 0, ke = int((K + BK - 1) / BK);
     if constexpr (EX) tile_k_range<T::BM>(ep, m0, K, kb, ke);

@@ -127,6 +127,23 @@ def _rotate(qkv, cfg: DecoderConfig, tables, inverse: bool):
         rope(qkv, cfg.heads + cfg.kv_heads, tables[0], tables[1], first=0, period=cfg.seq_len, inverse=inverse)
 
 
+def _after(stream, *others):
+    """Work queued on `stream` from now on waits for everything queued so far
+    on `others`."""
+    for o in others:
+        e = torch.cuda.Event()
+        e.record(o)
+        stream.wait_event(e)
+
+
+def side_streams(cfg: DecoderConfig, tokens: int, device):
+    """The side streams one layer's attention runs its independent products
+    on: per sequence, one for the scores / dP and softmax, one per query head
+    of a group (P V, dS K), and one each for the dV and dK chains."""
+    group = cfg.heads // cfg.kv_heads
+    return [torch.cuda.Stream(device) for _ in range(tokens // cfg.seq_len * (group + 3))]
+
+
 def _per_kv(t, rows, col0, kv, group, h, dh):
     """(kv, S, dh) view of query head h of every key/value group: the column
     block (k*group + h)*dh of rows, k = 0 .. kv-1 (a batch stride of
@@ -139,30 +156,60 @@ def _kv(t, rows, col0, kv, dh):
     return t[rows, col0:col0 + kv * dh].unflatten(1, (kv, dh)).transpose(0, 1)
 
 
-def attention(qkv, cfg: DecoderConfig, out, scores, probs=None):
+def attention(qkv, cfg: DecoderConfig, out, scores, probs=None, streams=None):
     """Causal grouped-query attention of every sequence into `out` (T x d).
-    scores: (kv_heads, group, S, S) scratch; probs: optional
-    (sequences * kv_heads, group, S, S) buffer that keeps every head's softmax
-    output for the backward pass.  Each GEMM call batches query head h of all
-    key/value groups (their operands sit at one stride apart)."""
+    scores: (sequences * kv_heads, group, S, S) scratch (or (kv_heads, group,
+    S, S), shared by the sequences in turn); probs: optional buffer shaped
+    like the first that keeps every head's softmax output for the backward
+    pass.  Each GEMM call batches query head h of all key/value groups (their
+    operands sit at one stride apart).  streams (from `side_streams`): the
+    sequences, and the P V products of the heads, run concurrently -- their
+    outputs are disjoint, so the bits do not change -- and the caller's
+    stream waits for all of them."""
     S, dh, kv = cfg.seq_len, cfg.d_head, cfg.kv_heads
     group = cfg.heads // kv
     k0, v0 = cfg.d, cfg.d + kv * dh
     scale = 1.0 / float(dh) ** 0.5
-    for s in range(qkv.shape[0] // S):
+    seqs = qkv.shape[0] // S
+    buf = probs if probs is not None else scores
+    shared = buf.shape[0] < seqs * kv
+    main = torch.cuda.current_stream()
+    used, joined = [], []
+    if streams is not None:
+        fork = torch.cuda.Event()
+        fork.record(main)
+    for s in range(seqs):
         rows = slice(s * S, (s + 1) * S)
-        sc = scores if probs is None else probs[s * kv:(s + 1) * kv]               # (kv, group, S, S)
+        sc = buf if shared else buf[s * kv:(s + 1) * kv]                         # (kv, group, S, S)
         Kt = _kv(qkv, rows, k0, kv, dh).transpose(1, 2)                          # (kv, dh, S)
         V = _kv(qkv, rows, v0, kv, dh)
+        if streams is None:
+            st, heads_st = main, [main] * group
+        else:
+            base = s * (group + 3)
+            st, heads_st = streams[base], streams[base + 1:base + 1 + group]
+            st.wait_event(fork)
+            if shared:                  # a shared scratch is reused after the previous sequence's products
+                _after(st, *used)
+        with torch.cuda.stream(st):
+            for h in range(group):
+                # tiles wholly above the diagonal are skipped: the causal
+                # softmax never reads them
+                gemm_batched(_per_kv(qkv, rows, 0, kv, group, h, dh), Kt, out=sc[:, h], alpha=scale,
+                             causal_first=0)
+            P = sc.view(kv * group * S, S)
+            softmax_rows(P, out=P, causal_first=0, causal_period=S)
         for h in range(group):
-            # tiles wholly above the diagonal are skipped: the causal softmax
-            # never reads them
-            gemm_batched(_per_kv(qkv, rows, 0, kv, group, h, dh), Kt, out=sc[:, h], alpha=scale, causal_first=0)
-        P = sc.view(kv * group * S, S)
-        softmax_rows(P, out=P, causal_first=0, causal_period=S)
-        for h in range(group):
-            # P is +0 past the diagonal: row i's chain stops at k = i
-            gemm_batched(sc[:, h], V, out=_per_kv(out, rows, 0, kv, group, h, dh), k_hi=0)
+            if streams is not None:
+                _after(heads_st[h], st)
+            with torch.cuda.stream(heads_st[h]):
+                # P is +0 past the diagonal: row i's chain stops at k = i
+                gemm_batched(sc[:, h], V, out=_per_kv(out, rows, 0, kv, group, h, dh), k_hi=0)
+        if streams is not None:
+            used = [st] + list(heads_st)
+            joined += used
+    if streams is not None:
+        _after(main, *joined)
 
 
 def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue: bool = False,
@@ -185,7 +232,7 @@ def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue
     rmsnorm_rows(x, w["g1"], cfg.eps, out=h)
     gemm(h, w["w_qkv"], out=qkv)
     _rotate(qkv, cfg, ws["rope"], inverse=False)
-    attention(qkv, cfg, attn, ws["scores"], save["probs"] if save is not None else None)
+    attention(qkv, cfg, attn, ws["scores"], save["probs"] if save is not None else None, ws.get("streams"))
     if fused:
         gemm_batched(attn, w["w_o"], out=x, residual=x)
     else:
@@ -267,11 +314,7 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None,
         dW_qkv = h1^T dqkv, dh1 = dqkv W_qkv^T
         dx0 = RMSNorm'(x0; dh1) + dx1, dg1 = colsum(dh1 * xhat1)
     """
-    T = dy.shape[0]
-    S, dh, group = cfg.seq_len, cfg.d_head, cfg.heads // cfg.kv_heads
-    f = cfg.ffn
-    scale = 1.0 / float(dh) ** 0.5
-    k0, v0 = cfg.d, cfg.d + cfg.kv_heads * dh
+    T, f = dy.shape[0], cfg.ffn
     ws = work if work is not None else backward_workspace(cfg, T, dy.device)
     g = {}
     o = grads if grads is not None else {}
@@ -292,29 +335,8 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None,
     g["g2"] = colsum(p2, out=o.get("g2"))
     g["w_o"] = gemm(saved["attn"].t(), dx1, out=o.get("w_o"))
     dattn = gemm(dx1, w["w_o"].t(), out=ws["t_d"])
+    _attention_backward(dattn, ws["dqkv"], saved, cfg, ws["dp"], ws.get("streams"))
     dqkv = ws["dqkv"]
-    qkv = saved["qkv"]
-    kv = cfg.kv_heads
-    dP = ws["dp"]                                                                # (kv, group, S, S)
-    for s in range(T // S):
-        rows = slice(s * S, (s + 1) * S)
-        P = saved["probs"][s * kv:(s + 1) * kv]
-        V, K = _kv(qkv, rows, v0, kv, dh), _kv(qkv, rows, k0, kv, dh)
-        dV, dK = _kv(dqkv, rows, v0, kv, dh), _kv(dqkv, rows, k0, kv, dh)
-        for h in range(group):
-            dO = _per_kv(dattn, rows, 0, kv, group, h, dh)
-            # dP_h = dO_h V^T on and below the diagonal (the causal backward reads no more)
-            gemm_batched(dO, V.transpose(1, 2), out=dP[:, h], causal_first=0)
-            # dV = sum over the group's heads, in head order, of P_h^T dO_h;
-            # row i of P^T is +0 before k = i
-            gemm_batched(P[:, h].transpose(1, 2), dO, out=dV, residual=dV if h else None, k_lo=0)
-        dS = dP.view(kv * group * S, S)
-        softmax_backward(P.view(kv * group * S, S), dS, out=dS, causal_first=0, causal_period=S)
-        for h in range(group):
-            gemm_batched(dP[:, h], K, out=_per_kv(dqkv, rows, 0, kv, group, h, dh), alpha=scale, k_hi=0)
-            # dK = sum over the group's heads, in head order, of s dS_h^T Q_h
-            gemm_batched(dP[:, h].transpose(1, 2), _per_kv(qkv, rows, 0, kv, group, h, dh), out=dK, alpha=scale,
-                         residual=dK if h else None, k_lo=0)
     _rotate(dqkv, cfg, ws["rope"], inverse=True)
     g["w_qkv"] = gemm(saved["h1"].t(), dqkv, out=o.get("w_qkv"))
     dh1 = gemm(dqkv, w["w_qkv"].t(), out=ws["t_d"])
@@ -323,21 +345,96 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None,
     return dx0, g
 
 
+def _attention_backward(dattn, dqkv, saved, cfg: DecoderConfig, dp, streams):
+    """The attention's part of dqkv (before the inverse rotation), per
+    sequence and key/value head k with its query heads h:
+        dP_h = dO_h V_k^T (on and below the diagonal); dV_k = sum_h P_h^T dO_h
+        dS_h = causal softmax'(P_h; dP_h)
+        dQ_h = s dS_h K_k;  dK_k = sum_h s dS_h^T Q_h
+    dp: (sequences * kv_heads, group, S, S) scratch, or (kv_heads, group, S, S)
+    shared by the sequences in turn.  With `streams` the sequences run
+    concurrently, and within one the dV chain, the dK chain and the dQ_h run
+    beside each other; the chains keep head order, so the bits do not change."""
+    S, dh, kv = cfg.seq_len, cfg.d_head, cfg.kv_heads
+    group = cfg.heads // kv
+    scale = 1.0 / float(dh) ** 0.5
+    k0, v0 = cfg.d, cfg.d + kv * dh
+    qkv = saved["qkv"]
+    seqs = qkv.shape[0] // S
+    shared = dp.shape[0] < seqs * kv
+    main = torch.cuda.current_stream()
+    used, joined = [], []
+    if streams is not None:
+        fork = torch.cuda.Event()
+        fork.record(main)
+    for s in range(seqs):
+        rows = slice(s * S, (s + 1) * S)
+        P = saved["probs"][s * kv:(s + 1) * kv]
+        dP = dp if shared else dp[s * kv:(s + 1) * kv]                        # (kv, group, S, S)
+        V, K = _kv(qkv, rows, v0, kv, dh), _kv(qkv, rows, k0, kv, dh)
+        dV, dK = _kv(dqkv, rows, v0, kv, dh), _kv(dqkv, rows, k0, kv, dh)
+        if streams is None:
+            sp = sv = sk = main
+            sq = [main] * group
+        else:
+            base = s * (group + 3)
+            sp, sq, sv, sk = streams[base], streams[base + 1:base + 1 + group], streams[base + 1 + group], \
+                streams[base + 2 + group]
+            for st in (sp, sv):
+                st.wait_event(fork)
+            if shared:
+                _after(sp, *used)
+        with torch.cuda.stream(sp):
+            for h in range(group):
+                # dP_h = dO_h V^T on and below the diagonal (the causal backward reads no more)
+                gemm_batched(_per_kv(dattn, rows, 0, kv, group, h, dh), V.transpose(1, 2), out=dP[:, h],
+                             causal_first=0)
+        with torch.cuda.stream(sv):
+            for h in range(group):
+                # dV = sum over the group's heads, in head order, of P_h^T dO_h;
+                # row i of P^T is +0 before k = i
+                gemm_batched(P[:, h].transpose(1, 2), _per_kv(dattn, rows, 0, kv, group, h, dh), out=dV,
+                             residual=dV if h else None, k_lo=0)
+        with torch.cuda.stream(sp):
+            dS = dP.view(kv * group * S, S)
+            softmax_backward(P.view(kv * group * S, S), dS, out=dS, causal_first=0, causal_period=S)
+        if streams is not None:
+            for st in list(sq) + [sk]:
+                _after(st, sp)
+        for h in range(group):
+            with torch.cuda.stream(sq[h]):
+                gemm_batched(dP[:, h], K, out=_per_kv(dqkv, rows, 0, kv, group, h, dh), alpha=scale, k_hi=0)
+        with torch.cuda.stream(sk):
+            for h in range(group):
+                # dK = sum over the group's heads, in head order, of s dS_h^T Q_h
+                gemm_batched(dP[:, h].transpose(1, 2), _per_kv(qkv, rows, 0, kv, group, h, dh), out=dK,
+                             alpha=scale, residual=dK if h else None, k_lo=0)
+        if streams is not None:
+            used = [sp, sv, sk] + list(sq)
+            joined += used
+    if streams is not None:
+        _after(main, *joined)
+
+
 def backward_workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
     e = dict(dtype=torch.float32, device=device)
     group, S = cfg.heads // cfg.kv_heads, cfg.seq_len
+    seqs = tokens // S
     return {"t_ffn": torch.empty(tokens, cfg.ffn, **e), "t_d": torch.empty(tokens, cfg.d, **e),
             "t_d2": torch.empty(tokens, cfg.d, **e), "dqkv": torch.empty(tokens, cfg.qkv_width, **e),
-            "dp": torch.empty(cfg.kv_heads, group, S, S, **e), "rope": rope_tables(cfg, device)}
+            "dp": torch.empty(seqs * cfg.kv_heads, group, S, S, **e), "rope": rope_tables(cfg, device),
+            "streams": side_streams(cfg, tokens, device)}
 
 
 def workspace(cfg: DecoderConfig, tokens: int, device) -> dict:
     e = dict(dtype=torch.float32, device=device)
     group = cfg.heads // cfg.kv_heads
+    seqs = tokens // cfg.seq_len
     out = {"h": torch.empty(tokens, cfg.d, **e), "qkv": torch.empty(tokens, cfg.qkv_width, **e),
            "attn": torch.empty(tokens, cfg.d, **e), "a": torch.empty(tokens, cfg.ffn, **e),
-           "scores": torch.empty(cfg.kv_heads, group, cfg.seq_len, cfg.seq_len, **e),
-           "tmp_d": torch.empty(tokens, cfg.d, **e), "rope": rope_tables(cfg, device)}
+           "scores": torch.empty(seqs * cfg.kv_heads, group, cfg.seq_len, cfg.seq_len, **e),
+           "tmp_d": torch.empty(tokens, cfg.d, **e), "rope": rope_tables(cfg, device),
+           "streams": side_streams(cfg, tokens, device)}
     if cfg.mlp == "swiglu":
         out["gu"] = torch.empty(tokens, 2 * cfg.ffn, **e)
     return out
