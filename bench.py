@@ -19,6 +19,7 @@ the elapsed time -- the path has no exchange step.
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -578,8 +579,10 @@ def run_sweep_gemm(dev, s, flush, peak):
 def run_sweep_rowops(dev, s, flush, hbm):
     """The order-fixed row operators on decoder-sized tensors: LayerNorm and
     RMSNorm over 16 x 4096 tokens x 2048, GeLU over 4096 x 8192 activations,
-    softmax over 8 heads of 4096 x 4096 scores.  Bytes = one read of x and one
-    write of y (HBM roofline); the L2 is flushed before each launch."""
+    softmax (plain, causal, causal backward) over 8 heads of 4096 x 4096
+    scores, SwiGLU and its backward over 4096 x 8192, the rotary embedding of
+    a 4096-token qkv matrix.  Bytes = the algorithmic reads and writes (HBM
+    roofline); the L2 is flushed before each launch."""
     def ev_time(fn, reps=5):
         with torch.cuda.stream(s):
             fn()
@@ -615,7 +618,33 @@ def run_sweep_rowops(dev, s, flush, hbm):
     S = inputs.normal((8 * T, T), 3.0, 104, dev)
     P = torch.empty_like(S)
     emit("softmax rows 8 x 4096 x 4096", 2 * S.numel() * 4, ev_time(lambda: rp.softmax_rows(S, out=P, stream=s)))
-    del S, P
+    # the causal forms read and write each row's prefix only (the rest of the
+    # output is written as +0): bytes = 2 x 4 x the prefix elements + 4 x the rest
+    n, rows = T, 8 * T
+    pre = rows // n * (n * (n + 1) // 2)
+    causal_bytes = 8 * pre + 4 * (S.numel() - pre)
+    emit("causal softmax rows 8 x 4096 x 4096", causal_bytes,
+         ev_time(lambda: rp.softmax_rows(S, out=P, causal_first=0, causal_period=T, stream=s)))
+    dP = inputs.normal((8 * T, T), 1.0, 105, dev)
+    emit("causal softmax backward 8 x 4096 x 4096", 12 * pre + 4 * (S.numel() - pre),
+         ev_time(lambda: rp.softmax_backward(P, dP, out=S, causal_first=0, causal_period=T, stream=s)))
+    del S, P, dP
+    # the Llama layer's element-wise operators at decoder sizes: SwiGLU over
+    # [g | u] of 4096 x 2 x 8192, its backward, the rotary embedding of the 40
+    # query and key heads of a 4096 x 3072 qkv matrix
+    GU = inputs.normal((T, 8 * D), 2.0, 106, dev)
+    A = torch.empty(T, 4 * D, device=dev)
+    emit("swiglu 4096 x 8192 (reads g, u; writes h)", 3 * A.numel() * 4,
+         ev_time(lambda: rp.swiglu(GU[:, :4 * D], GU[:, 4 * D:], out=A, stream=s)))
+    DG, DU = torch.empty_like(A), torch.empty_like(A)
+    emit("swiglu backward 4096 x 8192 (reads g, u, dh; writes dg, du)", 5 * A.numel() * 4,
+         ev_time(lambda: rp.swiglu_backward(GU[:, :4 * D], GU[:, 4 * D:], A, dg=DG, du=DU, stream=s)))
+    del GU, A, DG, DU
+    Q = inputs.normal((T, 3 * D // 2), 1.0, 107, dev)
+    cos, sin = rp.rope_table(T, rp.rope_frequencies(32, math.log(500000.0), dev))
+    emit("rotary 4096 x 40 heads of 64 (in place)", 2 * T * 40 * 64 * 4,
+         ev_time(lambda: rp.rope(Q, 40, cos, sin, stream=s)))
+    del Q
 
 
 def run_sweep_decoder(dev, s, flush, peak):

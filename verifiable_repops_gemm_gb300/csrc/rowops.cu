@@ -305,22 +305,11 @@ struct Square {
 template <int T, int R>
 __global__ void __launch_bounds__(T)
 softmax_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx, float *__restrict__ y,
-                    int64_t ldy, int64_t first, int64_t period) {
+                    int64_t ldy) {
     __shared__ float gbuf[2][RUN];
     int phase = 0;
     const int runs = int((n + RUN - 1) / RUN);
-    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr, int64_t row) {
-        if (first >= 0) {
-            // causal: scores past position first + row become -inf, so their
-            // exp is +0; adding +0 to a sum of non-negative terms changes no
-            // bit, and the result is the softmax of the prefix, then +0
-            const int64_t L = first + row % period + 1;
-#pragma unroll
-            for (int j = 0; j < R; ++j)
-#pragma unroll
-                for (int i = 0; i < RUN; ++i)
-                    if (int64_t(threadIdx.x + j * T) * RUN + i >= L) rr.v[j][i] = -__int_as_float(0x7f800000);
-        }
+    for_each_row<T, R>(rows, n, x, ldx, y, ldy, [&](RowRuns<T, R> &rr, int64_t) {
         const float m = rr.template reduce<Op::Max>(Ident(), gbuf, phase, runs);
         // element-wise steps need no guard: values past the row end are never
         // folded or stored
@@ -334,6 +323,63 @@ softmax_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_
 #pragma unroll
             for (int i = 0; i < RUN; ++i) rr.v[j][i] = __fmul_rn(rr.v[j][i], inv);
     });
+}
+
+// Causal softmax: row r is the softmax of its prefix of L = min(n, first +
+// (r mod period) + 1) values (the max and sum trees over those L values), then
+// +0.  Only the prefix is copied in and only its exponentials are computed;
+// the row loop is for_each_row's with the copy-in cut at L.
+template <int T, int R>
+__global__ void __launch_bounds__(T)
+softmax_causal_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
+                           float *__restrict__ y, int64_t ldy, int64_t first, int64_t period) {
+    extern __shared__ float4 stage_mem[];
+    __shared__ float gbuf[2][RUN];
+    int phase = 0;
+    constexpr bool PF = kPrefetch<T, R>;
+    float4 *in = stage_mem;
+    float4 *out = PF ? stage_mem + T * R * RUN / 4 : stage_mem;
+    auto prefix = [&](int64_t r) { return imin64(n, first + r % period + 1); };
+    int64_t row = blockIdx.x;
+    if (row < rows) stage_in<T, R>(in, x + row * ldx, prefix(row));
+    cp_async_commit();
+    for (; row < rows; row += gridDim.x) {
+        const int64_t next = row + gridDim.x;
+        const int64_t L = prefix(row);
+        cp_async_wait<0>();
+        __syncwarp();
+        RowRuns<T, R> rr;
+        read_stage(rr, in, L);
+        if constexpr (PF) {
+            __syncwarp();                       // every lane has its run before `in` is refilled
+            if (next < rows) stage_in<T, R>(in, x + next * ldx, prefix(next));
+            cp_async_commit();
+        }
+        const int runs = int((L + RUN - 1) / RUN);
+        const float m = rr.template reduce<Op::Max>(Ident(), gbuf, phase, runs);
+#pragma unroll
+        for (int j = 0; j < R; ++j)
+#pragma unroll
+            for (int i = 0; i < RUN; ++i)
+                if (i < rr.len[j]) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+        const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs));
+#pragma unroll
+        for (int j = 0; j < R; ++j) {
+            const int64_t s0 = int64_t(threadIdx.x + j * T) * RUN;
+#pragma unroll
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = i < rr.len[j] ? __fmul_rn(rr.v[j][i], inv) : 0.0f;
+            rr.len[j] = s0 < n ? int(imin64(RUN, n - s0)) : 0;      // the whole row is written
+        }
+        write_stage(rr, out);
+        __syncwarp();
+        stage_out<T, R>(out, y + row * ldy, n);
+        __syncwarp();                           // `out` read back before it is written again
+        if constexpr (!PF) {
+            if (next < rows) stage_in<T, R>(in, x + next * ldx, prefix(next));
+            cp_async_commit();
+        }
+    }
+    cp_async_wait<0>();
 }
 
 // psm: gamma and beta are staged in shared memory (aligned, and they fit).
@@ -711,9 +757,11 @@ int launch_fast(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, 
                 cudaStream_t s) {
     const int pvec = reinterpret_cast<uintptr_t>(gamma) % 16 == 0 && reinterpret_cast<uintptr_t>(beta) % 16 == 0;
     const size_t smem = kStageBytes<T, R>;
+    if (kind == 0 && first >= 0)
+        return launch_persistent(softmax_causal_rows_kernel<T, R>, T, smem, rows, s, rows, n, x, ldx, y, ldy,
+                                 first, period);
     if (kind == 0)
-        return launch_persistent(softmax_rows_kernel<T, R>, T, smem, rows, s, rows, n, x, ldx, y, ldy, first,
-                                 period);
+        return launch_persistent(softmax_rows_kernel<T, R>, T, smem, rows, s, rows, n, x, ldx, y, ldy);
     if (kind == 1) {
         const size_t p = pvec ? kParamBytes<T, R, 2> : 0;
         return launch_persistent(layernorm_rows_kernel<T, R>, T, smem + p, rows, s, rows, n, x, ldx, gamma, beta,
