@@ -512,6 +512,8 @@ def run_sweep(args):
         run_sweep_halfstore(dev, s, flush, peak, peaks.get("hbm_gbs", 6800.0))
     if args.sweep in ("all", "train"):
         run_sweep_train(dev, s, flush, peak)
+    if args.sweep == "decoder_step":
+        run_decoder_step(dev, s, peak)
 
 
 def run_sweep_gemm(dev, s, flush, peak):
@@ -719,6 +721,39 @@ def run_sweep_decoder(dev, s, flush, peak):
         del saved, bws, ws, w
 
 
+def run_decoder_step(dev, s, peak):
+    """Exactly two training steps of the Llama layer (forward keeping the
+    activations, then the backward pass), 2 x 2048 tokens: a short program whose
+    every kernel launch a profiler can list (the first step warms up, the
+    second is the one to read).  Not part of "all"."""
+    from verifiable_repops_gemm_gb300 import decoder
+    cfg = decoder.DecoderConfig()
+    T = 2 * cfg.seq_len
+    w = decoder.init_weights(cfg, 300, dev)
+    ws = decoder.workspace(cfg, T, dev)
+    saved = decoder.activations(cfg, T, dev)
+    bws = decoder.backward_workspace(cfg, T, dev)
+    x0 = inputs.normal((T, cfg.d), 1.0, 301, dev)
+    dy0 = inputs.normal((T, cfg.d), 1e-2, 302, dev)
+    x, dy = torch.empty_like(x0), torch.empty_like(dy0)
+    ms = []
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            x.copy_(x0)
+            dy.copy_(dy0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            decoder.forward(x, w, cfg, work=ws, save=saved)
+            decoder.backward(dy, w, cfg, saved, work=bws)
+            e1.record(s)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+    flops = 3 * cfg.flops(T)
+    print(json.dumps({"sweep": "llama layer training step, 2 steps", "tokens": T, "ms": ms,
+                      "tflops": flops / ms[-1] / 1e9, "frac_of_fp32_peak": flops / ms[-1] / 1e9 / peak}),
+          flush=True)
+
+
 def run_sweep_train(dev, s, flush, peak):
     """The verifiable training step end to end: 4 contributors (DIDs), each
     with 2 x 2048 tokens through 2 Llama-3.2-1B-sized decoder layers (rotary,
@@ -890,7 +925,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
-                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore", "train"),
+                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore", "train",
+                             "decoder_step"),
                     help="time every workload of a part (one JSON line each) instead of the step")
     args = ap.parse_args()
     if args.sweep:

@@ -48,7 +48,8 @@ def test_gelu_backward_matches_oracle(rp, orc, n):
     assert np.array_equal(u32(d2.cpu().numpy()), u32(want))
 
 
-@pytest.mark.parametrize("rows,cols", [(5, 1), (5, 33), (64, 2048), (3, 8193), (2, 40000)])
+@pytest.mark.parametrize("rows,cols", [(5, 1), (5, 33), (7, 100), (64, 2048), (33, 4092), (9, 8192), (3, 8193),
+                                       (2, 40000)])
 def test_rmsnorm_backward_matches_oracle(rp, orc, rows, cols):
     x = inputs.normal((rows, cols), 1.0, 400 + cols, DEV)
     g = inputs.normal((cols,), 1.0, 401, DEV)

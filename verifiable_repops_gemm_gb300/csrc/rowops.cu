@@ -621,6 +621,64 @@ rmsnorm_backward_kernel(int64_t rows, int64_t n, const float *__restrict__ x, in
     }
 }
 
+// RMSNorm backward on aligned rows of up to 8192 values, the operations of
+// rmsnorm_backward_kernel in the same order: each warp stages its runs of
+// the x, dy (and res) rows (coalesced 16-byte copies, swizzled) and gamma once
+// per CTA; the two tree reductions fold registers and shuffles; dx and dy*xh
+// leave through the x and dy stages.  res may be dx (its row is staged
+// before dx is written).
+template <int T>
+__global__ void __launch_bounds__(T)
+rmsnorm_backward_staged_kernel(int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma, float eps,
+                               const float *dy, int64_t lddy, const float *res, int64_t ldres, float *dx,
+                               int64_t lddx, float *p, int64_t ldp) {
+    extern __shared__ float4 stage_mem[];
+    __shared__ float gbuf[2][RUN];
+    int phase = 0;
+    constexpr int Q = T * RUN / 4;                     // float4 slots per stage
+    float4 *sx = stage_mem, *sd = sx + Q, *sg = sd + Q, *sr = sg + Q;
+    const int runs = int((n + RUN - 1) / RUN);
+    const float nf = float(n);
+    if (blockIdx.x < rows) stage_in<T, 1>(sg, gamma, n);   // waited for with the first row
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+        stage_in<T, 1>(sx, x + row * ldx, n);
+        stage_in<T, 1>(sd, dy + row * lddy, n);
+        if (res) stage_in<T, 1>(sr, res + row * ldres, n);
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+        RowRuns<T, 1> a, b;
+        read_stage(a, sx, n);
+        read_stage(b, sd, n);
+        const float ms = __fdiv_rn(a.template reduce<Op::Sum>(Square(), gbuf, phase, runs), nf);
+        const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
+        float g[RUN];
+        read_param_run<T, 1>(sg, threadIdx.x, g);
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) b.v[0][i] = __fmul_rn(__fmul_rn(b.v[0][i], g[i]), __fmul_rn(a.v[0][i], inv));
+        const float c = __fdiv_rn(b.template reduce<Op::Sum>(Ident(), gbuf, phase, runs), nf);
+        read_stage(b, sd, n);                          // dy again
+        float r[RUN];
+        if (res) read_param_run<T, 1>(sr, threadIdx.x, r);
+#pragma unroll
+        for (int i = 0; i < RUN; ++i) {
+            const float xh = __fmul_rn(a.v[0][i], inv), gy = __fmul_rn(b.v[0][i], g[i]);
+            float d = __fmul_rn(inv, __fsub_rn(gy, __fmul_rn(xh, c)));
+            if (res) d = __fadd_rn(d, r[i]);
+            a.v[0][i] = d;
+            b.v[0][i] = __fmul_rn(b.v[0][i], xh);
+        }
+        __syncwarp();                                  // every lane has read its stages before they are rewritten
+        write_stage(a, sx);
+        write_stage(b, sd);
+        __syncwarp();
+        stage_out<T, 1>(sx, dx + row * lddx, n);
+        stage_out<T, 1>(sd, p + row * ldp, n);
+        __syncwarp();
+    }
+    cp_async_wait<0>();
+}
+
 // Values of row r a causal softmax (first, period) saw: all n when first < 0.
 __device__ __forceinline__ int64_t causal_prefix(int64_t r, int64_t n, int64_t first, int64_t period) {
     return first < 0 ? n : imin64(n, first + r % period + 1);
@@ -907,6 +965,18 @@ extern "C" int repops_rmsnorm_backward_f32(int64_t rows, int64_t cols, const flo
             return REPOPS_ERR_ALIAS;
     }
     const int64_t runs = (cols + RUN - 1) / RUN;
+    const bool staged = runs <= 256 && rows_vec_ok(x, ldx, dx, lddx) && rows_vec_ok(dy, lddy, dyxh, ldp) &&
+                        reinterpret_cast<uintptr_t>(gamma) % 16 == 0 && (!res || rows_vec_ok(res, ldres, dx, lddx));
+    if (staged) {
+        auto go = [&](auto kern, int T) {
+            return launch_persistent(kern, T, size_t(4) * T * RUN * sizeof(float), rows, stream, rows, cols, x, ldx,
+                                     gamma, eps, dy, lddy, res, ldres, dx, lddx, dyxh, ldp);
+        };
+        if (runs <= 32) return go(rmsnorm_backward_staged_kernel<32>, 32);
+        if (runs <= 64) return go(rmsnorm_backward_staged_kernel<64>, 64);
+        if (runs <= 128) return go(rmsnorm_backward_staged_kernel<128>, 128);
+        return go(rmsnorm_backward_staged_kernel<256>, 256);
+    }
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(rmsnorm_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
