@@ -124,7 +124,7 @@ def lib():
         L.oracle_softmax_backward.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64]
         L.oracle_gemm_batched.restype = None
         L.oracle_gemm_batched.argtypes = [i32, i32, i64, i64, i64, i64, vp, i64, i64, vp, i64, i64,
-                                          vp, i64, i64, f32, vp, i32, vp, i64, i64, i64, i64]
+                                          vp, i64, i64, f32, vp, i32, vp, i64, i64, i64, i64, i64]
         L.oracle_softmax_backward_causal.restype = None
         L.oracle_softmax_backward_causal.argtypes = [i64, i64, vp, i64, vp, i64, vp, i64, i64, i64]
         L.oracle_silu.restype = f32
@@ -391,11 +391,12 @@ ACT_NONE, ACT_GELU = 0, 1
 
 def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, strideB,
                  C, ldc, strideC, alpha=1.0, bias=None, act=ACT_NONE, R=None, ldr=0, strideR=0,
-                 k_lo=-1, k_hi=-1):
+                 k_lo=-1, k_hi=-1, b_group=1):
     """Batched GEMM with the fused epilogue, on flat float32 buffers (element
     offsets and strides exactly as the library's batched entry point takes
     them).  C is written in place; R may be C itself.  k_lo / k_hi >= 0
-    restrict row i's k-chain to [i - k_lo, i + k_hi] (see the C source)."""
+    restrict row i's k-chain to [i - k_lo, i + k_hi]; b_group > 1 lets
+    b_group consecutive batches share one B (see the C source)."""
     L = lib()
     for X in (A, B, C) + tuple(x for x in (bias, R) if x is not None):
         if X.dtype != np.float32 or not X.flags.c_contiguous:
@@ -403,7 +404,7 @@ def gemm_batched(transA, transB, batch, M, N, K, A, lda, strideA, B, ldb, stride
     L.oracle_gemm_batched(int(bool(transA)), int(bool(transB)), batch, M, N, K,
                           _ptr(A), lda, strideA, _ptr(B), ldb, strideB, _ptr(C), ldc, strideC,
                           float(alpha), _ptr(bias) if bias is not None else None, int(act),
-                          _ptr(R) if R is not None else None, ldr, strideR, int(k_lo), int(k_hi))
+                          _ptr(R) if R is not None else None, ldr, strideR, int(k_lo), int(k_hi), int(b_group))
     return C
 
 

@@ -727,18 +727,22 @@ void oracle_rmsnorm_rows(int64_t rows, int64_t cols, const float *x, int64_t ldx
  * k_lo >= 0 the k-chain of row i starts at k = max(0, i - k_lo); when
  * k_hi >= 0 it ends at k = min(K - 1, i + k_hi); -1 leaves that side open.
  * The chain still starts from +0 and runs with k increasing; a row whose
- * window is empty gets the epilogue of +0. */
+ * window is empty gets the epilogue of +0.
+ *
+ * b_group >= 1: batch b takes B_(b / b_group) = B + (b / b_group)*strideB
+ * (integer division): consecutive batches share one B, as the query heads of
+ * a grouped-query attention group share their key/value head. */
 void oracle_gemm_batched(int transA, int transB, int64_t batch, int64_t M, int64_t N, int64_t K,
                          const float *A, int64_t lda, int64_t strideA,
                          const float *B, int64_t ldb, int64_t strideB,
                          float *C, int64_t ldc, int64_t strideC,
                          float alpha, const float *bias, int act,
                          const float *R, int64_t ldr, int64_t strideR,
-                         int64_t k_lo, int64_t k_hi)
+                         int64_t k_lo, int64_t k_hi, int64_t b_group)
 {
     for (int64_t b = 0; b < batch; ++b) {
         const float *Ab = A + b * strideA;
-        const float *Bb = B + b * strideB;
+        const float *Bb = B + (b / b_group) * strideB;
         float *Cb = C + b * strideC;
         const float *Rb = R ? R + b * strideR : NULL;
         for (int64_t i = 0; i < M; ++i) {

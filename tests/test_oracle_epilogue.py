@@ -20,8 +20,9 @@ def elem(buf, off):
 
 
 def ref_batched(orc, transA, transB, batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC,
-                alpha, bias, act, R, ldr, sR):
-    """Element-by-element restatement; returns the new contents of C."""
+                alpha, bias, act, R, ldr, sR, group=1):
+    """Element-by-element restatement; returns the new contents of C.  Batch
+    b reads the B of batch b // group."""
     out = C.copy()
     old = C.copy()                       # an in-place residual reads the old C
     src_R = old if R is C else R
@@ -31,7 +32,7 @@ def ref_batched(orc, transA, transB, batch, M, N, K, A, lda, sA, B, ldb, sB, C, 
                 s = 0.0
                 for k in range(K):
                     a = elem(A, b * sA + (k * lda + i if transA else i * lda + k))
-                    w = elem(B, b * sB + (j * ldb + k if transB else k * ldb + j))
+                    w = elem(B, (b // group) * sB + (j * ldb + k if transB else k * ldb + j))
                     s = fx.add(s, fx.mul(a, w))
                 y = fx.mul(s, float(np.float32(alpha)))
                 if bias is not None:
@@ -88,6 +89,22 @@ def test_batched_epilogue_exact_rational(orc, transA, transB, kind):
         orc.gemm_batched(transA, transB, batch, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, alpha,
                          bias if with_bias else None, act, R if with_R else None, ldc, sC)
         assert [fx.bits(float(v)) for v in C] == [fx.bits(float(v)) for v in want]
+
+
+@pytest.mark.parametrize("group,transB", [(2, 0), (3, 1), (6, 0)])
+def test_grouped_b_exact_rational(orc, group, transB):
+    # six batches whose B is shared by `group` consecutive ones (grouped-query
+    # attention: the query heads of a group share one key/value head)
+    rng = np.random.default_rng(40 + group + transB)
+    batch, M, N, K = 6, 3, 4, 5
+    br, bc = (N, K) if transB else (K, N)
+    nb = -(-batch // group)
+    A, B = wide(rng, batch * M * K), wide(rng, nb * br * bc)
+    C = np.zeros(batch * M * N, np.float32)
+    want = ref_batched(orc, 0, transB, batch, M, N, K, A, K, M * K, B, bc, br * bc, C, N, M * N,
+                       0.5, None, 0, None, N, M * N, group=group)
+    orc.gemm_batched(0, transB, batch, M, N, K, A, K, M * K, B, bc, br * bc, C, N, M * N, 0.5, b_group=group)
+    assert [fx.bits(float(v)) for v in C] == [fx.bits(float(v)) for v in want]
 
 
 def test_in_place_residual(orc):

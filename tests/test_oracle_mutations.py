@@ -96,6 +96,8 @@ MUTATIONS = {
     "batched: A advanced by B's stride": ("const float *Ab = A + b * strideA;", "const float *Ab = A + b * strideB;"),
     "window: one k past the upper band": ("if (k_hi >= 0 && i + k_hi + 1 < k1) k1 = i + k_hi + 1;",
                                           "if (k_hi >= 0 && i + k_hi + 2 < k1) k1 = i + k_hi + 2;"),
+    "batched: B group ignored": ("const float *Bb = B + (b / b_group) * strideB;",
+                                 "const float *Bb = B + b * strideB;"),
     "window: lower band ignored": ("if (k_lo >= 0 && i - k_lo > k0) k0 = i - k_lo;", ""),
     "causal softmax backward: one entry too many": ("int64_t seen = first + (i % period) + 1;",
                                                     "int64_t seen = first + (i % period) + 2;"),
