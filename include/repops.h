@@ -233,9 +233,13 @@ int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
  * k rows the tile reads -- as for a causal softmax output (+0 past each
  * row's prefix) times finite values.  The caller guarantees that; otherwise
  * the rows concerned are unspecified.
+ * b_group >= 1: batch b reads B_(b / b_group) = B + (b / b_group)*strideB,
+ * so b_group consecutive batches share one B (the query heads of a
+ * grouped-query attention group and their key/value head); 1 is the plain
+ * batched form.
  * Errors: INVALID_ARG (negative size or stride, bad leading dim, null
  * pointer with a non-empty operand, act not NONE/GELU, causal_first, k_lo or
- * k_hi < -1, spans that overflow); ALIAS; UNSUPPORTED (batch > 65535, or
+ * k_hi < -1, b_group < 1, spans that overflow); ALIAS; UNSUPPORTED (batch > 65535, or
  * loader TMA when TMA cannot serve the operands); CUDA. */
 int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
                             int64_t batch, int64_t M, int64_t N, int64_t K,
@@ -245,7 +249,7 @@ int repops_gemm_f32_batched(int config, int loader, int transA, int transB,
                             float alpha, const float *bias, int act,
                             const float *R, int64_t ldr, int64_t strideR,
                             int64_t causal_first, int64_t k_lo, int64_t k_hi,
-                            cudaStream_t stream);
+                            int64_t b_group, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Contributor order                                                         */

@@ -215,10 +215,10 @@ def test_row_operators_reject_bad_arguments(L):
 
 def _bat(L, batch=2, M=4, N=4, K=4, A=FAKE_A, lda=4, sA=16, B=FAKE_B, ldb=4, sB=16, C=FAKE_C, ldc=4,
          sC=16, alpha=1.0, bias=None, act=0, R=None, ldr=4, sR=16, config=-1, loader=0, tA=0, tB=0,
-         causal=-1, k_lo=-1, k_hi=-1):
+         causal=-1, k_lo=-1, k_hi=-1, b_group=1):
     return L.repops_gemm_f32_batched(config, loader, tA, tB, batch, M, N, K, A, lda, sA, B, ldb, sB,
                                      C, ldc, sC, ctypes.c_float(alpha), bias, act, R, ldr, sR, causal, k_lo, k_hi,
-                                     None)
+                                     b_group, None)
 
 
 def test_batched_gemm_rejects_bad_arguments(L):
@@ -227,6 +227,7 @@ def test_batched_gemm_rejects_bad_arguments(L):
     assert _bat(L, act=2) == -1                                    # unknown activation
     assert _bat(L, causal=-2) == -1
     assert _bat(L, k_lo=-2) == -1 and _bat(L, k_hi=-5) == -1                 # k window bounds
+    assert _bat(L, b_group=0) == -1
     assert _bat(L, ldc=3) == -1
     assert _bat(L, R=FAKE_B + 4096, ldr=3) == -1                   # residual ld < N
     assert _bat(L, config=99) == -1

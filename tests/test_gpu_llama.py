@@ -57,6 +57,30 @@ def test_band_gemms_every_config(rp, orc, config, loader):
     assert np.array_equal(bits(got_t), u32(want_t))
 
 
+@pytest.mark.parametrize("config,loader", list(itertools.product(range(5), (1, 2))))
+def test_grouped_b_every_config(rp, orc, config, loader):
+    # 6 query heads over 2 key/value heads (groups of 3): Q K^T with K^T a
+    # transposed view, then P V over the band k <= i
+    H, G, S, d = 6, 3, 136, 64
+    Q = inputs.normal((H, S, d), 1.0, 60, "cpu").numpy()
+    K = inputs.normal((H // G, S, d), 1.0, 61, "cpu").numpy()
+    Cs = np.zeros(H * S * S, F32)
+    orc.gemm_batched(0, 1, H, S, S, d, Q.reshape(-1), d, S * d, K.reshape(-1), d, S * d, Cs, S, S * S, 0.125,
+                     b_group=G)
+    Kd = torch.from_numpy(K).to(DEV)
+    got = rp.gemm_batched(torch.from_numpy(Q).to(DEV), Kd.transpose(1, 2), alpha=0.125, config=config,
+                          loader=loader)
+    assert np.array_equal(bits(got), u32(Cs.reshape(H, S, S)))
+    P = np.stack([orc.softmax_rows_causal(Cs.reshape(H, S, S)[h], 0) for h in range(H)])
+    V = inputs.normal((H // G, S, d), 1.0, 62, "cpu").numpy()
+    Co = np.zeros(H * S * d, F32)
+    orc.gemm_batched(0, 0, H, S, d, S, P.reshape(-1), S, S * S, V.reshape(-1), d, S * d, Co, d, S * d,
+                     k_hi=0, b_group=G)
+    got_o = rp.gemm_batched(torch.from_numpy(P).to(DEV), torch.from_numpy(V).to(DEV), k_hi=0, config=config,
+                            loader=loader)
+    assert np.array_equal(bits(got_o), u32(Co.reshape(H, S, d)))
+
+
 def test_band_matches_the_oracle_window_with_epilogue(rp, orc):
     # the oracle's own window (chain over the band only) with alpha and an
     # in-place residual, and rows whose window is empty (k_lo with M > K)

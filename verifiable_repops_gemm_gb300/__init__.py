@@ -129,7 +129,9 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
     y = alpha*acc, + bias[j], GeLU (act=ACT_GELU), + residual[b][i][j], each one
     binary32 rounding (repops_gemm_f32_batched).
 
-    A: (batch, M, K) or (M, K) shared; B: (batch, K, N) or (K, N) shared; every
+    A: (batch, M, K) or (M, K) shared; B: (batch, K, N), (K, N) shared, or
+    (batch / g, K, N) with each B shared by g consecutive batches (the query
+    heads of a grouped-query attention group and their key/value head); every
     matrix row-major or a transposed view, batches at any stride (attention
     heads as column blocks: X.view(T, H, d).transpose(0, 1)).  out: (batch, M,
     N) or (M, N), unit column stride, batches stacked or interleaved.
@@ -146,10 +148,12 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
     K2, N = B.shape[-2:]
     if K != K2:
         raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
-    sizes = {x for x in (ba, bb) if x is not None}
-    if len(sizes) > 1:
-        raise ValueError("A and B have different batch sizes")
-    batch = sizes.pop() if sizes else None
+    group = 1
+    if ba is not None and bb is not None and ba != bb:
+        if bb == 0 or ba % bb:
+            raise ValueError("B's batch count must equal A's or divide it")
+        group = ba // bb
+    batch = ba if ba is not None else bb
     if out is None:
         shape = (M, N) if batch is None else (batch, M, N)
         out = torch.empty(shape, dtype=torch.float32, device=A.device)
@@ -175,7 +179,8 @@ def gemm_batched(A, B, out=None, *, alpha: float = 1.0, bias=None, act: int = AC
         pbias = bias.data_ptr()
     rc = L.repops_gemm_f32_batched(config, loader, ta, tb, nb, M, N, K, pa, lda, sa, pb, ldb, sb,
                                    out.data_ptr(), ldc, sc, ctypes.c_float(alpha), pbias, int(act),
-                                   pr, ldr, sr, int(causal_first), int(k_lo), int(k_hi), _stream_handle(stream))
+                                   pr, ldr, sr, int(causal_first), int(k_lo), int(k_hi), group,
+                                   _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32_batched")
     return out
 

@@ -79,7 +79,8 @@ SIGNATURES = {
     "repops_softmax_rows_causal_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp]),
     "repops_gemm_f32_batched": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _i64,
                                        _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,
-                                       ctypes.c_float, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _vp]),
+                                       ctypes.c_float, _vp, _i32, _vp, _i64, _i64, _i64, _i64, _i64, _i64,
+                                       _vp]),
 }
 
 ACT_NONE, ACT_GELU = 0, 1

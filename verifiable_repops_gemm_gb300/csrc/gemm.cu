@@ -329,9 +329,10 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
                           int64_t K, const float *A, int64_t lda, int64_t strideA, const float *B, int64_t ldb,
                           int64_t strideB, float *C, int64_t ldc, int64_t strideC, float alpha,
                           const float *bias, int act, const float *R, int64_t ldr, int64_t strideR,
-                          int64_t causal_first, int64_t k_lo, int64_t k_hi, cudaStream_t stream) {
+                          int64_t causal_first, int64_t k_lo, int64_t k_hi, int64_t b_group,
+                          cudaStream_t stream) {
     if (batch < 0 || M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
-    if (causal_first < -1 || k_lo < -1 || k_hi < -1) return REPOPS_ERR_INVALID_ARG;
+    if (causal_first < -1 || k_lo < -1 || k_hi < -1 || b_group < 1) return REPOPS_ERR_INVALID_ARG;
     if (strideA < 0 || strideB < 0 || strideC < 0 || strideR < 0) return REPOPS_ERR_INVALID_ARG;
     if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
     if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC)
@@ -350,7 +351,8 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     if (!operand_span(a_rows, a_cols, lda, &a1) || !operand_span(b_rows, b_cols, ldb, &b1) ||
         !operand_span(M, N, ldc, &c1) || (R && !operand_span(M, N, ldr, &r1)))
         return REPOPS_ERR_INVALID_ARG;
-    if (!batched_span(batch, strideA, a1, &a_bytes) || !batched_span(batch, strideB, b1, &b_bytes) ||
+    const int64_t b_mats = (batch + b_group - 1) / b_group;   // distinct B matrices read
+    if (!batched_span(batch, strideA, a1, &a_bytes) || !batched_span(b_mats, strideB, b1, &b_bytes) ||
         !batched_span(batch, strideC, c1, &c_bytes) || (R && !batched_span(batch, strideR, r1, &r_bytes)))
         return REPOPS_ERR_INVALID_ARG;
     // The batches' outputs must not overlap one another: either stacked (each
@@ -378,7 +380,8 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     p.ex = true;
     p.batch = batch;
     p.strideA = batch > 1 ? strideA : 0;
-    p.strideB = batch > 1 ? strideB : 0;
+    p.strideB = b_mats > 1 ? strideB : 0;
+    p.b_group = b_mats > 1 ? b_group : 1;
     p.strideC = batch > 1 ? strideC : 0;
     p.alpha = alpha;
     p.bias = bias;
@@ -482,10 +485,10 @@ extern "C" int repops_gemm_f32_batched(int config, int loader, int transA, int t
                                        float *C, int64_t ldc, int64_t strideC, float alpha,
                                        const float *bias, int act, const float *R, int64_t ldr,
                                        int64_t strideR, int64_t causal_first, int64_t k_lo, int64_t k_hi,
-                                       cudaStream_t stream) {
+                                       int64_t b_group, cudaStream_t stream) {
     return gemm_dispatch_batched(config, loader, transA, transB, batch, M, N, K, A, lda, strideA, B, ldb,
                                  strideB, C, ldc, strideC, alpha, bias, act, R, ldr, strideR, causal_first,
-                                 k_lo, k_hi, stream);
+                                 k_lo, k_hi, b_group, stream);
 }
 
 namespace {

@@ -31,6 +31,7 @@ struct GemmProblem {
     int64_t causal = -1;   // >= 0: tiles wholly above j = causal + i are skipped
     int64_t k_lo = -1;     // >= 0: row i's k-chain starts at max(0, i - k_lo)
     int64_t k_hi = -1;     // >= 0: row i's k-chain ends at min(K - 1, i + k_hi)
+    int64_t b_group = 1;   // batch b reads B_(b / b_group)
 };
 
 struct GemmConfigInfo {

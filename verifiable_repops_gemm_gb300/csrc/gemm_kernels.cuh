@@ -302,6 +302,7 @@ struct ExArgs {
     int64_t ldr, sR;
     int64_t causal;        // >= 0: a tile wholly above j = causal + i is skipped
     int64_t k_lo, k_hi;    // >= 0: row i's k-chain covers [i - k_lo, i + k_hi] only
+    int b_group;           // batch b reads B_(b / b_group)
 };
 
 // True when every element (i, j) of the tile has j > causal + i: the tile is
@@ -450,7 +451,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 const int bx = B_KIN ? k0 : int(n0), by = B_KIN ? int(n0) : k0;
                 if (EX && ep.zA) tma_load_3d(As, &tmA, &full[s], ax, ay, int(blockIdx.y));
                 else             tma_load_2d(As, &tmA, &full[s], ax, ay);
-                if (EX && ep.zB) tma_load_3d(Bs, &tmB, &full[s], bx, by, int(blockIdx.y));
+                if (EX && ep.zB) tma_load_3d(Bs, &tmB, &full[s], bx, by, int(blockIdx.y) / ep.b_group);
                 else             tma_load_2d(Bs, &tmB, &full[s], bx, by);
                 issued = kt + 1;
             }
@@ -551,7 +552,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
     if constexpr (EX) {
         const int64_t b = blockIdx.y;
         A += b * ep.sA;
-        B += b * ep.sB;
+        B += (b / ep.b_group) * ep.sB;
         C += b * ep.sC;
     }
 
@@ -656,15 +657,19 @@ inline bool make_operand_map(CUtensorMap *map, const float *base, int64_t inner,
              : make_map(map, base, inner, outer, ld, box_inner, box_outer, swz);
 }
 
+// The number of distinct B matrices a batched call reads.
+inline int64_t b_batches(const GemmProblem &p) { return (p.batch + p.b_group - 1) / p.b_group; }
+
 inline ExArgs ex_args(const GemmProblem &p) {
     ExArgs ep{};
     ep.alpha = 1.0f;
     ep.causal = -1;
     ep.k_lo = ep.k_hi = -1;
+    ep.b_group = 1;
     if (!p.ex) return ep;
     ep.sA = p.strideA; ep.sB = p.strideB; ep.sC = p.strideC;
     ep.zA = p.batch > 1 && p.strideA != 0;
-    ep.zB = p.batch > 1 && p.strideB != 0;
+    ep.zB = b_batches(p) > 1 && p.strideB != 0;
     ep.alpha = p.alpha;
     ep.bias = p.bias;
     ep.act = p.act;
@@ -674,6 +679,7 @@ inline ExArgs ex_args(const GemmProblem &p) {
     ep.causal = p.causal;
     ep.k_lo = p.k_lo;
     ep.k_hi = p.k_hi;
+    ep.b_group = int(p.b_group);
     return ep;
 }
 
@@ -685,8 +691,8 @@ int launch_tma(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     const bool okA = A_KIN ? make_operand_map(&ma, p.A, p.K, p.M, p.lda, p.batch, p.strideA, ep.zA, BK, T::BM, true)
                            : make_operand_map(&ma, p.A, p.M, p.K, p.lda, p.batch, p.strideA, ep.zA, T::BM, BK, false);
     // B: transposed (K-inner) -> dims {K, N}; row-major (N-inner) -> {N, K}
-    const bool okB = B_KIN ? make_operand_map(&mb, p.B, p.K, p.N, p.ldb, p.batch, p.strideB, ep.zB, BK, T::BN, true)
-                           : make_operand_map(&mb, p.B, p.N, p.K, p.ldb, p.batch, p.strideB, ep.zB, T::BN, BK, false);
+    const bool okB = B_KIN ? make_operand_map(&mb, p.B, p.K, p.N, p.ldb, b_batches(p), p.strideB, ep.zB, BK, T::BN, true)
+                           : make_operand_map(&mb, p.B, p.N, p.K, p.ldb, b_batches(p), p.strideB, ep.zB, T::BN, BK, false);
     if (!okA || !okB) return REPOPS_ERR_UNSUPPORTED;
     auto kern = gemm_tma_ws_kernel<T, A_KIN, B_KIN, EX>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);

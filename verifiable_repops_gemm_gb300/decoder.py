@@ -9,8 +9,8 @@ Layer (pre-norm, causal, grouped-query attention):
     qkv  = h W_qkv                                  one GEMM
     q, k = rotary(q, k)                             in place, the heads' pairs
                                                     rotated to each token's position
-    for every sequence (each GEMM call batches one query head of every
-    key/value group, whose operands lie one stride apart):
+    for every sequence (each GEMM call covers every query head; the
+    `group` query heads of a key/value head share its K and V):
         S = (Q K^T) / sqrt(d_head)                  batched GEMM, alpha epilogue,
                                                     tiles above the diagonal skipped
         P = causal softmax of every head's rows     one row-operator call
@@ -137,11 +137,10 @@ def _after(stream, *others):
 
 
 def side_streams(cfg: DecoderConfig, tokens: int, device):
-    """The side streams one layer's attention runs its independent products
-    on: per sequence, one for the scores / dP and softmax, one per query head
-    of a group (P V, dS K), and one each for the dV and dK chains."""
-    group = cfg.heads // cfg.kv_heads
-    return [torch.cuda.Stream(device) for _ in range(tokens // cfg.seq_len * (group + 3))]
+    """The side streams one layer's attention runs its independent work on:
+    three per sequence (the scores, softmax and products of a sequence, or in
+    the backward its dP / dQ; the dV chain; the dK chain)."""
+    return [torch.cuda.Stream(device) for _ in range(tokens // cfg.seq_len * 3)]
 
 
 def _per_kv(t, rows, col0, kv, group, h, dh):
@@ -156,58 +155,51 @@ def _kv(t, rows, col0, kv, dh):
     return t[rows, col0:col0 + kv * dh].unflatten(1, (kv, dh)).transpose(0, 1)
 
 
+def _heads(t, rows, col0, n, dh):
+    """(n, S, dh) view of n consecutive heads: column block col0 + h*dh."""
+    return t[rows, col0:col0 + n * dh].unflatten(1, (n, dh)).transpose(0, 1)
+
+
 def attention(qkv, cfg: DecoderConfig, out, scores, probs=None, streams=None):
     """Causal grouped-query attention of every sequence into `out` (T x d).
     scores: (sequences * kv_heads, group, S, S) scratch (or (kv_heads, group,
     S, S), shared by the sequences in turn); probs: optional buffer shaped
     like the first that keeps every head's softmax output for the backward
-    pass.  Each GEMM call batches query head h of all key/value groups (their
-    operands sit at one stride apart).  streams (from `side_streams`): the
-    sequences, and the P V products of the heads, run concurrently -- their
-    outputs are disjoint, so the bits do not change -- and the caller's
+    pass.  One GEMM call covers every query head of a sequence: a key/value
+    head's K or V is shared by the `group` consecutive query heads of its
+    group.  streams (from `side_streams`): the sequences run concurrently --
+    their outputs are disjoint, so the bits do not change -- and the caller's
     stream waits for all of them."""
-    S, dh, kv = cfg.seq_len, cfg.d_head, cfg.kv_heads
-    group = cfg.heads // kv
+    S, dh, kv, H = cfg.seq_len, cfg.d_head, cfg.kv_heads, cfg.heads
     k0, v0 = cfg.d, cfg.d + kv * dh
     scale = 1.0 / float(dh) ** 0.5
     seqs = qkv.shape[0] // S
     buf = probs if probs is not None else scores
     shared = buf.shape[0] < seqs * kv
     main = torch.cuda.current_stream()
-    used, joined = [], []
+    prev, joined = None, []
     if streams is not None:
         fork = torch.cuda.Event()
         fork.record(main)
     for s in range(seqs):
         rows = slice(s * S, (s + 1) * S)
-        sc = buf if shared else buf[s * kv:(s + 1) * kv]                         # (kv, group, S, S)
-        Kt = _kv(qkv, rows, k0, kv, dh).transpose(1, 2)                          # (kv, dh, S)
-        V = _kv(qkv, rows, v0, kv, dh)
-        if streams is None:
-            st, heads_st = main, [main] * group
-        else:
-            base = s * (group + 3)
-            st, heads_st = streams[base], streams[base + 1:base + 1 + group]
-            st.wait_event(fork)
-            if shared:                  # a shared scratch is reused after the previous sequence's products
-                _after(st, *used)
-        with torch.cuda.stream(st):
-            for h in range(group):
-                # tiles wholly above the diagonal are skipped: the causal
-                # softmax never reads them
-                gemm_batched(_per_kv(qkv, rows, 0, kv, group, h, dh), Kt, out=sc[:, h], alpha=scale,
-                             causal_first=0)
-            P = sc.view(kv * group * S, S)
-            softmax_rows(P, out=P, causal_first=0, causal_period=S)
-        for h in range(group):
-            if streams is not None:
-                _after(heads_st[h], st)
-            with torch.cuda.stream(heads_st[h]):
-                # P is +0 past the diagonal: row i's chain stops at k = i
-                gemm_batched(sc[:, h], V, out=_per_kv(out, rows, 0, kv, group, h, dh), k_hi=0)
+        sc = (buf if shared else buf[s * kv:(s + 1) * kv]).view(H, S, S)       # head q = k*group + h
+        st = main if streams is None else streams[3 * s]
         if streams is not None:
-            used = [st] + list(heads_st)
-            joined += used
+            st.wait_event(fork)
+            if shared and prev is not None:    # a shared scratch is reused after the previous sequence
+                _after(st, prev)
+        with torch.cuda.stream(st):
+            # tiles wholly above the diagonal are skipped: the causal softmax
+            # never reads them
+            gemm_batched(_heads(qkv, rows, 0, H, dh), _kv(qkv, rows, k0, kv, dh).transpose(1, 2), out=sc,
+                         alpha=scale, causal_first=0)
+            P = sc.view(H * S, S)
+            softmax_rows(P, out=P, causal_first=0, causal_period=S)
+            # P is +0 past the diagonal: row i's chain stops at k = i
+            gemm_batched(sc, _kv(qkv, rows, v0, kv, dh), out=_heads(out, rows, 0, H, dh), k_hi=0)
+        prev = st
+        joined.append(st)
     if streams is not None:
         _after(main, *joined)
 
@@ -347,16 +339,17 @@ def backward(dy, w: dict, cfg: DecoderConfig, saved: dict, *, work: dict = None,
 
 def _attention_backward(dattn, dqkv, saved, cfg: DecoderConfig, dp, streams):
     """The attention's part of dqkv (before the inverse rotation), per
-    sequence and key/value head k with its query heads h:
-        dP_h = dO_h V_k^T (on and below the diagonal); dV_k = sum_h P_h^T dO_h
-        dS_h = causal softmax'(P_h; dP_h)
-        dQ_h = s dS_h K_k;  dK_k = sum_h s dS_h^T Q_h
-    dp: (sequences * kv_heads, group, S, S) scratch, or (kv_heads, group, S, S)
-    shared by the sequences in turn.  With `streams` the sequences run
-    concurrently, and within one the dV chain, the dK chain and the dQ_h run
-    beside each other; the chains keep head order, so the bits do not change."""
-    S, dh, kv = cfg.seq_len, cfg.d_head, cfg.kv_heads
-    group = cfg.heads // kv
+    sequence, every query head q = k*group + h of key/value head k:
+        dP_q = dO_q V_k^T (on and below the diagonal); dV_k = sum_h P_q^T dO_q
+        dS_q = causal softmax'(P_q; dP_q)
+        dQ_q = s dS_q K_k;  dK_k = sum_h s dS_q^T Q_q
+    with dP and dQ one GEMM call per sequence, the dV and dK sums in head
+    order through the residual epilogue.  dp: (sequences * kv_heads, group,
+    S, S) scratch, or (kv_heads, group, S, S) shared by the sequences in turn.
+    With `streams` the sequences run concurrently, and within one the dV
+    chain and the dK chain beside dP / dQ; the bits do not change."""
+    S, dh, kv, H = cfg.seq_len, cfg.d_head, cfg.kv_heads, cfg.heads
+    group = H // kv
     scale = 1.0 / float(dh) ** 0.5
     k0, v0 = cfg.d, cfg.d + kv * dh
     qkv = saved["qkv"]
@@ -369,26 +362,21 @@ def _attention_backward(dattn, dqkv, saved, cfg: DecoderConfig, dp, streams):
         fork.record(main)
     for s in range(seqs):
         rows = slice(s * S, (s + 1) * S)
-        P = saved["probs"][s * kv:(s + 1) * kv]
-        dP = dp if shared else dp[s * kv:(s + 1) * kv]                        # (kv, group, S, S)
+        P = saved["probs"][s * kv:(s + 1) * kv]                               # (kv, group, S, S)
+        dP = dp if shared else dp[s * kv:(s + 1) * kv]
         V, K = _kv(qkv, rows, v0, kv, dh), _kv(qkv, rows, k0, kv, dh)
         dV, dK = _kv(dqkv, rows, v0, kv, dh), _kv(dqkv, rows, k0, kv, dh)
         if streams is None:
             sp = sv = sk = main
-            sq = [main] * group
         else:
-            base = s * (group + 3)
-            sp, sq, sv, sk = streams[base], streams[base + 1:base + 1 + group], streams[base + 1 + group], \
-                streams[base + 2 + group]
+            sp, sv, sk = streams[3 * s:3 * s + 3]
             for st in (sp, sv):
                 st.wait_event(fork)
             if shared:
                 _after(sp, *used)
         with torch.cuda.stream(sp):
-            for h in range(group):
-                # dP_h = dO_h V^T on and below the diagonal (the causal backward reads no more)
-                gemm_batched(_per_kv(dattn, rows, 0, kv, group, h, dh), V.transpose(1, 2), out=dP[:, h],
-                             causal_first=0)
+            # dP = dO V^T on and below the diagonal (the causal backward reads no more)
+            gemm_batched(_heads(dattn, rows, 0, H, dh), V.transpose(1, 2), out=dP.view(H, S, S), causal_first=0)
         with torch.cuda.stream(sv):
             for h in range(group):
                 # dV = sum over the group's heads, in head order, of P_h^T dO_h;
@@ -396,21 +384,18 @@ def _attention_backward(dattn, dqkv, saved, cfg: DecoderConfig, dp, streams):
                 gemm_batched(P[:, h].transpose(1, 2), _per_kv(dattn, rows, 0, kv, group, h, dh), out=dV,
                              residual=dV if h else None, k_lo=0)
         with torch.cuda.stream(sp):
-            dS = dP.view(kv * group * S, S)
-            softmax_backward(P.view(kv * group * S, S), dS, out=dS, causal_first=0, causal_period=S)
+            dS = dP.view(H * S, S)
+            softmax_backward(P.view(H * S, S), dS, out=dS, causal_first=0, causal_period=S)
+            gemm_batched(dP.view(H, S, S), K, out=_heads(dqkv, rows, 0, H, dh), alpha=scale, k_hi=0)
         if streams is not None:
-            for st in list(sq) + [sk]:
-                _after(st, sp)
-        for h in range(group):
-            with torch.cuda.stream(sq[h]):
-                gemm_batched(dP[:, h], K, out=_per_kv(dqkv, rows, 0, kv, group, h, dh), alpha=scale, k_hi=0)
+            _after(sk, sp)
         with torch.cuda.stream(sk):
             for h in range(group):
                 # dK = sum over the group's heads, in head order, of s dS_h^T Q_h
                 gemm_batched(dP[:, h].transpose(1, 2), _per_kv(qkv, rows, 0, kv, group, h, dh), out=dK,
                              alpha=scale, residual=dK if h else None, k_lo=0)
         if streams is not None:
-            used = [sp, sv, sk] + list(sq)
+            used = [sp, sv, sk]
             joined += used
     if streams is not None:
         _after(main, *joined)
