@@ -44,6 +44,17 @@ __device__ __forceinline__ int64_t imin64(int64_t a, int64_t b) { return a < b ?
 constexpr int MAX_FAST_RUNS = 256 * 4;          // register-resident rows: up to 32768 values
 constexpr int MAX_GENERIC_RUNS = 12288;         // run results in 48 KB of shared memory
 
+// Resident CTAs per SM the staged backward kernels ask the compiler for.
+// Softmax backward: 10 warps (about 100 registers a thread for its p and dp
+// runs), measured 11% faster than the uncapped 151 registers; the forward
+// softmax kernels stay uncapped (capped at 64 registers they ran 13% slower:
+// their 32 exponentials a thread need the registers for overlap).
+template <int T>
+constexpr int kBwdRowBlocks = T == 32 ? 16 : 640 / T;
+// RMSNorm backward: 16 warps (128 registers; x, dy, gamma and res runs live).
+template <int T>
+constexpr int kNormBwdBlocks = T == 32 ? 12 : 512 / T;
+
 // ------------------------------------------------------------ arithmetic ----
 
 enum class Op { Sum, Max };
@@ -628,7 +639,7 @@ rmsnorm_backward_kernel(int64_t rows, int64_t n, const float *__restrict__ x, in
 // leave through the x and dy stages.  res may be dx (its row is staged
 // before dx is written).
 template <int T>
-__global__ void __launch_bounds__(T)
+__global__ void __launch_bounds__(T, kNormBwdBlocks<T>)
 rmsnorm_backward_staged_kernel(int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma, float eps,
                                const float *dy, int64_t lddy, const float *res, int64_t ldres, float *dx,
                                int64_t lddx, float *p, int64_t ldp) {
@@ -652,21 +663,39 @@ rmsnorm_backward_staged_kernel(int64_t rows, int64_t n, const float *x, int64_t 
         read_stage(b, sd, n);
         const float ms = __fdiv_rn(a.template reduce<Op::Sum>(Square(), gbuf, phase, runs), nf);
         const float inv = __frcp_rn(__fsqrt_rn(__fadd_rn(ms, eps)));
-        float g[RUN];
-        read_param_run<T, 1>(sg, threadIdx.x, g);
+        const int u = threadIdx.x;
+        // gamma and res are read from their stages four values at a time
+        // (registers hold the x and dy runs only)
 #pragma unroll
-        for (int i = 0; i < RUN; ++i) b.v[0][i] = __fmul_rn(__fmul_rn(b.v[0][i], g[i]), __fmul_rn(a.v[0][i], inv));
+        for (int q = 0; q < RUN / 4; ++q) {
+            const float4 g4 = sg[stage_slot(u, q)];
+            const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int i = 4 * q + t;
+                b.v[0][i] = __fmul_rn(__fmul_rn(b.v[0][i], g[t]), __fmul_rn(a.v[0][i], inv));
+            }
+        }
         const float c = __fdiv_rn(b.template reduce<Op::Sum>(Ident(), gbuf, phase, runs), nf);
         read_stage(b, sd, n);                          // dy again
-        float r[RUN];
-        if (res) read_param_run<T, 1>(sr, threadIdx.x, r);
 #pragma unroll
-        for (int i = 0; i < RUN; ++i) {
-            const float xh = __fmul_rn(a.v[0][i], inv), gy = __fmul_rn(b.v[0][i], g[i]);
-            float d = __fmul_rn(inv, __fsub_rn(gy, __fmul_rn(xh, c)));
-            if (res) d = __fadd_rn(d, r[i]);
-            a.v[0][i] = d;
-            b.v[0][i] = __fmul_rn(b.v[0][i], xh);
+        for (int q = 0; q < RUN / 4; ++q) {
+            const float4 g4 = sg[stage_slot(u, q)];
+            const float g[4] = {g4.x, g4.y, g4.z, g4.w};
+            float r[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (res) {
+                const float4 r4 = sr[stage_slot(u, q)];
+                r[0] = r4.x; r[1] = r4.y; r[2] = r4.z; r[3] = r4.w;
+            }
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const int i = 4 * q + t;
+                const float xh = __fmul_rn(a.v[0][i], inv), gy = __fmul_rn(b.v[0][i], g[t]);
+                float d = __fmul_rn(inv, __fsub_rn(gy, __fmul_rn(xh, c)));
+                if (res) d = __fadd_rn(d, r[t]);
+                a.v[0][i] = d;
+                b.v[0][i] = __fmul_rn(b.v[0][i], xh);
+            }
         }
         __syncwarp();                                  // every lane has read its stages before they are rewritten
         write_stage(a, sx);
@@ -713,7 +742,7 @@ softmax_backward_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, co
 // and ds leaves through the p stage.  dp is read back from its stage after
 // the reduction instead of being held in registers.
 template <int T>
-__global__ void __launch_bounds__(T)
+__global__ void __launch_bounds__(T, kBwdRowBlocks<T>)
 softmax_backward_staged_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, const float *dp, int64_t lddp,
                                float *ds, int64_t ldds, int64_t first, int64_t period) {
     extern __shared__ float4 stage_mem[];
