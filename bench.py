@@ -56,8 +56,8 @@ L2_BYTES = 129 * 10 ** 6
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
 # valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "752278687937feca11f702b4e0bb5c41d29e4c9bab7ada3d61790b976c449bde",
-                "bytes_per_launch": 4893530880 + 266178048}
+GEMM_TRAFFIC = {"src_sha256": "3ec237b66a7e805622688b5827306166d46442865de941cc9cbcc5f84f39dfab",
+                "bytes_per_launch": 4832763648 + 265803520}
 
 
 def measured_peaks():
