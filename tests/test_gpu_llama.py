@@ -241,3 +241,30 @@ def test_rope_scalar_path_and_round_trip(rp, orc):
     assert np.array_equal(bits(xd[:, 1:]), u32(want_shift)) and np.array_equal(bits(xd[:, 0]), u32(x[:, 0]))
     rp.rope(xd[:, 1:], heads, cd, sd, inverse=True)
     assert np.max(np.abs(xd.cpu().numpy() - x)) < 1e-5
+
+
+def same_bits_or_both_nan(got, want):
+    g, w = u32(got), u32(want)
+    nan_g, nan_w = np.isnan(np.asarray(got, np.float32)), np.isnan(np.asarray(want, np.float32))
+    return np.array_equal(nan_g, nan_w) and np.array_equal(g[~nan_g], w[~nan_w])
+
+
+def test_special_values(rp, orc):
+    # signed zeros, infinities, NaN, subnormals and overflow edges through
+    # SwiGLU, its backward and the rotation (NaN payloads are not compared)
+    sp = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 1e-45, -1e-45, 88.7, -88.7, 103.9, -103.9, 3e38, -3e38,
+                   1.0, -1.0, 0.5], np.float32)
+    g = np.tile(sp, (16, 1))
+    u = np.tile(sp, (16, 1)).T.copy()
+    gd, ud = torch.from_numpy(g).to(DEV), torch.from_numpy(u).to(DEV)
+    assert same_bits_or_both_nan(rp.swiglu(gd, ud).cpu().numpy(), orc.swiglu(g, u))
+    dh = np.roll(u, 3, axis=1)
+    dg, du = rp.swiglu_backward(gd, ud, torch.from_numpy(dh).to(DEV))
+    wg, wu = orc.swiglu_backward(g, u, dh)
+    assert same_bits_or_both_nan(dg.cpu().numpy(), wg) and same_bits_or_both_nan(du.cpu().numpy(), wu)
+    freq = orc.rope_frequencies(8, float(F32(LN_BASE)))
+    c, s = orc.rope_table(16, freq)
+    x = np.tile(sp, (16, 1))
+    xd = torch.from_numpy(x).to(DEV)
+    rp.rope(xd, 1, torch.from_numpy(c).to(DEV), torch.from_numpy(s).to(DEV))
+    assert same_bits_or_both_nan(xd.cpu().numpy(), orc.rope(x, 1, c, s))
