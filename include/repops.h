@@ -83,6 +83,14 @@ int repops_last_cuda_error(void);
  * REPOPS_ERR_CUDA / REPOPS_ERR_INVALID_ARG (null status_out). */
 int repops_device_status(cudaStream_t stream, int *status_out);
 
+/* Failure-detection self-test: launches one kernel on `stream` whose thread
+ * waits on an mbarrier phase that nothing completes, with a limit of limit_ns
+ * nanoseconds (1 .. 2e9, else INVALID_ARG) of the device's global timer.  The
+ * wait gives up and sets the sticky status word, as a GEMM whose copies never
+ * landed would: the next repops_device_status reports REPOPS_ERR_TIMEOUT, and
+ * the GPU context stays usable.  Nothing else is read or written. */
+int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Order-fixed FP32 GEMM                                                     */
 /* "Verde与RepOps" §3.2, matmul example; §3.1; §3.3                          */

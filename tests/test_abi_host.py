@@ -343,3 +343,8 @@ def test_llama_operators_reject_bad_arguments(L):
     assert rp(4, 2, 2, FAKE_A, 8, FAKE_B, FAKE_C, 16, 0, 0, 0, None) == -1      # period < 1
     assert rp(4, 2, 2, FAKE_B + 8, 8, FAKE_B, FAKE_C, 16, 0, 4, 0, None) == -2  # x overlaps cos
     assert rp(0, 2, 2, None, 8, None, None, 16, 0, 4, 0, None) == 0
+
+
+def test_selftest_rejects_bad_limits(L):
+    assert L.repops_selftest_bounded_wait(0, None) == -1
+    assert L.repops_selftest_bounded_wait(3_000_000_000, None) == -1

@@ -39,6 +39,17 @@ int status_address(unsigned **out) {
     return REPOPS_OK;
 }
 
+// Failure-detection self-test: thread 0 waits on a phase of an mbarrier that
+// nothing will complete, gives up after limit_ns and sets the sticky status
+// word, exactly as a GEMM wait that timed out would.  Nothing else is touched.
+__global__ void bounded_wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded_ns(&bar, 0u, limit_ns)) atomicOr(status, 1u);
+}
+
 const GemmLauncher kLaunch[kGemmConfigCount] = {gemm_launch_cfg0, gemm_launch_cfg1, gemm_launch_cfg2,
                                                 gemm_launch_cfg3, gemm_launch_cfg4};
 const GemmOccupancy kOccupancy[kGemmConfigCount] = {gemm_occupancy_cfg0, gemm_occupancy_cfg1,
@@ -620,4 +631,13 @@ extern "C" int repops_gemm_config_occupancy(int config) {
 extern "C" int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0) return -1;
     return choose_config(M, N, std::max<int64_t>(K, 1));
+}
+
+extern "C" int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1 || limit_ns > int64_t(kWaitLimitNs)) return REPOPS_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    int rc = status_address(&status);
+    if (rc != REPOPS_OK) return rc;
+    bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, uint64_t(limit_ns));
+    return check_launch();
 }

@@ -92,16 +92,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete; gives up after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+// Waits for phase `parity` of `bar` to complete; gives up after limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded_ns(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Waits for phase `parity` of `bar` to complete; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_bounded_ns(bar, parity, kWaitLimitNs);
 }
 
 // 2-D tiled TMA load of the box at (c0 = inner, c1 = outer) into smem, with
