@@ -198,16 +198,21 @@ class Workload:
         if ev: ev[3].record(s)
 
 
-def dist_setup(backend=None):
+def dist_setup(backend=None, timeout_s=None):
     """Rank layout from the torchrun environment; joins the process group
     (NCCL on GPUs unless `backend` says otherwise) when there is more than one
-    rank.  The group carries only a barrier and a max-reduction of times."""
+    rank.  The group carries only a barrier and a max-reduction of times.  A
+    rank that never reaches a collective makes the others' next collective
+    fail after `timeout_s` (REPOPS_PG_TIMEOUT_S, default 600 s) instead of
+    waiting forever."""
+    import datetime
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
+        t = float(timeout_s if timeout_s is not None else os.environ.get("REPOPS_PG_TIMEOUT_S", "600"))
         torch.distributed.init_process_group(
-            backend or ("nccl" if torch.cuda.is_available() else "gloo"))
+            backend or ("nccl" if torch.cuda.is_available() else "gloo"), timeout=datetime.timedelta(seconds=t))
     return world, rank, local
 
 

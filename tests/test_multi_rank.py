@@ -47,6 +47,35 @@ def test_two_replicas_barrier_and_max_time():
     assert out == [(0, 2, 0, 20.0), (1, 2, 1, 20.0)]
 
 
+def _worker_one_leaves(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    w, r, _ = bench.dist_setup("gloo", timeout_s=5)
+    if r == 1:
+        os._exit(3)                     # leaves between steps, before the next barrier
+    try:
+        bench.barrier(w)
+        q.put((r, "returned"))
+    except Exception as e:              # the failure reaches the host as an error
+        q.put((r, "error: " + type(e).__name__))
+
+
+def test_a_rank_that_leaves_fails_the_others_collective():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker_one_leaves, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    rank, what = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+    assert rank == 0 and what.startswith("error"), what
+    assert procs[1].exitcode == 3
+
+
 def test_reference_arm_under_torchrun_prints_one_line_from_rank_zero():
     env = dict(os.environ, OMP_NUM_THREADS="1")
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
