@@ -264,3 +264,22 @@ def test_transposed_b_large_problem_same_bits(rp):
     C_forced = run(rp, A, Bcm, config=1, loader=2)
     assert torch.equal(C_rm.view(torch.int32), C_cm.view(torch.int32))
     assert torch.equal(C_rm.view(torch.int32), C_forced.view(torch.int32))
+
+
+def test_row_major_a_large_problem_same_bits(rp, orc):
+    # >= 4 GFLOP with A row-major: A^T is copied into padded scratch and the
+    # M-inner kernels run; the bits equal the K-inner kernels' (explicit TMA
+    # loader, no copy) and the oracle's on sampled rows; M and K not multiples
+    # of the tile or of 4
+    M, N, K = 1029, 1024, 2051
+    A = inputs.normal((M, K), 1.0, 710, DEV)
+    B = inputs.normal((K, N), 1.0, 711, DEV)
+    C_auto = run(rp, A, B)
+    C_kin = run(rp, A, B, config=1, loader=2)
+    assert torch.equal(C_auto.view(torch.int32), C_kin.view(torch.int32))
+    rows = [0, 1, 517, M - 1]
+    want = orc.gemm(A[rows].cpu().numpy(), B.cpu().numpy())
+    assert np.array_equal(C_auto[rows].cpu().numpy().view(np.uint32), want.view(np.uint32))
+    # both transposes: B column-major as well
+    Bcm = B.t().contiguous().t()
+    assert torch.equal(run(rp, A, Bcm).view(torch.int32), C_auto.view(torch.int32))

@@ -233,10 +233,11 @@ __device__ __forceinline__ void mma_stage(const float *__restrict__ As, const fl
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
             if constexpr (PackedAcc<T, A_KIN>::PAIR_N) {
+                // column pairs outer: measured 0.7% faster at 8192^3 than rows outer
 #pragma unroll
-                for (int r = 0; r < T::TM; ++r)
+                for (int j = 0; j < T::TN / 2; ++j)
 #pragma unroll
-                    for (int j = 0; j < T::TN / 2; ++j)
+                    for (int r = 0; r < T::TM; ++r)
                         acc.v[r][j] = fold2(acc.v[r][j], a[r][kk], b[2 * j][kk], a[r][kk], b[2 * j + 1][kk]);
             } else {
 #pragma unroll
