@@ -56,8 +56,8 @@ L2_BYTES = 129 * 10 ** 6
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
 # valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "3ec237b66a7e805622688b5827306166d46442865de941cc9cbcc5f84f39dfab",
-                "bytes_per_launch": 4832763648 + 265803520}
+GEMM_TRAFFIC = {"src_sha256": "9767fe4e2afd909f89b1772567a0d0d4d3ceedd29bb5b6f2e6238f5f94b97270",
+                "bytes_per_launch": 4695637760 + 267883264}
 
 
 def measured_peaks():
@@ -72,7 +72,8 @@ def gemm_kernel_label():
     cfg = rp.gemm_auto_config(GEMM_N, GEMM_N, GEMM_N)
     ci = rp.gemm_config_info(cfg)
     return ("gemm_tma_ws_kernel config %d: %dx%d CTA tile, %d consumer threads + 1 producer warp, "
-            "%dx%d per thread" % (cfg, ci["bm"], ci["bn"], ci["threads"], ci["tm"], ci["tn"]))
+            "%dx%d per thread; A M-inner (row-major A transposed into scratch first, inside the timed "
+            "call), B N-inner" % (cfg, ci["bm"], ci["bn"], ci["threads"], ci["tm"], ci["tn"]))
 
 
 def kernel_source_sha():
