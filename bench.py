@@ -186,7 +186,9 @@ class Workload:
         self.root_C = torch.empty(32, dtype=torch.uint8, device=dev)
         self.gemm_flops = 2.0 * n * n * n
         self.mean_bytes = float((nC + 2) * ln * 4)
-        self.launches = 1 + 1 + merkle_launches(self.tbytes) + merkle_launches(self.cbytes)
+        # the GEMM call copies the row-major A into its M-inner scratch layout
+        # (one transpose launch) and runs one GEMM kernel
+        self.launches = 2 + 1 + merkle_launches(self.tbytes) + merkle_launches(self.cbytes)
 
     def step(self, s, ev=None):
         if ev: ev[0].record(s)
@@ -421,6 +423,14 @@ def run_ours(args):
     mean_max = max_over_ranks(sum(mean_ms), world, dev)
     merk_max = max_over_ranks(sum(merk_ms), world, dev)
 
+    # the step's commitments right after the timed region: the roots of T and
+    # of the GEMM output C (the same bits on every run of these seeds) and of
+    # theta after warmup + steps updates
+    theta_root = rp.merkle_sha256(w.theta)
+    commitments = {"T_root": bytes(w.root_T.cpu().numpy()).hex(),
+                   "C_root": bytes(w.root_C.cpu().numpy()).hex(),
+                   "theta_root": bytes(theta_root.cpu().numpy()).hex(),
+                   "theta_updates": args.warmup + args.steps}
     e2e = run_e2e(w, dev, args.e2e_steps) if args.e2e_steps > 0 else None
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -479,6 +489,7 @@ def run_ours(args):
         "clocks": clocks,
         "gpu_launches": w.launches * args.steps,
     }
+    line["commitments"] = commitments
     if clocks.get("sm_mhz"):
         line["roofline"]["frac_at_sampled_clock"] = achieved / (
             sms * FP32_LANES_PER_SM * clocks["sm_mhz"] * 1e6 / 1e12)
