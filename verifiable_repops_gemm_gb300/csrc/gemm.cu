@@ -203,6 +203,32 @@ int launch_repack(const float *src, int64_t ld_src, float *dst, int64_t ld_dst, 
     return check_launch();
 }
 
+// Copies a rows x cols operand (pitch ld) into stream-ordered scratch with a
+// 16-byte pitch: transposed (cols x rows) when `transpose`, else as it is.
+// *out is the scratch (null, and REPOPS_OK, when the allocation is refused:
+// the caller then keeps its operand) and *pitch its row pitch in elements.
+int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool transpose, cudaStream_t stream,
+                 void **out, int64_t *pitch) {
+    const int64_t outer = transpose ? cols : rows, inner = transpose ? rows : cols;
+    const int64_t pm = (inner + 3) / 4 * 4;
+    *out = nullptr;
+    if (cudaMallocAsync(out, size_t(outer) * size_t(pm) * 4u, stream) != cudaSuccess) {
+        cudaGetLastError();   // a refused allocation is not an error here
+        *out = nullptr;
+        return REPOPS_OK;
+    }
+    float *dst = static_cast<float *>(*out);
+    const int rc = transpose ? launch_transpose(src, ld, rows, cols, dst, pm, stream)
+                             : launch_repack(src, ld, dst, pm, rows, cols, stream);
+    if (rc != REPOPS_OK) {
+        cudaFreeAsync(*out, stream);
+        *out = nullptr;
+        return rc;
+    }
+    *pitch = pm;
+    return REPOPS_OK;
+}
+
 int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
                   cudaStream_t stream) {
@@ -261,57 +287,33 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     // scratch (a refused allocation) the caller's operands are used as they are.
     const bool large = loader == REPOPS_LOADER_AUTO && 2.0 * double(M) * double(N) * double(K) >= kRepackMinFlops;
     void *bscratch = nullptr, *ascratch = nullptr;
-    if (large && p.transB) {
-        const int64_t pn = (N + 3) / 4 * 4;
-        if (cudaMallocAsync(&bscratch, size_t(K) * size_t(pn) * 4u, stream) == cudaSuccess) {
-            rc = launch_transpose(B, ldb, N, K, static_cast<float *>(bscratch), pn, stream);
-            if (rc != REPOPS_OK) {
-                cudaFreeAsync(bscratch, stream);
-                return rc;
-            }
+    auto fail = [&](int code) {
+        for (void *m : {bscratch, ascratch})
+            if (m) cudaFreeAsync(m, stream);
+        return code;
+    };
+    if (large && (p.transB || !operand_tma_ready(p.B, p.ldb))) {
+        // B stored transposed (N x K) is transposed, an unaligned row-major B repacked
+        int64_t pitch = 0;
+        rc = p.transB ? copy_operand(B, ldb, N, K, true, stream, &bscratch, &pitch)
+                      : copy_operand(B, ldb, K, N, false, stream, &bscratch, &pitch);
+        if (rc != REPOPS_OK) return fail(rc);
+        if (bscratch) {
             p.B = static_cast<const float *>(bscratch);
-            p.ldb = pn;
+            p.ldb = pitch;
             p.transB = 0;
-        } else {
-            cudaGetLastError();   // a refused allocation is not an error here
-            bscratch = nullptr;
-        }
-    }
-    if (large && !p.transB && !operand_tma_ready(p.B, p.ldb)) {
-        const int64_t pn = (N + 3) / 4 * 4;
-        void *m = nullptr;
-        if (cudaMallocAsync(&m, size_t(K) * size_t(pn) * 4u, stream) == cudaSuccess) {
-            rc = launch_repack(p.B, p.ldb, static_cast<float *>(m), pn, K, N, stream);
-            if (rc != REPOPS_OK) {
-                cudaFreeAsync(m, stream);
-                if (bscratch) cudaFreeAsync(bscratch, stream);
-                return rc;
-            }
-            if (bscratch) cudaFreeAsync(bscratch, stream);
-            bscratch = m;
-            p.B = static_cast<const float *>(m);
-            p.ldb = pn;
-        } else {
-            cudaGetLastError();
         }
     }
     if (large && (!p.transA || !operand_tma_ready(p.A, p.lda))) {
-        // a K-inner A is transposed, an unaligned M-inner A repacked
-        const int64_t pm = (M + 3) / 4 * 4;
-        if (cudaMallocAsync(&ascratch, size_t(K) * size_t(pm) * 4u, stream) == cudaSuccess) {
-            rc = p.transA ? launch_repack(p.A, p.lda, static_cast<float *>(ascratch), pm, K, M, stream)
-                          : launch_transpose(p.A, p.lda, M, K, static_cast<float *>(ascratch), pm, stream);
-            if (rc != REPOPS_OK) {
-                cudaFreeAsync(ascratch, stream);
-                if (bscratch) cudaFreeAsync(bscratch, stream);
-                return rc;
-            }
+        // a K-inner A (M x K) is transposed, an unaligned M-inner A (K x M) repacked
+        int64_t pitch = 0;
+        rc = p.transA ? copy_operand(A, lda, K, M, false, stream, &ascratch, &pitch)
+                      : copy_operand(A, lda, M, K, true, stream, &ascratch, &pitch);
+        if (rc != REPOPS_OK) return fail(rc);
+        if (ascratch) {
             p.A = static_cast<const float *>(ascratch);
-            p.lda = pm;
+            p.lda = pitch;
             p.transA = 1;
-        } else {
-            cudaGetLastError();
-            ascratch = nullptr;
         }
     }
     tma_ok = gemm_tma_eligible(p);
@@ -424,23 +426,13 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     void *ascratch = nullptr;
     if (loader == REPOPS_LOADER_AUTO && batch == 1 && tma_ok && !p.transA &&
         2.0 * double(M) * double(N) * double(K) >= kRepackMinFlops) {
-        const int64_t pm = (M + 3) / 4 * 4;
-        if (cudaMallocAsync(&ascratch, size_t(K) * size_t(pm) * 4u, stream) == cudaSuccess) {
-            GemmProblem q = p;
-            q.A = static_cast<const float *>(ascratch);
-            q.lda = pm;
-            q.transA = 1;
-            if (gemm_tma_eligible(q) &&
-                launch_transpose(A, lda, M, K, static_cast<float *>(ascratch), pm, stream) == REPOPS_OK) {
-                p = q;
-            } else {
-                cudaGetLastError();
-                cudaFreeAsync(ascratch, stream);
-                ascratch = nullptr;
-            }
-        } else {
-            cudaGetLastError();   // a refused allocation is not an error here
-            ascratch = nullptr;
+        int64_t pitch = 0;
+        rc = copy_operand(A, lda, M, K, true, stream, &ascratch, &pitch);
+        if (rc != REPOPS_OK) return rc;
+        if (ascratch) {
+            p.A = static_cast<const float *>(ascratch);
+            p.lda = pitch;
+            p.transA = 1;
         }
     }
     const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
