@@ -119,6 +119,37 @@ int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) 
     return best;
 }
 
+// Tile choice for a banded product (k_lo / k_hi set): the tiles' k-ranges
+// differ -- a tile runs the whole 32-k slices covering its rows' bands -- so
+// the time is modelled as the longer of the longest tile (sharing its SM with
+// the other resident CTAs) and the total work spread over the SMs.  For the
+// per-head attention gradients (2048 x 64 outputs, 8 batches, band k >= i)
+// it picks the 32 x 64 tile, measured 18% faster than the 64 x 64 one the
+// unbanded model takes.
+int choose_config_banded(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t k_lo, int64_t k_hi) {
+    DeviceInfo di;
+    if (current_device_info(&di) != REPOPS_OK || di.device < 0 || di.device >= kMaxDevices) return 0;
+    double best_t = 0;
+    int best = 0;
+    for (int c = 0; c < kGemmConfigCount; ++c) {
+        const GemmConfigInfo ci = config_info(c);
+        const double eff = relative_efficiency(ci), conc = std::max(1, occupancy_of(di.device, c));
+        double longest = 0, total = 0;
+        for (int64_t m0 = 0; m0 < M; m0 += ci.bm) {
+            const int64_t lo = k_lo >= 0 ? std::max<int64_t>(0, m0 - k_lo) : 0;
+            const int64_t hi = k_hi >= 0 ? std::min<int64_t>(K, m0 + ci.bm + k_hi) : K;
+            const double slices = lo < hi ? double((hi + 31) / 32 - lo / 32) : 0.0;
+            const double w = double(ci.bm) * double(ci.bn) * slices / eff;
+            longest = std::max(longest, w);
+            total += w;
+        }
+        total *= double((N + ci.bn - 1) / ci.bn) * double(std::max<int64_t>(batch, 1));
+        const double t = std::max(longest * conc, total / di.sms);
+        if (c == 0 || t < best_t * 0.999) { best_t = t; best = c; }
+    }
+    return best;
+}
+
 // Span in elements of a rows x cols operand with leading dimension ld.
 bool operand_span(int64_t rows, int64_t cols, int64_t ld, uint64_t *bytes) {
     if (rows == 0 || cols == 0) { *bytes = 0; return true; }
@@ -415,7 +446,9 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
 
-    const int cfg = config >= 0 ? config : choose_config(M, N, K, batch);
+    const int cfg = config >= 0 ? config
+                    : (p.k_lo >= 0 || p.k_hi >= 0) ? choose_config_banded(M, N, K, batch, p.k_lo, p.k_hi)
+                                                   : choose_config(M, N, K, batch);
     // K == 0 has no k-slices to copy: the cp.async kernel runs the epilogue on +0
     bool tma_ok = K > 0 && gemm_tma_eligible(p);
     if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
