@@ -12,7 +12,7 @@
 // ZKDV page, proof.start(rolling_window=...): rolling hashes within each
 // committed row of a rectangular uint32 batch.  The page names no hash; the
 // library's is Rabin-Karp modulo the Mersenne prime 2^61 - 1.  Each thread
-// takes 16 consecutive window starts of one row: Horner's rule for the first,
+// takes 32 consecutive window starts of one row: Horner's rule for the first,
 // then h' = (h - w_out * B^(W-1)) * B + w_in for the rest -- exact modular
 // integers, so the split of a row across threads does not change a bit.
 // Windows up to 1024 words stage a warp's words and hashes in shared memory
@@ -147,7 +147,7 @@ bool span_bytes(int64_t rows, int64_t cols, int64_t ld, unsigned sz, uint64_t *o
 // ---------------------------------------------------------- rolling hash ----
 
 constexpr uint64_t P61 = (uint64_t(1) << 61) - 1;
-constexpr int ROLL_CHUNK = 16;   // window starts per thread
+constexpr int ROLL_CHUNK = 32;   // window starts per thread
 
 __device__ __forceinline__ uint64_t mulmod61(uint64_t a, uint64_t b) {
     // a, b < 2^61: a*b = hi*2^64 + lo, and 2^64 = 8 * 2^61 = 8 (mod P), so
@@ -189,15 +189,15 @@ rolling_hash_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ wo
 
 // Shared-memory staging: a warp takes SEG = 32 * ROLL_CHUNK consecutive window
 // starts of one row and copies the SEG + W - 1 words they read with coalesced
-// loads; lane L then rolls over starts 16L .. 16L + 15 reading the stage, and
+// loads; lane L then rolls over starts 32L .. 32L + 31 reading the stage, and
 // the hashes leave through a second stage with coalesced 8-byte stores.  Both
-// stages put one pad slot after every 16 (index j at j + j/16): lane L's
-// element k sits at 17L + k + k/16, so the 32 lanes hit 32 different banks.
+// stages put one pad slot after every 32 (index j at j + j/32): lane L's
+// element k sits at 33L + k + k/32, so the 32 lanes hit 32 different banks.
 constexpr int ROLL_SEG = 32 * ROLL_CHUNK;
 constexpr int ROLL_WARPS = 8;
 constexpr int64_t ROLL_MAX_STAGED_WINDOW = 1024;
 
-__device__ __forceinline__ int padded(int j) { return j + (j >> 4); }
+__device__ __forceinline__ int padded(int j) { return j + (j >> 5); }
 
 __global__ void __launch_bounds__(32 * ROLL_WARPS)
 rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ words, int64_t ldw, int W,
@@ -236,7 +236,7 @@ rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restri
     }
 }
 
-constexpr size_t padded_host(int j) { return size_t(j) + size_t(j >> 4); }
+constexpr size_t padded_host(int j) { return size_t(j) + size_t(j >> 5); }
 
 uint64_t powmod61_host(uint64_t b, int64_t e) {
     unsigned __int128 r = 1, x = b % P61;
@@ -335,7 +335,7 @@ extern "C" int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32
     const uint64_t bw1 = powmod61_host(REPOPS_ROLLING_HASH_BASE, window - 1);
     if (window <= ROLL_MAX_STAGED_WINDOW) {
         const int64_t segs = (n + ROLL_SEG - 1) / ROLL_SEG;
-        const int wcap = int(ROLL_SEG + window - 1) + int((ROLL_SEG + window - 1) >> 4) + 1;
+        const int wcap = int(ROLL_SEG + window - 1) + int((ROLL_SEG + window - 1) >> 5) + 1;
         const size_t smem = size_t(ROLL_WARPS) * ((padded_host(ROLL_SEG) + 1) * 8u + size_t(wcap) * 4u);
         cudaError_t e = cudaFuncSetAttribute(rolling_hash_staged_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
