@@ -369,10 +369,14 @@ softmax_causal_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x,
         const int runs = int((L + RUN - 1) / RUN);
         const float m = rr.template reduce<Op::Max>(Ident(), gbuf, phase, runs);
 #pragma unroll
-        for (int j = 0; j < R; ++j)
+        for (int j = 0; j < R; ++j) {
+            // runs past the prefix are skipped whole; inside a run every value
+            // is exponentiated (branch-free; the ones past the prefix are
+            // neither folded nor stored)
+            if (rr.len[j] == 0) continue;
 #pragma unroll
-            for (int i = 0; i < RUN; ++i)
-                if (i < rr.len[j]) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+            for (int i = 0; i < RUN; ++i) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+        }
         const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs));
 #pragma unroll
         for (int j = 0; j < R; ++j) {
