@@ -55,22 +55,18 @@ __device__ __forceinline__ uint32_t rotr(uint32_t x, int n) { return __funnelshi
 
 // SHA-256 is bound by the integer ALU pipe, which issues at half rate, while
 // the pipe that runs integer multiply-adds idles.  So every 32-bit addition is
-// written x * one + y and the two plain right shifts of the message schedule
-// as high halves of products (x >> 3 = umulhi(x, 2^29)); `one`, 2^29 and 2^22
-// arrive as kernel arguments, so the compiler cannot fold them back into adds
-// and shifts, and those instructions run on the multiply-add pipe.  Same
+// written x * one + y, with `one` a kernel argument the compiler cannot fold
+// back into an add: those instructions run on the multiply-add pipe.  Same
 // arithmetic mod 2^32, same bits.  (Measured on 4 GiB: 869 -> 1008 GB/s
-// together with the 16-round loop body below; moving a rotate as well was
-// slower.)
+// together with the 16-round loop body below.  Moving more there is slower:
+// the schedule's shifts as high halves of products 1008 -> 1020 GB/s when
+// taken back to the ALU, a rotate of a sigma as two products -3%, a
+// three-input sum as one ALU add instead of two multiply-adds -1 to -4%.)
 struct PipeConst {
     uint32_t one;     // 1
-    uint32_t two29;   // 2^29
-    uint32_t two22;   // 2^22
 };
 
 __device__ __forceinline__ uint32_t add_u(uint32_t x, uint32_t y, const PipeConst &c) { return x * c.one + y; }
-__device__ __forceinline__ uint32_t shr3(uint32_t x, const PipeConst &c) { return __umulhi(x, c.two29); }
-__device__ __forceinline__ uint32_t shr10(uint32_t x, const PipeConst &c) { return __umulhi(x, c.two22); }
 
 // One round of FIPS 180-4 §6.2.2 with message word w and constant k.
 __device__ __forceinline__ void sha256_round(uint32_t &a, uint32_t &b, uint32_t &c, uint32_t &d,
@@ -104,8 +100,8 @@ __device__ __forceinline__ void sha256_compress(uint32_t (&st)[8], uint32_t (&W)
         for (int j = 0; j < 16; ++j) {
             // W_t = s1(W_{t-2}) + W_{t-7} + s0(W_{t-15}) + W_{t-16}, in place: slot j holds W_{t-16}
             const uint32_t x = W[(j + 1) & 15], y = W[(j + 14) & 15];
-            const uint32_t s0 = rotr(x, 7) ^ rotr(x, 18) ^ shr3(x, pc);
-            const uint32_t s1 = rotr(y, 17) ^ rotr(y, 19) ^ shr10(y, pc);
+            const uint32_t s0 = rotr(x, 7) ^ rotr(x, 18) ^ (x >> 3);
+            const uint32_t s1 = rotr(y, 17) ^ rotr(y, 19) ^ (y >> 10);
             const uint32_t w = add_u(add_u(add_u(s1, W[(j + 9) & 15], pc), s0, pc), W[j], pc);
             W[j] = w;
             sha256_round(a, b, c, d, e, f, g, h, w, c_K[t0 + j], pc);
@@ -373,7 +369,7 @@ int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void 
         cudaStream_t stream, const TreeOut to = TreeOut{nullptr, 0}) {
     const uint8_t *data = static_cast<const uint8_t *>(ptr);
     const int fast_ok = reinterpret_cast<uintptr_t>(data) % 16 == 0;
-    const PipeConst pc{1u, 1u << 29, 1u << 22};
+    const PipeConst pc{1u};
     uint32_t *bufA = static_cast<uint32_t *>(ws);
     uint32_t *bufB = bufA ? bufA + 8 * pl.n1 : nullptr;
     merkle_leaf_subtree<<<unsigned(pl.n1), LEAF_CTA, 0, stream>>>(
@@ -597,7 +593,7 @@ extern "C" int repops_merkle_verify(const void *leaf_bytes, uint64_t leaf_len, u
     if ((!leaf_bytes && leaf_len) || !root || !ok_out || nleaves == 0 || index >= nleaves)
         return REPOPS_ERR_INVALID_ARG;
     if (!proof && path_steps(nleaves, index) > 0) return REPOPS_ERR_INVALID_ARG;
-    const PipeConst pc{1u, 1u << 29, 1u << 22};
+    const PipeConst pc{1u};
     merkle_verify_kernel<<<1, 32, 0, stream>>>(static_cast<const uint8_t *>(leaf_bytes), leaf_len, nleaves, index,
                                                proof, root, ok_out, pc);
     return check_launch();
