@@ -2,9 +2,10 @@
 
 Each case plants one mistake in a copy of oracle/repops_oracle.c, builds it
 with the oracle's own flags, and runs the pin suite (tests/test_oracle_*.py)
-against it in a subprocess: the suite must fail.  The unmodified source must
+against it in a subprocess (several at a time): the suite must fail.  The unmodified source must
 pass.  Nothing here touches the CUDA library.
 """
+import concurrent.futures as cf
 import os
 import subprocess
 import sys
@@ -137,15 +138,35 @@ def run_pins(lib):
     return r.returncode, r.stdout[-2000:]
 
 
-def test_unmodified_source_passes_the_pins(tmp_path):
-    rc, out = run_pins(build_variant(tmp_path, "original", open(SRC).read()))
+def _variant_result(tmp_path, name, source):
+    return run_pins(build_variant(tmp_path, name, source))
+
+
+@pytest.fixture(scope="session")
+def results(tmp_path_factory):
+    """Builds the unmodified source and every mutant and runs the pin suite on
+    each, several subprocesses at a time; maps a case name (None: unmodified)
+    to (return code, output tail)."""
+    src = open(SRC).read()
+    cases = {None: src}
+    for name, (old, new) in MUTATIONS.items():
+        if src.count(old) == 1:
+            cases[name] = src.replace(old, new)
+    workers = max(1, min(8, (os.cpu_count() or 2) - 1))
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        futs = {name: ex.submit(_variant_result, tmp_path_factory.mktemp("mut"), "v", text)
+                for name, text in cases.items()}
+        return {name: f.result() for name, f in futs.items()}
+
+
+def test_unmodified_source_passes_the_pins(results):
+    rc, out = results[None]
     assert rc == 0, out
 
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
-def test_planted_mistake_fails_a_pin(tmp_path, name):
+def test_planted_mistake_fails_a_pin(results, name):
     old, new = MUTATIONS[name]
-    src = open(SRC).read()
-    assert src.count(old) == 1, "mutation anchor not found exactly once: " + name
-    rc, out = run_pins(build_variant(tmp_path, "m", src.replace(old, new)))
+    assert open(SRC).read().count(old) == 1, "mutation anchor not found exactly once: " + name
+    rc, out = results[name]
     assert rc != 0, "the pins did not catch: " + name
