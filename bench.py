@@ -534,34 +534,44 @@ def run_sweep(args):
 
 
 def run_sweep_gemm(dev, s, flush, peak):
+    """Every GEMM workload, L2 flushed before each timed launch.  Beside each,
+    the library's FP32 GEMM (torch.mm on cuBLAS, TF32 off: fused multiply-adds,
+    no fixed order) on the same operands, timed the same way: the pages state
+    their cost as the overhead of the order-fixed GEMM over that one."""
 
-    def timed(A, B, C):
-        M, K = A.shape
-        N = B.shape[1]
-        flops = 2.0 * M * N * K
+    def timed(fn, flops):
         reps = max(3, min(50, int(2e11 / max(flops, 1.0))))
         with torch.cuda.stream(s):
             for _ in range(3):
-                rp.gemm(A, B, out=C, stream=s)
+                fn()
             evs = []
             for _ in range(reps):
                 flush.zero_()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(s)
-                rp.gemm(A, B, out=C, stream=s)
+                fn()
                 e1.record(s)
                 evs.append((e0, e1))
         torch.cuda.synchronize(dev)
-        ms = sum(a.elapsed_time(b) for a, b in evs) / reps
-        return flops, ms
+        return sum(a.elapsed_time(b) for a, b in evs) / reps
 
     def emit(name, A, B, extra=None):
-        C = torch.empty((A.shape[0], B.shape[1]), dtype=torch.float32, device=dev)
-        flops, ms = timed(A, B, C)
-        cfg = rp.gemm_auto_config(A.shape[0], B.shape[1], A.shape[1])
+        M, K = A.shape
+        N = B.shape[1]
+        C = torch.empty((M, N), dtype=torch.float32, device=dev)
+        flops = 2.0 * M * N * K
+        ms = timed(lambda: rp.gemm(A, B, out=C, stream=s), flops)
+        tf32 = torch.backends.cuda.matmul.allow_tf32
+        torch.backends.cuda.matmul.allow_tf32 = False
+        try:
+            lib_ms = timed(lambda: torch.mm(A, B, out=C), flops)
+        finally:
+            torch.backends.cuda.matmul.allow_tf32 = tf32
+        kernel = "small-output" if rp.gemm_small_output(M, N, K) else "tiled config %d" % rp.gemm_auto_config(M, N, K)
         tf = flops / ms / 1e9
-        rec = {"sweep": name, "M": A.shape[0], "N": B.shape[1], "K": A.shape[1], "ms": ms,
-               "tflops": tf, "frac_of_fp32_peak": tf / peak, "tile_config": cfg}
+        rec = {"sweep": name, "M": M, "N": N, "K": K, "ms": ms,
+               "tflops": tf, "frac_of_fp32_peak": tf / peak, "kernel": kernel,
+               "library_fp32_gemm_ms": lib_ms, "overhead_vs_library": ms / lib_ms - 1.0}
         rec.update(extra or {})
         print(json.dumps(rec), flush=True)
         return flops, ms

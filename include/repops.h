@@ -156,10 +156,17 @@ int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K,
                          cudaStream_t stream);
 
 /* Loader paths for repops_gemm_f32_config. */
-#define REPOPS_LOADER_AUTO 0      /* TMA when operands allow it, else CPASYNC */
+#define REPOPS_LOADER_AUTO 0      /* TMA when operands allow it, else CPASYNC; with
+                                     config -1, the DIRECT kernel for small outputs
+                                     (repops_gemm_small_output) */
 #define REPOPS_LOADER_TMA 1       /* tensor-memory-accelerator tiles; needs 16-byte
                                      aligned A/B and lda, ldb multiples of 4 */
 #define REPOPS_LOADER_CPASYNC 2   /* 4-byte cp.async with zero fill; any alignment */
+#define REPOPS_LOADER_DIRECT 3    /* the small-output kernel: 16 x 32 CTA tiles of
+                                     128 threads, 4-byte cp.async ring, any
+                                     alignment and storage order; `config` is
+                                     ignored.  Plain and typed GEMMs; the batched
+                                     call answers INVALID_ARG */
 
 /* As repops_gemm_f32_ex with an explicit tile configuration (0 <=
  * config < repops_gemm_config_count(), or -1 for the automatic choice) and
@@ -187,8 +194,13 @@ int repops_gemm_config_info(int config, int *bm, int *bn, int *threads,
 int repops_gemm_config_occupancy(int config);
 
 /* The configuration repops_gemm_f32 would choose for an M x N output on the
- * current device (-1 when M or N is 0). */
+ * current device (-1 when M or N is 0).  The tiled configuration; see
+ * repops_gemm_small_output for when the small-output kernel runs instead. */
 int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
+
+/* 1 when repops_gemm_f32 (automatic configuration and loader) runs an M x N x K
+ * problem on the small-output kernel (REPOPS_LOADER_DIRECT), else 0. */
+int repops_gemm_small_output(int64_t M, int64_t N, int64_t K);
 
 /* ------------------------------------------------------------------------ */
 /* Batched GEMM with a fused epilogue                                        */

@@ -47,6 +47,9 @@ def test_gemm_256_uniform_bit_exact(rp, orc):
         for loader in (rp.LOADER_TMA, rp.LOADER_CPASYNC):
             C = run(rp, A, B, cfg, loader)
             assert torch.equal(bits(C), want), (cfg, loader)
+    assert torch.equal(bits(run(rp, A, B, -1, rp.LOADER_DIRECT)), want)
+    # the automatic choice runs this size on the small-output kernel
+    assert rp.gemm_small_output(256, 256, 256)
     assert torch.equal(bits(run(rp, A, B)), want)
 
 
@@ -76,6 +79,8 @@ def test_gemm_ragged_all_configs_layouts_loaders(rp, orc, M, N, K):
             for loader in loaders:
                 C = run(rp, Aop, Bop, cfg, loader)
                 assert torch.equal(bits(C), want), (ta, tb, cfg, loader)
+        C = run(rp, Aop, Bop, -1, rp.LOADER_DIRECT)
+        assert torch.equal(bits(C), want), (ta, tb, "direct")
 
 
 def test_gemm_crafted_detectors_all_configs(rp, golden):
@@ -91,11 +96,11 @@ def test_gemm_crafted_detectors_all_configs(rp, golden):
     # FMA detector in row 69 (a ragged tile edge) against column 67
     A[69].zero_(); A[69, 38:40] = a_fd
     B[:, 67].zero_(); B[38:40, 67] = b_fd
-    for cfg in all_configs(rp):
-        for loader in (rp.LOADER_TMA, rp.LOADER_CPASYNC):
-            C = run(rp, A, B, cfg, loader).cpu()
-            assert int(C[33, 0].view(torch.int32)) == int(od["expected_bits"], 16)
-            assert int(C[69, 67].view(torch.int32)) == int(fd["expected_bits"], 16), (cfg, loader)
+    cases = [(c, l) for c in all_configs(rp) for l in (rp.LOADER_TMA, rp.LOADER_CPASYNC)]
+    for cfg, loader in cases + [(-1, rp.LOADER_DIRECT)]:
+        C = run(rp, A, B, cfg, loader).cpu()
+        assert int(C[33, 0].view(torch.int32)) == int(od["expected_bits"], 16)
+        assert int(C[69, 67].view(torch.int32)) == int(fd["expected_bits"], 16), (cfg, loader)
 
 
 def test_gemm_integer_exact_large(rp):
@@ -107,6 +112,7 @@ def test_gemm_integer_exact_large(rp):
     want = (A.cpu().to(torch.int64) @ B.cpu().to(torch.int64)).to(torch.float32)
     for cfg in all_configs(rp):
         assert torch.equal(run(rp, A, B, cfg).cpu(), want), cfg
+    assert torch.equal(run(rp, A, B, -1, rp.LOADER_DIRECT).cpu(), want)
 
 
 def test_gemm_unaligned_and_padded_operands(rp, orc):
@@ -118,9 +124,10 @@ def test_gemm_unaligned_and_padded_operands(rp, orc):
     want = np_bits(oracle_full(orc, A, B))
     Cbuf = torch.full((M, 104), float("nan"), device=DEV)
     C = Cbuf[:, 1:1 + N]                                  # ldc = 104, unaligned
-    for cfg in all_configs(rp):
-        run(rp, A, B, cfg, 0, out=C)
-        assert torch.equal(bits(C), want), cfg
+    for cfg, loader in [(c, 0) for c in all_configs(rp)] + [(-1, rp.LOADER_DIRECT)]:
+        C.fill_(float("nan"))
+        run(rp, A, B, cfg, loader, out=C)
+        assert torch.equal(bits(C), want), (cfg, loader)
     # padding columns untouched
     assert torch.isnan(Cbuf[:, 0]).all() and torch.isnan(Cbuf[:, 1 + N:]).all()
     with pytest.raises(rp.RepopsError):
@@ -144,8 +151,8 @@ def test_gemm_output_guard_band(rp):
     B = inputs.normal((K, N), 1.0, 9, DEV)
     buf = torch.full((M * N + 2048,), 12345.0, device=DEV)
     C = buf[1024:1024 + M * N].view(M, N)
-    for cfg in all_configs(rp):
-        run(rp, A, B, cfg, out=C)
+    for cfg, loader in [(c, 0) for c in all_configs(rp)] + [(-1, rp.LOADER_DIRECT)]:
+        run(rp, A, B, cfg, loader, out=C)
         assert (buf[:1024] == 12345.0).all() and (buf[1024 + M * N:] == 12345.0).all()
 
 
@@ -283,3 +290,18 @@ def test_row_major_a_large_problem_same_bits(rp, orc):
     # both transposes: B column-major as well
     Bcm = B.t().contiguous().t()
     assert torch.equal(run(rp, A, Bcm).view(torch.int32), C_auto.view(torch.int32))
+
+
+def test_gemm_direct_loader_typed_and_batched(rp, orc):
+    # the typed call widens its operands and runs the plain GEMM: the small-output
+    # kernel gives the same bytes as the tiled one; the batched call refuses it
+    M, N, K = 45, 70, 129
+    A = inputs.normal((M, K), 1.0, 41, DEV).half()
+    B = inputs.normal((K, N), 1.0, 42, DEV).half()
+    want = np_bits(orc.gemm(A.float().cpu().numpy(), B.float().cpu().numpy()))
+    for loader in (rp.LOADER_AUTO, rp.LOADER_DIRECT):
+        C = rp.gemm_typed(A, B, loader=loader)
+        torch.cuda.synchronize()
+        assert torch.equal(bits(C), want), loader
+    with pytest.raises(rp.RepopsError):
+        rp.gemm_batched(A.float().unsqueeze(0), B.float().unsqueeze(0), loader=rp.LOADER_DIRECT)

@@ -33,18 +33,18 @@ memory and streams.
 import ctypes
 
 from . import _capi
-from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_TMA,
+from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
 __all__ = ["load", "version", "gemm", "gemm_host", "gemm_config_count", "gemm_config_info",
-           "gemm_auto_config", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
+           "gemm_auto_config", "gemm_small_output", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
            "convert", "gemm_typed", "rolling_hash", "TYPE_F32", "TYPE_F16", "TYPE_BF16",
            "colsum", "gelu_backward", "rmsnorm_backward", "softmax_backward",
            "swiglu", "swiglu_backward", "rope_frequencies", "rope_table", "rope",
            "device_status", "RepopsError", "ACT_NONE", "ACT_GELU",
-           "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "MEAN_MAX_CONTRIBUTORS"]
+           "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "LOADER_DIRECT", "MEAN_MAX_CONTRIBUTORS"]
 
 
 # Outputs the functions below allocate come from torch's caching allocator on
@@ -229,6 +229,11 @@ def gemm_config_info(config: int) -> dict:
 
 def gemm_auto_config(M: int, N: int, K: int) -> int:
     return load().repops_gemm_auto_config(M, N, K)
+
+
+def gemm_small_output(M: int, N: int, K: int) -> bool:
+    """True when the automatic GEMM runs M x N x K on the small-output kernel."""
+    return bool(load().repops_gemm_small_output(M, N, K))
 
 
 def sort_ids(ids) -> list:

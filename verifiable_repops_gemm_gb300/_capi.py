@@ -22,6 +22,7 @@ ERR_UNSUPPORTED = -7
 LOADER_AUTO = 0
 LOADER_TMA = 1
 LOADER_CPASYNC = 2
+LOADER_DIRECT = 3
 
 MEAN_MAX_CONTRIBUTORS = 1024
 
@@ -40,6 +41,7 @@ SIGNATURES = {
     "repops_gemm_config_count": (_i32, []),
     "repops_gemm_config_info": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp]),
     "repops_gemm_auto_config": (_i32, [_i64, _i64, _i64]),
+    "repops_gemm_small_output": (_i32, [_i64, _i64, _i64]),
     "repops_sort_ids": (_i32, [_i32, _vp, _vp, _vp, _vp]),
     "repops_fixed_order_mean_sgd": (_i32, [_i32, _i64, _vp, _vp, _f32, _vp, _vp]),
     "repops_merkle_sha256": (_i32, [_vp, _u64, _u32, _vp, _vp]),

@@ -260,12 +260,23 @@ int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool 
     return REPOPS_OK;
 }
 
+// The small-output kernel (16 x 32 CTA tiles) runs outputs of at most
+// 196,608 elements, where the tiled kernels leave most SMs idle; measured
+// crossover on GB300 between 384^2 (small kernel 9.1 us, tiled 13.1 us) and
+// 512^2 (19.1 against 16.9 us); 64 x 2048 x 2048: 45.9 against 65.5 us.
+constexpr int64_t kSmallMaxOutputs = 3 << 16;
+
+bool small_output(int64_t M, int64_t N, int64_t K) {
+    return M > 0 && N > 0 && K > 0 && M * N <= kSmallMaxOutputs && N <= 65535LL * 32;
+}
+
 int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
                   cudaStream_t stream) {
     if (M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
     if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
-    if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC)
+    if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC &&
+        loader != REPOPS_LOADER_DIRECT)
         return REPOPS_ERR_INVALID_ARG;
     const int64_t a_rows = transA ? K : M, a_cols = transA ? M : K;
     const int64_t b_rows = transB ? N : K, b_cols = transB ? K : N;
@@ -298,6 +309,8 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     p.stream = stream;
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
+    if (loader == REPOPS_LOADER_DIRECT || (loader == REPOPS_LOADER_AUTO && config < 0 && small_output(M, N, K)))
+        return gemm_small_launch(p);
 
     const int cfg = config >= 0 ? config : choose_config(M, N, K);
     bool tma_ok = gemm_tma_eligible(p);
@@ -670,6 +683,8 @@ extern "C" int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float
 }
 
 extern "C" int repops_gemm_config_count(void) { return kGemmConfigCount; }
+
+extern "C" int repops_gemm_small_output(int64_t M, int64_t N, int64_t K) { return repops::small_output(M, N, K) ? 1 : 0; }
 
 extern "C" int repops_gemm_config_info(int config, int *bm, int *bn, int *threads, int *tm, int *tn) {
     if (config < 0 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;

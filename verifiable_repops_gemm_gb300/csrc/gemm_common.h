@@ -58,4 +58,7 @@ constexpr int kGemmConfigCount = 5;
 // True when the TMA loader can serve this problem (alignment, extents).
 bool gemm_tma_eligible(const GemmProblem &p);
 
+// The small-output kernel (gemm_small.cu): plain GEMM only (p.ex false).
+int gemm_small_launch(const GemmProblem &p);
+
 }  // namespace repops
