@@ -234,6 +234,25 @@ def max_over_ranks(x, world, dev):
 
 # ------------------------------------------------------------ CPU oracle ----
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def host_cores():
     try:
         return max(1, len(os.sched_getaffinity(0)))
@@ -367,6 +386,7 @@ def run_reference(args):
         "parts": {"mean_sgd": {"value": 18 * m * 4 * args.steps / tm / 1e9, "unit": "GB/s"},
                   "merkle": {"value": (32 << 20) * args.steps / tk / 1e9, "unit": "GB/s"}},
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "cpu_model": cpu_model(),
                          "sample": sample},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -544,7 +564,7 @@ def run_ours(args):
     if cpu is not None:
         allc = cpu["all_cores"]
         line["cpu_baseline"] = {"value": allc["gemm_tflops"], "unit": "TFLOP/s", "cores": cpu["cores"],
-                                "kind": "oracle", "sample": cpu["sample"],
+                                "kind": "oracle", "sample": cpu["sample"], "cpu_model": cpu_model(),
                                 "parts": {"mean_sgd_gbs": allc["mean_gbs"],
                                           "merkle_gbs": allc["merkle_gbs"]},
                                 "single_thread": {"value": cpu["gemm_tflops"], "cores": 1,
@@ -584,13 +604,14 @@ def run_sweep(args):
 
 
 def run_sweep_gemm(dev, s, flush, peak):
-    """Every GEMM workload, L2 flushed before each timed launch.  Beside each,
+    """Every GEMM workload, L2 flushed before each timed launch, the median of
+    at least 10 launches.  Beside each,
     the library's FP32 GEMM (torch.mm on cuBLAS, TF32 off: fused multiply-adds,
     no fixed order) on the same operands, timed the same way: the pages state
     their cost as the overhead of the order-fixed GEMM over that one."""
 
     def timed(fn, flops):
-        reps = max(3, min(50, int(2e11 / max(flops, 1.0))))
+        reps = max(10, min(50, int(2e11 / max(flops, 1.0))))
         with torch.cuda.stream(s):
             for _ in range(3):
                 fn()
@@ -603,7 +624,7 @@ def run_sweep_gemm(dev, s, flush, peak):
                 e1.record(s)
                 evs.append((e0, e1))
         torch.cuda.synchronize(dev)
-        return sum(a.elapsed_time(b) for a, b in evs) / reps
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
 
     def emit(name, A, B, extra=None):
         M, K = A.shape
