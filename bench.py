@@ -56,8 +56,8 @@ L2_BYTES = 129 * 10 ** 6
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
 # valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "9767fe4e2afd909f89b1772567a0d0d4d3ceedd29bb5b6f2e6238f5f94b97270",
-                "bytes_per_launch": 4695637760 + 267883264}
+GEMM_TRAFFIC = {"src_sha256": "3d8717bcffed01d029388328e35f29de1c586561eafeee42115c1faa573a232f",
+                "bytes_per_launch": 3770000000 + 266070000}
 
 
 def measured_peaks():
