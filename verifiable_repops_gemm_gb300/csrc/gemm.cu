@@ -262,8 +262,8 @@ int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool 
 
 // The small-output kernel (16 x 32 CTA tiles) runs outputs of at most
 // 196,608 elements, where the tiled kernels leave most SMs idle; measured
-// crossover on GB300 between 384^2 (small kernel 9.1 us, tiled 13.1 us) and
-// 512^2 (19.1 against 16.9 us); 64 x 2048 x 2048: 45.9 against 65.5 us.
+// crossover on GB300 between 384^2 (small kernel 8.4 us, tiled 13.1 us) and
+// 512^2 (18.8 against 16.9 us).
 constexpr int64_t kSmallMaxOutputs = 3 << 16;
 
 bool small_output(int64_t M, int64_t N, int64_t K) {

@@ -6,13 +6,15 @@
 // rounded to binary32 and added in increasing k from +0.  The chains are the
 // same as in the tiled kernels -- only the launch shape differs: 16 x 32 CTA
 // tiles of 128 threads, each thread two rows by two columns, operands staged
-// in k-chunks of 32 through a 4-deep cp.async ring (4-byte copies, any
-// alignment, either storage order), so a 256^3 problem runs as 128 CTAs.
-// Measured on GB300, CUDA-graph replays (operands in L2): 256^3 in 5.3 us
-// against 9.5 us on the tiled kernels (6.0 us for the library's FP32 GEMM with
-// fused multiply-adds); 384^3 9.1 against 13.1 us; 512^3 19.1 against 16.9 us,
-// where the tiled kernels take over.  Computing each copy's address once per
-// thread instead of per chunk took 256^3 from 9.5 to 5.3 us.
+// in k-chunks of 64 through a 3-deep cp.async ring (4-byte copies, any
+// alignment, either storage order; 39 KB of shared memory), so a 256^3
+// problem runs as 128 CTAs.  Measured on GB300, CUDA-graph replays (operands
+// in L2): 256^3 in 4.4 us against 9.5 us on the tiled kernels (6.0 us for the
+// library's FP32 GEMM with fused multiply-adds); 384^3 8.4 against 13.1 us;
+// 512^3 18.8 against 16.9 us, where the tiled kernels take over.  Computing
+// each copy's address once per thread instead of per chunk took 256^3 from
+// 9.5 to 5.3 us, chunks of 64 instead of 32 to 4.4 us; one output per thread
+// row (8 x 32 tiles, twice the warps) was slower from 256^3 up.
 #include "gemm_common.h"
 #include "gemm_kernels.cuh"
 #include "internal.cuh"
@@ -26,7 +28,7 @@ using gemm::pack2;
 using gemm::u64;
 using gemm::unpack2;
 
-constexpr int kSmBM = 16, kSmBN = 32, kSmKC = 32;   // CTA tile and k-chunk
+constexpr int kSmBM = 16, kSmBN = 32, kSmKC = 64;   // CTA tile and k-chunk
 constexpr int kSmThreads = 128;                      // 8 x 16 threads, 2 x 2 outputs each
 constexpr int kSmLdA = kSmBM + 2, kSmLdB = kSmBN + 2;   // padded rows (even: 8-byte reads)
 
@@ -147,19 +149,16 @@ gemm_small_kernel(int transA, int transB, int64_t M, int64_t N, int64_t K,
     }
 }
 
-constexpr int kSmStages = 4;
+constexpr int kSmStages = 3;
 
 }  // namespace
 
 int gemm_small_launch(const GemmProblem &p) {
     const int64_t gm = (p.M + kSmBM - 1) / kSmBM, gn = (p.N + kSmBN - 1) / kSmBN;
     if (gm > 0x7fffffffLL || gn > 65535) return REPOPS_ERR_UNSUPPORTED;
-    const int smem = int(sizeof(SmallSmem<kSmStages>));
+    constexpr int smem = int(sizeof(SmallSmem<kSmStages>));
+    static_assert(smem <= 48 * 1024, "the ring fits the default dynamic shared memory limit");
     auto kern = gemm_small_kernel<kSmStages>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return set_cuda_error(e);
-    }
     kern<<<dim3(unsigned(gm), unsigned(gn)), kSmThreads, smem, p.stream>>>(
         p.transA, p.transB, p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc);
     return check_launch();
