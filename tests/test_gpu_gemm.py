@@ -62,7 +62,7 @@ def make_operand(X, transposed):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 1), (7, 5, 3), (129, 257, 33), (300, 200, 100),
-                                   (64, 64, 32), (65, 129, 97), (256, 130, 1000)])
+                                   (64, 64, 32), (65, 129, 97), (256, 130, 1000), (17, 19, 20011)])
 def test_gemm_ragged_all_configs_layouts_loaders(rp, orc, M, N, K):
     A = inputs.normal((M, K), 1.0, 10 + M, DEV)
     B = inputs.normal((K, N), 1.0, 20 + N, DEV)

@@ -130,10 +130,15 @@ struct RowRuns {
             }
             const int have = runs - u0;         // runs present in the group, >= 1
             float g = __shfl_sync(0xffffffffu, acc, 0);
+            if (have >= RUN) {                  // a full group (warp-uniform): no per-lane test
 #pragma unroll
-            for (int i = 1; i < RUN; ++i) {
-                const float o = __shfl_sync(0xffffffffu, acc, i);
-                if (i < have) g = combine<OP>(g, o);
+                for (int i = 1; i < RUN; ++i) g = combine<OP>(g, __shfl_sync(0xffffffffu, acc, i));
+            } else {
+#pragma unroll
+                for (int i = 1; i < RUN; ++i) {
+                    const float o = __shfl_sync(0xffffffffu, acc, i);
+                    if (i < have) g = combine<OP>(g, o);
+                }
             }
             if constexpr (GROUPS == 1) root = g;
             else if (lane == 0) gb[j * (T / RUN) + warp] = g;
