@@ -56,8 +56,8 @@ L2_BYTES = 129 * 10 ** 6
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
 # valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "3d8717bcffed01d029388328e35f29de1c586561eafeee42115c1faa573a232f",
-                "bytes_per_launch": 3770000000 + 266070000}
+GEMM_TRAFFIC = {"src_sha256": "6b9cc139ef0c83c832e861e28b5591bb26e83c2eff18074c611a650c2f157963",
+                "bytes_per_launch": 3820000000 + 266220000}
 
 
 def measured_peaks():

@@ -23,11 +23,6 @@
 namespace repops {
 namespace {
 
-using gemm::fold2;
-using gemm::pack2;
-using gemm::u64;
-using gemm::unpack2;
-
 constexpr int kSmBM = 16, kSmBN = 32, kSmKC = 64;   // CTA tile and k-chunk
 constexpr int kSmThreads = 128;                      // 8 x 16 threads, 2 x 2 outputs each
 constexpr int kSmLdA = kSmBM + 2, kSmLdB = kSmBN + 2;   // padded rows (even: 8-byte reads)

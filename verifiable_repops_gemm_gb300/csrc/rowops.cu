@@ -311,6 +311,15 @@ __device__ __forceinline__ void for_each_row(int64_t rows, int64_t n, const floa
     cp_async_wait<0>();
 }
 
+// (a, b) <- (exp(a - m), exp(b - m)), the subtractions as one packed add of -m
+__device__ __forceinline__ void exp_minus2(float &a, float &b, float m) {
+    float d0, d1;
+    unpack2(add2_rn(pack2(a, b), pack2(-m, -m)), d0, d1);
+    const float2 e = exp_fixed2(d0, d1);
+    a = e.x;
+    b = e.y;
+}
+
 struct Ident {
     __device__ __forceinline__ float operator()(float x) const { return x; }
 };
@@ -332,7 +341,7 @@ softmax_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_
 #pragma unroll
         for (int j = 0; j < R; ++j)
 #pragma unroll
-            for (int i = 0; i < RUN; ++i) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+            for (int i = 0; i < RUN; i += 2) exp_minus2(rr.v[j][i], rr.v[j][i + 1], m);
         const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs));
 #pragma unroll
         for (int j = 0; j < R; ++j)
@@ -380,7 +389,7 @@ softmax_causal_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x,
             // neither folded nor stored)
             if (rr.len[j] == 0) continue;
 #pragma unroll
-            for (int i = 0; i < RUN; ++i) rr.v[j][i] = exp_fixed(__fsub_rn(rr.v[j][i], m));
+            for (int i = 0; i < RUN; i += 2) exp_minus2(rr.v[j][i], rr.v[j][i + 1], m);
         }
         const float inv = __frcp_rn(rr.template reduce<Op::Sum>(Ident(), gbuf, phase, runs));
 #pragma unroll
@@ -548,8 +557,8 @@ gelu_kernel(int64_t n, const float *__restrict__ x, float *__restrict__ y, int v
         const int64_t n4 = n / 4;
         for (int64_t i = first; i < n4; i += stride) {
             const float4 v = __ldcs(reinterpret_cast<const float4 *>(x) + i);
-            __stcs(reinterpret_cast<float4 *>(y) + i,
-                   make_float4(gelu_fixed(v.x), gelu_fixed(v.y), gelu_fixed(v.z), gelu_fixed(v.w)));
+            const float2 lo = gelu_fixed2(v.x, v.y), hi = gelu_fixed2(v.z, v.w);
+            __stcs(reinterpret_cast<float4 *>(y) + i, make_float4(lo.x, lo.y, hi.x, hi.y));
         }
         for (int64_t i = n4 * 4 + first; i < n; i += stride) y[i] = gelu_fixed(x[i]);
     } else {
