@@ -166,7 +166,8 @@ int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K,
                                      128 threads, 4-byte cp.async ring, any
                                      alignment and storage order; `config` is
                                      ignored.  Plain and typed GEMMs; the batched
-                                     call answers INVALID_ARG */
+                                     call answers INVALID_ARG; N above 2,097,120
+                                     (65535 column tiles) UNSUPPORTED */
 
 /* As repops_gemm_f32_ex with an explicit tile configuration (0 <=
  * config < repops_gemm_config_count(), or -1 for the automatic choice) and
@@ -199,7 +200,9 @@ int repops_gemm_config_occupancy(int config);
 int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
 
 /* 1 when repops_gemm_f32 (automatic configuration and loader) runs an M x N x K
- * problem on the small-output kernel (REPOPS_LOADER_DIRECT), else 0. */
+ * problem on the small-output kernel (REPOPS_LOADER_DIRECT): M, N, K > 0 and
+ * M * N <= 196,608 (384 x 384 and below, where the tiled kernels leave most
+ * SMs idle); else 0.  Host-only; either kernel gives the same bits. */
 int repops_gemm_small_output(int64_t M, int64_t N, int64_t K);
 
 /* ------------------------------------------------------------------------ */
