@@ -234,6 +234,25 @@ def max_over_ranks(x, world, dev):
 
 # ------------------------------------------------------------ CPU oracle ----
 
+def sha256_probe_rate(dev, sms, iters=500):
+    """Compressions per second of the library's SHA-256 compression with its
+    message in registers (repops_sha256_rate_probe: no loads, no tree), 8 CTAs
+    of 128 threads per SM, iters + 1 compressions a thread, median of 5
+    launches: the ceiling the Merkle kernels are measured against."""
+    threads = sms * 8 * 128
+    out = torch.empty((threads, 8), dtype=torch.int32, device=dev)
+    rp.sha256_rate_probe(threads, iters, out=out)
+    ts = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        rp.sha256_rate_probe(threads, iters, out=out)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1))
+    return threads * (iters + 1) / (statistics.median(ts) / 1e3) / 1e9
+
+
 def cpu_model():
     """The host CPU's model name (lscpu, else /proc/cpuinfo), or "unknown"."""
     try:
@@ -498,6 +517,7 @@ def run_ours(args):
                    "theta_root": bytes(theta_root.cpu().numpy()).hex(),
                    "theta_updates": args.warmup + args.steps}
     e2e = run_e2e(w, dev, args.e2e_steps) if args.e2e_steps > 0 else None
+    probe_rate = sha256_probe_rate(dev, sms)   # outside the timed region
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample()
@@ -544,7 +564,12 @@ def run_ours(args):
                                              "adds run on the multiply-add pipe)"
                                              % (sms, peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL),
                                                 SHA_ALU_OPS_PER_COMPRESSION),
-                                    "frac_if_both_pipes_shared_all_ops": comp_rate / comp_peak_shared}},
+                                    "frac_if_both_pipes_shared_all_ops": comp_rate / comp_peak_shared,
+                                    "measured_ceiling": {
+                                        "value": probe_rate, "unit": "Gcompressions/s",
+                                        "basis": "repops_sha256_rate_probe: the same compression, message in "
+                                                 "registers, no loads or tree, 8 x 128 threads per SM"},
+                                    "frac_of_measured_ceiling": comp_rate / probe_rate}},
         },
         "roofline": {"kernel": gemm_kernel_label(), "bound": "alu",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

@@ -492,6 +492,17 @@ int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len,
                                   const float *etas, float *theta, uint32_t leaf,
                                   uint8_t *roots_out, cudaStream_t stream);
 
+/* Compression-rate probe: the ceiling the Merkle kernels are measured against.
+ * Launches `threads` threads (a multiple of 128, 128 .. 2^24) on `stream`; thread
+ * t computes, with the library's SHA-256 compression and its message held in
+ * registers (no memory traffic, no tree), the digest of the message M_t
+ * repeated `iters` times (0 .. 2^30), M_t being the 64 bytes of the 16
+ * big-endian words 16t, 16t + 1, ..., 16t + 15, and writes it to
+ * digests[8t .. 8t + 7] (device memory, big-endian state words).  That is
+ * iters + 1 compressions a thread.  INVALID_ARG for a null pointer or a bad
+ * count. */
+int repops_sha256_rate_probe(uint32_t threads, uint32_t iters, uint32_t *digests, cudaStream_t stream);
+
 /* Size of the fixed device scratch behind repops_merkle_sha256_noalloc. */
 #define REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES (1u << 20)
 

@@ -78,3 +78,20 @@ def test_merkle_4gib_tensor(rp, orc):
     x = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300, DEV)
     got = root(rp, x)
     assert got == orc.merkle_root(x.cpu().numpy(), 4096)
+
+
+def test_sha256_rate_probe_digests(rp):
+    # thread t hashes its 64-byte block (big-endian words 16t .. 16t + 15)
+    # repeated `iters` times; hashlib is the reference
+    import hashlib
+    import struct
+    for iters in (0, 1, 3):
+        D = rp.sha256_rate_probe(256, iters)
+        torch.cuda.synchronize()
+        got = D.cpu().numpy().astype(np.uint32)
+        for t in (0, 1, 127, 255):
+            block = struct.pack(">16I", *[16 * t + i for i in range(16)])
+            want = hashlib.sha256(block * iters).digest()
+            assert struct.pack(">8I", *got[t]) == want, (iters, t)
+    with pytest.raises(rp.RepopsError):
+        rp.sha256_rate_probe(100, 1)

@@ -37,7 +37,7 @@ from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRE
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
 __all__ = ["load", "version", "gemm", "gemm_host", "gemm_config_count", "gemm_config_info",
-           "gemm_auto_config", "gemm_small_output", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
+           "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
            "convert", "gemm_typed", "rolling_hash", "TYPE_F32", "TYPE_F16", "TYPE_BF16",
@@ -234,6 +234,21 @@ def gemm_auto_config(M: int, N: int, K: int) -> int:
 def gemm_small_output(M: int, N: int, K: int) -> bool:
     """True when the automatic GEMM runs M x N x K on the small-output kernel."""
     return bool(load().repops_gemm_small_output(M, N, K))
+
+
+def sha256_rate_probe(threads: int, iters: int, out=None, stream=None):
+    """(threads, 8) int32 tensor of SHA-256 state words: thread t's digest of
+    its 64-byte block (big-endian words 16t .. 16t + 15) repeated `iters`
+    times, computed with the message in registers (repops_sha256_rate_probe,
+    the Merkle kernels' compression-rate ceiling)."""
+    import torch
+    if out is None:
+        out = torch.empty((threads, 8), dtype=torch.int32, device="cuda")
+    if out.dtype != torch.int32 or not out.is_contiguous() or out.numel() != 8 * threads:
+        raise ValueError("out must be a contiguous int32 tensor of threads x 8 words")
+    rc = load().repops_sha256_rate_probe(threads, iters, out.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_sha256_rate_probe")
+    return out
 
 
 def sort_ids(ids) -> list:

@@ -48,6 +48,7 @@ SIGNATURES = {
     "repops_merkle_workspace_bytes": (_u64, [_u64, _u32]),
     "repops_merkle_sha256_ws": (_i32, [_vp, _u64, _u32, _vp, _vp, _u64, _vp]),
     "repops_merkle_sha256_noalloc": (_i32, [_vp, _u64, _u32, _vp, _vp]),
+    "repops_sha256_rate_probe": (_i32, [_u32, _u32, _vp, _vp]),
     "repops_merkle_tree_bytes": (_u64, [_u64, _u32]),
     "repops_merkle_tree_sha256": (_i32, [_vp, _u64, _u32, _vp, _u64, _vp, _vp]),
     "repops_merkle_proof_steps": (_i32, [_u64, _u64]),

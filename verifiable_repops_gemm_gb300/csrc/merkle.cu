@@ -600,6 +600,53 @@ extern "C" int repops_merkle_verify(const void *leaf_bytes, uint64_t leaf_len, u
 }
 
 // ---------------------------------------------------------------------------
+// Compression-rate probe: the same compression with its message in registers,
+// no loads and no tree, as the ceiling the Merkle kernels are measured
+// against.  Thread t hashes the message M_t^iters (M_t = the 16 big-endian
+// words 16t, 16t + 1, ..., 16t + 15, repeated iters times) and writes its
+// SHA-256 digest as 8 words.
+// ---------------------------------------------------------------------------
+
+namespace repops {
+namespace {
+
+__global__ void __launch_bounds__(LEAF_CTA)
+sha256_rate_kernel(uint32_t iters, uint32_t *__restrict__ out, const PipeConst pc) {
+    const uint32_t t = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t st[8];
+    sha256_init(st);
+#pragma unroll 1
+    for (uint32_t r = 0; r < iters; ++r) {
+        uint32_t W[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) W[i] = 16u * t + uint32_t(i);
+        sha256_compress(st, W, pc);
+    }
+    const uint64_t bits = uint64_t(iters) * 512u;
+    uint32_t W[16];
+    W[0] = 0x80000000u;
+#pragma unroll
+    for (int i = 1; i < 14; ++i) W[i] = 0u;
+    W[14] = uint32_t(bits >> 32);
+    W[15] = uint32_t(bits);
+    sha256_compress(st, W, pc);
+#pragma unroll
+    for (int w = 0; w < 8; ++w) out[8 * uint64_t(t) + w] = st[w];
+}
+
+}  // namespace
+}  // namespace repops
+
+extern "C" int repops_sha256_rate_probe(uint32_t threads, uint32_t iters, uint32_t *digests, cudaStream_t stream) {
+    using namespace repops;
+    if (!digests || threads == 0 || threads % LEAF_CTA != 0 || threads > (1u << 24) || iters > (1u << 30))
+        return REPOPS_ERR_INVALID_ARG;
+    const PipeConst pc{1u};
+    sha256_rate_kernel<<<threads / LEAF_CTA, LEAF_CTA, 0, stream>>>(iters, digests, pc);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------------------
 // Allocation-free variant.
 //
 // For callers that must not allocate device memory when they hash: a host
