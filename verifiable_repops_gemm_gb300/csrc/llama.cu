@@ -29,16 +29,32 @@ __device__ __forceinline__ float sigmoid_fixed(float x) {
     return __frcp_rn(__fadd_rn(1.0f, exp_fixed(-x)));   // correctly rounded 1/(1 + e)
 }
 
+// Two sigmoids: the same steps lane by lane, the exponentials and the 1 + e
+// additions of the pair as packed adds (exp_fixed2): the same bits.
+__device__ __forceinline__ float2 sigmoid_fixed2(float x0, float x1) {
+    const float2 e = exp_fixed2(-x0, -x1);
+    float d0, d1;
+    unpack2(add2_rn(pack2(1.0f, 1.0f), pack2(e.x, e.y)), d0, d1);
+    return make_float2(__frcp_rn(d0), __frcp_rn(d1));
+}
+
 __device__ __forceinline__ float swiglu1(float g, float u) {
     return __fmul_rn(__fmul_rn(g, sigmoid_fixed(g)), u);
 }
 
-__device__ __forceinline__ void swiglu_grad1(float g, float u, float dh, float &dg, float &du) {
-    const float sg = sigmoid_fixed(g);
+__device__ __forceinline__ float swiglu_s(float g, float u, float sg) {
+    return __fmul_rn(__fmul_rn(g, sg), u);
+}
+
+__device__ __forceinline__ void swiglu_grad_s(float g, float u, float dh, float sg, float &dg, float &du) {
     du = __fmul_rn(dh, __fmul_rn(g, sg));
     const float t = __fmul_rn(dh, u);
     const float d = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(g, __fsub_rn(1.0f, sg))));
     dg = __fmul_rn(t, d);
+}
+
+__device__ __forceinline__ void swiglu_grad1(float g, float u, float dh, float &dg, float &du) {
+    swiglu_grad_s(g, u, dh, sigmoid_fixed(g), dg, du);
 }
 
 // Columns in units of 4 (vec) or 1; h may be g or u (each element is read
@@ -55,8 +71,9 @@ swiglu_kernel(int64_t rows, int64_t cols, const float *g, int64_t ldg, const flo
             if (vec) {
                 const float4 a = reinterpret_cast<const float4 *>(gr)[c];
                 const float4 b = reinterpret_cast<const float4 *>(ur)[c];
-                reinterpret_cast<float4 *>(hr)[c] =
-                    make_float4(swiglu1(a.x, b.x), swiglu1(a.y, b.y), swiglu1(a.z, b.z), swiglu1(a.w, b.w));
+                const float2 s01 = sigmoid_fixed2(a.x, a.y), s23 = sigmoid_fixed2(a.z, a.w);
+                reinterpret_cast<float4 *>(hr)[c] = make_float4(swiglu_s(a.x, b.x, s01.x), swiglu_s(a.y, b.y, s01.y),
+                                                                swiglu_s(a.z, b.z, s23.x), swiglu_s(a.w, b.w, s23.y));
             } else {
                 hr[c] = swiglu1(gr[c], ur[c]);
             }
@@ -78,10 +95,11 @@ swiglu_backward_kernel(int64_t rows, int64_t cols, const float *g, int64_t ldg, 
                 const float4 b = reinterpret_cast<const float4 *>(ur)[c];
                 const float4 d = reinterpret_cast<const float4 *>(dr)[c];
                 float4 og, ou;
-                swiglu_grad1(a.x, b.x, d.x, og.x, ou.x);
-                swiglu_grad1(a.y, b.y, d.y, og.y, ou.y);
-                swiglu_grad1(a.z, b.z, d.z, og.z, ou.z);
-                swiglu_grad1(a.w, b.w, d.w, og.w, ou.w);
+                const float2 s01 = sigmoid_fixed2(a.x, a.y), s23 = sigmoid_fixed2(a.z, a.w);
+                swiglu_grad_s(a.x, b.x, d.x, s01.x, og.x, ou.x);
+                swiglu_grad_s(a.y, b.y, d.y, s01.y, og.y, ou.y);
+                swiglu_grad_s(a.z, b.z, d.z, s23.x, og.z, ou.z);
+                swiglu_grad_s(a.w, b.w, d.w, s23.y, og.w, ou.w);
                 reinterpret_cast<float4 *>(dgr)[c] = og;
                 reinterpret_cast<float4 *>(dur)[c] = ou;
             } else {
