@@ -187,3 +187,51 @@ def test_causal_softmax_with_period(rp, orc, cols, period):
     want = orc.softmax_rows_causal(x.cpu().numpy(), 5, period)
     got = rp.softmax_rows(x, causal_first=5, causal_period=period)
     assert np.array_equal(u32(got.cpu().numpy()), u32(want))
+
+
+def same_bits_or_both_nan(got, want):
+    """Equal bits wherever the oracle's value is not NaN; NaN where it is
+    (NaN payloads are not pinned)."""
+    got, want = np.asarray(got, dtype=np.float32), np.asarray(want, dtype=np.float32)
+    nan = np.isnan(want)
+    return bool(np.array_equal(np.isnan(got), nan) and np.array_equal(u32(got[~nan]), u32(want[~nan])))
+
+
+def special_rows(cols, seed):
+    """Rows of N(0, 3) values with infinities, huge values, NaNs at the start
+    of a 32-value run (a NaN there hides the rest of that run from the max), an
+    all -inf row and a row of one huge value among tiny ones."""
+    g = np.random.default_rng(seed)
+    x = (g.standard_normal((8, cols)) * 3.0).astype(np.float32)
+    x[0, 5] = np.inf
+    x[1, 7] = -np.inf
+    x[2, 32] = np.nan
+    x[2, 33] = 1000.0
+    x[3, :] = -np.inf
+    x[4, 64] = np.nan
+    x[4, 65] = 200.0
+    x[4, 3] = 150.0
+    x[5, 10] = 3.0e38
+    x[5, 11] = -3.0e38
+    x[6, :] = 1e-30
+    x[6, cols - 1] = 90.0
+    x[7, 0] = np.nan
+    return x
+
+
+@pytest.mark.parametrize("cols", [96, 2048, 4096])
+def test_softmax_special_values_match_oracle(rp, orc, cols):
+    x = special_rows(cols, 15000 + cols)
+    xd = torch.from_numpy(x).to(DEV)
+    assert same_bits_or_both_nan(rp.softmax_rows(xd).cpu().numpy(), orc.softmax_rows(x))
+    for first in (0, 40):
+        want = orc.softmax_rows_causal(x, first)
+        assert same_bits_or_both_nan(rp.softmax_rows(xd, causal_first=first).cpu().numpy(), want)
+
+
+def test_gelu_special_values_match_oracle(rp, orc):
+    v = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, 3.0e38, -3.0e38, 1e-45, -1e-45, 10.0, -10.0,
+                  5.9, -5.9, 100.0, -100.0, 1e-20], dtype=np.float32)
+    x = np.concatenate([v, (np.random.default_rng(16000).standard_normal(4093) * 5).astype(np.float32)])
+    got = rp.gelu(torch.from_numpy(x).to(DEV)).cpu().numpy()
+    assert same_bits_or_both_nan(got, orc.gelu(x))
