@@ -305,3 +305,36 @@ def test_gemm_direct_loader_typed_and_batched(rp, orc):
         assert torch.equal(bits(C), want), loader
     with pytest.raises(rp.RepopsError):
         rp.gemm_batched(A.float().unsqueeze(0), B.float().unsqueeze(0), loader=rp.LOADER_DIRECT)
+
+
+def test_gemm_special_values_every_kernel(rp, orc):
+    # infinities, NaN, values whose products or sums overflow, subnormals and
+    # signed zeros, on ragged edges: the same bits as the oracle (NaN where the
+    # oracle has NaN; payloads are not pinned) on every tile configuration,
+    # loader and the small-output kernel
+    M, N, K = 70, 68, 44                 # leading dimensions TMA can describe
+    g = np.random.default_rng(17000)
+    A = (g.standard_normal((M, K)) * 2).astype(np.float32)
+    B = (g.standard_normal((K, N)) * 2).astype(np.float32)
+    A[3, 7] = np.inf
+    A[5, :] = 0.0
+    A[5, 43] = -np.inf
+    B[43, 9] = 0.0                       # -inf * 0 = NaN in column 9 of row 5
+    A[11, 2] = np.nan
+    A[20, 0] = 3.0e38
+    B[0, :] = 3.0e38                     # row 20 overflows to +inf
+    A[30, 1] = -3.0e38
+    B[1, 30] = 3.0e38                    # row 30, column 30: -inf
+    A[40, :] = -0.0
+    A[50, 3] = 1e-40                     # subnormal products
+    B[3, 50] = 1e-3
+    A[69, :] = -1e-45
+    B[:, 67] = 1e-45                     # products round to -0 / +0
+    want = orc.gemm(A, B)
+    nan = np.isnan(want)
+    Ad, Bd = torch.from_numpy(A).to(DEV), torch.from_numpy(B).to(DEV)
+    cases = [(c, l) for c in all_configs(rp) for l in (rp.LOADER_TMA, rp.LOADER_CPASYNC)]
+    for cfg, loader in cases + [(-1, rp.LOADER_DIRECT)]:
+        got = run(rp, Ad, Bd, cfg, loader).cpu().numpy()
+        assert np.array_equal(np.isnan(got), nan), (cfg, loader)
+        assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32)), (cfg, loader)
