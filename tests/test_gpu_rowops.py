@@ -235,3 +235,18 @@ def test_gelu_special_values_match_oracle(rp, orc):
     x = np.concatenate([v, (np.random.default_rng(16000).standard_normal(4093) * 5).astype(np.float32)])
     got = rp.gelu(torch.from_numpy(x).to(DEV)).cpu().numpy()
     assert same_bits_or_both_nan(got, orc.gelu(x))
+
+
+@pytest.mark.parametrize("cols", [96, 2048, 40000])
+def test_norms_special_values_match_oracle(rp, orc, cols):
+    # rows with infinities, NaN, overflowing squares, all-zero and constant rows,
+    # on the staged kernels and (40000 columns) the long-row kernel
+    x = special_rows(cols, 18000 + cols)
+    x[3, :] = 0.0                         # variance 0: 1/sqrt(eps)
+    x[6, :] = 7.0                         # constant row
+    g = np.random.default_rng(18100 + cols).standard_normal(cols).astype(np.float32)
+    b = np.random.default_rng(18200 + cols).standard_normal(cols).astype(np.float32)
+    xd, gd, bd = (torch.from_numpy(a).to(DEV) for a in (x, g, b))
+    assert same_bits_or_both_nan(rp.layernorm_rows(xd, gd, bd, 1e-5).cpu().numpy(),
+                                 orc.layernorm_rows(x, g, b, 1e-5))
+    assert same_bits_or_both_nan(rp.rmsnorm_rows(xd, gd, 1e-6).cpu().numpy(), orc.rmsnorm_rows(x, g, 1e-6))
