@@ -109,3 +109,32 @@ def test_mean_sgd_full_size_sampled(rp, orc):
         want = orc.mean_sgd([gr[s:s + 4096].cpu().numpy() for gr in grads], order, 1e-3, before[s])
         got = theta[s:s + 4096].cpu().numpy()
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), s
+
+
+@pytest.mark.parametrize("nC", [3, 16])
+def test_mean_sgd_special_values(rp, orc, nC):
+    # infinities of both signs (their sum NaN), NaN, sums that overflow, -0 and
+    # subnormal gradients, θ at ±inf and ±0, on a ragged length (vector body and
+    # scalar tail): the same bits as the oracle wherever it is not NaN
+    n = 4099
+    g = np.random.default_rng(19000 + nC)
+    G = (g.standard_normal((nC, n)) * 1e-2).astype(np.float32)
+    th = (g.standard_normal(n) * 0.02).astype(np.float32)
+    G[0, 1] = np.inf
+    G[1, 2] = np.inf
+    G[2, 2] = -np.inf
+    G[1, 3] = np.nan
+    G[:, 4] = 3.0e38
+    G[:, 5] = -0.0
+    th[5] = -0.0
+    G[:, 6] = 1e-45
+    th[7] = np.inf
+    th[8] = -np.inf
+    G[:, 4098] = -3.0e38
+    grads = [torch.from_numpy(G[r].copy()).to(DEV) for r in range(nC)]
+    theta = torch.from_numpy(th.copy()).to(DEV)
+    order = rp.sort_ids(inputs.contributor_ids(nC, 19100 + nC))
+    got, want = run_both(rp, orc, grads, order, 1e-3, theta)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
