@@ -192,3 +192,31 @@ def test_causal_tile_skip_keeps_the_lower_part_exact(rp, orc, config, first):
     P = rp.softmax_rows(S.view(H * T, T), causal_first=first, causal_period=T)
     Ph = orc.softmax_rows_causal(want.reshape(H * T, T), first, T)
     assert np.array_equal(u32(P.cpu().numpy()), u32(Ph))
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_epilogue_special_values(rp, orc, act):
+    # infinities and NaN in the operands, a product that overflows, a bias at
+    # +inf, a residual at -inf: the epilogue (alpha, bias, GeLU, residual) gives
+    # the same bits as the oracle wherever its value is not NaN
+    batch, M, N, K = 2, 37, 40, 24
+    g = np.random.default_rng(20000 + act)
+    A = (g.standard_normal((batch, M, K)) * 2).astype(np.float32)
+    B = (g.standard_normal((batch, K, N)) * 2).astype(np.float32)
+    A[0, 3, 5] = np.inf
+    A[1, 4, :] = 0.0
+    A[1, 4, 2] = np.nan
+    A[0, 9, 0] = 3.0e38
+    B[0, 0, :] = 3.0e38
+    bias = (g.standard_normal(N)).astype(np.float32)
+    bias[7] = np.inf
+    R = (g.standard_normal((batch, M, N))).astype(np.float32)
+    R[1, 30, :] = -np.inf
+    C = np.zeros((batch, M, N), dtype=np.float32)
+    Ad, Bd, bd, Rd = (torch.from_numpy(x.copy()).to(DEV) for x in (A, B, bias, R))
+    got = rp.gemm_batched(Ad, Bd, alpha=0.5, bias=bd, act=act, residual=Rd).cpu().numpy()
+    orc.gemm_batched(0, 0, batch, M, N, K, A.reshape(-1), K, M * K, B.reshape(-1), N, K * N,
+                     C.reshape(-1), N, M * N, 0.5, bias, act, R.reshape(-1), N, M * N)
+    nan = np.isnan(C)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(u32(got[~nan]), u32(C[~nan]))
