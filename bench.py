@@ -622,6 +622,8 @@ def run_sweep(args):
         run_sweep_decoder(dev, s, flush, peak)
     if args.sweep in ("all", "halfstore"):
         run_sweep_halfstore(dev, s, flush, peak, peaks.get("hbm_gbs", 6800.0))
+    if args.sweep in ("all", "halfstore", "rolling"):
+        run_sweep_rolling(dev, s, flush, peaks.get("hbm_gbs", 6800.0))
     if args.sweep in ("all", "train"):
         run_sweep_train(dev, s, flush, peak)
     if args.sweep == "decoder_step":
@@ -930,8 +932,7 @@ def run_sweep_halfstore(dev, s, flush, peak, hbm):
     """Half-precision storage around the binary32 path: the mean + SGD step of
     the hot path (16 contributors x 2^28) with bfloat16 gradients next to
     float32 ones, a float32 -> bfloat16 conversion, the 8192^3 GEMM on
-    bfloat16 operands; and the rolling hash of a 8192 x 4096-word uint32
-    batch, window 32.  L2 flushed before each timed launch."""
+    bfloat16 operands.  L2 flushed before each timed launch."""
     def ev_time(fn, reps=5):
         with torch.cuda.stream(s):
             fn()
@@ -971,13 +972,30 @@ def run_sweep_halfstore(dev, s, flush, peak, hbm):
     print(json.dumps({"sweep": "gemm 8192^3 on bfloat16 operands (widened, binary32 k-chain)", "ms": ms,
                       "tflops": tf, "frac_of_fp32_peak": tf / peak}), flush=True)
     del A, B, C
+
+
+def run_sweep_rolling(dev, s, flush, hbm):
+    """The rolling hash of a 8192 x 4096-word uint32 batch, window 32 (128 MiB
+    read, 256 MiB of hashes written).  L2 flushed before each timed launch;
+    the mean of 10 launches."""
     rows, width, win = 8192, 4096, 32
     g = torch.Generator(device=dev)
     g.manual_seed(540)
     words = torch.randint(-(1 << 31), 1 << 31, (rows, width), generator=g, dtype=torch.int64,
                           device=dev).to(torch.int32)
     out = torch.empty(rows, width - win + 1, dtype=torch.int64, device=dev)
-    ms = ev_time(lambda: rp.rolling_hash(words, win, out=out, stream=s))
+    with torch.cuda.stream(s):
+        rp.rolling_hash(words, win, out=out, stream=s)
+        evs = []
+        for _ in range(10):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            rp.rolling_hash(words, win, out=out, stream=s)
+            e1.record(s)
+            evs.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
     nb = words.numel() * 4 + out.numel() * 8
     print(json.dumps({"sweep": "rolling hash 8192 x 4096 uint32 words, window 32", "ms": ms,
                       "hashes_per_s": out.numel() / ms * 1e3, "gbs": nb / ms / 1e6,
@@ -1048,8 +1066,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
-                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore", "train",
-                             "decoder_step"),
+                    choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore", "rolling",
+                             "train", "decoder_step"),
                     help="time every workload of a part (one JSON line each) instead of the step")
     args = ap.parse_args()
     if args.sweep:

@@ -117,7 +117,8 @@ def test_half_gradient_mean_matches_oracle(rp, orc, t, dt, nC, offset):
     assert np.array_equal(theta.cpu().numpy().view(np.uint32), want.view(np.uint32))
 
 
-@pytest.mark.parametrize("width,window", [(1, 1), (50, 1), (50, 2), (50, 50), (1000, 32), (1000, 7), (4096, 32)])
+@pytest.mark.parametrize("width,window", [(1, 1), (50, 1), (50, 2), (50, 50), (1000, 32), (1000, 7), (4096, 32),
+                                          (2100, 1024), (2100, 1025), (3000, 1500)])
 def test_rolling_hash_matches_oracle(rp, orc, width, window):
     g = torch.Generator(device=DEV)
     g.manual_seed(width + window)
@@ -125,6 +126,18 @@ def test_rolling_hash_matches_oracle(rp, orc, width, window):
     words = w.to(torch.int32)[:, :width]                  # pitch width + 3
     h = rp.rolling_hash(words, window)
     want = orc.rolling_hash(words.cpu().numpy().view(np.uint32), window)
+    assert np.array_equal(h.cpu().numpy().view(np.uint64), want)
+
+
+@pytest.mark.parametrize("width,window", [(1100, 32), (2100, 1025)])
+def test_rolling_hash_extreme_words(rp, orc, width, window):
+    # every word 0xFFFFFFFF gives the largest intermediate sums; runs of zeros
+    # between them give windows whose hash is 0 or a single power of the base
+    w = torch.full((3, width), -1, dtype=torch.int32, device=DEV)
+    w[1, ::3] = 0
+    w[2, width // 2:] = 0
+    h = rp.rolling_hash(w, window)
+    want = orc.rolling_hash(w.cpu().numpy().view(np.uint32), window)
     assert np.array_equal(h.cpu().numpy().view(np.uint64), want)
 
 

@@ -13,8 +13,9 @@
 // committed row of a rectangular uint32 batch.  The page names no hash; the
 // library's is Rabin-Karp modulo the Mersenne prime 2^61 - 1.  Each thread
 // takes 32 consecutive window starts of one row: Horner's rule for the first,
-// then h' = (h - w_out * B^(W-1)) * B + w_in for the rest -- exact modular
-// integers, so the split of a row across threads does not change a bit.
+// then h' = h * B - w_out * B^W + w_in for the rest -- exact modular integers,
+// so the split of a row across threads does not change a bit.  With
+// B = 2^32 + 15 the products by B are 61-bit rotations (roll61.cuh).
 // Windows up to 1024 words stage a warp's words and hashes in shared memory
 // (coalesced global accesses); longer ones read global memory directly.
 #include <algorithm>
@@ -23,6 +24,7 @@
 #include <cuda_fp16.h>
 
 #include "internal.cuh"
+#include "roll61.cuh"
 
 namespace repops {
 namespace {
@@ -146,27 +148,12 @@ bool span_bytes(int64_t rows, int64_t cols, int64_t ld, unsigned sz, uint64_t *o
 
 // ---------------------------------------------------------- rolling hash ----
 
-constexpr uint64_t P61 = (uint64_t(1) << 61) - 1;
 constexpr int ROLL_CHUNK = 32;   // window starts per thread
-
-__device__ __forceinline__ uint64_t mulmod61(uint64_t a, uint64_t b) {
-    // a, b < 2^61: a*b = hi*2^64 + lo, and 2^64 = 8 * 2^61 = 8 (mod P), so
-    // a*b = (lo & P) + (lo >> 61) + 8*hi (mod P); 8*hi < 2^61 leaves the low
-    // three bits free for lo >> 61
-    const uint64_t lo = a * b, hi = __umul64hi(a, b);
-    uint64_t r = (lo & P61) + ((lo >> 61) | (hi << 3));   // < 2^62
-    r = (r & P61) + (r >> 61);                              // <= P + 1
-    return r >= P61 ? r - P61 : r;
-}
-
-__device__ __forceinline__ uint64_t addmod61(uint64_t a, uint64_t b) {   // a, b < P
-    const uint64_t s = a + b;
-    return s >= P61 ? s - P61 : s;
-}
+static_assert(REPOPS_ROLLING_HASH_BASE == roll61::BASE, "roll61 specialises the products by B = 2^32 + 15");
 
 __global__ void __launch_bounds__(256)
 rolling_hash_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ words, int64_t ldw, int64_t W,
-                    uint64_t base, uint64_t base_w1, uint64_t *__restrict__ out, int64_t ldo, int64_t chunks) {
+                    uint64_t base_w, uint64_t *__restrict__ out, int64_t ldo, int64_t chunks) {
     const int64_t n = width - W + 1;
     const int64_t total = rows * chunks;
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -176,12 +163,10 @@ rolling_hash_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ wo
         const uint32_t *w = words + r * ldw;
         uint64_t *o = out + r * ldo;
         uint64_t h = 0;
-        for (int64_t k = 0; k < W; ++k) h = addmod61(mulmod61(h, base), w[i0 + k]);
+        for (int64_t k = 0; k < W; ++k) h = roll61::push(h, w[i0 + k]);
         o[i0] = h;
         for (int64_t i = i0 + 1; i < i1; ++i) {
-            const uint64_t drop = mulmod61(w[i - 1], base_w1);
-            h = h >= drop ? h - drop : h + (P61 - drop);
-            h = addmod61(mulmod61(h, base), w[i + W - 1]);
+            h = roll61::slide(h, w[i - 1], w[i + W - 1], base_w);
             o[i] = h;
         }
     }
@@ -201,7 +186,7 @@ __device__ __forceinline__ int padded(int j) { return j + (j >> 5); }
 
 __global__ void __launch_bounds__(32 * ROLL_WARPS)
 rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ words, int64_t ldw, int W,
-                           uint64_t base, uint64_t base_w1, uint64_t *__restrict__ out, int64_t ldo, int64_t segs) {
+                           uint64_t base_w, uint64_t *__restrict__ out, int64_t ldo, int64_t segs) {
     extern __shared__ uint64_t roll_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wcap = padded(ROLL_SEG + W - 1) + 1;                       // words per warp stage
@@ -219,12 +204,10 @@ rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restri
         const int cnt = int(max(int64_t(0), min(int64_t(ROLL_CHUNK), n - s0 - i0)));
         if (cnt > 0) {
             uint64_t h = 0;
-            for (int k = 0; k < W; ++k) h = addmod61(mulmod61(h, base), wstage[padded(i0 + k)]);
+            for (int k = 0; k < W; ++k) h = roll61::push(h, wstage[padded(i0 + k)]);
             ostage[padded(i0)] = h;
             for (int i = 1; i < cnt; ++i) {
-                const uint64_t drop = mulmod61(wstage[padded(i0 + i - 1)], base_w1);
-                h = h >= drop ? h - drop : h + (P61 - drop);
-                h = addmod61(mulmod61(h, base), wstage[padded(i0 + i + W - 1)]);
+                h = roll61::slide(h, wstage[padded(i0 + i - 1)], wstage[padded(i0 + i + W - 1)], base_w);
                 ostage[padded(i0 + i)] = h;
             }
         }
@@ -239,10 +222,10 @@ rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restri
 constexpr size_t padded_host(int j) { return size_t(j) + size_t(j >> 5); }
 
 uint64_t powmod61_host(uint64_t b, int64_t e) {
-    unsigned __int128 r = 1, x = b % P61;
+    unsigned __int128 r = 1, x = b % roll61::P;
     while (e > 0) {
-        if (e & 1) r = (r * x) % P61;
-        x = (x * x) % P61;
+        if (e & 1) r = (r * x) % roll61::P;
+        x = (x * x) % roll61::P;
         e >>= 1;
     }
     return uint64_t(r);
@@ -332,7 +315,7 @@ extern "C" int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32
     if (ranges_overlap(words, wb, out, ob)) return REPOPS_ERR_ALIAS;
     DeviceInfo di;
     const int sms = current_device_info(&di) == REPOPS_OK ? di.sms : 152;
-    const uint64_t bw1 = powmod61_host(REPOPS_ROLLING_HASH_BASE, window - 1);
+    const uint64_t bw = powmod61_host(REPOPS_ROLLING_HASH_BASE, window);   // B^W mod P
     if (window <= ROLL_MAX_STAGED_WINDOW) {
         const int64_t segs = (n + ROLL_SEG - 1) / ROLL_SEG;
         const int wcap = int(ROLL_SEG + window - 1) + int((ROLL_SEG + window - 1) >> 5) + 1;
@@ -346,12 +329,11 @@ extern "C" int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32
         const int blocks = int(std::min<int64_t>((rows * segs + ROLL_WARPS - 1) / ROLL_WARPS,
                                                  int64_t(std::max(per_sm, 1)) * sms));
         rolling_hash_staged_kernel<<<blocks, 32 * ROLL_WARPS, smem, stream>>>(
-            rows, width, words, ldw, int(window), REPOPS_ROLLING_HASH_BASE, bw1, out, ldo, segs);
+            rows, width, words, ldw, int(window), bw, out, ldo, segs);
         return check_launch();
     }
     const int64_t chunks = (n + ROLL_CHUNK - 1) / ROLL_CHUNK;
     const int blocks = int(std::min<int64_t>((rows * chunks + 255) / 256, int64_t(sms) * 16));
-    rolling_hash_kernel<<<blocks, 256, 0, stream>>>(rows, width, words, ldw, window, REPOPS_ROLLING_HASH_BASE, bw1,
-                                                    out, ldo, chunks);
+    rolling_hash_kernel<<<blocks, 256, 0, stream>>>(rows, width, words, ldw, window, bw, out, ldo, chunks);
     return check_launch();
 }
