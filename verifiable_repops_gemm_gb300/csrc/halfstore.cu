@@ -12,7 +12,7 @@
 // ZKDV page, proof.start(rolling_window=...): rolling hashes within each
 // committed row of a rectangular uint32 batch.  The page names no hash; the
 // library's is Rabin-Karp modulo the Mersenne prime 2^61 - 1.  Each thread
-// takes 32 consecutive window starts of one row: Horner's rule for the first,
+// takes 64 consecutive window starts of one row: Horner's rule for the first,
 // then h' = h * B - w_out * B^W + w_in for the rest -- exact modular integers,
 // so the split of a row across threads does not change a bit.  With
 // B = 2^32 + 15 the products by B are 61-bit rotations (roll61.cuh).
@@ -148,7 +148,7 @@ bool span_bytes(int64_t rows, int64_t cols, int64_t ld, unsigned sz, uint64_t *o
 
 // ---------------------------------------------------------- rolling hash ----
 
-constexpr int ROLL_CHUNK = 32;   // window starts per thread
+constexpr int ROLL_CHUNK = 64;   // window starts per thread
 static_assert(REPOPS_ROLLING_HASH_BASE == roll61::BASE, "roll61 specialises the products by B = 2^32 + 15");
 
 __global__ void __launch_bounds__(256)
@@ -174,15 +174,23 @@ rolling_hash_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ wo
 
 // Shared-memory staging: a warp takes SEG = 32 * ROLL_CHUNK consecutive window
 // starts of one row and copies the SEG + W - 1 words they read with coalesced
-// loads; lane L then rolls over starts 32L .. 32L + 31 reading the stage, and
-// the hashes leave through a second stage with coalesced 8-byte stores.  Both
-// stages put one pad slot after every 32 (index j at j + j/32): lane L's
-// element k sits at 33L + k + k/32, so the 32 lanes hit 32 different banks.
+// loads; lane L then rolls over starts 64L .. 64L + 63 reading the stage.  The
+// word stage puts one pad slot after every 64 (index j at j + j/64): lane L's
+// word k sits at 65L + k + k/64, so the 32 lanes hit 32 different banks.  The
+// hashes leave ROLL_GROUP steps at a time through a small second stage (row L
+// holds lane L's last ROLL_GROUP hashes, rows padded to an odd count of
+// 8-byte slots): each 8-byte store instruction then writes four runs of 64
+// contiguous bytes.  64 starts a lane halve the share of Horner's rule at
+// window 32; blocks of 4 warps then still fit 5 to an SM.
 constexpr int ROLL_SEG = 32 * ROLL_CHUNK;
-constexpr int ROLL_WARPS = 8;
+constexpr int ROLL_WARPS = 4;
+constexpr int ROLL_GROUP = 8;                              // steps per output copy
+constexpr int ROLL_OROW = ROLL_GROUP + 1;                  // 8-byte slots per stage row
+constexpr int ROLL_OSTAGE = 32 * ROLL_OROW;                // 8-byte slots per warp
 constexpr int64_t ROLL_MAX_STAGED_WINDOW = 1024;
+static_assert(ROLL_CHUNK % ROLL_GROUP == 0, "whole groups");
 
-__device__ __forceinline__ int padded(int j) { return j + (j >> 5); }
+__device__ __forceinline__ int padded(int j) { return j + j / ROLL_CHUNK; }
 
 __global__ void __launch_bounds__(32 * ROLL_WARPS)
 rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restrict__ words, int64_t ldw, int W,
@@ -190,8 +198,8 @@ rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restri
     extern __shared__ uint64_t roll_smem[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int wcap = padded(ROLL_SEG + W - 1) + 1;                       // words per warp stage
-    uint64_t *ostage = roll_smem + warp * (padded(ROLL_SEG) + 1);
-    uint32_t *wstage = reinterpret_cast<uint32_t *>(roll_smem + ROLL_WARPS * (padded(ROLL_SEG) + 1)) + warp * wcap;
+    uint64_t *ostage = roll_smem + warp * ROLL_OSTAGE;
+    uint32_t *wstage = reinterpret_cast<uint32_t *>(roll_smem + ROLL_WARPS * ROLL_OSTAGE) + warp * wcap;
     const int64_t n = width - W + 1;
     const int64_t total = rows * segs;
     for (int64_t t = int64_t(blockIdx.x) * ROLL_WARPS + warp; t < total; t += int64_t(gridDim.x) * ROLL_WARPS) {
@@ -202,24 +210,31 @@ rolling_hash_staged_kernel(int64_t rows, int64_t width, const uint32_t *__restri
         __syncwarp();
         const int i0 = lane * ROLL_CHUNK;                                // local start of this lane
         const int cnt = int(max(int64_t(0), min(int64_t(ROLL_CHUNK), n - s0 - i0)));
-        if (cnt > 0) {
-            uint64_t h = 0;
-            for (int k = 0; k < W; ++k) h = roll61::push(h, wstage[padded(i0 + k)]);
-            ostage[padded(i0)] = h;
-            for (int i = 1; i < cnt; ++i) {
-                h = roll61::slide(h, wstage[padded(i0 + i - 1)], wstage[padded(i0 + i + W - 1)], base_w);
-                ostage[padded(i0 + i)] = h;
-            }
-        }
-        __syncwarp();
-        const int nout = int(min(int64_t(ROLL_SEG), n - s0));
+        const int nout = int(min(int64_t(ROLL_SEG), n - s0));            // hashes of this segment
         uint64_t *o = out + r * ldo + s0;
-        for (int j = lane; j < nout; j += 32) __stcs(o + j, ostage[padded(j)]);
-        __syncwarp();                                                     // stages free for the next segment
+        uint64_t h = 0;
+        if (cnt > 0)
+            for (int k = 0; k < W; ++k) h = roll61::push(h, wstage[padded(i0 + k)]);
+        for (int g = 0; g < ROLL_CHUNK && g < nout; g += ROLL_GROUP) {   // lane 0 holds start g
+#pragma unroll
+            for (int k = 0; k < ROLL_GROUP; ++k) {
+                const int i = g + k;
+                if (i > 0 && i < cnt)
+                    h = roll61::slide(h, wstage[padded(i0 + i - 1)], wstage[padded(i0 + i + W - 1)], base_w);
+                ostage[lane * ROLL_OROW + k] = h;                        // slots past cnt are never copied
+            }
+            __syncwarp();
+            // slot q*32 + lane: row (lane L' = its 8-slot run) and step within the group
+#pragma unroll
+            for (int q = 0; q < ROLL_GROUP; ++q) {
+                const int idx = q * 32 + lane, row = idx / ROLL_GROUP, k = idx % ROLL_GROUP;
+                const int j = row * ROLL_CHUNK + g + k;                  // local window start
+                if (j < nout) __stcs(o + j, ostage[row * ROLL_OROW + k]);
+            }
+            __syncwarp();                                                 // stage free for the next group
+        }
     }
 }
-
-constexpr size_t padded_host(int j) { return size_t(j) + size_t(j >> 5); }
 
 uint64_t powmod61_host(uint64_t b, int64_t e) {
     unsigned __int128 r = 1, x = b % roll61::P;
@@ -318,8 +333,8 @@ extern "C" int repops_rolling_hash_u32(int64_t rows, int64_t width, const uint32
     const uint64_t bw = powmod61_host(REPOPS_ROLLING_HASH_BASE, window);   // B^W mod P
     if (window <= ROLL_MAX_STAGED_WINDOW) {
         const int64_t segs = (n + ROLL_SEG - 1) / ROLL_SEG;
-        const int wcap = int(ROLL_SEG + window - 1) + int((ROLL_SEG + window - 1) >> 5) + 1;
-        const size_t smem = size_t(ROLL_WARPS) * ((padded_host(ROLL_SEG) + 1) * 8u + size_t(wcap) * 4u);
+        const int wcap = int(ROLL_SEG + window - 1) + int((ROLL_SEG + window - 1) / ROLL_CHUNK) + 1;
+        const size_t smem = size_t(ROLL_WARPS) * (size_t(ROLL_OSTAGE) * 8u + size_t(wcap) * 4u);
         cudaError_t e = cudaFuncSetAttribute(rolling_hash_staged_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
         if (e != cudaSuccess) return set_cuda_error(e);
