@@ -54,8 +54,8 @@ SHA_OPS_PER_COMPRESSION = 64 * 14 + 48 * 10 + 24
 L2_BYTES = 129 * 10 ** 6
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
-# launch at 8192^3 from one ncu capture (profiles/gemm_8192_tma_ws_kernel.md),
-# valid only for the kernel source it was taken on (sha256 of gemm_kernels.cuh).
+# launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
+# the kernel source it was taken on (sha256 of gemm_kernels.cuh).
 GEMM_TRAFFIC = {"src_sha256": "6b9cc139ef0c83c832e861e28b5591bb26e83c2eff18074c611a650c2f157963",
                 "bytes_per_launch": 3820000000 + 266220000}
 
@@ -665,11 +665,19 @@ def run_sweep_gemm(dev, s, flush, peak):
             lib_ms = timed(lambda: torch.mm(A, B, out=C), flops)
         finally:
             torch.backends.cuda.matmul.allow_tf32 = tf32
-        kernel = "small-output" if rp.gemm_small_output(M, N, K) else "tiled config %d" % rp.gemm_auto_config(M, N, K)
+        cfg = rp.gemm_auto_config(M, N, K)
+        chained = rp.gemm_auto_chained(M, N, K)
+        kernel = ("small-output" if rp.gemm_small_output(M, N, K) else
+                  "tiled config %d%s" % (cfg, ", chained k-split" if chained else ""))
         tf = flops / ms / 1e9
         rec = {"sweep": name, "M": M, "N": N, "K": K, "ms": ms,
                "tflops": tf, "frac_of_fp32_peak": tf / peak, "kernel": kernel,
                "library_fp32_gemm_ms": lib_ms, "overhead_vs_library": ms / lib_ms - 1.0}
+        if chained:
+            # the same configuration with one CTA per tile (no split)
+            one_ms = timed(lambda: rp.gemm(A, B, out=C, config=cfg, stream=s), flops)
+            rec["one_cta_per_tile_ms"] = one_ms
+            rec["one_cta_per_tile_tflops"] = flops / one_ms / 1e9
         rec.update(extra or {})
         print(json.dumps(rec), flush=True)
         return flops, ms

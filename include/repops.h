@@ -28,8 +28,10 @@
  *     call says otherwise.  Argument checks run on the host before any launch;
  *     a call that returns an error launched nothing.
  *   - The library never takes ownership of a buffer.  It keeps no per-call
- *     state between calls, except the sticky device status word read by
- *     repops_device_status().
+ *     state between calls, except the sticky device status word of the
+ *     bounded waits: by default one word per device shared by every caller,
+ *     or a word the caller owns, bound per host thread with
+ *     repops_set_thread_status_word().
  *   - Floating point is IEEE-754 binary32, round-to-nearest-even, subnormals
  *     kept (no flush-to-zero), no fused multiply-add, no tensor cores.
  *   - NaN results compare equal as a class (payload bits are not pinned);
@@ -76,12 +78,26 @@ const char *repops_status_string(int status);
  * thread (0 if none). */
 int repops_last_cuda_error(void);
 
-/* Synchronises `stream`, then reads and clears the library's sticky device
- * status word.  *status_out = REPOPS_OK, or REPOPS_ERR_TIMEOUT if a kernel's
- * bounded wait on its own asynchronous copies gave up since the last read (the
- * output of that kernel is then undefined).  Returns REPOPS_OK or
+/* Synchronises `stream`, then reads and clears the sticky device status word
+ * of this host thread's launches: the word bound with
+ * repops_set_thread_status_word(), else the library's shared word of the
+ * current device.  *status_out = REPOPS_OK, or REPOPS_ERR_TIMEOUT if a
+ * kernel's bounded wait on its own asynchronous copies gave up since the last
+ * read (the output of that kernel is then undefined).  Returns REPOPS_OK or
  * REPOPS_ERR_CUDA / REPOPS_ERR_INVALID_ARG (null status_out). */
 int repops_device_status(cudaStream_t stream, int *status_out);
+
+/* Scopes failure reports to the caller.  From this call on, every kernel that
+ * this host thread launches through the library ORs its failure bits (bit 0:
+ * a bounded wait gave up) into `word` -- 4 bytes of device memory of the
+ * device the kernels run on, 4-byte aligned, owned, zeroed and read by the
+ * caller -- instead of the device's shared word; repops_device_status() on
+ * this thread then reads and clears `word`.  So a timeout on one caller's
+ * stream is neither reported to nor cleared by another caller that has bound
+ * its own word.  NULL goes back to the shared word.  The binding belongs to
+ * the host thread only (thread-local) and is not read by the device until a
+ * launch.  INVALID_ARG for a pointer that is not 4-byte aligned. */
+int repops_set_thread_status_word(unsigned *word);
 
 /* Failure-detection self-test: launches one kernel on `stream` whose thread
  * waits on an mbarrier phase that nothing completes, with a limit of limit_ns
@@ -181,6 +197,33 @@ int repops_gemm_f32_config(int config, int loader, int transA, int transB,
                            float *C, int64_t ldc,
                            cudaStream_t stream);
 
+/* As repops_gemm_f32_config with the TMA loader and the chained k-split
+ * schedule, which repops_gemm_f32 takes by itself where its model finds it
+ * faster (tile counts that leave the last wave of CTAs partly empty).
+ * `workers` persistent CTAs (1 .. min(tiles, resident CTAs of the
+ * configuration on the device), 0 = that maximum) run whole tiles one per
+ * worker per wave, then split the k-slices of the remaining tiles (more than
+ * `workers`, fewer than twice as many) equally in tile order, so that a tile
+ * may be computed by two consecutive workers.  Such a tile's k-chains are
+ * continued, never reordered or combined: the first worker runs slices 0 .. h-1
+ * of every element's chain from +0 and stores the running binary32 sums
+ * exactly as they stand; the second loads them and runs slices h .. end.  Every
+ * element therefore gets the same operations in the same order as in
+ * repops_gemm_f32 -- the same bits for every worker count (a split-K that adds
+ * separately computed partial sums would not be).  ("Verde与RepOps" §3.2: the
+ * order-critical dimension stays serial; only who computes which part of a
+ * chain changes.)  Scratch (about workers x 32 KB) is taken with
+ * cudaMallocAsync on `stream`; the kernel is launched cooperatively and every
+ * wait between workers is bounded (status word).  UNSUPPORTED when the
+ * operands do not meet the TMA rule, `workers` is too large, or the scratch is
+ * refused; INVALID_ARG for workers < 0; other errors as repops_gemm_f32. */
+int repops_gemm_f32_chained(int config, int workers, int transA, int transB,
+                            int64_t M, int64_t N, int64_t K,
+                            const float *A, int64_t lda,
+                            const float *B, int64_t ldb,
+                            float *C, int64_t ldc,
+                            cudaStream_t stream);
+
 /* Number of GEMM tile configurations compiled into the library. */
 int repops_gemm_config_count(void);
 
@@ -198,6 +241,14 @@ int repops_gemm_config_occupancy(int config);
  * current device (-1 when M or N is 0).  The tiled configuration; see
  * repops_gemm_small_output for when the small-output kernel runs instead. */
 int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K);
+
+/* 1 when repops_gemm_f32 (automatic configuration and loader) runs an M x N x K
+ * problem whose operands the TMA loader can read on the chained k-split
+ * schedule of repops_gemm_f32_chained (its model finds the last wave of
+ * one-tile CTAs too empty), 0 when it runs one CTA per tile.  The same holds
+ * for a single (batch 1) product of repops_gemm_f32_batched without a causal
+ * skip or k band.  Host-only; the bits are the same either way. */
+int repops_gemm_auto_chained(int64_t M, int64_t N, int64_t K);
 
 /* 1 when repops_gemm_f32 (automatic configuration and loader) runs an M x N x K
  * problem on the small-output kernel (REPOPS_LOADER_DIRECT): M, N, K > 0 and
@@ -492,7 +543,12 @@ int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len,
                                   const float *etas, float *theta, uint32_t leaf,
                                   uint8_t *roots_out, cudaStream_t stream);
 
-/* Compression-rate probe: the ceiling the Merkle kernels are measured against.
+/* MEASUREMENT AID, not part of the operator surface: nothing in the
+ * library's operators calls it and a user of the operators needs it for
+ * nothing; it is exported so that the benchmark can time the library's own
+ * compression without linking a second binary.
+ *
+ * Compression-rate probe: the ceiling the Merkle kernels are measured against.
  * Launches `threads` threads (a multiple of 128, 128 .. 2^24) on `stream`; thread
  * t computes, with the library's SHA-256 compression and its message held in
  * registers (no memory traffic, no tree), the digest of the message M_t
@@ -525,8 +581,10 @@ int repops_sha256_rate_probe(uint32_t threads, uint32_t iters, uint32_t *digests
  * leaves need no scratch at all.
  *
  * The first call on each device looks up the array's device address (once
- * per device, with that device current) and caches it; make that first call
- * before any stream capture.  All calls share the array and it keeps the last
+ * per device and CUDA context, with that device current) and caches it; make
+ * that first call before any stream capture.  A new context on the device
+ * (after cudaDeviceReset, say) makes the next call look the address up again
+ * -- again before any capture.  All calls share the array and it keeps the last
  * call's contents (nothing in it needs to start at zero).  Calls whose work
  * overlaps on the GPU -- e.g. on two streams with no ordering between them --
  * race on the array: order them on one stream.  Other errors as

@@ -10,6 +10,8 @@ import torch
 
 from verifiable_repops_gemm_gb300 import inputs
 
+import oracle_par
+
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
@@ -158,71 +160,159 @@ def test_gemm_output_guard_band(rp):
 
 def sampled_check(orc, A, B, C, rows, cols):
     """Oracle on the selected rows x cols only (any order over i, j)."""
-    Ar = A[rows].cpu().numpy()
-    Bc = B[:, cols].cpu().numpy()
-    want = orc.gemm(Ar, Bc)
+    rows = [int(r) for r in rows]
+    cols = [int(c) for c in cols]
+    want = oracle_par.gemm(orc, A, B, rows=rows, cols=cols)
     got = C[rows][:, cols].cpu().numpy()
     assert np.array_equal(np_bits(got), np_bits(want))
 
 
+def plant_detectors(A, B, golden, seed):
+    """Plants the hand-derived order and FMA detectors into the logical
+    operands A (M x K) and B (K x N), in place, whatever their storage.
+
+    Each detector gets a row of A of its own (zero apart from the detector's
+    entries) and a column of B of its own (its entries set over the
+    detector's k positions, random elsewhere).  The zero products before and
+    after the detector add ±0 to an accumulator that starts at +0, so the
+    element's value is the detector's hand-derived one.  k positions: the
+    chain's start, a 32-wide k-slice boundary crossed, the chain's end, and a
+    random offset; rows include the last (a ragged tile edge) and columns the
+    last.  Returns [(i, j, expected bits)]."""
+    od, fd = golden["gemm_order_detector"], golden["gemm_fma_detector"]
+    M, K = A.shape
+    N = B.shape[1]
+    dev = A.device
+    g = np.random.default_rng(seed)
+    n_det = 8
+    rows = [M - 1, 0] + [int(x) for x in g.choice(np.arange(1, M - 1), n_det - 2, replace=False)]
+    cols = [N - 1, 0] + [int(x) for x in g.choice(np.arange(1, N - 1), n_det - 2, replace=False)]
+    a_od = torch.tensor(od["a_row"], dtype=torch.float32, device=dev)
+    b_od = torch.tensor(od["b_col"], dtype=torch.float32, device=dev)
+
+    def from_bits(lst):
+        return torch.tensor([int(x, 16) for x in lst], dtype=torch.int64).to(torch.int32).view(torch.float32).to(dev)
+
+    a_fd, b_fd = from_bits(fd["a_row_bits"]), from_bits(fd["b_col_bits"])
+    k_order = [0, 30, K - 4, int(g.integers(0, K - 4))]
+    k_fma = [31, K - 2, 0, int(g.integers(0, K - 2))]
+    planted = []
+    for d in range(n_det):
+        i, j = rows[d], cols[d]
+        A[i].zero_()
+        if d % 2 == 0:
+            k0 = k_order[d // 2]
+            A[i, k0:k0 + 4] = a_od
+            B[k0:k0 + 4, j] = b_od
+            planted.append((i, j, int(od["expected_bits"], 16)))
+        else:
+            k0 = k_fma[d // 2]
+            A[i, k0:k0 + 2] = a_fd
+            B[k0:k0 + 2, j] = b_fd
+            planted.append((i, j, int(fd["expected_bits"], 16)))
+    return planted
+
+
+def check_planted(C, planted, what):
+    Cb = C.view(torch.int32) if isinstance(C, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(C)).view(torch.int32)
+    for i, j, bits_ in planted:
+        assert int(Cb[i, j]) & 0xFFFFFFFF == bits_, (what, i, j)
+
+
+def assert_same_bits(got, want_bits, what):
+    """got: device tensor; want_bits: int32 CPU tensor of the oracle's bytes."""
+    g = got.contiguous().view(torch.int32).cpu()
+    if not torch.equal(g, want_bits):
+        bad = (g != want_bits).nonzero()
+        raise AssertionError("%s: %d elements differ from the oracle, first at %s"
+                             % (what, bad.shape[0], tuple(bad[0].tolist())))
+
+
+def full_parity(rp, orc, A, B, want_bits, configs, what, loaders=None):
+    """Every configuration (and loader) gives the oracle's bytes on the whole
+    output."""
+    for cfg in configs:
+        for loader in (loaders or [rp.LOADER_TMA]):
+            assert_same_bits(run(rp, A, B, cfg, loader), want_bits, (what, cfg, loader))
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("n", inputs.SQUARE_SWEEP)
-def test_gemm_square_sweep_sampled_and_layout_invariant(rp, orc, n):
+def test_gemm_square_sweep_full_output(rp, orc, golden, n):
+    # N(0,1) operands with the order and FMA detectors planted; the whole
+    # output against the oracle for the automatic choice with B row-major and
+    # column-major, A transposed, and every tile configuration with both
+    # loaders (each configuration has its own CTA shape and thread count)
     idx = inputs.SQUARE_SWEEP.index(n)
     A = inputs.normal((n, n), 1.0, 10 + idx, DEV)
     B = inputs.normal((n, n), 1.0, 20 + idx, DEV)
+    planted = plant_detectors(A, B, golden, 900 + idx)
+    want = oracle_par.gemm(orc, A, B)
+    check_planted(want, planted, "oracle")
+    want_bits = np_bits(want)
     C = run(rp, A, B)
-    g = torch.Generator().manual_seed(n)
-    rows = torch.cat([torch.tensor([0, n - 1]), torch.randint(0, n, (6,), generator=g)])
-    cols = torch.cat([torch.tensor([0, n - 1]), torch.randint(0, n, (30,), generator=g)])
-    sampled_check(orc, A, B, C, rows, cols)
-    # B column-major (same logical B, transposed storage): identical bytes
+    assert_same_bits(C, want_bits, "auto")
+    check_planted(C.cpu(), planted, "auto")
     Bcm = B.t().contiguous().t()
-    C2 = run(rp, A, Bcm)
-    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
-    # another tile configuration: identical bytes
-    C3 = run(rp, A, B, config=3 if n <= 2048 else 1)
-    assert torch.equal(C.view(torch.int32), C3.view(torch.int32))
-    # Merkle root of the output matches the oracle's root of the same bytes
+    assert_same_bits(run(rp, A, Bcm), want_bits, "B column-major")
+    Atr = A.t().contiguous().t()
+    assert_same_bits(run(rp, Atr, B), want_bits, "A transposed")
+    del Atr
+    full_parity(rp, orc, A, B, want_bits, all_configs(rp), n)
+    full_parity(rp, orc, A, Bcm, want_bits, all_configs(rp), (n, "B column-major"))
+    for cfg in (0, 2, 3):
+        assert_same_bits(run(rp, A, B, cfg, rp.LOADER_CPASYNC), want_bits, (n, cfg, "cp.async"))
+    # Merkle root of the output equals the oracle's root of the oracle's bytes
     root = rp.merkle_sha256(C).cpu().numpy().tobytes()
-    assert root == orc.merkle_root(C.cpu().numpy(), 4096)
+    assert root == orc.merkle_root(want, 4096)
 
 
 @pytest.mark.slow
-def test_gemm_ragged_4097_1023_3001(rp, orc):
+def test_gemm_ragged_4097_1023_3001_full_output(rp, orc, golden):
     M, N, K = inputs.RAGGED
     A = inputs.normal((M, K), 1.0, 30, DEV)
     B = inputs.normal((K, N), 1.0, 31, DEV)
-    C = run(rp, A, B)
-    rows = torch.tensor([0, 1, 2047, 4095, 4096])
-    cols = torch.tensor(list(range(0, N, 61)) + [N - 2, N - 1])
-    sampled_check(orc, A, B, C, rows, cols)
-    C2 = run(rp, A.t().contiguous().t(), B.t().contiguous().t())
-    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
+    planted = plant_detectors(A, B, golden, 930)
+    want = oracle_par.gemm(orc, A, B)
+    check_planted(want, planted, "oracle")
+    want_bits = np_bits(want)
+    C = run(rp, A, B)                       # operands repacked to 16-byte pitches, TMA
+    assert_same_bits(C, want_bits, "auto")
+    # lda = 3001, ldb = 1023: only the 4-byte loader reads the caller's storage
+    full_parity(rp, orc, A, B, want_bits, all_configs(rp), "ragged", [rp.LOADER_CPASYNC])
+    At, Bt = A.t().contiguous().t(), B.t().contiguous().t()
+    assert_same_bits(run(rp, At, Bt), want_bits, "both transposed")
+    assert_same_bits(run(rp, At, B, 1, rp.LOADER_CPASYNC), want_bits, "A transposed, cp.async")
     root = rp.merkle_sha256(C).cpu().numpy().tobytes()
-    assert root == orc.merkle_root(C.cpu().numpy(), 4096)
+    assert root == orc.merkle_root(want, 4096)
+
+
+def decoder_gemms():
+    return [(li, name, kind) for li, (name, _, _) in enumerate(inputs.DECODER_LAYERS)
+            for kind in ("forward", "dX", "dW")]
 
 
 @pytest.mark.slow
-def test_gemm_decoder_layer_set(rp, orc):
+@pytest.mark.parametrize("li,name,kind", decoder_gemms())
+def test_gemm_decoder_layer_set_full_output(rp, orc, golden, li, name, kind):
+    # the 15 GEMMs of the 1B-class layer set, each on its whole output with
+    # the detectors planted: forward Y = X W, dX = dY W^T (B a transposed
+    # view), dW = X^T dY (A a transposed view)
     T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
-    X = inputs.normal((T, D), 1.0, 100, DEV)
-    g = torch.Generator().manual_seed(7)
-    for li, (name, kin, nout) in enumerate(inputs.DECODER_LAYERS):
-        Xin = X if kin == D else inputs.normal((T, kin), 1.0, 150 + li, DEV)
-        W = inputs.normal((kin, nout), 0.02, 110 + li, DEV)
-        dY = inputs.normal((T, nout), 1e-3, 120 + li, DEV)
-        Y = run(rp, Xin, W)                       # forward
-        dX = run(rp, dY, W.t())                   # dX = dY W^T (B as a transposed view)
-        dW = run(rp, Xin.t(), dY)                 # dW = X^T dY (A as a transposed view)
-        for out, a, b in ((Y, Xin, W), (dX, dY, W.t()), (dW, Xin.t(), dY)):
-            m, n = out.shape
-            rows = torch.cat([torch.tensor([m - 1]), torch.randint(0, m, (3,), generator=g)])
-            cols = torch.cat([torch.tensor([n - 1]), torch.randint(0, n, (16,), generator=g)])
-            sampled_check(orc, a, b, out, rows, cols)
-        # transposed views give the bytes of materialised transposes
-        assert torch.equal(dX.view(torch.int32), run(rp, dY, W.t().contiguous()).view(torch.int32))
-        assert torch.equal(dW.view(torch.int32), run(rp, Xin.t().contiguous(), dY).view(torch.int32))
+    _, kin, nout = inputs.DECODER_LAYERS[li]
+    X = inputs.normal((T, D), 1.0, 100, DEV) if kin == D else inputs.normal((T, kin), 1.0, 150 + li, DEV)
+    W = inputs.normal((kin, nout), 0.02, 110 + li, DEV)
+    dY = inputs.normal((T, nout), 1e-3, 120 + li, DEV)
+    a, b = {"forward": (X, W), "dX": (dY, W.t()), "dW": (X.t(), dY)}[kind]
+    planted = plant_detectors(a, b, golden, 940 + 3 * li + ("forward", "dX", "dW").index(kind))
+    want = oracle_par.gemm(orc, a, b)
+    check_planted(want, planted, "oracle")
+    want_bits = np_bits(want)
+    C = run(rp, a, b)
+    assert_same_bits(C, want_bits, (name, kind))
+    # a materialised copy of a transposed operand gives the same bytes
+    assert_same_bits(run(rp, a.contiguous(), b.contiguous()), want_bits, (name, kind, "row-major copies"))
+    assert_same_bits(run(rp, a, b, 3), want_bits, (name, kind, "64x64 tiles"))
 
 
 def test_gemm_repacked_operands_match_every_loader(rp, orc):
@@ -338,3 +428,84 @@ def test_gemm_special_values_every_kernel(rp, orc):
         got = run(rp, Ad, Bd, cfg, loader).cpu().numpy()
         assert np.array_equal(np.isnan(got), nan), (cfg, loader)
         assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32)), (cfg, loader)
+
+
+# ---------------------------------------------------------------- chained ----
+# The chained k-split schedule: persistent workers, the last tiles' k-slices
+# shared out so that a tile's chain may be begun by one worker and continued
+# by the next.  Every worker count must give the oracle's bytes ("Verde与RepOps"
+# §3.2: only who computes which part of the serial chain changes).
+
+@pytest.mark.parametrize("M,N,K", [(300, 260, 1000), (129, 257, 33), (64, 64, 32), (257, 130, 4099)])
+def test_chained_split_every_worker_count_bit_exact(rp, orc, golden, M, N, K):
+    A = inputs.normal((M, K), 1.0, 60 + M, DEV)
+    B = inputs.normal((K, N), 1.0, 61 + N, DEV)
+    planted = plant_detectors(A, B, golden, 62 + K) if K >= 40 and M >= 8 and N >= 8 else []
+    want = orc.gemm(A.cpu().numpy(), B.cpu().numpy())
+    check_planted(want, planted, "oracle")
+    want_bits = np_bits(want)
+    for cfg in all_configs(rp):
+        info = rp.gemm_config_info(cfg)
+        tiles = -(-M // info["bm"]) * -(-N // info["bn"])
+        slots = rp.gemm_config_occupancy(cfg) * torch.cuda.get_device_properties(0).multi_processor_count
+        counts = sorted({w for w in (1, 2, 3, 5, 7, tiles - 1, tiles, 0) if 0 <= w <= min(tiles, slots)})
+        for w in counts:
+            for ta, tb in LAYOUTS:
+                Aop, Bop = make_operand(A, ta), make_operand(B, tb)
+                lda = Aop.stride(1) if ta else Aop.stride(0)
+                ldb = Bop.stride(1) if tb else Bop.stride(0)
+                if lda % 4 or ldb % 4:
+                    continue
+                C = rp.gemm_chained(Aop, Bop, config=cfg, workers=w)
+                torch.cuda.synchronize()
+                assert rp.device_status() == 0
+                assert_same_bits(C, want_bits, ("chained", cfg, w, ta, tb))
+
+
+def test_chained_split_rejects_what_it_cannot_run(rp):
+    A = inputs.normal((100, 64), 1.0, 1, DEV)
+    B = inputs.normal((64, 96), 1.0, 2, DEV)
+    with pytest.raises(rp.RepopsError):
+        rp.gemm_chained(A, B, config=3, workers=1000)          # more workers than tiles
+    Au = inputs.normal((100 * 65 + 1,), 1.0, 3, DEV)[1:].view(100, 65)[:, :64]
+    with pytest.raises(rp.RepopsError):
+        rp.gemm_chained(Au, B, config=3, workers=2)            # not TMA-readable
+    with pytest.raises(rp.RepopsError):
+        rp.gemm_chained(A, B, config=3, workers=-1)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (4096, 3072, 2048), (4097, 1023, 3001)])
+def test_chained_split_auto_and_worker_counts_same_bytes(rp, orc, M, N, K):
+    # shapes the automatic choice runs on the chained split; every worker count
+    # and the one-tile-per-CTA kernel of every configuration give the same bytes,
+    # and rows spread over the tiles match the oracle
+    A = inputs.normal((M, K), 1.0, 70, DEV)
+    B = inputs.normal((K, N), 1.0, 71, DEV)
+    C = run(rp, A, B)
+    ref = run(rp, A, B, config=1, loader=rp.LOADER_CPASYNC)
+    assert torch.equal(C.view(torch.int32), ref.view(torch.int32))
+    rows = sorted({0, 63, 64, M // 2, M - 1})
+    want = oracle_par.gemm(orc, A, B, rows=rows)
+    assert np.array_equal(C[rows].cpu().numpy().view(np.uint32), want.view(np.uint32))
+    if M % 4 == 0 and N % 4 == 0 and K % 4 == 0:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        for cfg in all_configs(rp):
+            info = rp.gemm_config_info(cfg)
+            tiles = -(-M // info["bm"]) * -(-N // info["bn"])
+            most = min(tiles, rp.gemm_config_occupancy(cfg) * sms)
+            for w in sorted({0, 151, most - 1, most}):
+                Cw = rp.gemm_chained(A, B, config=cfg, workers=w)
+                assert torch.equal(Cw.view(torch.int32), ref.view(torch.int32)), (cfg, w)
+            Cw = rp.gemm_chained(A.t().contiguous().t(), B, config=cfg, workers=0)
+            assert torch.equal(Cw.view(torch.int32), ref.view(torch.int32)), (cfg, "A transposed")
+    torch.cuda.synchronize()
+    assert rp.device_status() == 0
+
+
+def test_chained_split_is_the_automatic_choice_where_waves_are_uneven(rp):
+    # 2048^3 with 64 x 128 tiles is 512 tiles on 304 resident CTAs: the last
+    # wave would be two-thirds empty; 8192^3 (8192 tiles) is not split
+    assert rp.gemm_auto_chained(2048, 2048, 2048)
+    assert not rp.gemm_auto_chained(8192, 8192, 8192)
+    assert not rp.gemm_auto_chained(256, 256, 256)

@@ -9,6 +9,8 @@ import torch
 
 from verifiable_repops_gemm_gb300 import inputs
 
+import oracle_par
+
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
@@ -92,23 +94,26 @@ def test_mean_sgd_rejects_alias_and_order(rp):
 
 
 @pytest.mark.slow
-def test_mean_sgd_full_size_sampled(rp, orc):
-    # 16 contributors x 2^28 fp32, N(0, 1e-2); theta 2^28, N(0, 0.02); eta = 1e-3
+def test_mean_sgd_full_size_every_element(rp, orc):
+    # 16 contributors x 2^28 fp32, N(0, 1e-2); theta 2^28, N(0, 0.02); eta = 1e-3.
+    # Every element of theta after the update against the oracle on the same
+    # buffers, in element ranges of 2^25 (the oracle split across the host cores)
     nC, n = inputs.MEAN_CONTRIBUTORS, inputs.MEAN_LEN
     grads = [inputs.normal((n,), 1e-2, 200 + r, DEV) for r in range(nC)]
     theta = inputs.normal((n,), 0.02, 199, DEV)
     order = rp.sort_ids(inputs.contributor_ids(nC, 200))
-    before = {}
-    g = torch.Generator().manual_seed(1)
-    starts = [0, n - 4096] + [int(x) for x in torch.randint(0, n - 4096, (14,), generator=g)]
-    for s in starts:
-        before[s] = theta[s:s + 4096].cpu().numpy()
+    before = theta.cpu().numpy()
     rp.fixed_order_mean_sgd(grads, order, 1e-3, theta)
     torch.cuda.synchronize()
-    for s in starts:   # elements are independent: the oracle on a slice is exact
-        want = orc.mean_sgd([gr[s:s + 4096].cpu().numpy() for gr in grads], order, 1e-3, before[s])
-        got = theta[s:s + 4096].cpu().numpy()
-        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), s
+    chunk = 1 << 25
+    for lo in range(0, n, chunk):
+        hi = min(n, lo + chunk)
+        gs = [g[lo:hi].cpu().numpy() for g in grads]
+        want = oracle_par.mean_sgd(orc, gs, order, 1e-3, before[lo:hi], 0, hi - lo)
+        got = theta[lo:hi].cpu().numpy()
+        if not np.array_equal(got.view(np.uint32), want.view(np.uint32)):
+            bad = np.nonzero(got.view(np.uint32) != want.view(np.uint32))[0]
+            raise AssertionError("%d elements differ, first at %d" % (bad.size, lo + int(bad[0])))
 
 
 @pytest.mark.parametrize("nC", [3, 16])

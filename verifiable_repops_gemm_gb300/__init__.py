@@ -36,14 +36,14 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "gemm", "gemm_host", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "gemm", "gemm_chained", "gemm_auto_chained", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
            "convert", "gemm_typed", "rolling_hash", "TYPE_F32", "TYPE_F16", "TYPE_BF16",
            "colsum", "gelu_backward", "rmsnorm_backward", "softmax_backward",
            "swiglu", "swiglu_backward", "rope_frequencies", "rope_table", "rope",
-           "device_status", "RepopsError", "ACT_NONE", "ACT_GELU",
+           "device_status", "set_thread_status_word", "RepopsError", "ACT_NONE", "ACT_GELU",
            "LOADER_AUTO", "LOADER_TMA", "LOADER_CPASYNC", "LOADER_DIRECT", "MEAN_MAX_CONTRIBUTORS"]
 
 
@@ -99,6 +99,30 @@ def gemm(A, B, out=None, *, config: int = -1, loader: int = LOADER_AUTO, stream=
     rc = L.repops_gemm_f32_config(config, loader, ta, tb, M, N, K, pa, lda, pb, ldb,
                                   out.data_ptr(), ldc, _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32")
+    return out
+
+
+def gemm_chained(A, B, out=None, *, config: int = -1, workers: int = 0, stream=None):
+    """C = A @ B on the chained k-split schedule (repops_gemm_f32_chained):
+    `workers` persistent CTAs, a tile's k-chain possibly continued by the next
+    worker; the same bits as gemm()."""
+    import torch
+    L = load()
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    pa, lda, ta = _operand(A, "A")
+    pb, ldb, tb = _operand(B, "B")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=A.device)
+    if out.dtype != torch.float32 or out.dim() != 2 or tuple(out.shape) != (M, N) or \
+            (N > 0 and out.stride(1) != 1):
+        raise ValueError("out must be a (M, N) float32 tensor with unit column stride")
+    ldc = max(out.stride(0), N, 1)
+    rc = L.repops_gemm_f32_chained(config, workers, ta, tb, M, N, K, pa, lda, pb, ldb,
+                                   out.data_ptr(), ldc, _stream_handle(stream))
+    _capi.check(rc, "repops_gemm_f32_chained")
     return out
 
 
@@ -227,8 +251,20 @@ def gemm_config_info(config: int) -> dict:
     return dict(zip(("bm", "bn", "threads", "tm", "tn"), (x.value for x in v)))
 
 
+def gemm_config_occupancy(config: int) -> int:
+    """Resident CTAs per SM of a configuration's TMA kernel on the current device."""
+    rc = load().repops_gemm_config_occupancy(config)
+    _capi.check(rc if rc < 0 else 0, "repops_gemm_config_occupancy")
+    return rc
+
+
 def gemm_auto_config(M: int, N: int, K: int) -> int:
     return load().repops_gemm_auto_config(M, N, K)
+
+
+def gemm_auto_chained(M: int, N: int, K: int) -> bool:
+    """True when the automatic choice runs M x N x K on the chained k-split."""
+    return bool(load().repops_gemm_auto_chained(M, N, K))
 
 
 def gemm_small_output(M: int, N: int, K: int) -> bool:
@@ -348,6 +384,18 @@ def device_status(stream=None) -> int:
     rc = load().repops_device_status(_stream_handle(stream), ctypes.byref(v))
     _capi.check(rc, "repops_device_status")
     return v.value
+
+
+def set_thread_status_word(word=None) -> None:
+    """Binds a caller-owned device status word (a 1-element int32/uint32 CUDA
+    tensor, or None for the library's shared word) to this host thread's
+    launches (see repops_set_thread_status_word)."""
+    ptr = None
+    if word is not None:
+        if not word.is_cuda or word.element_size() != 4 or word.numel() < 1:
+            raise ValueError("word must be a CUDA tensor of 4-byte elements")
+        ptr = word.data_ptr()
+    _capi.check(load().repops_set_thread_status_word(ptr), "repops_set_thread_status_word")
 
 
 def merkle_tree(t, leaf: int = 4096, *, nbytes: int = None, tree=None, root=None, stream=None):

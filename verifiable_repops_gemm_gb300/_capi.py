@@ -34,14 +34,18 @@ SIGNATURES = {
     "repops_status_string": (_cs, [_i32]),
     "repops_last_cuda_error": (_i32, []),
     "repops_device_status": (_i32, [_vp, _vp]),
+    "repops_set_thread_status_word": (_i32, [_vp]),
     "repops_gemm_f32": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "repops_gemm_f32_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "repops_gemm_f32_config": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                       _vp, _i64, _vp]),
+    "repops_gemm_f32_chained": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
+                                       _vp, _i64, _vp]),
     "repops_gemm_config_count": (_i32, []),
     "repops_gemm_config_info": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp]),
     "repops_gemm_auto_config": (_i32, [_i64, _i64, _i64]),
     "repops_gemm_small_output": (_i32, [_i64, _i64, _i64]),
+    "repops_gemm_auto_chained": (_i32, [_i64, _i64, _i64]),
     "repops_sort_ids": (_i32, [_i32, _vp, _vp, _vp, _vp]),
     "repops_fixed_order_mean_sgd": (_i32, [_i32, _i64, _vp, _vp, _f32, _vp, _vp]),
     "repops_merkle_sha256": (_i32, [_vp, _u64, _u32, _vp, _vp]),

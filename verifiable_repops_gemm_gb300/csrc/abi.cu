@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "internal.cuh"
@@ -49,6 +50,45 @@ int current_device_info(DeviceInfo *out) {
         c.ready.store(1, std::memory_order_release);
     }
     *out = c.info;
+    return REPOPS_OK;
+}
+
+namespace {
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+std::once_flag g_ctx_once;
+
+template <class Fn>
+Fn driver_entry(const char *name) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<Fn>(p);
+    return nullptr;
+}
+}  // namespace
+
+int current_context_key(uint64_t *key) {
+    std::call_once(g_ctx_once, [] {
+        g_ctx_get_current = driver_entry<CtxGetCurrentFn>("cuCtxGetCurrent");
+        g_ctx_get_id = driver_entry<CtxGetIdFn>("cuCtxGetId");
+    });
+    if (!g_ctx_get_current || !g_ctx_get_id) return REPOPS_ERR_UNSUPPORTED;
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return REPOPS_ERR_UNSUPPORTED;
+    if (!ctx) {
+        // a host thread whose first runtime call this is: the runtime makes
+        // the current device's primary context current
+        cudaError_t e = cudaFree(nullptr);
+        if (e != cudaSuccess) return set_cuda_error(e);
+        if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || !ctx) return REPOPS_ERR_UNSUPPORTED;
+    }
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return REPOPS_ERR_UNSUPPORTED;
+    *key = uint64_t(id) + 1u;   // never 0
     return REPOPS_OK;
 }
 

@@ -18,25 +18,54 @@ namespace repops {
 namespace {
 
 // Sticky status word: bit 0 = a TMA wait gave up.  One per device (a
-// __device__ variable exists once per device that loads the library).
+// __device__ variable exists once per device that loads the library), shared
+// by every caller that has not bound a word of its own.
 __device__ unsigned g_gemm_status;
 
-constexpr int kMaxDevices = 64;
-std::atomic<unsigned *> g_status_addr[kMaxDevices];
+// The caller's own status word for this host thread's launches
+// (repops_set_thread_status_word), or null for the shared one.
+thread_local unsigned *t_status_word = nullptr;
 
-int status_address(unsigned **out) {
+constexpr int kMaxDevices = 64;
+
+// The shared word's device address, looked up once per device and context: a
+// symbol's address is only valid in the context it was looked up in, so a new
+// context (after cudaDeviceReset, say) looks it up again.
+struct StatusAddr {
+    std::mutex mu;
+    uint64_t ctx_key = 0;
+    unsigned *addr = nullptr;
+};
+StatusAddr g_status_addr[kMaxDevices];
+
+int shared_status_address(unsigned **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 0 || dev >= kMaxDevices) return REPOPS_ERR_UNSUPPORTED;
-    unsigned *p = g_status_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
+    uint64_t key = 0;
+    int rc = current_context_key(&key);
+    if (rc != REPOPS_OK) return rc;
+    StatusAddr &s = g_status_addr[dev];
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (s.ctx_key != key || !s.addr) {
+        unsigned *p = nullptr;
         e = cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_gemm_status);
         if (e != cudaSuccess) return set_cuda_error(e);
-        g_status_addr[dev].store(p, std::memory_order_release);
+        s.addr = p;
+        s.ctx_key = key;
     }
-    *out = p;
+    *out = s.addr;
     return REPOPS_OK;
+}
+
+// The word the kernels this thread launches report into.
+int status_address(unsigned **out) {
+    if (t_status_word) {
+        *out = t_status_word;
+        return REPOPS_OK;
+    }
+    return shared_status_address(out);
 }
 
 // Failure-detection self-test: thread 0 waits on a phase of an mbarrier that
@@ -55,6 +84,10 @@ const GemmLauncher kLaunch[kGemmConfigCount] = {gemm_launch_cfg0, gemm_launch_cf
 const GemmOccupancy kOccupancy[kGemmConfigCount] = {gemm_occupancy_cfg0, gemm_occupancy_cfg1,
                                                     gemm_occupancy_cfg2, gemm_occupancy_cfg3,
                                                     gemm_occupancy_cfg4};
+using GemmSkScratch = size_t (*)(int);
+const GemmSkScratch kSkScratch[kGemmConfigCount] = {gemm_sk_scratch_cfg0, gemm_sk_scratch_cfg1,
+                                                    gemm_sk_scratch_cfg2, gemm_sk_scratch_cfg3,
+                                                    gemm_sk_scratch_cfg4};
 GemmConfigInfo config_info(int c) {
     switch (c) {
         case 0: return gemm_info_cfg0();
@@ -98,11 +131,22 @@ double relative_efficiency(const GemmConfigInfo &ci) {
 // warps for long k-chains, more as K shrinks below 256.  Fitted to the same
 // measurements: its choice is within 2% of the fastest configuration on all
 // 20 shapes and within 1% on 19 (the previous round-based model lost up to 9%).
-int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) {
+//
+// With `allow_sk`, each configuration whose tiles outnumber its resident CTAs
+// is also costed with the chained k-split (every SM gets tiles / SMs tiles'
+// worth of k-slices, plus 2% for the heads' stores and loads), and *sk tells
+// whether that schedule won.  Persistent CTAs run as fast as one-tile CTAs
+// when one fills an SM (128 x 128, 8 consumer warps: 34.9 against 35.1
+// TFLOP/s at 8192^3, where nothing is left to balance), but two persistent
+// CTAs sharing an SM measured 7% slower than two one-tile CTAs (32.8 against
+// 35.2 for 64 x 128), so those are charged 1/0.93.
+int choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, bool allow_sk, bool *sk) {
+    if (sk) *sk = false;
     DeviceInfo di;
     if (current_device_info(&di) != REPOPS_OK || di.device < 0 || di.device >= kMaxDevices) return 0;
     double best_t = 0;
     int best = 0;
+    bool best_sk = false;
     for (int c = 0; c < kGemmConfigCount; ++c) {
         const GemmConfigInfo ci = config_info(c);
         const double tiles =
@@ -114,9 +158,20 @@ int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) 
         const double need = std::min(32.0, 8.0 * std::max(1.0, 256.0 / double(std::max<int64_t>(K, 1))));
         const double eff = relative_efficiency(ci) * std::min(1.0, warps / need);
         const double t = (full * conc + (rem > 0 ? 0.7 * conc : 0.0)) * double(ci.bm) * double(ci.bn) / eff;
-        if (c == 0 || t < best_t * 0.999) { best_t = t; best = c; }
+        if (c == 0 || t < best_t * 0.999) { best_t = t; best = c; best_sk = false; }
+        if (allow_sk && tiles >= conc * di.sms) {
+            const double eff_sk = relative_efficiency(ci) * std::min(1.0, conc * ci.threads / 32.0 / need);
+            const double shared_sm = conc > 1 ? 1.0 / 0.93 : 1.0;
+            const double t_sk = 1.02 * shared_sm * tiles / di.sms * double(ci.bm) * double(ci.bn) / eff_sk;
+            if (t_sk < best_t * 0.999) { best_t = t_sk; best = c; best_sk = true; }
+        }
     }
+    if (sk) *sk = best_sk;
     return best;
+}
+
+int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) {
+    return choose_plan(M, N, K, batch, false, nullptr);
 }
 
 // Tile choice for a banded product (k_lo / k_hi set): the tiles' k-ranges
@@ -270,9 +325,50 @@ bool small_output(int64_t M, int64_t N, int64_t K) {
     return M > 0 && N > 0 && K > 0 && M * N <= kSmallMaxOutputs && N <= 65535LL * 32;
 }
 
+// Chained k-split request of a call: kSkAuto lets the automatic choice decide
+// (config -1 and the automatic loader only), kSkOff never splits, and a value
+// >= 0 asks for it with that many workers (0 = every resident CTA slot).
+constexpr int kSkAuto = -1, kSkOff = -2;
+
+// Runs p with the chained k-split on `workers` persistent CTAs of configuration
+// cfg (0 = every resident slot, at most one per tile): stream-ordered scratch
+// for the heads' accumulators and flags, the flags zeroed, the launch, the
+// scratch released.  REPOPS_ERR_UNSUPPORTED when the split cannot run (the
+// caller then runs the one-tile-per-CTA kernel): no TMA, too many workers, or
+// a refused allocation.
+int launch_chained_split(GemmProblem p, int cfg, int workers) {
+    DeviceInfo di;
+    int rc = current_device_info(&di);
+    if (rc != REPOPS_OK) return rc;
+    const GemmConfigInfo ci = config_info(cfg);
+    const int64_t tiles = ((p.M + ci.bm - 1) / ci.bm) * ((p.N + ci.bn - 1) / ci.bn);
+    const int64_t slots = int64_t(occupancy_of(di.device, cfg)) * di.sms;
+    if (workers == 0) workers = int(std::min<int64_t>(slots, tiles));
+    if (workers < 1 || workers > slots || workers > tiles) return REPOPS_ERR_UNSUPPORTED;
+    const size_t bytes = kSkScratch[cfg](workers);
+    const size_t flag_bytes = size_t(workers) * size_t(ci.threads) * 4u;
+    void *scratch = nullptr;
+    if (cudaMallocAsync(&scratch, bytes, p.stream) != cudaSuccess) {
+        cudaGetLastError();
+        return REPOPS_ERR_UNSUPPORTED;
+    }
+    cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(scratch) + (bytes - flag_bytes), 0, flag_bytes,
+                                    p.stream);
+    if (e != cudaSuccess) {
+        cudaFreeAsync(scratch, p.stream);
+        return set_cuda_error(e);
+    }
+    p.sk_workers = workers;
+    p.sk_scratch = scratch;
+    rc = kLaunch[cfg](p, REPOPS_LOADER_TMA);
+    e = cudaFreeAsync(scratch, p.stream);
+    if (rc == REPOPS_OK && e != cudaSuccess) rc = set_cuda_error(e);
+    return rc;
+}
+
 int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, int sk_req = kSkAuto) {
     if (M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
     if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
     if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC &&
@@ -309,12 +405,18 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     p.stream = stream;
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
-    if (loader == REPOPS_LOADER_DIRECT || (loader == REPOPS_LOADER_AUTO && config < 0 && small_output(M, N, K)))
+    const bool sk_explicit = sk_req >= 0;
+    if (!sk_explicit &&
+        (loader == REPOPS_LOADER_DIRECT || (loader == REPOPS_LOADER_AUTO && config < 0 && small_output(M, N, K))))
         return gemm_small_launch(p);
 
-    const int cfg = config >= 0 ? config : choose_config(M, N, K);
+    bool sk_auto = false;
+    const int cfg = config >= 0 ? config
+                                : choose_plan(M, N, K, 1, sk_req == kSkAuto && loader == REPOPS_LOADER_AUTO,
+                                              &sk_auto);
+    const bool want_sk = sk_explicit || sk_auto;
     bool tma_ok = gemm_tma_eligible(p);
-    if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
+    if ((loader == REPOPS_LOADER_TMA || sk_explicit) && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
 
     // Large problems (>= 4 GFLOP, automatic loader) run on stream-ordered
     // scratch copies where that is faster; the kernels then compute the same
@@ -362,7 +464,12 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     }
     tma_ok = gemm_tma_eligible(p);
     const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
-    rc = kLaunch[cfg](p, use);
+    rc = REPOPS_ERR_UNSUPPORTED;
+    if (want_sk && use == REPOPS_LOADER_TMA) {
+        rc = launch_chained_split(p, cfg, sk_explicit ? sk_req : 0);
+        if (rc == REPOPS_ERR_UNSUPPORTED && sk_explicit) return fail(rc);
+    }
+    if (rc == REPOPS_ERR_UNSUPPORTED) rc = kLaunch[cfg](p, use);
     if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO) {
         // the encoder refused a map: run on the caller's operands with the 4-byte loader
         p.A = A; p.lda = lda; p.B = B; p.ldb = ldb;
@@ -459,9 +566,12 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
 
+    const bool sk_allowed = loader == REPOPS_LOADER_AUTO && config < 0 && batch == 1 && p.causal < 0 &&
+                            p.k_lo < 0 && p.k_hi < 0;
+    bool sk_auto = false;
     const int cfg = config >= 0 ? config
                     : (p.k_lo >= 0 || p.k_hi >= 0) ? choose_config_banded(M, N, K, batch, p.k_lo, p.k_hi)
-                                                   : choose_config(M, N, K, batch);
+                                                   : choose_plan(M, N, K, batch, sk_allowed, &sk_auto);
     // K == 0 has no k-slices to copy: the cp.async kernel runs the epilogue on +0
     bool tma_ok = K > 0 && gemm_tma_eligible(p);
     if (loader == REPOPS_LOADER_TMA && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
@@ -482,7 +592,9 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
         }
     }
     const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
-    rc = kLaunch[cfg](p, use);
+    rc = REPOPS_ERR_UNSUPPORTED;
+    if (sk_auto && use == REPOPS_LOADER_TMA) rc = launch_chained_split(p, cfg, 0);
+    if (rc == REPOPS_ERR_UNSUPPORTED) rc = kLaunch[cfg](p, use);
     if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO) {
         p.A = A; p.lda = lda; p.transA = transA ? 1 : 0;
         rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);   // the encoder refused a map
@@ -564,6 +676,14 @@ extern "C" int repops_gemm_f32_config(int config, int loader, int transA, int tr
                                       const float *B, int64_t ldb, float *C, int64_t ldc,
                                       cudaStream_t stream) {
     return gemm_dispatch(config, loader, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+extern "C" int repops_gemm_f32_chained(int config, int workers, int transA, int transB, int64_t M, int64_t N,
+                                       int64_t K, const float *A, int64_t lda, const float *B, int64_t ldb,
+                                       float *C, int64_t ldc, cudaStream_t stream) {
+    if (workers < 0) return REPOPS_ERR_INVALID_ARG;
+    return gemm_dispatch(config, REPOPS_LOADER_TMA, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream,
+                         workers);
 }
 
 extern "C" int repops_gemm_f32_batched(int config, int loader, int transA, int transB, int64_t batch,
@@ -708,7 +828,20 @@ extern "C" int repops_gemm_config_occupancy(int config) {
 
 extern "C" int repops_gemm_auto_config(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0) return -1;
-    return choose_config(M, N, std::max<int64_t>(K, 1));
+    return choose_plan(M, N, std::max<int64_t>(K, 1), 1, true, nullptr);
+}
+
+extern "C" int repops_gemm_auto_chained(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0 || small_output(M, N, K)) return 0;
+    bool sk = false;
+    choose_plan(M, N, K, 1, true, &sk);
+    return sk ? 1 : 0;
+}
+
+extern "C" int repops_set_thread_status_word(unsigned *word) {
+    if (reinterpret_cast<uintptr_t>(word) % 4) return REPOPS_ERR_INVALID_ARG;
+    t_status_word = word;
+    return REPOPS_OK;
 }
 
 extern "C" int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream) {

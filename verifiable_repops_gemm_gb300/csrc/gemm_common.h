@@ -2,6 +2,7 @@
 // configurations compiled into the library.
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -32,6 +33,12 @@ struct GemmProblem {
     int64_t k_lo = -1;     // >= 0: row i's k-chain starts at max(0, i - k_lo)
     int64_t k_hi = -1;     // >= 0: row i's k-chain ends at min(K - 1, i + k_hi)
     int64_t b_group = 1;   // batch b reads B_(b / b_group)
+    // Chained k-split (TMA loader, batch 1, no causal skip or band): a
+    // persistent grid of sk_workers CTAs; sk_scratch holds their heads'
+    // accumulators and flags (gemm_sk_scratch_cfg<N>, flags zeroed).  0 = one
+    // CTA per tile.
+    int sk_workers = 0;
+    void *sk_scratch = nullptr;
 };
 
 struct GemmConfigInfo {
@@ -45,7 +52,8 @@ using GemmOccupancy = int (*)();   // resident CTAs per SM (TMA kernel), current
 #define REPOPS_DECLARE_GEMM_CONFIG(N)          \
     int gemm_launch_cfg##N(const GemmProblem &, int); \
     int gemm_occupancy_cfg##N();               \
-    GemmConfigInfo gemm_info_cfg##N();
+    GemmConfigInfo gemm_info_cfg##N();         \
+    size_t gemm_sk_scratch_cfg##N(int workers);
 
 REPOPS_DECLARE_GEMM_CONFIG(0)
 REPOPS_DECLARE_GEMM_CONFIG(1)

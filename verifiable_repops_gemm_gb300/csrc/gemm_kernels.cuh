@@ -469,6 +469,252 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 }
 
+// ------------------------------------------------------- chained k-split ----
+//
+// The same warp-specialised TMA pipeline run by a persistent grid of `workers`
+// CTAs that together balance the work when the tile count is not a multiple of
+// the resident CTAs.  Whole waves first: worker w runs tiles i*workers + w,
+// exactly as the one-tile-per-CTA kernel's resident CTAs would.  The remaining
+// tiles (more than `workers`, fewer than twice as many) are cut into k-slices,
+// and worker w takes an equal share of those slices in tile order, so a tile
+// may be split between two consecutive workers.  A split tile's k-chains are
+// CONTINUED, never reordered: worker w-1 runs slices [0, h) of the tile from
+// +0 and stores every accumulator as it stands (a binary32 value, stored and
+// loaded exactly); worker w loads them and runs slices [h, KT), so every
+// element still sees k = 0, 1, 2, ... in one serial chain of separately
+// rounded products and sums -- the same operations, the same bits.
+//
+// Worker w runs its share's head (the first part of its last tile) before the
+// tail (the rest of its first tile), so the head worker w-1 stores is ready
+// long before w needs it: w reaches its tail after (share - (KT - h)) >= h
+// slices of its own split work.  Every wait is bounded.  The grid is launched
+// cooperatively (all workers resident), which the waits between workers need.
+struct SkArgs {
+    int64_t dp_tiles;    // tiles run whole, one per worker per wave (waves * workers)
+    int64_t sk_tiles;    // the remaining tiles, split by k-slices
+    int kt;              // k-slices of a whole tile
+    int waves;
+    u64 *partial;        // [workers][pairs per thread][THREADS] accumulator pairs
+    unsigned *flags;     // [workers][THREADS], zero before the launch
+};
+
+// One piece of a worker's schedule.  kind 0: slices [kb, ke) from +0, then
+// store the accumulators for the next worker (a head); 1: a whole tile; 2:
+// load the previous worker's accumulators, slices [kb, ke), store C (a tail).
+struct SkSeg {
+    int64_t tile;
+    int kb, ke, kind;
+};
+
+struct SkPlan {
+    int waves, w;
+    int64_t dp_tiles, workers;
+    int kt;
+    int64_t t_first, t_last;   // split tiles touched (absolute tile indices)
+    int k_first, k_end;        // the share starts at slice k_first of t_first, ends before k_end of t_last
+    int has_head, has_tail;
+    int64_t full_first, nfull;
+    int nseg;
+
+    __device__ __forceinline__ SkPlan(const SkArgs &sk, int w_, int workers_) {
+        waves = sk.waves;
+        w = w_;
+        workers = workers_;
+        dp_tiles = sk.dp_tiles;
+        kt = sk.kt;
+        has_head = has_tail = 0;
+        nfull = 0;
+        full_first = 0;
+        t_first = t_last = 0;
+        k_first = 0;
+        k_end = kt;
+        if (sk.sk_tiles > 0) {
+            const int64_t units = sk.sk_tiles * kt;
+            const int64_t q = units / workers, r = units % workers;
+            const int64_t u0 = q * w + (w < r ? w : r);
+            const int64_t u1 = u0 + q + (w < r ? 1 : 0);
+            t_first = dp_tiles + u0 / kt;
+            k_first = int(u0 % kt);
+            t_last = dp_tiles + (u1 - 1) / kt;
+            k_end = int((u1 - 1) % kt) + 1;
+            has_head = k_end < kt;
+            has_tail = k_first > 0;
+            full_first = t_first + has_tail;
+            nfull = (t_last - has_head) - full_first + 1;
+            if (nfull < 0) nfull = 0;
+        }
+        nseg = waves + has_head + int(nfull) + has_tail;
+    }
+
+    // Segment s in execution order: whole waves, the head, whole split-part
+    // tiles, the tail.
+    __device__ __forceinline__ SkSeg seg(int s) const {
+        SkSeg g;
+        if (s < waves) {
+            g.tile = int64_t(s) * workers + w; g.kb = 0; g.ke = kt; g.kind = 1;
+            return g;
+        }
+        s -= waves;
+        if (has_head) {
+            if (s == 0) { g.tile = t_last; g.kb = 0; g.ke = k_end; g.kind = 0; return g; }
+            --s;
+        }
+        if (s < nfull) {
+            g.tile = full_first + s; g.kb = 0; g.ke = kt; g.kind = 1;
+            return g;
+        }
+        g.tile = t_first; g.kb = k_first; g.ke = kt; g.kind = 2;
+        return g;
+    }
+};
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Waits until *flag is non-zero; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned *flag) {
+    if (ld_acquire_gpu(flag)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i) {
+            __nanosleep(64);
+            if (ld_acquire_gpu(flag)) return true;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+template <class T, bool A_KIN, bool B_KIN, bool EX>
+__global__ void __launch_bounds__(T::THREADS + 32, T::MINB)
+gemm_tma_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   float *__restrict__ C, int64_t M, int64_t N, int64_t K, int64_t ldc,
+                   int tiles_m, int tiles_n, int c_vec, unsigned *status, const ExArgs ep, const SkArgs sk) {
+    constexpr int CONSUMER_WARPS = T::THREADS / 32;
+    constexpr int PAIRS = PackedAcc<T, A_KIN>::R * PackedAcc<T, A_KIN>::C;
+    extern __shared__ unsigned char smem_raw[];
+    float *smem = aligned_smem_base(smem_raw);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + T::STAGES * T::STAGE_FLOATS);
+    uint64_t *empty = full + T::STAGES;
+
+    const int tid = threadIdx.x;
+    const SkPlan plan(sk, int(blockIdx.x), int(gridDim.x));
+
+    if (tid == T::THREADS) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB);
+#pragma unroll 1
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], CONSUMER_WARPS);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (tid >= T::THREADS) {   // producer warp: every slice of every segment, in order
+        if (tid == T::THREADS) {
+            int issued = 0;
+            bool ok = true;
+#pragma unroll 1
+            for (int si = 0; si < plan.nseg && ok; ++si) {
+                const SkSeg g = plan.seg(si);
+                int tm, tn;
+                tile_coords<T::BM>(int(g.tile), tiles_m, tiles_n, tm, tn);
+                const int m0 = tm * T::BM, n0 = tn * T::BN;
+#pragma unroll 1
+                for (int k = g.kb; k < g.ke; ++k) {
+                    const int s = issued % T::STAGES;
+                    if (issued >= T::STAGES &&
+                        !mbar_wait_bounded(&empty[s], uint32_t(issued / T::STAGES - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    float *As = smem + s * T::STAGE_FLOATS;
+                    float *Bs = As + T::A_FLOATS;
+                    mbar_arrive_expect_tx(&full[s], T::STAGE_BYTES);
+                    const int k0 = k * BK;
+                    tma_load_2d(As, &tmA, &full[s], A_KIN ? k0 : m0, A_KIN ? m0 : k0);
+                    tma_load_2d(Bs, &tmB, &full[s], B_KIN ? k0 : n0, B_KIN ? n0 : k0);
+                    ++issued;
+                }
+            }
+            if (!ok) atomicOr(status, 1u);
+#pragma unroll 1
+            for (int it = max(0, issued - T::STAGES); it < issued; ++it)
+                mbar_wait_bounded(&full[it % T::STAGES], uint32_t(it / T::STAGES) & 1u);
+        }
+        return;
+    }
+
+    const int warp = tid >> 5, lane = tid & 31;
+    const int warp_m = warp % T::WARPS_M, warp_n = warp / T::WARPS_M;
+    const int lm = lane >> 3, ln = lane & 7;
+    const int abase = warp_m * T::WM + (A_KIN ? lm : lm * T::TM);
+    const int bbase = warp_n * T::WN + (B_KIN ? ln : ln * 4);
+    const int64_t w = blockIdx.x;
+
+    int consumed = 0;
+#pragma unroll 1
+    for (int si = 0; si < plan.nseg; ++si) {
+        const SkSeg g = plan.seg(si);
+        int tm, tn;
+        tile_coords<T::BM>(int(g.tile), tiles_m, tiles_n, tm, tn);
+        const int64_t m0 = int64_t(tm) * T::BM, n0 = int64_t(tn) * T::BN;
+        PackedAcc<T, A_KIN> acc;
+        if (g.kind == 2) {
+            // continue the chains the previous worker stored (its head of this tile)
+            if (!flag_wait_bounded(sk.flags + (w - 1) * T::THREADS + tid)) {
+                atomicOr(status, 1u);
+                return;
+            }
+            const u64 *src = sk.partial + (w - 1) * int64_t(PAIRS) * T::THREADS + tid;
+#pragma unroll
+            for (int i = 0; i < PackedAcc<T, A_KIN>::R; ++i)
+#pragma unroll
+                for (int j = 0; j < PackedAcc<T, A_KIN>::C; ++j)
+                    acc.v[i][j] = __ldcg(src + (i * PackedAcc<T, A_KIN>::C + j) * T::THREADS);
+        } else {
+            acc.zero();
+        }
+#pragma unroll 1
+        for (int k = g.kb; k < g.ke; ++k) {
+            const int s = consumed % T::STAGES;
+            if (!mbar_wait_bounded(&full[s], uint32_t(consumed / T::STAGES) & 1u)) {
+                atomicOr(status, 1u);
+                return;
+            }
+            const float *As = smem + s * T::STAGE_FLOATS;
+            mma_stage<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, abase, bbase, lm, ln, acc);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+            ++consumed;
+        }
+        if (g.kind == 0) {
+            // the accumulators as they stand, for worker w + 1 (same thread index,
+            // same element mapping); then release them
+            u64 *dst = sk.partial + w * int64_t(PAIRS) * T::THREADS + tid;
+#pragma unroll
+            for (int i = 0; i < PackedAcc<T, A_KIN>::R; ++i)
+#pragma unroll
+                for (int j = 0; j < PackedAcc<T, A_KIN>::C; ++j)
+                    dst[(i * PackedAcc<T, A_KIN>::C + j) * T::THREADS] = acc.v[i][j];
+            st_release_gpu(sk.flags + w * T::THREADS + tid, 1u);
+        } else if constexpr (EX) {
+            store_tile_ex<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep, ep.R);
+        } else {
+            store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+        }
+    }
+}
+
 // ------------------------------------------------------------- cp.async ----
 
 // Fills one ring slot with k-slice [k0, k0 + 32) of both operands, 4 bytes per
@@ -679,6 +925,65 @@ int launch_tma(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     return check_launch();
 }
 
+// Scratch of the chained k-split: accumulator pairs of every worker's head,
+// then one flag per worker thread (zeroed by the caller before each launch).
+template <class T>
+constexpr size_t sk_partial_bytes(int workers) {
+    return size_t(workers) * size_t(T::THREADS) * size_t(T::TM * T::TN) * 4u;
+}
+
+template <class T, bool A_KIN, bool B_KIN, bool EX>
+int launch_tma_sk(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
+    if (p.batch != 1 || (p.ex && (p.causal >= 0 || p.k_lo >= 0 || p.k_hi >= 0))) return REPOPS_ERR_UNSUPPORTED;
+    CUtensorMap ma, mb;
+    const ExArgs ep = ex_args(p);
+    const bool okA = A_KIN ? make_map(&ma, p.A, p.K, p.M, p.lda, BK, T::BM, true)
+                           : make_map(&ma, p.A, p.M, p.K, p.lda, T::BM, BK, false);
+    const bool okB = B_KIN ? make_map(&mb, p.B, p.K, p.N, p.ldb, BK, T::BN, true)
+                           : make_map(&mb, p.B, p.N, p.K, p.ldb, T::BN, BK, false);
+    if (!okA || !okB) return REPOPS_ERR_UNSUPPORTED;
+    auto kern = gemm_tma_sk_kernel<T, A_KIN, B_KIN, EX>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    // every worker must be resident at once (the cooperative launch checks it too)
+    int per_sm = 0, dev = 0, sms = 0;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, T::THREADS + 32, T::SMEM_BYTES)) !=
+            cudaSuccess ||
+        (e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return set_cuda_error(e);
+    const int64_t tiles = int64_t(tiles_m) * tiles_n;
+    const int workers = p.sk_workers;
+    if (workers < 1 || workers > int64_t(per_sm) * sms || workers > tiles) return REPOPS_ERR_UNSUPPORTED;
+    SkArgs sk{};
+    sk.kt = int((p.K + BK - 1) / BK);
+    if (tiles % workers == 0) {
+        sk.waves = int(tiles / workers);
+        sk.sk_tiles = 0;
+    } else {
+        sk.waves = int(tiles / workers) - 1;
+        sk.sk_tiles = tiles - int64_t(sk.waves) * workers;
+    }
+    sk.dp_tiles = int64_t(sk.waves) * workers;
+    sk.partial = static_cast<u64 *>(p.sk_scratch);
+    sk.flags = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(p.sk_scratch) +
+                                            sk_partial_bytes<T>(workers));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(workers), 1u, 1u);
+    cfg.blockDim = dim3(unsigned(T::THREADS + 32), 1u, 1u);
+    cfg.dynamicSmemBytes = T::SMEM_BYTES;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n, c_vec, p.status, ep,
+                           sk);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return check_launch();
+}
+
 template <class T, bool A_KIN, bool B_KIN, bool EX>
 int launch_cpasync(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     auto kern = gemm_cpasync_kernel<T, A_KIN, B_KIN, EX>;
@@ -693,6 +998,12 @@ int launch_cpasync(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
 template <class T, bool EX>
 int launch_layout(const GemmProblem &p, int loader, int tmi, int tni, int c_vec) {
     const bool a_kin = p.transA == 0, b_kin = p.transB != 0;
+    if (loader == REPOPS_LOADER_TMA && p.sk_workers > 0) {
+        if (a_kin && !b_kin) return launch_tma_sk<T, true, false, EX>(p, tmi, tni, c_vec);
+        if (a_kin && b_kin) return launch_tma_sk<T, true, true, EX>(p, tmi, tni, c_vec);
+        if (!a_kin && !b_kin) return launch_tma_sk<T, false, false, EX>(p, tmi, tni, c_vec);
+        return launch_tma_sk<T, false, true, EX>(p, tmi, tni, c_vec);
+    }
     if (loader == REPOPS_LOADER_TMA) {
         if (a_kin && !b_kin) return launch_tma<T, true, false, EX>(p, tmi, tni, c_vec);
         if (a_kin && b_kin) return launch_tma<T, true, true, EX>(p, tmi, tni, c_vec);
@@ -736,6 +1047,14 @@ GemmConfigInfo info() {
     return GemmConfigInfo{T::BM, T::BN, T::THREADS, T::TM, T::TN, T::STAGES};
 }
 
+// Bytes of chained k-split scratch for `workers` workers: their heads'
+// accumulators, then one flag per worker thread (the last workers * THREADS * 4
+// bytes, which the caller zeroes before the launch).
+template <class T>
+size_t sk_scratch_bytes(int workers) {
+    return sk_partial_bytes<T>(workers) + size_t(workers) * size_t(T::THREADS) * 4u;
+}
+
 }  // namespace gemm
 }  // namespace repops
 
@@ -745,4 +1064,5 @@ GemmConfigInfo info() {
     int gemm_launch_cfg##N(const GemmProblem &p, int loader) { return gemm::launch_config<TILE>(p, loader); } \
     int gemm_occupancy_cfg##N() { return gemm::occupancy<TILE>(); }                               \
     GemmConfigInfo gemm_info_cfg##N() { return gemm::info<TILE>(); }                              \
+    size_t gemm_sk_scratch_cfg##N(int workers) { return gemm::sk_scratch_bytes<TILE>(workers); }  \
     }

@@ -40,8 +40,14 @@ inline bool ranges_overlap(const void *a, uint64_t abytes, const void *b, uint64
     return a0 < b0 + bbytes && b0 < a0 + abytes;
 }
 
-// Sticky device status of the GEMM translation unit (bounded waits).
+// Sticky device status of the GEMM translation unit (bounded waits): the
+// word this host thread's launches use (its bound word, else the shared one).
 int gemm_read_and_clear_device_status(cudaStream_t stream, unsigned *value);
+
+// A key of the current CUDA context (the driver's context id): addresses
+// looked up in one context (a __device__ variable's, say) are only valid
+// while the key stays the same.  0 when there is no current context.
+int current_context_key(uint64_t *key);
 
 // Limit for every device-side wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s

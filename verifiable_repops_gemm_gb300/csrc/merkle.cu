@@ -22,6 +22,7 @@
 // message byte), far below HBM bandwidth.
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "internal.cuh"
 
@@ -671,23 +672,37 @@ namespace repops {
 namespace {
 
 constexpr int kNoallocMaxDevices = 64;
-std::atomic<void *> g_noalloc_scratch_addr[kNoallocMaxDevices];
 
-// Device address of the scratch array on the current device.  In host code the
-// array's name only stands in for the symbol, so the address is looked up once
-// per device, with that device current, and cached.
+// Device address of the scratch array, looked up once per device and context
+// with that device current.  In host code the array's name only stands in for
+// the symbol; its device address is valid in the context it was looked up in
+// only, so a new context on the device (after cudaDeviceReset, say) looks it
+// up again instead of reusing a stale address.
+struct NoallocAddr {
+    std::mutex mu;
+    uint64_t ctx_key = 0;
+    void *addr = nullptr;
+};
+NoallocAddr g_noalloc_scratch_addr[kNoallocMaxDevices];
+
 int noalloc_scratch_address(void **out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 0 || dev >= kNoallocMaxDevices) return REPOPS_ERR_UNSUPPORTED;
-    void *p = g_noalloc_scratch_addr[dev].load(std::memory_order_acquire);
-    if (!p) {
+    uint64_t key = 0;
+    int rc = current_context_key(&key);
+    if (rc != REPOPS_OK) return rc;
+    NoallocAddr &a = g_noalloc_scratch_addr[dev];
+    std::lock_guard<std::mutex> lock(a.mu);
+    if (a.ctx_key != key || !a.addr) {
+        void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_merkle_noalloc_scratch);
         if (e != cudaSuccess) return set_cuda_error(e);
-        g_noalloc_scratch_addr[dev].store(p, std::memory_order_release);
+        a.addr = p;
+        a.ctx_key = key;
     }
-    *out = p;
+    *out = a.addr;
     return REPOPS_OK;
 }
 
