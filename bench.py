@@ -52,6 +52,8 @@ SHA_ALU_OPS_PER_COMPRESSION = 64 * 10 + 48 * 6 + 16
 # all (64 ALU + 64 multiply-add lanes): a looser figure, reported beside it
 SHA_OPS_PER_COMPRESSION = 64 * 14 + 48 * 10 + 24
 L2_BYTES = 129 * 10 ** 6
+# GB300 HBM3e bandwidth as specified (nominal, not measured)
+HBM_SPEC_GBS = 7900.0
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
@@ -431,6 +433,7 @@ def run_e2e(w, dev, steps):
     hth = pinned_copy(w.theta)
     hT = pinned_copy(w.T)
     hroot = torch.empty((2, 32), dtype=torch.uint8, pin_memory=True)
+    link = host_link_rate(dev, s)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps + 1)]
     torch.cuda.synchronize(dev)
     for i in range(steps + 1):          # the first pass is an untimed warm-up
@@ -458,13 +461,44 @@ def run_e2e(w, dev, steps):
     tg = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
     tm = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
     tk = sum(e[2].elapsed_time(e[3]) for e in ev) / 1e3
+    step_s = [e[0].elapsed_time(e[3]) / 1e3 for e in ev]
     h2d = 2 * w.A.numel() * 4 + len(w.grads) * w.theta.numel() * 4 + w.theta.numel() * 4 + w.tbytes
     d2h = w.C.numel() * 4 + w.theta.numel() * 4 + 64
     return {"value": w.gemm_flops * steps / tg / 1e12, "unit": "TFLOP/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "parts": {"mean_sgd_gbs": w.mean_bytes * steps / tm / 1e9,
                       "merkle_gbs": (w.tbytes + w.cbytes) * steps / tk / 1e9},
+            "whole_step": {"ms": 1e3 * statistics.mean(step_s), "ms_min": 1e3 * min(step_s),
+                           "ms_max": 1e3 * max(step_s),
+                           "host_bytes_moved_gbs": (h2d + d2h) * steps / sum(step_s) / 1e9,
+                           "basis": "copies in, GEMM 8192^3 through repops_gemm_f32_host, mean + SGD "
+                                    "16 x 2^28, both commitments, results copied out; mean of the steps"},
+            "host_link_gbs": link,
             "steps": steps}
+
+
+def host_link_rate(dev, s, nbytes=1 << 30):
+    """Pinned host <-> device copy rate of 1 GiB, each direction timed alone
+    (CUDA events, best of 3), sampled right before the end-to-end steps: the
+    end-to-end figures are bound by it, and it is shared with other jobs."""
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out = {}
+    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)),
+                     ("d2h", lambda: h.copy_(d, non_blocking=True))):
+        best = None
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(s):
+                a.record(s)
+                fn()
+                b.record(s)
+            b.synchronize()
+            t = a.elapsed_time(b) / 1e3
+            best = t if best is None else min(best, t)
+        out[name] = nbytes / best / 1e9
+    del h, d
+    return out
 
 
 def run_ours(args):
@@ -553,8 +587,11 @@ def run_ours(args):
             "mean_sgd": {"value": mean_gbs, "unit": "GB/s", "ms": statistics.mean(mean_ms),
                          "roofline": {"bound": "hbm", "achieved": mean_gbs / world, "peak": hbm,
                                       "unit": "GB/s", "frac": mean_gbs / world / hbm,
-                                      "basis": "(16 + 2) x 2^28 x 4 B per step; peak = %s hbm_gbs"
-                                               % peaks_kind}},
+                                      "peak_is": "the %s copy bandwidth (hbm_gbs: a STREAM-style copy), "
+                                                 "which a read-mostly stream can slightly exceed" % peaks_kind,
+                                      "spec_hbm_gbs": HBM_SPEC_GBS,
+                                      "frac_of_spec_hbm": mean_gbs / world / HBM_SPEC_GBS,
+                                      "basis": "(16 + 2) x 2^28 x 4 B per step"}},
             "merkle": {"value": merk_gbs, "unit": "GB/s", "ms": statistics.mean(merk_ms),
                        "sha256_compressions_per_step": ncomp,
                        "roofline": {"bound": "alu", "achieved": comp_rate, "peak": comp_peak,
@@ -1065,20 +1102,50 @@ def run_sweep_commitments(dev, s, flush):
                       "ms_per_block": ms, "gbs": per_block / ms / 1e6}), flush=True)
 
 
+def run_gemm_once(spec):
+    """A few launches of one automatic-choice GEMM (M,N,K with N(0,1)
+    operands, A row-major): for profiling one kernel in isolation.  Prints the
+    kernel the automatic choice runs and the event time of the last launch."""
+    M, N, K = (int(x) for x in spec.split(","))
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rp.load()
+    A = inputs.normal((M, K), 1.0, 1, dev)
+    B = inputs.normal((K, N), 1.0, 2, dev)
+    C = torch.empty((M, N), dtype=torch.float32, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for i in range(3):
+            if i == 2:
+                e0.record(s)
+            rp.gemm(A, B, out=C, stream=s)
+        e1.record(s)
+    torch.cuda.synchronize(dev)
+    if rp.device_status(s) != 0:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    print(json.dumps({"gemm": [M, N, K], "config": rp.gemm_auto_config(M, N, K),
+                      "chained": rp.gemm_auto_chained(M, N, K), "ms": e0.elapsed_time(e1)}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--sweep", nargs="?", const="all", default=None,
                     choices=("all", "gemm", "rowops", "commitments", "decoder", "halfstore", "rolling",
                              "train", "decoder_step"),
                     help="time every workload of a part (one JSON line each) instead of the step")
+    ap.add_argument("--gemm-once", metavar="M,N,K", default=None,
+                    help="three launches of one automatic-choice GEMM (for a profiler)")
     args = ap.parse_args()
-    if args.sweep:
+    if args.gemm_once:
+        run_gemm_once(args.gemm_once)
+    elif args.sweep:
         run_sweep(args)
     elif args.impl == "reference":
         run_reference(args)
