@@ -58,8 +58,8 @@ HBM_SPEC_GBS = 7900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
 # the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "6b9cc139ef0c83c832e861e28b5591bb26e83c2eff18074c611a650c2f157963",
-                "bytes_per_launch": 3820000000 + 266220000}
+GEMM_TRAFFIC = {"src_sha256": "e6247199581a86e5d79ee7be7daed103da588360ad93caf68bb53c1f9221c4ed",
+                "bytes_per_launch": 3645192192 + 265768960}
 
 
 def measured_peaks():

@@ -129,6 +129,22 @@ def test_rolling_hash_matches_oracle(rp, orc, width, window):
     assert np.array_equal(h.cpu().numpy().view(np.uint64), want)
 
 
+@pytest.mark.parametrize("width,window", [(5000, 1024), (6000, 700), (4200, 33), (4100, 1000)])
+def test_rolling_hash_several_segments_per_row(rp, orc, width, window):
+    # rows longer than one 2048-start segment with windows up to the staged
+    # kernel's largest (1024 words): non-last segments stage their full
+    # 2048 + W - 1 words, the largest per-warp stage, and more rows than warps
+    # per block put warps of one block on different rows and segments
+    rows = 9
+    g = torch.Generator(device=DEV)
+    g.manual_seed(width * 7 + window)
+    w = torch.randint(-(1 << 31), 1 << 31, (rows, width + 5), generator=g, dtype=torch.int64, device=DEV)
+    words = w.to(torch.int32)[:, :width]                  # pitch width + 5
+    h = rp.rolling_hash(words, window)
+    want = orc.rolling_hash(words.cpu().numpy().view(np.uint32), window)
+    assert np.array_equal(h.cpu().numpy().view(np.uint64), want)
+
+
 @pytest.mark.parametrize("width,window", [(1100, 32), (2100, 1025)])
 def test_rolling_hash_extreme_words(rp, orc, width, window):
     # every word 0xFFFFFFFF gives the largest intermediate sums; runs of zeros
