@@ -870,9 +870,26 @@ def run_sweep_decoder(dev, s, flush, peak):
         if cfg is llama:
             S = cfg.seq_len
             attn_flops = 2 * 2.0 * (T // S) * cfg.heads * (S * (S + 1) / 2) * cfg.d_head
-            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"], streams=ws["streams"]))
-            print(json.dumps({"sweep": "causal grouped-query attention (batched QK^T, softmax, banded PV)",
-                              "tokens": T, "ms": ms, "tflops": attn_flops / ms / 1e9}), flush=True)
+            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"], streams=ws["streams"],
+                                                 fused=False))
+            print(json.dumps({"sweep": "causal grouped-query attention, unfused (batched QK^T, softmax, banded PV)",
+                              "tokens": T, "ms": ms, "tflops": attn_flops / ms / 1e9,
+                              "frac_of_fp32_peak": attn_flops / ms / 1e9 / peak}), flush=True)
+            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"], fused=True))
+            print(json.dumps({"sweep": "causal grouped-query attention, fused kernel (one launch)",
+                              "tokens": T, "ms": ms, "tflops": attn_flops / ms / 1e9,
+                              "frac_of_fp32_peak": attn_flops / ms / 1e9 / peak}), flush=True)
+            probs = torch.empty((T // S) * cfg.heads * S * S, device=dev)
+            ms = timed(lambda: decoder.attention(ws["qkv"], cfg, ws["attn"], ws["scores"], probs=probs,
+                                                 fused=True))
+            print(json.dumps({"sweep": "causal grouped-query attention, fused kernel writing every probability",
+                              "tokens": T, "ms": ms, "tflops": attn_flops / ms / 1e9,
+                              "frac_of_fp32_peak": attn_flops / ms / 1e9 / peak}), flush=True)
+            del probs
+            ms = timed(lambda: decoder.forward(x, w, cfg, work=ws, fused_attention=True))
+            print(json.dumps({"sweep": "%s forward, fused epilogues, fused attention kernel" % label, "tokens": T,
+                              "ms": ms, "tokens_per_s": T / ms * 1e3, "tflops": flops / ms / 1e9,
+                              "frac_of_fp32_peak": flops / ms / 1e9 / peak}), flush=True)
         # the training step: forward keeping its activations, then the backward
         # pass (every weight's gradient and dx): 3x the forward FLOPs
         saved = decoder.activations(cfg, T, dev)

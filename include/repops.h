@@ -650,6 +650,49 @@ int repops_softmax_backward_causal_f32(int64_t rows, int64_t cols, const float *
                                        int64_t first, int64_t period, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Fused causal attention                                                    */
+/* "Verde与RepOps" §3.2 (order-critical reductions keep one fixed order, the */
+/* rest runs in parallel) and §4.3 (the Llama-1B training measurement); the  */
+/* pages fix no attention form: this is the composition of the operators    */
+/* above, fused.                                                             */
+/* ------------------------------------------------------------------------ */
+
+/* Causal grouped-query attention of `seqs` sequences of S tokens, in one
+ * launch.  Row t of sequence b is row b*S + t of every matrix; query head h
+ * uses key/value head g = h / (heads / kv_heads):
+ *   q (device): head h of a row at q + row*ldq + h*dh      (ldq >= heads*dh)
+ *   k, v (device): head g at k + row*ldk + g*dh, v + row*ldv + g*dh
+ *   out (device): head h at out + row*ldo + h*dh            (ldo >= heads*dh)
+ *   probs (device, optional): (seqs*heads) x S x S, P[(b*heads + h)*S + i][j]
+ * For every sequence, head and query row i, with one binary32 rounding per
+ * step and no FMA:
+ *   s_ij = fl(scale * (the k-chain over d = 0 .. dh-1 of q_i[d]*k_j[d] from
+ *          +0)), j <= i  (scale == 1 applies no multiply);
+ *   p_i. = the causal softmax of repops_softmax_rows_causal_f32 over s_i0 ..
+ *          s_ii (32-ary max and sum trees, the library's exp, one correctly
+ *          rounded reciprocal), +0 for j > i;
+ *   out_i[c] = the chain over j = 0 .. i of fl(p_ij * v_j[c]) from +0.
+ * This is exactly, bit for bit, repops_gemm_f32_batched (alpha = scale, tiles
+ * above the diagonal skipped), then repops_softmax_rows_causal_f32 (first 0,
+ * period S), then repops_gemm_f32_batched with the band k_hi = 0, for finite
+ * inputs; terms past a row's prefix are skipped, not multiplied by +0, so
+ * out_i also holds for a V with non-finite rows past i.  With probs, every
+ * row of P is written in full (+0 past the prefix), as the unfused softmax
+ * writes it, for a backward pass.
+ * One CTA computes 16 query rows of one head: the scores and probabilities
+ * stay in shared memory, keys and values stream through it.  Limits: dh = 64,
+ * S <= 2048, q, k, v 16-byte aligned with ldq, ldk, ldv multiples of 4, out
+ * 8-byte aligned with ldo even, probs (if any) 16-byte aligned with S a
+ * multiple of 4; anything else is UNSUPPORTED (run the unfused operators
+ * then).  INVALID_ARG for negative sizes, heads not a multiple of kv_heads,
+ * null pointers or short leading dimensions; ALIAS when out or probs overlap
+ * an input or each other.  seqs, S or heads == 0: nothing to do. */
+int repops_attention_causal_f32(int64_t seqs, int64_t S, int64_t heads, int64_t kv_heads, int64_t dh,
+                                const float *q, int64_t ldq, const float *k, int64_t ldk,
+                                const float *v, int64_t ldv, float scale, float *out, int64_t ldo,
+                                float *probs, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Half-precision storage                                                    */
 /* "Verde与RepOps" §3.3 (IEEE-754 hardware needed; FP16 support limited) and */
 /* §5.3 (lower-precision training as future work).  The pages fix no format  */

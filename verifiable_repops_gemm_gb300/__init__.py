@@ -36,7 +36,7 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "gemm", "gemm_chained", "gemm_auto_chained", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "gemm", "gemm_chained", "gemm_auto_chained", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
@@ -485,6 +485,36 @@ def _row_out(x, out):
         out = torch.empty(x.shape, dtype=torch.float32, device=x.device)
     if tuple(out.shape) != tuple(x.shape):
         raise ValueError("out must have the shape of x")
+    return out
+
+
+def attention_causal(q, k, v, out, *, seq_len: int, heads: int, kv_heads: int, scale: float, probs=None,
+                     stream=None):
+    """Fused causal grouped-query attention (repops_attention_causal_f32).
+
+    q: (T, heads*dh), k and v: (T, kv_heads*dh), out: (T, heads*dh) float32
+    CUDA views with unit column stride (any row pitch); T = sequences *
+    seq_len.  probs: optional (sequences*heads, seq_len, seq_len) contiguous
+    float32 tensor that receives every row of P.  Raises RepopsError
+    (UNSUPPORTED) outside the kernel's limits."""
+    L = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.dim() != 2 or t.dtype.itemsize != 4 or (t.shape[1] > 1 and t.stride(1) != 1):
+            raise ValueError("%s must be a 2-D float32 view with unit column stride" % name)
+    T = q.shape[0]
+    if T % seq_len:
+        raise ValueError("rows are not a whole number of sequences")
+    dh = q.shape[1] // heads
+    pp = None
+    if probs is not None:
+        if not probs.is_contiguous() or probs.numel() != (T // seq_len) * heads * seq_len * seq_len:
+            raise ValueError("probs must be a contiguous (sequences*heads, S, S) tensor")
+        pp = probs.data_ptr()
+    rc = L.repops_attention_causal_f32(T // seq_len, seq_len, heads, kv_heads, dh,
+                                       q.data_ptr(), q.stride(0), k.data_ptr(), k.stride(0),
+                                       v.data_ptr(), v.stride(0), float(scale), out.data_ptr(), out.stride(0),
+                                       pp, _stream_handle(stream))
+    _capi.check(rc, "repops_attention_causal_f32")
     return out
 
 

@@ -160,20 +160,39 @@ def _heads(t, rows, col0, n, dh):
     return t[rows, col0:col0 + n * dh].unflatten(1, (n, dh)).transpose(0, 1)
 
 
-def attention(qkv, cfg: DecoderConfig, out, scores, probs=None, streams=None):
+def attention(qkv, cfg: DecoderConfig, out, scores, probs=None, streams=None, fused: bool = False):
     """Causal grouped-query attention of every sequence into `out` (T x d).
     scores: (sequences * kv_heads, group, S, S) scratch (or (kv_heads, group,
     S, S), shared by the sequences in turn); probs: optional buffer shaped
     like the first that keeps every head's softmax output for the backward
-    pass.  One GEMM call covers every query head of a sequence: a key/value
+    pass.
+
+    fused: one launch of the fused kernel (repops_attention_causal_f32:
+    scores, causal softmax and the banded product per block of 16 query rows in
+    shared memory) where its limits allow; it computes the same bits as the
+    operators below and needs no S x S scratch (`scores` is not touched), but
+    it is slower at decoder sizes, so the unfused operators are the default.
+    Unfused: one GEMM call covers every query head of a sequence: a key/value
     head's K or V is shared by the `group` consecutive query heads of its
-    group.  streams (from `side_streams`): the sequences run concurrently --
-    their outputs are disjoint, so the bits do not change -- and the caller's
-    stream waits for all of them."""
+    group.  streams (from
+    `side_streams`): the sequences run concurrently -- their outputs are
+    disjoint, so the bits do not change -- and the caller's stream waits for
+    all of them."""
     S, dh, kv, H = cfg.seq_len, cfg.d_head, cfg.kv_heads, cfg.heads
     k0, v0 = cfg.d, cfg.d + kv * dh
     scale = 1.0 / float(dh) ** 0.5
     seqs = qkv.shape[0] // S
+    if fused:
+        from . import attention_causal
+        from ._capi import RepopsError, ERR_UNSUPPORTED
+        try:
+            attention_causal(qkv[:, :H * dh], qkv[:, k0:k0 + kv * dh], qkv[:, v0:v0 + kv * dh], out,
+                             seq_len=S, heads=H, kv_heads=kv, scale=scale,
+                             probs=probs.view(seqs * H, S, S) if probs is not None else None)
+            return
+        except RepopsError as e:
+            if e.code != ERR_UNSUPPORTED:
+                raise
     buf = probs if probs is not None else scores
     shared = buf.shape[0] < seqs * kv
     main = torch.cuda.current_stream()
@@ -205,7 +224,7 @@ def attention(qkv, cfg: DecoderConfig, out, scores, probs=None, streams=None):
 
 
 def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue: bool = False,
-            work: dict = None, save: dict = None):
+            work: dict = None, save: dict = None, fused_attention: bool = False):
     """Runs the layer on x (T x d, T a multiple of seq_len) in place and
     returns it.  `work`: reusable buffers from `workspace` (allocated when
     absent).  `save`: a dict (from `activations`) that receives what
@@ -224,7 +243,8 @@ def forward(x, w: dict, cfg: DecoderConfig, *, fused: bool = True, gelu_epilogue
     rmsnorm_rows(x, w["g1"], cfg.eps, out=h)
     gemm(h, w["w_qkv"], out=qkv)
     _rotate(qkv, cfg, ws["rope"], inverse=False)
-    attention(qkv, cfg, attn, ws["scores"], save["probs"] if save is not None else None, ws.get("streams"))
+    attention(qkv, cfg, attn, ws["scores"], save["probs"] if save is not None else None, ws.get("streams"),
+              fused=fused_attention)
     if fused:
         gemm_batched(attn, w["w_o"], out=x, residual=x)
     else:
