@@ -56,7 +56,8 @@ typedef enum {
     REPOPS_ERR_CUDA = -4,         /* a CUDA runtime call failed (see repops_last_cuda_error) */
     REPOPS_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (sticky, see below) */
     REPOPS_ERR_ALLOC = -6,        /* stream-ordered scratch allocation failed */
-    REPOPS_ERR_UNSUPPORTED = -7   /* request outside the documented limits */
+    REPOPS_ERR_UNSUPPORTED = -7,  /* request outside the documented limits */
+    REPOPS_ERR_BOUNDS = -8        /* checked build only: an access outside its buffer was skipped */
 } repops_status;
 
 /* Storage types of tensors whose elements the order-fixed binary32 path reads
@@ -83,7 +84,10 @@ int repops_last_cuda_error(void);
  * repops_set_thread_status_word(), else the library's shared word of the
  * current device.  *status_out = REPOPS_OK, or REPOPS_ERR_TIMEOUT if a
  * kernel's bounded wait on its own asynchronous copies gave up since the last
- * read (the output of that kernel is then undefined).  Returns REPOPS_OK or
+ * read (the output of that kernel is then undefined), or -- in the checked
+ * build librepops_debug.so only, whose hot-path kernels (GEMM, mean + SGD,
+ * Merkle) test every global access against its buffer's span and skip one
+ * outside it -- REPOPS_ERR_BOUNDS if such an access was skipped.  Returns REPOPS_OK or
  * REPOPS_ERR_CUDA / REPOPS_ERR_INVALID_ARG (null status_out). */
 int repops_device_status(cudaStream_t stream, int *status_out);
 

@@ -17,6 +17,11 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librepops.so")
+# The checked build: every hot-path kernel tests each global access against
+# its buffer's span and skips one outside it (REPOPS_ERR_BOUNDS), in place of
+# a memory sanitizer.  Same sources, -DREPOPS_DEBUG_BOUNDS, its own objects.
+OUT_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(OUT_CHECKED, "librepops_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 ARITH = ["-fmad=false", "-ftz=false", "-prec-div=true", "-prec-sqrt=true"]
@@ -52,8 +57,8 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def _compile(src: str, extra) -> str:
-    obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra, out_dir: str = OUT) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     deps = [src, __file__] + _headers()
     if not _stale(obj, deps):
         return obj
@@ -67,26 +72,30 @@ def _compile(src: str, extra) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0) -> str:
-    """Compiles (incrementally) and links librepops.so; returns its path."""
-    os.makedirs(OUT, exist_ok=True)
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0, checked: bool = False) -> str:
+    """Compiles (incrementally) and links librepops.so -- or, with checked,
+    the access-checking librepops_debug.so -- and returns its path."""
+    out_dir, lib = (OUT_CHECKED, LIB_CHECKED) if checked else (OUT, LIB)
+    os.makedirs(out_dir, exist_ok=True)
     if force:
-        for f in glob.glob(os.path.join(OUT, "*.o")):
+        for f in glob.glob(os.path.join(out_dir, "*.o")):
             os.remove(f)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if checked:
+        extra = extra + ["-DREPOPS_DEBUG_BOUNDS"]
     srcs = _sources()
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(max_workers=jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    if _stale(LIB, objs) or force:
-        tmp = LIB + ".tmp.%d" % os.getpid()
+        objs = list(ex.map(lambda s: _compile(s, extra, out_dir), srcs))
+    if _stale(lib, objs) or force:
+        tmp = lib + ".tmp.%d" % os.getpid()
         cmd = [nvcc()] + ARCH + ["-shared", "-o", tmp] + objs
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv, checked="--checked" in sys.argv))

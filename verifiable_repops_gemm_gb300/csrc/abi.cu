@@ -114,6 +114,7 @@ extern "C" const char *repops_status_string(int status) {
         case REPOPS_ERR_TIMEOUT: return "a bounded device-side wait gave up";
         case REPOPS_ERR_ALLOC: return "scratch allocation failed";
         case REPOPS_ERR_UNSUPPORTED: return "outside the supported limits";
+        case REPOPS_ERR_BOUNDS: return "a checked access fell outside its buffer (checked build)";
         default: return "unknown status";
     }
 }
@@ -125,7 +126,7 @@ extern "C" int repops_device_status(cudaStream_t stream, int *status_out) {
     unsigned v = 0;
     int rc = gemm_read_and_clear_device_status(stream, &v);
     if (rc != REPOPS_OK) return rc;
-    *status_out = v ? REPOPS_ERR_TIMEOUT : REPOPS_OK;
+    *status_out = (v & 2u) ? REPOPS_ERR_BOUNDS : v ? REPOPS_ERR_TIMEOUT : REPOPS_OK;
     return REPOPS_OK;
 }
 

@@ -68,6 +68,12 @@ int status_address(unsigned **out) {
     return shared_status_address(out);
 }
 
+}  // namespace
+
+int status_word_address(unsigned **out) { return status_address(out); }
+
+namespace {
+
 // Failure-detection self-test: thread 0 waits on a phase of an mbarrier that
 // nothing will complete, gives up after limit_ns and sets the sticky status
 // word, exactly as a GEMM wait that timed out would.  Nothing else is touched.
@@ -214,6 +220,16 @@ bool operand_span(int64_t rows, int64_t cols, int64_t ld, uint64_t *bytes) {
     if (elems > INT64_MAX / 4) return false;
     *bytes = uint64_t(elems) * 4u;
     return true;
+}
+
+// The spans of the caller's operands, for the checked build's access tests.
+void set_spans(GemmProblem &p, uint64_t a_bytes, uint64_t b_bytes, uint64_t c_bytes) {
+    p.span_a[0] = reinterpret_cast<uintptr_t>(p.A);
+    p.span_a[1] = p.span_a[0] + a_bytes;
+    p.span_b[0] = reinterpret_cast<uintptr_t>(p.B);
+    p.span_b[1] = p.span_b[0] + b_bytes;
+    p.span_c[0] = reinterpret_cast<uintptr_t>(p.C);
+    p.span_c[1] = p.span_c[0] + c_bytes;
 }
 
 __global__ void fill_positive_zero(float *C, int64_t M, int64_t N, int64_t ldc) {
@@ -403,6 +419,7 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     p.M = M; p.N = N; p.K = K;
     p.A = A; p.lda = lda; p.B = B; p.ldb = ldb; p.C = C; p.ldc = ldc;
     p.stream = stream;
+    set_spans(p, a_bytes, b_bytes, c_bytes);
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
     const bool sk_explicit = sk_req >= 0;
@@ -448,6 +465,8 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
             p.B = static_cast<const float *>(bscratch);
             p.ldb = pitch;
             p.transB = 0;
+            p.span_b[0] = reinterpret_cast<uintptr_t>(bscratch);
+            p.span_b[1] = p.span_b[0] + uint64_t(K) * uint64_t(pitch) * 4u;
         }
     }
     if (large && (!p.transA || !operand_tma_ready(p.A, p.lda))) {
@@ -460,6 +479,8 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
             p.A = static_cast<const float *>(ascratch);
             p.lda = pitch;
             p.transA = 1;
+            p.span_a[0] = reinterpret_cast<uintptr_t>(ascratch);
+            p.span_a[1] = p.span_a[0] + uint64_t(K) * uint64_t(pitch) * 4u;
         }
     }
     tma_ok = gemm_tma_eligible(p);
@@ -475,6 +496,7 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
         p.A = A; p.lda = lda; p.B = B; p.ldb = ldb;
         p.transA = transA ? 1 : 0;
         p.transB = transB ? 1 : 0;
+        set_spans(p, a_bytes, b_bytes, c_bytes);
         rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);
     }
     for (void *m : {bscratch, ascratch}) {
@@ -563,6 +585,7 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     // a bound that no row reaches leaves that side open
     p.k_lo = k_lo >= 0 && k_lo < M - 1 ? k_lo : -1;
     p.k_hi = k_hi >= 0 && k_hi < K - 1 ? k_hi : -1;
+    set_spans(p, a_bytes, b_bytes, c_bytes);
     int rc = status_address(&p.status);
     if (rc != REPOPS_OK) return rc;
 
@@ -589,6 +612,8 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
             p.A = static_cast<const float *>(ascratch);
             p.lda = pitch;
             p.transA = 1;
+            p.span_a[0] = reinterpret_cast<uintptr_t>(ascratch);
+            p.span_a[1] = p.span_a[0] + uint64_t(K) * uint64_t(pitch) * 4u;
         }
     }
     const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
@@ -597,6 +622,7 @@ int gemm_dispatch_batched(int config, int loader, int transA, int transB, int64_
     if (rc == REPOPS_ERR_UNSUPPORTED) rc = kLaunch[cfg](p, use);
     if (rc == REPOPS_ERR_UNSUPPORTED && use == REPOPS_LOADER_TMA && loader == REPOPS_LOADER_AUTO) {
         p.A = A; p.lda = lda; p.transA = transA ? 1 : 0;
+        set_spans(p, a_bytes, b_bytes, c_bytes);
         rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);   // the encoder refused a map
     }
     if (ascratch) {

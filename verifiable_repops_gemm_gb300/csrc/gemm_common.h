@@ -39,6 +39,9 @@ struct GemmProblem {
     // CTA per tile.
     int sk_workers = 0;
     void *sk_scratch = nullptr;
+    // Spans of A, B and C the checked build tests every access against
+    // (filled by the dispatchers; unused in the release build).
+    uintptr_t span_a[2] = {0, 0}, span_b[2] = {0, 0}, span_c[2] = {0, 0};
 };
 
 struct GemmConfigInfo {

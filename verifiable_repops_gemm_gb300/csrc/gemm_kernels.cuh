@@ -225,48 +225,6 @@ __device__ __forceinline__ void mma_stage(const float *__restrict__ As, const fl
     }
 }
 
-// Writes the thread's results; rows/columns past M/N are skipped.
-template <class T, bool A_KIN, bool B_KIN>
-__device__ __forceinline__ void store_acc(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
-                                          int64_t m0, int64_t n0, int abase, int bbase,
-                                          const float (&acc)[T::TM][T::TN], bool c_vec) {
-#pragma unroll
-    for (int r = 0; r < T::TM; ++r) {
-        const int64_t gm = m0 + a_row<A_KIN>(abase, r);
-        if (gm >= M) break;   // rows increase with r
-        float *crow = C + gm * ldc;
-        if constexpr (!B_KIN) {
-#pragma unroll
-            for (int q = 0; q < T::TN / 4; ++q) {
-                const int64_t gn = n0 + bbase + 32 * q;
-                if (c_vec && gn + 3 < N) {
-                    *reinterpret_cast<float4 *>(crow + gn) =
-                        make_float4(acc[r][4 * q], acc[r][4 * q + 1], acc[r][4 * q + 2], acc[r][4 * q + 3]);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        if (gn + t < N) crow[gn + t] = acc[r][4 * q + t];
-                }
-            }
-        } else {
-#pragma unroll
-            for (int c = 0; c < T::TN; ++c) {
-                const int64_t gn = n0 + b_col<true>(bbase, c);
-                if (gn < N) crow[gn] = acc[r][c];
-            }
-        }
-    }
-}
-
-template <class T, bool A_KIN, bool B_KIN>
-__device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
-                                           int64_t m0, int64_t n0, int abase, int bbase,
-                                           const PackedAcc<T, A_KIN> &pacc, bool c_vec) {
-    float acc[T::TM][T::TN];
-    pacc.to_float(acc);
-    store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec);
-}
-
 // Batch strides and epilogue of the EX kernels (kernel parameter).
 struct ExArgs {
     int64_t sA, sB, sC;    // batch strides of the operands, elements (cp.async path)
@@ -279,7 +237,55 @@ struct ExArgs {
     int64_t causal;        // >= 0: a tile wholly above j = causal + i is skipped
     int64_t k_lo, k_hi;    // >= 0: row i's k-chain covers [i - k_lo, i + k_hi] only
     int b_group;           // batch b reads B_(b / b_group)
+    DbgSpan da, db, dc;    // checked build: the spans of A, B and C,
+    DbgSpan dsk;           // of the chained split's scratch,
+    unsigned *dstat;       // and the status word
 };
+
+// Writes the thread's results; rows/columns past M/N are skipped.
+template <class T, bool A_KIN, bool B_KIN>
+__device__ __forceinline__ void store_acc(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
+                                          int64_t m0, int64_t n0, int abase, int bbase,
+                                          const float (&acc)[T::TM][T::TN], bool c_vec, const ExArgs &ep) {
+#pragma unroll
+    for (int r = 0; r < T::TM; ++r) {
+        const int64_t gm = m0 + a_row<A_KIN>(abase, r);
+        if (gm >= M) break;   // rows increase with r
+        float *crow = C + gm * ldc;
+        if constexpr (!B_KIN) {
+#pragma unroll
+            for (int q = 0; q < T::TN / 4; ++q) {
+                const int64_t gn = n0 + bbase + 32 * q;
+                if (c_vec && gn + 3 < N) {
+                    if (REPOPS_DBG_OK(ep.dc, crow + gn, 16, ep.dstat))
+                        *reinterpret_cast<float4 *>(crow + gn) =
+                            make_float4(acc[r][4 * q], acc[r][4 * q + 1], acc[r][4 * q + 2], acc[r][4 * q + 3]);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        if (gn + t < N && REPOPS_DBG_OK(ep.dc, crow + gn + t, 4, ep.dstat))
+                            crow[gn + t] = acc[r][4 * q + t];
+                }
+            }
+        } else {
+#pragma unroll
+            for (int c = 0; c < T::TN; ++c) {
+                const int64_t gn = n0 + b_col<true>(bbase, c);
+                if (gn < N && REPOPS_DBG_OK(ep.dc, crow + gn, 4, ep.dstat)) crow[gn] = acc[r][c];
+            }
+        }
+    }
+}
+
+template <class T, bool A_KIN, bool B_KIN>
+__device__ __forceinline__ void store_tile(float *__restrict__ C, int64_t ldc, int64_t M, int64_t N,
+                                           int64_t m0, int64_t n0, int abase, int bbase,
+                                           const PackedAcc<T, A_KIN> &pacc, bool c_vec, const ExArgs &ep) {
+    float acc[T::TM][T::TN];
+    pacc.to_float(acc);
+    store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec, ep);
+}
+
 
 // True when every element (i, j) of the tile has j > causal + i: the tile is
 // neither computed nor written.
@@ -358,7 +364,7 @@ __device__ __forceinline__ void store_tile_ex(float *__restrict__ C, int64_t ldc
             }
         }
     }
-    store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec);
+    store_acc<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec, ep);
 }
 
 __device__ __forceinline__ float *aligned_smem_base(unsigned char *raw) {
@@ -465,7 +471,7 @@ gemm_tma_ws_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         store_tile_ex<T, A_KIN, B_KIN>(C + b * ep.sC, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep,
                                        ep.R ? ep.R + b * ep.sR : nullptr);
     } else {
-        store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+        store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep);
     }
 }
 
@@ -671,7 +677,8 @@ gemm_tma_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         PackedAcc<T, A_KIN> acc;
         if (g.kind == 2) {
             // continue the chains the previous worker stored (its head of this tile)
-            if (!flag_wait_bounded(sk.flags + (w - 1) * T::THREADS + tid)) {
+            if (!REPOPS_DBG_OK(ep.dsk, sk.flags + (w - 1) * T::THREADS + tid, 4, ep.dstat) ||
+                !flag_wait_bounded(sk.flags + (w - 1) * T::THREADS + tid)) {
                 atomicOr(status, 1u);
                 return;
             }
@@ -680,7 +687,10 @@ gemm_tma_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             for (int i = 0; i < PackedAcc<T, A_KIN>::R; ++i)
 #pragma unroll
                 for (int j = 0; j < PackedAcc<T, A_KIN>::C; ++j)
-                    acc.v[i][j] = __ldcg(src + (i * PackedAcc<T, A_KIN>::C + j) * T::THREADS);
+                    acc.v[i][j] = REPOPS_DBG_OK(ep.dsk, src + (i * PackedAcc<T, A_KIN>::C + j) * T::THREADS, 8,
+                                                ep.dstat)
+                                      ? __ldcg(src + (i * PackedAcc<T, A_KIN>::C + j) * T::THREADS)
+                                      : 0ull;
         } else {
             acc.zero();
         }
@@ -705,12 +715,14 @@ gemm_tma_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             for (int i = 0; i < PackedAcc<T, A_KIN>::R; ++i)
 #pragma unroll
                 for (int j = 0; j < PackedAcc<T, A_KIN>::C; ++j)
-                    dst[(i * PackedAcc<T, A_KIN>::C + j) * T::THREADS] = acc.v[i][j];
-            st_release_gpu(sk.flags + w * T::THREADS + tid, 1u);
+                    if (REPOPS_DBG_OK(ep.dsk, dst + (i * PackedAcc<T, A_KIN>::C + j) * T::THREADS, 8, ep.dstat))
+                        dst[(i * PackedAcc<T, A_KIN>::C + j) * T::THREADS] = acc.v[i][j];
+            if (REPOPS_DBG_OK(ep.dsk, sk.flags + w * T::THREADS + tid, 4, ep.dstat))
+                st_release_gpu(sk.flags + w * T::THREADS + tid, 1u);
         } else if constexpr (EX) {
             store_tile_ex<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep, ep.R);
         } else {
-            store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+            store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep);
         }
     }
 }
@@ -723,7 +735,7 @@ template <class T, bool A_KIN, bool B_KIN>
 __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const float *__restrict__ A,
                                                    int64_t lda, const float *__restrict__ B, int64_t ldb,
                                                    int64_t M, int64_t N, int64_t K,
-                                                   int64_t m0, int64_t n0, int64_t k0, int tid) {
+                                                   int64_t m0, int64_t n0, int64_t k0, int tid, const ExArgs &ep) {
     constexpr int NW = T::THREADS / 32;
     if constexpr (A_KIN) {
         // element (r, k): a warp copies one 128-byte row segment
@@ -732,7 +744,7 @@ __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const f
 #pragma unroll 4
         for (int r = tid >> 5; r < T::BM; r += NW) {
             const int64_t gm = m0 + r;
-            const bool ok = gk < K && gm < M;
+            const bool ok = gk < K && gm < M && REPOPS_DBG_OK(ep.da, A + gm * lda + gk, 4, ep.dstat);
             cp_async_4(As + kin_off(r, k), ok ? A + gm * lda + gk : A, ok ? 4u : 0u);
         }
     } else {
@@ -740,7 +752,7 @@ __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const f
         for (int e = tid; e < BK * T::BM; e += T::THREADS) {
             const int k = e / T::BM, r = e % T::BM;
             const int64_t gk = k0 + k, gm = m0 + r;
-            const bool ok = gk < K && gm < M;
+            const bool ok = gk < K && gm < M && REPOPS_DBG_OK(ep.da, A + gk * lda + gm, 4, ep.dstat);
             cp_async_4(As + k * T::BM + r, ok ? A + gk * lda + gm : A, ok ? 4u : 0u);
         }
     }
@@ -750,7 +762,7 @@ __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const f
 #pragma unroll 4
         for (int r = tid >> 5; r < T::BN; r += NW) {
             const int64_t gn = n0 + r;
-            const bool ok = gk < K && gn < N;
+            const bool ok = gk < K && gn < N && REPOPS_DBG_OK(ep.db, B + gn * ldb + gk, 4, ep.dstat);
             cp_async_4(Bs + kin_off(r, k), ok ? B + gn * ldb + gk : B, ok ? 4u : 0u);
         }
     } else {
@@ -758,7 +770,7 @@ __device__ __forceinline__ void load_slice_cpasync(float *As, float *Bs, const f
         for (int e = tid; e < BK * T::BN; e += T::THREADS) {
             const int k = e / T::BN, r = e % T::BN;
             const int64_t gk = k0 + k, gn = n0 + r;
-            const bool ok = gk < K && gn < N;
+            const bool ok = gk < K && gn < N && REPOPS_DBG_OK(ep.db, B + gk * ldb + gn, 4, ep.dstat);
             cp_async_4(Bs + k * T::BN + r, ok ? B + gk * ldb + gn : B, ok ? 4u : 0u);
         }
     }
@@ -793,7 +805,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
         if (s < KT) {
             float *As = smem + s * T::STAGE_FLOATS;
             load_slice_cpasync<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, A, lda, B, ldb, M, N, K,
-                                                m0, n0, int64_t(kb + s) * BK, tid);
+                                                m0, n0, int64_t(kb + s) * BK, tid, ep);
         }
         cp_async_commit();
     }
@@ -814,7 +826,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
         if (nk < KT) {
             float *As = smem + (nk % T::STAGES) * T::STAGE_FLOATS;
             load_slice_cpasync<T, A_KIN, B_KIN>(As, As + T::A_FLOATS, A, lda, B, ldb, M, N, K,
-                                                m0, n0, int64_t(kb + nk) * BK, tid);
+                                                m0, n0, int64_t(kb + nk) * BK, tid, ep);
         }
         cp_async_commit();
         const float *As = smem + (kt % T::STAGES) * T::STAGE_FLOATS;
@@ -825,7 +837,7 @@ gemm_cpasync_kernel(const float *__restrict__ A, int64_t lda, const float *__res
         store_tile_ex<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep,
                                        ep.R ? ep.R + int64_t(blockIdx.y) * ep.sR : nullptr);
     else
-        store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0);
+        store_tile<T, A_KIN, B_KIN>(C, ldc, M, N, m0, n0, abase, bbase, acc, c_vec != 0, ep);
 }
 
 // --------------------------------------------------------------- host ----
@@ -888,6 +900,10 @@ inline ExArgs ex_args(const GemmProblem &p) {
     ep.causal = -1;
     ep.k_lo = ep.k_hi = -1;
     ep.b_group = 1;
+    ep.da.lo = p.span_a[0]; ep.da.hi = p.span_a[1];
+    ep.db.lo = p.span_b[0]; ep.db.hi = p.span_b[1];
+    ep.dc.lo = p.span_c[0]; ep.dc.hi = p.span_c[1];
+    ep.dstat = p.status;
     if (!p.ex) return ep;
     ep.sA = p.strideA; ep.sB = p.strideB; ep.sC = p.strideC;
     ep.zA = p.batch > 1 && p.strideA != 0;
@@ -968,6 +984,8 @@ int launch_tma_sk(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     sk.partial = static_cast<u64 *>(p.sk_scratch);
     sk.flags = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(p.sk_scratch) +
                                             sk_partial_bytes<T>(workers));
+    ExArgs eps = ep;
+    eps.dsk = dbg_span(p.sk_scratch, sk_partial_bytes<T>(workers) + size_t(workers) * T::THREADS * 4u);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(workers), 1u, 1u);
     cfg.blockDim = dim3(unsigned(T::THREADS + 32), 1u, 1u);
@@ -978,7 +996,7 @@ int launch_tma_sk(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n, c_vec, p.status, ep,
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, p.C, p.M, p.N, p.K, p.ldc, tiles_m, tiles_n, c_vec, p.status, eps,
                            sk);
     if (e != cudaSuccess) return set_cuda_error(e);
     return check_launch();

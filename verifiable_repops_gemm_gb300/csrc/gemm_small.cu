@@ -47,11 +47,18 @@ __device__ __forceinline__ void cp_async_4_to(uint32_t dst, const float *src, ui
                  : "memory");
 }
 
+// The checked build's spans of A, B and C and the status word (unused in the
+// release build).
+struct SmallDbg {
+    DbgSpan a, b, c;
+    unsigned *status;
+};
+
 template <int STAGES>
 __global__ void __launch_bounds__(kSmThreads)
 gemm_small_kernel(int transA, int transB, int64_t M, int64_t N, int64_t K,
                   const float *__restrict__ A, int64_t lda, const float *__restrict__ B, int64_t ldb,
-                  float *__restrict__ C, int64_t ldc) {
+                  float *__restrict__ C, int64_t ldc, const SmallDbg dbg) {
     extern __shared__ __align__(16) unsigned char small_smem_raw[];
     SmallSmem<STAGES> &sm = *reinterpret_cast<SmallSmem<STAGES> *>(small_smem_raw);
     const int64_t m0 = int64_t(blockIdx.x) * kSmBM, n0 = int64_t(blockIdx.y) * kSmBN;
@@ -93,12 +100,12 @@ gemm_small_kernel(int transA, int transB, int64_t M, int64_t N, int64_t K,
         const float *Ac = A + c * ainc, *Bc = B + c * binc;
 #pragma unroll
         for (int r = 0; r < kRA; ++r) {
-            const bool ok = alim[r] < kr;
+            const bool ok = alim[r] < kr && REPOPS_DBG_OK(dbg.a, Ac + aoff[r], 4, dbg.status);
             cp_async_4_to(adst[r] + s * kStageA, ok ? Ac + aoff[r] : A, ok ? 4u : 0u);
         }
 #pragma unroll
         for (int r = 0; r < kRB; ++r) {
-            const bool ok = blim[r] < kr;
+            const bool ok = blim[r] < kr && REPOPS_DBG_OK(dbg.b, Bc + boff[r], 4, dbg.status);
             cp_async_4_to(bdst[r] + s * kStageB, ok ? Bc + boff[r] : B, ok ? 4u : 0u);
         }
     };
@@ -134,14 +141,13 @@ gemm_small_kernel(int transA, int transB, int64_t M, int64_t N, int64_t K,
     unpack2(acc0, c00, c01);
     unpack2(acc1, c10, c11);
     const int64_t i0 = m0 + 2 * ty, j0 = n0 + 2 * tx;
-    if (i0 < M) {
-        if (j0 < N) C[i0 * ldc + j0] = c00;
-        if (j0 + 1 < N) C[i0 * ldc + j0 + 1] = c01;
-    }
-    if (i0 + 1 < M) {
-        if (j0 < N) C[(i0 + 1) * ldc + j0] = c10;
-        if (j0 + 1 < N) C[(i0 + 1) * ldc + j0 + 1] = c11;
-    }
+    auto put = [&](int64_t i, int64_t j, float v) {
+        if (i < M && j < N && REPOPS_DBG_OK(dbg.c, C + i * ldc + j, 4, dbg.status)) C[i * ldc + j] = v;
+    };
+    put(i0, j0, c00);
+    put(i0, j0 + 1, c01);
+    put(i0 + 1, j0, c10);
+    put(i0 + 1, j0 + 1, c11);
 }
 
 constexpr int kSmStages = 3;
@@ -154,8 +160,13 @@ int gemm_small_launch(const GemmProblem &p) {
     constexpr int smem = int(sizeof(SmallSmem<kSmStages>));
     static_assert(smem <= 48 * 1024, "the ring fits the default dynamic shared memory limit");
     auto kern = gemm_small_kernel<kSmStages>;
+    SmallDbg dbg;
+    dbg.a.lo = p.span_a[0]; dbg.a.hi = p.span_a[1];
+    dbg.b.lo = p.span_b[0]; dbg.b.hi = p.span_b[1];
+    dbg.c.lo = p.span_c[0]; dbg.c.hi = p.span_c[1];
+    dbg.status = p.status;
     kern<<<dim3(unsigned(gm), unsigned(gn)), kSmThreads, smem, p.stream>>>(
-        p.transA, p.transB, p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc);
+        p.transA, p.transB, p.M, p.N, p.K, p.A, p.lda, p.B, p.ldb, p.C, p.ldc, dbg);
     return check_launch();
 }
 

@@ -49,6 +49,41 @@ int gemm_read_and_clear_device_status(cudaStream_t stream, unsigned *value);
 // while the key stays the same.  0 when there is no current context.
 int current_context_key(uint64_t *key);
 
+// The device address of the status word this host thread's launches report
+// into (its bound word, else the device's shared one).
+int status_word_address(unsigned **out);
+
+// ------------------------------------------------------- debug bounds ----
+// The checked build (compiled with -DREPOPS_DEBUG_BOUNDS into
+// librepops_debug.so by build.build(debug_bounds=True)): the hot-path kernels
+// test every global access against the span of the buffer it belongs to; an
+// access outside it is skipped and bit 1 of the status word is set, which
+// repops_device_status reports as REPOPS_ERR_BOUNDS.  A stand-in for a memory
+// sanitizer that never traps or faults.  In the release build the test is the
+// constant `true` and compiles away; the spans are then unused parameters.
+struct DbgSpan {
+    uintptr_t lo = 0, hi = 0;   // the allowed bytes [lo, hi)
+};
+
+inline DbgSpan dbg_span(const void *p, uint64_t bytes) {
+    DbgSpan s;
+    s.lo = reinterpret_cast<uintptr_t>(p);
+    s.hi = s.lo + bytes;
+    return s;
+}
+
+#ifdef REPOPS_DEBUG_BOUNDS
+__device__ __forceinline__ bool dbg_in(const DbgSpan &s, const void *p, uint32_t n, unsigned *status) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if (a >= s.lo && a <= s.hi && n <= s.hi - a) return true;
+    if (status) atomicOr(status, 2u);
+    return false;
+}
+#define REPOPS_DBG_OK(span, p, n, status) ::repops::dbg_in((span), (p), (n), (status))
+#else
+#define REPOPS_DBG_OK(span, p, n, status) true
+#endif
+
 // Limit for every device-side wait, in nanoseconds of %globaltimer.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 

@@ -54,6 +54,10 @@ struct MeanScalars {
     float count;     // (float)k, exact for k < 2^24
     float inv;       // 1/k when pow2
     float eta;
+    // checked build: theta's span, the bytes of one gradient (every gradient
+    // access is tested as an offset into [0, gbytes)), the status word
+    DbgSpan th, goff;
+    unsigned *status;
 };
 
 __device__ __forceinline__ float mean_of(float S, const MeanScalars &s) {
@@ -90,7 +94,11 @@ __global__ void __launch_bounds__(256)
 mean_sgd_vec4(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t n4,
               float *__restrict__ theta) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    constexpr uint32_t GB = TY == REPOPS_TYPE_F32 ? 16u : 8u;   // bytes of 4 gradient elements
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < n4; i += stride) {
+        if (!REPOPS_DBG_OK(sc.th, reinterpret_cast<const float4 *>(theta) + i, 16, sc.status) ||
+            !REPOPS_DBG_OK(sc.goff, reinterpret_cast<const void *>(uintptr_t(i) * GB), GB, sc.status))
+            continue;
         float4 th = __ldcs(reinterpret_cast<const float4 *>(theta) + i);
         float4 S;
         if constexpr (NC > 0) {
@@ -127,7 +135,11 @@ __global__ void __launch_bounds__(256)
 mean_sgd_scalar(const __grid_constant__ GradPtrs gp, const MeanScalars sc, int64_t first, int64_t len,
                 float *__restrict__ theta) {
     const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    constexpr uint32_t GB = TY == REPOPS_TYPE_F32 ? 4u : 2u;   // bytes of one gradient element
     for (int64_t e = first + blockIdx.x * int64_t(blockDim.x) + threadIdx.x; e < len; e += stride) {
+        if (!REPOPS_DBG_OK(sc.th, theta + e, 4, sc.status) ||
+            !REPOPS_DBG_OK(sc.goff, reinterpret_cast<const void *>(uintptr_t(e) * GB), GB, sc.status))
+            continue;
         float S = ld1<TY>(gp.g[0], e);
         for (int r = 1; r < sc.nC; ++r) S = __fadd_rn(S, ld1<TY>(gp.g[r], e));
         theta[e] = sgd(theta[e], mean_of(S, sc), sc.eta);
@@ -204,6 +216,10 @@ int mean_sgd_typed(int nC, int64_t len, const void *const *ptrs, int gtype, cons
     sc.count = float(nC);
     sc.inv = sc.pow2 ? 1.0f / float(nC) : 0.0f;   // exact: a power of two
     sc.eta = eta;
+    sc.th = dbg_span(theta, bytes);
+    sc.goff = dbg_span(nullptr, gbytes);
+    int rs = status_word_address(&sc.status);
+    if (rs != REPOPS_OK) return rs;
 
     DeviceInfo di;
     int rc = current_device_info(&di);

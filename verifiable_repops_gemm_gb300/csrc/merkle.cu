@@ -238,8 +238,17 @@ __device__ __forceinline__ uint64_t level_offset(uint64_t n, int level) {
     return off;
 }
 
-__device__ __forceinline__ void store_node(const TreeOut &to, int level, uint64_t idx, const uint32_t (&st)[8]) {
+// The checked build's spans (input bytes, level scratch, root, stored tree)
+// and the status word; unused in the release build.
+struct MerkleDbg {
+    DbgSpan data, ws, root, tree;
+    unsigned *status;
+};
+
+__device__ __forceinline__ void store_node(const TreeOut &to, int level, uint64_t idx, const uint32_t (&st)[8],
+                                           const MerkleDbg &dbg) {
     uint4 *dst = reinterpret_cast<uint4 *>(to.tree + 32 * (level_offset(to.nleaves, level) + idx));
+    if (!REPOPS_DBG_OK(dbg.tree, dst, 32, dbg.status)) return;
     dst[0] = make_uint4(__byte_perm(st[0], 0, 0x0123), __byte_perm(st[1], 0, 0x0123),
                         __byte_perm(st[2], 0, 0x0123), __byte_perm(st[3], 0, 0x0123));
     dst[1] = make_uint4(__byte_perm(st[4], 0, 0x0123), __byte_perm(st[5], 0, 0x0123),
@@ -251,7 +260,8 @@ __device__ __forceinline__ void store_node(const TreeOut &to, int level, uint64_
 // of the CTA must call it (it synchronises).
 template <int N>
 __device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const PipeConst &pc,
-                                        const TreeOut &to, int level_in, uint64_t base, int fold_levels) {
+                                        const TreeOut &to, int level_in, uint64_t base, int fold_levels,
+                                        const MerkleDbg &dbg) {
     int cur = 0;
     int k = 0;   // levels folded so far
     while (cnt > 1) {   // uniform across the CTA
@@ -270,7 +280,7 @@ __device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const Pi
             }
 #pragma unroll
             for (int w = 0; w < 8; ++w) buf[cur ^ 1][w][j] = o[w];
-            if (to.tree) store_node(to, level_in + k + 1, (base >> (k + 1)) + j, o);
+            if (to.tree) store_node(to, level_in + k + 1, (base >> (k + 1)) + j, o, dbg);
         }
         cur ^= 1;
         cnt = (cnt + 1) / 2;
@@ -285,7 +295,7 @@ __device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const Pi
             uint32_t o[8];
 #pragma unroll
             for (int w = 0; w < 8; ++w) o[w] = buf[cur][w][0];
-            for (int kk = k + 1; kk <= last; ++kk) store_node(to, level_in + kk, base >> kk, o);
+            for (int kk = k + 1; kk <= last; ++kk) store_node(to, level_in + kk, base >> kk, o, dbg);
         }
     }
     return cur;
@@ -294,29 +304,31 @@ __device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const Pi
 __global__ void __launch_bounds__(LEAF_CTA)
 merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t leaf, uint64_t nleaves,
                     int fast_ok, uint32_t *__restrict__ level_out, uint8_t *__restrict__ root_out,
-                    const PipeConst pc, const TreeOut to) {
+                    const PipeConst pc, const TreeOut to, const MerkleDbg dbg) {
     __shared__ uint32_t buf[2][8][LEAF_CTA];
     const uint64_t base = uint64_t(blockIdx.x) * LEAF_CTA;
     const uint64_t i = base + threadIdx.x;
     if (i < nleaves) {
         const uint64_t start = i * leaf;
         const uint64_t len = min(uint64_t(leaf), bytes - start);
-        uint32_t st[8];
-        if (fast_ok && len == leaf) leaf_digest_fast(data + start, leaf, st, pc);
-        else leaf_digest_generic(data + start, len, st, pc);
+        uint32_t st[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+        if (REPOPS_DBG_OK(dbg.data, data + start, uint32_t(len), dbg.status)) {
+            if (fast_ok && len == leaf) leaf_digest_fast(data + start, leaf, st, pc);
+            else leaf_digest_generic(data + start, len, st, pc);
+        }
 #pragma unroll
         for (int w = 0; w < 8; ++w) buf[0][w][threadIdx.x] = st[w];
-        if (to.tree) store_node(to, 0, i, st);
+        if (to.tree) store_node(to, 0, i, st, dbg);
     }
     const int cnt = int(min(uint64_t(LEAF_CTA), nleaves - base));
-    const int cur = cta_fold<LEAF_CTA>(buf, cnt, pc, to, 0, base, LOG_LEAF_CTA);
+    const int cur = cta_fold<LEAF_CTA>(buf, cnt, pc, to, 0, base, LOG_LEAF_CTA, dbg);
     if (threadIdx.x == 0) {
         uint32_t st[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w) st[w] = buf[cur][w][0];
         if (root_out) {
-            store_root(root_out, st);
-        } else {
+            if (REPOPS_DBG_OK(dbg.root, root_out, 32, dbg.status)) store_root(root_out, st);
+        } else if (REPOPS_DBG_OK(dbg.ws, level_out + 8 * blockIdx.x, 32, dbg.status)) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) level_out[8 * blockIdx.x + w] = st[w];
         }
@@ -325,24 +337,26 @@ merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t l
 
 __global__ void __launch_bounds__(RED_CTA)
 merkle_reduce(const uint32_t *__restrict__ in, uint64_t n, uint32_t *__restrict__ out,
-              uint8_t *__restrict__ root_out, const PipeConst pc, const TreeOut to, int level_in) {
+              uint8_t *__restrict__ root_out, const PipeConst pc, const TreeOut to, int level_in,
+              const MerkleDbg dbg) {
     __shared__ uint32_t buf[2][8][2 * RED_CTA];
     const uint64_t base = uint64_t(blockIdx.x) * 2 * RED_CTA;
     const int cnt = int(min(uint64_t(2 * RED_CTA), n - base));
     for (int j = threadIdx.x; j < cnt; j += RED_CTA) {
-        const uint4 lo = *reinterpret_cast<const uint4 *>(in + 8 * (base + j));
-        const uint4 hi = *reinterpret_cast<const uint4 *>(in + 8 * (base + j) + 4);
+        const bool ok = REPOPS_DBG_OK(dbg.ws, in + 8 * (base + j), 32, dbg.status);
+        const uint4 lo = ok ? *reinterpret_cast<const uint4 *>(in + 8 * (base + j)) : make_uint4(0, 0, 0, 0);
+        const uint4 hi = ok ? *reinterpret_cast<const uint4 *>(in + 8 * (base + j) + 4) : make_uint4(0, 0, 0, 0);
         buf[0][0][j] = lo.x; buf[0][1][j] = lo.y; buf[0][2][j] = lo.z; buf[0][3][j] = lo.w;
         buf[0][4][j] = hi.x; buf[0][5][j] = hi.y; buf[0][6][j] = hi.z; buf[0][7][j] = hi.w;
     }
-    const int cur = cta_fold<2 * RED_CTA>(buf, cnt, pc, to, level_in, base, LOG_RED_NODES);
+    const int cur = cta_fold<2 * RED_CTA>(buf, cnt, pc, to, level_in, base, LOG_RED_NODES, dbg);
     if (threadIdx.x == 0) {
         uint32_t st[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w) st[w] = buf[cur][w][0];
         if (root_out) {
-            store_root(root_out, st);
-        } else {
+            if (REPOPS_DBG_OK(dbg.root, root_out, 32, dbg.status)) store_root(root_out, st);
+        } else if (REPOPS_DBG_OK(dbg.ws, out + 8 * blockIdx.x, 32, dbg.status)) {
 #pragma unroll
             for (int w = 0; w < 8; ++w) out[8 * blockIdx.x + w] = st[w];
         }
@@ -366,6 +380,8 @@ bool plan_for(uint64_t bytes, uint32_t leaf, Plan *p) {
     return true;
 }
 
+uint64_t total_nodes(uint64_t nleaves);
+
 int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void *ws, const Plan &pl,
         cudaStream_t stream, const TreeOut to = TreeOut{nullptr, 0}) {
     const uint8_t *data = static_cast<const uint8_t *>(ptr);
@@ -373,9 +389,16 @@ int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void 
     const PipeConst pc{1u};
     uint32_t *bufA = static_cast<uint32_t *>(ws);
     uint32_t *bufB = bufA ? bufA + 8 * pl.n1 : nullptr;
+    MerkleDbg dbg{};
+    dbg.data = dbg_span(data, bytes);
+    dbg.ws = dbg_span(ws, pl.ws_bytes);
+    dbg.root = dbg_span(root_out, 32);
+    dbg.tree = dbg_span(to.tree, to.tree ? total_nodes(to.nleaves) * 32u : 0);
+    int rc = status_word_address(&dbg.status);
+    if (rc != REPOPS_OK) return rc;
     merkle_leaf_subtree<<<unsigned(pl.n1), LEAF_CTA, 0, stream>>>(
-        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr, pc, to);
-    int rc = check_launch();
+        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr, pc, to, dbg);
+    rc = check_launch();
     if (rc != REPOPS_OK) return rc;
     uint64_t n = pl.n1;
     int level = LOG_LEAF_CTA;
@@ -383,7 +406,7 @@ int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void 
     while (n > 1) {
         const uint64_t blocks = (n + 2 * RED_CTA - 1) / (2 * RED_CTA);
         merkle_reduce<<<unsigned(blocks), RED_CTA, 0, stream>>>(src, n, dst, blocks == 1 ? root_out : nullptr,
-                                                                pc, to, level);
+                                                                pc, to, level, dbg);
         rc = check_launch();
         if (rc != REPOPS_OK) return rc;
         n = blocks;
