@@ -156,8 +156,8 @@ def test_persistent_row_loop(rp, orc):
 
 # causal: every kernel shape, aligned and unaligned rows, in place, first = 0
 # and first > 0 (a later query block), and first past the row (no mask)
-@pytest.mark.parametrize("cols,pad", [(5, 0), (37, 3), (1000, 0), (2048, 0), (4096, 1), (8193, 3),
-                                      (16385, 3), (40000, 0)])
+@pytest.mark.parametrize("cols,pad", [(5, 0), (37, 3), (1000, 0), (2048, 0), (4095, 1), (4096, 0), (4096, 1),
+                                      (4097, 3), (8193, 3), (16385, 3), (40000, 0)])
 @pytest.mark.parametrize("first", [0, 700])
 def test_causal_softmax_matches_oracle(rp, orc, cols, pad, first):
     rows = 6 if cols <= 8192 else 3
@@ -167,6 +167,20 @@ def test_causal_softmax_matches_oracle(rp, orc, cols, pad, first):
     z = x.clone()
     rp.softmax_rows(z, out=z, causal_first=first)
     assert np.array_equal(u32(z.cpu().numpy()), u32(want))
+
+
+@pytest.mark.parametrize("cols,first,period", [(300, 0, 300), (2048, 0, 2048), (130, 3, 50)])
+def test_causal_softmax_many_rows(rp, orc, cols, first, period):
+    # more rows than the persistent grid has warps: every warp runs several
+    # rows of different prefix lengths
+    rows = 7000
+    x = rows_input(rows, cols, 14000 + cols, 3.0)
+    got = rp.softmax_rows(x, causal_first=first, causal_period=period)
+    pick = [0, 1, 2, 3, 607, 608, 2431, 4095, 6998, 6999]
+    xp = x[pick].cpu().numpy()
+    want = np.stack([orc.softmax_rows_causal(xp[k:k + 1], first + (r % period), 10 ** 9)[0]
+                     for k, r in enumerate(pick)])
+    assert np.array_equal(u32(got[pick].cpu().numpy()), u32(want))
 
 
 def test_causal_softmax_ignores_masked_values(rp):

@@ -411,6 +411,122 @@ softmax_causal_rows_kernel(int64_t rows, int64_t n, const float *__restrict__ x,
     cp_async_wait<0>();
 }
 
+// Causal softmax with one warp per row and no CTA-wide barrier, for aligned
+// rows of at most WARP_CAUSAL_MAX_COLS values: a short prefix no longer keeps
+// a whole CTA waiting at the row's barriers.  The warp copies the prefix into
+// its own shared-memory row (16-byte groups of each 32-value run permuted by
+// the run index, so that a lane per run reads without bank conflicts and
+// 4 consecutive values stay contiguous), folds the max tree (a lane per run,
+// then shuffles), exponentiates with every lane (4 values at a time, in
+// place), folds the sum tree the same way, and writes the row: e * (1/s) in
+// the prefix, +0 after.  The same operations as softmax_causal_rows_kernel.
+constexpr int WARP_CAUSAL_MAX_COLS = 4096;
+constexpr int WARP_CAUSAL_WARPS = 4;
+
+__device__ __forceinline__ int wc_pos(int j) { return (j & ~31) | ((j & 31) ^ (((j >> 5) & 7) << 2)); }
+
+// Run results of a row held by lane l for runs l, l + 32, l + 64, l + 96
+// (present below nruns): the tree's upper levels, to every lane.
+template <Op OP>
+__device__ __forceinline__ float warp_runs_root(const float (&rr)[4], int nruns) {
+    float root = 0.0f;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        const int have = nruns - 32 * g;
+        if (have <= 0) break;                       // warp-uniform
+        float acc = __shfl_sync(0xffffffffu, rr[g], 0);
+#pragma unroll
+        for (int i = 1; i < 32; ++i) {
+            const float o = __shfl_sync(0xffffffffu, rr[g], i);
+            if (i < have) acc = combine<OP>(acc, o);
+        }
+        root = g == 0 ? acc : combine<OP>(root, acc);
+    }
+    return root;
+}
+
+// The fold of one 32-value run of a staged row, left to right over its first
+// len values.
+template <Op OP>
+__device__ __forceinline__ float fold_run(const float *run, int u, int len) {
+    float acc = 0.0f;
+#pragma unroll
+    for (int q4 = 0; q4 < 8; ++q4) {
+        const float4 t = *reinterpret_cast<const float4 *>(run + 4 * (q4 ^ (u & 7)));
+        const float v4[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int idx = 4 * q4 + e;
+            if (idx == 0) acc = v4[0];
+            else if (idx < len) acc = combine<OP>(acc, v4[e]);
+        }
+    }
+    return acc;
+}
+
+__global__ void __launch_bounds__(32 * WARP_CAUSAL_WARPS)
+softmax_causal_warp_kernel(int64_t rows, int n, const float *__restrict__ x, int64_t ldx, float *__restrict__ y,
+                           int64_t ldy, int64_t first, int64_t period, int row_floats) {
+    extern __shared__ float4 wc_smem4[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float *stage = reinterpret_cast<float *>(wc_smem4) + warp * row_floats;
+    const int64_t gw = int64_t(blockIdx.x) * WARP_CAUSAL_WARPS + warp;
+    const int64_t nw = int64_t(gridDim.x) * WARP_CAUSAL_WARPS;
+    for (int64_t row = gw; row < rows; row += nw) {
+        const int L = int(imin64(n, first + row % period + 1));
+        const float *xr = x + row * ldx;
+        // the prefix, 16 bytes a copy (a short last group reads only its values)
+        for (int j4 = 4 * lane; j4 < L; j4 += 128) {
+            const int have = L - j4;
+            cp_async_16(stage + wc_pos(j4), xr + j4, have >= 4 ? 16u : uint32_t(have) * 4u);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        __syncwarp();
+        const int nruns = (L + RUN - 1) / RUN;
+        float rr[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int u = lane + 32 * g;
+            rr[g] = u < nruns ? fold_run<Op::Max>(stage + 32 * u, u, min(RUN, L - 32 * u)) : 0.0f;
+        }
+        const float m = warp_runs_root<Op::Max>(rr, nruns);
+        __syncwarp();                               // every run read before it is overwritten
+        for (int j4 = 4 * lane; j4 < L; j4 += 128) {
+            float4 *p4 = reinterpret_cast<float4 *>(stage + wc_pos(j4));
+            float4 t = *p4;
+            exp_minus2(t.x, t.y, m);
+            exp_minus2(t.z, t.w, m);
+            *p4 = t;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int u = lane + 32 * g;
+            rr[g] = u < nruns ? fold_run<Op::Sum>(stage + 32 * u, u, min(RUN, L - 32 * u)) : 0.0f;
+        }
+        const float inv = __frcp_rn(warp_runs_root<Op::Sum>(rr, nruns));
+        float *yr = y + row * ldy;
+        for (int j4 = 4 * lane; j4 < n; j4 += 128) {
+            float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (j4 < L) {
+                t = *reinterpret_cast<const float4 *>(stage + wc_pos(j4));
+                t.x = j4 + 0 < L ? __fmul_rn(t.x, inv) : 0.0f;
+                t.y = j4 + 1 < L ? __fmul_rn(t.y, inv) : 0.0f;
+                t.z = j4 + 2 < L ? __fmul_rn(t.z, inv) : 0.0f;
+                t.w = j4 + 3 < L ? __fmul_rn(t.w, inv) : 0.0f;
+            }
+            if (j4 + 3 < n) {
+                __stcs(reinterpret_cast<float4 *>(yr + j4), t);
+            } else {                                // the row's last, short group
+                const float v[4] = {t.x, t.y, t.z, t.w};
+                for (int e = 0; j4 + e < n; ++e) yr[j4 + e] = v[e];
+            }
+        }
+        __syncwarp();                               // the stage is refilled by the next row
+    }
+}
+
 // psm: gamma and beta are staged in shared memory (aligned, and they fit).
 template <int T, int R>
 __global__ void __launch_bounds__(T)
@@ -915,6 +1031,13 @@ extern "C" int repops_softmax_rows_causal_f32(int64_t rows, int64_t cols, const 
     int rc = check_rows(rows, cols, x, ldx, y, ldy);
     if (rc != REPOPS_OK || rows == 0 || cols == 0) return rc;
     // from first >= cols on, every row sees all its columns
+    if (first < cols && cols <= WARP_CAUSAL_MAX_COLS && rows_vec_ok(x, ldx, y, ldy)) {
+        const int row_floats = int((cols + RUN - 1) / RUN * RUN);
+        const size_t smem = size_t(WARP_CAUSAL_WARPS) * row_floats * sizeof(float);
+        return launch_persistent(softmax_causal_warp_kernel, 32 * WARP_CAUSAL_WARPS, smem,
+                                 (rows + WARP_CAUSAL_WARPS - 1) / WARP_CAUSAL_WARPS, stream, rows, int(cols), x, ldx,
+                                 y, ldy, first, period, row_floats);
+    }
     return run_rows(0, rows, cols, x, ldx, nullptr, nullptr, 0.0f, y, ldy, stream, first < cols ? first : -1,
                     period);
 }
