@@ -220,3 +220,78 @@ def test_epilogue_special_values(rp, orc, act):
     nan = np.isnan(C)
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(u32(got[~nan]), u32(C[~nan]))
+
+
+# ------------------------------------------------- attention-sized ----
+# Batched, causal and banded products with many tiles (attention's shapes,
+# shrunk): the automatic choice against explicit configurations and the
+# oracle -- causal scores of grouped heads, both bands, an epilogue with bias
+# and residual over 24 batches, and B shared by groups of batches.
+
+def _oracle_batched(orc, A, B, alpha=1.0, k_lo=-1, k_hi=-1, b_group=1, bias=None, R=None):
+    """Oracle of out[b] = A[b] @ B[b // b_group] on contiguous host copies."""
+    A = np.ascontiguousarray(A.cpu().numpy(), dtype=np.float32)
+    B = np.ascontiguousarray(B.cpu().numpy(), dtype=np.float32)
+    batch, M, K = A.shape
+    N = B.shape[2]
+    C = np.zeros(batch * M * N, np.float32)
+    Rh = np.ascontiguousarray(R.cpu().numpy(), dtype=np.float32).reshape(-1) if R is not None else None
+    orc.gemm_batched(0, 0, batch, M, N, K, A.reshape(-1), K, M * K, B.reshape(-1), N, K * N, C, N, M * N, alpha,
+                     bias.cpu().numpy() if bias is not None else None, 0, Rh, N, M * N, k_lo=k_lo, k_hi=k_hi,
+                     b_group=b_group)
+    return C.reshape(batch, M, N)
+
+
+@pytest.mark.parametrize("case", ["scores", "band_hi", "band_lo", "epilogue", "grouped"])
+def test_attention_sized_batched_products(rp, orc, case):
+    g = 1000 + ["scores", "band_hi", "band_lo", "epilogue", "grouped"].index(case)
+    if case == "scores":          # Q K^T of 12 heads over 3 key/value heads, causal tiles skipped
+        Q = inputs.normal((12, 700, 64), 1.0, g, DEV)
+        Kt = inputs.normal((3, 700, 64), 1.0, g + 1, DEV).transpose(1, 2)
+        kw = dict(alpha=0.125, causal_first=0)
+        got = rp.gemm_batched(Q, Kt, **kw)
+        ref = rp.gemm_batched(Q, Kt, config=1, loader=rp.LOADER_TMA, **kw)
+        # only tiles on or below the diagonal are specified: compare the lower triangle
+        mask = torch.tril(torch.ones(700, 700, dtype=torch.bool, device=DEV)).expand(12, -1, -1)
+        assert torch.equal(got[mask].view(torch.int32), ref[mask].view(torch.int32))
+        Qh, Kh = Q.cpu().numpy(), Kt.cpu().numpy()
+        for h in (0, 5, 11):
+            want = orc.gemm(np.ascontiguousarray(Qh[h]), np.ascontiguousarray(Kh[h // 4])) * np.float32(0.125)
+            tri = np.tril(np.ones((700, 700), bool))
+            assert np.array_equal(u32(got[h].cpu().numpy()[tri]), u32(want.astype(np.float32)[tri])), h
+        return
+    if case in ("band_hi", "band_lo"):   # P V over k <= i, and P^T dO over k >= i
+        S = 900
+        P = torch.tril(inputs.uniform_pm1((10, S, S), g, DEV))
+        V = inputs.normal((10, S, 64), 1.0, g + 1, DEV)
+        if case == "band_hi":
+            A, kw = P, dict(k_hi=0)
+        else:
+            A, kw = P.transpose(1, 2).contiguous(), dict(k_lo=0)
+        got = rp.gemm_batched(A, V, **kw)
+        for cfg in (3, 4):
+            ref = rp.gemm_batched(A, V, config=cfg, loader=rp.LOADER_TMA, **kw)
+            assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), cfg
+        want = _oracle_batched(orc, A, V, **kw)
+        assert np.array_equal(u32(got.cpu().numpy()), u32(want))
+        return
+    if case == "epilogue":        # bias and a residual, 24 batches
+        A = inputs.normal((24, 300, 200), 1.0, g, DEV)
+        B = inputs.normal((24, 200, 260), 1.0, g + 1, DEV)
+        bias = inputs.normal((260,), 1.0, g + 2, DEV)
+        R = inputs.normal((24, 300, 260), 1.0, g + 3, DEV)
+        got = rp.gemm_batched(A, B, alpha=0.5, bias=bias, residual=R)
+        ref = rp.gemm_batched(A, B, alpha=0.5, bias=bias, residual=R, config=3, loader=rp.LOADER_TMA)
+        assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+        want = _oracle_batched(orc, A, B, alpha=0.5, bias=bias, R=R)
+        assert np.array_equal(u32(got.cpu().numpy()), u32(want))
+        return
+    # grouped: 16 batches over 4 shared B matrices (a stride-0 expansion per group)
+    A = inputs.normal((16, 400, 96), 1.0, g, DEV)
+    B = inputs.normal((4, 96, 320), 1.0, g + 1, DEV)
+    Bx = B.repeat_interleave(4, dim=0)        # the oracle's view: batch b reads B[b // 4]
+    got = rp.gemm_batched(A, B)
+    ref = rp.gemm_batched(A, B, config=1, loader=rp.LOADER_TMA)
+    assert torch.equal(got.view(torch.int32), ref.view(torch.int32))
+    want = _oracle_batched(orc, A, Bx)
+    assert np.array_equal(u32(got.cpu().numpy()), u32(want))
