@@ -371,6 +371,22 @@ int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs,
                                 const int *order, float eta, float *theta,
                                 cudaStream_t stream);
 
+/* As repops_fixed_order_mean_sgd with the gradients and theta in HOST memory
+ * (page-locked for full speed): ptrs (host) holds nC host pointers of len
+ * floats each, theta (host, len floats) is updated in place.  The call takes
+ * device memory for two element chunks (up to 2^22 elements, at most about
+ * 1 GiB in all) with cudaMallocAsync on `stream`, copies each chunk of every
+ * gradient and of theta in on a helper stream while the previous chunk is
+ * folded on `stream`, copies theta's chunk back on a second helper stream, and
+ * releases the memory; everything is ordered before work later enqueued on
+ * `stream`.  Asynchronous: the buffers must stay valid, and theta is complete,
+ * once `stream` has reached this point.  The bits equal
+ * repops_fixed_order_mean_sgd's (elements are independent).  Errors as that
+ * call, plus ALLOC; ALIAS compares host ranges. */
+int repops_fixed_order_mean_sgd_host(int nC, int64_t len, const float *const *ptrs,
+                                     const int *order, float eta, float *theta,
+                                     cudaStream_t stream);
+
 /* As repops_fixed_order_mean_sgd with the gradients stored as grad_type
  * (REPOPS_TYPE_F32, _F16 or _BF16, see "Half-precision storage" below): each
  * gradient element is widened exactly to binary32 before the fold; theta stays
@@ -562,6 +578,18 @@ int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len,
  * iters + 1 compressions a thread.  INVALID_ARG for a null pointer or a bad
  * count. */
 int repops_sha256_rate_probe(uint32_t threads, uint32_t iters, uint32_t *digests, cudaStream_t stream);
+
+/* As repops_merkle_sha256 with the input bytes (ptr) and root_out in HOST
+ * memory (page-locked for full speed).  The call takes device memory (two
+ * chunks of whole 128-leaf groups, about 64 MiB each, and the level scratch)
+ * with cudaMallocAsync on `stream`; each chunk is copied in on a helper stream
+ * while the previous one is hashed on `stream`, the upper levels are folded
+ * once every chunk is in, and the 32-byte root is copied back to root_out;
+ * then the memory is released.  Asynchronous: read root_out once `stream` has
+ * reached this point.  The root equals repops_merkle_sha256's.  Errors as that
+ * call, plus ALLOC; ALIAS compares host ranges. */
+int repops_merkle_sha256_host(const void *ptr, uint64_t bytes, uint32_t leaf,
+                              uint8_t *root_out, cudaStream_t stream);
 
 /* Size of the fixed device scratch behind repops_merkle_sha256_noalloc. */
 #define REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES (1u << 20)

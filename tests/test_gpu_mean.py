@@ -143,3 +143,23 @@ def test_mean_sgd_special_values(rp, orc, nC):
     nan = np.isnan(want)
     assert np.array_equal(np.isnan(got), nan)
     assert np.array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+
+
+@pytest.mark.parametrize("nC,n,pinned", [(16, (1 << 23) + 3, True), (3, 1000003, False), (1, 5, True)])
+def test_host_buffer_mean_sgd_same_bits(rp, orc, nC, n, pinned):
+    # chunks of the host call are independent element ranges: the bits equal
+    # the device call's and the oracle's, pinned or pageable host memory
+    grads = [inputs.normal((n,), 1e-2, 300 + r, "cpu") for r in range(nC)]
+    theta = inputs.normal((n,), 0.02, 299, "cpu")
+    if pinned:
+        grads = [g.pin_memory() for g in grads]
+        theta = theta.pin_memory()
+    order = rp.sort_ids(inputs.contributor_ids(nC, 301))
+    want = orc.mean_sgd([g.numpy() for g in grads], order, 1e-3, theta.numpy())
+    dev = theta.to(DEV)
+    rp.fixed_order_mean_sgd([g.to(DEV) for g in grads], order, 1e-3, dev)
+    s = torch.cuda.Stream()
+    rp.fixed_order_mean_sgd_host(grads, order, 1e-3, theta, stream=s)
+    s.synchronize()
+    assert np.array_equal(theta.numpy().view(np.uint32), want.view(np.uint32))
+    assert np.array_equal(dev.cpu().numpy().view(np.uint32), want.view(np.uint32))

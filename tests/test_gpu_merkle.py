@@ -95,3 +95,20 @@ def test_sha256_rate_probe_digests(rp):
             assert struct.pack(">8I", *got[t]) == want, (iters, t)
     with pytest.raises(rp.RepopsError):
         rp.sha256_rate_probe(100, 1)
+
+
+@pytest.mark.parametrize("nbytes,leaf,pinned", [(700 * 128 * 4096 + 333, 4096, True), (77 * 4096 + 5, 4096, False),
+                                                (300 * 1024 * 1024 + 64, 64, True), (1, 4096, True)])
+def test_host_buffer_merkle_same_root(rp, orc, nbytes, leaf, pinned):
+    # chunked copies of whole 128-leaf groups, the leaf kernel per chunk, the
+    # upper levels once: the root equals the device call's and the oracle's
+    g = torch.Generator().manual_seed(nbytes % 1000)
+    t = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8)
+    if pinned:
+        t = t.pin_memory()
+    s = torch.cuda.Stream()
+    root = rp.merkle_sha256_host(t, leaf, stream=s)
+    s.synchronize()
+    assert bytes(root.numpy()) == rp.merkle_sha256(t.to(DEV), leaf).cpu().numpy().tobytes()
+    if nbytes < (1 << 30):
+        assert bytes(root.numpy()) == orc.merkle_root(t.numpy(), leaf)

@@ -36,7 +36,7 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "gemm", "gemm_chained", "gemm_auto_chained", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
@@ -348,6 +348,43 @@ def fixed_order_mean_sgd(grads, order, eta: float, theta, *, grad_dtype=None, st
                                                  theta.data_ptr(), _stream_handle(stream))
         _capi.check(rc, "repops_fixed_order_mean_sgd_typed")
     return theta
+
+
+def fixed_order_mean_sgd_host(grads, order, eta: float, theta, *, stream=None):
+    """fixed_order_mean_sgd on float32 CPU tensors (pin them for full speed):
+    the copies overlap the fold chunk by chunk (repops_fixed_order_mean_sgd_host).
+    Asynchronous on `stream`: synchronise it before reading theta."""
+    nC = len(grads)
+    for t in list(grads) + [theta]:
+        if t.is_cuda or t.dtype.itemsize != 4 or not t.is_contiguous() or t.numel() != theta.numel():
+            raise ValueError("gradients and theta must be contiguous float32 CPU tensors of one size")
+    if len(order) != nC:
+        raise ValueError("order must have one entry per contributor")
+    parr = (ctypes.c_void_p * max(nC, 1))(*[g.data_ptr() for g in grads])
+    oarr = (ctypes.c_int * max(nC, 1))(*[int(x) for x in order])
+    rc = load().repops_fixed_order_mean_sgd_host(nC, theta.numel(), ctypes.cast(parr, ctypes.c_void_p),
+                                                 ctypes.cast(oarr, ctypes.c_void_p), ctypes.c_float(eta),
+                                                 theta.data_ptr(), _stream_handle(stream))
+    _capi.check(rc, "repops_fixed_order_mean_sgd_host")
+    return theta
+
+
+def merkle_sha256_host(t, leaf: int = 4096, out=None, *, stream=None):
+    """Merkle root of a contiguous CPU tensor's bytes (pin it for full speed)
+    into `out` (a 32-byte uint8 CPU tensor, allocated if None): chunks are
+    copied in while the previous chunk is hashed (repops_merkle_sha256_host).
+    Asynchronous on `stream`: synchronise it before reading out."""
+    import torch
+    if t.is_cuda or not t.is_contiguous():
+        raise ValueError("t must be a contiguous CPU tensor")
+    if out is None:
+        out = torch.zeros(32, dtype=torch.uint8, pin_memory=t.is_pinned())
+    if out.is_cuda or out.dtype != torch.uint8 or out.numel() != 32:
+        raise ValueError("out must be a 32-byte uint8 CPU tensor")
+    rc = load().repops_merkle_sha256_host(t.data_ptr(), t.numel() * t.element_size(), leaf, out.data_ptr(),
+                                          _stream_handle(stream))
+    _capi.check(rc, "repops_merkle_sha256_host")
+    return out
 
 
 def merkle_workspace_bytes(nbytes: int, leaf: int = 4096) -> int:

@@ -43,6 +43,8 @@ SIGNATURES = {
                                        _vp, _i64, _vp]),
     "repops_attention_causal_f32": (_i32, [_i64, _i64, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _f32,
                                            _vp, _i64, _vp, _vp]),
+    "repops_fixed_order_mean_sgd_host": (_i32, [_i32, _i64, _vp, _vp, _f32, _vp, _vp]),
+    "repops_merkle_sha256_host": (_i32, [_vp, _u64, _u32, _vp, _vp]),
     "repops_gemm_config_count": (_i32, []),
     "repops_gemm_config_info": (_i32, [_i32, _vp, _vp, _vp, _vp, _vp]),
     "repops_gemm_auto_config": (_i32, [_i64, _i64, _i64]),

@@ -246,3 +246,84 @@ extern "C" int repops_fixed_order_mean_sgd_typed(int nC, int64_t len, const void
                                                  const int *order, float eta, float *theta, cudaStream_t stream) {
     return mean_sgd_typed(nC, len, ptrs, grad_type, order, eta, theta, stream);
 }
+
+extern "C" int repops_fixed_order_mean_sgd_host(int nC, int64_t len, const float *const *ptrs, const int *order,
+                                                float eta, float *theta, cudaStream_t stream) {
+    if (nC < 1 || nC > REPOPS_MEAN_MAX_CONTRIBUTORS || len < 0) return REPOPS_ERR_INVALID_ARG;
+    if (!ptrs || !order) return REPOPS_ERR_INVALID_ARG;
+    std::vector<char> seen(size_t(nC), 0);
+    for (int r = 0; r < nC; ++r) {
+        if (order[r] < 0 || order[r] >= nC || seen[size_t(order[r])]) return REPOPS_ERR_ORDER;
+        seen[size_t(order[r])] = 1;
+    }
+    if (len == 0) return REPOPS_OK;
+    if (!theta || len > INT64_MAX / 4) return REPOPS_ERR_INVALID_ARG;
+    const uint64_t bytes = uint64_t(len) * 4u;
+    for (int r = 0; r < nC; ++r) {
+        if (!ptrs[r]) return REPOPS_ERR_INVALID_ARG;
+        if (ranges_overlap(theta, bytes, ptrs[r], bytes)) return REPOPS_ERR_ALIAS;
+    }
+    // element chunks, double-buffered on the device: nC gradient slices and a
+    // theta slice per buffer, at most about 1 GiB in all
+    const int64_t cap = std::max<int64_t>(1 << 16, (int64_t(1) << 30) / (8 * int64_t(nC + 1)));
+    const int64_t ch = std::min<int64_t>(len, std::min<int64_t>(int64_t(1) << 22, cap / 4 * 4));
+    const size_t slot = size_t(ch) * 4u;
+    void *mem = nullptr;
+    if (cudaMallocAsync(&mem, 2 * size_t(nC + 1) * slot, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return REPOPS_ERR_ALLOC;
+    }
+    float *dev = static_cast<float *>(mem);
+    auto buf = [&](int b, int r) { return dev + (size_t(b) * (nC + 1) + size_t(r)) * size_t(ch); };
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t ready = nullptr, got[2] = {nullptr, nullptr}, back[2] = {nullptr, nullptr};
+    cudaError_t e = cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+        e = cudaEventCreateWithFlags(&got[b], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&back[b], cudaEventDisableTiming);
+    }
+    // the helper streams start once the allocation is ordered on `stream`
+    if (e == cudaSuccess) e = cudaEventRecord(ready, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(in, ready, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(out, ready, 0);
+    int rc = REPOPS_OK;
+    std::vector<const float *> dptr(static_cast<size_t>(nC));
+    for (int64_t c = 0, lo = 0; e == cudaSuccess && rc == REPOPS_OK && lo < len; ++c, lo += ch) {
+        const int b = int(c & 1);
+        const int64_t n = std::min<int64_t>(ch, len - lo);
+        // a buffer is refilled once its previous theta slice has gone back
+        if (c >= 2 && (e = cudaStreamWaitEvent(in, back[b], 0)) != cudaSuccess) break;
+        for (int r = 0; r < nC && e == cudaSuccess; ++r) {
+            e = cudaMemcpyAsync(buf(b, r), ptrs[r] + lo, size_t(n) * 4u, cudaMemcpyHostToDevice, in);
+            dptr[size_t(r)] = buf(b, r);
+        }
+        if (e == cudaSuccess) e = cudaMemcpyAsync(buf(b, nC), theta + lo, size_t(n) * 4u, cudaMemcpyHostToDevice, in);
+        if (e == cudaSuccess) e = cudaEventRecord(got[b], in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, got[b], 0);
+        if (e != cudaSuccess) break;
+        // elements are independent: a slice's update is the whole call's
+        rc = mean_sgd_typed(nC, n, reinterpret_cast<const void *const *>(dptr.data()), REPOPS_TYPE_F32, order, eta,
+                            buf(b, nC), stream);
+        if (rc != REPOPS_OK) break;
+        if ((e = cudaEventRecord(got[b], stream)) != cudaSuccess || (e = cudaStreamWaitEvent(out, got[b], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(theta + lo, buf(b, nC), size_t(n) * 4u, cudaMemcpyDeviceToHost, out)) != cudaSuccess ||
+            (e = cudaEventRecord(back[b], out)) != cudaSuccess)
+            break;
+    }
+    // `stream` resumes after the last copy back; then the memory is released
+    cudaEvent_t fin = nullptr;
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fin, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(fin, out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, fin, 0);
+    const cudaError_t f = cudaFreeAsync(mem, stream);
+    for (cudaEvent_t x : {ready, got[0], got[1], back[0], back[1], fin})
+        if (x) cudaEventDestroy(x);
+    if (in) cudaStreamDestroy(in);
+    if (out) cudaStreamDestroy(out);
+    if (rc != REPOPS_OK) return rc;
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (f != cudaSuccess) return set_cuda_error(f);
+    return REPOPS_OK;
+}

@@ -302,19 +302,24 @@ __device__ __forceinline__ int cta_fold(uint32_t (*buf)[8][N], int cnt, const Pi
 }
 
 __global__ void __launch_bounds__(LEAF_CTA)
+// data: the bytes of leaf `first_leaf` onwards (the whole input when 0);
+// bytes, nleaves: of the whole input; CTA b folds leaves (cta0 + b) * 128 ..
 merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t leaf, uint64_t nleaves,
                     int fast_ok, uint32_t *__restrict__ level_out, uint8_t *__restrict__ root_out,
-                    const PipeConst pc, const TreeOut to, const MerkleDbg dbg) {
+                    const PipeConst pc, const TreeOut to, const MerkleDbg dbg, uint64_t first_leaf,
+                    uint64_t cta0) {
     __shared__ uint32_t buf[2][8][LEAF_CTA];
-    const uint64_t base = uint64_t(blockIdx.x) * LEAF_CTA;
+    const uint64_t cta = cta0 + blockIdx.x;
+    const uint64_t base = cta * LEAF_CTA;
     const uint64_t i = base + threadIdx.x;
     if (i < nleaves) {
         const uint64_t start = i * leaf;
         const uint64_t len = min(uint64_t(leaf), bytes - start);
+        const uint8_t *src = data + (start - first_leaf * leaf);
         uint32_t st[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-        if (REPOPS_DBG_OK(dbg.data, data + start, uint32_t(len), dbg.status)) {
-            if (fast_ok && len == leaf) leaf_digest_fast(data + start, leaf, st, pc);
-            else leaf_digest_generic(data + start, len, st, pc);
+        if (REPOPS_DBG_OK(dbg.data, src, uint32_t(len), dbg.status)) {
+            if (fast_ok && len == leaf) leaf_digest_fast(src, leaf, st, pc);
+            else leaf_digest_generic(src, len, st, pc);
         }
 #pragma unroll
         for (int w = 0; w < 8; ++w) buf[0][w][threadIdx.x] = st[w];
@@ -328,9 +333,9 @@ merkle_leaf_subtree(const uint8_t *__restrict__ data, uint64_t bytes, uint32_t l
         for (int w = 0; w < 8; ++w) st[w] = buf[cur][w][0];
         if (root_out) {
             if (REPOPS_DBG_OK(dbg.root, root_out, 32, dbg.status)) store_root(root_out, st);
-        } else if (REPOPS_DBG_OK(dbg.ws, level_out + 8 * blockIdx.x, 32, dbg.status)) {
+        } else if (REPOPS_DBG_OK(dbg.ws, level_out + 8 * cta, 32, dbg.status)) {
 #pragma unroll
-            for (int w = 0; w < 8; ++w) level_out[8 * blockIdx.x + w] = st[w];
+            for (int w = 0; w < 8; ++w) level_out[8 * cta + w] = st[w];
         }
     }
 }
@@ -381,6 +386,8 @@ bool plan_for(uint64_t bytes, uint32_t leaf, Plan *p) {
 }
 
 uint64_t total_nodes(uint64_t nleaves);
+int reduce_levels(const Plan &pl, uint8_t *root_out, uint32_t *bufA, uint32_t *bufB, const PipeConst &pc,
+                  const TreeOut &to, const MerkleDbg &dbg, cudaStream_t stream);
 
 int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void *ws, const Plan &pl,
         cudaStream_t stream, const TreeOut to = TreeOut{nullptr, 0}) {
@@ -397,9 +404,17 @@ int run(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out, void 
     int rc = status_word_address(&dbg.status);
     if (rc != REPOPS_OK) return rc;
     merkle_leaf_subtree<<<unsigned(pl.n1), LEAF_CTA, 0, stream>>>(
-        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr, pc, to, dbg);
+        data, bytes, leaf, pl.nleaves, fast_ok, bufA, pl.n1 == 1 ? root_out : nullptr, pc, to, dbg, 0, 0);
     rc = check_launch();
     if (rc != REPOPS_OK) return rc;
+    return reduce_levels(pl, root_out, bufA, bufB, pc, to, dbg, stream);
+}
+
+// The reduce passes over the leaf kernel's level-7 nodes in bufA (bufB the
+// other half of the scratch), down to the root.
+int reduce_levels(const Plan &pl, uint8_t *root_out, uint32_t *bufA, uint32_t *bufB, const PipeConst &pc,
+                  const TreeOut &to, const MerkleDbg &dbg, cudaStream_t stream) {
+    int rc = REPOPS_OK;
     uint64_t n = pl.n1;
     int level = LOG_LEAF_CTA;
     uint32_t *src = bufA, *dst = bufB;
@@ -571,6 +586,96 @@ extern "C" uint64_t repops_merkle_tree_bytes(uint64_t bytes, uint32_t leaf) {
     Plan pl;
     if (!plan_for(bytes, leaf, &pl)) return 0;
     return 32 * total_nodes(pl.nleaves);
+}
+
+namespace repops {
+namespace {
+
+// Streams and events of one host-buffer call, destroyed (deferred by the
+// runtime until their work completes) when the call returns.
+struct HostMerkleRes {
+    cudaStream_t in = nullptr;
+    cudaEvent_t ev[4] = {};
+    ~HostMerkleRes() {
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);
+        if (in) cudaStreamDestroy(in);
+    }
+};
+
+}  // namespace
+}  // namespace repops
+
+extern "C" int repops_merkle_sha256_host(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *root_out,
+                                         cudaStream_t stream) {
+    Plan pl;
+    int rc = check_args(ptr, bytes, leaf, root_out, &pl);
+    if (rc != REPOPS_OK) return rc;
+    // chunks of whole 128-leaf CTAs, about 64 MiB each, double-buffered
+    const uint64_t cta_bytes = uint64_t(LEAF_CTA) * leaf;
+    const uint64_t per_chunk = std::max<uint64_t>(1, (uint64_t(64) << 20) / cta_bytes);
+    const uint64_t chunk_bytes = std::min<uint64_t>(per_chunk * cta_bytes, (bytes + cta_bytes - 1) / cta_bytes * cta_bytes);
+    const uint64_t nchunks = (bytes + chunk_bytes - 1) / chunk_bytes;
+    const uint64_t ws_bytes = (pl.ws_bytes + 255) / 256 * 256;
+    void *mem = nullptr;
+    if (cudaMallocAsync(&mem, ws_bytes + 2 * chunk_bytes + 256, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return REPOPS_ERR_ALLOC;
+    }
+    unsigned char *base = static_cast<unsigned char *>(mem);
+    uint32_t *bufA = pl.ws_bytes ? reinterpret_cast<uint32_t *>(base) : nullptr;
+    uint32_t *bufB = bufA ? bufA + 8 * pl.n1 : nullptr;
+    uint8_t *chunk[2] = {base + ws_bytes, base + ws_bytes + chunk_bytes};
+    uint8_t *droot = base + ws_bytes + 2 * chunk_bytes;
+    HostMerkleRes res;
+    cudaError_t e = cudaStreamCreateWithFlags(&res.in, cudaStreamNonBlocking);
+    for (int k = 0; k < 4 && e == cudaSuccess; ++k) e = cudaEventCreateWithFlags(&res.ev[k], cudaEventDisableTiming);
+    // ev[0]: the allocation is ordered; ev[1 + b]: chunk buffer b's bytes are in;
+    // ev[3]: reused per chunk for "the leaf kernel of the previous use of a
+    // buffer is done" (recorded on `stream`, waited on by `in`)
+    if (e == cudaSuccess) e = cudaEventRecord(res.ev[0], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(res.in, res.ev[0], 0);
+    const PipeConst pc{1u};
+    MerkleDbg dbg{};
+    dbg.ws = dbg_span(bufA, pl.ws_bytes);
+    dbg.root = dbg_span(droot, 32);
+    if (e == cudaSuccess) rc = status_word_address(&dbg.status);
+    cudaEvent_t done[2] = {nullptr, nullptr};
+    for (uint64_t c = 0; e == cudaSuccess && rc == REPOPS_OK && c < nchunks; ++c) {
+        const int b = int(c & 1);
+        const uint64_t off = c * chunk_bytes, cb = std::min(chunk_bytes, bytes - off);
+        if (done[b] && (e = cudaStreamWaitEvent(res.in, done[b], 0)) != cudaSuccess) break;
+        if ((e = cudaMemcpyAsync(chunk[b], static_cast<const uint8_t *>(ptr) + off, cb, cudaMemcpyHostToDevice,
+                                 res.in)) != cudaSuccess ||
+            (e = cudaEventRecord(res.ev[1 + b], res.in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, res.ev[1 + b], 0)) != cudaSuccess)
+            break;
+        const uint64_t first_leaf = off / leaf, leaves = (cb + leaf - 1) / leaf;
+        const uint64_t ctas = (leaves + LEAF_CTA - 1) / LEAF_CTA;
+        dbg.data = dbg_span(chunk[b], cb);
+        merkle_leaf_subtree<<<unsigned(ctas), LEAF_CTA, 0, stream>>>(
+            chunk[b], bytes, leaf, pl.nleaves, 1, bufA, pl.n1 == 1 ? droot : nullptr, pc, TreeOut{nullptr, 0}, dbg,
+            first_leaf, off / cta_bytes);
+        rc = check_launch();
+        if (rc != REPOPS_OK) break;
+        // the buffer is free again once this leaf kernel is done
+        cudaEvent_t ev = nullptr;
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) break;
+        e = cudaEventRecord(ev, stream);
+        if (done[b]) cudaEventDestroy(done[b]);
+        done[b] = ev;
+    }
+    for (cudaEvent_t d : done)
+        if (d) cudaEventDestroy(d);
+    if (rc == REPOPS_OK && e == cudaSuccess && pl.n1 > 1)
+        rc = reduce_levels(pl, droot, bufA, bufB, pc, TreeOut{nullptr, 0}, dbg, stream);
+    if (rc == REPOPS_OK && e == cudaSuccess)
+        e = cudaMemcpyAsync(root_out, droot, 32, cudaMemcpyDeviceToHost, stream);
+    const cudaError_t f = cudaFreeAsync(mem, stream);
+    if (rc != REPOPS_OK) return rc;
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (f != cudaSuccess) return set_cuda_error(f);
+    return REPOPS_OK;
 }
 
 extern "C" int repops_merkle_tree_sha256(const void *ptr, uint64_t bytes, uint32_t leaf, uint8_t *tree,
