@@ -45,7 +45,7 @@ def test_manifest_names_arithmetic_flags(L):
 
 
 def test_status_strings(L):
-    for code in range(-7, 1):
+    for code in range(-8, 1):
         assert L.repops_status_string(code).decode() != "unknown status"
 
 
@@ -348,3 +348,38 @@ def test_llama_operators_reject_bad_arguments(L):
 def test_selftest_rejects_bad_limits(L):
     assert L.repops_selftest_bounded_wait(0, None) == -1
     assert L.repops_selftest_bounded_wait(3_000_000_000, None) == -1
+
+
+def test_added_entry_points_reject_bad_arguments(L):
+    # the chained k-split: a negative worker count; the usual GEMM checks first
+    assert L.repops_gemm_f32_chained(0, -1, 0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert L.repops_gemm_f32_chained(0, 2, 0, 0, 4, 4, 4, FAKE_A, 3, FAKE_B, 4, FAKE_C, 4, None) == -1
+    assert L.repops_gemm_f32_chained(0, 2, 0, 0, 4, 4, 4, FAKE_A, 4, FAKE_B, 4, FAKE_A + 32, 4, None) == -2
+    # fused attention: heads not a multiple of kv heads, short leading dims,
+    # null pointers, nothing to do
+    att = L.repops_attention_causal_f32
+    assert att(1, 32, 3, 2, 64, FAKE_A, 256, FAKE_B, 256, FAKE_C, 256, 0.125, FAKE_C + (1 << 20), 256,
+               None, None) == -1
+    assert att(1, 32, 4, 2, 64, FAKE_A, 100, FAKE_B, 256, FAKE_C, 256, 0.125, FAKE_C + (1 << 20), 256,
+               None, None) == -1
+    assert att(1, 32, 4, 2, 64, None, 256, FAKE_B, 256, FAKE_C, 256, 0.125, FAKE_C + (1 << 20), 256,
+               None, None) == -1
+    assert att(0, 32, 4, 2, 64, None, 0, None, 0, None, 0, 0.125, None, 0, None, None) == 0
+    assert att(1, 32, 4, -1, 64, FAKE_A, 256, FAKE_B, 256, FAKE_C, 256, 0.125, FAKE_C, 256, None, None) == -1
+    # the per-thread status word must be 4-byte aligned; null restores the shared one
+    assert L.repops_set_thread_status_word(FAKE_A + 2) == -1
+    assert L.repops_set_thread_status_word(None) == 0
+    # host-buffer mean + SGD: counts, orders, aliasing host ranges
+    import ctypes as C
+    ptrs = (C.c_void_p * 2)(FAKE_A, FAKE_B)
+    order_ok = (C.c_int * 2)(1, 0)
+    order_dup = (C.c_int * 2)(0, 0)
+    mh = L.repops_fixed_order_mean_sgd_host
+    assert mh(0, 8, C.cast(ptrs, C.c_void_p), C.cast(order_ok, C.c_void_p), C.c_float(1e-3), FAKE_C, None) == -1
+    assert mh(2, 8, C.cast(ptrs, C.c_void_p), C.cast(order_dup, C.c_void_p), C.c_float(1e-3), FAKE_C, None) == -3
+    assert mh(2, 8, C.cast(ptrs, C.c_void_p), C.cast(order_ok, C.c_void_p), C.c_float(1e-3), FAKE_A + 4,
+              None) == -2
+    # host-buffer Merkle: empty input, bad leaf, the root over the input
+    assert L.repops_merkle_sha256_host(FAKE_A, 0, 4096, FAKE_C, None) == -1
+    assert L.repops_merkle_sha256_host(FAKE_A, 100, 100, FAKE_C, None) == -1
+    assert L.repops_merkle_sha256_host(FAKE_A, 100, 4096, FAKE_A + 8, None) == -2
