@@ -58,8 +58,8 @@ HBM_SPEC_GBS = 7900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
 # the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "e6247199581a86e5d79ee7be7daed103da588360ad93caf68bb53c1f9221c4ed",
-                "bytes_per_launch": 3645192192 + 265768960}
+GEMM_TRAFFIC = {"src_sha256": "64c3360a81a253776f745fb9fc383e3be043e6f6bed1b1d59c2aab3cd254ffd0",
+                "bytes_per_launch": 3738461696 + 265764096}
 
 
 def measured_peaks():
