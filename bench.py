@@ -1141,6 +1141,34 @@ def run_gemm_once(spec):
                       "chained": rp.gemm_auto_chained(M, N, K), "ms": e0.elapsed_time(e1)}), flush=True)
 
 
+def run_attention_once():
+    """The unfused attention of one 2048-token sequence of the decoder layer
+    (32 query / 8 key-value heads of 64): the scores QK^T with alpha 1/8 and
+    the causal tile skip, the causal softmax, and P V over the band k <= i,
+    three times: for profiling those kernels in isolation."""
+    from verifiable_repops_gemm_gb300 import decoder
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rp.load()
+    cfg = decoder.DecoderConfig()
+    S, dh, kv, H = cfg.seq_len, cfg.d_head, cfg.kv_heads, cfg.heads
+    qkv = inputs.normal((S, cfg.qkv_width), 1.0, 1, dev)
+    k0, v0 = cfg.d, cfg.d + kv * dh
+    sc = torch.empty((H, S, S), device=dev)
+    out = torch.empty((S, cfg.d), device=dev)
+    rows = slice(0, S)
+    Q, K = decoder._heads(qkv, rows, 0, H, dh), decoder._kv(qkv, rows, k0, kv, dh)
+    V, O = decoder._kv(qkv, rows, v0, kv, dh), decoder._heads(out, rows, 0, H, dh)
+    for _ in range(3):
+        rp.gemm_batched(Q, K.transpose(1, 2), out=sc, alpha=1.0 / 8.0, causal_first=0)
+        rp.softmax_rows(sc.view(H * S, S), out=sc.view(H * S, S), causal_first=0, causal_period=S)
+        rp.gemm_batched(sc, V, out=O, k_hi=0)
+    torch.cuda.synchronize(dev)
+    if rp.device_status() != 0:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    print(json.dumps({"attention_once": "ok"}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1155,8 +1183,12 @@ def main():
                     help="time every workload of a part (one JSON line each) instead of the step")
     ap.add_argument("--gemm-once", metavar="M,N,K", default=None,
                     help="three launches of one automatic-choice GEMM (for a profiler)")
+    ap.add_argument("--attention-once", action="store_true",
+                    help="three passes of one sequence's unfused attention kernels (for a profiler)")
     args = ap.parse_args()
-    if args.gemm_once:
+    if args.attention_once:
+        run_attention_once()
+    elif args.gemm_once:
         run_gemm_once(args.gemm_once)
     elif args.sweep:
         run_sweep(args)
