@@ -504,6 +504,22 @@ struct SkArgs {
     unsigned *flags;     // [workers][THREADS], zero before the launch
 };
 
+// The schedule of `tiles` tiles of kt k-slices over `workers` workers
+// (workers <= tiles): whole waves while more than one wave of tiles is left,
+// then the rest split by k-slices.  Host and device agree on it through
+// SkPlan below; a host test checks its invariants.
+inline void sk_schedule(int64_t tiles, int kt, int workers, SkArgs &sk) {
+    sk.kt = kt;
+    if (tiles % workers == 0) {
+        sk.waves = int(tiles / workers);
+        sk.sk_tiles = 0;
+    } else {
+        sk.waves = int(tiles / workers) - 1;
+        sk.sk_tiles = tiles - int64_t(sk.waves) * workers;
+    }
+    sk.dp_tiles = int64_t(sk.waves) * workers;
+}
+
 // One piece of a worker's schedule.  kind 0: slices [kb, ke) from +0, then
 // store the accumulators for the next worker (a head); 1: a whole tile; 2:
 // load the previous worker's accumulators, slices [kb, ke), store C (a tail).
@@ -522,7 +538,7 @@ struct SkPlan {
     int64_t full_first, nfull;
     int nseg;
 
-    __device__ __forceinline__ SkPlan(const SkArgs &sk, int w_, int workers_) {
+    __host__ __device__ __forceinline__ SkPlan(const SkArgs &sk, int w_, int workers_) {
         waves = sk.waves;
         w = w_;
         workers = workers_;
@@ -554,7 +570,7 @@ struct SkPlan {
 
     // Segment s in execution order: whole waves, the head, whole split-part
     // tiles, the tail.
-    __device__ __forceinline__ SkSeg seg(int s) const {
+    __host__ __device__ __forceinline__ SkSeg seg(int s) const {
         SkSeg g;
         if (s < waves) {
             g.tile = int64_t(s) * workers + w; g.kb = 0; g.ke = kt; g.kind = 1;
@@ -972,15 +988,7 @@ int launch_tma_sk(const GemmProblem &p, int tiles_m, int tiles_n, int c_vec) {
     const int workers = p.sk_workers;
     if (workers < 1 || workers > int64_t(per_sm) * sms || workers > tiles) return REPOPS_ERR_UNSUPPORTED;
     SkArgs sk{};
-    sk.kt = int((p.K + BK - 1) / BK);
-    if (tiles % workers == 0) {
-        sk.waves = int(tiles / workers);
-        sk.sk_tiles = 0;
-    } else {
-        sk.waves = int(tiles / workers) - 1;
-        sk.sk_tiles = tiles - int64_t(sk.waves) * workers;
-    }
-    sk.dp_tiles = int64_t(sk.waves) * workers;
+    sk_schedule(tiles, int((p.K + BK - 1) / BK), workers, sk);
     sk.partial = static_cast<u64 *>(p.sk_scratch);
     sk.flags = reinterpret_cast<unsigned *>(static_cast<unsigned char *>(p.sk_scratch) +
                                             sk_partial_bytes<T>(workers));
