@@ -58,8 +58,8 @@ HBM_SPEC_GBS = 7900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
 # the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "64c3360a81a253776f745fb9fc383e3be043e6f6bed1b1d59c2aab3cd254ffd0",
-                "bytes_per_launch": 3738461696 + 265764096}
+GEMM_TRAFFIC = {"src_sha256": "0618417c046709d7083f63c493debdd10f14a7ade4fc940a7a40feaf6eb746e1",
+                "bytes_per_launch": 3754447616 + 265766400}
 
 
 def measured_peaks():
