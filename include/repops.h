@@ -29,9 +29,10 @@
  *     a call that returns an error launched nothing.
  *   - The library never takes ownership of a buffer.  It keeps no per-call
  *     state between calls, except the sticky device status word of the
- *     bounded waits: by default one word per device shared by every caller,
+ *     bounded waits (by default one word per device shared by every caller,
  *     or a word the caller owns, bound per host thread with
- *     repops_set_thread_status_word().
+ *     repops_set_thread_status_word()) and the freed memory its scratch pool
+ *     keeps mapped (see "Scratch memory" below).
  *   - Floating point is IEEE-754 binary32, round-to-nearest-even, subnormals
  *     kept (no flush-to-zero), no fused multiply-add, no tensor cores.
  *   - NaN results compare equal as a class (payload bits are not pinned);
@@ -111,6 +112,25 @@ int repops_set_thread_status_word(unsigned *word);
  * the GPU context stays usable.  Nothing else is read or written. */
 int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
 
+/* Scratch memory.  Entry points that need device scratch (operand copies and
+ * chained-split partial sums of the GEMM, Merkle level nodes, the staging
+ * buffers of the host-buffer calls, ...) allocate it stream-ordered, on the
+ * caller's stream, from a memory pool the library creates for each device
+ * (one per CUDA context; the device's default pool is neither used nor
+ * changed).  Freed memory stays mapped in that pool, up to 2 GiB, across
+ * synchronisations, so a call made after a synchronisation does not map its
+ * scratch again.  Thread-safe.
+ *
+ * repops_scratch_release: hands back to the system the memory of the current
+ * device's pool that no allocation holds (scratch of calls still in flight,
+ * whose frees have not run on their streams yet, stays).  REPOPS_OK, or
+ * REPOPS_ERR_CUDA.
+ * repops_scratch_reserved_bytes: *bytes_out = device memory the current
+ * device's pool holds mapped now (0 before its first allocation).
+ * REPOPS_ERR_INVALID_ARG for a null bytes_out. */
+int repops_scratch_release(void);
+int repops_scratch_reserved_bytes(uint64_t *bytes_out);
+
 /* ------------------------------------------------------------------------ */
 /* Order-fixed FP32 GEMM                                                     */
 /* "Verde与RepOps" §3.2, matmul example; §3.1; §3.3                          */
@@ -136,7 +156,7 @@ int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
  * Pointers need no alignment.  An operand TMA cannot describe (base not
  * 16-byte aligned, or leading dimension not a multiple of 4) is, for problems
  * of at least 4 GFLOP (2*M*N*K), first copied with a 16-byte pitch into
- * scratch taken with cudaMallocAsync on `stream` (and released the same way);
+ * scratch taken from the library's scratch pool on `stream` (and released there);
  * smaller problems, or a refused allocation, read it with 4-byte copies.  The
  * bits are the same on every path. */
 int repops_gemm_f32(int64_t M, int64_t N, int64_t K,
@@ -150,7 +170,11 @@ int repops_gemm_f32(int64_t M, int64_t N, int64_t K,
  *   transA != 0: A[i][k] at A[k*lda + i], lda >= max(1, M)   (dW = X^T dY)
  *   transB == 0: B[k][j] at B[k*ldb + j], ldb >= max(1, N)
  *   transB != 0: B[k][j] at B[j*ldb + k], ldb >= max(1, K)   (dX = dY W^T)
- * The result bits do not depend on transA/transB, only on the element values. */
+ * The result bits do not depend on transA/transB, only on the element values.
+ * Where it is faster, operands are first copied into the kernels' fastest
+ * layouts in scratch from the scratch pool on `stream`: a transposed B into
+ * row-major from 1 GFLOP (2*M*N*K) on, a row-major A into the transposed
+ * layout from 4 GFLOP on.  A refused allocation keeps the caller's layout. */
 int repops_gemm_f32_ex(int transA, int transB,
                        int64_t M, int64_t N, int64_t K,
                        const float *A, int64_t lda,
@@ -160,7 +184,7 @@ int repops_gemm_f32_ex(int transA, int transB,
 
 /* As repops_gemm_f32 with A, B and C in HOST memory (row-major, pitches as
  * there; page-locked memory for full speed).  The call takes device memory
- * for A, B and C (16-byte pitches) with cudaMallocAsync on `stream`, copies B,
+ * for A, B and C (16-byte pitches) from the scratch pool on `stream`, copies B,
  * then copies A in row blocks on a helper stream while the previous block's
  * GEMM runs on `stream`, copies each block of C back on a second helper stream
  * as it completes, and releases the memory; everything is ordered before work
@@ -217,7 +241,7 @@ int repops_gemm_f32_config(int config, int loader, int transA, int transB,
  * separately computed partial sums would not be).  ("Verde与RepOps" §3.2: the
  * order-critical dimension stays serial; only who computes which part of a
  * chain changes.)  Scratch (about workers x 32 KB) is taken with
- * cudaMallocAsync on `stream`; the kernel is launched cooperatively and every
+ * from the scratch pool on `stream`; the kernel is launched cooperatively and every
  * wait between workers is bounded (status word).  UNSUPPORTED when the
  * operands do not meet the TMA rule, `workers` is too large, or the scratch is
  * refused; INVALID_ARG for workers < 0; other errors as repops_gemm_f32. */
@@ -375,7 +399,7 @@ int repops_fixed_order_mean_sgd(int nC, int64_t len, const float *const *ptrs,
  * (page-locked for full speed): ptrs (host) holds nC host pointers of len
  * floats each, theta (host, len floats) is updated in place.  The call takes
  * device memory for two element chunks (up to 2^22 elements, at most about
- * 1 GiB in all) with cudaMallocAsync on `stream`, copies each chunk of every
+ * 1 GiB in all) from the scratch pool on `stream`, copies each chunk of every
  * gradient and of theta in on a helper stream while the previous chunk is
  * folded on `stream`, copies theta's chunk back on a second helper stream, and
  * releases the memory; everything is ordered before work later enqueued on
@@ -417,7 +441,7 @@ int repops_fixed_order_mean_sgd_typed(int nC, int64_t len, const void *const *pt
  * leaf <= 2^30.  root_out (device): receives the 32-byte root, written
  * asynchronously on `stream`.
  * Scratch of repops_merkle_workspace_bytes(bytes, leaf) bytes is taken with
- * cudaMallocAsync on `stream` and released with cudaFreeAsync on the same
+ * from the scratch pool on `stream` and released with cudaFreeAsync on the same
  * stream.  Errors: INVALID_ARG (null pointer, bytes == 0, bad leaf); ALIAS
  * (root_out inside the input); ALLOC; CUDA. */
 int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t leaf,
@@ -557,7 +581,7 @@ int repops_gelu_f32(int64_t n, const float *x, float *y, cudaStream_t stream);
  * ints, each step's row a permutation), etas (host, steps floats), theta
  * (device, updated in place), roots_out (device, 32*steps bytes).  Every step
  * is validated before the first launch (ORDER, ALIAS, INVALID_ARG as the two
- * calls it makes).  Merkle scratch comes from cudaMallocAsync on `stream`. */
+ * calls it makes).  Merkle scratch comes from the scratch pool on `stream`. */
 int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len,
                                   const float *const *ptrs, const int *orders,
                                   const float *etas, float *theta, uint32_t leaf,
@@ -582,7 +606,7 @@ int repops_sha256_rate_probe(uint32_t threads, uint32_t iters, uint32_t *digests
 /* As repops_merkle_sha256 with the input bytes (ptr) and root_out in HOST
  * memory (page-locked for full speed).  The call takes device memory (two
  * chunks of whole 128-leaf groups, about 64 MiB each, and the level scratch)
- * with cudaMallocAsync on `stream`; each chunk is copied in on a helper stream
+ * from the scratch pool on `stream`; each chunk is copied in on a helper stream
  * while the previous one is hashed on `stream`, the upper levels are folded
  * once every chunk is in, and the 32-byte root is copied back to root_out;
  * then the memory is released.  Asynchronous: read root_out once `stream` has
@@ -597,7 +621,7 @@ int repops_merkle_sha256_host(const void *ptr, uint64_t bytes, uint32_t leaf,
 /* The paper has no counterpart to this entry point; it is a deployment aid.
  *
  * As repops_merkle_sha256, but it allocates nothing: no cudaMalloc, no
- * cudaMallocAsync, no caller workspace.  It is meant for callers that cannot
+ * stream-ordered scratch, no caller workspace.  It is meant for callers that cannot
  * allocate device memory when they hash -- a host framework that has reserved
  * all device memory for its own pool, a latency-critical path on which an
  * allocation could block or synchronise, a plug-in whose host forbids
@@ -635,7 +659,7 @@ int repops_merkle_sha256_noalloc(const void *ptr, uint64_t bytes, uint32_t leaf,
 /* y[j] = tree sum over i = 0 .. rows-1 of x[i*ldx + j] (the column's values in
  * row order, folded by the 32-ary tree): bias and gain gradients.  rows == 0
  * gives +0.  Scratch for the tree's middle levels (about rows/31 * cols
- * floats) is taken with cudaMallocAsync on `stream` (ALLOC when refused).
+ * floats) is taken from the scratch pool on `stream` (ALLOC when refused).
  * y (device, cols floats) must not overlap x (ALIAS). */
 int repops_colsum_f32(int64_t rows, int64_t cols, const float *x, int64_t ldx, float *y,
                       cudaStream_t stream);
@@ -746,7 +770,7 @@ int repops_convert(int64_t n, const void *src, int src_type, void *dst, int dst_
  * operands are widened exactly to binary32, the order-fixed k-chain runs, and
  * the result is narrowed once to typeC.  The bits equal repops_gemm_f32 on the
  * widened operands, narrowed.  Half operands are widened into scratch taken
- * with cudaMallocAsync on `stream` (4 bytes per element of each widened
+ * from the scratch pool on `stream` (4 bytes per element of each widened
  * operand, and of C when typeC is a half type), released the same way; ALLOC
  * when it cannot be had.  INVALID_ARG for unknown types, and as
  * repops_gemm_f32_ex otherwise; ALIAS when C's bytes overlap A's or B's. */

@@ -369,6 +369,8 @@ def test_added_entry_points_reject_bad_arguments(L):
     # the per-thread status word must be 4-byte aligned; null restores the shared one
     assert L.repops_set_thread_status_word(FAKE_A + 2) == -1
     assert L.repops_set_thread_status_word(None) == 0
+    # the scratch pool's size query needs somewhere to write
+    assert L.repops_scratch_reserved_bytes(None) == -1
     # host-buffer mean + SGD: counts, orders, aliasing host ranges
     import ctypes as C
     ptrs = (C.c_void_p * 2)(FAKE_A, FAKE_B)

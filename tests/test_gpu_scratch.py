@@ -1,0 +1,84 @@
+"""GPU tests of the library's scratch pool (repops_scratch_release,
+repops_scratch_reserved_bytes; "Scratch memory" in include/repops.h).
+
+Scratch taken by one call stays mapped after a synchronisation, so the next
+call does not map it again; a release hands it back; the device's default
+pool is neither used nor changed; and the bits are the oracle's before and
+after a release.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle_par
+from verifiable_repops_gemm_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+def default_pool_release_threshold() -> int:
+    cu = ctypes.CDLL("libcuda.so.1")
+    d = ctypes.c_int()
+    assert cu.cuDeviceGet(ctypes.byref(d), torch.cuda.current_device()) == 0
+    pool = ctypes.c_void_p()
+    assert cu.cuDeviceGetDefaultMemPool(ctypes.byref(pool), d) == 0
+    v = ctypes.c_uint64()
+    assert cu.cuMemPoolGetAttribute(pool, 4, ctypes.byref(v)) == 0   # release threshold
+    return v.value
+
+
+def bits(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def test_scratch_stays_mapped_until_released(rp, orc):
+    # 1000 x 1001 x 520 with B stored transposed (1.04 GFLOP): B is copied
+    # into a row-major scratch copy before the kernel runs
+    A = inputs.normal((1000, 520), 1.0, 41, DEV)
+    B = inputs.normal((1001, 520), 1.0, 42, DEV).t()
+    want = oracle_par.gemm(orc, A, B).view(np.uint32)
+    threshold = default_pool_release_threshold()
+    C1 = rp.gemm(A, B)
+    torch.cuda.synchronize()
+    assert rp.scratch_reserved_bytes() >= 1001 * 520 * 4
+    C2 = rp.gemm(A, B)
+    torch.cuda.synchronize()
+    rp.scratch_release()
+    torch.cuda.synchronize()
+    assert rp.scratch_reserved_bytes() == 0
+    C3 = rp.gemm(A, B)
+    torch.cuda.synchronize()
+    for C in (C1, C2, C3):
+        assert np.array_equal(bits(C), want)
+    assert default_pool_release_threshold() == threshold
+    assert rp.device_status() == 0
+
+
+def test_scratch_shared_by_streams_and_entry_points(rp, orc):
+    # a chained-split GEMM, a Merkle root and a transposed-B GEMM on two
+    # streams, over and over, with releases in between: every result the
+    # oracle's
+    A = inputs.normal((2048, 2048), 1.0, 43, DEV)
+    B = inputs.normal((2048, 2048), 1.0, 44, DEV)
+    T = inputs.normal((1 << 20,), 0.02, 45, DEV)
+    rows = list(range(0, 2048, 97))
+    want_rows = oracle_par.gemm(orc, A, B, rows=rows)
+    want_root = orc.merkle_root(T.cpu().numpy(), 4096)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for it in range(4):
+        with torch.cuda.stream(s1):
+            C = rp.gemm(A, B)
+        with torch.cuda.stream(s2):
+            C2 = rp.gemm(A, B.t().contiguous().t())
+            root = rp.merkle_sha256(T)
+        torch.cuda.synchronize()
+        for X in (C, C2):
+            assert np.array_equal(X[rows].cpu().numpy().view(np.uint32), want_rows.view(np.uint32)), it
+        assert bytes(root.cpu().numpy()) == want_root, it
+        if it % 2:
+            rp.scratch_release()
+    assert rp.device_status() == 0

@@ -423,6 +423,20 @@ def device_status(stream=None) -> int:
     return v.value
 
 
+def scratch_release() -> None:
+    """Hands the current device's unused scratch-pool memory back to the system
+    (repops_scratch_release)."""
+    _capi.check(load().repops_scratch_release(), "repops_scratch_release")
+
+
+def scratch_reserved_bytes() -> int:
+    """Device memory the library's scratch pool of the current device holds
+    mapped (repops_scratch_reserved_bytes)."""
+    v = ctypes.c_uint64(0)
+    _capi.check(load().repops_scratch_reserved_bytes(ctypes.byref(v)), "repops_scratch_reserved_bytes")
+    return v.value
+
+
 def set_thread_status_word(word=None) -> None:
     """Binds a caller-owned device status word (a 1-element int32/uint32 CUDA
     tensor, or None for the library's shared word) to this host thread's

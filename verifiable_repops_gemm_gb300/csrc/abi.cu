@@ -92,6 +92,66 @@ int current_context_key(uint64_t *key) {
     return REPOPS_OK;
 }
 
+namespace {
+// The scratch pool of each device, created in the CUDA context current at
+// the first allocation and again when that context changes (after
+// cudaDeviceReset the old handle is gone with its context).  A device's
+// default pool returns its free memory to the system at every
+// synchronisation (release threshold 0), so each call made after one paid
+// ~120 us of host time mapping its scratch again, with the GPU idle if
+// nothing else was queued: measured on a GB300, a 1536^3 GEMM 318 -> 242 us
+// and a 2048^3 one 598 -> 522 us a call, synchronised after each.
+struct ScratchPool {
+    std::mutex mu;
+    uint64_t ctx_key = 0;
+    cudaMemPool_t pool = nullptr;
+};
+ScratchPool g_scratch_pool[kMaxDevices];
+
+// The current device's pool; *pool stays null when there is no pool to use.
+int scratch_pool(cudaMemPool_t *pool) {
+    *pool = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev < 0 || dev >= kMaxDevices) return REPOPS_ERR_UNSUPPORTED;
+    uint64_t key = 0;
+    int rc = current_context_key(&key);
+    if (rc != REPOPS_OK) return rc;
+    ScratchPool &s = g_scratch_pool[dev];
+    std::lock_guard<std::mutex> lock(s.mu);
+    if (s.ctx_key != key || !s.pool) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof props);
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if ((e = cudaMemPoolCreate(&p, &props)) != cudaSuccess) return set_cuda_error(e);
+        uint64_t keep = kScratchKeepBytes;
+        if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+            cudaMemPoolDestroy(p);
+            return set_cuda_error(e);
+        }
+        s.pool = p;
+        s.ctx_key = key;
+    }
+    *pool = s.pool;
+    return REPOPS_OK;
+}
+}  // namespace
+
+cudaError_t scratch_malloc(void **ptr, size_t bytes, cudaStream_t stream) {
+    cudaMemPool_t pool = nullptr;
+    if (scratch_pool(&pool) != REPOPS_OK || !pool) {
+        // no pool of our own (it could not be created): the device's default one
+        cudaGetLastError();
+        return cudaMallocAsync(ptr, bytes, stream);
+    }
+    return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
 }  // namespace repops
 
 using namespace repops;
@@ -127,6 +187,26 @@ extern "C" int repops_device_status(cudaStream_t stream, int *status_out) {
     int rc = gemm_read_and_clear_device_status(stream, &v);
     if (rc != REPOPS_OK) return rc;
     *status_out = (v & 2u) ? REPOPS_ERR_BOUNDS : v ? REPOPS_ERR_TIMEOUT : REPOPS_OK;
+    return REPOPS_OK;
+}
+
+extern "C" int repops_scratch_release(void) {
+    cudaMemPool_t pool = nullptr;
+    int rc = scratch_pool(&pool);
+    if (rc != REPOPS_OK) return rc;
+    const cudaError_t e = cudaMemPoolTrimTo(pool, 0);
+    return e == cudaSuccess ? REPOPS_OK : set_cuda_error(e);
+}
+
+extern "C" int repops_scratch_reserved_bytes(uint64_t *bytes_out) {
+    if (!bytes_out) return REPOPS_ERR_INVALID_ARG;
+    cudaMemPool_t pool = nullptr;
+    int rc = scratch_pool(&pool);
+    if (rc != REPOPS_OK) return rc;
+    cuuint64_t v = 0;
+    const cudaError_t e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &v);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    *bytes_out = uint64_t(v);
     return REPOPS_OK;
 }
 

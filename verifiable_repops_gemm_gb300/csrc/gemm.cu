@@ -289,8 +289,15 @@ int launch_transpose(const float *src, int64_t lds, int64_t rows, int64_t cols, 
 
 // Work (2*M*N*K) from which repacking TMA-incompatible operands pays off: the
 // copy streams each operand once (~10-20 us for the ragged 4097x1023x3001
-// workload) and lets the TMA kernels run instead of the 4-byte loader.
+// workload) and lets the TMA kernels run instead of the 4-byte loader.  The
+// same bound holds for transposing a row-major A into the M-inner layout.
 constexpr double kRepackMinFlops = 4.0e9;
+// A B stored transposed (K-inner) is transposed from 1 GFLOP on: measured on
+// a GB300 (L2 flushed, synchronised after each call), 1024^3 20.4 -> 21.7,
+// 1024 x 1024 x 1536 21.2 -> 23.3 and 2048 x 1024 x 512 21.2 -> 22.9 TFLOP/s;
+// 768^3 (0.9 GFLOP) 18.2 -> 17.5, slower.  Transposing A pays only from
+// kRepackMinFlops: at 1024^3 it measured 23.1 -> 22.9.
+constexpr double kTransposeBMinFlops = 1.0e9;
 
 bool operand_tma_ready(const float *ptr, int64_t ld) {
     return reinterpret_cast<uintptr_t>(ptr) % 16 == 0 && ld % 4 == 0;
@@ -314,7 +321,7 @@ int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool 
     const int64_t outer = transpose ? cols : rows, inner = transpose ? rows : cols;
     const int64_t pm = (inner + 3) / 4 * 4;
     *out = nullptr;
-    if (cudaMallocAsync(out, size_t(outer) * size_t(pm) * 4u, stream) != cudaSuccess) {
+    if (scratch_malloc(out, size_t(outer) * size_t(pm) * 4u, stream) != cudaSuccess) {
         cudaGetLastError();   // a refused allocation is not an error here
         *out = nullptr;
         return REPOPS_OK;
@@ -364,7 +371,7 @@ int launch_chained_split(GemmProblem p, int cfg, int workers) {
     const size_t bytes = kSkScratch[cfg](workers);
     const size_t flag_bytes = size_t(workers) * size_t(ci.threads) * 4u;
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, bytes, p.stream) != cudaSuccess) {
+    if (scratch_malloc(&scratch, bytes, p.stream) != cudaSuccess) {
         cudaGetLastError();
         return REPOPS_ERR_UNSUPPORTED;
     }
@@ -435,11 +442,12 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     bool tma_ok = gemm_tma_eligible(p);
     if ((loader == REPOPS_LOADER_TMA || sk_explicit) && !tma_ok) return REPOPS_ERR_UNSUPPORTED;
 
-    // Large problems (>= 4 GFLOP, automatic loader) run on stream-ordered
-    // scratch copies where that is faster; the kernels then compute the same
-    // products and sums in the same order, so the bits do not change:
+    // Large problems (automatic loader) run on stream-ordered scratch copies
+    // where that is faster; the kernels then compute the same products and
+    // sums in the same order, so the bits do not change:
     //  - B stored transposed (K-inner, the slowest layout: 0.78 of the FP32
-    //    pipe at 8192^3) is transposed into a row-major B with a 16-byte pitch;
+    //    pipe at 8192^3) is transposed into a row-major B with a 16-byte pitch
+    //    (from 1 GFLOP; the other copies from 4 GFLOP);
     //  - A stored row-major (K-inner) is transposed into an M-inner A: those
     //    kernels (products paired along m) run 3% faster at 8192^3 (35.1
     //    against 34.0 TFLOP/s);
@@ -448,14 +456,16 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     //    pitch, so that the TMA kernels run instead of the 4-byte loader.
     // Each copy streams its operand once (~0.1 ms for 8192^2).  Without the
     // scratch (a refused allocation) the caller's operands are used as they are.
-    const bool large = loader == REPOPS_LOADER_AUTO && 2.0 * double(M) * double(N) * double(K) >= kRepackMinFlops;
+    const double flops = 2.0 * double(M) * double(N) * double(K);
+    const bool large = loader == REPOPS_LOADER_AUTO && flops >= kRepackMinFlops;
+    const bool transpose_b = loader == REPOPS_LOADER_AUTO && p.transB && flops >= kTransposeBMinFlops;
     void *bscratch = nullptr, *ascratch = nullptr;
     auto fail = [&](int code) {
         for (void *m : {bscratch, ascratch})
             if (m) cudaFreeAsync(m, stream);
         return code;
     };
-    if (large && (p.transB || !operand_tma_ready(p.B, p.ldb))) {
+    if (transpose_b || (large && !operand_tma_ready(p.B, p.ldb))) {
         // B stored transposed (N x K) is transposed, an unaligned row-major B repacked
         int64_t pitch = 0;
         rc = p.transB ? copy_operand(B, ldb, N, K, true, stream, &bscratch, &pitch)
@@ -771,7 +781,7 @@ extern "C" int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&res.out, cudaStreamNonBlocking);
     if (e != cudaSuccess) return set_cuda_error(e);
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, bytesA + bytesB + bytesC, stream) != cudaSuccess) {
+    if (scratch_malloc(&mem, bytesA + bytesB + bytesC, stream) != cudaSuccess) {
         cudaGetLastError();
         return REPOPS_ERR_ALLOC;
     }

@@ -298,7 +298,7 @@ extern "C" int repops_gemm_typed(int config, int loader, int transA, int transB,
     const uint64_t na = wa ? uint64_t(a_rows) * pa : 0, nb = wb ? uint64_t(b_rows) * pb : 0;
     const uint64_t nc = wc ? uint64_t(M) * pc : 0;
     void *scratch = nullptr;
-    if (cudaMallocAsync(&scratch, (na + nb + nc) * 4u, stream) != cudaSuccess) {
+    if (scratch_malloc(&scratch, (na + nb + nc) * 4u, stream) != cudaSuccess) {
         cudaGetLastError();
         return REPOPS_ERR_ALLOC;
     }

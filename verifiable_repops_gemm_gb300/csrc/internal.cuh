@@ -53,6 +53,14 @@ int current_context_key(uint64_t *key);
 // into (its bound word, else the device's shared one).
 int status_word_address(unsigned **out);
 
+// Stream-ordered scratch for the entry points: `bytes` on `stream` from the
+// library's own memory pool of the current device (one per device and CUDA
+// context), which keeps up to kScratchKeepBytes mapped across synchronisations.
+// Freed with cudaFreeAsync like any stream-ordered allocation.  Returns the
+// CUDA error of the allocation (cudaSuccess, or e.g. out of memory).
+constexpr uint64_t kScratchKeepBytes = uint64_t(2) << 30;
+cudaError_t scratch_malloc(void **ptr, size_t bytes, cudaStream_t stream);
+
 // ------------------------------------------------------- debug bounds ----
 // The checked build (compiled with -DREPOPS_DEBUG_BOUNDS into
 // librepops_debug.so by build.build(debug_bounds=True)): the hot-path kernels

@@ -269,7 +269,7 @@ extern "C" int repops_fixed_order_mean_sgd_host(int nC, int64_t len, const float
     const int64_t ch = std::min<int64_t>(len, std::min<int64_t>(int64_t(1) << 22, cap / 4 * 4));
     const size_t slot = size_t(ch) * 4u;
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, 2 * size_t(nC + 1) * slot, stream) != cudaSuccess) {
+    if (scratch_malloc(&mem, 2 * size_t(nC + 1) * slot, stream) != cudaSuccess) {
         cudaGetLastError();
         return REPOPS_ERR_ALLOC;
     }

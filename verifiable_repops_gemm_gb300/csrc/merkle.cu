@@ -470,7 +470,7 @@ extern "C" int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t le
     if (rc != REPOPS_OK) return rc;
     void *ws = nullptr;
     if (pl.ws_bytes > 0) {
-        cudaError_t e = cudaMallocAsync(&ws, pl.ws_bytes, stream);
+        cudaError_t e = scratch_malloc(&ws, pl.ws_bytes, stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return REPOPS_ERR_ALLOC;
@@ -618,7 +618,7 @@ extern "C" int repops_merkle_sha256_host(const void *ptr, uint64_t bytes, uint32
     const uint64_t nchunks = (bytes + chunk_bytes - 1) / chunk_bytes;
     const uint64_t ws_bytes = (pl.ws_bytes + 255) / 256 * 256;
     void *mem = nullptr;
-    if (cudaMallocAsync(&mem, ws_bytes + 2 * chunk_bytes + 256, stream) != cudaSuccess) {
+    if (scratch_malloc(&mem, ws_bytes + 2 * chunk_bytes + 256, stream) != cudaSuccess) {
         cudaGetLastError();
         return REPOPS_ERR_ALLOC;
     }
@@ -688,7 +688,7 @@ extern "C" int repops_merkle_tree_sha256(const void *ptr, uint64_t bytes, uint32
     if (ranges_overlap(tree, need, ptr, bytes) || ranges_overlap(tree, need, root_out, 32)) return REPOPS_ERR_ALIAS;
     void *ws = nullptr;
     if (pl.ws_bytes > 0) {
-        cudaError_t e = cudaMallocAsync(&ws, pl.ws_bytes, stream);
+        cudaError_t e = scratch_malloc(&ws, pl.ws_bytes, stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return REPOPS_ERR_ALLOC;
@@ -782,8 +782,8 @@ extern "C" int repops_sha256_rate_probe(uint32_t threads, uint32_t iters, uint32
 // framework that has reserved all device memory for its own pool, a
 // latency-critical path on which an allocation could block or synchronise, or
 // a plug-in whose host forbids allocations after start-up.  The scratch of the
-// level nodes lives in the fixed array below instead of coming from
-// cudaMallocAsync or from the caller.
+// level nodes lives in the fixed array below instead of coming from the
+// library's scratch pool or from the caller.
 //
 // The array is part of the library's device image: every GPU that loads the
 // library holds these bytes until the process exits.  All calls share it and

@@ -41,7 +41,7 @@ extern "C" int repops_replay_mean_sgd_commit(int steps, int nC, int64_t len, con
     if (ws_bytes == 0 && repops_merkle_tree_bytes(bytes, leaf) == 0) return REPOPS_ERR_INVALID_ARG;
     void *ws = nullptr;
     if (ws_bytes > 0) {
-        cudaError_t e = cudaMallocAsync(&ws, ws_bytes, stream);
+        cudaError_t e = scratch_malloc(&ws, ws_bytes, stream);
         if (e != cudaSuccess) {
             cudaGetLastError();
             return REPOPS_ERR_ALLOC;

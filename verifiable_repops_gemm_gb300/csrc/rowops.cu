@@ -1229,7 +1229,7 @@ extern "C" int repops_colsum_f32(int64_t rows, int64_t cols, const float *x, int
     for (int64_t r = (rows + RUN - 1) / RUN; r > 1; r = (r + RUN - 1) / RUN) need += r;
     float *scratch = nullptr;
     if (need > 0) {
-        if (cudaMallocAsync(reinterpret_cast<void **>(&scratch), size_t(need) * size_t(cols) * 4u, stream) != cudaSuccess) {
+        if (scratch_malloc(reinterpret_cast<void **>(&scratch), size_t(need) * size_t(cols) * 4u, stream) != cudaSuccess) {
             cudaGetLastError();
             return REPOPS_ERR_ALLOC;
         }
