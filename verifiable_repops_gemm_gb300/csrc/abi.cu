@@ -1,6 +1,6 @@
 // abi.cu -- library-wide C-ABI entry points: build manifest, status strings,
-// CUDA error bookkeeping, device properties, the contributor sort and the
-// sticky device status word.
+// CUDA error bookkeeping, device properties, the contributor sort, the sticky
+// device status word and the stream-ordered scratch pool.
 #include <algorithm>
 #include <atomic>
 #include <cstring>
@@ -150,6 +150,23 @@ cudaError_t scratch_malloc(void **ptr, size_t bytes, cudaStream_t stream) {
         return cudaMallocAsync(ptr, bytes, stream);
     }
     return cudaMallocFromPoolAsync(ptr, bytes, pool, stream);
+}
+
+cudaError_t join_helper_streams(cudaStream_t stream, cudaStream_t a, cudaStream_t b) {
+    cudaError_t first = cudaSuccess;
+    for (cudaStream_t h : {a, b}) {
+        if (!h) continue;
+        cudaEvent_t ev = nullptr;
+        cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventRecord(ev, h);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, ev, 0);
+        if (ev) cudaEventDestroy(ev);
+        if (e != cudaSuccess) {
+            cudaStreamSynchronize(h);
+            if (first == cudaSuccess) first = e;
+        }
+    }
+    return first;
 }
 
 }  // namespace repops

@@ -786,10 +786,9 @@ extern "C" int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float
         return REPOPS_ERR_ALLOC;
     }
     float *dA = static_cast<float *>(mem), *dB = dA + bytesA / 4, *dC = dB + bytesB / 4;
-    cudaEvent_t ready, b_in, done_in, done_out;
+    cudaEvent_t ready, b_in;
     int rc = REPOPS_OK;
-    if ((e = res.event(&ready)) != cudaSuccess || (e = res.event(&b_in)) != cudaSuccess ||
-        (e = res.event(&done_in)) != cudaSuccess || (e = res.event(&done_out)) != cudaSuccess) {
+    if ((e = res.event(&ready)) != cudaSuccess || (e = res.event(&b_in)) != cudaSuccess) {
         cudaFreeAsync(mem, stream);
         return set_cuda_error(e);
     }
@@ -828,11 +827,9 @@ extern "C" int repops_gemm_f32_host(int64_t M, int64_t N, int64_t K, const float
                                    size_t(r1 - r0), cudaMemcpyDeviceToHost, res.out)) != cudaSuccess)
             rc = set_cuda_error(e);
     }
-    // `stream` resumes after every copy in and back; then the memory is released
-    if ((e = cudaEventRecord(done_in, res.in)) != cudaSuccess || (e = cudaStreamWaitEvent(stream, done_in, 0)) != cudaSuccess ||
-        (e = cudaEventRecord(done_out, res.out)) != cudaSuccess || (e = cudaStreamWaitEvent(stream, done_out, 0)) != cudaSuccess) {
-        if (rc == REPOPS_OK) rc = set_cuda_error(e);
-    }
+    // `stream` resumes after every copy in and back (or what an error left
+    // queued); then the memory is released
+    if ((e = join_helper_streams(stream, res.in, res.out)) != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
     e = cudaFreeAsync(mem, stream);
     if (rc == REPOPS_OK && e != cudaSuccess) rc = set_cuda_error(e);
     return rc;

@@ -61,9 +61,16 @@ int status_word_address(unsigned **out);
 constexpr uint64_t kScratchKeepBytes = uint64_t(2) << 30;
 cudaError_t scratch_malloc(void **ptr, size_t bytes, cudaStream_t stream);
 
+// Makes `stream` wait for everything queued so far on the helper streams a and
+// b (either may be null), so that memory released on `stream` afterwards is
+// no longer in use by them -- also when the caller stopped half-way on an
+// error.  If an event call fails, the helpers are waited for on the host
+// instead.  Returns the first error of those calls (cudaSuccess if none).
+cudaError_t join_helper_streams(cudaStream_t stream, cudaStream_t a, cudaStream_t b);
+
 // ------------------------------------------------------- debug bounds ----
 // The checked build (compiled with -DREPOPS_DEBUG_BOUNDS into
-// librepops_debug.so by build.build(debug_bounds=True)): the hot-path kernels
+// librepops_debug.so by build.build(checked=True)): the hot-path kernels
 // test every global access against the span of the buffer it belongs to; an
 // access outside it is skipped and bit 1 of the status word is set, which
 // repops_device_status reports as REPOPS_ERR_BOUNDS.  A stand-in for a memory

@@ -312,13 +312,12 @@ extern "C" int repops_fixed_order_mean_sgd_host(int nC, int64_t len, const float
             (e = cudaEventRecord(back[b], out)) != cudaSuccess)
             break;
     }
-    // `stream` resumes after the last copy back; then the memory is released
-    cudaEvent_t fin = nullptr;
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&fin, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventRecord(fin, out);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, fin, 0);
+    // `stream` resumes after every copy queued on the helper streams (the last
+    // copy back, or what an error left queued); then the memory is released
+    const cudaError_t j = join_helper_streams(stream, in, out);
+    if (e == cudaSuccess) e = j;
     const cudaError_t f = cudaFreeAsync(mem, stream);
-    for (cudaEvent_t x : {ready, got[0], got[1], back[0], back[1], fin})
+    for (cudaEvent_t x : {ready, got[0], got[1], back[0], back[1]})
         if (x) cudaEventDestroy(x);
     if (in) cudaStreamDestroy(in);
     if (out) cudaStreamDestroy(out);

@@ -671,6 +671,10 @@ extern "C" int repops_merkle_sha256_host(const void *ptr, uint64_t bytes, uint32
         rc = reduce_levels(pl, droot, bufA, bufB, pc, TreeOut{nullptr, 0}, dbg, stream);
     if (rc == REPOPS_OK && e == cudaSuccess)
         e = cudaMemcpyAsync(root_out, droot, 32, cudaMemcpyDeviceToHost, stream);
+    // every copy into the chunk buffers is over before they are released, also
+    // when an error stopped the loop half-way
+    const cudaError_t j = join_helper_streams(stream, res.in, nullptr);
+    if (e == cudaSuccess) e = j;
     const cudaError_t f = cudaFreeAsync(mem, stream);
     if (rc != REPOPS_OK) return rc;
     if (e != cudaSuccess) return set_cuda_error(e);
