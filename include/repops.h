@@ -240,8 +240,8 @@ int repops_gemm_f32_config(int config, int loader, int transA, int transB,
  * repops_gemm_f32 -- the same bits for every worker count (a split-K that adds
  * separately computed partial sums would not be).  ("Verde与RepOps" §3.2: the
  * order-critical dimension stays serial; only who computes which part of a
- * chain changes.)  Scratch (about workers x 32 KB) is taken with
- * from the scratch pool on `stream`; the kernel is launched cooperatively and every
+ * chain changes.)  Scratch (about workers x 32 KB) is taken from the scratch
+ * pool on `stream`; the kernel is launched cooperatively and every
  * wait between workers is bounded (status word).  UNSUPPORTED when the
  * operands do not meet the TMA rule, `workers` is too large, or the scratch is
  * refused; INVALID_ARG for workers < 0; other errors as repops_gemm_f32. */
@@ -440,8 +440,8 @@ int repops_fixed_order_mean_sgd_typed(int nC, int64_t len, const void *const *pt
  * ptr (device): `bytes` bytes, bytes >= 1.  leaf: a multiple of 64, 64 <=
  * leaf <= 2^30.  root_out (device): receives the 32-byte root, written
  * asynchronously on `stream`.
- * Scratch of repops_merkle_workspace_bytes(bytes, leaf) bytes is taken with
- * from the scratch pool on `stream` and released with cudaFreeAsync on the same
+ * Scratch of repops_merkle_workspace_bytes(bytes, leaf) bytes is taken from
+ * the scratch pool on `stream` and released with cudaFreeAsync on the same
  * stream.  Errors: INVALID_ARG (null pointer, bytes == 0, bad leaf); ALIAS
  * (root_out inside the input); ALLOC; CUDA. */
 int repops_merkle_sha256(const void *ptr, uint64_t bytes, uint32_t leaf,
