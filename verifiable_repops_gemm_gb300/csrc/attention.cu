@@ -366,10 +366,12 @@ extern "C" int repops_attention_causal_f32(int64_t seqs, int64_t S, int64_t head
     if (seqs == 0 || S == 0 || heads == 0) return REPOPS_OK;
     if (kv_heads == 0 || heads % kv_heads != 0) return REPOPS_ERR_INVALID_ARG;
     if (!q || !k || !v || !out) return REPOPS_ERR_INVALID_ARG;
+    // the limits first: they bound every product below
+    if (dh != ADH || S > AMAXS) return REPOPS_ERR_UNSUPPORTED;
+    if (heads > (int64_t(1) << 31) || seqs > (int64_t(1) << 31) / heads || seqs * S > (int64_t(1) << 40))
+        return REPOPS_ERR_UNSUPPORTED;
     if (ldq < heads * dh || ldk < kv_heads * dh || ldv < kv_heads * dh || ldo < heads * dh)
         return REPOPS_ERR_INVALID_ARG;
-    if (dh != ADH || S > AMAXS) return REPOPS_ERR_UNSUPPORTED;
-    if (seqs > (int64_t(1) << 31) / heads || seqs * S > (int64_t(1) << 40)) return REPOPS_ERR_UNSUPPORTED;
     // 16-byte copies of every query, key and value row; float4 rows of probs
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || ldq % 4 || ldk % 4 || ldv % 4 || ldo % 2 ||
         reinterpret_cast<uintptr_t>(out) % 8 || (probs && (!aligned16(probs) || S % 4)))
