@@ -88,6 +88,8 @@ if __name__ == "__main__":
     import verifiable_repops_gemm_gb300 as rp
     from verifiable_repops_gemm_gb300 import _capi
     _capi.load(sys.argv[1])
+    # the manifest names the build that produced the bits
+    assert "-DREPOPS_DEBUG_BOUNDS" in rp.version(), rp.version()
     res = workloads(rp)
     np.savez(sys.argv[2], **res)
     print("checked run ok:", len(res), "results")

@@ -45,3 +45,18 @@ def rp():
     import verifiable_repops_gemm_gb300 as rp
     rp.load()
     return rp
+
+
+@pytest.fixture(autouse=True)
+def _no_pending_device_failure(request):
+    """After every test that used the library on the GPU, its shared status
+    word must be clear: no bounded wait gave up and -- when REPOPS_LIBRARY
+    names the access-checking build -- no access fell outside its buffer.
+    Tests that provoke a failure on purpose read (and so clear) it themselves."""
+    yield
+    if "rp" not in request.fixturenames:
+        return
+    import verifiable_repops_gemm_gb300 as lib
+    from verifiable_repops_gemm_gb300 import _capi
+    st = lib.device_status()
+    assert st == 0, "device status %d (%s) left by the test" % (st, _capi.status_string(st))

@@ -42,6 +42,9 @@ def test_manifest_names_arithmetic_flags(L):
     v = L.repops_version().decode()
     for s in ("sm_103a", "-fmad=false", "-ftz=false", "-prec-div=true", "no tensor cores"):
         assert s in v, s
+    # the release build; the checked build's manifest adds -DREPOPS_DEBUG_BOUNDS
+    if not os.environ.get("REPOPS_LIBRARY"):
+        assert "REPOPS_DEBUG_BOUNDS" not in v
 
 
 def test_status_strings(L):

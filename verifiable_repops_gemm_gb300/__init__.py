@@ -36,7 +36,7 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "scratch_release", "scratch_reserved_bytes", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",

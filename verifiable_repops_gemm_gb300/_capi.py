@@ -115,11 +115,16 @@ class RepopsError(RuntimeError):
 
 
 def load(path: str = None) -> ctypes.CDLL:
-    """Loads librepops.so (once).  Raises if it has not been built."""
+    """Loads librepops.so (once).  Raises if it has not been built.
+
+    Without `path`, the environment variable REPOPS_LIBRARY, when set, names
+    the library file to load instead of the in-tree release build -- e.g. the
+    access-checking build _build_checked/librepops_debug.so, to run a whole
+    program or test suite with every hot-path global access checked."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    path = path or os.environ.get("REPOPS_LIBRARY") or LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError(
             "librepops.so is not built (%s); run `python -c \"import __graft_entry__ as g; g.build()\"` "

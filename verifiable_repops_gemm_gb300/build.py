@@ -46,8 +46,8 @@ def _headers():
             glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def _flag_string() -> str:
-    return " ".join(ARCH + ARITH)
+def _flag_string(extra=()) -> str:
+    return " ".join(ARCH + ARITH + [f for f in extra if f.startswith("-D")])
 
 
 def _stale(target: str, deps) -> bool:
@@ -64,7 +64,7 @@ def _compile(src: str, extra, out_dir: str = OUT) -> str:
         return obj
     tmp = obj + ".tmp.%d" % os.getpid()
     cmd = ([nvcc()] + NVCC_FLAGS + extra +
-           ['-DREPOPS_BUILD_FLAGS="%s"' % _flag_string(), "-c", src, "-o", tmp])
+           ['-DREPOPS_BUILD_FLAGS="%s"' % _flag_string(extra), "-c", src, "-o", tmp])
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (os.path.basename(src), r.stdout, r.stderr))
