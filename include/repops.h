@@ -31,8 +31,8 @@
  *     state between calls, except the sticky device status word of the
  *     bounded waits (by default one word per device shared by every caller,
  *     or a word the caller owns, bound per host thread with
- *     repops_set_thread_status_word()) and the freed memory its scratch pool
- *     keeps mapped (see "Scratch memory" below).
+ *     repops_set_thread_status_word()) and, only where the caller asks for
+ *     it, freed scratch its memory pool keeps mapped (see "Scratch memory").
  *   - Floating point is IEEE-754 binary32, round-to-nearest-even, subnormals
  *     kept (no flush-to-zero), no fused multiply-add, no tensor cores.
  *   - NaN results compare equal as a class (payload bits are not pinned);
@@ -117,17 +117,24 @@ int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
  * buffers of the host-buffer calls, ...) allocate it stream-ordered, on the
  * caller's stream, from a memory pool the library creates for each device
  * (one per CUDA context; the device's default pool is neither used nor
- * changed).  Freed memory stays mapped in that pool, up to 2 GiB, across
- * synchronisations, so a call made after a synchronisation does not map its
- * scratch again.  Thread-safe.
+ * changed).  By default that pool, like the default one, hands freed memory
+ * back at the next synchronisation: the library holds no memory between
+ * calls.  A call made after a synchronisation then maps its scratch again,
+ * which costs ~120 us of host time (on a GB300, synchronising after every
+ * call: a 1536^3 GEMM 318 us a call against 242 us with its scratch kept).
+ * Thread-safe.
  *
+ * repops_scratch_set_keep_bytes: lets the current device's pool keep up to
+ * `bytes` of freed scratch mapped across synchronisations (0, the default,
+ * keeps none).  REPOPS_OK, or REPOPS_ERR_CUDA.
  * repops_scratch_release: hands back to the system the memory of the current
  * device's pool that no allocation holds (scratch of calls still in flight,
  * whose frees have not run on their streams yet, stays).  REPOPS_OK, or
  * REPOPS_ERR_CUDA.
  * repops_scratch_reserved_bytes: *bytes_out = device memory the current
- * device's pool holds mapped now (0 before its first allocation).
- * REPOPS_ERR_INVALID_ARG for a null bytes_out. */
+ * device's pool holds mapped now.  REPOPS_ERR_INVALID_ARG for a null
+ * bytes_out. */
+int repops_scratch_set_keep_bytes(uint64_t bytes);
 int repops_scratch_release(void);
 int repops_scratch_reserved_bytes(uint64_t *bytes_out);
 

@@ -1,10 +1,12 @@
-"""GPU tests of the library's scratch pool (repops_scratch_release,
-repops_scratch_reserved_bytes; "Scratch memory" in include/repops.h).
+"""GPU tests of the library's scratch pool (repops_scratch_set_keep_bytes,
+repops_scratch_release, repops_scratch_reserved_bytes; "Scratch memory" in
+include/repops.h).
 
-Scratch taken by one call stays mapped after a synchronisation, so the next
-call does not map it again; a release hands it back; the device's default
-pool is neither used nor changed; and the bits are the oracle's before and
-after a release.
+By default the library holds no memory between calls: scratch taken by a call
+is handed back at the next synchronisation.  When the caller asks for it, the
+pool keeps freed scratch mapped across synchronisations (so the next call does
+not map it again) until a release.  The device's default pool is neither used
+nor changed, and the bits are the oracle's in every mode.
 """
 import ctypes
 
@@ -35,27 +37,39 @@ def bits(t):
     return t.cpu().numpy().view(np.uint32)
 
 
-def test_scratch_stays_mapped_until_released(rp, orc):
+def test_scratch_kept_only_when_asked_and_until_released(rp, orc):
     # 1000 x 1001 x 520 with B stored transposed (1.04 GFLOP): B is copied
     # into a row-major scratch copy before the kernel runs
     A = inputs.normal((1000, 520), 1.0, 41, DEV)
     B = inputs.normal((1001, 520), 1.0, 42, DEV).t()
     want = oracle_par.gemm(orc, A, B).view(np.uint32)
     threshold = default_pool_release_threshold()
-    C1 = rp.gemm(A, B)
-    torch.cuda.synchronize()
-    assert rp.scratch_reserved_bytes() >= 1001 * 520 * 4
-    C2 = rp.gemm(A, B)
-    torch.cuda.synchronize()
-    rp.scratch_release()
+    results = []
+    try:
+        # default: nothing held once the call's work has been synchronised
+        results.append(rp.gemm(A, B))
+        torch.cuda.synchronize()
+        assert rp.scratch_reserved_bytes() == 0
+        # kept on request, across synchronisations, until released
+        rp.scratch_set_keep_bytes(1 << 30)
+        for _ in range(2):
+            results.append(rp.gemm(A, B))
+            torch.cuda.synchronize()
+            assert rp.scratch_reserved_bytes() >= 1001 * 520 * 4
+        rp.scratch_release()
+        torch.cuda.synchronize()
+        assert rp.scratch_reserved_bytes() == 0
+        results.append(rp.gemm(A, B))
+        torch.cuda.synchronize()
+        assert rp.scratch_reserved_bytes() >= 1001 * 520 * 4
+    finally:
+        rp.scratch_set_keep_bytes(0)
+        rp.scratch_release()
     torch.cuda.synchronize()
     assert rp.scratch_reserved_bytes() == 0
-    C3 = rp.gemm(A, B)
-    torch.cuda.synchronize()
-    for C in (C1, C2, C3):
+    for C in results:
         assert np.array_equal(bits(C), want)
     assert default_pool_release_threshold() == threshold
-    assert rp.device_status() == 0
 
 
 def test_scratch_shared_by_streams_and_entry_points(rp, orc):
@@ -69,6 +83,7 @@ def test_scratch_shared_by_streams_and_entry_points(rp, orc):
     want_rows = oracle_par.gemm(orc, A, B, rows=rows)
     want_root = orc.merkle_root(T.cpu().numpy(), 4096)
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    rp.scratch_set_keep_bytes(256 << 20)
     for it in range(4):
         with torch.cuda.stream(s1):
             C = rp.gemm(A, B)
@@ -81,4 +96,6 @@ def test_scratch_shared_by_streams_and_entry_points(rp, orc):
         assert bytes(root.cpu().numpy()) == want_root, it
         if it % 2:
             rp.scratch_release()
+    rp.scratch_set_keep_bytes(0)
+    rp.scratch_release()
     assert rp.device_status() == 0

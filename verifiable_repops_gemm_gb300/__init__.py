@@ -36,7 +36,7 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "scratch_release", "scratch_reserved_bytes", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "scratch_set_keep_bytes", "scratch_release", "scratch_reserved_bytes", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
@@ -421,6 +421,13 @@ def device_status(stream=None) -> int:
     rc = load().repops_device_status(_stream_handle(stream), ctypes.byref(v))
     _capi.check(rc, "repops_device_status")
     return v.value
+
+
+def scratch_set_keep_bytes(nbytes: int) -> None:
+    """Lets the library's scratch pool of the current device keep up to
+    `nbytes` of freed scratch mapped across synchronisations (0, the default,
+    keeps none; repops_scratch_set_keep_bytes)."""
+    _capi.check(load().repops_scratch_set_keep_bytes(int(nbytes)), "repops_scratch_set_keep_bytes")
 
 
 def scratch_release() -> None:

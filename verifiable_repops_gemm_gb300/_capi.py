@@ -34,6 +34,7 @@ SIGNATURES = {
     "repops_status_string": (_cs, [_i32]),
     "repops_last_cuda_error": (_i32, []),
     "repops_device_status": (_i32, [_vp, _vp]),
+    "repops_scratch_set_keep_bytes": (_i32, [ctypes.c_uint64]),
     "repops_scratch_release": (_i32, []),
     "repops_scratch_reserved_bytes": (_i32, [_vp]),
     "repops_set_thread_status_word": (_i32, [_vp]),

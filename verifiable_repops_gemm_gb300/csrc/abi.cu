@@ -95,21 +95,24 @@ int current_context_key(uint64_t *key) {
 namespace {
 // The scratch pool of each device, created in the CUDA context current at
 // the first allocation and again when that context changes (after
-// cudaDeviceReset the old handle is gone with its context).  A device's
-// default pool returns its free memory to the system at every
-// synchronisation (release threshold 0), so each call made after one paid
-// ~120 us of host time mapping its scratch again, with the GPU idle if
-// nothing else was queued: measured on a GB300, a 1536^3 GEMM 318 -> 242 us
-// and a 2048^3 one 598 -> 522 us a call, synchronised after each.
+// cudaDeviceReset the old handle is gone with its context).  `keep` is the
+// caller's setting (repops_scratch_set_keep_bytes), 0 by default: the pool
+// then hands freed memory back at every synchronisation, as the device's
+// default pool does, and the library holds no memory between calls.  A call
+// made after a synchronisation then maps its scratch again: ~120 us of host
+// time with the GPU idle if nothing else was queued (measured on a GB300,
+// synchronised after every call: a 1536^3 GEMM 318 us a call, 242 us with
+// the scratch kept; 2048^3 598 -> 522 us).
 struct ScratchPool {
     std::mutex mu;
     uint64_t ctx_key = 0;
     cudaMemPool_t pool = nullptr;
+    uint64_t keep = 0;
 };
 ScratchPool g_scratch_pool[kMaxDevices];
 
-// The current device's pool; *pool stays null when there is no pool to use.
-int scratch_pool(cudaMemPool_t *pool) {
+// The current device's pool (created if needed) and its slot.
+int scratch_pool(cudaMemPool_t *pool, ScratchPool **slot = nullptr) {
     *pool = nullptr;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -129,7 +132,7 @@ int scratch_pool(cudaMemPool_t *pool) {
         props.location.id = dev;
         cudaMemPool_t p = nullptr;
         if ((e = cudaMemPoolCreate(&p, &props)) != cudaSuccess) return set_cuda_error(e);
-        uint64_t keep = kScratchKeepBytes;
+        uint64_t keep = s.keep;
         if ((e = cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
             cudaMemPoolDestroy(p);
             return set_cuda_error(e);
@@ -138,6 +141,7 @@ int scratch_pool(cudaMemPool_t *pool) {
         s.ctx_key = key;
     }
     *pool = s.pool;
+    if (slot) *slot = &s;
     return REPOPS_OK;
 }
 }  // namespace
@@ -213,6 +217,19 @@ extern "C" int repops_scratch_release(void) {
     if (rc != REPOPS_OK) return rc;
     const cudaError_t e = cudaMemPoolTrimTo(pool, 0);
     return e == cudaSuccess ? REPOPS_OK : set_cuda_error(e);
+}
+
+extern "C" int repops_scratch_set_keep_bytes(uint64_t bytes) {
+    cudaMemPool_t pool = nullptr;
+    ScratchPool *slot = nullptr;
+    int rc = scratch_pool(&pool, &slot);
+    if (rc != REPOPS_OK) return rc;
+    std::lock_guard<std::mutex> lock(slot->mu);
+    uint64_t v = bytes;
+    const cudaError_t e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &v);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    slot->keep = bytes;
+    return REPOPS_OK;
 }
 
 extern "C" int repops_scratch_reserved_bytes(uint64_t *bytes_out) {

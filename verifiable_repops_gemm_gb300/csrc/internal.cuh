@@ -55,10 +55,10 @@ int status_word_address(unsigned **out);
 
 // Stream-ordered scratch for the entry points: `bytes` on `stream` from the
 // library's own memory pool of the current device (one per device and CUDA
-// context), which keeps up to kScratchKeepBytes mapped across synchronisations.
-// Freed with cudaFreeAsync like any stream-ordered allocation.  Returns the
-// CUDA error of the allocation (cudaSuccess, or e.g. out of memory).
-constexpr uint64_t kScratchKeepBytes = uint64_t(2) << 30;
+// context; how much freed memory it keeps across synchronisations is the
+// caller's setting, none by default).  Freed with cudaFreeAsync like any
+// stream-ordered allocation.  Returns the CUDA error of the allocation
+// (cudaSuccess, or e.g. out of memory).
 cudaError_t scratch_malloc(void **ptr, size_t bytes, cudaStream_t stream);
 
 // Makes `stream` wait for everything queued so far on the helper streams a and
