@@ -73,6 +73,24 @@ def test_unaligned_rows_and_in_place(rp, orc, cols):
     assert np.array_equal(u32(z.cpu().numpy()), u32(want_ln))
 
 
+@pytest.mark.parametrize("cols", [32769, 38437, 393216])
+def test_unaligned_long_rows(rp, orc, cols):
+    # rows past 32,768 values that are not 16-byte aligned: the long-row
+    # kernel, whose shared buffer holds every run result of the row (it was
+    # once sized for 1,025 runs whenever the rows were unaligned)
+    x = rows_input(2, cols, 4500 + cols, 3.0, pad=1)
+    xh = x.cpu().numpy()
+    assert np.array_equal(u32(rp.softmax_rows(x).cpu().numpy()), u32(orc.softmax_rows(xh)))
+    y = rp.softmax_rows(x, causal_first=cols - 2, causal_period=2)
+    assert np.array_equal(u32(y.cpu().numpy()), u32(orc.softmax_rows_causal(xh, cols - 2, 2)))
+    g = inputs.normal((cols,), 1.0, 8, DEV)
+    b = inputs.normal((cols,), 1.0, 9, DEV)
+    want = orc.layernorm_rows(xh, g.cpu().numpy(), b.cpu().numpy(), 1e-5)
+    assert np.array_equal(u32(rp.layernorm_rows(x, g, b, 1e-5).cpu().numpy()), u32(want))
+    want = orc.rmsnorm_rows(xh, g.cpu().numpy(), 1e-6)
+    assert np.array_equal(u32(rp.rmsnorm_rows(x, g, 1e-6).cpu().numpy()), u32(want))
+
+
 @pytest.mark.parametrize("n", [1, 7, 4096, (1 << 20) + 3])
 def test_gelu_matches_oracle(rp, orc, n):
     x = inputs.normal((n,), 3.0, 5000 + n, DEV)

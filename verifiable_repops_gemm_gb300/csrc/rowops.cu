@@ -1005,16 +1005,21 @@ int launch_fast(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, 
 
 int run_rows(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, const float *gamma, const float *beta,
              float eps, float *y, int64_t ldy, cudaStream_t s, int64_t first = -1, int64_t period = 1) {
-    int64_t runs = (n + RUN - 1) / RUN;
-    // threads per row: enough for one run each up to 256, then up to 4 runs per thread
-    // rows that are not 16-byte aligned take the long-row kernel (same bits)
-    if (!rows_vec_ok(x, ldx, y, ldy)) runs = MAX_FAST_RUNS + 1;
-    if (runs <= 32) return launch_fast<32, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
-    if (runs <= 64) return launch_fast<64, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
-    if (runs <= 128) return launch_fast<128, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
-    if (runs <= 256) return launch_fast<256, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
-    if (runs <= 512) return launch_fast<256, 2>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
-    if (runs <= MAX_FAST_RUNS) return launch_fast<256, 4>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    const int64_t runs = (n + RUN - 1) / RUN;
+    // threads per row: enough for one run each up to 256, then up to 4 runs
+    // per thread; rows that are not 16-byte aligned, and longer rows, take
+    // the long-row kernel (same bits)
+    if (rows_vec_ok(x, ldx, y, ldy)) {
+        if (runs <= 32) return launch_fast<32, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+        if (runs <= 64) return launch_fast<64, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+        if (runs <= 128) return launch_fast<128, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+        if (runs <= 256) return launch_fast<256, 1>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+        if (runs <= 512) return launch_fast<256, 2>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+        if (runs <= MAX_FAST_RUNS)
+            return launch_fast<256, 4>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy, first, period, s);
+    }
+    // its shared buffer holds the row's run results and their group results:
+    // sized from the row's own run count, whatever the path choice
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(rows_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
