@@ -236,3 +236,51 @@ def test_random_batched_gemm_epilogue(rp, orc, case):
         want[b] = C.reshape(M, N)
     same(host(out), want, dict(batch=batch, M=M, N=N, K=K, alpha=alpha, bias=use_bias, res=use_res, act=act,
                                ta=ta, tb=tb, shared_b=shared_b))
+
+
+@pytest.mark.parametrize("case", range(60))
+def test_random_batched_causal_and_banded(rp, orc, case):
+    # interleaved heads (batch matrices as column blocks of one matrix),
+    # B shared by groups of consecutive batches, then either a causal tile
+    # skip (only elements on or below the boundary are defined) or a k band
+    # per row with A +0 outside it (the attention products)
+    rng = np.random.default_rng(23_000 + case)
+    groups = int(rng.integers(1, 4))
+    group = int(rng.integers(1, 4))
+    batch = groups * group
+    M = int(np.exp(rng.uniform(0.0, np.log(400.0))))
+    N = int(np.exp(rng.uniform(0.0, np.log(200.0))))
+    K = int(np.exp(rng.uniform(0.0, np.log(400.0))))
+    X = inputs.normal((M, batch * K + 4), 1.0, 23_100 + case, DEV)
+    A = X[:, :batch * K].view(M, batch, K).transpose(0, 1)          # (batch, M, K), stride K apart
+    Bm = inputs.normal((groups, K, N), 1.0, 23_200 + case, DEV)
+    banded = bool(case % 2)
+    first, k_lo, k_hi = -1, -1, -1
+    if banded:
+        k_lo = int(rng.integers(0, K + 1)) if rng.integers(3) else -1
+        k_hi = int(rng.integers(0, K + 1)) if (rng.integers(3) or k_lo < 0) else -1
+        i = torch.arange(M, device=DEV)[:, None]
+        k = torch.arange(K, device=DEV)[None, :]
+        inside = torch.ones((M, K), dtype=torch.bool, device=DEV)
+        if k_lo >= 0:
+            inside &= k >= i - k_lo
+        if k_hi >= 0:
+            inside &= k <= i + k_hi
+        A.mul_(inside.to(torch.float32))                                # +0 (or -0) outside each row's band
+    else:
+        first = int(rng.integers(0, max(1, N)))
+    out = torch.full((batch, M, N), CANARY, device=DEV)
+    rp.gemm_batched(A, Bm, out=out, causal_first=first, k_lo=k_lo, k_hi=k_hi)
+    torch.cuda.synchronize()
+    Ah = np.ascontiguousarray(host(X)[:, :batch * K])
+    want = np.zeros(batch * M * N, np.float32)
+    orc.gemm_batched(0, 0, batch, M, N, K, Ah.reshape(-1), batch * K, K, host(Bm).reshape(-1), N, K * N,
+                     want, N, M * N, k_lo=k_lo, k_hi=k_hi, b_group=group)
+    want = want.reshape(batch, M, N)
+    got = host(out)
+    what = dict(batch=batch, group=group, M=M, N=N, K=K, first=first, k_lo=k_lo, k_hi=k_hi)
+    if first >= 0:
+        defined = np.arange(N)[None, :] <= first + np.arange(M)[:, None]
+        assert np.array_equal(got[:, defined].view(np.uint32), want[:, defined].view(np.uint32)), what
+    else:
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), what
