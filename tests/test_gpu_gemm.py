@@ -509,3 +509,24 @@ def test_chained_split_is_the_automatic_choice_where_waves_are_uneven(rp):
     assert rp.gemm_auto_chained(2048, 2048, 2048)
     assert not rp.gemm_auto_chained(8192, 8192, 8192)
     assert not rp.gemm_auto_chained(256, 256, 256)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("M,N,K", [(2048, 2048, 2048), (4097, 1024, 3000), (3000, 3000, 1000)])
+def test_chained_split_repeated_runs_identical(rp, M, N, K):
+    # the heads' stores and the tails' flag-acquired loads race only if the
+    # release/acquire protocol is wrong: 200 runs across worker counts (every
+    # resident slot, one per SM, odd counts) must all give the one-CTA-per-tile
+    # bytes, with no bounded wait giving up
+    A = inputs.normal((M, K), 1.0, 31, DEV)
+    B = inputs.normal((K, N), 1.0, 32, DEV)
+    ref = rp.gemm(A, B, config=0, loader=rp.LOADER_TMA).view(torch.int32).clone()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mismatches = 0
+    for w in (0, sms, sms - 1, 97, 64):
+        for _ in range(40):
+            C = rp.gemm_chained(A, B, config=0, workers=w)
+            mismatches += int(not torch.equal(C.view(torch.int32), ref))
+    torch.cuda.synchronize()
+    assert mismatches == 0
+    assert rp.device_status() == 0
