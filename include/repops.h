@@ -189,6 +189,38 @@ int repops_gemm_f32_ex(int transA, int transB,
                        float *C, int64_t ldc,
                        cudaStream_t stream);
 
+/* Device scratch, in bytes, that repops_gemm_f32_ex (automatic choice) takes
+ * for this problem and these operands: copies of operands into the kernels'
+ * faster layouts and the chained k-split's running sums and flags (see
+ * repops_gemm_f32_chained).  0 when the call runs on the caller's operands
+ * alone, or for arguments repops_gemm_f32_ex would reject.  Host-only (reads
+ * the device's properties, no launch); the pointers are looked at for their
+ * alignment only. */
+uint64_t repops_gemm_workspace_bytes(int transA, int transB,
+                                     int64_t M, int64_t N, int64_t K,
+                                     const float *A, int64_t lda,
+                                     const float *B, int64_t ldb);
+
+/* As repops_gemm_f32_ex, with the scratch taken from `workspace` (device,
+ * 256-byte aligned, `workspace_bytes` bytes, owned by the caller and touched
+ * by nothing else until the call's work on `stream` is done) instead of the
+ * library's scratch pool, when workspace_bytes is at least
+ * repops_gemm_workspace_bytes() for the same arguments; a smaller workspace
+ * is not used (the scratch then comes from the pool).  The library then holds
+ * no memory of its own for the call, and a caller that keeps its workspace
+ * (or takes it from a caching allocator) pays no mapping of fresh memory
+ * after a synchronisation.  The bits equal repops_gemm_f32_ex's.  Errors as
+ * repops_gemm_f32_ex, plus INVALID_ARG (a workspace that is not 256-byte
+ * aligned, or null with workspace_bytes > 0) and ALIAS (the workspace
+ * overlaps A, B or C). */
+int repops_gemm_f32_ws(int transA, int transB,
+                       int64_t M, int64_t N, int64_t K,
+                       const float *A, int64_t lda,
+                       const float *B, int64_t ldb,
+                       float *C, int64_t ldc,
+                       void *workspace, uint64_t workspace_bytes,
+                       cudaStream_t stream);
+
 /* As repops_gemm_f32 with A, B and C in HOST memory (row-major, pitches as
  * there; page-locked memory for full speed).  The call takes device memory
  * for A, B and C (16-byte pitches) from the scratch pool on `stream`, copies B,

@@ -374,6 +374,13 @@ def test_added_entry_points_reject_bad_arguments(L):
     assert L.repops_set_thread_status_word(None) == 0
     # the scratch pool's size query needs somewhere to write
     assert L.repops_scratch_reserved_bytes(None) == -1
+    # GEMM workspace: sizes of rejected arguments are 0; a misaligned or
+    # null-but-sized workspace is refused before any launch
+    assert L.repops_gemm_workspace_bytes(0, 0, -1, 8, 8, FAKE_A, 8, FAKE_B, 8) == 0
+    assert L.repops_gemm_workspace_bytes(0, 0, 8, 8, 8, FAKE_A, 4, FAKE_B, 8) == 0
+    assert L.repops_gemm_f32_ws(0, 0, 8, 8, 8, FAKE_A, 8, FAKE_B, 8, FAKE_C, 8, FAKE_C + (1 << 20) + 16, 4096,
+                                None) == -1
+    assert L.repops_gemm_f32_ws(0, 0, 8, 8, 8, FAKE_A, 8, FAKE_B, 8, FAKE_C, 8, None, 4096, None) == -1
     # host-buffer mean + SGD: counts, orders, aliasing host ranges
     import ctypes as C
     ptrs = (C.c_void_p * 2)(FAKE_A, FAKE_B)

@@ -45,21 +45,29 @@ def test_scratch_kept_only_when_asked_and_until_released(rp, orc):
     want = oracle_par.gemm(orc, A, B).view(np.uint32)
     threshold = default_pool_release_threshold()
     results = []
+
+    def gemm_pool():
+        # the C entry point itself (the binding's gemm passes a workspace instead)
+        C = torch.empty((1000, 1001), device=DEV)
+        assert rp.gemm_raw(1000, 1001, 520, A.data_ptr(), 520, B.data_ptr(), 520, C.data_ptr(), 1001,
+                           transB=1) == 0
+        return C
+
     try:
         # default: nothing held once the call's work has been synchronised
-        results.append(rp.gemm(A, B))
+        results.append(gemm_pool())
         torch.cuda.synchronize()
         assert rp.scratch_reserved_bytes() == 0
         # kept on request, across synchronisations, until released
         rp.scratch_set_keep_bytes(1 << 30)
         for _ in range(2):
-            results.append(rp.gemm(A, B))
+            results.append(gemm_pool())
             torch.cuda.synchronize()
             assert rp.scratch_reserved_bytes() >= 1001 * 520 * 4
         rp.scratch_release()
         torch.cuda.synchronize()
         assert rp.scratch_reserved_bytes() == 0
-        results.append(rp.gemm(A, B))
+        results.append(gemm_pool())
         torch.cuda.synchronize()
         assert rp.scratch_reserved_bytes() >= 1001 * 520 * 4
     finally:
@@ -98,4 +106,55 @@ def test_scratch_shared_by_streams_and_entry_points(rp, orc):
             rp.scratch_release()
     rp.scratch_set_keep_bytes(0)
     rp.scratch_release()
+    assert rp.device_status() == 0
+
+
+@pytest.mark.parametrize("M,N,K,tb", [(2048, 2048, 2048, False), (1536, 1536, 1536, True), (4097, 1024, 3000, False),
+                                      (300, 200, 100, False)])
+def test_gemm_caller_workspace(rp, orc, M, N, K, tb):
+    # repops_gemm_workspace_bytes sizes the automatic plan's scratch (operand
+    # copies, chained-split sums); repops_gemm_f32_ws takes it from the
+    # caller's buffer: the same bits, and nothing from the library's pool
+    L = rp.load()
+    A = inputs.normal((M, K), 1.0, 51, DEV)
+    B = inputs.normal((N, K), 1.0, 52, DEV).t() if tb else inputs.normal((K, N), 1.0, 52, DEV)
+    ldb = B.stride(1) if tb else B.stride(0)
+    need = L.repops_gemm_workspace_bytes(0, int(tb), M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), ldb)
+    if M * N <= 196_608 or 2.0 * M * N * K < 1e9:
+        assert need == 0
+    else:
+        assert need > 0
+    rows = list(range(0, M, max(1, M // 17))) + [M - 1]
+    want = oracle_par.gemm(orc, A, B, rows=rows).view(np.uint32)
+    s = torch.cuda.current_stream().cuda_stream
+    try:
+        rp.scratch_set_keep_bytes(1 << 30)
+        rp.scratch_release()
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=DEV)
+        C = torch.full((M, N), float("nan"), device=DEV)
+        assert L.repops_gemm_f32_ws(0, int(tb), M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), ldb, C.data_ptr(),
+                                    N, ws.data_ptr(), need, s) == 0
+        torch.cuda.synchronize()
+        assert rp.scratch_reserved_bytes() == 0                     # the pool was not used
+        assert np.array_equal(C[rows].cpu().numpy().view(np.uint32), want)
+        C2 = rp.gemm(A, B)                                           # the binding passes a workspace too
+        torch.cuda.synchronize()
+        assert rp.scratch_reserved_bytes() == 0
+        assert torch.equal(C2.view(torch.int32), C.view(torch.int32))
+        if need:
+            # a workspace one byte short is not used: the scratch comes from the pool
+            C3 = torch.full((M, N), float("nan"), device=DEV)
+            assert L.repops_gemm_f32_ws(0, int(tb), M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), ldb,
+                                        C3.data_ptr(), N, ws.data_ptr(), need - 1, s) == 0
+            torch.cuda.synchronize()
+            assert rp.scratch_reserved_bytes() > 0
+            assert torch.equal(C3.view(torch.int32), C.view(torch.int32))
+            # misaligned or overlapping workspaces are refused before any launch
+            assert L.repops_gemm_f32_ws(0, int(tb), M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), ldb,
+                                        C3.data_ptr(), N, ws.data_ptr() + 16, need, s) == -1
+            assert L.repops_gemm_f32_ws(0, int(tb), M, N, K, A.data_ptr(), A.stride(0), B.data_ptr(), ldb,
+                                        C3.data_ptr(), N, C3.data_ptr(), need, s) == -2
+    finally:
+        rp.scratch_set_keep_bytes(0)
+        rp.scratch_release()
     assert rp.device_status() == 0

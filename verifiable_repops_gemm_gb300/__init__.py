@@ -96,10 +96,33 @@ def gemm(A, B, out=None, *, config: int = -1, loader: int = LOADER_AUTO, stream=
             (N > 0 and out.stride(1) != 1):
         raise ValueError("out must be a (M, N) float32 tensor with unit column stride")
     ldc = max(out.stride(0), N, 1)
+    if config < 0 and loader == LOADER_AUTO:
+        # the automatic choice's scratch comes from torch's caching allocator
+        # (repops_gemm_f32_ws), so nothing is mapped afresh after a sync
+        need = L.repops_gemm_workspace_bytes(ta, tb, M, N, K, pa, lda, pb, ldb)
+        ws = _workspace(need, A.device, stream) if need else None
+        if ws is not None:
+            rc = L.repops_gemm_f32_ws(ta, tb, M, N, K, pa, lda, pb, ldb, out.data_ptr(), ldc, ws.data_ptr(),
+                                      need, _stream_handle(stream))
+            _capi.check(rc, "repops_gemm_f32_ws")
+            return out
     rc = L.repops_gemm_f32_config(config, loader, ta, tb, M, N, K, pa, lda, pb, ldb,
                                   out.data_ptr(), ldc, _stream_handle(stream))
     _capi.check(rc, "repops_gemm_f32")
     return out
+
+
+def _workspace(nbytes, device, stream):
+    """A byte buffer from torch's caching allocator for a call on `stream`,
+    kept from reuse until that stream's work is done; None when the stream is
+    a raw handle the allocator cannot track (the library's pool is used)."""
+    import torch
+    if isinstance(stream, int):
+        return None
+    ws = torch.empty(int(nbytes), dtype=torch.uint8, device=device)
+    if stream is not None and stream != torch.cuda.current_stream(device):
+        ws.record_stream(stream)
+    return ws
 
 
 def gemm_chained(A, B, out=None, *, config: int = -1, workers: int = 0, stream=None):

@@ -40,6 +40,9 @@ SIGNATURES = {
     "repops_set_thread_status_word": (_i32, [_vp]),
     "repops_gemm_f32": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "repops_gemm_f32_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
+    "repops_gemm_workspace_bytes": (_u64, [_i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64]),
+    "repops_gemm_f32_ws": (_i32, [_i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp, _u64,
+                                  _vp]),
     "repops_gemm_f32_config": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,
                                       _vp, _i64, _vp]),
     "repops_gemm_f32_chained": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64,

@@ -312,16 +312,24 @@ int launch_repack(const float *src, int64_t ld_src, float *dst, int64_t ld_dst, 
     return check_launch();
 }
 
-// Copies a rows x cols operand (pitch ld) into stream-ordered scratch with a
-// 16-byte pitch: transposed (cols x rows) when `transpose`, else as it is.
-// *out is the scratch (null, and REPOPS_OK, when the allocation is refused:
-// the caller then keeps its operand) and *pitch its row pitch in elements.
-int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool transpose, cudaStream_t stream,
-                 void **out, int64_t *pitch) {
+// Bytes of the copy copy_operand makes of a rows x cols operand.
+uint64_t copy_operand_bytes(int64_t rows, int64_t cols, bool transpose) {
     const int64_t outer = transpose ? cols : rows, inner = transpose ? rows : cols;
+    return uint64_t(outer) * uint64_t((inner + 3) / 4 * 4) * 4u;
+}
+
+// Copies a rows x cols operand (pitch ld) into scratch with a 16-byte pitch:
+// transposed (cols x rows) when `transpose`, else as it is.  The scratch is
+// `pre` (the caller's workspace, copy_operand_bytes bytes) or, when that is
+// null, stream-ordered memory from the pool that the caller releases.  *out
+// is the scratch (null, and REPOPS_OK, when the allocation is refused: the
+// caller then keeps its operand) and *pitch its row pitch in elements.
+int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool transpose, cudaStream_t stream,
+                 void **out, int64_t *pitch, void *pre = nullptr) {
+    const int64_t inner = transpose ? rows : cols;
     const int64_t pm = (inner + 3) / 4 * 4;
-    *out = nullptr;
-    if (scratch_malloc(out, size_t(outer) * size_t(pm) * 4u, stream) != cudaSuccess) {
+    *out = pre;
+    if (!pre && scratch_malloc(out, size_t(copy_operand_bytes(rows, cols, transpose)), stream) != cudaSuccess) {
         cudaGetLastError();   // a refused allocation is not an error here
         *out = nullptr;
         return REPOPS_OK;
@@ -330,7 +338,7 @@ int copy_operand(const float *src, int64_t ld, int64_t rows, int64_t cols, bool 
     const int rc = transpose ? launch_transpose(src, ld, rows, cols, dst, pm, stream)
                              : launch_repack(src, ld, dst, pm, rows, cols, stream);
     if (rc != REPOPS_OK) {
-        cudaFreeAsync(*out, stream);
+        if (!pre) cudaFreeAsync(*out, stream);
         *out = nullptr;
         return rc;
     }
@@ -353,45 +361,68 @@ bool small_output(int64_t M, int64_t N, int64_t K) {
 // >= 0 asks for it with that many workers (0 = every resident CTA slot).
 constexpr int kSkAuto = -1, kSkOff = -2;
 
-// Runs p with the chained k-split on `workers` persistent CTAs of configuration
-// cfg (0 = every resident slot, at most one per tile): stream-ordered scratch
-// for the heads' accumulators and flags, the flags zeroed, the launch, the
-// scratch released.  REPOPS_ERR_UNSUPPORTED when the split cannot run (the
-// caller then runs the one-tile-per-CTA kernel): no TMA, too many workers, or
-// a refused allocation.
-int launch_chained_split(GemmProblem p, int cfg, int workers) {
+// Workers and scratch bytes (the heads' accumulators, then the flags) of a
+// chained k-split of an M x N output on configuration cfg with `req` workers
+// (0 = every resident slot, at most one per tile).  REPOPS_ERR_UNSUPPORTED
+// when it cannot run with that many.
+int chained_split_shape(int64_t M, int64_t N, int cfg, int req, int *workers, uint64_t *bytes) {
     DeviceInfo di;
     int rc = current_device_info(&di);
     if (rc != REPOPS_OK) return rc;
     const GemmConfigInfo ci = config_info(cfg);
-    const int64_t tiles = ((p.M + ci.bm - 1) / ci.bm) * ((p.N + ci.bn - 1) / ci.bn);
+    const int64_t tiles = ((M + ci.bm - 1) / ci.bm) * ((N + ci.bn - 1) / ci.bn);
     const int64_t slots = int64_t(occupancy_of(di.device, cfg)) * di.sms;
-    if (workers == 0) workers = int(std::min<int64_t>(slots, tiles));
-    if (workers < 1 || workers > slots || workers > tiles) return REPOPS_ERR_UNSUPPORTED;
-    const size_t bytes = kSkScratch[cfg](workers);
-    const size_t flag_bytes = size_t(workers) * size_t(ci.threads) * 4u;
-    void *scratch = nullptr;
-    if (scratch_malloc(&scratch, bytes, p.stream) != cudaSuccess) {
+    const int64_t w = req == 0 ? std::min<int64_t>(slots, tiles) : req;
+    if (w < 1 || w > slots || w > tiles) return REPOPS_ERR_UNSUPPORTED;
+    *workers = int(w);
+    *bytes = kSkScratch[cfg](int(w));
+    return REPOPS_OK;
+}
+
+// Runs p with the chained k-split on `workers` persistent CTAs of configuration
+// cfg (0 = every resident slot, at most one per tile): scratch for the heads'
+// accumulators and flags (`pre`, the caller's workspace, or stream-ordered
+// memory from the pool), the flags zeroed, the launch, pool scratch released.
+// REPOPS_ERR_UNSUPPORTED when the split cannot run (the caller then runs the
+// one-tile-per-CTA kernel): no TMA, too many workers, or a refused allocation.
+int launch_chained_split(GemmProblem p, int cfg, int workers, void *pre = nullptr) {
+    uint64_t bytes = 0;
+    int rc = chained_split_shape(p.M, p.N, cfg, workers, &workers, &bytes);
+    if (rc != REPOPS_OK) return rc;
+    const size_t flag_bytes = size_t(workers) * size_t(config_info(cfg).threads) * 4u;
+    void *scratch = pre;
+    if (!pre && scratch_malloc(&scratch, size_t(bytes), p.stream) != cudaSuccess) {
         cudaGetLastError();
         return REPOPS_ERR_UNSUPPORTED;
     }
     cudaError_t e = cudaMemsetAsync(static_cast<unsigned char *>(scratch) + (bytes - flag_bytes), 0, flag_bytes,
                                     p.stream);
     if (e != cudaSuccess) {
-        cudaFreeAsync(scratch, p.stream);
+        if (!pre) cudaFreeAsync(scratch, p.stream);
         return set_cuda_error(e);
     }
     p.sk_workers = workers;
     p.sk_scratch = scratch;
     rc = kLaunch[cfg](p, REPOPS_LOADER_TMA);
-    e = cudaFreeAsync(scratch, p.stream);
-    if (rc == REPOPS_OK && e != cudaSuccess) rc = set_cuda_error(e);
+    if (!pre) {
+        e = cudaFreeAsync(scratch, p.stream);
+        if (rc == REPOPS_OK && e != cudaSuccess) rc = set_cuda_error(e);
+    }
     return rc;
 }
 
+inline uint64_t round_up_256(uint64_t x) { return (x + 255) / 256 * 256; }
+
+// The GEMM's dispatch.  Scratch (operand copies, chained-split accumulators)
+// comes from `ws` (ws_bytes bytes, 256-byte aligned) when it is large enough
+// for the whole plan, else from the pool.  With need_out set nothing is
+// launched: *need_out receives the bytes of scratch the plan takes (0 when it
+// runs on the caller's operands alone), and C is not looked at.
 int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int64_t N, int64_t K,
                   const float *A, int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
-                  cudaStream_t stream, int sk_req = kSkAuto) {
+                  cudaStream_t stream, int sk_req = kSkAuto, void *ws = nullptr, uint64_t ws_bytes = 0,
+                  uint64_t *need_out = nullptr) {
+    if (need_out) *need_out = 0;
     if (M < 0 || N < 0 || K < 0) return REPOPS_ERR_INVALID_ARG;
     if (config < -1 || config >= kGemmConfigCount) return REPOPS_ERR_INVALID_ARG;
     if (loader != REPOPS_LOADER_AUTO && loader != REPOPS_LOADER_TMA && loader != REPOPS_LOADER_CPASYNC &&
@@ -403,16 +434,23 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
         ldc < std::max<int64_t>(1, N))
         return REPOPS_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return REPOPS_OK;
-    if (!C) return REPOPS_ERR_INVALID_ARG;
+    if (!C && !need_out) return REPOPS_ERR_INVALID_ARG;
     if (K > 0 && (!A || !B)) return REPOPS_ERR_INVALID_ARG;
     uint64_t a_bytes = 0, b_bytes = 0, c_bytes = 0;
     if (!operand_span(a_rows, a_cols, lda, &a_bytes) || !operand_span(b_rows, b_cols, ldb, &b_bytes) ||
         !operand_span(M, N, ldc, &c_bytes))
         return REPOPS_ERR_INVALID_ARG;
-    if (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes))
+    if (!need_out && (ranges_overlap(C, c_bytes, A, a_bytes) || ranges_overlap(C, c_bytes, B, b_bytes)))
         return REPOPS_ERR_ALIAS;
+    if (ws && !need_out) {
+        if (reinterpret_cast<uintptr_t>(ws) % 256) return REPOPS_ERR_INVALID_ARG;
+        if (ranges_overlap(ws, ws_bytes, A, a_bytes) || ranges_overlap(ws, ws_bytes, B, b_bytes) ||
+            ranges_overlap(ws, ws_bytes, C, c_bytes))
+            return REPOPS_ERR_ALIAS;
+    }
 
     if (K == 0) {
+        if (need_out) return REPOPS_OK;
         const int64_t total = M * N;
         const int threads = 256;
         const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 65536);
@@ -432,7 +470,7 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     const bool sk_explicit = sk_req >= 0;
     if (!sk_explicit &&
         (loader == REPOPS_LOADER_DIRECT || (loader == REPOPS_LOADER_AUTO && config < 0 && small_output(M, N, K))))
-        return gemm_small_launch(p);
+        return need_out ? REPOPS_OK : gemm_small_launch(p);
 
     bool sk_auto = false;
     const int cfg = config >= 0 ? config
@@ -459,17 +497,43 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     const double flops = 2.0 * double(M) * double(N) * double(K);
     const bool large = loader == REPOPS_LOADER_AUTO && flops >= kRepackMinFlops;
     const bool transpose_b = loader == REPOPS_LOADER_AUTO && p.transB && flops >= kTransposeBMinFlops;
+    const bool copy_b = transpose_b || (large && !operand_tma_ready(p.B, p.ldb));
+    const bool copy_a = large && (!p.transA || !operand_tma_ready(p.A, p.lda));
+    // The plan's scratch: the copies (A M-inner, B N-inner, 16-byte pitches),
+    // then the chained split's accumulators when it runs on those operands.
+    const uint64_t need_a = copy_a ? copy_operand_bytes(K, M, false) : 0;
+    const uint64_t need_b = copy_b ? copy_operand_bytes(K, N, false) : 0;
+    uint64_t need_sk = 0;
+    if (want_sk && loader != REPOPS_LOADER_CPASYNC) {
+        GemmProblem q = p;   // the operands as the kernels will see them (any 16-byte aligned base)
+        const float *aligned = reinterpret_cast<const float *>(uintptr_t(256));
+        if (copy_a) { q.A = aligned; q.lda = (M + 3) / 4 * 4; q.transA = 1; }
+        if (copy_b) { q.B = aligned; q.ldb = (N + 3) / 4 * 4; q.transB = 0; }
+        int workers = 0;
+        if (!gemm_tma_eligible(q) ||
+            chained_split_shape(M, N, cfg, sk_explicit ? sk_req : 0, &workers, &need_sk) != REPOPS_OK)
+            need_sk = 0;
+    }
+    const uint64_t need = round_up_256(need_a) + round_up_256(need_b) + round_up_256(need_sk);
+    if (need_out) {
+        *need_out = need;
+        return REPOPS_OK;
+    }
+    // carved from the caller's workspace when it holds the whole plan
+    unsigned char *wsp = (ws && need > 0 && ws_bytes >= need) ? static_cast<unsigned char *>(ws) : nullptr;
+    void *pre_a = wsp, *pre_b = wsp ? wsp + round_up_256(need_a) : nullptr;
+    void *pre_sk = wsp ? wsp + round_up_256(need_a) + round_up_256(need_b) : nullptr;
     void *bscratch = nullptr, *ascratch = nullptr;
     auto fail = [&](int code) {
-        for (void *m : {bscratch, ascratch})
-            if (m) cudaFreeAsync(m, stream);
+        if (bscratch && !pre_b) cudaFreeAsync(bscratch, stream);
+        if (ascratch && !pre_a) cudaFreeAsync(ascratch, stream);
         return code;
     };
-    if (transpose_b || (large && !operand_tma_ready(p.B, p.ldb))) {
+    if (copy_b) {
         // B stored transposed (N x K) is transposed, an unaligned row-major B repacked
         int64_t pitch = 0;
-        rc = p.transB ? copy_operand(B, ldb, N, K, true, stream, &bscratch, &pitch)
-                      : copy_operand(B, ldb, K, N, false, stream, &bscratch, &pitch);
+        rc = p.transB ? copy_operand(B, ldb, N, K, true, stream, &bscratch, &pitch, pre_b)
+                      : copy_operand(B, ldb, K, N, false, stream, &bscratch, &pitch, pre_b);
         if (rc != REPOPS_OK) return fail(rc);
         if (bscratch) {
             p.B = static_cast<const float *>(bscratch);
@@ -479,11 +543,11 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
             p.span_b[1] = p.span_b[0] + uint64_t(K) * uint64_t(pitch) * 4u;
         }
     }
-    if (large && (!p.transA || !operand_tma_ready(p.A, p.lda))) {
+    if (copy_a) {
         // a K-inner A (M x K) is transposed, an unaligned M-inner A (K x M) repacked
         int64_t pitch = 0;
-        rc = p.transA ? copy_operand(A, lda, K, M, false, stream, &ascratch, &pitch)
-                      : copy_operand(A, lda, M, K, true, stream, &ascratch, &pitch);
+        rc = p.transA ? copy_operand(A, lda, K, M, false, stream, &ascratch, &pitch, pre_a)
+                      : copy_operand(A, lda, M, K, true, stream, &ascratch, &pitch, pre_a);
         if (rc != REPOPS_OK) return fail(rc);
         if (ascratch) {
             p.A = static_cast<const float *>(ascratch);
@@ -497,7 +561,7 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
     const int use = (loader == REPOPS_LOADER_CPASYNC || !tma_ok) ? REPOPS_LOADER_CPASYNC : REPOPS_LOADER_TMA;
     rc = REPOPS_ERR_UNSUPPORTED;
     if (want_sk && use == REPOPS_LOADER_TMA) {
-        rc = launch_chained_split(p, cfg, sk_explicit ? sk_req : 0);
+        rc = launch_chained_split(p, cfg, sk_explicit ? sk_req : 0, need_sk ? pre_sk : nullptr);
         if (rc == REPOPS_ERR_UNSUPPORTED && sk_explicit) return fail(rc);
     }
     if (rc == REPOPS_ERR_UNSUPPORTED) rc = kLaunch[cfg](p, use);
@@ -509,7 +573,7 @@ int gemm_dispatch(int config, int loader, int transA, int transB, int64_t M, int
         set_spans(p, a_bytes, b_bytes, c_bytes);
         rc = kLaunch[cfg](p, REPOPS_LOADER_CPASYNC);
     }
-    for (void *m : {bscratch, ascratch}) {
+    for (void *m : {bscratch != pre_b ? bscratch : nullptr, ascratch != pre_a ? ascratch : nullptr}) {
         if (!m) continue;
         cudaError_t e = cudaFreeAsync(m, stream);
         if (e != cudaSuccess && rc == REPOPS_OK) rc = set_cuda_error(e);
@@ -698,6 +762,24 @@ extern "C" int repops_gemm_f32(int64_t M, int64_t N, int64_t K, const float *A, 
                                const float *B, int64_t ldb, float *C, int64_t ldc,
                                cudaStream_t stream) {
     return gemm_dispatch(-1, REPOPS_LOADER_AUTO, 0, 0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+extern "C" uint64_t repops_gemm_workspace_bytes(int transA, int transB, int64_t M, int64_t N, int64_t K,
+                                                const float *A, int64_t lda, const float *B, int64_t ldb) {
+    uint64_t need = 0;
+    const int64_t ldc = std::max<int64_t>(N, 1);
+    if (gemm_dispatch(-1, REPOPS_LOADER_AUTO, transA, transB, M, N, K, A, lda, B, ldb, nullptr, ldc, nullptr,
+                      kSkAuto, nullptr, 0, &need) != REPOPS_OK)
+        return 0;
+    return need;
+}
+
+extern "C" int repops_gemm_f32_ws(int transA, int transB, int64_t M, int64_t N, int64_t K, const float *A,
+                                  int64_t lda, const float *B, int64_t ldb, float *C, int64_t ldc,
+                                  void *workspace, uint64_t workspace_bytes, cudaStream_t stream) {
+    if (!workspace && workspace_bytes) return REPOPS_ERR_INVALID_ARG;
+    return gemm_dispatch(-1, REPOPS_LOADER_AUTO, transA, transB, M, N, K, A, lda, B, ldb, C, ldc, stream,
+                         kSkAuto, workspace, workspace_bytes);
 }
 
 extern "C" int repops_gemm_f32_ex(int transA, int transB, int64_t M, int64_t N, int64_t K,
