@@ -8,9 +8,10 @@ elements, float32, binary16 or bfloat16 gradients, each gradient and theta at
 a random element offset (so most are not 16-byte aligned), a random fold
 order and step size, on the device or from host buffers.  Merkle: 1 byte to
 6 MiB at a random byte offset, leaves of 64 bytes to 64 KiB, through the
-allocating call, a caller workspace, the allocation-free call, the stored
-tree and the host-buffer call.  Every theta element and every root byte must
-equal the oracle's.
+allocating call (pool scratch), a caller workspace, the binding (a workspace
+from torch's caching allocator), the allocation-free call, the stored tree
+and the host-buffer call.  Every theta element and every root byte must equal
+the oracle's.
 """
 import numpy as np
 import pytest
@@ -79,8 +80,14 @@ def test_random_merkle_case_matches_oracle(rp, orc, case):
     buf = torch.randint(0, 256, (off + nbytes + 16,), generator=g, dtype=torch.uint8, device=DEV)
     data = buf[off:off + nbytes]
     want = orc.merkle_root(data.cpu().numpy(), leaf)
-    path = ["device", "workspace", "noalloc", "tree", "host"][case % 5]
+    path = ["device", "workspace", "noalloc", "tree", "host", "binding"][case % 6]
     if path == "device":
+        # the C entry point itself: scratch from the library's pool
+        root = torch.empty(32, dtype=torch.uint8, device=DEV)
+        rc = rp.load().repops_merkle_sha256(data.data_ptr(), nbytes, leaf, root.data_ptr(),
+                                            torch.cuda.current_stream().cuda_stream)
+        assert rc == 0, rc
+    elif path == "binding":
         root = rp.merkle_sha256(data, leaf)
     elif path == "workspace":
         need = rp.merkle_workspace_bytes(nbytes, leaf)

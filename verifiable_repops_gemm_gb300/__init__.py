@@ -420,7 +420,8 @@ def merkle_sha256(t, leaf: int = 4096, out=None, *, nbytes: int = None, workspac
 
     t: a contiguous CUDA tensor; its storage bytes are hashed as stored.
     nbytes: hash only the first nbytes bytes.  workspace: optional uint8 CUDA
-    tensor used as scratch instead of a stream-ordered allocation."""
+    tensor used as scratch; by default one comes from torch's caching
+    allocator (the library's pool when `stream` is a raw handle)."""
     import torch
     L = load()
     if not t.is_cuda or not t.is_contiguous():
@@ -429,6 +430,11 @@ def merkle_sha256(t, leaf: int = 4096, out=None, *, nbytes: int = None, workspac
     if out is None:
         out = torch.empty(32, dtype=torch.uint8, device=t.device)
     s = _stream_handle(stream)
+    if workspace is None:
+        # the level scratch from torch's caching allocator where it can follow
+        # the stream (repops_merkle_sha256_ws), else from the library's pool
+        need = L.repops_merkle_workspace_bytes(n, leaf)
+        workspace = _workspace(max(need, 16), t.device, stream) if need else None
     if workspace is None:
         rc = L.repops_merkle_sha256(t.data_ptr(), n, leaf, out.data_ptr(), s)
     else:
