@@ -6,7 +6,8 @@
  * expected results are closed forms computed here:
  *   - GEMM ("Verde与RepOps" §3.2): C[i][j] = sum_k A[i][k] * B[k][j] over a
  *     ragged 300 x 200 x 777 problem, |sum| < 2^24, with B row-major and
- *     stored transposed;
+ *     stored transposed, and a 1100 x 1000 x 600 one whose scratch (the
+ *     transposed B copied) comes from a caller workspace;
  *   - mean + SGD ("Zoo Per-LLM Chain Soundness" §5): four contributors (the
  *     divide by 4 is exact), eta = 1/16, in the order repops_sort_ids gives
  *     for four DIDs of different lengths;
@@ -91,6 +92,39 @@ int main(void) {
     CUDA_OK(cudaMemcpyAsync(hC, dC, sizeof(float) * M * N, cudaMemcpyDeviceToHost, s));
     CUDA_OK(cudaStreamSynchronize(s));
     if (check_gemm(hC, M, N, K, "repops_gemm_f32_ex (B transposed)")) return 1;
+
+    /* a larger product with B stored transposed: its scratch (B copied into the
+     * kernels' row-major layout) from a workspace of the caller's */
+    {
+        const int64_t M2 = 1100, N2 = 1000, K2 = 600;
+        float *hA2 = malloc(sizeof(float) * M2 * K2), *hBt2 = malloc(sizeof(float) * N2 * K2);
+        float *hC2 = malloc(sizeof(float) * M2 * N2);
+        if (!hA2 || !hBt2 || !hC2) return 1;
+        for (int64_t i = 0; i < M2; ++i)
+            for (int64_t k = 0; k < K2; ++k) hA2[i * K2 + k] = val(i, k, 1);
+        for (int64_t j = 0; j < N2; ++j)
+            for (int64_t k = 0; k < K2; ++k) hBt2[j * K2 + k] = val(k, j, 2);
+        float *dA2, *dBt2, *dC2;
+        void *ws;
+        CUDA_OK(cudaMalloc((void **)&dA2, sizeof(float) * M2 * K2));
+        CUDA_OK(cudaMalloc((void **)&dBt2, sizeof(float) * N2 * K2));
+        CUDA_OK(cudaMalloc((void **)&dC2, sizeof(float) * M2 * N2));
+        CUDA_OK(cudaMemcpy(dA2, hA2, sizeof(float) * M2 * K2, cudaMemcpyHostToDevice));
+        CUDA_OK(cudaMemcpy(dBt2, hBt2, sizeof(float) * N2 * K2, cudaMemcpyHostToDevice));
+        const uint64_t need = repops_gemm_workspace_bytes(0, 1, M2, N2, K2, dA2, K2, dBt2, K2);
+        if (need == 0) {
+            printf("repops_gemm_workspace_bytes: 0 for a transposed B of %lld GFLOP\n",
+                   (long long)(2 * M2 * N2 * K2 / 1000000000));
+            return 1;
+        }
+        CUDA_OK(cudaMalloc(&ws, need));
+        REPOPS_OK_(repops_gemm_f32_ws(0, 1, M2, N2, K2, dA2, K2, dBt2, K2, dC2, N2, ws, need, s));
+        CUDA_OK(cudaMemcpyAsync(hC2, dC2, sizeof(float) * M2 * N2, cudaMemcpyDeviceToHost, s));
+        CUDA_OK(cudaStreamSynchronize(s));
+        if (check_gemm(hC2, M2, N2, K2, "repops_gemm_f32_ws (B transposed)")) return 1;
+        cudaFree(dA2); cudaFree(dBt2); cudaFree(dC2); cudaFree(ws);
+        free(hA2); free(hBt2); free(hC2);
+    }
 
     /* contributor order: DIDs compared as unsigned bytes, a proper prefix first */
     const uint8_t ids[] = {0xb0, 0x01, /* 0: b0 01 */ 0x7f, /* 1: 7f */ 0xb0, /* 2: b0 */ 0x80, 0x00 /* 3: 80 00 */};
