@@ -168,18 +168,21 @@ def sha_compressions(nbytes, leaf=4096):
 
 
 class Workload:
-    def __init__(self, dev):
+    def __init__(self, dev, tile=-1, seed=0):
+        # tile: the GEMM's tile configuration (-1: the automatic choice); seed:
+        # added to every input seed (0: the seeds the roots below are quoted for)
         n = GEMM_N
         idx = inputs.SQUARE_SWEEP.index(n)
-        self.A = inputs.normal((n, n), 1.0, 10 + idx, dev)
-        self.B = inputs.normal((n, n), 1.0, 20 + idx, dev)
+        self.tile = tile
+        self.A = inputs.normal((n, n), 1.0, 10 + idx + seed, dev)
+        self.B = inputs.normal((n, n), 1.0, 20 + idx + seed, dev)
         self.C = torch.empty((n, n), dtype=torch.float32, device=dev)
         nC, ln = inputs.MEAN_CONTRIBUTORS, inputs.MEAN_LEN
-        self.grads = [inputs.normal((ln,), 1e-2, 200 + r, dev) for r in range(nC)]
-        self.theta = inputs.normal((ln,), 0.02, 199, dev)
-        self.order = rp.sort_ids(inputs.contributor_ids(nC, 200))
+        self.grads = [inputs.normal((ln,), 1e-2, 200 + r + seed, dev) for r in range(nC)]
+        self.theta = inputs.normal((ln,), 0.02, 199 + seed, dev)
+        self.order = rp.sort_ids(inputs.contributor_ids(nC, 200 + seed))
         self.eta = 1e-3
-        self.T = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300, dev)
+        self.T = inputs.normal((inputs.MERKLE_ELEMS,), 0.02, 300 + seed, dev)
         self.tbytes = self.T.numel() * 4
         self.cbytes = self.C.numel() * 4
         ws = max(rp.merkle_workspace_bytes(self.tbytes), rp.merkle_workspace_bytes(self.cbytes), 16)
@@ -194,7 +197,7 @@ class Workload:
 
     def step(self, s, ev=None):
         if ev: ev[0].record(s)
-        rp.gemm(self.A, self.B, out=self.C, stream=s)
+        rp.gemm(self.A, self.B, out=self.C, config=self.tile, stream=s)
         if ev: ev[1].record(s)
         rp.fixed_order_mean_sgd(self.grads, self.order, self.eta, self.theta, stream=s)
         if ev: ev[2].record(s)
@@ -504,7 +507,7 @@ def run_ours(args):
     rp.load()
     peaks, peaks_kind = measured_peaks()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    w = Workload(dev)
+    w = Workload(dev, args.tile, args.seed)
     s = torch.cuda.Stream(device=dev)
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(s):
@@ -577,7 +580,8 @@ def run_ours(args):
         "config": {"workload": "order-fixed fp32 GEMM 8192^3 (A,B ~ N(0,1)) + fixed-order mean/SGD "
                                "16 x 2^28 + SHA-256 Merkle of 4 GiB and of C, 4096-B leaves",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (129 MB); no flush"},
+                   "l2": "inputs larger than L2 (129 MB); no flush",
+                   "gemm_tile": "automatic" if args.tile < 0 else args.tile, "seed_offset": args.seed},
         "parts": {
             "gemm": {"value": value, "unit": "TFLOP/s", "ms": statistics.mean(gemm_ms)},
             "mean_sgd": {"value": mean_gbs, "unit": "GB/s", "ms": statistics.mean(mean_ms),
@@ -663,7 +667,63 @@ def run_sweep(args):
         run_decoder_step(dev, s, peak)
 
 
-def run_sweep_gemm(dev, s, flush, peak):
+def run_config(c):
+    """One workload configuration: one JSON line per workload, with the Merkle
+    roots of the GEMM outputs (configurations 0 and 1) and of theta after the
+    update (3); 4 times the 4 GiB commitment and prints the roots of the
+    square-sweep outputs (the same for both B layouts)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    rp.load()
+    peaks, _ = measured_peaks()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * FP32_LANES_PER_SM * peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL) * 1e6 / 1e12
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    if c in (0, 1, 2):
+        run_sweep_gemm(dev, s, flush, peak, parts=(c,), roots=c in (0, 1))
+        return
+    w = Workload(dev)
+
+    def timed(fn, reps=10):
+        with torch.cuda.stream(s):
+            fn()
+            evs = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                fn()
+                e1.record(s)
+                evs.append((e0, e1))
+        torch.cuda.synchronize(dev)
+        return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    if c == 3:
+        reps = 10
+        ms = timed(lambda: rp.fixed_order_mean_sgd(w.grads, w.order, w.eta, w.theta, stream=s), reps)
+        gbs = w.mean_bytes / ms / 1e6
+        print(json.dumps({"config": 3, "workload": "fixed-order mean + SGD, 16 contributors x 2^28 (inputs above "
+                          "L2)", "ms": ms, "gbs": gbs, "frac_of_measured_hbm": gbs / hbm,
+                          "theta_updates": reps + 1, "theta_root": bytes(rp.merkle_sha256(w.theta).cpu().numpy()).hex()}),
+              flush=True)
+        return
+    ms = timed(lambda: rp.merkle_sha256(w.T, 4096, out=w.root_T, workspace=w.ws, stream=s))
+    print(json.dumps({"config": 4, "workload": "SHA-256 Merkle root of 2^30 fp32 (4 GiB), 4096-byte leaves",
+                      "ms": ms, "gbs": w.tbytes / ms / 1e6,
+                      "root": bytes(w.root_T.cpu().numpy()).hex()}), flush=True)
+    del w
+    for i, n in enumerate(inputs.SQUARE_SWEEP):
+        A = inputs.normal((n, n), 1.0, 10 + i, dev)
+        B = inputs.normal((n, n), 1.0, 20 + i, dev)
+        r1 = bytes(rp.merkle_sha256(rp.gemm(A, B)).cpu().numpy()).hex()
+        r2 = bytes(rp.merkle_sha256(rp.gemm(A, B.t().contiguous().t())).cpu().numpy()).hex()
+        print(json.dumps({"config": 4, "workload": "Merkle root of the %d^3 GEMM output" % n, "root": r1,
+                          "same_for_column_major_B": r1 == r2}), flush=True)
+        del A, B
+
+
+def run_sweep_gemm(dev, s, flush, peak, parts=(0, 1, 2), roots=False):
     """Every GEMM workload, L2 flushed before each timed launch, the median of
     at least 10 launches.  Beside each,
     the library's FP32 GEMM (torch.mm on cuBLAS, TF32 off: fused multiply-adds,
@@ -715,19 +775,28 @@ def run_sweep_gemm(dev, s, flush, peak):
         print(json.dumps(rec), flush=True)
         return flops, ms
 
-    A = inputs.uniform_pm1((256, 256), 0, dev)
-    B = inputs.uniform_pm1((256, 256), 1, dev)
-    emit("gemm 256^3 U[-1,1)", A, B)
-    for i, n in enumerate(inputs.SQUARE_SWEEP):
-        A = inputs.normal((n, n), 1.0, 10 + i, dev)
-        B = inputs.normal((n, n), 1.0, 20 + i, dev)
-        emit("gemm %d^3 B row-major" % n, A, B)
-        emit("gemm %d^3 B column-major" % n, A, B.t().contiguous().t())
-        del A, B
-    M, N, K = inputs.RAGGED
-    A = inputs.normal((M, K), 1.0, 30, dev)
-    B = inputs.normal((K, N), 1.0, 31, dev)
-    emit("gemm ragged 4097x1023x3001 (lda = 3001: operands repacked to a 16-byte pitch)", A, B)
+    def root(A, B):
+        # the Merkle root of the output (the same bits for every layout)
+        return {"C_root": bytes(rp.merkle_sha256(rp.gemm(A, B)).cpu().numpy()).hex()} if roots else None
+
+    if 0 in parts:
+        A = inputs.uniform_pm1((256, 256), 0, dev)
+        B = inputs.uniform_pm1((256, 256), 1, dev)
+        emit("gemm 256^3 U[-1,1)", A, B, root(A, B))
+    if 1 in parts:
+        for i, n in enumerate(inputs.SQUARE_SWEEP):
+            A = inputs.normal((n, n), 1.0, 10 + i, dev)
+            B = inputs.normal((n, n), 1.0, 20 + i, dev)
+            emit("gemm %d^3 B row-major" % n, A, B, root(A, B))
+            Bc = B.t().contiguous().t()
+            emit("gemm %d^3 B column-major" % n, A, Bc, root(A, Bc))
+            del A, B, Bc
+        M, N, K = inputs.RAGGED
+        A = inputs.normal((M, K), 1.0, 30, dev)
+        B = inputs.normal((K, N), 1.0, 31, dev)
+        emit("gemm ragged 4097x1023x3001 (lda = 3001: operands repacked to a 16-byte pitch)", A, B, root(A, B))
+    if 2 not in parts:
+        return
     T, D = inputs.DECODER_TOKENS, inputs.DECODER_DIM
     X = inputs.normal((T, D), 1.0, 100, dev)
     tot_f = tot_ms = 0.0
@@ -1185,8 +1254,18 @@ def main():
                     help="three launches of one automatic-choice GEMM (for a profiler)")
     ap.add_argument("--attention-once", action="store_true",
                     help="three passes of one sequence's unfused attention kernels (for a profiler)")
+    ap.add_argument("--config", type=int, choices=range(5), default=None,
+                    help="one JSON line per workload of one of the five workload configurations: 0 the "
+                         "256^3 GEMM, 1 the square sweep and the ragged GEMM, 2 the decoder GEMM set, 3 the "
+                         "mean + SGD, 4 the Merkle commitments")
+    ap.add_argument("--tile", type=int, default=-1,
+                    help="the step's GEMM tile configuration (default -1: the automatic choice); the "
+                         "commitments are the same for every one")
+    ap.add_argument("--seed", type=int, default=0, help="added to every input seed of the step")
     args = ap.parse_args()
-    if args.attention_once:
+    if args.config is not None:
+        run_config(args.config)
+    elif args.attention_once:
         run_attention_once()
     elif args.gemm_once:
         run_gemm_once(args.gemm_once)
