@@ -62,7 +62,9 @@ __device__ __forceinline__ uint32_t rotr(uint32_t x, int n) { return __funnelshi
 // together with the 16-round loop body below.  Moving more there is slower:
 // the schedule's shifts as high halves of products 1008 -> 1020 GB/s when
 // taken back to the ALU, a rotate of a sigma as two products -3%, a
-// three-input sum as one ALU add instead of two multiply-adds -1 to -4%.)
+// three-input sum as one ALU add instead of two multiply-adds -1 to -4%, two
+// rotates of each Sigma as the two halves of one 64-bit product each (one
+// ALU operation fewer per Sigma) -18%.)
 struct PipeConst {
     uint32_t one;     // 1
 };
