@@ -87,6 +87,13 @@ inline DbgSpan dbg_span(const void *p, uint64_t bytes) {
     return s;
 }
 
+// Bytes of dynamic shared memory this launch was given.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t v;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+    return v;
+}
+
 #ifdef REPOPS_DEBUG_BOUNDS
 __device__ __forceinline__ bool dbg_in(const DbgSpan &s, const void *p, uint32_t n, unsigned *status) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
@@ -94,9 +101,19 @@ __device__ __forceinline__ bool dbg_in(const DbgSpan &s, const void *p, uint32_t
     if (status) atomicOr(status, 2u);
     return false;
 }
+// A kernel whose shared-memory need depends on its arguments tests, on entry,
+// that the launch gave it that many bytes; if not, it does nothing and sets
+// bit 1 of the status word (the same for every thread: no barrier is split).
+__device__ __forceinline__ bool dbg_smem(uint64_t need, unsigned *status) {
+    if (need <= dynamic_smem_bytes()) return true;
+    if (status && threadIdx.x == 0) atomicOr(status, 2u);
+    return false;
+}
 #define REPOPS_DBG_OK(span, p, n, status) ::repops::dbg_in((span), (p), (n), (status))
+#define REPOPS_DBG_SMEM_OK(need, status) ::repops::dbg_smem((need), (status))
 #else
 #define REPOPS_DBG_OK(span, p, n, status) true
+#define REPOPS_DBG_SMEM_OK(need, status) true
 #endif
 
 // Limit for every device-side wait, in nanoseconds of %globaltimer.

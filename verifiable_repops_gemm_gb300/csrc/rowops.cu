@@ -466,8 +466,9 @@ __device__ __forceinline__ float fold_run(const float *run, int u, int len) {
 
 __global__ void __launch_bounds__(32 * WARP_CAUSAL_WARPS)
 softmax_causal_warp_kernel(int64_t rows, int n, const float *__restrict__ x, int64_t ldx, float *__restrict__ y,
-                           int64_t ldy, int64_t first, int64_t period, int row_floats) {
+                           int64_t ldy, int64_t first, int64_t period, int row_floats, unsigned *status) {
     extern __shared__ float4 wc_smem4[];
+    if (!REPOPS_DBG_SMEM_OK(uint64_t(WARP_CAUSAL_WARPS) * row_floats * sizeof(float), status)) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float *stage = reinterpret_cast<float *>(wc_smem4) + warp * row_floats;
     const int64_t gw = int64_t(blockIdx.x) * WARP_CAUSAL_WARPS + warp;
@@ -631,10 +632,11 @@ struct SquareShift {
 __global__ void __launch_bounds__(256)
 rows_generic_kernel(int kind, int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
                     const float *__restrict__ gamma, const float *__restrict__ beta, float eps,
-                    float *__restrict__ y, int64_t ldy, int64_t first, int64_t period) {
+                    float *__restrict__ y, int64_t ldy, int64_t first, int64_t period, unsigned *status) {
     extern __shared__ float buf[];   // runs + ceil(runs / 32) floats
     __shared__ float bcast;
     const int runs = int((n + RUN - 1) / RUN);
+    if (!REPOPS_DBG_SMEM_OK(uint64_t(runs + (runs + RUN - 1) / RUN) * sizeof(float), status)) return;
     float *buf2 = buf + runs;
     const float nf = float(n);
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
@@ -749,8 +751,12 @@ __global__ void __launch_bounds__(256)
 rmsnorm_backward_kernel(int64_t rows, int64_t n, const float *__restrict__ x, int64_t ldx,
                         const float *__restrict__ gamma, float eps, const float *__restrict__ dy, int64_t lddy,
                         const float *res, int64_t ldres, float *dx, int64_t lddx, float *__restrict__ p,
-                        int64_t ldp) {
+                        int64_t ldp, unsigned *status) {
     extern __shared__ float buf[];
+    {
+        const int64_t runs = (n + RUN - 1) / RUN;
+        if (!REPOPS_DBG_SMEM_OK(uint64_t(runs + (runs + RUN - 1) / RUN) * sizeof(float), status)) return;
+    }
     __shared__ float bcast;
     const int runs = int((n + RUN - 1) / RUN);
     float *buf2 = buf + runs;
@@ -863,10 +869,11 @@ __device__ __forceinline__ int64_t causal_prefix(int64_t r, int64_t n, int64_t f
 // elements it read in the same pass, so ds may be dp or p.
 __global__ void __launch_bounds__(256)
 softmax_backward_kernel(int64_t rows, int64_t n, const float *p, int64_t ldp, const float *dp, int64_t lddp,
-                        float *ds, int64_t ldds, int64_t first, int64_t period) {
+                        float *ds, int64_t ldds, int64_t first, int64_t period, unsigned *status) {
     extern __shared__ float buf[];
     __shared__ float bcast;
     const int runs = int((n + RUN - 1) / RUN);
+    if (!REPOPS_DBG_SMEM_OK(uint64_t(runs + (runs + RUN - 1) / RUN) * sizeof(float), status)) return;
     float *buf2 = buf + runs;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const float *pr = p + r * ldp, *gr = dp + r * lddp;
@@ -1023,8 +1030,11 @@ int run_rows(int kind, int64_t rows, int64_t n, const float *x, int64_t ldx, con
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(rows_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
+    unsigned *status = nullptr;
+    int rc = status_word_address(&status);
+    if (rc != REPOPS_OK) return rc;
     rows_generic_kernel<<<grid_for_rows(rows), 256, smem, s>>>(kind, rows, n, x, ldx, gamma, beta, eps, y, ldy,
-                                                               first, period);
+                                                               first, period, status);
     return check_launch();
 }
 
@@ -1049,9 +1059,11 @@ extern "C" int repops_softmax_rows_causal_f32(int64_t rows, int64_t cols, const 
     if (first < cols && cols <= WARP_CAUSAL_MAX_COLS && rows_vec_ok(x, ldx, y, ldy)) {
         const int row_floats = int((cols + RUN - 1) / RUN * RUN);
         const size_t smem = size_t(WARP_CAUSAL_WARPS) * row_floats * sizeof(float);
+        unsigned *status = nullptr;
+        if ((rc = status_word_address(&status)) != REPOPS_OK) return rc;
         return launch_persistent(softmax_causal_warp_kernel, 32 * WARP_CAUSAL_WARPS, smem,
                                  (rows + WARP_CAUSAL_WARPS - 1) / WARP_CAUSAL_WARPS, stream, rows, int(cols), x, ldx,
-                                 y, ldy, first, period, row_floats);
+                                 y, ldy, first, period, row_floats, status);
     }
     return run_rows(0, rows, cols, x, ldx, nullptr, nullptr, 0.0f, y, ldy, stream, first < cols ? first : -1,
                     period);
@@ -1165,8 +1177,10 @@ extern "C" int repops_rmsnorm_backward_f32(int64_t rows, int64_t cols, const flo
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(rmsnorm_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
+    unsigned *status = nullptr;
+    if (status_word_address(&status) != REPOPS_OK) status = nullptr;
     rmsnorm_backward_kernel<<<grid_for_rows(rows), 256, smem, stream>>>(rows, cols, x, ldx, gamma, eps, dy, lddy, res,
-                                                                         ldres, dx, lddx, dyxh, ldp);
+                                                                         ldres, dx, lddx, dyxh, ldp, status);
     return check_launch();
 }
 
@@ -1198,8 +1212,10 @@ int softmax_backward(int64_t rows, int64_t cols, const float *p, int64_t ldp, co
     const size_t smem = size_t(runs + (runs + RUN - 1) / RUN) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(softmax_backward_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return set_cuda_error(e);
+    unsigned *status = nullptr;
+    if (status_word_address(&status) != REPOPS_OK) status = nullptr;
     softmax_backward_kernel<<<grid_for_rows(rows), 256, smem, stream>>>(rows, cols, p, ldp, dp, lddp, ds, ldds,
-                                                                        first, period);
+                                                                        first, period, status);
     return check_launch();
 }
 }  // namespace
