@@ -15,6 +15,13 @@ same workload), printing the same JSON line with "impl": "reference".
 Multi-GPU (torchrun): every rank runs the same workload on its own GPU
 (replicas, weak scaling); ranks share only a barrier and a max-reduction of
 the elapsed time -- the path has no exchange step.
+
+Other modes: `--sweep [part]` times every workload of a part (one JSON line
+each); `--config N` runs one of the five workload configurations with the
+Merkle roots of its results; `--tile c` / `--seed s` run the step with the
+GEMM on tile configuration c (the roots do not change) or with shifted input
+seeds; `--gemm-once` / `--attention-once` launch one GEMM or one sequence's
+attention kernels a few times, for a profiler.
 """
 import argparse
 import hashlib
