@@ -65,8 +65,8 @@ HBM_SPEC_GBS = 7900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
 # the kernel source it was taken on (sha256 of gemm_kernels.cuh).
-GEMM_TRAFFIC = {"src_sha256": "0618417c046709d7083f63c493debdd10f14a7ade4fc940a7a40feaf6eb746e1",
-                "bytes_per_launch": 3754447616 + 265766400}
+GEMM_TRAFFIC = {"src_sha256": "a18f733c4b730ab375a6ca15bf294ac6f4821df7e42a730824418dbbe26ae9fe",
+                "bytes_per_launch": 3748467200 + 265021184}
 
 
 def measured_peaks():

@@ -112,6 +112,14 @@ int repops_set_thread_status_word(unsigned *word);
  * the GPU context stays usable.  Nothing else is read or written. */
 int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t stream);
 
+/* The same for the other kind of bounded wait: one kernel thread polls, as a
+ * chained-split worker does for the previous worker's partial sums (acquire
+ * loads with short sleeps), a flag word that nothing sets, gives up after
+ * limit_ns (1 .. 2e9, else INVALID_ARG) and sets the status word: the next
+ * repops_device_status reports REPOPS_ERR_TIMEOUT and the context stays
+ * usable.  Nothing else is read or written. */
+int repops_selftest_bounded_flag_wait(int64_t limit_ns, cudaStream_t stream);
+
 /* Scratch memory.  Entry points that need device scratch (operand copies and
  * chained-split partial sums of the GEMM, Merkle level nodes, the staging
  * buffers of the host-buffer calls, ...) allocate it stream-ordered, on the

@@ -351,6 +351,8 @@ def test_llama_operators_reject_bad_arguments(L):
 def test_selftest_rejects_bad_limits(L):
     assert L.repops_selftest_bounded_wait(0, None) == -1
     assert L.repops_selftest_bounded_wait(3_000_000_000, None) == -1
+    assert L.repops_selftest_bounded_flag_wait(0, None) == -1
+    assert L.repops_selftest_bounded_flag_wait(3_000_000_000, None) == -1
 
 
 def test_added_entry_points_reject_bad_arguments(L):

@@ -1,8 +1,9 @@
 """Failure detection on the GPU without a fault: a kernel's bounded wait on
-an mbarrier phase that nothing completes gives up after its limit, sets the
-library's sticky status word, and the host reads REPOPS_ERR_TIMEOUT from it;
-the context stays usable (the next GEMM is bit-exact and the status clean).
-No trap, no assert, no bad address: the wait simply runs out."""
+an mbarrier phase that nothing completes, or on a flag word that nothing
+sets, gives up after its limit, sets the library's sticky status word, and
+the host reads REPOPS_ERR_TIMEOUT from it; the context stays usable (the next
+GEMM is bit-exact and the status clean).  No trap, no assert, no bad
+address: the wait simply runs out."""
 import numpy as np
 import pytest
 import torch
@@ -26,6 +27,26 @@ def test_bounded_wait_times_out_and_the_context_survives(rp, orc):
     A = inputs.normal((130, 70), 1.0, 1, DEV)
     B = inputs.normal((70, 90), 1.0, 2, DEV)
     C = rp.gemm(A, B)
+    want = orc.gemm(A.cpu().numpy(), B.cpu().numpy())
+    assert np.array_equal(C.cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert rp.device_status() == 0
+
+
+def test_flag_wait_times_out_and_the_context_survives(rp, orc):
+    # the chained split's kind of wait (acquire loads of a flag another worker
+    # releases): on a flag that nothing sets it gives up, the host reads the
+    # timeout, and the next chained-split GEMM on the same context is
+    # bit-exact with a clean status
+    L = rp.load()
+    torch.cuda.synchronize()
+    assert rp.device_status() == 0
+    s = torch.cuda.current_stream()
+    assert L.repops_selftest_bounded_flag_wait(20_000_000, s.cuda_stream) == 0   # 20 ms limit
+    assert rp.device_status() == REPOPS_ERR_TIMEOUT
+    assert rp.device_status() == 0
+    A = inputs.normal((300, 260), 1.0, 3, DEV)
+    B = inputs.normal((260, 1000), 1.0, 4, DEV)
+    C = rp.gemm_chained(A, B, config=4, workers=5)
     want = orc.gemm(A.cpu().numpy(), B.cpu().numpy())
     assert np.array_equal(C.cpu().numpy().view(np.uint32), want.view(np.uint32))
     assert rp.device_status() == 0

@@ -94,6 +94,7 @@ SIGNATURES = {
     "repops_rope_table_f32": (_i32, [_i64, _i64, _vp, _vp, _vp, _vp]),
     "repops_rope_f32": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _i64, _i64, _i32, _vp]),
     "repops_selftest_bounded_wait": (_i32, [_i64, _vp]),
+    "repops_selftest_bounded_flag_wait": (_i32, [_i64, _vp]),
     "repops_softmax_rows_causal_f32": (_i32, [_i64, _i64, _vp, _i64, _vp, _i64, _i64, _i64, _vp]),
     "repops_gemm_f32_batched": (_i32, [_i32, _i32, _i32, _i32, _i64, _i64, _i64, _i64,
                                        _vp, _i64, _i64, _vp, _i64, _i64, _vp, _i64, _i64,

@@ -85,6 +85,17 @@ __global__ void bounded_wait_selftest_kernel(unsigned *status, uint64_t limit_ns
     if (!mbar_wait_bounded_ns(&bar, 0u, limit_ns)) atomicOr(status, 1u);
 }
 
+// The flag of the second self-test: zero, and nothing ever sets it.
+__device__ unsigned g_selftest_flag;
+
+// Failure-detection self-test of the chained split's wait: thread 0 waits for
+// a flag that nothing sets (the wait a tail makes for its head's partial
+// sums), gives up after limit_ns and sets the sticky status word.
+__global__ void flag_wait_selftest_kernel(unsigned *status, uint64_t limit_ns) {
+    if (threadIdx.x != 0) return;
+    if (!gemm::flag_wait_bounded_ns(&g_selftest_flag, limit_ns)) atomicOr(status, 1u);
+}
+
 const GemmLauncher kLaunch[kGemmConfigCount] = {gemm_launch_cfg0, gemm_launch_cfg1, gemm_launch_cfg2,
                                                 gemm_launch_cfg3, gemm_launch_cfg4};
 const GemmOccupancy kOccupancy[kGemmConfigCount] = {gemm_occupancy_cfg0, gemm_occupancy_cfg1,
@@ -965,5 +976,14 @@ extern "C" int repops_selftest_bounded_wait(int64_t limit_ns, cudaStream_t strea
     int rc = status_address(&status);
     if (rc != REPOPS_OK) return rc;
     bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, uint64_t(limit_ns));
+    return check_launch();
+}
+
+extern "C" int repops_selftest_bounded_flag_wait(int64_t limit_ns, cudaStream_t stream) {
+    if (limit_ns < 1 || limit_ns > int64_t(kWaitLimitNs)) return REPOPS_ERR_INVALID_ARG;
+    unsigned *status = nullptr;
+    int rc = status_address(&status);
+    if (rc != REPOPS_OK) return rc;
+    flag_wait_selftest_kernel<<<1, 32, 0, stream>>>(status, uint64_t(limit_ns));
     return check_launch();
 }

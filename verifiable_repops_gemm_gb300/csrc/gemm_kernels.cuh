@@ -600,8 +600,8 @@ __device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Waits until *flag is non-zero; gives up after kWaitLimitNs.
-__device__ __forceinline__ bool flag_wait_bounded(const unsigned *flag) {
+// Waits until *flag is non-zero; gives up after limit_ns.
+__device__ __forceinline__ bool flag_wait_bounded_ns(const unsigned *flag, uint64_t limit_ns) {
     if (ld_acquire_gpu(flag)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
@@ -610,8 +610,13 @@ __device__ __forceinline__ bool flag_wait_bounded(const unsigned *flag) {
             __nanosleep(64);
             if (ld_acquire_gpu(flag)) return true;
         }
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if (global_timer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Waits until *flag is non-zero; gives up after kWaitLimitNs.
+__device__ __forceinline__ bool flag_wait_bounded(const unsigned *flag) {
+    return flag_wait_bounded_ns(flag, kWaitLimitNs);
 }
 
 template <class T, bool A_KIN, bool B_KIN, bool EX>
