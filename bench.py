@@ -65,6 +65,13 @@ HBM_SPEC_GBS = 7900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one GEMM
 # launch at 8192^3 from one ncu capture of the tiled kernel, valid only for
 # the kernel source it was taken on (sha256 of gemm_kernels.cuh).
+# Integer-ALU instructions per SHA-256 compression as executed, from one ncu
+# capture of repops_sha256_rate_probe (sm__inst_executed_pipe_alu.sum x 32 /
+# compressions), valid only for the merkle.cu source it was taken on: the
+# measured instruction bound of the commitment (the ALU pipe issuing these
+# and nothing else).
+SHA_ALU_INSTR = {"src_sha256": "af05b29961a133e97eea5debe9cd92cf231e9b3bcf1a6d137024bca3cf942c07",
+                 "per_compression": 1023.23}
 GEMM_TRAFFIC = {"src_sha256": "a18f733c4b730ab375a6ca15bf294ac6f4821df7e42a730824418dbbe26ae9fe",
                 "bytes_per_launch": 3748467200 + 265021184}
 
@@ -85,10 +92,25 @@ def gemm_kernel_label():
             "call), B N-inner" % (cfg, ci["bm"], ci["bn"], ci["threads"], ci["tm"], ci["tn"]))
 
 
-def kernel_source_sha():
-    p = os.path.join(ROOT, "verifiable_repops_gemm_gb300", "csrc", "gemm_kernels.cuh")
+def kernel_source_sha(name="gemm_kernels.cuh"):
+    p = os.path.join(ROOT, "verifiable_repops_gemm_gb300", "csrc", name)
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
+
+
+def sha_instruction_bound(comp_rate, sms, peaks):
+    """The commitment against the ALU pipe issuing the ALU instructions a
+    compression executes (ncu on the rate probe), while merkle.cu is the
+    source they were counted on; else None."""
+    if SHA_ALU_INSTR["src_sha256"] != kernel_source_sha("merkle.cu"):
+        return None
+    clk = peaks.get("sm_max_mhz", SM_MAX_MHZ_NOMINAL) * 1e6
+    bound = sms * ALU_LANES_PER_SM * clk / SHA_ALU_INSTR["per_compression"] / 1e9
+    return {"peak": bound, "unit": "Gcompressions/s", "frac": comp_rate / bound,
+            "alu_instructions_per_compression": SHA_ALU_INSTR["per_compression"],
+            "basis": "64 ALU lanes x %d SMs x %.0f MHz / the ALU instructions one compression executes "
+                     "(ncu sm__inst_executed_pipe_alu on repops_sha256_rate_probe)"
+                     % (sms, clk / 1e6)}
 
 
 # ----------------------------------------------------------------- clocks ----
@@ -613,7 +635,8 @@ def run_ours(args):
                                         "value": probe_rate, "unit": "Gcompressions/s",
                                         "basis": "repops_sha256_rate_probe: the same compression, message in "
                                                  "registers, no loads or tree, 8 x 128 threads per SM"},
-                                    "frac_of_measured_ceiling": comp_rate / probe_rate}},
+                                    "frac_of_measured_ceiling": comp_rate / probe_rate,
+                                    "measured_instruction_bound": sha_instruction_bound(comp_rate, sms, peaks)}},
         },
         "roofline": {"kernel": gemm_kernel_label(), "bound": "alu",
                      "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
