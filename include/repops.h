@@ -665,7 +665,7 @@ int repops_merkle_sha256_host(const void *ptr, uint64_t bytes, uint32_t leaf,
 /* Size of the fixed device scratch behind repops_merkle_sha256_noalloc. */
 #define REPOPS_MERKLE_NOALLOC_SCRATCH_BYTES (1u << 20)
 
-/* The paper has no counterpart to this entry point; it is a deployment aid.
+/* Neither page describes anything like this entry point; it is a deployment aid.
  *
  * As repops_merkle_sha256, but it allocates nothing: no cudaMalloc, no
  * stream-ordered scratch, no caller workspace.  It is meant for callers that cannot

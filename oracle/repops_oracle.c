@@ -28,8 +28,7 @@
  *            §4.2.2 constants, §5.1.1 padding, §5.3.3 initial value,
  *            §6.2 computation).
  *
- * Readings taken where the pages are silent (all stated again in the design
- * notes):
+ * Readings taken where the pages are silent:
  *  - no FMA: the product is rounded to binary32, then added with its own
  *    rounding; rounding is to nearest even; subnormals are kept (no FTZ/DAZ);
  *  - the GEMM sum starts at +0.0f;
