@@ -56,7 +56,7 @@ typedef enum {
     REPOPS_ERR_ORDER = -3,        /* contributor order is not a permutation / duplicate IDs */
     REPOPS_ERR_CUDA = -4,         /* a CUDA runtime call failed (see repops_last_cuda_error) */
     REPOPS_ERR_TIMEOUT = -5,      /* a bounded device-side wait gave up (sticky, see below) */
-    REPOPS_ERR_ALLOC = -6,        /* stream-ordered scratch allocation failed */
+    REPOPS_ERR_ALLOC = -6,        /* an allocation failed: stream-ordered scratch, or host memory */
     REPOPS_ERR_UNSUPPORTED = -7,  /* request outside the documented limits */
     REPOPS_ERR_BOUNDS = -8        /* checked build only: an access outside its buffer was skipped */
 } repops_status;
@@ -145,6 +145,39 @@ int repops_selftest_bounded_flag_wait(int64_t limit_ns, cudaStream_t stream);
 int repops_scratch_set_keep_bytes(uint64_t bytes);
 int repops_scratch_release(void);
 int repops_scratch_reserved_bytes(uint64_t *bytes_out);
+
+/* Host memory for the host-buffer entry points (repops_gemm_f32_host,
+ * repops_fixed_order_mean_sgd_host, repops_merkle_sha256_host).  Neither page
+ * describes anything like this; it is a deployment aid.
+ *
+ * Those calls copy their operands over the host link, and page-locked
+ * ("pinned") host memory is what lets the copy engines read it directly.  How
+ * that memory is paged matters on a Grace host: a GB300's copies out of
+ * memory pinned in 64 KB pages (what cudaHostAlloc returned there) ran at 8
+ * to 212 GB/s once a step touched more than ~16 GiB of it, varying from pass
+ * to pass, while the same copies out of memory held in transparent huge pages
+ * ran at 209-212 GB/s at every size tried up to 24 GiB.  The kernel may still
+ * split huge pages later (on that host the buffers allocated first lost
+ * theirs when more memory was allocated after them); copies over those pages
+ * then vary again.
+ *
+ * repops_host_alloc: *ptr_out = `bytes` of zero-filled, page-locked host
+ * memory registered with CUDA for every device (cudaHostRegisterPortable),
+ * its pages transparent huge pages where the kernel provides them: an
+ * anonymous mapping whose start is aligned to the huge page size
+ * (/sys/kernel/mm/transparent_hugepage/hpage_pmd_size, 2 MiB if unknown),
+ * advised MADV_HUGEPAGE (memory below one huge page is mapped the ordinary
+ * way).  Owned by the caller until repops_host_free.  bytes == 0 gives
+ * *ptr_out = NULL and REPOPS_OK.  REPOPS_ERR_INVALID_ARG for a null ptr_out;
+ * REPOPS_ERR_ALLOC if the mapping is refused; REPOPS_ERR_CUDA if the
+ * registration fails (no usable device, or the pages cannot be locked); on
+ * any error *ptr_out = NULL and nothing is kept.
+ * repops_host_free: unregisters and unmaps memory from repops_host_alloc,
+ * which no copy may still be reading or writing.  NULL is a no-op (REPOPS_OK);
+ * a pointer repops_host_alloc did not return, or one already freed, is
+ * REPOPS_ERR_INVALID_ARG.  Thread-safe. */
+int repops_host_alloc(uint64_t bytes, void **ptr_out);
+int repops_host_free(void *ptr);
 
 /* ------------------------------------------------------------------------ */
 /* Order-fixed FP32 GEMM                                                     */

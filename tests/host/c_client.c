@@ -11,6 +11,7 @@
  *   - mean + SGD ("Zoo Per-LLM Chain Soundness" §5): four contributors (the
  *     divide by 4 is exact), eta = 1/16, in the order repops_sort_ids gives
  *     for four DIDs of different lengths;
+ *   - the host-buffer GEMM on buffers from repops_host_alloc;
  *   - the Merkle root of C's bytes (4096-byte leaves, a short last leaf) is
  *     printed for the caller to compare with the oracle's.
  * Prints "ok <root hex>" and exits 0, else the first mismatch and exits 1.
@@ -124,6 +125,26 @@ int main(void) {
         if (check_gemm(hC2, M2, N2, K2, "repops_gemm_f32_ws (B transposed)")) return 1;
         cudaFree(dA2); cudaFree(dBt2); cudaFree(dC2); cudaFree(ws);
         free(hA2); free(hBt2); free(hC2);
+    }
+
+    /* the host-buffer GEMM on buffers from the library's host allocator */
+    {
+        float *pA = NULL, *pB = NULL, *pC = NULL;
+        REPOPS_OK_(repops_host_alloc(sizeof(float) * M * K, (void **)&pA));
+        REPOPS_OK_(repops_host_alloc(sizeof(float) * K * N, (void **)&pB));
+        REPOPS_OK_(repops_host_alloc(sizeof(float) * M * N, (void **)&pC));
+        memcpy(pA, hA, sizeof(float) * M * K);
+        memcpy(pB, hB, sizeof(float) * K * N);
+        REPOPS_OK_(repops_gemm_f32_host(M, N, K, pA, K, pB, N, pC, N, s));
+        CUDA_OK(cudaStreamSynchronize(s));
+        if (check_gemm(pC, M, N, K, "repops_gemm_f32_host (repops_host_alloc buffers)")) return 1;
+        REPOPS_OK_(repops_host_free(pA));
+        REPOPS_OK_(repops_host_free(pB));
+        REPOPS_OK_(repops_host_free(pC));
+        if (repops_host_free(pC) != REPOPS_ERR_INVALID_ARG) {
+            printf("repops_host_free accepted a pointer freed already\n");
+            return 1;
+        }
     }
 
     /* contributor order: DIDs compared as unsigned bytes, a proper prefix first */

@@ -397,3 +397,28 @@ def test_added_entry_points_reject_bad_arguments(L):
     assert L.repops_merkle_sha256_host(FAKE_A, 0, 4096, FAKE_C, None) == -1
     assert L.repops_merkle_sha256_host(FAKE_A, 100, 100, FAKE_C, None) == -1
     assert L.repops_merkle_sha256_host(FAKE_A, 100, 4096, FAKE_A + 8, None) == -2
+
+
+def test_host_allocator_arguments(L):
+    import ctypes as C
+    p = C.c_void_p(12345)
+    # nothing to allocate: a null pointer and OK; nowhere to write: refused
+    assert L.repops_host_alloc(0, C.byref(p)) == 0 and p.value is None
+    assert L.repops_host_alloc(4096, None) == -1
+    # freeing null is a no-op; a pointer the allocator did not return is refused
+    assert L.repops_host_free(None) == 0
+    assert L.repops_host_free(FAKE_A) == -1
+    # a size no mapping can hold
+    p = C.c_void_p(12345)
+    assert L.repops_host_alloc((1 << 64) - 1, C.byref(p)) == -1 and p.value is None
+
+
+def test_host_allocator_without_a_device_keeps_nothing(L):
+    # with no usable GPU the registration fails: an error, a null pointer,
+    # and the mapping is gone again (a free of whatever was returned is refused)
+    import ctypes as C
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    p = C.c_void_p(12345)
+    assert L.repops_host_alloc(1 << 20, C.byref(p)) == -4 and p.value is None

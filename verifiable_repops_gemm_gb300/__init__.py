@@ -29,6 +29,8 @@ memory and streams.
   swiglu / swiglu_backward /        SiLU-gated MLP activation and rotary
   rope_frequencies / rope_table /   position embeddings of a Llama-style layer
   rope                              ("Verde与RepOps" §4.3)
+  host_empty(shape, dtype)          page-locked host memory in huge pages for the
+                                    host-buffer calls (gemm_host, ..._host)
 """
 import ctypes
 
@@ -36,7 +38,7 @@ from . import _capi
 from ._capi import (ACT_GELU, ACT_NONE, LOADER_AUTO, LOADER_CPASYNC, LOADER_DIRECT, LOADER_TMA,
                     MEAN_MAX_CONTRIBUTORS, TYPE_BF16, TYPE_F16, TYPE_F32, RepopsError, load)
 
-__all__ = ["load", "version", "scratch_set_keep_bytes", "scratch_release", "scratch_reserved_bytes", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
+__all__ = ["load", "version", "scratch_set_keep_bytes", "scratch_release", "scratch_reserved_bytes", "host_empty", "gemm", "gemm_chained", "gemm_auto_chained", "fixed_order_mean_sgd_host", "merkle_sha256_host", "attention_causal", "gemm_config_occupancy", "gemm_host", "gemm_config_count", "gemm_config_info",
            "gemm_auto_config", "gemm_small_output", "sha256_rate_probe", "sort_ids", "fixed_order_mean_sgd", "merkle_sha256",
            "merkle_workspace_bytes", "merkle_tree", "merkle_proof", "merkle_verify", "replay",
            "softmax_rows", "layernorm_rows", "rmsnorm_rows", "gelu", "gemm_batched",
@@ -471,6 +473,50 @@ def scratch_reserved_bytes() -> int:
     v = ctypes.c_uint64(0)
     _capi.check(load().repops_scratch_reserved_bytes(ctypes.byref(v)), "repops_scratch_reserved_bytes")
     return v.value
+
+
+class _HostBlock:
+    """One repops_host_alloc allocation, exposed to NumPy (and through it to
+    torch) by its array interface; unregistered and unmapped when the last
+    array or tensor over it is gone."""
+
+    def __init__(self, nbytes: int):
+        p = ctypes.c_void_p()
+        _capi.check(load().repops_host_alloc(int(nbytes), ctypes.byref(p)), "repops_host_alloc")
+        self.ptr = p.value
+        self.__array_interface__ = {"shape": (int(nbytes),), "typestr": "|u1", "data": (self.ptr, False),
+                                    "version": 3}
+
+    def __del__(self):
+        if getattr(self, "ptr", None):
+            try:
+                load().repops_host_free(self.ptr)
+            except Exception:   # interpreter shutdown: the process's memory goes anyway
+                pass
+            self.ptr = None
+
+
+def host_empty(shape, dtype=None):
+    """A contiguous CPU tensor over page-locked host memory in transparent huge
+    pages (repops_host_alloc), for the host-buffer calls: zero-filled, freed
+    when the tensor and every view of it are gone.  On a Grace host such
+    buffers keep the copy engines at the link's rate where memory pinned in
+    64 KB pages does not."""
+    import numpy as np
+    import torch
+    dtype = torch.float32 if dtype is None else dtype
+    shape = tuple(int(x) for x in shape) if isinstance(shape, (tuple, list)) else (int(shape),)
+    if any(x < 0 for x in shape):
+        raise ValueError("negative dimension in %s" % (shape,))
+    n = 1
+    for x in shape:
+        n *= x
+    nbytes = n * torch.empty((), dtype=dtype).element_size()
+    if nbytes == 0:
+        return torch.empty(shape, dtype=dtype)
+    if torch.cuda.is_available():
+        torch.cuda.init()   # torch reports host memory as pinned only once its CUDA state exists
+    return torch.from_numpy(np.asarray(_HostBlock(nbytes))).view(dtype).view(shape)
 
 
 def set_thread_status_word(word=None) -> None:

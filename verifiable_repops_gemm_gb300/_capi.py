@@ -37,6 +37,8 @@ SIGNATURES = {
     "repops_scratch_set_keep_bytes": (_i32, [ctypes.c_uint64]),
     "repops_scratch_release": (_i32, []),
     "repops_scratch_reserved_bytes": (_i32, [_vp]),
+    "repops_host_alloc": (_i32, [_u64, _vp]),
+    "repops_host_free": (_i32, [_vp]),
     "repops_set_thread_status_word": (_i32, [_vp]),
     "repops_gemm_f32": (_i32, [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),
     "repops_gemm_f32_ex": (_i32, [_i32, _i32, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]),

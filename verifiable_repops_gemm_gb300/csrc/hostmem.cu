@@ -1,0 +1,116 @@
+// hostmem.cu -- page-locked host memory in transparent huge pages for the
+// host-buffer entry points (host code only).
+//
+// A copy engine reads pinned host memory through the host's address
+// translation.  On a GB300's Grace host the base page is 64 KB, and copies out
+// of buffers pinned in such pages ran anywhere from 8 to 212 GB/s once a
+// step's buffers passed ~16 GiB, varying from pass to pass; buffers held in
+// transparent huge pages (512 MB there) kept the link's 209-212 GB/s.  So this
+// allocator maps anonymous memory at a huge-page-aligned address, advises it
+// MADV_HUGEPAGE and registers it with CUDA (which faults every page in and
+// locks it).
+#include <sys/mman.h>
+#include <unistd.h>
+
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <unordered_map>
+
+#include "internal.cuh"
+
+namespace repops {
+namespace {
+
+struct HostBlocks {
+    std::mutex mu;
+    std::unordered_map<void *, size_t> len;   // start -> mapped length
+};
+
+HostBlocks &host_blocks() {
+    static HostBlocks b;
+    return b;
+}
+
+size_t page_size() {
+    const long p = sysconf(_SC_PAGESIZE);
+    return p > 0 ? size_t(p) : size_t(4096);
+}
+
+// The kernel's transparent huge page size, 2 MiB when it does not say.
+size_t huge_page_size() {
+    static size_t h = [] {
+        size_t v = 0;
+        if (FILE *f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+            unsigned long long x = 0;
+            if (std::fscanf(f, "%llu", &x) == 1) v = size_t(x);
+            std::fclose(f);
+        }
+        const size_t pg = page_size();
+        if (v < pg || (v & (v - 1)) != 0) v = size_t(2) << 20;
+        return v;
+    }();
+    return h;
+}
+
+}  // namespace
+}  // namespace repops
+
+using namespace repops;
+
+extern "C" int repops_host_alloc(uint64_t bytes, void **ptr_out) {
+    if (!ptr_out) return REPOPS_ERR_INVALID_ARG;
+    *ptr_out = nullptr;
+    if (bytes == 0) return REPOPS_OK;
+    const size_t pg = page_size(), huge = huge_page_size();
+    if (bytes > uint64_t(SIZE_MAX / 2) - huge) return REPOPS_ERR_INVALID_ARG;
+    const size_t len = (size_t(bytes) + pg - 1) / pg * pg;
+    // a huge-page-aligned start: reserve `huge` more, trim both ends
+    const size_t align = len >= huge ? huge : pg;
+    const size_t span = len + (align > pg ? align : 0);
+    void *raw = mmap(nullptr, span, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (raw == MAP_FAILED) return REPOPS_ERR_ALLOC;
+    const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
+    const uintptr_t start = (r + align - 1) / align * align;
+    const size_t head = start - r, tail = span - head - len;
+    if (head) munmap(raw, head);
+    if (tail) munmap(reinterpret_cast<void *>(start + len), tail);
+    void *p = reinterpret_cast<void *>(start);
+#ifdef MADV_HUGEPAGE
+    if (align == huge) {
+        madvise(p, len, MADV_HUGEPAGE);   // advice only: ordinary pages if refused
+        // one write per huge page faults each whole aligned range in at once
+        // (the pages are zero either way)
+        volatile unsigned char *q = static_cast<volatile unsigned char *>(p);
+        for (size_t off = 0; off < len; off += huge) q[off] = 0;
+    }
+#endif
+    const cudaError_t e = cudaHostRegister(p, len, cudaHostRegisterPortable);
+    if (e != cudaSuccess) {
+        munmap(p, len);
+        return set_cuda_error(e);
+    }
+    {
+        HostBlocks &b = host_blocks();
+        std::lock_guard<std::mutex> g(b.mu);
+        b.len[p] = len;
+    }
+    *ptr_out = p;
+    return REPOPS_OK;
+}
+
+extern "C" int repops_host_free(void *ptr) {
+    if (!ptr) return REPOPS_OK;
+    size_t len = 0;
+    {
+        HostBlocks &b = host_blocks();
+        std::lock_guard<std::mutex> g(b.mu);
+        auto it = b.len.find(ptr);
+        if (it == b.len.end()) return REPOPS_ERR_INVALID_ARG;
+        len = it->second;
+        b.len.erase(it);
+    }
+    const cudaError_t e = cudaHostUnregister(ptr);
+    munmap(ptr, len);
+    return e == cudaSuccess ? REPOPS_OK : set_cuda_error(e);
+}
