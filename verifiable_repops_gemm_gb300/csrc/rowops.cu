@@ -673,20 +673,19 @@ gelu_kernel(int64_t n, const float *__restrict__ x, float *__restrict__ y, int v
     const int64_t first = blockIdx.x * int64_t(blockDim.x) + threadIdx.x;
     if (vec) {
         const int64_t n4 = n / 4;
-        // two float4 groups a trip (8 independent GeLUs in flight), then one
+        const float4 *x4 = reinterpret_cast<const float4 *>(x);
+        float4 *y4 = reinterpret_cast<float4 *>(y);
+        // one float4 group a trip, the next trip's group loaded before this
+        // trip's four GeLUs run
         int64_t i = first;
-        for (; i + stride < n4; i += 2 * stride) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(x) + i);
-            const float4 w = __ldcs(reinterpret_cast<const float4 *>(x) + i + stride);
-            const float2 a = gelu_fixed2(v.x, v.y), b = gelu_fixed2(v.z, v.w);
-            const float2 c = gelu_fixed2(w.x, w.y), d = gelu_fixed2(w.z, w.w);
-            __stcs(reinterpret_cast<float4 *>(y) + i, make_float4(a.x, a.y, b.x, b.y));
-            __stcs(reinterpret_cast<float4 *>(y) + i + stride, make_float4(c.x, c.y, d.x, d.y));
-        }
+        const float4 zero = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float4 v = i < n4 ? __ldcs(x4 + i) : zero;
         for (; i < n4; i += stride) {
-            const float4 v = __ldcs(reinterpret_cast<const float4 *>(x) + i);
-            const float2 lo = gelu_fixed2(v.x, v.y), hi = gelu_fixed2(v.z, v.w);
-            __stcs(reinterpret_cast<float4 *>(y) + i, make_float4(lo.x, lo.y, hi.x, hi.y));
+            const bool next = i + stride < n4;
+            const float4 nv = next ? __ldcs(x4 + i + stride) : zero;
+            const float2 a = gelu_fixed2(v.x, v.y), b = gelu_fixed2(v.z, v.w);
+            __stcs(y4 + i, make_float4(a.x, a.y, b.x, b.y));
+            v = nv;
         }
         for (int64_t i = n4 * 4 + first; i < n; i += stride) y[i] = gelu_fixed(x[i]);
     } else {
