@@ -474,7 +474,11 @@ def run_e2e(w, dev, steps):
     hth = pinned_copy(w.theta)
     hT = pinned_copy(w.T)
     hroot = rp.host_empty((2, 32), torch.uint8)
-    link = host_link_rate(dev, s)
+    # the link probes copy from and to the step's own buffers (the output C is
+    # written over by the first step): another GiB of host memory here cost
+    # the step's first buffers their huge pages on a host with ~22 GiB of
+    # huge-page blocks free
+    link = host_link_rate(dev, s, src=hg[0], dst=hC)
     link["h2d_gradients_16gib"] = working_set_rate(dev, s, hg)
     huge = anon_huge_page_bytes()
     want_root_C = bytes(w.root_C.cpu().numpy())
@@ -563,16 +567,17 @@ def anon_huge_page_bytes():
     return None
 
 
-def host_link_rate(dev, s, nbytes=1 << 30):
-    """Host <-> device copy rate of 1 GiB from the same kind of host memory as
-    the end-to-end steps use (rp.host_empty), each direction timed alone (CUDA
-    events, best of 3), sampled right before those steps: the end-to-end
-    figures are bound by it."""
-    h = rp.host_empty((nbytes,), torch.uint8)
-    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+def host_link_rate(dev, s, src, dst):
+    """Host <-> device copy rate over one host buffer each way (src read,
+    dst written: host memory of the end-to-end steps' kind, rp.host_empty),
+    each direction timed alone (CUDA events, best of 3), sampled right before
+    those steps: the end-to-end figures are bound by it."""
+    hs, hd = src.view(-1).view(torch.uint8), dst.view(-1).view(torch.uint8)
+    d = torch.empty(max(hs.numel(), hd.numel()), dtype=torch.uint8, device=dev)
+    sizes = {"h2d": hs.numel(), "d2h": hd.numel()}
     out = {}
-    for name, fn in (("h2d", lambda: d.copy_(h, non_blocking=True)),
-                     ("d2h", lambda: h.copy_(d, non_blocking=True))):
+    for name, fn in (("h2d", lambda: d[:hs.numel()].copy_(hs, non_blocking=True)),
+                     ("d2h", lambda: hd.copy_(d[:hd.numel()], non_blocking=True))):
         best = None
         for _ in range(3):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -583,8 +588,8 @@ def host_link_rate(dev, s, nbytes=1 << 30):
             b.synchronize()
             t = a.elapsed_time(b) / 1e3
             best = t if best is None else min(best, t)
-        out[name] = nbytes / best / 1e9
-    del h, d
+        out[name] = sizes[name] / best / 1e9
+    del d
     return out
 
 
