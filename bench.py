@@ -468,8 +468,13 @@ def run_e2e(w, dev, steps):
         h = rp.host_empty(t.shape, t.dtype)
         h.copy_(t)
         return h
-    hA, hB = pinned_copy(w.A), pinned_copy(w.B)
-    hC = rp.host_empty(w.C.shape, torch.float32)
+    # A, B and C (256 MiB each, below a 512 MB huge page) share one block, so
+    # that they sit in huge pages without rounding each of them up to one
+    hABC = rp.host_empty((3,) + tuple(w.A.shape), torch.float32)
+    assert tuple(w.A.shape) == tuple(w.B.shape) == tuple(w.C.shape)
+    hA, hB, hC = hABC[0], hABC[1], hABC[2]
+    hA.copy_(w.A)
+    hB.copy_(w.B)
     hg = [pinned_copy(g) for g in w.grads]
     hth = pinned_copy(w.theta)
     hT = pinned_copy(w.T)

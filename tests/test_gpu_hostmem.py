@@ -42,6 +42,12 @@ def test_host_empty_is_pinned_zero_and_aligned(rp):
     assert big.data_ptr() % hp == 0
     big[-1] = 3.0
     assert float(big[-1]) == 3.0 and float(big[0]) == 0.0
+    # a quarter of a huge page or more: rounded up to whole huge pages, so
+    # its start is aligned to one too
+    mid = rp.host_empty((hp // 4,), torch.uint8)
+    assert mid.data_ptr() % hp == 0 and mid.numel() == hp // 4
+    mid[-1] = 9
+    assert int(mid[-1]) == 9 and int(mid[0]) == 0
     # empty shapes need no memory
     assert rp.host_empty((0, 4)).numel() == 0
 
