@@ -169,7 +169,8 @@ int repops_scratch_reserved_bytes(uint64_t *bytes_out);
  * advised MADV_HUGEPAGE.  A request of at least a quarter of a huge page is
  * rounded up to whole huge pages (up to one huge page more is mapped and
  * locked: 512 MB on a host with 64 KB base pages), so that all of it can be
- * held in them; a smaller one is mapped the ordinary way.  Owned by the
+ * held in them; a smaller one, or any where the kernel's transparent huge
+ * pages are off ("never"), is mapped the ordinary way.  Owned by the
  * caller until repops_host_free.  bytes == 0 gives
  * *ptr_out = NULL and REPOPS_OK.  REPOPS_ERR_INVALID_ARG for a null ptr_out;
  * REPOPS_ERR_ALLOC if the mapping is refused; REPOPS_ERR_CUDA if the

@@ -20,6 +20,13 @@ DEV = "cuda:0"
 
 
 def huge_page_bytes():
+    """The transparent huge page size, or None where huge pages are off."""
+    try:
+        with open("/sys/kernel/mm/transparent_hugepage/enabled") as f:
+            if "[never]" in f.read():
+                return None
+    except OSError:
+        return None
     try:
         with open("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size") as f:
             return int(f.read())
@@ -38,6 +45,8 @@ def test_host_empty_is_pinned_zero_and_aligned(rp):
         assert torch.equal(t, torch.full(shape, 7, dtype=dtype))
     # at least one huge page: its start is aligned to the huge page size
     hp = huge_page_bytes()
+    if hp is None:
+        return   # huge pages off: ordinary pages, nothing more to check
     big = rp.host_empty((hp // 4 + 1000,), torch.float32)
     assert big.data_ptr() % hp == 0
     big[-1] = 3.0

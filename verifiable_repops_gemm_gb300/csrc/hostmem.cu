@@ -14,6 +14,7 @@
 
 #include <cstdint>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 #include <unordered_map>
 
@@ -37,16 +38,30 @@ size_t page_size() {
     return p > 0 ? size_t(p) : size_t(4096);
 }
 
-// The kernel's transparent huge page size, 2 MiB when it does not say.
+// Whether the kernel hands out transparent huge pages for madvised memory:
+// its mode is "always" or "madvise", not "never" (unreadable: not assumed).
+bool huge_pages_enabled() {
+    char mode[128] = {0};
+    FILE *f = std::fopen("/sys/kernel/mm/transparent_hugepage/enabled", "r");
+    if (!f) return false;
+    const size_t n = std::fread(mode, 1, sizeof(mode) - 1, f);
+    std::fclose(f);
+    mode[n] = 0;
+    return std::strstr(mode, "[never]") == nullptr && std::strchr(mode, '[') != nullptr;
+}
+
+// The kernel's transparent huge page size (2 MiB when it does not say), or
+// the base page size where huge pages are off: then nothing is rounded up.
 size_t huge_page_size() {
     static size_t h = [] {
+        const size_t pg = page_size();
+        if (!huge_pages_enabled()) return pg;
         size_t v = 0;
         if (FILE *f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
             unsigned long long x = 0;
             if (std::fscanf(f, "%llu", &x) == 1) v = size_t(x);
             std::fclose(f);
         }
-        const size_t pg = page_size();
         if (v < pg || (v & (v - 1)) != 0) v = size_t(2) << 20;
         return v;
     }();
@@ -68,7 +83,7 @@ extern "C" int repops_host_alloc(uint64_t bytes, void **ptr_out) {
     // mapped the ordinary way, below the 512 MB huge page of a 64 KB-page
     // host, was the one part of a step whose copies swung between 33.8 and
     // 114 ms); smaller: base pages.
-    const bool in_huge = size_t(bytes) >= huge / 4;
+    const bool in_huge = huge > pg && size_t(bytes) >= huge / 4;
     const size_t unit = in_huge ? huge : pg;
     const size_t len = (size_t(bytes) + unit - 1) / unit * unit;
     // a huge-page-aligned start: reserve `huge` more, trim both ends
@@ -83,7 +98,7 @@ extern "C" int repops_host_alloc(uint64_t bytes, void **ptr_out) {
     if (tail) munmap(reinterpret_cast<void *>(start + len), tail);
     void *p = reinterpret_cast<void *>(start);
 #ifdef MADV_HUGEPAGE
-    if (align == huge) {
+    if (in_huge) {
         madvise(p, len, MADV_HUGEPAGE);   // advice only: ordinary pages if refused
         // one write per huge page faults each whole aligned range in at once
         // (the pages are zero either way)
