@@ -18,6 +18,7 @@
 #include <mutex>
 #include <unordered_map>
 
+#include "hostmem_plan.h"
 #include "internal.cuh"
 
 namespace repops {
@@ -77,23 +78,19 @@ extern "C" int repops_host_alloc(uint64_t bytes, void **ptr_out) {
     if (!ptr_out) return REPOPS_ERR_INVALID_ARG;
     *ptr_out = nullptr;
     if (bytes == 0) return REPOPS_OK;
-    const size_t pg = page_size(), huge = huge_page_size();
-    if (bytes > uint64_t(SIZE_MAX / 2) - huge) return REPOPS_ERR_INVALID_ARG;
     // At least a quarter of a huge page: whole huge pages (a 256 MiB buffer
     // mapped the ordinary way, below the 512 MB huge page of a 64 KB-page
     // host, was the one part of a step whose copies swung between 33.8 and
-    // 114 ms); smaller: base pages.
-    const bool in_huge = huge > pg && size_t(bytes) >= huge / 4;
-    const size_t unit = in_huge ? huge : pg;
-    const size_t len = (size_t(bytes) + unit - 1) / unit * unit;
-    // a huge-page-aligned start: reserve `huge` more, trim both ends
-    const size_t align = in_huge ? huge : pg;
-    const size_t span = len + (align > pg ? align : 0);
+    // 114 ms); smaller: base pages (hostmem_plan.h).
+    HostAllocPlan plan;
+    if (!host_alloc_plan(bytes, page_size(), huge_page_size(), &plan)) return REPOPS_ERR_INVALID_ARG;
+    const size_t len = plan.len, span = plan.span, huge = huge_page_size();
+    const bool in_huge = plan.in_huge;
     void *raw = mmap(nullptr, span, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
     if (raw == MAP_FAILED) return REPOPS_ERR_ALLOC;
-    const uintptr_t r = reinterpret_cast<uintptr_t>(raw);
-    const uintptr_t start = (r + align - 1) / align * align;
-    const size_t head = start - r, tail = span - head - len;
+    uintptr_t start = 0;
+    size_t head = 0, tail = 0;
+    host_alloc_trim(reinterpret_cast<uintptr_t>(raw), plan, &start, &head, &tail);
     if (head) munmap(raw, head);
     if (tail) munmap(reinterpret_cast<void *>(start + len), tail);
     void *p = reinterpret_cast<void *>(start);
