@@ -9,6 +9,10 @@ Every input is larger than the 129 MB L2, so no flush is needed between steps.
 
 `value` is the GEMM's TFLOP/s (2*M*N*K per launch / its device time, CUDA
 events on the launching stream); `parts` gives each stage's own throughput.
+`e2e` is the same step from host memory through the library's host-buffer
+calls (buffers from its huge-page host allocator), the copies inside the
+timed region; its `value` is the GEMM's TFLOP/s measured that way, and
+`whole_step` the whole step's time, with the host link's rate beside them.
 `--impl reference` times the CPU oracle instead (on a bounded sample of the
 same workload), printing the same JSON line with "impl": "reference".
 
@@ -454,7 +458,7 @@ KEEP_SCRATCH_E2E = 2 << 30   # freed scratch the pool may keep mapped during the
 
 def run_e2e(w, dev, steps):
     """Same metric through the library's host-buffer entry points, all three
-    parts from pinned host memory: repops_gemm_f32_host (A and B in, C back,
+    parts from page-locked host memory: repops_gemm_f32_host (A and B in, C back,
     the copies overlapping the GEMM's row blocks), then
     repops_fixed_order_mean_sgd_host (16 gradients and theta in, theta back,
     chunk by chunk), then repops_merkle_sha256_host of T and of C (chunks in,
