@@ -172,7 +172,8 @@ int repops_scratch_reserved_bytes(uint64_t *bytes_out);
  * held in them; a smaller one, or any where the kernel's transparent huge
  * pages are off ("never"), is mapped the ordinary way.  Owned by the
  * caller until repops_host_free.  bytes == 0 gives
- * *ptr_out = NULL and REPOPS_OK.  REPOPS_ERR_INVALID_ARG for a null ptr_out;
+ * *ptr_out = NULL and REPOPS_OK.  REPOPS_ERR_INVALID_ARG for a null ptr_out
+ * or a size no mapping can hold (above SIZE_MAX / 2 less one huge page);
  * REPOPS_ERR_ALLOC if the mapping is refused; REPOPS_ERR_CUDA if the
  * registration fails (no usable device, or the pages cannot be locked); on
  * any error *ptr_out = NULL and nothing is kept.
