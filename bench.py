@@ -495,23 +495,26 @@ def run_e2e(w, dev, steps):
     # a caller that runs step after step lets the scratch pool keep its memory
     # mapped across the per-step synchronisation (the default hands it back)
     rp.scratch_set_keep_bytes(KEEP_SCRATCH_E2E)
-    torch.cuda.synchronize(dev)
-    for i in range(steps + 1):          # the first pass is an untimed warm-up
-        e = ev[i]
-        e[0].record(s)
-        rp.gemm_host(hA, hB, out=hC, stream=s)
-        e[1].record(s)
-        rp.fixed_order_mean_sgd_host(hg, w.order, w.eta, hth, stream=s)
-        e[2].record(s)
-        rp.merkle_sha256_host(hT, 4096, out=hroot[0], stream=s)
-        rp.merkle_sha256_host(hC, 4096, out=hroot[1], stream=s)
-        e[3].record(s)
-        # the step's result read on the host: the roots
-        e[3].synchronize()
-        if bytes(hroot[1].numpy()) != want_root_C:
-            raise RuntimeError("the host-buffer step's root of C differs from the device step's")
-    rp.scratch_set_keep_bytes(0)
-    rp.scratch_release()
+    try:
+        torch.cuda.synchronize(dev)
+        for i in range(steps + 1):          # the first pass is an untimed warm-up
+            e = ev[i]
+            e[0].record(s)
+            rp.gemm_host(hA, hB, out=hC, stream=s)
+            e[1].record(s)
+            rp.fixed_order_mean_sgd_host(hg, w.order, w.eta, hth, stream=s)
+            e[2].record(s)
+            rp.merkle_sha256_host(hT, 4096, out=hroot[0], stream=s)
+            rp.merkle_sha256_host(hC, 4096, out=hroot[1], stream=s)
+            e[3].record(s)
+            # the step's result read on the host: the roots
+            e[3].synchronize()
+            if bytes(hroot[1].numpy()) != want_root_C:
+                raise RuntimeError("the host-buffer step's root of C differs from the device step's")
+    finally:
+        torch.cuda.synchronize(dev)
+        rp.scratch_set_keep_bytes(0)
+        rp.scratch_release()
     ev = ev[1:]
     tg = sum(e[0].elapsed_time(e[1]) for e in ev) / 1e3
     tm = sum(e[1].elapsed_time(e[2]) for e in ev) / 1e3
