@@ -422,3 +422,38 @@ def test_host_allocator_without_a_device_keeps_nothing(L):
         pytest.skip("a device is present")
     p = C.c_void_p(12345)
     assert L.repops_host_alloc(1 << 20, C.byref(p)) == -4 and p.value is None
+
+
+def declared_signatures():
+    """name -> (return type text, [parameter texts]) for every declaration in
+    include/repops.h (comments and preprocessor lines removed)."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = "\n".join(l for l in text.split("\n") if not l.lstrip().startswith("#"))
+    out = {}
+    for m in re.finditer(r"([A-Za-z_][\w\s\*]*?)\b(repops_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        ret, name, params = m.group(1).strip(), m.group(2), m.group(3).strip()
+        ret = ret.split("\n")[-1].strip()
+        plist = [] if params in ("", "void") else [p.strip() for p in params.split(",")]
+        out[name] = (ret, plist)
+    return out
+
+
+def test_binding_signatures_match_the_header():
+    import ctypes as C
+    from verifiable_repops_gemm_gb300 import _capi
+    decl = declared_signatures()
+    assert set(decl) == set(_capi.SIGNATURES), set(decl) ^ set(_capi.SIGNATURES)
+    ret_types = {"int": C.c_int, "uint64_t": C.c_uint64, "const char *": C.c_char_p}
+    scalar = {"int": C.c_int, "int64_t": C.c_int64, "uint32_t": C.c_uint32, "uint64_t": C.c_uint64,
+              "float": C.c_float}
+    for name, (ret, params) in decl.items():
+        restype, argtypes = _capi.SIGNATURES[name]
+        assert ret in ret_types and restype is ret_types[ret], (name, ret, restype)
+        assert len(argtypes) == len(params), (name, len(argtypes), len(params))
+        for p, a in zip(params, argtypes):
+            base = re.sub(r"\s+\w+$", "", p).replace("const ", "").strip()   # the type, without the name
+            if "*" in p or base == "cudaStream_t":
+                assert a is C.c_void_p, (name, p, a)       # pointers and the stream: passed as addresses
+            else:
+                assert base in scalar and a is scalar[base], (name, p, a)
