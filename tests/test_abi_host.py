@@ -457,3 +457,26 @@ def test_binding_signatures_match_the_header():
                 assert a is C.c_void_p, (name, p, a)       # pointers and the stream: passed as addresses
             else:
                 assert base in scalar and a is scalar[base], (name, p, a)
+
+
+def test_library_exports_exactly_the_declared_functions(L):
+    # every extern "C" definition in the sources is declared in the header and
+    # the other way round; and where binutils are at hand, the shared object's
+    # exported repops_ symbols are exactly those
+    import glob
+    import shutil
+    import subprocess
+    decl = set(declared_signatures())
+    csrc = os.path.join(ROOT, "verifiable_repops_gemm_gb300", "csrc")
+    defs = set()
+    for f in glob.glob(os.path.join(csrc, "*.cu")):
+        defs |= set(re.findall(r'extern "C"[^;{(]*?\b(repops_\w+)\s*\(', open(f).read()))
+    assert defs == decl, sorted(defs ^ decl)
+    nm = shutil.which("nm")
+    if nm:
+        from verifiable_repops_gemm_gb300 import build
+        r = subprocess.run([nm, "-D", "--defined-only", build.LIB], capture_output=True, text=True)
+        if r.returncode == 0:
+            exported = {line.split()[-1] for line in r.stdout.splitlines()
+                        if line.split() and line.split()[-1].startswith("repops_")}
+            assert exported == decl, sorted(exported ^ decl)
