@@ -73,7 +73,11 @@ typedef enum {
  * Chain Soundness" §5 Setup): it names what produced the bits.  Static string. */
 const char *repops_version(void);
 
-/* Human-readable text for a status code.  Static string. */
+/* Library infrastructure from here to the GEMM section: status codes,
+ * failure detection of the library's bounded waits, scratch and host memory.
+ * The pages describe none of these; they define no operation.
+ *
+ * Human-readable text for a status code.  Static string. */
 const char *repops_status_string(int status);
 
 /* The cudaError_t value of the most recent REPOPS_ERR_CUDA on this host
