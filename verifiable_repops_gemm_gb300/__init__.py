@@ -501,7 +501,12 @@ def host_empty(shape, dtype=None):
     pages (repops_host_alloc), for the host-buffer calls: zero-filled, freed
     when the tensor and every view of it are gone.  On a Grace host such
     buffers keep the copy engines at the link's rate where memory pinned in
-    64 KB pages does not."""
+    64 KB pages does not.
+
+    Unlike PyTorch's pinned memory, nothing holds the block back for copies
+    still in flight: keep a tensor (or a view of it) alive until every copy
+    that reads or writes it has completed, e.g. until its stream is
+    synchronised."""
     import numpy as np
     import torch
     dtype = torch.float32 if dtype is None else dtype
