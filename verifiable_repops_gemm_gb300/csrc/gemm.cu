@@ -187,10 +187,6 @@ int choose_plan(int64_t M, int64_t N, int64_t K, int64_t batch, bool allow_sk, b
     return best;
 }
 
-int choose_config(int64_t M, int64_t N, int64_t K = 1 << 20, int64_t batch = 1) {
-    return choose_plan(M, N, K, batch, false, nullptr);
-}
-
 // Tile choice for a banded product (k_lo / k_hi set): the tiles' k-ranges
 // differ -- a tile runs the whole 32-k slices covering its rows' bands -- so
 // the time is modelled as the longer of the longest tile (sharing its SM with
