@@ -364,9 +364,10 @@ bool small_output(int64_t M, int64_t N, int64_t K) {
 }
 
 // Chained k-split request of a call: kSkAuto lets the automatic choice decide
-// (config -1 and the automatic loader only), kSkOff never splits, and a value
-// >= 0 asks for it with that many workers (0 = every resident CTA slot).
-constexpr int kSkAuto = -1, kSkOff = -2;
+// (config -1 and the automatic loader only), a value >= 0 asks for it with
+// that many workers (0 = every resident CTA slot), and any other negative
+// value never splits.
+constexpr int kSkAuto = -1;
 
 // Workers and scratch bytes (the heads' accumulators, then the flags) of a
 // chained k-split of an M x N output on configuration cfg with `req` workers
